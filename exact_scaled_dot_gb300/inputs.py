@@ -1,0 +1,108 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only describes shapes and draws random numbers: it holds none of
+the attention arithmetic, so both the CUDA path and the CPU oracle can take
+their inputs from it without sharing any computation.
+
+Recipe (the same for every workload): a CPU ``torch.Generator`` seeded with
+``seed`` draws, in this order, fp32 samples N(0, sigma_qk^2) for Q and K and
+N(0, sigma_v^2) for V and dO, each rounded to bfloat16 (round to nearest
+even); then, for key-padded workloads, per-batch key lengths uniform on the
+inclusive range ``kv_len_range``.  The pages fix no dataset: these draws stand
+in for real activations, with the shapes, masks and value scales of the five
+workloads the method is measured on (the peaked-softmax cross-attention case
+scales Q and K by 3, so the logits have standard deviation 9 by the variance
+argument of eq. A.10.4 of "Appendix A.10 -- Attention matrices and
+backpropagation").
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+from typing import Dict, Optional, Tuple
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, visible-set description and value scales."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    nq: int
+    nk: int
+    dh: int
+    dv: int
+    causal: bool = False
+    offset: Optional[int] = None          # None: n_k - n_q (bottom-right aligned)
+    kv_len_range: Optional[Tuple[int, int]] = None   # inclusive, or None (no padding)
+    sigma_qk: float = 1.0
+    sigma_v: float = 1.0
+    seed: int = 0
+
+    @property
+    def causal_offset(self) -> int:
+        return (self.nk - self.nq) if self.offset is None else int(self.offset)
+
+    def with_seed(self, seed: int) -> "Workload":
+        return replace(self, seed=seed)
+
+    def scaled(self, **kw) -> "Workload":
+        """A copy with some fields replaced (e.g. smaller sizes for quick tests)."""
+        return replace(self, **kw)
+
+
+# The five workloads: a tiny single head, causal MHA, causal GQA with key
+# padding, peaked cross-attention with key padding, and MQA chunked prefill
+# (new queries over a long history, causal with an offset).  Seeds 1000 + k.
+WORKLOADS: Dict[str, Workload] = {
+    "single_head_full": Workload("single_head_full", B=1, Hq=1, Hkv=1, nq=128, nk=128,
+                                 dh=64, dv=64, seed=1001),
+    "mha_causal": Workload("mha_causal", B=4, Hq=16, Hkv=16, nq=2048, nk=2048,
+                           dh=128, dv=128, causal=True, seed=1002),
+    "gqa_causal_padded": Workload("gqa_causal_padded", B=2, Hq=32, Hkv=8, nq=4096, nk=4096,
+                                  dh=128, dv=128, causal=True, kv_len_range=(2048, 4096),
+                                  seed=1003),
+    "cross_padded_peaked": Workload("cross_padded_peaked", B=8, Hq=16, Hkv=16, nq=512, nk=8192,
+                                    dh=128, dv=64, kv_len_range=(4096, 8192), sigma_qk=3.0,
+                                    seed=1004),
+    "mqa_chunked_prefill": Workload("mqa_chunked_prefill", B=1, Hq=64, Hkv=1, nq=1024, nk=16384,
+                                    dh=128, dv=128, causal=True, seed=1005),
+}
+
+WORKLOAD_ORDER = ["single_head_full", "mha_causal", "gqa_causal_padded",
+                  "cross_padded_peaked", "mqa_chunked_prefill"]
+
+
+@dataclass
+class Inputs:
+    """bf16 tensors on the CPU (contiguous [B, H, n, d]) and int32 key lengths."""
+    Q: torch.Tensor
+    K: torch.Tensor
+    V: torch.Tensor
+    dO: torch.Tensor
+    kv_len: Optional[torch.Tensor]
+
+
+def make_inputs(w: Workload, seed: Optional[int] = None) -> Inputs:
+    """Draw the workload's inputs (see the module docstring for the recipe)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed if seed is None else seed))
+
+    def draw(shape, sigma):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x.mul_(sigma)
+        return x.to(torch.bfloat16).contiguous()
+
+    Q = draw((w.B, w.Hq, w.nq, w.dh), w.sigma_qk)
+    K = draw((w.B, w.Hkv, w.nk, w.dh), w.sigma_qk)
+    V = draw((w.B, w.Hkv, w.nk, w.dv), w.sigma_v)
+    dO = draw((w.B, w.Hq, w.nq, w.dv), w.sigma_v)
+    kv_len = None
+    if w.kv_len_range is not None:
+        lo, hi = w.kv_len_range
+        kv_len = torch.randint(int(lo), int(hi) + 1, (w.B,), generator=g, dtype=torch.int64)
+        kv_len = kv_len.to(torch.int32)
+    return Inputs(Q, K, V, dO, kv_len)
