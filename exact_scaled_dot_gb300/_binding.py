@@ -1,0 +1,279 @@
+"""ctypes binding of the C ABI in include/attn.h.
+
+Argument marshalling only: shapes, masks, pointers and the current torch
+stream go in; every step of the computation runs in the CUDA library.  There
+is no fallback: if the compiled library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+from typing import Optional, Sequence, Tuple, Union
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libesd_attn.so"
+
+ATTN_OK = 0
+ATTN_ERR_NULL = 1
+ATTN_ERR_SHAPE = 2
+ATTN_ERR_UNSUPPORTED = 3
+ATTN_ERR_ALIGN = 4
+ATTN_ERR_EMPTY_ROW = 5
+ATTN_ERR_SCALE = 6
+ATTN_ERR_WORKSPACE = 7
+ATTN_ERR_CUDA = 8
+ATTN_ERR_TIMEOUT = 9
+ATTN_ERR_DEVICE = 10
+ATTN_MAX_BATCH = 512
+ATTN_OFFSET_DEFAULT = -(2 ** 63)
+
+# Every symbol include/attn.h declares.
+EXPORTS = ("attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+           "attn_bwd_finalize", "attn_visible_pairs", "attn_get_status", "attn_clear_status",
+           "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version")
+
+
+class AttnError(RuntimeError):
+    """A non-zero status from the C ABI."""
+
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {strerror(code)} (status {code})")
+
+
+class AttnShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "Hq", "Hkv", "n_q", "n_k", "d_h", "d_v")]
+
+
+class AttnMask(ctypes.Structure):
+    _fields_ = [("causal", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("causal_offset", ctypes.c_int64), ("kv_len", ctypes.POINTER(ctypes.c_int32))]
+
+
+_lib: Optional[ctypes.CDLL] = None
+_vp = ctypes.c_void_p
+
+
+def load(path: Optional[Path] = None) -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path is not None else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"CUDA library {p} not found; build it with exact_scaled_dot_gb300.build.build()")
+    lib = ctypes.CDLL(str(p))
+    S, M = ctypes.POINTER(AttnShape), ctypes.POINTER(AttnMask)
+    f = ctypes.c_float
+    lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_workspace_bytes.argtypes = [S]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_finalize.argtypes = [S, f, _vp, _vp, _vp]
+    lib.attn_visible_pairs.argtypes = [S, M]
+    lib.attn_visible_pairs.restype = ctypes.c_int64
+    lib.attn_get_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.attn_clear_status.argtypes = []
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
+    lib.attn_strerror.argtypes = [ctypes.c_int]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_abi_version.restype = ctypes.c_int
+    for name in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
+                 "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().attn_strerror(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != ATTN_OK:
+        raise AttnError(rc, where)
+
+
+# ---------------------------------------------------------------------------
+# Marshalling helpers
+# ---------------------------------------------------------------------------
+def make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> AttnShape:
+    return AttnShape(int(B), int(Hq), int(Hkv), int(n_q), int(n_k), int(d_h), int(d_v))
+
+
+class _MaskArg:
+    """Holds an AttnMask and keeps its host kv_len array alive."""
+
+    def __init__(self, causal: bool, causal_offset: Optional[int], kv_len):
+        self._keep = None
+        kv = ctypes.POINTER(ctypes.c_int32)()
+        if kv_len is not None:
+            if isinstance(kv_len, torch.Tensor):
+                vals = [int(x) for x in kv_len.detach().cpu().reshape(-1).tolist()]
+            else:
+                vals = [int(x) for x in kv_len]
+            arr = (ctypes.c_int32 * max(1, len(vals)))(*vals)
+            self._keep = arr
+            kv = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        off = ATTN_OFFSET_DEFAULT if causal_offset is None else int(causal_offset)
+        self.mask = AttnMask(1 if causal else 0, 0, off, kv)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_tensor(t: torch.Tensor, name: str, dtype, shape: Tuple[int, ...], device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda or (device is not None and t.device != device):
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _qkv_shape(Q, K, V):
+    if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("Q, K, V must be 4-D [B, H, n, d]")
+    B, Hq, n_q, d_h = Q.shape
+    _, Hkv, n_k, _ = K.shape
+    d_v = V.shape[3]
+    return int(B), int(Hq), int(Hkv), int(n_q), int(n_k), int(d_h), int(d_v)
+
+
+def _check_qkv(Q, K, V):
+    B, Hq, Hkv, n_q, n_k, d_h, d_v = _qkv_shape(Q, K, V)
+    dev = Q.device
+    _check_tensor(Q, "Q", torch.bfloat16, (B, Hq, n_q, d_h), dev)
+    _check_tensor(K, "K", torch.bfloat16, (B, Hkv, n_k, d_h), dev)
+    _check_tensor(V, "V", torch.bfloat16, (B, Hkv, n_k, d_v), dev)
+    return (B, Hq, Hkv, n_q, n_k, d_h, d_v), dev
+
+
+# ---------------------------------------------------------------------------
+# Public functions (names follow the C ABI)
+# ---------------------------------------------------------------------------
+def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
+             causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
+             O: Optional[torch.Tensor] = None, LSE: Optional[torch.Tensor] = None, stream=None):
+    """Forward pass: returns (O [B,Hq,n_q,d_v] bf16, LSE [B,Hq,n_q] fp32)."""
+    dims, dev = _check_qkv(Q, K, V)
+    B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
+    scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
+    if O is None:
+        O = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
+    if LSE is None:
+        LSE = torch.empty((B, Hq, n_q), dtype=torch.float32, device=dev)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
+    shape = make_shape(*dims)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
+                         _ptr(V), _ptr(O), _ptr(LSE), _stream(dev, stream))
+    _check(rc, "attn_fwd")
+    return O, LSE
+
+
+def attn_bwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
+    shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
+    return int(load().attn_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def attn_bwd(Q, K, V, O, dO, LSE, *, causal: bool = False, causal_offset: Optional[int] = None, kv_len=None,
+             scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+    """Backward pass: returns (dQ, dK, dV) in bf16; dK, dV summed over each KV head's group."""
+    dims, dev = _check_qkv(Q, K, V)
+    B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
+    scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
+    if dQ is None:
+        dQ = torch.empty_like(Q)
+    if dK is None:
+        dK = torch.empty_like(K)
+    if dV is None:
+        dV = torch.empty_like(V)
+    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev)
+    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev)
+    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev)
+    need = attn_bwd_workspace_bytes(*dims)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must hold at least {need} bytes")
+    shape = make_shape(*dims)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    rc = load().attn_bwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
+                         _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
+    _check(rc, "attn_bwd")
+    return dQ, dK, dV
+
+
+def attn_bwd_preprocess(O, dO, D, dQacc, *, shape: AttnShape, stream=None):
+    rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(O), _ptr(dO), _ptr(D), _ptr(dQacc),
+                                    _stream(O.device, stream))
+    _check(rc, "attn_bwd_preprocess")
+
+
+def attn_bwd_main(Q, K, V, dO, LSE, D, dQacc, dK, dV, *, shape: AttnShape, causal=False, causal_offset=None,
+                  kv_len=None, scale: Optional[float] = None, stream=None):
+    scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
+                              _ptr(V), _ptr(dO), _ptr(LSE), _ptr(D), _ptr(dQacc), _ptr(dK), _ptr(dV),
+                              _stream(Q.device, stream))
+    _check(rc, "attn_bwd_main")
+
+
+def attn_bwd_finalize(dQacc, dQ, *, shape: AttnShape, scale: Optional[float] = None, stream=None):
+    scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
+    rc = load().attn_bwd_finalize(ctypes.byref(shape), ctypes.c_float(scale), _ptr(dQacc), _ptr(dQ),
+                                  _stream(dQ.device, stream))
+    _check(rc, "attn_bwd_finalize")
+
+
+def attn_visible_pairs(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, causal=False, causal_offset=None, kv_len=None) -> int:
+    """Visible (i, j) pairs over batch and query heads (closed form; -1 if invalid)."""
+    shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    return int(load().attn_visible_pairs(ctypes.byref(shape), ctypes.byref(m.mask)))
+
+
+def attn_get_status() -> int:
+    v = ctypes.c_int(0)
+    _check(load().attn_get_status(ctypes.byref(v)), "attn_get_status")
+    return int(v.value)
+
+
+def attn_clear_status() -> None:
+    _check(load().attn_clear_status(), "attn_clear_status")
+
+
+def attn_selftest_wait_timeout(limit_ns: int, stream=None, device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(load().attn_selftest_wait_timeout(ctypes.c_uint64(int(limit_ns)), _stream(dev, stream)),
+           "attn_selftest_wait_timeout")
+
+
+def attn_abi_version() -> int:
+    return int(load().attn_abi_version())

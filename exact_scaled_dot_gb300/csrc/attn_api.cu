@@ -1,0 +1,394 @@
+// attn_api.cu -- the C ABI (include/attn.h): argument validation, TMA tensor
+// descriptors, launches, the device status word and the failure-detection
+// self test.  Every argument check runs before the first CUDA call, so an
+// invalid call returns its error code without touching the GPU.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace esd {
+namespace {
+
+// Device status word: ATTN_OK, or the first failure a kernel recorded.
+__device__ unsigned int g_attn_status = 0u;
+
+constexpr int kMaxDevices = 64;
+
+// ---------------------------------------------------------------------------
+// Validation (host only, no CUDA calls)
+// ---------------------------------------------------------------------------
+bool supported_dims(int dh, int dv) {
+  return (dh == 64 && dv == 64) || (dh == 128 && dv == 128) || (dh == 128 && dv == 64);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const attn_shape* s) {
+  if (!s) return ATTN_ERR_NULL;
+  if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->n_q <= 0 || s->n_k <= 0 || s->d_h <= 0 || s->d_v <= 0)
+    return ATTN_ERR_SHAPE;
+  if (s->Hq % s->Hkv != 0) return ATTN_ERR_SHAPE;
+  if (s->B > ATTN_MAX_BATCH) return ATTN_ERR_SHAPE;
+  // Grid and index limits: (B*Hq) blocks along x; element counts fit int64.
+  const int64_t bhq = static_cast<int64_t>(s->B) * s->Hq;
+  if (bhq > (int64_t{1} << 31) - 1) return ATTN_ERR_SHAPE;
+  if (!supported_dims(s->d_h, s->d_v)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+// Effective mask parameters.  The visible set of row i in batch b is
+// { j < kv_len[b] } intersected, when causal, with { j <= i + offset }.
+// Because both bounds only grow with i, every row is non-empty iff row 0 is:
+// kv_len[b] >= 1 for every b and, when causal, offset >= 0.
+int build_mask(const attn_shape* s, const attn_mask* m, MaskParams* out) {
+  std::memset(out, 0, sizeof(*out));
+  if (!m) return ATTN_ERR_NULL;
+  if (m->reserved != 0 || (m->causal != 0 && m->causal != 1)) return ATTN_ERR_SHAPE;
+  out->causal = m->causal;
+  if (m->kv_len) {
+    out->has_kv_len = 1;
+    for (int b = 0; b < s->B; ++b) {
+      const int32_t L = m->kv_len[b];
+      if (L < 0 || L > s->n_k) return ATTN_ERR_SHAPE;
+      if (L == 0) return ATTN_ERR_EMPTY_ROW;
+      out->kv_len[b] = L;
+    }
+  }
+  if (m->causal) {
+    int64_t off = (m->causal_offset == ATTN_OFFSET_DEFAULT)
+                      ? static_cast<int64_t>(s->n_k) - static_cast<int64_t>(s->n_q)
+                      : m->causal_offset;
+    if (off < 0) return ATTN_ERR_EMPTY_ROW;
+    if (off > s->n_k) off = s->n_k;   // beyond n_k the causal bound never binds
+    out->offset = off;
+  }
+  return ATTN_OK;
+}
+
+int check_scale(float scale) {
+  return (std::isfinite(scale) && scale > 0.f) ? ATTN_OK : ATTN_ERR_SCALE;
+}
+
+int check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (!p) return ATTN_ERR_NULL;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Sum over query rows of max(0, lim(b, i)) for one batch element.
+int64_t pairs_one_batch(const MaskParams& m, int n_q, int n_k, int b) {
+  const int64_t L = key_len(m, n_k, b);
+  if (!m.causal) return L * n_q;
+  // Rows with i + offset + 1 < L see i + offset + 1 keys; the rest see L.
+  int64_t split = L - m.offset - 1;        // rows i < split are causal-bound
+  if (split < 0) split = 0;
+  if (split > n_q) split = n_q;
+  const int64_t head = split * (m.offset + 1) + split * (split - 1) / 2;
+  return head + (n_q - split) * L;
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-side helpers
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D view [bh][n][d] of a contiguous bf16 tensor, read in 128-row x 64-col
+// boxes with the 128-byte swizzle the tensor-core operand layout expects.
+// Rows beyond n of a head read as zeros (bounds fill), never the next head.
+bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  bool probed = false;
+  bool ok = false;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Checks that the current device is an sm_103 GPU and returns the device
+// address of its status word.
+int device_status_ptr(unsigned int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    void* sym = nullptr;
+    if (major == 10 && minor == 3) {
+      if (cudaGetSymbolAddress(&sym, g_attn_status) != cudaSuccess) return ATTN_ERR_CUDA;
+      d.status = static_cast<unsigned int*>(sym);
+      d.ok = true;
+    }
+    d.probed = true;
+  }
+  if (!d.ok) return ATTN_ERR_DEVICE;
+  *out = d.status;
+  return ATTN_OK;
+}
+
+ShapeParams shape_params(const attn_shape* s) {
+  ShapeParams sp;
+  sp.B = s->B;
+  sp.Hq = s->Hq;
+  sp.Hkv = s->Hkv;
+  sp.n_q = s->n_q;
+  sp.n_k = s->n_k;
+  sp.group = s->Hq / s->Hkv;
+  return sp;
+}
+
+int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq * s->n_q; }
+
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* status) {
+  __shared__ __align__(8) uint64_t never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&never), 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  // Nothing ever arrives on this barrier: the wait has to give up by itself.
+  const bool ok = mbar_wait(smem_u32(&never), 0, &abort_flag, limit_ns);
+  if (!ok && threadIdx.x == 0) atomicCAS(status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+}
+
+}  // namespace
+}  // namespace esd
+
+using namespace esd;
+
+extern "C" {
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+const char* attn_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid shape or mask parameters";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head widths (d_h, d_v)";
+    case ATTN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case ATTN_ERR_EMPTY_ROW: return "a query row has an empty visible set";
+    case ATTN_ERR_SCALE: return "scale must be finite and > 0";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ATTN_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case ATTN_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask) {
+  if (check_shape(shape) != ATTN_OK) return -1;
+  MaskParams m;
+  if (build_mask(shape, mask, &m) != ATTN_OK) return -1;
+  int64_t total = 0;
+  for (int b = 0; b < shape->B; ++b) total += pairs_one_batch(m, shape->n_q, shape->n_k, b);
+  return total * shape->Hq;
+}
+
+size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
+  if (check_shape(shape) != ATTN_OK) return 0;
+  const size_t rows = static_cast<size_t>(q_rows(shape));
+  return round256(rows * sizeof(float)) + round256(rows * static_cast<size_t>(shape->d_h) * sizeof(float));
+}
+
+int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
+             const void* V, void* O, float* LSE, void* stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  FwdParams p;
+  rc = build_mask(shape, mask, &p.mask);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_ptrs({Q, K, V, O, LSE});
+  if (rc) return rc;
+  // ---- CUDA from here on ----
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tq, tk, tv;
+  const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
+  const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
+  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
+      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk))
+    return ATTN_ERR_CUDA;
+  p.sh = shape_params(shape);
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.O = O;
+  p.LSE = LSE;
+  p.status = status;
+  const cudaError_t e =
+      launch_attn_fwd(shape->d_h, shape->d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* dO, float* D, float* dQacc,
+                        void* stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  rc = check_ptrs({O, dO, D, dQacc});
+  if (rc) return rc;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  const cudaError_t e = launch_attn_bwd_preprocess(q_rows(shape), shape->d_v, shape->d_h, O, dO, D, dQacc,
+                                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
+                  const void* V, const void* dO, const float* LSE, const float* D, float* dQacc, void* dK,
+                  void* dV, void* stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  BwdParams p;
+  rc = build_mask(shape, mask, &p.mask);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_ptrs({Q, K, V, dO, LSE, D, dQacc, dK, dV});
+  if (rc) return rc;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
+  const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
+  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
+      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, dO, shape->d_v, shape->n_q, bhq))
+    return ATTN_ERR_CUDA;
+  p.sh = shape_params(shape);
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.LSE = LSE;
+  p.D = D;
+  p.dQacc = dQacc;
+  p.dK = dK;
+  p.dV = dV;
+  p.status = status;
+  const cudaError_t e =
+      launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd_finalize(const attn_shape* shape, float scale, const float* dQacc, void* dQ, void* stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_ptrs({dQacc, dQ});
+  if (rc) return rc;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  const cudaError_t e = launch_attn_bwd_finalize(q_rows(shape) * shape->d_h, scale, dQacc, dQ,
+                                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
+             const void* V, const void* O, const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+             void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  MaskParams m;
+  rc = build_mask(shape, mask, &m);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV});
+  if (rc) return rc;
+  const size_t need = attn_bwd_workspace_bytes(shape);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  float* D = static_cast<float*>(workspace);
+  float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        round256(static_cast<size_t>(q_rows(shape)) * sizeof(float)));
+  rc = attn_bwd_preprocess(shape, O, dO, D, acc, stream);
+  if (rc) return rc;
+  rc = attn_bwd_main(shape, mask, scale, Q, K, V, dO, LSE, D, acc, dK, dV, stream);
+  if (rc) return rc;
+  return attn_bwd_finalize(shape, scale, acc, dQ, stream);
+}
+
+int attn_get_status(int* status) {
+  if (!status) return ATTN_ERR_NULL;
+  unsigned int* dev_status = nullptr;
+  const int rc = device_status_ptr(&dev_status);
+  if (rc) return rc;
+  unsigned int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpy(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  *status = static_cast<int>(v);
+  return ATTN_OK;
+}
+
+int attn_clear_status(void) {
+  unsigned int* dev_status = nullptr;
+  const int rc = device_status_ptr(&dev_status);
+  if (rc) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(dev_status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  unsigned int* dev_status = nullptr;
+  const int rc = device_status_ptr(&dev_status);
+  if (rc) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, dev_status);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,566 @@
+// attn_bwd.cu -- backward kernels of masked scaled dot-product attention on
+// sm_103a.
+//
+// What they compute ("Appendix A.10 -- Attention matrices and
+// backpropagation", eqs. A.10.5-A.10.9; "Chapter 31 -- attention backprop",
+// sections 2-4):
+//   dV = A^T dO,  dA = dO V^T,  dS = A .* (dA - c) with c_i = rowsum(dO .* O),
+//   dQ = scale dS K,  dK = scale dS^T Q,
+// with dK and dV summed over the query heads that share a KV head (A.10.5).
+// The weights A are never stored: the main kernel rebuilds them from the
+// scores and the forward's log-sum-exp, A_ij = exp(scale q_i.k_j - LSE_i)
+// (the recomputation the appendix names in section A.10.6).
+//
+// Three kernels:
+//   preprocess  D_i = sum_l dO_il O_il (equal to c_i of A.10.7 because
+//               O_i = sum_j A_ij v_j), and zeroes the fp32 dQ accumulator.
+//   main        one CTA per (batch, KV head, 128-key tile).  It loops over
+//               the query heads of its group and the query tiles that can
+//               see its keys, keeps dK and dV in tensor memory for the whole
+//               loop, and adds each tile's dS K product into the fp32 dQ
+//               accumulator with vector atomics.
+//   finalize    dQ = scale * accumulator, rounded to bf16.
+//
+// Main-kernel warp roles (384 threads):
+//   warp 0      TMA producer: the K and V tile once, then Q and dO tiles
+//               of every step into a two-stage ring.
+//   warp 1      MMA issuer (lane 0 issues; the warp zeroes padded K rows).
+//   warps 4-7   "score" warpgroup, thread = key row = TMEM lane:
+//               P^T = exp2(S^T scale log2e - LSE log2e) and
+//               dS^T = P^T (dP^T - D), written back to tensor memory (bf16)
+//               and dS to shared memory for the dQ product.
+//   warps 8-11  dQ read-out (atomics) and the final dK, dV epilogue.
+// Per step (query tile of 128 rows) the MMA order is
+//   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dK += dS^T Q,
+//   dQ = dS K -> X,
+// where tensor memory holds X [0,128), Y [128,256), dK [256, 256+DH) and
+// dV [256+DH, 256+DH+DV).  P^T and dS^T overwrite the first 64 columns of X
+// and Y once their fp32 inputs are consumed; dQ reuses X after the dV
+// product has read P^T (MMAs run in issue order).
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace esd {
+namespace {
+
+template <int DH, int DV>
+struct BwdCfg {
+  static constexpr int kStages = 2;
+  static constexpr int kKTileBytes = kTileN * DH * 2;
+  static constexpr int kVTileBytes = kTileN * DV * 2;
+  static constexpr int kQTileBytes = kTileM * DH * 2;
+  static constexpr int kDOTileBytes = kTileM * DV * 2;
+  static constexpr int kDSTileBytes = kTileN * kTileM * 2;
+  static constexpr int kBlockBytes = 128 * 128;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKTileBytes;
+  static constexpr int kOffQ = kOffV + kVTileBytes;
+  static constexpr int kOffDO = kOffQ + kStages * kQTileBytes;
+  static constexpr int kOffDS = kOffDO + kStages * kDOTileBytes;
+  static constexpr int kOffLse = kOffDS + kDSTileBytes;
+  static constexpr int kOffDd = kOffLse + kTileM * 4;
+  static constexpr int kOffBar = kOffDd + kTileM * 4;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarQFull = 1;                 // [2]
+  static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
+  static constexpr int kBarSFull = kBarQEmpty + 2;
+  static constexpr int kBarDPFull = kBarSFull + 1;
+  static constexpr int kBarPReady = kBarDPFull + 1;
+  static constexpr int kBarDSReady = kBarPReady + 1;
+  static constexpr int kBarDQFull = kBarDSReady + 1;
+  static constexpr int kBarDQFree = kBarDQFull + 1;
+  static constexpr int kBarDKDV = kBarDQFree + 1;
+  static constexpr int kBarLse = kBarDKDV + 1;        // score warps loaded LSE, D
+  static constexpr int kBarDrain = kBarLse + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemUsed = kOffAbort + 4;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(256 + DH + DV <= 512, "tensor memory budget");
+};
+
+template <int DH, int DV>
+__global__ void __launch_bounds__(384, 1)
+attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<DH, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int idx) -> uint32_t { return sbase + C::kOffBar + 8 * idx; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+  float* lse_s = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* dd_s = reinterpret_cast<float*>(smem + C::kOffDd);
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+
+  // ---- work item: key tile blockIdx.x of (batch, KV head) blockIdx.y ----
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.sh.Hkv;
+  const int hkv = bkv - b * p.sh.Hkv;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kTileN;
+  const int64_t i_first = first_row_seeing_key(p.mask, p.sh.n_q, p.sh.n_k, b, j0);
+  const int nqt = (p.sh.n_q + kTileM - 1) / kTileM;
+  const int qt_first = static_cast<int>(i_first / kTileM);
+  const int per_head = (i_first < p.sh.n_q) ? (nqt - qt_first) : 0;
+  const int total = per_head * p.sh.group;
+  auto step_head = [&](int s) { return hkv * p.sh.group + s / per_head; };
+  auto step_q0 = [&](int s) { return (qt_first + s % per_head) * kTileM; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarKV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kBarQFull + s), 1);
+      mbar_init(bar(C::kBarQEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarSFull), 1);
+    mbar_init(bar(C::kBarDPFull), 1);
+    mbar_init(bar(C::kBarPReady), 128);
+    mbar_init(bar(C::kBarDSReady), 128);
+    mbar_init(bar(C::kBarDQFull), 1);
+    mbar_init(bar(C::kBarDQFree), 128);
+    mbar_init(bar(C::kBarDKDV), 1);
+    mbar_init(bar(C::kBarLse), 128);
+    mbar_init(bar(C::kBarDrain), 1);
+    fence_mbar_init();
+    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+  auto wait_all = [&](int idx, uint32_t parity) -> bool {
+    const bool w = mbar_wait(bar(idx), parity, abort_flag, limit);
+    return __all_sync(0xffffffffu, w);
+  };
+
+  if (warp == 0) {
+    // =========================== TMA producer ===========================
+    if (lane == 0 && *abort_flag == 0 && total > 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmdO);
+      mbar_arrive_expect_tx(bar(C::kBarKV), C::kKTileBytes + C::kVTileBytes);
+      for (int c = 0; c < DH / 64; ++c)
+        tma_load_3d(sbase + C::kOffK + c * C::kBlockBytes, &tmK, bar(C::kBarKV), c * 64,
+                    static_cast<int32_t>(j0), bkv);
+      for (int c = 0; c < DV / 64; ++c)
+        tma_load_3d(sbase + C::kOffV + c * C::kBlockBytes, &tmV, bar(C::kBarKV), c * 64,
+                    static_cast<int32_t>(j0), bkv);
+      int issued[2] = {0, 0};
+      for (int s = 0; s < total; ++s) {
+        const int st = s & 1;
+        if (!mbar_wait(bar(C::kBarQEmpty + st), static_cast<uint32_t>(((s >> 1) & 1) ^ 1), abort_flag,
+                       limit))
+          break;
+        const int bhq = b * p.sh.Hq + step_head(s);
+        const int q0 = step_q0(s);
+        mbar_arrive_expect_tx(bar(C::kBarQFull + st), C::kQTileBytes + C::kDOTileBytes);
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_3d(sbase + C::kOffQ + st * C::kQTileBytes + c * C::kBlockBytes, &tmQ,
+                      bar(C::kBarQFull + st), c * 64, q0, bhq);
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(sbase + C::kOffDO + st * C::kDOTileBytes + c * C::kBlockBytes, &tmdO,
+                      bar(C::kBarQFull + st), c * 64, q0, bhq);
+        ++issued[st];
+      }
+      if (*abort_flag) {
+        int no_abort = 0;
+        mbar_wait(bar(C::kBarKV), 0, &no_abort, limit);
+        for (int st = 0; st < 2; ++st)
+          if (issued[st]) mbar_wait(bar(C::kBarQFull + st), (issued[st] - 1) & 1, &no_abort, limit);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ============================
+    if (*abort_flag == 0 && total > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV += P^T dO
+      constexpr uint32_t kIdDK = idesc_bf16_f32(128, DH, false, true);    // dK += dS^T Q
+      constexpr uint32_t kIdDQ = idesc_bf16_f32(128, DH, true, true);     // dQ = dS K
+      bool ok = wait_all(C::kBarKV, 0);
+      if (ok) {
+        // K rows in [kv_len, n_k) hold caller memory; their dS entries are 0
+        // but 0 * NaN would poison dQ, so they are zeroed.  Rows at or beyond
+        // n_k arrive as zeros from the TMA bounds check.
+        int64_t r0 = key_len(p.mask, p.sh.n_k, b) - j0, r1 = static_cast<int64_t>(p.sh.n_k) - j0;
+        if (r0 < 0) r0 = 0;
+        if (r1 > kTileN) r1 = kTileN;
+        if (r0 < r1) {
+          const int chunks = static_cast<int>(r1 - r0) * (DH / 64) * 8;
+          for (int q = static_cast<int>(lane); q < chunks; q += 32) {
+            const int row = static_cast<int>(r0) + q / ((DH / 64) * 8);
+            const int rem = q % ((DH / 64) * 8);
+            *reinterpret_cast<uint4*>(smem + C::kOffK + (rem / 8) * C::kBlockBytes + row * 128 +
+                                      (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+      }
+      const uint32_t kA = sbase + C::kOffK, vA = sbase + C::kOffV, dsA = sbase + C::kOffDS;
+      for (int s = 0; s < total && ok; ++s) {
+        const int st = s & 1;
+        ok = wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1));
+        if (!ok) break;
+        if (s > 0) {
+          ok = wait_all(C::kBarDQFree, static_cast<uint32_t>((s - 1) & 1));
+          if (!ok) break;
+        }
+        tc_fence_after_sync();
+        const uint32_t qB = sbase + C::kOffQ + st * C::kQTileBytes;
+        const uint32_t doB = sbase + C::kOffDO + st * C::kDOTileBytes;
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            umma_ss(tmem + C::kTX, sw128_desc(kA + off, 16, 1024), sw128_desc(qB + off, 16, 1024), kIdS,
+                    kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::kBarSFull));
+#pragma unroll
+          for (int kk = 0; kk < DV / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB + off, 16, 1024), kIdS,
+                    kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::kBarDPFull));
+        }
+        __syncwarp();
+        ok = wait_all(C::kBarPReady, static_cast<uint32_t>(s & 1));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            umma_ts(tmem + C::kTdV, tmem + C::kTX + kk * 8,
+                    sw128_desc(doB + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            umma_ts(tmem + C::kTdK, tmem + C::kTY + kk * 8,
+                    sw128_desc(qB + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            umma_ss(tmem + C::kTX, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
+                    sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::kBarDQFull));
+          umma_commit(bar(C::kBarQEmpty + st));
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        if (ok) umma_commit(bar(C::kBarDKDV));
+        int no_abort = 0;
+        umma_commit(bar(C::kBarDrain));
+        mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
+      }
+      __syncwarp();
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ============================ score warps ===========================
+    const uint32_t quad = warp & 3;
+    const int jj = static_cast<int>(quad * 32 + lane);
+    const int tid = static_cast<int>(threadIdx.x) - 128;
+    const int64_t j = j0 + jj;
+    const bool row_masked = j >= key_len(p.mask, p.sh.n_k, b);
+    const uint32_t lane_base = (quad * 32u) << 16;
+    const uint32_t tX = tmem + lane_base + C::kTX;
+    const uint32_t tY = tmem + lane_base + C::kTY;
+    const float sl2 = p.scale_log2;
+    uint8_t* ds_row = smem + C::kOffDS + jj * 128;
+    bool ok = *abort_flag == 0;
+    uint32_t rr[32];
+    uint32_t pw[64];
+    for (int s = 0; s < total && ok; ++s) {
+      const int bhq = b * p.sh.Hq + step_head(s);
+      const int q0 = step_q0(s);
+      // The single LSE/D buffer is rewritten only after every score thread
+      // has finished the previous step (its dS-ready barrier completed).
+      if (s > 0) {
+        ok = wait_all(C::kBarDSReady, static_cast<uint32_t>((s - 1) & 1));
+        if (!ok) break;
+      }
+      {
+        const int64_t i = static_cast<int64_t>(q0) + tid;
+        const bool in = i < p.sh.n_q;
+        lse_s[tid] = in ? p.LSE[static_cast<int64_t>(bhq) * p.sh.n_q + i] * kLog2e : INFINITY;
+        dd_s[tid] = in ? p.D[static_cast<int64_t>(bhq) * p.sh.n_q + i] : 0.f;
+      }
+      mbar_arrive(bar(C::kBarLse));
+      ok = wait_all(C::kBarLse, static_cast<uint32_t>(s & 1));
+      if (!ok) break;
+      // Column c (query q0 + c) is visible iff this key row is inside
+      // kv_len and, when causal, q0 + c >= j - offset.
+      const int64_t cmin64 = p.mask.causal ? (j - p.mask.offset - q0) : INT64_MIN / 2;
+      const int cmin = cmin64 > kTileM ? kTileM + 1 : (cmin64 < -1 ? -1 : static_cast<int>(cmin64));
+      const bool need_mask = __any_sync(0xffffffffu, row_masked || cmin > 0);
+      ok = wait_all(C::kBarSFull, static_cast<uint32_t>(s & 1));
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tX + cc * 32, rr);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const int c = cc * 32 + k;
+          float p0 = fast_exp2(fmaf(__uint_as_float(rr[k]), sl2, -lse_s[c]));
+          float p1 = fast_exp2(fmaf(__uint_as_float(rr[k + 1]), sl2, -lse_s[c + 1]));
+          if (need_mask) {
+            p0 = (!row_masked && c >= cmin) ? p0 : 0.f;
+            p1 = (!row_masked && c + 1 >= cmin) ? p1 : 0.f;
+          }
+          w[k >> 1] = pack_bf16x2(p0, p1);
+          pw[cc * 16 + (k >> 1)] = w[k >> 1];
+        }
+        tmem_st16(tX + cc * 16, w);
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::kBarPReady));
+      ok = wait_all(C::kBarDPFull, static_cast<uint32_t>(s & 1));
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tY + cc * 32, rr);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const int c = cc * 32 + k;
+          const uint32_t pp = pw[cc * 16 + (k >> 1)];
+          float d0 = bf16_lo(pp) * (__uint_as_float(rr[k]) - dd_s[c]);
+          float d1 = bf16_hi(pp) * (__uint_as_float(rr[k + 1]) - dd_s[c + 1]);
+          if (need_mask) {
+            d0 = (!row_masked && c >= cmin) ? d0 : 0.f;
+            d1 = (!row_masked && c + 1 >= cmin) ? d1 : 0.f;
+          }
+          w[k >> 1] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tY + cc * 16, w);
+        // dS (queries contiguous per key row) for the dQ = dS K product:
+        // block cc/2 holds queries [64*(cc/2), +64); 16-byte chunk index
+        // is XOR-swizzled with the key row (128-byte swizzle pattern).
+        uint8_t* blk = ds_row + (cc >> 1) * C::kBlockBytes;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int chunk = (cc & 1) * 4 + v;
+          *reinterpret_cast<uint4*>(blk + ((chunk ^ (jj & 7)) * 16)) =
+              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::kBarDSReady));
+    }
+  } else if (warp >= 8) {
+    // ===================== dQ read-out and dK/dV epilogue ================
+    const uint32_t quad = warp & 3;
+    const int row = static_cast<int>(quad * 32 + lane);
+    const uint32_t lane_base = (quad * 32u) << 16;
+    const uint32_t tX = tmem + lane_base + C::kTX;
+    bool ok = *abort_flag == 0;
+    uint32_t rr[32];
+    for (int s = 0; s < total && ok; ++s) {
+      const int bhq = b * p.sh.Hq + step_head(s);
+      const int64_t i = static_cast<int64_t>(step_q0(s)) + row;
+      ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
+      if (!ok) break;
+      tc_fence_after_sync();
+      float4* dst = reinterpret_cast<float4*>(p.dQacc + (static_cast<int64_t>(bhq) * p.sh.n_q + i) * DH);
+#pragma unroll
+      for (int cc = 0; cc < DH / 32; ++cc) {
+        tmem_ld32(tX + cc * 32, rr);
+        if (i < p.sh.n_q) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            atomicAdd(dst + cc * 8 + v,
+                      make_float4(__uint_as_float(rr[4 * v]), __uint_as_float(rr[4 * v + 1]),
+                                  __uint_as_float(rr[4 * v + 2]), __uint_as_float(rr[4 * v + 3])));
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::kBarDQFree));
+    }
+    if (ok && total > 0) {
+      ok = wait_all(C::kBarDKDV, 0);
+      tc_fence_after_sync();
+    }
+    if (ok) {
+      const int64_t j = j0 + row;
+      const bool in = j < p.sh.n_k;
+      const int64_t krow = static_cast<int64_t>(bkv) * p.sh.n_k + j;
+      uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + krow * DH);
+      uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + krow * DV);
+#pragma unroll
+      for (int cc = 0; cc < DH / 32; ++cc) {
+        uint32_t w[16];
+        if (total > 0) {
+          tmem_ld32(tmem + lane_base + C::kTdK + cc * 32, rr);
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * p.scale, __uint_as_float(rr[k + 1]) * p.scale);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) w[k] = 0u;
+        }
+        if (in) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dk[cc * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < DV / 32; ++cc) {
+        uint32_t w[16];
+        if (total > 0) {
+          tmem_ld32(tmem + lane_base + C::kTdV + cc * 32, rr);
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) w[k] = 0u;
+        }
+        if (in) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dv[cc * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+}
+
+// D_i = sum_l dO_il O_il: each row is read by DV/8 threads (16 bytes each)
+// and reduced with shuffles; the same grid zeroes the dQ accumulator.
+template <int DV>
+__global__ void __launch_bounds__(256)
+attn_bwd_preprocess_kernel(int64_t rows, const uint4* __restrict__ O, const uint4* __restrict__ dO,
+                           float* __restrict__ D, float4* __restrict__ dQacc, int64_t acc_vec4) {
+  constexpr int kG = DV / 8;   // threads per row
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gtid / kG;
+  const int part = static_cast<int>(gtid % kG);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = O[row * kG + part];
+    const uint4 g = dO[row * kG + part];
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = fmaf(bf16_lo(aw[k]), bf16_lo(gw[k]), acc);
+      acc = fmaf(bf16_hi(aw[k]), bf16_hi(gw[k]), acc);
+    }
+  }
+#pragma unroll
+  for (int off = kG / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) D[row] = acc;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k = gtid; k < acc_vec4; k += nthreads) dQacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = scale * acc, eight elements per thread per iteration.
+__global__ void __launch_bounds__(256)
+attn_bwd_finalize_kernel(int64_t n8, float scale, const float4* __restrict__ acc, uint4* __restrict__ dQ) {
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n8; k += nthreads) {
+    const float4 a = acc[2 * k];
+    const float4 c = acc[2 * k + 1];
+    dQ[k] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                       pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+  }
+}
+
+template <int DH, int DV>
+cudaError_t launch_bwd_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              const CUtensorMap& tmdO, const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<DH, DV>;
+  auto kern = attn_bwd_main_kernel<DH, DV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN), static_cast<unsigned>(p.sh.B * p.sh.Hkv));
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO, p);
+  return cudaGetLastError();
+}
+
+int grid_for(int64_t work_threads) {
+  int64_t blocks = (work_threads + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdParams& p,
+                                 cudaStream_t stream) {
+  if (dh == 128 && dv == 128) return launch_bwd_main_t<128, 128>(tmQ, tmK, tmV, tmdO, p, stream);
+  if (dh == 64 && dv == 64) return launch_bwd_main_t<64, 64>(tmQ, tmK, tmV, tmdO, p, stream);
+  if (dh == 128 && dv == 64) return launch_bwd_main_t<128, 64>(tmQ, tmK, tmV, tmdO, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* dO, float* D,
+                                       float* dQacc, cudaStream_t stream) {
+  const int64_t acc_vec4 = static_cast<int64_t>(rows) * dh / 4;
+  const int64_t row_threads = static_cast<int64_t>(rows) * (dv / 8);
+  const int64_t work = row_threads > acc_vec4 ? row_threads : acc_vec4;
+  int64_t blocks = (row_threads + 255) / 256;
+  const int64_t zero_blocks = grid_for(acc_vec4);
+  if (blocks < zero_blocks) blocks = zero_blocks;
+  (void)work;
+  if (dv == 128)
+    attn_bwd_preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(dO), D, reinterpret_cast<float4*>(dQacc),
+        acc_vec4);
+  else if (dv == 64)
+    attn_bwd_preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(dO), D, reinterpret_cast<float4*>(dQacc),
+        acc_vec4);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
+                                     cudaStream_t stream) {
+  const int64_t n8 = elems / 8;
+  attn_bwd_finalize_kernel<<<grid_for(n8), 256, 0, stream>>>(n8, scale, reinterpret_cast<const float4*>(dQacc),
+                                                           static_cast<uint4*>(dQ));
+  return cudaGetLastError();
+}
+
+}  // namespace esd

@@ -1,0 +1,441 @@
+// attn_fwd.cu -- forward kernel of masked scaled dot-product attention on
+// sm_103a: TMA-staged tiles, tcgen05 MMAs into tensor memory, and a
+// register-level online softmax.
+//
+// What it computes ("Appendix A.10 -- Attention matrices and
+// backpropagation", eqs. A.10.1-A.10.3): for each query row i,
+//   S_ij = scale q_i.k_j on the visible set, A = row softmax with the row
+//   maximum subtracted, O = A V, and LSE_i = m_i + ln sum_j exp(S_ij - m_i).
+// The blockwise evaluation visits the visible key tiles one at a time and
+// keeps a running maximum and running sum per row (the online softmax the
+// appendix mentions in section A.10.6); in real arithmetic it is the same
+// function, only the rounding order differs.
+//
+// CTA = two 128-row query tiles of one (batch, query head), sharing every
+// K/V tile the CTA loads.  Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K_j and V_j into rings.
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
+//               O_t += P_t V_j with P_t read back from tensor memory.
+//   warps 4-7   softmax for query tile 0 (thread = row = TMEM lane).
+//   warps 8-11  softmax for query tile 1.
+// While one tile's softmax runs, the tensor core works on the other tile.
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [t*128, t*128+128)   S_t (fp32); P_t (bf16 pairs) overwrites its first
+//                        64 columns once the scores are consumed.
+//   [256 + t*DV, ...)    O_t accumulator (fp32).
+//
+// Running-max rescaling is lazy: the reference maximum of a row moves only
+// when a new score exceeds it by more than 2^8 in the exp2 domain, so most
+// tiles skip the O rescale.  Both the numerator (O) and the denominator (l)
+// always use the same reference, so the result is unchanged in real
+// arithmetic and no term exceeds 2^8 before normalisation.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace esd {
+namespace {
+
+template <int DH, int DV>
+struct FwdCfg {
+  static constexpr int kQTiles = 2;
+  static constexpr int kKStages = (DH == 128) ? 2 : 3;
+  static constexpr int kVStages = (DV == 128) ? 2 : 3;
+  static constexpr int kQTileBytes = kTileM * DH * 2;
+  static constexpr int kKTileBytes = kTileN * DH * 2;
+  static constexpr int kVTileBytes = kTileN * DV * 2;
+  static constexpr int kBlockBytes = 128 * 128;       // one 128-row x 64-col bf16 block
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQTiles * kQTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kVTileBytes;
+  // barrier indices
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarKFull = 1;
+  static constexpr int kBarKEmpty = kBarKFull + kKStages;
+  static constexpr int kBarVFull = kBarKEmpty + kKStages;
+  static constexpr int kBarVEmpty = kBarVFull + kVStages;
+  static constexpr int kBarSFull = kBarVEmpty + kVStages;   // [2]
+  static constexpr int kBarPReady = kBarSFull + 2;          // [2]
+  static constexpr int kBarOFull = kBarPReady + 2;          // [2]
+  static constexpr int kBarDrain = kBarOFull + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemUsed = kOffAbort + 4;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;   // slack for 1024-byte alignment
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(2 * 128 + 2 * DV <= 512, "tensor memory budget");
+};
+
+template <int DH, int DV>
+__global__ void __launch_bounds__(384, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<DH, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int idx) -> uint32_t { return sbase + C::kOffBar + 8 * idx; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+
+  // ---- work item ----
+  const int bh = blockIdx.x;                        // b * Hq + r
+  const int b = bh / p.sh.Hq;
+  const int r = bh - b * p.sh.Hq;
+  const int bkv = b * p.sh.Hkv + r / p.sh.group;    // g(r) = r / (Hq / Hkv)
+  const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy first
+  int q0[2], ntiles[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    q0[t] = (pair * 2 + t) * kTileM;
+    ntiles[t] = kv_tiles_for_q_tile(p.mask, p.sh.n_q, p.sh.n_k, b, q0[t]);
+  }
+  const int nkv = ntiles[0] > ntiles[1] ? ntiles[0] : ntiles[1];
+
+  // ---- setup ----
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarQFull), 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarKEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(bar(C::kBarVFull + s), 1);
+      mbar_init(bar(C::kBarVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPReady + t), 128);
+      mbar_init(bar(C::kBarOFull + t), 1);
+    }
+    mbar_init(bar(C::kBarDrain), 1);
+    fence_mbar_init();
+    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // =========================== TMA producer ===========================
+    if (lane == 0 && *abort_flag == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      mbar_arrive_expect_tx(bar(C::kBarQFull), C::kQTiles * C::kQTileBytes);
+      for (int t = 0; t < C::kQTiles; ++t)
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_3d(sbase + C::kOffQ + t * C::kQTileBytes + c * C::kBlockBytes, &tmQ,
+                      bar(C::kBarQFull), c * 64, q0[t], bh);
+      int k_issued[C::kKStages > C::kVStages ? C::kKStages : C::kVStages] = {};
+      int v_issued[C::kKStages > C::kVStages ? C::kKStages : C::kVStages] = {};
+      bool ok = true;
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int ks = j % C::kKStages;
+        const uint32_t kph = static_cast<uint32_t>((j / C::kKStages) & 1);
+        ok = mbar_wait(bar(C::kBarKEmpty + ks), kph ^ 1u, abort_flag, limit);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kKTileBytes);
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_3d(sbase + C::kOffK + ks * C::kKTileBytes + c * C::kBlockBytes, &tmK,
+                      bar(C::kBarKFull + ks), c * 64, j * kTileN, bkv);
+        ++k_issued[ks];
+        const int vs = j % C::kVStages;
+        const uint32_t vph = static_cast<uint32_t>((j / C::kVStages) & 1);
+        ok = mbar_wait(bar(C::kBarVEmpty + vs), vph ^ 1u, abort_flag, limit);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kVTileBytes);
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(sbase + C::kOffV + vs * C::kVTileBytes + c * C::kBlockBytes, &tmV,
+                      bar(C::kBarVFull + vs), c * 64, j * kTileN, bkv);
+        ++v_issued[vs];
+      }
+      if (*abort_flag) {
+        // Let every copy already in flight land before the CTA can exit.
+        int no_abort = 0;
+        mbar_wait(bar(C::kBarQFull), 0, &no_abort, limit);
+        for (int s = 0; s < C::kKStages; ++s)
+          if (k_issued[s]) mbar_wait(bar(C::kBarKFull + s), (k_issued[s] - 1) & 1, &no_abort, limit);
+        for (int s = 0; s < C::kVStages; ++s)
+          if (v_issued[s]) mbar_wait(bar(C::kBarVFull + s), (v_issued[s] - 1) & 1, &no_abort, limit);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ============================
+    // The whole warp follows the schedule; lane 0 issues the MMAs.  The
+    // other lanes help zero padded V rows in shared memory.
+    if (*abort_flag == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
+      auto issue_qk = [&](int t, int ks) {
+        const uint32_t qa = sbase + C::kOffQ + t * C::kQTileBytes;
+        const uint32_t kb = sbase + C::kOffK + ks * C::kKTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          umma_ss(tmem + t * 128, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
+                  kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int vs, bool accumulate) {
+        const uint32_t vb = sbase + C::kOffV + vs * C::kVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          umma_ts(tmem + 256 + t * DV, tmem + t * 128 + kk * 8,
+                  sw128_desc(vb + kk * 16 * 128, C::kBlockBytes, 1024), kIdescPV,
+                  (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto wait_all = [&](int idx, uint32_t parity) -> bool {
+        const bool w = mbar_wait(bar(idx), parity, abort_flag, limit);
+        return __all_sync(0xffffffffu, w);
+      };
+      // Key rows in [kv_len, n_k) hold caller memory that may be anything
+      // (even NaN); their weights are exactly 0, but 0 * NaN would still
+      // poison O, so those V rows are zeroed before the PV product.  Rows
+      // at or beyond n_k arrive as zeros from the TMA bounds check.
+      const int64_t klen = key_len(p.mask, p.sh.n_k, b);
+      auto zero_padded_v = [&](int j, int vs) {
+        const int64_t j0 = static_cast<int64_t>(j) * kTileN;
+        int64_t r0 = klen - j0, r1 = static_cast<int64_t>(p.sh.n_k) - j0;
+        if (r0 < 0) r0 = 0;
+        if (r1 > kTileN) r1 = kTileN;
+        if (r0 >= r1) return;
+        uint8_t* vbase = smem + C::kOffV + vs * C::kVTileBytes;
+        const int chunks = static_cast<int>(r1 - r0) * (DV / 64) * 8;   // 16-byte chunks
+        for (int q = static_cast<int>(lane); q < chunks; q += 32) {
+          const int row = static_cast<int>(r0) + q / ((DV / 64) * 8);
+          const int rem = q % ((DV / 64) * 8);
+          *reinterpret_cast<uint4*>(vbase + (rem / 8) * C::kBlockBytes + row * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      };
+      bool ok = wait_all(C::kBarQFull, 0);
+      if (ok && nkv > 0) {
+        ok = wait_all(C::kBarKFull + 0, 0);
+        if (ok) {
+          tc_fence_after_sync();
+          if (lane == 0) {
+            for (int t = 0; t < 2; ++t)
+              if (ntiles[t] > 0) {
+                issue_qk(t, 0);
+                umma_commit(bar(C::kBarSFull + t));
+              }
+            umma_commit(bar(C::kBarKEmpty + 0));
+          }
+          __syncwarp();
+        }
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int vs = j % C::kVStages;
+        ok = wait_all(C::kBarVFull + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
+        if (!ok) break;
+        if (static_cast<int64_t>(j + 1) * kTileN > klen) zero_padded_v(j, vs);
+        const int kn = (j + 1) % C::kKStages;
+        bool k_next_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j < ntiles[t]) {
+            ok = wait_all(C::kBarPReady + t, static_cast<uint32_t>(j & 1));
+            if (!ok) break;
+            tc_fence_after_sync();
+            if (lane == 0) {
+              issue_pv(t, vs, j > 0);
+              if (j == ntiles[t] - 1) umma_commit(bar(C::kBarOFull + t));
+            }
+            __syncwarp();
+          }
+          if (j + 1 < ntiles[t]) {
+            if (!k_next_ready) {
+              ok = wait_all(C::kBarKFull + kn, static_cast<uint32_t>(((j + 1) / C::kKStages) & 1));
+              if (!ok) break;
+              tc_fence_after_sync();
+              k_next_ready = true;
+            }
+            if (lane == 0) {
+              issue_qk(t, kn);
+              umma_commit(bar(C::kBarSFull + t));
+            }
+            __syncwarp();
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          umma_commit(bar(C::kBarVEmpty + vs));
+          if (k_next_ready) umma_commit(bar(C::kBarKEmpty + kn));
+        }
+        __syncwarp();
+      }
+      // Every MMA issued above must finish before tensor memory is freed.
+      if (lane == 0) {
+        int no_abort = 0;
+        umma_commit(bar(C::kBarDrain));
+        mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
+      }
+      __syncwarp();
+    }
+  } else if (warp >= 4) {
+    // ============================== softmax =============================
+    const int t = (warp - 4) / 4;
+    const uint32_t quad = warp & 3;
+    const int row = static_cast<int>(quad * 32 + lane);
+    const int64_t i = static_cast<int64_t>(q0[t]) + row;
+    const int64_t lim = row_key_limit(p.mask, p.sh.n_k, b, i);
+    const uint32_t lane_base = (quad * 32u) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + 256 + t * DV;
+    const float sl2 = p.scale_log2;
+    float m_ref = -INFINITY;   // reference maximum, exp2 domain
+    float l_sum = 0.f;
+    bool ok = *abort_flag == 0;
+    uint32_t rr[32];
+    for (int j = 0; j < ntiles[t] && ok; ++j) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarSFull + t), static_cast<uint32_t>(j & 1), abort_flag, limit));
+      if (!ok) break;
+      tc_fence_after_sync();
+      int64_t lrel64 = lim - static_cast<int64_t>(j) * kTileN;
+      const int lim_rel = lrel64 > kTileN ? kTileN : (lrel64 < 0 ? 0 : static_cast<int>(lrel64));
+      const bool masked = __any_sync(0xffffffffu, lim_rel < kTileN);
+
+      // pass 1: row maximum of the visible scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tS + c * 32, rr);
+        if (masked) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float s = (c * 32 + k < lim_rel) ? __uint_as_float(rr[k]) : -INFINITY;
+            mx = fmaxf(mx, s);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(rr[k]));
+        }
+      }
+      const float m_new = fmaxf(m_ref, mx * sl2);
+      if (j == 0) {
+        m_ref = m_new;
+      } else {
+        const bool need = m_new > m_ref + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? fast_exp2(m_ref - m_new) : 1.0f;
+          if (need) {
+            l_sum *= alpha;
+            m_ref = m_new;
+          }
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            tmem_ld32(tO + c * 32, rr);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) rr[k] = __float_as_uint(__uint_as_float(rr[k]) * alpha);
+            tmem_st32(tO + c * 32, rr);
+          }
+        }
+      }
+      const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
+
+      // pass 2: P = exp2(S*scale*log2e - m_ref) -> bf16 into tensor memory
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tS + c * 32, rr);
+        uint32_t pw[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float p0 = fast_exp2(fmaf(__uint_as_float(rr[k]), sl2, -m_sub));
+          float p1 = fast_exp2(fmaf(__uint_as_float(rr[k + 1]), sl2, -m_sub));
+          if (masked) {
+            p0 = (c * 32 + k < lim_rel) ? p0 : 0.f;
+            p1 = (c * 32 + k + 1 < lim_rel) ? p1 : 0.f;
+          }
+          l_sum += p0 + p1;
+          pw[k >> 1] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pw);
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::kBarPReady + t));
+    }
+
+    // ---- epilogue: O = acc / l, LSE = (m_ref + log2 l) ln 2 ----
+    if (ok && ntiles[t] > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull + t), 0, abort_flag, limit));
+      tc_fence_after_sync();
+      if (ok) {
+        const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+        const bool in_range = i < p.sh.n_q;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) +
+                                               (static_cast<int64_t>(bh) * p.sh.n_q + i) * DV);
+#pragma unroll
+        for (int c = 0; c < DV / 32; ++c) {
+          tmem_ld32(tO + c * 32, rr);
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * inv_l, __uint_as_float(rr[k + 1]) * inv_l);
+          if (in_range) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              orow[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+        if (in_range)
+          p.LSE[static_cast<int64_t>(bh) * p.sh.n_q + i] = (m_ref + fast_log2(l_sum)) * kLn2;
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+}
+
+template <int DH, int DV>
+cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                         const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<DH, DV>;
+  auto kern = attn_fwd_kernel<DH, DV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int pairs = (p.sh.n_q + 2 * kTileM - 1) / (2 * kTileM);
+  dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hq), static_cast<unsigned>(pairs));
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream) {
+  if (dh == 128 && dv == 128) return launch_fwd_t<128, 128>(tmQ, tmK, tmV, p, stream);
+  if (dh == 64 && dv == 64) return launch_fwd_t<64, 64>(tmQ, tmK, tmV, p, stream);
+  if (dh == 128 && dv == 64) return launch_fwd_t<128, 64>(tmQ, tmK, tmV, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace esd

@@ -1,0 +1,176 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) masked scaled dot-product attention
+ * library, forward and backward.
+ *
+ * What is computed.  For every batch element b and query head r, with KV head
+ * h = g(r) = floor(r / (Hq / Hkv)) ("Appendix A.10 -- Attention matrices and
+ * backpropagation", section A.10.5: MHA when Hkv = Hq, MQA when Hkv = 1, GQA
+ * in between):
+ *   S_ij = scale * q_i . k_j              for j in the visible set V_i   (A.10.1)
+ *   A_ij = exp(S_ij - m_i) / sum_{r in V_i} exp(S_ir - m_i),
+ *          m_i = max_{j in V_i} S_ij, and A_ij = 0 off V_i               (A.10.2)
+ *   O    = A V                                                           (A.10.3)
+ *   LSE_i = m_i + ln sum_{j in V_i} exp(S_ij - m_i)
+ * and the backward pass, given dO = dL/dO:
+ *   dV   = A^T dO                                                        (A.10.5)
+ *   dA   = dO V^T                                                        (A.10.6)
+ *   dS_ij = A_ij (dA_ij - c_i) on V_i, 0 elsewhere,
+ *          c_i = sum_j A_ij dA_ij = sum_l dO_il O_il                     (A.10.7)
+ *   dQ   = scale * dS K,     dK = scale * dS^T Q                         (A.10.8-9)
+ * with dK, dV summed over the query heads that share a KV head (A.10.5).
+ * The usual scale is 1/sqrt(d_h); it is passed explicitly.
+ *
+ * Visible set.  V_i = { j : j < kv_len[b], and j <= i + causal_offset when
+ * causal }.  Causal self-attention is V_i = { j <= i } ("Appendix A.10",
+ * section A.10.6); for n_q != n_k the default offset n_k - n_q aligns the
+ * last query with the last key (a new chunk of queries over a long history,
+ * "Chapter 31 -- attention backprop", section 1).  kv_len is key padding.
+ * A row with an empty visible set is undefined (A.10.2) and rejected
+ * ("Chapter 31", section 3): every call checks this in closed form on the
+ * host and returns ATTN_ERR_EMPTY_ROW before launching anything.
+ *
+ * Layout.  All tensors are contiguous, row-major, innermost index last:
+ *   Q, dQ   [B][Hq ][n_q][d_h]  bf16        K, dK [B][Hkv][n_k][d_h] bf16
+ *   O, dO   [B][Hq ][n_q][d_v]  bf16        V, dV [B][Hkv][n_k][d_v] bf16
+ *   LSE, D  [B][Hq ][n_q]       fp32
+ * Supported head widths (d_h, d_v): (64, 64), (128, 128), (128, 64).
+ * Every tensor pointer must be 16-byte aligned.
+ *
+ * Ownership and execution.  The caller allocates and owns every buffer,
+ * including the backward workspace; the library allocates no device memory
+ * and keeps no state between calls other than a cached driver entry point.
+ * Device pointers refer to memory of the current CUDA device.  `stream` is a
+ * cudaStream_t (NULL = the legacy default stream); every call only enqueues
+ * work on it and returns without synchronising.  Host arrays (kv_len) are
+ * read during the call only.
+ *
+ * Errors.  Every function returns ATTN_OK (0) or one of the codes below; no
+ * exception or abort crosses the ABI.  Argument checks happen before any
+ * CUDA call.  Device-side failures (a bounded wait that ran out) are recorded
+ * in a device status word: attn_get_status() reads it; while it is set, the
+ * kernels return immediately without writing outputs, until
+ * attn_clear_status() resets it.
+ */
+#ifndef EXACT_SCALED_DOT_GB300_ATTN_H
+#define EXACT_SCALED_DOT_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+/* Status codes. */
+#define ATTN_OK               0
+#define ATTN_ERR_NULL         1  /* a required pointer is NULL                         */
+#define ATTN_ERR_SHAPE        2  /* non-positive size, Hq % Hkv != 0, kv_len out of   */
+                                 /* [1, n_k], B > ATTN_MAX_BATCH, size overflow         */
+#define ATTN_ERR_UNSUPPORTED  3  /* (d_h, d_v) not one of the supported pairs          */
+#define ATTN_ERR_ALIGN        4  /* a tensor pointer is not 16-byte aligned            */
+#define ATTN_ERR_EMPTY_ROW    5  /* some query row has an empty visible set            */
+#define ATTN_ERR_SCALE        6  /* scale is not finite or not > 0                     */
+#define ATTN_ERR_WORKSPACE    7  /* workspace NULL, misaligned or too small            */
+#define ATTN_ERR_CUDA         8  /* a CUDA runtime/driver call or launch failed        */
+#define ATTN_ERR_TIMEOUT      9  /* a kernel's bounded wait ran out (device status)    */
+#define ATTN_ERR_DEVICE      10  /* the current device is not an sm_103 GPU            */
+
+/* Largest batch whose per-batch key lengths travel with the launch. */
+#define ATTN_MAX_BATCH 512
+
+/* Sentinel for attn_mask.causal_offset: use n_k - n_q. */
+#define ATTN_OFFSET_DEFAULT INT64_MIN
+
+typedef struct {
+  int32_t B;    /* batch                                     */
+  int32_t Hq;   /* query heads                               */
+  int32_t Hkv;  /* key/value heads; Hq % Hkv == 0            */
+  int32_t n_q;  /* query rows per head                       */
+  int32_t n_k;  /* key rows per head                         */
+  int32_t d_h;  /* query/key width                           */
+  int32_t d_v;  /* value width                               */
+} attn_shape;
+
+typedef struct {
+  int32_t causal;          /* 0: no causal bound; 1: j <= i + causal_offset          */
+  int32_t reserved;        /* must be 0                                               */
+  int64_t causal_offset;   /* ATTN_OFFSET_DEFAULT, or an explicit offset (>= 0 keeps  */
+                           /* row 0 non-empty)                                        */
+  const int32_t* kv_len;   /* NULL (= n_k for all) or HOST array [B], each in [1,n_k] */
+} attn_mask;
+
+/* Forward pass (A.10.1-A.10.3).  Inputs Q, K, V (bf16, device); outputs
+ * O (bf16) and LSE (fp32, natural log), both device, fully overwritten. */
+int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
+             const void* Q, const void* K, const void* V,
+             void* O, float* LSE, void* stream);
+
+/* Bytes of device workspace attn_bwd needs: D (fp32 [B*Hq*n_q]) followed by
+ * an fp32 dQ accumulator [B*Hq*n_q*d_h], each 256-byte aligned.  Returns 0
+ * for an invalid shape. */
+size_t attn_bwd_workspace_bytes(const attn_shape* shape);
+
+/* Backward pass (A.10.5-A.10.9).  Q, K, V, O, LSE must be those of the
+ * forward call with the same mask and scale ("Chapter 31", section 3: the
+ * backward must use the forward's semantics).  dO is the upstream gradient.
+ * Outputs dQ, dK, dV (bf16, device) are fully overwritten; dK and dV hold the
+ * sums over each KV head's query heads.  `workspace` is caller-owned device
+ * memory of at least attn_bwd_workspace_bytes(shape) bytes, 256-byte aligned;
+ * its contents on entry do not matter.  Equivalent to the three stage calls
+ * below, in order. */
+int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
+             const void* Q, const void* K, const void* V,
+             const void* O, const void* dO, const float* LSE,
+             void* dQ, void* dK, void* dV,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage 1 of the backward: D_i = sum_l dO_il O_il (= c_i of A.10.7) into the
+ * fp32 array D [B*Hq*n_q], and zero the fp32 accumulator dQacc
+ * [B*Hq*n_q*d_h]. */
+int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* dO,
+                        float* D, float* dQacc, void* stream);
+
+/* Stage 2: the key-tile-stationary main kernel.  Recomputes A from Q, K and
+ * LSE, writes dK (scaled) and dV (bf16) and adds the unscaled dS K products
+ * into dQacc (fp32, zeroed by stage 1). */
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale,
+                  const void* Q, const void* K, const void* V, const void* dO,
+                  const float* LSE, const float* D, float* dQacc,
+                  void* dK, void* dV, void* stream);
+
+/* Stage 3: dQ = scale * dQacc, rounded to bf16. */
+int attn_bwd_finalize(const attn_shape* shape, float scale, const float* dQacc,
+                      void* dQ, void* stream);
+
+/* Number of visible (i, j) pairs over all batch elements and query heads,
+ * from the same closed form the kernels use to classify tiles; -1 on an
+ * invalid shape or mask.  Host only. */
+int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask);
+
+/* Device status word of the current device: ATTN_OK, or the first failure a
+ * kernel recorded (ATTN_ERR_TIMEOUT).  Synchronises the device.  Writes the
+ * status to *status and returns ATTN_OK, or ATTN_ERR_CUDA. */
+int attn_get_status(int* status);
+
+/* Reset the device status word to ATTN_OK.  Synchronises the device. */
+int attn_clear_status(void);
+
+/* Failure-detection self test: launches one tiny kernel that waits on a
+ * barrier nothing will complete, with a limit of `limit_ns` nanoseconds, so
+ * the bounded-wait path records ATTN_ERR_TIMEOUT in the status word and the
+ * kernel returns.  Enqueued on `stream`. */
+int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* attn_strerror(int status);
+
+/* ATTN_ABI_VERSION of the loaded library. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_SCALED_DOT_GB300_ATTN_H */

@@ -1,0 +1,145 @@
+"""Host-side tests of the C ABI: the library builds, loads and exports every
+symbol include/attn.h declares, and argument checks reject bad calls before
+any CUDA call (so they run without a GPU)."""
+import ctypes
+import math
+import re
+from pathlib import Path
+
+import pytest
+
+import exact_scaled_dot_gb300 as esd
+from exact_scaled_dot_gb300 import _binding as bnd
+from exact_scaled_dot_gb300.build import build
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "attn.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return esd.load()
+
+
+def _declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_exactly_the_bound_symbols():
+    assert sorted(bnd.EXPORTS) == _declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert esd.attn_abi_version() == 1
+
+
+def test_strerror_covers_every_code(lib):
+    codes = [getattr(bnd, n) for n in dir(bnd) if n.startswith("ATTN_ERR_") or n == "ATTN_OK"]
+    for c in codes:
+        assert lib.attn_strerror(c).decode() not in ("", "unknown status")
+    assert lib.attn_strerror(999).decode() == "unknown status"
+
+
+def _call_fwd(lib, shape, mask, scale=None, ptr=256):
+    p = ctypes.c_void_p(ptr)
+    scale = 1.0 / math.sqrt(max(shape.d_h, 1)) if scale is None else scale
+    return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None,
+                        ctypes.c_float(scale), p, p, p, p, p, None)
+
+
+def _mask(causal=0, offset=bnd.ATTN_OFFSET_DEFAULT, kv=None, reserved=0):
+    keep = None
+    ptr = ctypes.POINTER(ctypes.c_int32)()
+    if kv is not None:
+        keep = (ctypes.c_int32 * len(kv))(*kv)
+        ptr = ctypes.cast(keep, ctypes.POINTER(ctypes.c_int32))
+    m = bnd.AttnMask(causal, reserved, offset, ptr)
+    m._keep = keep
+    return m
+
+
+GOOD = dict(B=2, Hq=4, Hkv=2, n_q=100, n_k=100, d_h=128, d_v=128)
+
+
+def _shape(**kw):
+    d = dict(GOOD)
+    d.update(kw)
+    return bnd.make_shape(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), bnd.ATTN_ERR_SHAPE),
+    (dict(n_q=-1), bnd.ATTN_ERR_SHAPE),
+    (dict(Hq=3), bnd.ATTN_ERR_SHAPE),
+    (dict(B=bnd.ATTN_MAX_BATCH + 1), bnd.ATTN_ERR_SHAPE),
+    (dict(d_h=96, d_v=96), bnd.ATTN_ERR_UNSUPPORTED),
+    (dict(d_h=64, d_v=128), bnd.ATTN_ERR_UNSUPPORTED),
+])
+def test_bad_shapes_rejected(lib, kw, code):
+    assert _call_fwd(lib, _shape(**kw), _mask()) == code
+
+
+def test_empty_rows_rejected_in_closed_form(lib):
+    # causal with a negative offset: row 0 sees nothing ("Chapter 31", section 3).
+    assert _call_fwd(lib, _shape(), _mask(causal=1, offset=-1)) == bnd.ATTN_ERR_EMPTY_ROW
+    # default bottom-right alignment with more queries than keys: first rows empty.
+    assert _call_fwd(lib, _shape(n_q=200, n_k=100), _mask(causal=1)) == bnd.ATTN_ERR_EMPTY_ROW
+    # a batch element with no keys.
+    assert _call_fwd(lib, _shape(), _mask(kv=[100, 0])) == bnd.ATTN_ERR_EMPTY_ROW
+
+
+def test_bad_masks_rejected(lib):
+    assert _call_fwd(lib, _shape(), _mask(kv=[100, 101])) == bnd.ATTN_ERR_SHAPE
+    assert _call_fwd(lib, _shape(), _mask(kv=[-3, 10])) == bnd.ATTN_ERR_SHAPE
+    assert _call_fwd(lib, _shape(), _mask(reserved=1)) == bnd.ATTN_ERR_SHAPE
+    assert _call_fwd(lib, _shape(), _mask(causal=2)) == bnd.ATTN_ERR_SHAPE
+    assert _call_fwd(lib, _shape(), None) == bnd.ATTN_ERR_NULL
+
+
+def test_bad_scale_and_pointers_rejected(lib):
+    assert _call_fwd(lib, _shape(), _mask(), scale=0.0) == bnd.ATTN_ERR_SCALE
+    assert _call_fwd(lib, _shape(), _mask(), scale=float("nan")) == bnd.ATTN_ERR_SCALE
+    assert _call_fwd(lib, _shape(), _mask(), scale=-1.0) == bnd.ATTN_ERR_SCALE
+    assert _call_fwd(lib, _shape(), _mask(), ptr=0) == bnd.ATTN_ERR_NULL
+    assert _call_fwd(lib, _shape(), _mask(), ptr=0x1008) == bnd.ATTN_ERR_ALIGN
+
+
+def test_bwd_workspace_checks(lib):
+    s = _shape()
+    need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
+    rows = 2 * 4 * 100
+    assert need == ((rows * 4 + 255) // 256) * 256 + ((rows * 128 * 4 + 255) // 256) * 256
+    p = ctypes.c_void_p(256)
+    m = _mask()
+    args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 9
+    assert lib.attn_bwd(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(_shape(B=0))) == 0
+
+
+def test_visible_pairs_closed_form(lib, orc):
+    """The library's closed form equals the oracle's pair-by-pair count."""
+    import oracle
+    cases = [
+        dict(B=2, Hq=2, Hkv=1, n_q=37, n_k=37, causal=True, offset=None, kv=[37, 20]),
+        dict(B=1, Hq=3, Hkv=3, n_q=10, n_k=50, causal=True, offset=None, kv=None),
+        dict(B=3, Hq=1, Hkv=1, n_q=20, n_k=30, causal=True, offset=4, kv=[30, 1, 9]),
+        dict(B=2, Hq=2, Hkv=2, n_q=7, n_k=40, causal=False, offset=None, kv=[40, 13]),
+        dict(B=1, Hq=1, Hkv=1, n_q=5, n_k=8, causal=True, offset=100, kv=None),
+    ]
+    for c in cases:
+        got = esd.attn_visible_pairs(c["B"], c["Hq"], c["Hkv"], c["n_q"], c["n_k"], 64, 64, causal=c["causal"],
+                                     causal_offset=c["offset"], kv_len=c["kv"])
+        p = oracle.Problem(c["B"], c["Hq"], c["Hkv"], c["n_q"], c["n_k"], 64, 64, causal=c["causal"],
+                           offset=c["offset"], kv_len=c["kv"])
+        assert got == orc.visible_pairs(p), c
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        bnd.load(tmp_path / "nope.so")
