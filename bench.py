@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark: masked attention forward + backward on GB300, one JSON line.
+
+A step is one forward and one backward pass (every kernel of the path) over
+the causal GQA workload with key padding (B=2, Hq=32, Hkv=8, n=4096,
+d_h=d_v=128, per-batch key lengths uniform in [2048, 4096]) -- the n=4096,
+d=128 causal configuration the throughput target is stated on.  The value is
+TFLOP/s counted on visible (i, j) pairs only: 2(d_h+d_v) FLOPs per pair
+forward and 2(2 d_h + 3 d_v) backward, summed over all ranks.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun each rank runs its own full replica (the path needs no
+exchange between GPUs); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "attention fwd+bwd TFLOP/s (visible pairs) and % of GB300 dense-BF16 peak"
+DEFAULT_WORKLOAD = "gqa_causal_padded"
+PEAKS_FILE = ROOT / "MEASURED_PEAKS.json"
+TRAFFIC_FILE = ROOT / "profiles" / "ncu_traffic.json"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# Helpers shared by both arms
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def flops_per_pair(dh: int, dv: int):
+    return 2 * (dh + dv), 2 * (2 * dh + 3 * dv)
+
+
+def load_peaks():
+    if PEAKS_FILE.exists():
+        try:
+            d = json.loads(PEAKS_FILE.read_text())
+            return d, "measured"
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "exact_scaled_dot_gb300" / "csrc").glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.error = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            self.error = "nvidia-smi not found"
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                [exe, f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError as e:
+            self.error = str(e)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.error or "not sampled"}
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"error": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(r[1]) for r in rows) if v is not None)
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_cpu_sample(w, inp, rows: int):
+    """Time the fp64 oracle (forward + backward) on a bounded sub-problem of the
+    workload: batch 0, KV head 0 with its query heads, the first `rows` query
+    rows and the keys they can see.  Returns (TFLOP/s, description, threads)."""
+    import numpy as np
+    import oracle
+
+    orc = oracle.default()
+    g = w.Hq // w.Hkv
+    n_q = min(rows, w.nq)
+    L0 = int(inp.kv_len[0]) if inp.kv_len is not None else w.nk
+    if w.causal:
+        n_k = min(w.nk, L0, n_q + w.causal_offset)
+    else:
+        n_k = min(w.nk, L0)
+    n_k = max(n_k, 1)
+    off = w.causal_offset if w.causal else None
+    p = oracle.Problem(1, g, 1, n_q, n_k, w.dh, w.dv, causal=w.causal, offset=off, kv_len=None)
+    f64 = lambda t: t.to(__import__("torch").float64).numpy()  # noqa: E731
+    Q = f64(inp.Q[0:1, 0:g, :n_q])
+    K = f64(inp.K[0:1, 0:1, :n_k])
+    V = f64(inp.V[0:1, 0:1, :n_k])
+    G = f64(inp.dO[0:1, 0:g, :n_q])
+    pairs = orc.visible_pairs(p)
+    ff, fb = flops_per_pair(w.dh, w.dv)
+    t0 = time.perf_counter()
+    orc.forward(p, Q, K, V)
+    orc.backward(p, Q, K, V, G)
+    dt = time.perf_counter() - t0
+    desc = (f"batch 0, KV head 0 with its {g} query heads, first {n_q} query rows over {n_k} keys "
+            f"({pairs} visible pairs), fp64 forward+backward")
+    return pairs * (ff + fb) / dt / 1e12, desc, orc.threads, dt
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from exact_scaled_dot_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    rows = args.reference_rows
+    for _ in range(max(0, args.warmup)):
+        oracle_cpu_sample(w, inp, min(rows, 64))
+    vals, times = [], []
+    desc, threads = "", 0
+    for _ in range(args.steps):
+        v, desc, threads, dt = oracle_cpu_sample(w, inp, rows)
+        vals.append(v)
+        times.append(dt)
+    value = len(vals) / sum(1.0 / v for v in vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) draws rounded to bf16, upcast to fp64)",
+        "config": {"workload": w.name, "sample_of": "see cpu_baseline.sample"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# CUDA arm
+# ---------------------------------------------------------------------------
+def run_cuda(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from exact_scaled_dot_gb300 import build as lib_build
+    if rank == 0 or world == 1:
+        lib_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    import exact_scaled_dot_gb300 as esd
+    from exact_scaled_dot_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    kv = None if inp.kv_len is None else inp.kv_len.tolist()
+    off = w.causal_offset if w.causal else None
+    mask = dict(causal=w.causal, causal_offset=off, kv_len=kv)
+    shape = esd.make_shape(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv)
+    pairs = esd.attn_visible_pairs(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv, **mask)
+    ff, fb = flops_per_pair(w.dh, w.dv)
+    flops_fwd, flops_bwd = pairs * ff, pairs * fb
+    scale = 1.0 / math.sqrt(w.dh)
+
+    Q, K, V, dO = (x.to(dev) for x in (inp.Q, inp.K, inp.V, inp.dO))
+    O = torch.empty((w.B, w.Hq, w.nq, w.dv), dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty((w.B, w.Hq, w.nq), dtype=torch.float32, device=dev)
+    O_lo = torch.empty_like(O)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    rows = w.B * w.Hq * w.nq
+    D = torch.empty((rows,), dtype=torch.float32, device=dev)
+    dQacc = torch.empty((rows * w.dh,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    esd.attn_clear_status()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        esd.attn_fwd(Q, K, V, scale=scale, O=O, LSE=LSE, O_lo=O_lo, **mask)
+        if ev is not None:
+            ev[1].record(stream)
+        esd.attn_bwd_preprocess(O, dO, D, dQacc, shape=shape, O_lo=O_lo)
+        if ev is not None:
+            ev[2].record(stream)
+        esd.attn_bwd_main(Q, K, V, dO, LSE, D, dQacc, dK, dV, shape=shape, scale=scale, **mask)
+        if ev is not None:
+            ev[3].record(stream)
+        esd.attn_bwd_finalize(dQacc, dQ, shape=shape, scale=scale)
+        if ev is not None:
+            ev[4].record(stream)
+
+    launches_per_step = 4
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-timed region: K steps, inputs resident in HBM ----
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_stop.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    status = esd.attn_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {esd.strerror(status)}")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * (flops_fwd + flops_bwd) / (ms_per_step * 1e-3) / 1e12
+
+    names = ["attn_fwd_kernel", "attn_bwd_preprocess_kernel", "attn_bwd_main_kernel", "attn_bwd_finalize_kernel"]
+    per_kernel = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i, n in enumerate(names)}
+
+    # ---- roofline of the dominant kernel ----
+    peaks, peak_src = load_peaks()
+    bhq = w.B * w.Hq
+    bytes_io = {
+        "attn_bwd_preprocess_kernel": rows * w.dv * 2 * 3 + rows * 4 + rows * w.dh * 4,
+        "attn_bwd_finalize_kernel": rows * w.dh * 4 + rows * w.dh * 2,
+    }
+    dominant = max(per_kernel, key=per_kernel.get)
+    if dominant in ("attn_fwd_kernel", "attn_bwd_main_kernel"):
+        work = flops_fwd if dominant == "attn_fwd_kernel" else flops_bwd
+        achieved = work / (per_kernel[dominant] * 1e-3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": f"bf16_tflops_sustained ({peak_src})"}
+    else:
+        achieved = bytes_io[dominant] / (per_kernel[dominant] * 1e-3) / 1e9
+        peak = peaks.get("hbm_gbs")
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": f"hbm_gbs ({peak_src})"}
+    roof["kernel"] = dominant
+    roof["traffic"] = None
+    if TRAFFIC_FILE.exists():
+        try:
+            tr = json.loads(TRAFFIC_FILE.read_text())
+            ent = tr.get("kernels", {}).get(dominant)
+            if ent and tr.get("source_digest") == source_digest() and tr.get("workload") == w.name:
+                roof["traffic"] = ent.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            pass
+    kernels = {}
+    for n in names:
+        ms = per_kernel[n]
+        ent = {"ms": ms, "share": ms / sum(per_kernel.values())}
+        if n == "attn_fwd_kernel":
+            ent["tflops"] = flops_fwd / (ms * 1e-3) / 1e12
+        elif n == "attn_bwd_main_kernel":
+            ent["tflops"] = flops_bwd / (ms * 1e-3) / 1e12
+        else:
+            ent["gbs"] = bytes_io[n] / (ms * 1e-3) / 1e9
+        kernels[n] = ent
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()  # noqa: E731
+        hQ, hK, hV, hdO = (pin(x) for x in (inp.Q, inp.K, inp.V, inp.dO))
+        hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+        hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+        hdQ, hdK, hdV = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dQ, dK, dV))
+        ws = torch.empty((esd.attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv),),
+                         dtype=torch.uint8, device=dev)
+        h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hdO))
+        d2h = sum(x.numel() * x.element_size() for x in (hO, hL, hdQ, hdK, hdV))
+
+        def e2e_step():
+            Q.copy_(hQ, non_blocking=True)
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            dO.copy_(hdO, non_blocking=True)
+            esd.attn_fwd(Q, K, V, scale=scale, O=O, LSE=LSE, O_lo=O_lo, **mask)
+            esd.attn_bwd(Q, K, V, O, dO, LSE, O_lo=O_lo, scale=scale, dQ=dQ, dK=dK, dV=dV, workspace=ws, **mask)
+            hO.copy_(O, non_blocking=True)
+            hL.copy_(LSE, non_blocking=True)
+            hdQ.copy_(dQ, non_blocking=True)
+            hdK.copy_(dK, non_blocking=True)
+            hdV.copy_(dV, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b) / args.steps
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * (flops_fwd + flops_bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # ---- parity spot check (oracle rows, forward and dQ) and CPU baseline ----
+    parity = None
+    cpu = None
+    if rank == 0 and not args.no_oracle:
+        import oracle
+        orc = oracle.default()
+        p = oracle.Problem(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv, causal=w.causal, offset=off, kv_len=kv)
+        rng = np.random.default_rng(0)
+        rsel = np.unique(np.concatenate([[0, rows - 1], rng.integers(0, rows, 30)]))
+        f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()  # noqa: E731
+        Qn, Kn, Vn, Gn = (f64(x) for x in (inp.Q, inp.K, inp.V, inp.dO))
+        rO, rL = orc.forward(p, Qn, Kn, Vn, rows=rsel)
+        rdQ, _, _, _, _ = orc.backward(p, Qn, Kn, Vn, Gn, q_rows=rsel, want_dkdv=False)
+        # outputs of the last device-timed step
+        gO = f64(O).reshape(-1, w.dv)[rsel]
+        gL = f64(LSE).reshape(-1)[rsel]
+        gQ = f64(dQ).reshape(-1, w.dh)[rsel]
+        ok = bool(np.all(np.abs(gO - rO) <= 1e-2 + 2e-2 * np.abs(rO)) and np.all(np.abs(gL - rL) <= 1e-3)
+                  and np.all(np.abs(gQ - rdQ) <= 1e-2 + 2e-2 * np.abs(rdQ)))
+        parity = {"rows_checked": int(rsel.size), "ok": ok,
+                  "max_abs_err": {"O": float(np.max(np.abs(gO - rO))), "LSE": float(np.max(np.abs(gL - rL))),
+                                  "dQ": float(np.max(np.abs(gQ - rdQ)))}}
+        v, desc, threads, _dt = oracle_cpu_sample(w, inp, args.cpu_rows)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) draws rounded to bf16; random key lengths)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n_q": w.nq, "n_k": w.nk,
+                       "d_h": w.dh, "d_v": w.dv, "causal": w.causal, "kv_len": kv, "seed": w.seed,
+                       "visible_pairs": pairs, "flops_per_step": flops_fwd + flops_bwd,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (about %.0f MB touched per step)" % (
+                           sum(x.numel() * x.element_size() for x in (Q, K, V, dO, O, O_lo, LSE, dQ, dK, dV, dQacc))
+                           / 1e6)},
+            "peak_fraction": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+            "roofline": roof,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "parity": parity,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-rows", type=int, default=768, help="query rows in the timed oracle sample")
+    ap.add_argument("--reference-rows", type=int, default=384, help="query rows per reference-arm step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-oracle", action="store_true", help="skip the parity spot check and CPU baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 0 or args.steps < 1:
+        ap.error("need --steps >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_cuda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -68,11 +68,12 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(str(p))
     S, M = ctypes.POINTER(AttnShape), ctypes.POINTER(AttnMask)
     f = ctypes.c_float
-    lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.attn_bwd_workspace_bytes.argtypes = [S]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                             _vp]
+    lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.attn_bwd_finalize.argtypes = [S, f, _vp, _vp, _vp]
     lib.attn_visible_pairs.argtypes = [S, M]
@@ -173,8 +174,13 @@ def _check_qkv(Q, K, V):
 # ---------------------------------------------------------------------------
 def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
              causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
-             O: Optional[torch.Tensor] = None, LSE: Optional[torch.Tensor] = None, stream=None):
-    """Forward pass: returns (O [B,Hq,n_q,d_v] bf16, LSE [B,Hq,n_q] fp32)."""
+             O: Optional[torch.Tensor] = None, LSE: Optional[torch.Tensor] = None,
+             O_lo: Optional[torch.Tensor] = None, residual: bool = True, stream=None):
+    """Forward pass: returns (O [B,Hq,n_q,d_v] bf16, LSE [B,Hq,n_q] fp32, O_lo).
+
+    O_lo is the bf16 rounding residual of O (O + O_lo ~ the fp32 result), for
+    the backward's row term; it is None when ``residual`` is False and no
+    O_lo tensor is given."""
     dims, dev = _check_qkv(Q, K, V)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
@@ -182,14 +188,18 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool 
         O = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
     if LSE is None:
         LSE = torch.empty((B, Hq, n_q), dtype=torch.float32, device=dev)
+    if O_lo is None and residual:
+        O_lo = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
     _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
     _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
+    if O_lo is not None:
+        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
     rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
-                         _ptr(V), _ptr(O), _ptr(LSE), _stream(dev, stream))
+                         _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), _stream(dev, stream))
     _check(rc, "attn_fwd")
-    return O, LSE
+    return O, LSE, O_lo
 
 
 def attn_bwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
@@ -197,8 +207,8 @@ def attn_bwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
     return int(load().attn_bwd_workspace_bytes(ctypes.byref(shape)))
 
 
-def attn_bwd(Q, K, V, O, dO, LSE, *, causal: bool = False, causal_offset: Optional[int] = None, kv_len=None,
-             scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_offset: Optional[int] = None,
+             kv_len=None, scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
     """Backward pass: returns (dQ, dK, dV) in bf16; dK, dV summed over each KV head's group."""
     dims, dev = _check_qkv(Q, K, V)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
@@ -206,6 +216,8 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, causal: bool = False, causal_offset: Option
     _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
     _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev)
     _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
+    if O_lo is not None:
+        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
     if dQ is None:
         dQ = torch.empty_like(Q)
     if dK is None:
@@ -223,14 +235,15 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, causal: bool = False, causal_offset: Option
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
     rc = load().attn_bwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
-                         _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                         _ptr(V), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+                         _ptr(workspace),
                          ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
     _check(rc, "attn_bwd")
     return dQ, dK, dV
 
 
-def attn_bwd_preprocess(O, dO, D, dQacc, *, shape: AttnShape, stream=None):
-    rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(O), _ptr(dO), _ptr(D), _ptr(dQacc),
+def attn_bwd_preprocess(O, dO, D, dQacc, *, shape: AttnShape, O_lo=None, stream=None):
+    rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(D), _ptr(dQacc),
                                     _stream(O.device, stream))
     _check(rc, "attn_bwd_preprocess")
 

@@ -240,7 +240,7 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
 }
 
 int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-             const void* V, void* O, float* LSE, void* stream) {
+             const void* V, void* O, float* LSE, void* O_lo, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   FwdParams p;
@@ -250,6 +250,7 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, LSE});
   if (rc) return rc;
+  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   // ---- CUDA from here on ----
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
@@ -264,6 +265,7 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
   p.O = O;
+  p.O_lo = O_lo;
   p.LSE = LSE;
   p.status = status;
   const cudaError_t e =
@@ -271,17 +273,18 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* dO, float* D, float* dQacc,
-                        void* stream) {
+int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo, const void* dO, float* D,
+                        float* dQacc, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   rc = check_ptrs({O, dO, D, dQacc});
   if (rc) return rc;
+  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  const cudaError_t e = launch_attn_bwd_preprocess(q_rows(shape), shape->d_v, shape->d_h, O, dO, D, dQacc,
-                                                   static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_attn_bwd_preprocess(q_rows(shape), shape->d_v, shape->d_h, O, O_lo, dO, D,
+                                                   dQacc, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -337,8 +340,8 @@ int attn_bwd_finalize(const attn_shape* shape, float scale, const float* dQacc, 
 }
 
 int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-             const void* V, const void* O, const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-             void* workspace, size_t workspace_bytes, void* stream) {
+             const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
+             void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   MaskParams m;
@@ -348,13 +351,14 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV});
   if (rc) return rc;
+  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   const size_t need = attn_bwd_workspace_bytes(shape);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
     return ATTN_ERR_WORKSPACE;
   float* D = static_cast<float*>(workspace);
   float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                         round256(static_cast<size_t>(q_rows(shape)) * sizeof(float)));
-  rc = attn_bwd_preprocess(shape, O, dO, D, acc, stream);
+  rc = attn_bwd_preprocess(shape, O, O_lo, dO, D, acc, stream);
   if (rc) return rc;
   rc = attn_bwd_main(shape, mask, scale, Q, K, V, dO, LSE, D, acc, dK, dV, stream);
   if (rc) return rc;

@@ -14,6 +14,9 @@
 // Three kernels:
 //   preprocess  D_i = sum_l dO_il O_il (equal to c_i of A.10.7 because
 //               O_i = sum_j A_ij v_j), and zeroes the fp32 dQ accumulator.
+//               O is taken as the bf16 output plus, when given, the
+//               forward's bf16 rounding residual, so D is not limited by the
+//               bf16 rounding of O.
 //   main        one CTA per (batch, KV head, 128-key tile).  It loops over
 //               the query heads of its group and the query tiles that can
 //               see its keys, keeps dK and dV in tensor memory for the whole
@@ -466,8 +469,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 // and reduced with shuffles; the same grid zeroes the dQ accumulator.
 template <int DV>
 __global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(int64_t rows, const uint4* __restrict__ O, const uint4* __restrict__ dO,
-                           float* __restrict__ D, float4* __restrict__ dQacc, int64_t acc_vec4) {
+attn_bwd_preprocess_kernel(int64_t rows, const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
+                           const uint4* __restrict__ dO, float* __restrict__ D, float4* __restrict__ dQacc,
+                           int64_t acc_vec4) {
   constexpr int kG = DV / 8;   // threads per row
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = gtid / kG;
@@ -482,6 +486,15 @@ attn_bwd_preprocess_kernel(int64_t rows, const uint4* __restrict__ O, const uint
     for (int k = 0; k < 4; ++k) {
       acc = fmaf(bf16_lo(aw[k]), bf16_lo(gw[k]), acc);
       acc = fmaf(bf16_hi(aw[k]), bf16_hi(gw[k]), acc);
+    }
+    if (O_lo != nullptr) {
+      const uint4 r = O_lo[row * kG + part];
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(bf16_lo(rw[k]), bf16_lo(gw[k]), acc);
+        acc = fmaf(bf16_hi(rw[k]), bf16_hi(gw[k]), acc);
+      }
     }
   }
 #pragma unroll
@@ -533,8 +546,8 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* dO, float* D,
-                                       float* dQacc, cudaStream_t stream) {
+cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* O_lo,
+                                       const void* dO, float* D, float* dQacc, cudaStream_t stream) {
   const int64_t acc_vec4 = static_cast<int64_t>(rows) * dh / 4;
   const int64_t row_threads = static_cast<int64_t>(rows) * (dv / 8);
   const int64_t work = row_threads > acc_vec4 ? row_threads : acc_vec4;
@@ -544,12 +557,12 @@ cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void*
   (void)work;
   if (dv == 128)
     attn_bwd_preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(dO), D, reinterpret_cast<float4*>(dQacc),
-        acc_vec4);
+        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo), static_cast<const uint4*>(dO), D,
+        reinterpret_cast<float4*>(dQacc), acc_vec4);
   else if (dv == 64)
     attn_bwd_preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(dO), D, reinterpret_cast<float4*>(dQacc),
-        acc_vec4);
+        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo), static_cast<const uint4*>(dO), D,
+        reinterpret_cast<float4*>(dQacc), acc_vec4);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

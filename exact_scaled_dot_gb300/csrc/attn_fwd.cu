@@ -384,19 +384,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (ok) {
         const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
         const bool in_range = i < p.sh.n_q;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) +
-                                               (static_cast<int64_t>(bh) * p.sh.n_q + i) * DV);
+        const int64_t row_off = (static_cast<int64_t>(bh) * p.sh.n_q + i) * DV;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + row_off);
+        uint4* lorow = p.O_lo ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O_lo) + row_off) : nullptr;
 #pragma unroll
         for (int c = 0; c < DV / 32; ++c) {
           tmem_ld32(tO + c * 32, rr);
-          uint32_t w[16];
+          uint32_t w[16], lo[16];
 #pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * inv_l, __uint_as_float(rr[k + 1]) * inv_l);
+          for (int k = 0; k < 32; k += 2) {
+            const float o0 = __uint_as_float(rr[k]) * inv_l, o1 = __uint_as_float(rr[k + 1]) * inv_l;
+            w[k >> 1] = pack_bf16x2(o0, o1);
+            lo[k >> 1] = pack_bf16x2(o0 - bf16_lo(w[k >> 1]), o1 - bf16_hi(w[k >> 1]));
+          }
           if (in_range) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               orow[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            if (lorow) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                lorow[c * 4 + v] = make_uint4(lo[4 * v], lo[4 * v + 1], lo[4 * v + 2], lo[4 * v + 3]);
+            }
           }
         }
         if (in_range)

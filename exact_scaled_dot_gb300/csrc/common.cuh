@@ -78,6 +78,7 @@ struct FwdParams {
   float scale_log2;            // scale * log2(e)
   uint64_t wait_limit_ns;
   void* O;                     // bf16 [B][Hq][n_q][d_v]
+  void* O_lo;                  // bf16 rounding residual of O, or nullptr
   float* LSE;                  // fp32 [B][Hq][n_q]
   unsigned int* status;        // device status word
 };
@@ -105,8 +106,8 @@ cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtens
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                  const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* dO,
-                                       float* D, float* dQacc, cudaStream_t stream);
+cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* O_lo,
+                                       const void* dO, float* D, float* dQacc, cudaStream_t stream);
 cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
                                      cudaStream_t stream);
 

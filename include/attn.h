@@ -102,10 +102,18 @@ typedef struct {
 } attn_mask;
 
 /* Forward pass (A.10.1-A.10.3).  Inputs Q, K, V (bf16, device); outputs
- * O (bf16) and LSE (fp32, natural log), both device, fully overwritten. */
+ * O (bf16) and LSE (fp32, natural log), both device, fully overwritten.
+ *
+ * O_lo (optional, NULL to skip): bf16 [B][Hq][n_q][d_v] receiving the
+ * rounding residual of O, so that O + O_lo carries the fp32 result to about
+ * 16 significant bits.  The backward's row term c_i = sum_l dO_il O_il
+ * (A.10.7) feeds dQ_i with weight -scale * sum_j A_ij k_j, which for a
+ * sharply peaked softmax row is a whole key row; bf16 rounding of O alone
+ * then moves dQ and dK by a few 1e-2.  Passing O_lo on to the backward
+ * removes that error. */
 int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
-             void* O, float* LSE, void* stream);
+             void* O, float* LSE, void* O_lo, void* stream);
 
 /* Bytes of device workspace attn_bwd needs: D (fp32 [B*Hq*n_q]) followed by
  * an fp32 dQ accumulator [B*Hq*n_q*d_h], each 256-byte aligned.  Returns 0
@@ -114,7 +122,9 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
 
 /* Backward pass (A.10.5-A.10.9).  Q, K, V, O, LSE must be those of the
  * forward call with the same mask and scale ("Chapter 31", section 3: the
- * backward must use the forward's semantics).  dO is the upstream gradient.
+ * backward must use the forward's semantics); O_lo is the forward's residual
+ * output or NULL (then D is computed from the bf16 O alone).  dO is the
+ * upstream gradient.
  * Outputs dQ, dK, dV (bf16, device) are fully overwritten; dK and dV hold the
  * sums over each KV head's query heads.  `workspace` is caller-owned device
  * memory of at least attn_bwd_workspace_bytes(shape) bytes, 256-byte aligned;
@@ -122,15 +132,15 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * below, in order. */
 int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
-             const void* O, const void* dO, const float* LSE,
+             const void* O, const void* O_lo, const void* dO, const float* LSE,
              void* dQ, void* dK, void* dV,
              void* workspace, size_t workspace_bytes, void* stream);
 
-/* Stage 1 of the backward: D_i = sum_l dO_il O_il (= c_i of A.10.7) into the
- * fp32 array D [B*Hq*n_q], and zero the fp32 accumulator dQacc
- * [B*Hq*n_q*d_h]. */
-int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* dO,
-                        float* D, float* dQacc, void* stream);
+/* Stage 1 of the backward: D_i = sum_l dO_il (O_il + O_lo_il) (= c_i of
+ * A.10.7; O_lo may be NULL) into the fp32 array D [B*Hq*n_q], and zero the
+ * fp32 accumulator dQacc [B*Hq*n_q*d_h]. */
+int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo,
+                        const void* dO, float* D, float* dQacc, void* stream);
 
 /* Stage 2: the key-tile-stationary main kernel.  Recomputes A from Q, K and
  * LSE, writes dK (scaled) and dV (bf16) and adds the unscaled dS K products

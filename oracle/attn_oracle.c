@@ -358,8 +358,9 @@ int oracle_forward(const oracle_shape *sh, const oracle_mask *mk, double scale,
 /* row's m_i, l_i and c_i, so every term is the one part 1 used.             */
 /*                                                                            */
 /* q_rows / k_rows select outputs like oracle_forward's rows (NULL = all).  */
-/* Per-row statistics are always computed for every query row, because a    */
-/* key's gradient sums over all rows that see it.  Outputs:                  */
+/* Per-row statistics are computed for every query row whenever dK or dV is */
+/* requested, because a key's gradient sums over all rows that see it;      */
+/* with neither requested only the selected rows are visited.  Outputs:     */
 /*   dQ[t] for q_rows[t]; D[t], C[t] likewise;                                */
 /*   dK[t], dV[t] for k_rows[t] (flattened (b, h, j)).                        */
 /* Any output pointer may be NULL.  Returns -1 on an empty row.              */
@@ -398,6 +399,9 @@ int oracle_backward(const oracle_shape *sh, const oracle_mask *mk, double scale,
         double *o = (double *)malloc(sizeof(double) * (size_t)sh->dv);
 #pragma omp for schedule(dynamic, 4)
         for (int64_t row = 0; row < all_rows; ++row) {
+            if (!dK && !dV && slot[row] < 0) {
+                continue;
+            }
             const int64_t i = row % sh->nq;
             const int64_t r = (row / sh->nq) % sh->Hq;
             const int64_t b = row / (sh->nq * sh->Hq);

@@ -51,8 +51,9 @@ def run_gpu(w: Workload, inp: Inputs, scale: Optional[float] = None, poison: boo
     dK = torch.full_like(K, fill)
     dV = torch.full_like(V, fill)
     off = w.causal_offset if w.causal else None
-    esd.attn_fwd(Q, K, V, causal=w.causal, causal_offset=off, kv_len=kv, scale=scale, O=O, LSE=LSE)
-    esd.attn_bwd(Q, K, V, O, dO, LSE, causal=w.causal, causal_offset=off, kv_len=kv, scale=scale,
+    O_lo = torch.full_like(O, fill)
+    esd.attn_fwd(Q, K, V, causal=w.causal, causal_offset=off, kv_len=kv, scale=scale, O=O, LSE=LSE, O_lo=O_lo)
+    esd.attn_bwd(Q, K, V, O, dO, LSE, O_lo=O_lo, causal=w.causal, causal_offset=off, kv_len=kv, scale=scale,
                  dQ=dQ, dK=dK, dV=dV)
     torch.cuda.synchronize()
     status = esd.attn_get_status()

@@ -48,7 +48,7 @@ def _call_fwd(lib, shape, mask, scale=None, ptr=256):
     p = ctypes.c_void_p(ptr)
     scale = 1.0 / math.sqrt(max(shape.d_h, 1)) if scale is None else scale
     return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None,
-                        ctypes.c_float(scale), p, p, p, p, p, None)
+                        ctypes.c_float(scale), p, p, p, p, p, None, None)
 
 
 def _mask(causal=0, offset=bnd.ATTN_OFFSET_DEFAULT, kv=None, reserved=0):
@@ -115,7 +115,7 @@ def test_bwd_workspace_checks(lib):
     assert need == ((rows * 4 + 255) // 256) * 256 + ((rows * 128 * 4 + 255) // 256) * 256
     p = ctypes.c_void_p(256)
     m = _mask()
-    args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 9
+    args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5
     assert lib.attn_bwd(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
