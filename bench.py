@@ -240,8 +240,8 @@ def run_cuda(args):
     O_lo = torch.empty_like(O)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     rows = w.B * w.Hq * w.nq
-    D = torch.empty((rows,), dtype=torch.float32, device=dev)
-    dQacc = torch.empty((rows * w.dh,), dtype=torch.float32, device=dev)
+    ws = torch.empty((esd.attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv),),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     esd.attn_clear_status()
 
@@ -251,13 +251,13 @@ def run_cuda(args):
         esd.attn_fwd(Q, K, V, scale=scale, O=O, LSE=LSE, O_lo=O_lo, **mask)
         if ev is not None:
             ev[1].record(stream)
-        esd.attn_bwd_preprocess(O, dO, D, dQacc, shape=shape, O_lo=O_lo)
+        esd.attn_bwd_preprocess(O, dO, ws, shape=shape, O_lo=O_lo)
         if ev is not None:
             ev[2].record(stream)
-        esd.attn_bwd_main(Q, K, V, dO, LSE, D, dQacc, dK, dV, shape=shape, scale=scale, **mask)
+        esd.attn_bwd_main(Q, K, V, dO, LSE, ws, dK, dV, shape=shape, scale=scale, **mask)
         if ev is not None:
             ev[3].record(stream)
-        esd.attn_bwd_finalize(dQacc, dQ, shape=shape, scale=scale)
+        esd.attn_bwd_finalize(ws, dQ, shape=shape, scale=scale)
         if ev is not None:
             ev[4].record(stream)
 
@@ -304,7 +304,7 @@ def run_cuda(args):
     peaks, peak_src = load_peaks()
     bhq = w.B * w.Hq
     bytes_io = {
-        "attn_bwd_preprocess_kernel": rows * w.dv * 2 * 3 + rows * 4 + rows * w.dh * 4,
+        "attn_bwd_preprocess_kernel": rows * w.dv * 2 * 3 + rows * 4 + rows * w.dh * 4 + bhq * (w.nq // 128 + 1) * 8,
         "attn_bwd_finalize_kernel": rows * w.dh * 4 + rows * w.dh * 2,
     }
     dominant = max(per_kernel, key=per_kernel.get)
@@ -349,8 +349,6 @@ def run_cuda(args):
         hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
         hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
         hdQ, hdK, hdV = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dQ, dK, dV))
-        ws = torch.empty((esd.attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv),),
-                         dtype=torch.uint8, device=dev)
         h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hdO))
         d2h = sum(x.numel() * x.element_size() for x in (hO, hL, hdQ, hdK, hdV))
 
@@ -424,7 +422,7 @@ def run_cuda(args):
                        "visible_pairs": pairs, "flops_per_step": flops_fwd + flops_bwd,
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (about %.0f MB touched per step)" % (
-                           sum(x.numel() * x.element_size() for x in (Q, K, V, dO, O, O_lo, LSE, dQ, dK, dV, dQacc))
+                           sum(x.numel() * x.element_size() for x in (Q, K, V, dO, O, O_lo, LSE, dQ, dK, dV, ws))
                            / 1e6)},
             "peak_fraction": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
             "roofline": roof,

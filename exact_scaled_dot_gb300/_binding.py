@@ -73,9 +73,9 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                              _vp]
-    lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, _vp, _vp]
-    lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
-    lib.attn_bwd_finalize.argtypes = [S, f, _vp, _vp, _vp]
+    lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
+    lib.attn_bwd_finalize.argtypes = [S, f, _vp, ctypes.c_size_t, _vp, _vp]
     lib.attn_visible_pairs.argtypes = [S, M]
     lib.attn_visible_pairs.restype = ctypes.c_int64
     lib.attn_get_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -242,25 +242,32 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_off
     return dQ, dK, dV
 
 
-def attn_bwd_preprocess(O, dO, D, dQacc, *, shape: AttnShape, O_lo=None, stream=None):
-    rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(D), _ptr(dQacc),
+def _ws(workspace):
+    return _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size())
+
+
+def attn_bwd_preprocess(O, dO, workspace, *, shape: AttnShape, O_lo=None, stream=None):
+    """Stage 1 of the backward (row terms, tile bounds, zeroed dQ accumulator)."""
+    rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(O), _ptr(O_lo), _ptr(dO), *_ws(workspace),
                                     _stream(O.device, stream))
     _check(rc, "attn_bwd_preprocess")
 
 
-def attn_bwd_main(Q, K, V, dO, LSE, D, dQacc, dK, dV, *, shape: AttnShape, causal=False, causal_offset=None,
+def attn_bwd_main(Q, K, V, dO, LSE, workspace, dK, dV, *, shape: AttnShape, causal=False, causal_offset=None,
                   kv_len=None, scale: Optional[float] = None, stream=None):
+    """Stage 2 of the backward (the key-tile-stationary main kernel)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
     m = _MaskArg(causal, causal_offset, kv_len)
     rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
-                              _ptr(V), _ptr(dO), _ptr(LSE), _ptr(D), _ptr(dQacc), _ptr(dK), _ptr(dV),
+                              _ptr(V), _ptr(dO), _ptr(LSE), *_ws(workspace), _ptr(dK), _ptr(dV),
                               _stream(Q.device, stream))
     _check(rc, "attn_bwd_main")
 
 
-def attn_bwd_finalize(dQacc, dQ, *, shape: AttnShape, scale: Optional[float] = None, stream=None):
+def attn_bwd_finalize(workspace, dQ, *, shape: AttnShape, scale: Optional[float] = None, stream=None):
+    """Stage 3 of the backward (dQ = scale * accumulator in bf16)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
-    rc = load().attn_bwd_finalize(ctypes.byref(shape), ctypes.c_float(scale), _ptr(dQacc), _ptr(dQ),
+    rc = load().attn_bwd_finalize(ctypes.byref(shape), ctypes.c_float(scale), *_ws(workspace), _ptr(dQ),
                                   _stream(dQ.device, stream))
     _check(rc, "attn_bwd_finalize")
 

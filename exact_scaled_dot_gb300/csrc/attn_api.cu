@@ -40,6 +40,10 @@ int check_shape(const attn_shape* s) {
   // Grid and index limits: (B*Hq) blocks along x; element counts fit int64.
   const int64_t bhq = static_cast<int64_t>(s->B) * s->Hq;
   if (bhq > (int64_t{1} << 31) - 1) return ATTN_ERR_SHAPE;
+  // Grid dimensions y: forward query-tile pairs, preprocess query tiles and
+  // backward (batch, KV head) pairs must stay within 65535.
+  if (static_cast<int64_t>(s->B) * s->Hkv > 65535) return ATTN_ERR_SHAPE;
+  if ((static_cast<int64_t>(s->n_q) + 127) / 128 > 65535) return ATTN_ERR_SHAPE;
   if (!supported_dims(s->d_h, s->d_v)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -184,6 +188,36 @@ ShapeParams shape_params(const attn_shape* s) {
 
 int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq * s->n_q; }
 
+// Backward workspace: D [rows] | per-query-tile maxima float2 [B*Hq*nqt] |
+// fp32 dQ accumulator [rows * d_h], each 256-byte aligned.
+struct Workspace {
+  float* D;
+  float2* tilemax;
+  float* dQacc;
+  size_t bytes;
+};
+
+Workspace workspace_layout(const attn_shape* s, void* base) {
+  const size_t rows = static_cast<size_t>(q_rows(s));
+  const size_t nqt = (static_cast<size_t>(s->n_q) + 127) / 128;
+  const size_t tiles = static_cast<size_t>(s->B) * s->Hq * nqt;
+  const size_t off_t = round256(rows * sizeof(float));
+  const size_t off_a = off_t + round256(tiles * sizeof(float2));
+  Workspace w;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  w.D = reinterpret_cast<float*>(b);
+  w.tilemax = reinterpret_cast<float2*>(b + off_t);
+  w.dQacc = reinterpret_cast<float*>(b + off_a);
+  w.bytes = off_a + round256(rows * static_cast<size_t>(s->d_h) * sizeof(float));
+  return w;
+}
+
+int check_workspace(const attn_shape* s, const void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_WORKSPACE;
+  if (bytes < workspace_layout(s, nullptr).bytes) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
 __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* status) {
   __shared__ __align__(8) uint64_t never;
   __shared__ int abort_flag;
@@ -235,8 +269,7 @@ int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask) {
 
 size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
   if (check_shape(shape) != ATTN_OK) return 0;
-  const size_t rows = static_cast<size_t>(q_rows(shape));
-  return round256(rows * sizeof(float)) + round256(rows * static_cast<size_t>(shape->d_h) * sizeof(float));
+  return workspace_layout(shape, nullptr).bytes;
 }
 
 int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
@@ -273,24 +306,28 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo, const void* dO, float* D,
-                        float* dQacc, void* stream) {
+int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo, const void* dO, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
-  rc = check_ptrs({O, dO, D, dQacc});
+  rc = check_ptrs({O, dO});
   if (rc) return rc;
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+  rc = check_workspace(shape, workspace, workspace_bytes);
+  if (rc) return rc;
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  const cudaError_t e = launch_attn_bwd_preprocess(q_rows(shape), shape->d_v, shape->d_h, O, O_lo, dO, D,
-                                                   dQacc, static_cast<cudaStream_t>(stream));
+  const Workspace w = workspace_layout(shape, workspace);
+  const cudaError_t e = launch_attn_bwd_preprocess(static_cast<int64_t>(shape->B) * shape->Hq, shape->n_q,
+                                                   shape->d_v, shape->d_h, O, O_lo, dO, w.D, w.tilemax, w.dQacc,
+                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-                  const void* V, const void* dO, const float* LSE, const float* D, float* dQacc, void* dK,
-                  void* dV, void* stream) {
+                  const void* V, const void* dO, const float* LSE, void* workspace, size_t workspace_bytes,
+                  void* dK, void* dV, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   BwdParams p;
@@ -298,8 +335,11 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
-  rc = check_ptrs({Q, K, V, dO, LSE, D, dQacc, dK, dV});
+  rc = check_ptrs({Q, K, V, dO, LSE, dK, dV});
   if (rc) return rc;
+  rc = check_workspace(shape, workspace, workspace_bytes);
+  if (rc) return rc;
+  const Workspace w = workspace_layout(shape, workspace);
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
@@ -314,8 +354,10 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
   p.LSE = LSE;
-  p.D = D;
-  p.dQacc = dQacc;
+  p.D = w.D;
+  p.tilemax = w.tilemax;
+  p.nqt = (shape->n_q + 127) / 128;
+  p.dQacc = w.dQacc;
   p.dK = dK;
   p.dV = dV;
   p.status = status;
@@ -324,17 +366,21 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_finalize(const attn_shape* shape, float scale, const float* dQacc, void* dQ, void* stream) {
+int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspace, size_t workspace_bytes,
+                      void* dQ, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
-  rc = check_ptrs({dQacc, dQ});
+  rc = check_ptrs({dQ});
+  if (rc) return rc;
+  rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  const cudaError_t e = launch_attn_bwd_finalize(q_rows(shape) * shape->d_h, scale, dQacc, dQ,
+  const Workspace w = workspace_layout(shape, const_cast<void*>(workspace));
+  const cudaError_t e = launch_attn_bwd_finalize(q_rows(shape) * shape->d_h, scale, w.dQacc, dQ,
                                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -352,17 +398,13 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   rc = check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV});
   if (rc) return rc;
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
-  const size_t need = attn_bwd_workspace_bytes(shape);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
-    return ATTN_ERR_WORKSPACE;
-  float* D = static_cast<float*>(workspace);
-  float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                        round256(static_cast<size_t>(q_rows(shape)) * sizeof(float)));
-  rc = attn_bwd_preprocess(shape, O, O_lo, dO, D, acc, stream);
+  rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
-  rc = attn_bwd_main(shape, mask, scale, Q, K, V, dO, LSE, D, acc, dK, dV, stream);
+  rc = attn_bwd_preprocess(shape, O, O_lo, dO, workspace, workspace_bytes, stream);
   if (rc) return rc;
-  return attn_bwd_finalize(shape, scale, acc, dQ, stream);
+  rc = attn_bwd_main(shape, mask, scale, Q, K, V, dO, LSE, workspace, workspace_bytes, dK, dV, stream);
+  if (rc) return rc;
+  return attn_bwd_finalize(shape, scale, workspace, workspace_bytes, dQ, stream);
 }
 
 int attn_get_status(int* status) {

@@ -16,7 +16,8 @@
 //               O_i = sum_j A_ij v_j), and zeroes the fp32 dQ accumulator.
 //               O is taken as the bf16 output plus, when given, the
 //               forward's bf16 rounding residual, so D is not limited by the
-//               bf16 rounding of O.
+//               bf16 rounding of O.  Per 128-row query tile it also records
+//               max ||dO_i|| and max |D_i|, which bound |dS| (below).
 //   main        one CTA per (batch, KV head, 128-key tile).  It loops over
 //               the query heads of its group and the query tiles that can
 //               see its keys, keeps dK and dV in tensor memory for the whole
@@ -27,12 +28,26 @@
 // Main-kernel warp roles (384 threads):
 //   warp 0      TMA producer: the K and V tile once, then Q and dO tiles
 //               of every step into a two-stage ring.
-//   warp 1      MMA issuer (lane 0 issues; the warp zeroes padded K rows).
+//   warp 1      MMA issuer (lane 0 issues).
 //   warps 4-7   "score" warpgroup, thread = key row = TMEM lane:
 //               P^T = exp2(S^T scale log2e - LSE log2e) and
-//               dS^T = P^T (dP^T - D), written back to tensor memory (bf16)
-//               and dS to shared memory for the dQ product.
-//   warps 8-11  dQ read-out (atomics) and the final dK, dV epilogue.
+//               dS^T = P^T (dP^T - D), written back to tensor memory and
+//               dS to shared memory for the dQ product.
+//   warps 8-11  converts K and each Q tile to fp16 in shared memory, reads
+//               dQ out (atomics) and writes the final dK, dV.
+//
+// Precision of the dS products.  dQ_i = scale sum_j dS_ij k_j sums terms
+// that largely cancel when a softmax row is sharply peaked, so rounding dS
+// to bf16 (8 significant bits) alone can use up most of a 1e-2 error
+// budget.  dS therefore enters the dK and dQ products as fp16 (11 bits),
+// multiplied by a per-CTA power of two 2^e chosen from the bound
+//   |dS_ij| <= P_ij |dP_ij - D_i| <= max_i ||dO_i|| max_j ||v_j|| + max_i |D_i|
+// so that |2^e dS| <= 2^14: no fp16 overflow, and small gradients stay far
+// from the fp16 subnormal range.  The scale is exact and undone exactly when
+// dQ is read out and when dK is written.  Q and K are re-encoded as fp16 in
+// shared memory (the MMA takes one type for both operands; the conversion
+// is exact for |x| up to 65504 and saturates beyond).  The weights P used
+// inside dS are kept as fp16 too; dP = dO V^T and dV = P^T dO stay bf16.
 // Per step (query tile of 128 rows) the MMA order is
 //   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dK += dS^T Q,
 //   dQ = dS K -> X,
@@ -66,11 +81,15 @@ struct BwdCfg {
   static constexpr int kOffDS = kOffDO + kStages * kDOTileBytes;
   static constexpr int kOffLse = kOffDS + kDSTileBytes;
   static constexpr int kOffDd = kOffLse + kTileM * 4;
-  static constexpr int kOffBar = kOffDd + kTileM * 4;
+  static constexpr int kOffRed = kOffDd + kTileM * 4;      // 4 warps x 4 floats
+  static constexpr int kOffBar = kOffRed + 64;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;                 // [2]
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
-  static constexpr int kBarSFull = kBarQEmpty + 2;
+  static constexpr int kBarQ16 = kBarQEmpty + 2;      // [2] Q tile re-encoded as fp16
+  static constexpr int kBarK16 = kBarQ16 + 2;         // K tile re-encoded as fp16
+  static constexpr int kBarScale = kBarK16 + 1;       // dS scale bound reduced
+  static constexpr int kBarSFull = kBarScale + 1;
   static constexpr int kBarDPFull = kBarSFull + 1;
   static constexpr int kBarPReady = kBarDPFull + 1;
   static constexpr int kBarDSReady = kBarPReady + 1;
@@ -91,6 +110,16 @@ struct BwdCfg {
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
 
+// Power-of-two exponent e with 2^e * bound <= 2^14 (0 for a zero or
+// non-finite bound), clamped so that 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int ds_scale_exponent(float bound) {
+  if (!(bound > 0.f) || !(bound < INFINITY)) return 0;
+  int E;
+  frexpf(bound, &E);           // bound = m 2^E, m in [0.5, 1)
+  int e = 14 - E;
+  return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+
 template <int DH, int DV>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -106,6 +135,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
   float* lse_s = reinterpret_cast<float*>(smem + C::kOffLse);
   float* dd_s = reinterpret_cast<float*>(smem + C::kOffDd);
+  float* red_s = reinterpret_cast<float*>(smem + C::kOffRed);
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
@@ -115,6 +145,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   const int b = bkv / p.sh.Hkv;
   const int hkv = bkv - b * p.sh.Hkv;
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kTileN;
+  const int64_t klen = key_len(p.mask, p.sh.n_k, b);
   const int64_t i_first = first_row_seeing_key(p.mask, p.sh.n_q, p.sh.n_k, b, j0);
   const int nqt = (p.sh.n_q + kTileM - 1) / kTileM;
   const int qt_first = static_cast<int>(i_first / kTileM);
@@ -128,7 +159,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
       mbar_init(bar(C::kBarQEmpty + s), 1);
+      mbar_init(bar(C::kBarQ16 + s), 128);
     }
+    mbar_init(bar(C::kBarK16), 128);
+    mbar_init(bar(C::kBarScale), 128);
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
     mbar_init(bar(C::kBarPReady), 128);
@@ -153,6 +187,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   auto wait_all = [&](int idx, uint32_t parity) -> bool {
     const bool w = mbar_wait(bar(idx), parity, abort_flag, limit);
     return __all_sync(0xffffffffu, w);
+  };
+  // e of the dS scale, from the four score warps' partial maxima.
+  auto scale_exponent = [&]() -> int {
+    float mv = 0.f, mdo = 0.f, md = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      mv = fmaxf(mv, red_s[4 * w]);
+      mdo = fmaxf(mdo, red_s[4 * w + 1]);
+      md = fmaxf(md, red_s[4 * w + 2]);
+    }
+    return ds_scale_exponent(mdo * mv + md);
   };
 
   if (warp == 0) {
@@ -196,34 +241,18 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
     if (*abort_flag == 0 && total > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdS = idesc_f16_f32(128, 128, false, false);    // S^T = K Q^T (fp16)
+      constexpr uint32_t kIdDP = idesc_bf16_f32(128, 128, false, false);  // dP^T = V dO^T
       constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV += P^T dO
-      constexpr uint32_t kIdDK = idesc_bf16_f32(128, DH, false, true);    // dK += dS^T Q
-      constexpr uint32_t kIdDQ = idesc_bf16_f32(128, DH, true, true);     // dQ = dS K
-      bool ok = wait_all(C::kBarKV, 0);
-      if (ok) {
-        // K rows in [kv_len, n_k) hold caller memory; their dS entries are 0
-        // but 0 * NaN would poison dQ, so they are zeroed.  Rows at or beyond
-        // n_k arrive as zeros from the TMA bounds check.
-        int64_t r0 = key_len(p.mask, p.sh.n_k, b) - j0, r1 = static_cast<int64_t>(p.sh.n_k) - j0;
-        if (r0 < 0) r0 = 0;
-        if (r1 > kTileN) r1 = kTileN;
-        if (r0 < r1) {
-          const int chunks = static_cast<int>(r1 - r0) * (DH / 64) * 8;
-          for (int q = static_cast<int>(lane); q < chunks; q += 32) {
-            const int row = static_cast<int>(r0) + q / ((DH / 64) * 8);
-            const int rem = q % ((DH / 64) * 8);
-            *reinterpret_cast<uint4*>(smem + C::kOffK + (rem / 8) * C::kBlockBytes + row * 128 +
-                                      (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-      }
+      constexpr uint32_t kIdDK = idesc_f16_f32(128, DH, false, true);     // dK += dS^T Q
+      constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
+      bool ok = wait_all(C::kBarK16, 0);
       const uint32_t kA = sbase + C::kOffK, vA = sbase + C::kOffV, dsA = sbase + C::kOffDS;
       for (int s = 0; s < total && ok; ++s) {
         const int st = s & 1;
         ok = wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1));
+        if (!ok) break;
+        ok = wait_all(C::kBarQ16 + st, static_cast<uint32_t>((s >> 1) & 1));
         if (!ok) break;
         if (s > 0) {
           ok = wait_all(C::kBarDQFree, static_cast<uint32_t>((s - 1) & 1));
@@ -243,7 +272,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB + off, 16, 1024), kIdS,
+            umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB + off, 16, 1024), kIdDP,
                     kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(C::kBarDPFull));
@@ -290,13 +319,55 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int jj = static_cast<int>(quad * 32 + lane);
     const int tid = static_cast<int>(threadIdx.x) - 128;
     const int64_t j = j0 + jj;
-    const bool row_masked = j >= key_len(p.mask, p.sh.n_k, b);
+    const bool row_masked = j >= klen;
     const uint32_t lane_base = (quad * 32u) << 16;
     const uint32_t tX = tmem + lane_base + C::kTX;
     const uint32_t tY = tmem + lane_base + C::kTY;
     const float sl2 = p.scale_log2;
     uint8_t* ds_row = smem + C::kOffDS + jj * 128;
-    bool ok = *abort_flag == 0;
+    bool ok = *abort_flag == 0 && total > 0;
+    float ds_scale = 1.f;
+    if (ok) {
+      // ---- bound on |dS| for this CTA -> power-of-two scale ----
+      ok = wait_all(C::kBarKV, 0);
+      float vn2 = 0.f;
+      if (ok && !row_masked) {
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 u = *reinterpret_cast<const uint4*>(smem + C::kOffV + c * C::kBlockBytes + jj * 128 + q * 16);
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              vn2 = fmaf(bf16_lo(wv[k]), bf16_lo(wv[k]), vn2);
+              vn2 = fmaf(bf16_hi(wv[k]), bf16_hi(wv[k]), vn2);
+            }
+          }
+        }
+      }
+      float mv = sqrtf(vn2), mdo = 0.f, md = 0.f;
+      for (int idx = tid; idx < total; idx += 128) {
+        const int bhq = b * p.sh.Hq + step_head(idx);
+        const float2 t = p.tilemax[static_cast<int64_t>(bhq) * p.nqt + step_q0(idx) / kTileM];
+        mdo = fmaxf(mdo, t.x);
+        md = fmaxf(md, t.y);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+        mdo = fmaxf(mdo, __shfl_xor_sync(0xffffffffu, mdo, off));
+        md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
+      }
+      if (lane == 0) {
+        red_s[4 * quad] = mv;
+        red_s[4 * quad + 1] = mdo;
+        red_s[4 * quad + 2] = md;
+      }
+      mbar_arrive(bar(C::kBarScale));
+      ok = ok && wait_all(C::kBarScale, 0);
+      ds_scale = exp2_int(scale_exponent());
+    }
     uint32_t rr[32];
     uint32_t pw[64];
     for (int s = 0; s < total && ok; ++s) {
@@ -339,7 +410,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             p1 = (!row_masked && c + 1 >= cmin) ? p1 : 0.f;
           }
           w[k >> 1] = pack_bf16x2(p0, p1);
-          pw[cc * 16 + (k >> 1)] = w[k >> 1];
+          pw[cc * 16 + (k >> 1)] = pack_f16x2(p0, p1);
         }
         tmem_st16(tX + cc * 16, w);
       }
@@ -356,13 +427,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int k = 0; k < 32; k += 2) {
           const int c = cc * 32 + k;
           const uint32_t pp = pw[cc * 16 + (k >> 1)];
-          float d0 = bf16_lo(pp) * (__uint_as_float(rr[k]) - dd_s[c]);
-          float d1 = bf16_hi(pp) * (__uint_as_float(rr[k + 1]) - dd_s[c + 1]);
+          float d0 = f16_lo(pp) * (__uint_as_float(rr[k]) - dd_s[c]);
+          float d1 = f16_hi(pp) * (__uint_as_float(rr[k + 1]) - dd_s[c + 1]);
           if (need_mask) {
             d0 = (!row_masked && c >= cmin) ? d0 : 0.f;
             d1 = (!row_masked && c + 1 >= cmin) ? d1 : 0.f;
           }
-          w[k >> 1] = pack_bf16x2(d0, d1);
+          w[k >> 1] = pack_f16x2(d0 * ds_scale, d1 * ds_scale);
         }
         tmem_st16(tY + cc * 16, w);
         // dS (queries contiguous per key row) for the dQ = dS K product:
@@ -381,14 +452,51 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_arrive(bar(C::kBarDSReady));
     }
   } else if (warp >= 8) {
-    // ===================== dQ read-out and dK/dV epilogue ================
+    // ====== fp16 re-encoding of K and Q, dQ read-out, dK/dV epilogue ======
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
+    const int tid2 = static_cast<int>(threadIdx.x) - 256;
     const uint32_t lane_base = (quad * 32u) << 16;
     const uint32_t tX = tmem + lane_base + C::kTX;
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
+    auto to_f16 = [](uint4 u) {
+      return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+    };
+    auto convert_q = [&](int st) {
+      uint4* q = reinterpret_cast<uint4*>(smem + C::kOffQ + st * C::kQTileBytes);
+      for (int k = tid2; k < C::kQTileBytes / 16; k += 128) q[k] = to_f16(q[k]);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarQ16 + st));
+    };
+    float inv_scale = 1.f;
+    if (ok && total > 0) {
+      // K: re-encode as fp16; rows in [kv_len, n_k) hold caller memory that
+      // may be anything (even NaN) and become zeros -- their dS entries are
+      // 0, but 0 * NaN would still poison dQ.  Rows at or beyond n_k arrive
+      // as zeros from the TMA bounds check.
+      ok = wait_all(C::kBarKV, 0);
+      if (ok) {
+        uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
+        for (int k = tid2; k < C::kKTileBytes / 16; k += 128) {
+          const int krow = (k % (C::kBlockBytes / 16)) / 8;
+          kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::kBarK16));
+        ok = wait_all(C::kBarQFull + 0, 0);
+      }
+      if (ok) convert_q(0);
+      if (ok) ok = wait_all(C::kBarScale, 0);
+      if (ok) inv_scale = exp2_int(-scale_exponent());
+    }
     for (int s = 0; s < total && ok; ++s) {
+      if (s + 1 < total) {
+        const int st1 = (s + 1) & 1;
+        ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+        if (!ok) break;
+        convert_q(st1);
+      }
       const int bhq = b * p.sh.Hq + step_head(s);
       const int64_t i = static_cast<int64_t>(step_q0(s)) + row;
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
@@ -402,8 +510,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
           for (int v = 0; v < 8; ++v)
             atomicAdd(dst + cc * 8 + v,
-                      make_float4(__uint_as_float(rr[4 * v]), __uint_as_float(rr[4 * v + 1]),
-                                  __uint_as_float(rr[4 * v + 2]), __uint_as_float(rr[4 * v + 3])));
+                      make_float4(__uint_as_float(rr[4 * v]) * inv_scale, __uint_as_float(rr[4 * v + 1]) * inv_scale,
+                                  __uint_as_float(rr[4 * v + 2]) * inv_scale,
+                                  __uint_as_float(rr[4 * v + 3]) * inv_scale));
         }
       }
       tc_fence_before_sync();
@@ -419,6 +528,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const int64_t krow = static_cast<int64_t>(bkv) * p.sh.n_k + j;
       uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + krow * DH);
       uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + krow * DV);
+      const float dk_scale = p.scale * inv_scale;
 #pragma unroll
       for (int cc = 0; cc < DH / 32; ++cc) {
         uint32_t w[16];
@@ -426,7 +536,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tmem_ld32(tmem + lane_base + C::kTdK + cc * 32, rr);
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
-            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * p.scale, __uint_as_float(rr[k + 1]) * p.scale);
+            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * dk_scale, __uint_as_float(rr[k + 1]) * dk_scale);
         } else {
 #pragma unroll
           for (int k = 0; k < 16; ++k) w[k] = 0u;
@@ -465,43 +575,69 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
 }
 
-// D_i = sum_l dO_il O_il: each row is read by DV/8 threads (16 bytes each)
-// and reduced with shuffles; the same grid zeroes the dQ accumulator.
-template <int DV>
+// One block per 128-row query tile of one (batch, query head), two threads
+// per row:
+//   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
+//   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
+// and the tile's rows of the fp32 dQ accumulator are zeroed.
+template <int DV, int DH>
 __global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(int64_t rows, const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
-                           const uint4* __restrict__ dO, float* __restrict__ D, float4* __restrict__ dQacc,
-                           int64_t acc_vec4) {
-  constexpr int kG = DV / 8;   // threads per row
-  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = gtid / kG;
-  const int part = static_cast<int>(gtid % kG);
-  float acc = 0.f;
-  if (row < rows) {
-    const uint4 a = O[row * kG + part];
-    const uint4 g = dO[row * kG + part];
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
+                           const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
+                           float4* __restrict__ dQacc) {
+  constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
+  __shared__ float red[2][8];
+  const int64_t bh = blockIdx.x;
+  const int qt = blockIdx.y;
+  const int r = static_cast<int>(threadIdx.x >> 1), half = static_cast<int>(threadIdx.x & 1);
+  const int64_t i = static_cast<int64_t>(qt) * kTileM + r;
+  const bool valid = i < n_q;
+  const int64_t row = bh * n_q + i;
+  float acc = 0.f, nrm = 0.f;
+  if (valid) {
+    const int64_t base = row * (DV / 8) + half * kChunks;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc = fmaf(bf16_lo(aw[k]), bf16_lo(gw[k]), acc);
-      acc = fmaf(bf16_hi(aw[k]), bf16_hi(gw[k]), acc);
-    }
-    if (O_lo != nullptr) {
-      const uint4 r = O_lo[row * kG + part];
-      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 a = O[base + c];
+      const uint4 g = dO[base + c];
+      const uint4 lo = O_lo ? O_lo[base + c] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        acc = fmaf(bf16_lo(rw[k]), bf16_lo(gw[k]), acc);
-        acc = fmaf(bf16_hi(rw[k]), bf16_hi(gw[k]), acc);
+        const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+        acc = fmaf(bf16_lo(aw[k]) + bf16_lo(lw[k]), g0, acc);
+        acc = fmaf(bf16_hi(aw[k]) + bf16_hi(lw[k]), g1, acc);
+        nrm = fmaf(g0, g0, nrm);
+        nrm = fmaf(g1, g1, nrm);
       }
     }
   }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  nrm += __shfl_xor_sync(0xffffffffu, nrm, 1);
+  if (valid && half == 0) D[row] = acc;
+  float mn = valid ? sqrtf(nrm) : 0.f, md = valid ? fabsf(acc) : 0.f;
 #pragma unroll
-  for (int off = kG / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) D[row] = acc;
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t k = gtid; k < acc_vec4; k += nthreads) dQacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = mn;
+    red[1][threadIdx.x >> 5] = md;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.f, c = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      a = fmaxf(a, red[0][w]);
+      c = fmaxf(c, red[1][w]);
+    }
+    tilemax[bh * nqt + qt] = make_float2(a, c);
+  }
+  const int64_t rows_here = (n_q - static_cast<int64_t>(qt) * kTileM) < kTileM ? (n_q - static_cast<int64_t>(qt) * kTileM)
+                                                                                : kTileM;
+  float4* acc_tile = dQacc + (bh * n_q + static_cast<int64_t>(qt) * kTileM) * (DH / 4);
+  for (int64_t k = threadIdx.x; k < rows_here * (DH / 4); k += 256) acc_tile[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dQ = scale * acc, eight elements per thread per iteration.
@@ -535,6 +671,15 @@ int grid_for(int64_t work_threads) {
   return static_cast<int>(blocks);
 }
 
+template <int DV, int DH>
+void launch_pre_t(int64_t bhq, int n_q, int nqt, const void* O, const void* O_lo, const void* dO, float* D,
+                  float2* tilemax, float* dQacc, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(bhq), static_cast<unsigned>(nqt));
+  attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(
+      n_q, nqt, static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo), static_cast<const uint4*>(dO), D,
+      tilemax, reinterpret_cast<float4*>(dQacc));
+}
+
 }  // namespace
 
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -546,23 +691,16 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* O_lo,
-                                       const void* dO, float* D, float* dQacc, cudaStream_t stream) {
-  const int64_t acc_vec4 = static_cast<int64_t>(rows) * dh / 4;
-  const int64_t row_threads = static_cast<int64_t>(rows) * (dv / 8);
-  const int64_t work = row_threads > acc_vec4 ? row_threads : acc_vec4;
-  int64_t blocks = (row_threads + 255) / 256;
-  const int64_t zero_blocks = grid_for(acc_vec4);
-  if (blocks < zero_blocks) blocks = zero_blocks;
-  (void)work;
-  if (dv == 128)
-    attn_bwd_preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo), static_cast<const uint4*>(dO), D,
-        reinterpret_cast<float4*>(dQacc), acc_vec4);
-  else if (dv == 64)
-    attn_bwd_preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        rows, static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo), static_cast<const uint4*>(dO), D,
-        reinterpret_cast<float4*>(dQacc), acc_vec4);
+cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* O, const void* O_lo,
+                                       const void* dO, float* D, float2* tilemax, float* dQacc,
+                                       cudaStream_t stream) {
+  const int nqt = (n_q + kTileM - 1) / kTileM;
+  if (dv == 128 && dh == 128)
+    launch_pre_t<128, 128>(bhq, n_q, nqt, O, O_lo, dO, D, tilemax, dQacc, stream);
+  else if (dv == 64 && dh == 64)
+    launch_pre_t<64, 64>(bhq, n_q, nqt, O, O_lo, dO, D, tilemax, dQacc, stream);
+  else if (dv == 64 && dh == 128)
+    launch_pre_t<64, 128>(bhq, n_q, nqt, O, O_lo, dO, D, tilemax, dQacc, stream);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

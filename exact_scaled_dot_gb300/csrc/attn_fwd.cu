@@ -29,7 +29,10 @@
 // when a new score exceeds it by more than 2^8 in the exp2 domain, so most
 // tiles skip the O rescale.  Both the numerator (O) and the denominator (l)
 // always use the same reference, so the result is unchanged in real
-// arithmetic and no term exceeds 2^8 before normalisation.
+// arithmetic and no term exceeds 2^8 before normalisation.  The weight of
+// the dominant key is then 2^d with d in [0, 8) rather than exactly 1, and
+// its bf16 rounding would leave a 2^-9 relative error in O; normalising by
+// the sum of the rounded weights removes it (the LSE keeps the exact sum).
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -305,7 +308,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t tO = tmem + lane_base + 256 + t * DV;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;   // reference maximum, exp2 domain
-    float l_sum = 0.f;
+    float l_sum = 0.f;         // sum of the weights p (for the LSE)
+    float l_used = 0.f;        // sum of the bf16-rounded weights the PV product used
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
     for (int j = 0; j < ntiles[t] && ok; ++j) {
@@ -342,6 +346,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           const float alpha = need ? fast_exp2(m_ref - m_new) : 1.0f;
           if (need) {
             l_sum *= alpha;
+            l_used *= alpha;
             m_ref = m_new;
           }
 #pragma unroll
@@ -370,6 +375,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
           l_sum += p0 + p1;
           pw[k >> 1] = pack_bf16x2(p0, p1);
+          l_used += bf16_lo(pw[k >> 1]) + bf16_hi(pw[k >> 1]);
         }
         tmem_st16(tS + c * 16, pw);
       }
@@ -382,7 +388,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull + t), 0, abort_flag, limit));
       tc_fence_after_sync();
       if (ok) {
-        const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+        // O is normalised by the sum of the weights the PV product actually
+        // used (their bf16 roundings), so each output row is an exact convex
+        // combination of V rows up to fp32 accumulation; the LSE keeps the
+        // unrounded sum.
+        const float inv_l = l_used > 0.f ? 1.0f / l_used : 0.f;
         const bool in_range = i < p.sh.n_q;
         const int64_t row_off = (static_cast<int64_t>(bh) * p.sh.n_q + i) * DV;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + row_off);

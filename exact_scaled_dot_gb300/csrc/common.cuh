@@ -91,6 +91,8 @@ struct BwdParams {
   uint64_t wait_limit_ns;
   const float* LSE;            // fp32 [B][Hq][n_q]
   const float* D;              // fp32 [B][Hq][n_q]
+  const float2* tilemax;       // per 128-row query tile: (max ||dO_i||, max |D_i|)
+  int32_t nqt;                 // query tiles per head
   float* dQacc;                // fp32 [B][Hq][n_q][d_h]
   void* dK;                    // bf16 [B][Hkv][n_k][d_h]
   void* dV;                    // bf16 [B][Hkv][n_k][d_v]
@@ -106,8 +108,9 @@ cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtens
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                  const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_attn_bwd_preprocess(int64_t rows, int dv, int dh, const void* O, const void* O_lo,
-                                       const void* dO, float* D, float* dQacc, cudaStream_t stream);
+cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* O, const void* O_lo,
+                                       const void* dO, float* D, float2* tilemax, float* dQacc,
+                                       cudaStream_t stream);
 cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
                                      cudaStream_t stream);
 

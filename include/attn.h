@@ -67,7 +67,8 @@ extern "C" {
 #define ATTN_OK               0
 #define ATTN_ERR_NULL         1  /* a required pointer is NULL                         */
 #define ATTN_ERR_SHAPE        2  /* non-positive size, Hq % Hkv != 0, kv_len out of   */
-                                 /* [1, n_k], B > ATTN_MAX_BATCH, size overflow         */
+                                 /* [1, n_k], B > ATTN_MAX_BATCH, B*Hkv > 65535,        */
+                                 /* n_q > 65535*128, size overflow                      */
 #define ATTN_ERR_UNSUPPORTED  3  /* (d_h, d_v) not one of the supported pairs          */
 #define ATTN_ERR_ALIGN        4  /* a tensor pointer is not 16-byte aligned            */
 #define ATTN_ERR_EMPTY_ROW    5  /* some query row has an empty visible set            */
@@ -115,9 +116,10 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
              void* O, float* LSE, void* O_lo, void* stream);
 
-/* Bytes of device workspace attn_bwd needs: D (fp32 [B*Hq*n_q]) followed by
- * an fp32 dQ accumulator [B*Hq*n_q*d_h], each 256-byte aligned.  Returns 0
- * for an invalid shape. */
+/* Bytes of device workspace the backward needs (attn_bwd and its three
+ * stages): row terms D, per-128-row-tile bounds used to scale dS, and an
+ * fp32 dQ accumulator, about B*Hq*n_q*(4*d_h + 4) bytes.  The layout is
+ * private to the library.  Returns 0 for an invalid shape. */
 size_t attn_bwd_workspace_bytes(const attn_shape* shape);
 
 /* Backward pass (A.10.5-A.10.9).  Q, K, V, O, LSE must be those of the
@@ -129,7 +131,11 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * sums over each KV head's query heads.  `workspace` is caller-owned device
  * memory of at least attn_bwd_workspace_bytes(shape) bytes, 256-byte aligned;
  * its contents on entry do not matter.  Equivalent to the three stage calls
- * below, in order. */
+ * below, in order, on the same workspace.
+ *
+ * Precision: the products with dS (dK and dQ) take dS in fp16 scaled by a
+ * power of two derived from a bound on |dS|, with Q and K re-encoded as fp16
+ * (exact for |x| <= 65504; larger entries saturate). */
 int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
              const void* O, const void* O_lo, const void* dO, const float* LSE,
@@ -137,22 +143,23 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Stage 1 of the backward: D_i = sum_l dO_il (O_il + O_lo_il) (= c_i of
- * A.10.7; O_lo may be NULL) into the fp32 array D [B*Hq*n_q], and zero the
- * fp32 accumulator dQacc [B*Hq*n_q*d_h]. */
+ * A.10.7; O_lo may be NULL), per-tile bounds max ||dO_i|| and max |D_i|, and
+ * a zeroed dQ accumulator, all in `workspace`. */
 int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo,
-                        const void* dO, float* D, float* dQacc, void* stream);
+                        const void* dO, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /* Stage 2: the key-tile-stationary main kernel.  Recomputes A from Q, K and
- * LSE, writes dK (scaled) and dV (bf16) and adds the unscaled dS K products
- * into dQacc (fp32, zeroed by stage 1). */
+ * LSE, writes dK (scaled) and dV (bf16) and adds the dS K products into the
+ * workspace's fp32 dQ accumulator (zeroed by stage 1). */
 int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale,
                   const void* Q, const void* K, const void* V, const void* dO,
-                  const float* LSE, const float* D, float* dQacc,
+                  const float* LSE, void* workspace, size_t workspace_bytes,
                   void* dK, void* dV, void* stream);
 
-/* Stage 3: dQ = scale * dQacc, rounded to bf16. */
-int attn_bwd_finalize(const attn_shape* shape, float scale, const float* dQacc,
-                      void* dQ, void* stream);
+/* Stage 3: dQ = scale * accumulator, rounded to bf16. */
+int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspace,
+                      size_t workspace_bytes, void* dQ, void* stream);
 
 /* Number of visible (i, j) pairs over all batch elements and query heads,
  * from the same closed form the kernels use to classify tiles; -1 on an

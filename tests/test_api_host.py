@@ -112,7 +112,8 @@ def test_bwd_workspace_checks(lib):
     s = _shape()
     need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
     rows = 2 * 4 * 100
-    assert need == ((rows * 4 + 255) // 256) * 256 + ((rows * 128 * 4 + 255) // 256) * 256
+    r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
+    assert need == r256(rows * 4) + r256(2 * 4 * 1 * 8) + r256(rows * 128 * 4)
     p = ctypes.c_void_p(256)
     m = _mask()
     args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5

@@ -39,6 +39,8 @@ SMALL = {
                                   causal=True, kv_len_range=(140, 333), seed=12),
     "cross_padded_peaked": Workload("cross_padded_peaked", B=2, Hq=2, Hkv=2, nq=200, nk=700, dh=128, dv=64,
                                     kv_len_range=(300, 700), sigma_qk=3.0, seed=13),
+    "cross_padded_peaked_2": Workload("cross_padded_peaked_2", B=2, Hq=2, Hkv=2, nq=256, nk=1024, dh=128, dv=64,
+                                      kv_len_range=(512, 1024), sigma_qk=3.0, seed=99),
     "mqa_chunked_prefill": Workload("mqa_chunked_prefill", B=1, Hq=4, Hkv=1, nq=130, nk=520, dh=128, dv=128,
                                     causal=True, seed=14),
     "d64_causal_gqa": Workload("d64_causal_gqa", B=1, Hq=4, Hkv=1, nq=257, nk=257, dh=64, dv=64, causal=True,
@@ -70,12 +72,17 @@ def test_small_second_seed(orc):
 
 
 def test_key_length_one(orc):
-    """kv_len = 1 for every batch element: A = e_0, O_i = v_0, dQ = dK = 0."""
+    """kv_len = 1 for every batch element: A = e_0, O_i = v_0 exactly, and dQ, dK
+    vanish up to rounding (dP and D are summed in different orders on the GPU,
+    so dS is of the order of 1e-7 rather than exactly 0)."""
     w = Workload("kv1", B=2, Hq=2, Hkv=1, nq=140, nk=200, dh=128, dv=128, kv_len_range=(1, 1), seed=21)
     inp = make_inputs(w)
     res = run_gpu(w, inp)
     compare_full(w, inp, res, orc)
-    assert bool((res.dQ == 0).all()) and bool((res.dK == 0).all())
+    for b in range(w.B):
+        for r in range(w.Hq):
+            assert torch.equal(res.O[b, r], inp.V[b, 0, 0].to(res.O.device).expand(w.nq, w.dv))
+    assert float(res.dQ.float().abs().max()) <= 1e-4 and float(res.dK.float().abs().max()) <= 1e-4
 
 
 def test_nan_in_key_padding_does_not_leak(orc):
