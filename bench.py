@@ -224,6 +224,8 @@ def run_cuda(args):
     from exact_scaled_dot_gb300.inputs import WORKLOADS, make_inputs
 
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = w.scaled(B=args.batch)
     inp = make_inputs(w)
     kv = None if inp.kv_len is None else inp.kv_len.tolist()
     off = w.causal_offset if w.causal else None
@@ -446,6 +448,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiling)")
     ap.add_argument("--cpu-rows", type=int, default=768, help="query rows in the timed oracle sample")
     ap.add_argument("--reference-rows", type=int, default=384, help="query rows per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
