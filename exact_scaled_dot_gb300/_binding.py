@@ -33,7 +33,8 @@ ATTN_OFFSET_DEFAULT = -(2 ** 63)
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
            "attn_bwd_finalize", "attn_visible_pairs", "attn_get_status", "attn_clear_status",
-           "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version")
+           "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
+           "attn_bwd_noalloc_max_scratch_bytes")
 
 
 class AttnError(RuntimeError):
@@ -84,6 +85,10 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_strerror.argtypes = [ctypes.c_int]
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_abi_version.restype = ctypes.c_int
+    lib.attn_bwd_noalloc.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_noalloc.restype = ctypes.c_int
+    lib.attn_bwd_noalloc_max_scratch_bytes.argtypes = []
+    lib.attn_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
     for name in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
                  "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
@@ -293,6 +298,47 @@ def attn_selftest_wait_timeout(limit_ns: int, stream=None, device=None) -> None:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check(load().attn_selftest_wait_timeout(ctypes.c_uint64(int(limit_ns)), _stream(dev, stream)),
            "attn_selftest_wait_timeout")
+
+
+def attn_bwd_noalloc(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False,
+                     causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
+                     dQ=None, dK=None, dV=None, stream=None):
+    """Backward pass that allocates no device memory in the library.
+
+    For callers that cannot allocate where they run the backward (memory owned
+    by a fixed arena or another runtime, or loops that cannot afford the
+    device-wide synchronisation of an allocation): the scratch comes from a
+    static buffer inside the library instead of a caller workspace.  Outputs
+    passed in (dQ, dK, dV) are filled; missing ones are created here by torch,
+    which is the caller's allocation, not the library's.  Problems needing more
+    than attn_bwd_noalloc_max_scratch_bytes() of scratch raise AttnError
+    (ATTN_ERR_WORKSPACE).  Calls that overlap on the GPU share the buffer and
+    race; serialise them."""
+    dims, dev = _check_qkv(Q, K, V)
+    B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
+    scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
+    if O_lo is not None:
+        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev)
+    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev)
+    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev)
+    shape = make_shape(*dims)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    rc = load().attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q),
+                                 _ptr(K), _ptr(V), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
+                                 _ptr(dV), _stream(dev, stream))
+    _check(rc, "attn_bwd_noalloc")
+    return dQ, dK, dV
+
+
+def attn_bwd_noalloc_max_scratch_bytes() -> int:
+    return int(load().attn_bwd_noalloc_max_scratch_bytes())
 
 
 def attn_abi_version() -> int:

@@ -233,6 +233,38 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* status) {
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Static backward scratch for callers that cannot allocate device memory.
+//
+// The array is part of the library's device image: every GPU on which the
+// library is loaded holds these bytes until the process exits.  In host code
+// the name `g_static_bwd_scratch` is only a host-side stand-in for the
+// symbol, never a device address, so it is never handed to a kernel; the
+// device address comes from cudaGetSymbolAddress, looked up once per device
+// (with that device current) on the first attn_bwd_noalloc call there.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticBwdScratchBytes = size_t{16} << 20;   // 16 MiB
+static __device__ __align__(256) unsigned char g_static_bwd_scratch[kStaticBwdScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+int static_scratch_ptr(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_bwd_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+}  // namespace
 }  // namespace esd
 
 using namespace esd;
@@ -436,5 +468,28 @@ int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, dev_status);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
+
+// The backward pass for callers that cannot call cudaMalloc: identical to
+// attn_bwd, but its scratch is the library's static device buffer instead of
+// a caller workspace.  Problems whose scratch would exceed the buffer are
+// refused with ATTN_ERR_WORKSPACE before anything is launched.  The stage
+// kernels rewrite every byte they read back (the dQ accumulator is zeroed by
+// the preprocess stage), so leftovers from an earlier call do not matter; but
+// all calls share the one buffer, so calls that overlap on the GPU (other
+// streams, other host threads) race and must be serialised by the caller.
+int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
+                     const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
+                     void* dK, void* dV, void* stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (workspace_layout(shape, nullptr).bytes > kStaticBwdScratchBytes) return ATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  rc = static_scratch_ptr(&scratch);
+  if (rc) return rc;
+  return attn_bwd(shape, mask, scale, Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV, scratch, kStaticBwdScratchBytes,
+                  stream);
+}
+
+size_t attn_bwd_noalloc_max_scratch_bytes(void) { return kStaticBwdScratchBytes; }
 
 }  // extern "C"

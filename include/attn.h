@@ -161,6 +161,32 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale,
 int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspace,
                       size_t workspace_bytes, void* dQ, void* stream);
 
+/* The backward pass without any device allocation, for callers that cannot
+ * call cudaMalloc where they run it: applications whose device memory is all
+ * owned by a fixed arena or by another runtime that forbids further
+ * allocations, and latency-critical loops that cannot afford cudaMalloc's
+ * implicit device-wide synchronisation.  There is no counterpart on the
+ * pages: it is attn_bwd with its workspace taken from a static buffer
+ * compiled into the library (attn_bwd_noalloc_max_scratch_bytes() bytes,
+ * 16 MiB, held on every GPU that loads the library until the process exits).
+ *
+ * Arguments and results are those of attn_bwd minus the workspace; the
+ * caller still provides every input and output.  A problem whose workspace
+ * (attn_bwd_workspace_bytes) exceeds the buffer returns ATTN_ERR_WORKSPACE
+ * before anything is launched.  The first call on a device looks up the
+ * buffer's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  Every call shares the one
+ * buffer, whose contents persist between calls: the kernels clear what must
+ * start at zero, but calls that overlap on the GPU race and must be
+ * serialised by the caller. */
+int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale,
+                     const void* Q, const void* K, const void* V,
+                     const void* O, const void* O_lo, const void* dO, const float* LSE,
+                     void* dQ, void* dK, void* dV, void* stream);
+
+/* Size in bytes of the static buffer attn_bwd_noalloc uses. */
+size_t attn_bwd_noalloc_max_scratch_bytes(void);
+
 /* Number of visible (i, j) pairs over all batch elements and query heads,
  * from the same closed form the kernels use to classify tiles; -1 on an
  * invalid shape or mask.  Host only. */
