@@ -140,6 +140,21 @@ bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [bh][n][d] of the fp32 dQ accumulator for TMA reduce-add in
+// 128-row x 32-column boxes (128 bytes, 128-byte swizzle); rows beyond n of
+// a head are clipped.
+bool make_tmap_acc(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(n) * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
   bool probed = false;
   bool ok = false;
@@ -375,11 +390,12 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
   if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
-      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, dO, shape->d_v, shape->n_q, bhq))
+      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, dO, shape->d_v, shape->n_q, bhq) ||
+      !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
     return ATTN_ERR_CUDA;
   p.sh = shape_params(shape);
   p.scale = scale;
@@ -394,7 +410,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   p.dV = dV;
   p.status = status;
   const cudaError_t e =
-      launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+      launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -48,13 +48,14 @@
 // shared memory (the MMA takes one type for both operands; the conversion
 // is exact for |x| up to 65504 and saturates beyond).  The weights P used
 // inside dS are kept as fp16 too; dP = dO V^T and dV = P^T dO stay bf16.
-// Per step (query tile of 128 rows) the MMA order is
+// Per step (query tile of 128 rows) the products are
 //   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dK += dS^T Q,
-//   dQ = dS K -> X,
+//   dQ = dS K -> Y,
 // where tensor memory holds X [0,128), Y [128,256), dK [256, 256+DH) and
 // dV [256+DH, 256+DH+DV).  P^T and dS^T overwrite the first 64 columns of X
-// and Y once their fp32 inputs are consumed; dQ reuses X after the dV
-// product has read P^T (MMAs run in issue order).
+// and Y once their fp32 inputs are consumed; dQ reuses Y after the dK
+// product has read dS^T (MMAs run in issue order), which leaves X free for
+// the next step's scores while dQ is read out.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -97,7 +98,9 @@ struct BwdCfg {
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKDV = kBarDQFree + 1;
   static constexpr int kBarLse = kBarDKDV + 1;        // score warps loaded LSE, D
-  static constexpr int kBarDrain = kBarLse + 1;
+  static constexpr int kBarStageFull = kBarLse + 1;   // dQ staging written (read-out warps)
+  static constexpr int kBarStageFree = kBarStageFull + 1;   // staging read by the TMA reduce
+  static constexpr int kBarDrain = kBarStageFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -106,6 +109,11 @@ struct BwdCfg {
   static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
+  static constexpr int kDQBoxCols = 32;                       // fp32 columns per reduce box (128 B)
+  static constexpr int kDQBoxBytes = kTileM * kDQBoxCols * 4;  // 16 KB
+  static constexpr int kDQBoxes = DH / kDQBoxCols;
+  static constexpr int kDQBoxesPerRound = kDSTileBytes / kDQBoxBytes;   // 2 (staging = dS buffer)
+  static constexpr int kDQRounds = kDQBoxes / kDQBoxesPerRound;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
@@ -124,7 +132,7 @@ template <int DH, int DV>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const __grid_constant__ BwdParams p) {
+                     const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ BwdParams p) {
   using C = BwdCfg<DH, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -171,6 +179,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDKDV), 1);
     mbar_init(bar(C::kBarLse), 128);
+    mbar_init(bar(C::kBarStageFull), 128);
+    mbar_init(bar(C::kBarStageFree), 1);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
@@ -248,36 +258,42 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
       bool ok = wait_all(C::kBarK16, 0);
       const uint32_t kA = sbase + C::kOffK, vA = sbase + C::kOffV, dsA = sbase + C::kOffDS;
-      for (int s = 0; s < total && ok; ++s) {
-        const int st = s & 1;
-        ok = wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1));
-        if (!ok) break;
-        ok = wait_all(C::kBarQ16 + st, static_cast<uint32_t>((s >> 1) & 1));
-        if (!ok) break;
-        if (s > 0) {
-          ok = wait_all(C::kBarDQFree, static_cast<uint32_t>((s - 1) & 1));
-          if (!ok) break;
+      auto qB = [&](int s) { return sbase + C::kOffQ + (s & 1) * C::kQTileBytes; };
+      auto doB = [&](int s) { return sbase + C::kOffDO + (s & 1) * C::kDOTileBytes; };
+      auto issue_s = [&](int s) {   // S^T = K Q^T -> X
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          umma_ss(tmem + C::kTX, sw128_desc(kA + off, 16, 1024), sw128_desc(qB(s) + off, 16, 1024), kIdS,
+                  kk > 0 ? 1u : 0u);
         }
+        umma_commit(bar(C::kBarSFull));
+      };
+      auto issue_dp = [&](int s) {  // dP^T = V dO^T -> Y
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB(s) + off, 16, 1024), kIdDP,
+                  kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(C::kBarDPFull));
+      };
+      // Order per step s:  dV(s) | dK(s), dQ(s) -> Y | S(s+1) -> X | [dQ read out] dP(s+1) -> Y.
+      // S(s+1) only needs X, which dV(s) has finished reading (MMAs run in
+      // issue order), so the score warps start on step s+1 while dQ(s) is
+      // being read out of Y; dP(s+1) waits for that read-out.
+      if (ok) ok = wait_all(C::kBarQFull + 0, 0);
+      if (ok) ok = wait_all(C::kBarQ16 + 0, 0);
+      if (ok) {
         tc_fence_after_sync();
-        const uint32_t qB = sbase + C::kOffQ + st * C::kQTileBytes;
-        const uint32_t doB = sbase + C::kOffDO + st * C::kDOTileBytes;
         if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            umma_ss(tmem + C::kTX, sw128_desc(kA + off, 16, 1024), sw128_desc(qB + off, 16, 1024), kIdS,
-                    kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::kBarSFull));
-#pragma unroll
-          for (int kk = 0; kk < DV / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB + off, 16, 1024), kIdDP,
-                    kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::kBarDPFull));
+          issue_s(0);
+          issue_dp(0);
         }
         __syncwarp();
+      }
+      for (int s = 0; s < total && ok; ++s) {
+        const int st = s & 1;
         ok = wait_all(C::kBarPReady, static_cast<uint32_t>(s & 1));
         if (!ok) break;
         tc_fence_after_sync();
@@ -285,7 +301,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ts(tmem + C::kTdV, tmem + C::kTX + kk * 8,
-                    sw128_desc(doB + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
+                    sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
         ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
@@ -295,15 +311,29 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ts(tmem + C::kTdK, tmem + C::kTY + kk * 8,
-                    sw128_desc(qB + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
+                    sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            umma_ss(tmem + C::kTX, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
+            umma_ss(tmem + C::kTY, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
                     sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
           umma_commit(bar(C::kBarDQFull));
           umma_commit(bar(C::kBarQEmpty + st));
         }
         __syncwarp();
+        if (s + 1 < total) {
+          const int st1 = (s + 1) & 1;
+          ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          if (ok) ok = wait_all(C::kBarQ16 + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after_sync();
+          if (lane == 0) issue_s(s + 1);
+          __syncwarp();
+          ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
+          if (!ok) break;
+          tc_fence_after_sync();
+          if (lane == 0) issue_dp(s + 1);
+          __syncwarp();
+        }
       }
       if (lane == 0) {
         if (ok) umma_commit(bar(C::kBarDKDV));
@@ -370,8 +400,18 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     uint32_t rr[32];
     uint32_t pw[64];
+    // This thread's LSE and D entry (query q0 + tid) of a step, loaded one
+    // step ahead so the global-memory latency is off the critical path.
+    auto load_row_terms = [&](int s, float& lse2, float& dd) {
+      const int64_t i = static_cast<int64_t>(step_q0(s)) + tid;
+      const int64_t r = static_cast<int64_t>(b * p.sh.Hq + step_head(s)) * p.sh.n_q + i;
+      const bool in = i < p.sh.n_q;
+      lse2 = in ? p.LSE[r] * kLog2e : INFINITY;
+      dd = in ? p.D[r] : 0.f;
+    };
+    float lse_next = 0.f, d_next = 0.f;
+    if (ok) load_row_terms(0, lse_next, d_next);
     for (int s = 0; s < total && ok; ++s) {
-      const int bhq = b * p.sh.Hq + step_head(s);
       const int q0 = step_q0(s);
       // The single LSE/D buffer is rewritten only after every score thread
       // has finished the previous step (its dS-ready barrier completed).
@@ -379,12 +419,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         ok = wait_all(C::kBarDSReady, static_cast<uint32_t>((s - 1) & 1));
         if (!ok) break;
       }
-      {
-        const int64_t i = static_cast<int64_t>(q0) + tid;
-        const bool in = i < p.sh.n_q;
-        lse_s[tid] = in ? p.LSE[static_cast<int64_t>(bhq) * p.sh.n_q + i] * kLog2e : INFINITY;
-        dd_s[tid] = in ? p.D[static_cast<int64_t>(bhq) * p.sh.n_q + i] : 0.f;
-      }
+      lse_s[tid] = lse_next;
+      dd_s[tid] = d_next;
+      if (s + 1 < total) load_row_terms(s + 1, lse_next, d_next);
       mbar_arrive(bar(C::kBarLse));
       ok = wait_all(C::kBarLse, static_cast<uint32_t>(s & 1));
       if (!ok) break;
@@ -490,6 +527,14 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (ok) ok = wait_all(C::kBarScale, 0);
       if (ok) inv_scale = exp2_int(-scale_exponent());
     }
+    // dQ read-out: the tile (128 query rows x DH fp32, in Y) is staged
+    // through the dS buffer, which no one uses between the dQ product and the
+    // next step's dS, in the 128-byte swizzle pattern (conflict-free stores),
+    // and added into the fp32 accumulator by TMA reduce-add boxes of
+    // 128 rows x 32 columns; rows past n_q are clipped by the tensor map.
+    const uint32_t tY = tmem + lane_base + C::kTY;
+    uint8_t* stage = smem + C::kOffDS;
+    int rounds_done = 0;
     for (int s = 0; s < total && ok; ++s) {
       if (s + 1 < total) {
         const int st1 = (s + 1) & 1;
@@ -498,26 +543,44 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         convert_q(st1);
       }
       const int bhq = b * p.sh.Hq + step_head(s);
-      const int64_t i = static_cast<int64_t>(step_q0(s)) + row;
+      const int q0 = step_q0(s);
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      float4* dst = reinterpret_cast<float4*>(p.dQacc + (static_cast<int64_t>(bhq) * p.sh.n_q + i) * DH);
+      for (int rd = 0; rd < C::kDQRounds && ok; ++rd) {
 #pragma unroll
-      for (int cc = 0; cc < DH / 32; ++cc) {
-        tmem_ld32(tX + cc * 32, rr);
-        if (i < p.sh.n_q) {
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
+          const int box = rd * C::kDQBoxesPerRound + bx;
+          tmem_ld32(tY + box * C::kDQBoxCols, rr);
+          uint8_t* dst = stage + bx * C::kDQBoxBytes + row * 128;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            atomicAdd(dst + cc * 8 + v,
-                      make_float4(__uint_as_float(rr[4 * v]) * inv_scale, __uint_as_float(rr[4 * v + 1]) * inv_scale,
-                                  __uint_as_float(rr[4 * v + 2]) * inv_scale,
-                                  __uint_as_float(rr[4 * v + 3]) * inv_scale));
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(dst + ((c ^ (row & 7)) * 16)) =
+                make_float4(__uint_as_float(rr[4 * c]) * inv_scale, __uint_as_float(rr[4 * c + 1]) * inv_scale,
+                            __uint_as_float(rr[4 * c + 2]) * inv_scale, __uint_as_float(rr[4 * c + 3]) * inv_scale);
         }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::kBarStageFull));
+        const uint32_t ph = static_cast<uint32_t>(rounds_done & 1);
+        if (tid2 == 0) {
+          ok = mbar_wait(bar(C::kBarStageFull), ph, abort_flag, limit);
+          if (ok) {
+#pragma unroll
+            for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
+              tma_reduce_add_3d(&tmdQ, smem_u32(stage + bx * C::kDQBoxBytes),
+                                (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, q0, bhq);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+          }
+          mbar_arrive(bar(C::kBarStageFree));
+        }
+        ok = wait_all(C::kBarStageFree, ph) && ok;
+        ++rounds_done;
       }
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarDQFree));
     }
+    if (tid2 == 0) bulk_wait_group0();
     if (ok && total > 0) {
       ok = wait_all(C::kBarDKDV, 0);
       tc_fence_after_sync();
@@ -654,13 +717,14 @@ attn_bwd_finalize_kernel(int64_t n8, float scale, const float4* __restrict__ acc
 
 template <int DH, int DV>
 cudaError_t launch_bwd_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              const CUtensorMap& tmdO, const BwdParams& p, cudaStream_t stream) {
+                              const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdParams& p,
+                              cudaStream_t stream) {
   using C = BwdCfg<DH, DV>;
   auto kern = attn_bwd_main_kernel<DH, DV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN), static_cast<unsigned>(p.sh.B * p.sh.Hkv));
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, p);
   return cudaGetLastError();
 }
 
@@ -683,11 +747,11 @@ void launch_pre_t(int64_t bhq, int n_q, int nqt, const void* O, const void* O_lo
 }  // namespace
 
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdParams& p,
-                                 cudaStream_t stream) {
-  if (dh == 128 && dv == 128) return launch_bwd_main_t<128, 128>(tmQ, tmK, tmV, tmdO, p, stream);
-  if (dh == 64 && dv == 64) return launch_bwd_main_t<64, 64>(tmQ, tmK, tmV, tmdO, p, stream);
-  if (dh == 128 && dv == 64) return launch_bwd_main_t<128, 64>(tmQ, tmK, tmV, tmdO, p, stream);
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
+                                 const BwdParams& p, cudaStream_t stream) {
+  if (dh == 128 && dv == 128) return launch_bwd_main_t<128, 128>(tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
+  if (dh == 64 && dv == 64) return launch_bwd_main_t<64, 64>(tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
+  if (dh == 128 && dv == 64) return launch_bwd_main_t<128, 64>(tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
   return cudaErrorInvalidValue;
 }
 

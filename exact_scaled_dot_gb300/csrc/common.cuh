@@ -106,7 +106,7 @@ constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                 const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* O, const void* O_lo,
                                        const void* dO, float* D, float2* tilemax, float* dQacc,
