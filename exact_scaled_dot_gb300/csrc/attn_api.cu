@@ -41,8 +41,8 @@ int check_shape(const attn_shape* s) {
   const int64_t bhq = static_cast<int64_t>(s->B) * s->Hq;
   if (bhq > (int64_t{1} << 31) - 1) return ATTN_ERR_SHAPE;
   // Grid dimensions y: forward query-tile pairs, preprocess query tiles and
-  // backward (batch, KV head) pairs must stay within 65535.
-  if (static_cast<int64_t>(s->B) * s->Hkv > 65535) return ATTN_ERR_SHAPE;
+  // backward key tiles must stay within 65535.
+  if ((static_cast<int64_t>(s->n_k) + 127) / 128 > 65535) return ATTN_ERR_SHAPE;
   if ((static_cast<int64_t>(s->n_q) + 127) / 128 > 65535) return ATTN_ERR_SHAPE;
   if (!supported_dims(s->d_h, s->d_v)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
@@ -141,14 +141,14 @@ bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
 }
 
 // 3-D view [bh][n][d] of the fp32 dQ accumulator for TMA reduce-add in
-// 128-row x 32-column boxes (128 bytes, 128-byte swizzle); rows beyond n of
-// a head are clipped.
+// 32-row x 32-column boxes (128-byte rows, 128-byte swizzle); rows beyond n
+// of a head are clipped.
 bool make_tmap_acc(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(n) * d * 4};
-  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

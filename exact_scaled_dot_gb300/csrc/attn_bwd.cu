@@ -98,9 +98,8 @@ struct BwdCfg {
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKDV = kBarDQFree + 1;
   static constexpr int kBarLse = kBarDKDV + 1;        // score warps loaded LSE, D
-  static constexpr int kBarStageFull = kBarLse + 1;   // dQ staging written (read-out warps)
-  static constexpr int kBarStageFree = kBarStageFull + 1;   // staging read by the TMA reduce
-  static constexpr int kBarDrain = kBarStageFree + 1;
+  static constexpr int kBarDSFree = kBarLse + 1;     // dS buffer no longer read by the dQ reduce
+  static constexpr int kBarDrain = kBarDSFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -109,11 +108,14 @@ struct BwdCfg {
   static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
-  static constexpr int kDQBoxCols = 32;                       // fp32 columns per reduce box (128 B)
-  static constexpr int kDQBoxBytes = kTileM * kDQBoxCols * 4;  // 16 KB
+  // dQ read-out: each read-out warp stages its 32 query rows as DH/32 boxes
+  // of 32 rows x 32 fp32 (4 KB), warps 0-1 in the dS buffer and warps 2-3
+  // in the step's Q stage (both consumed once the dQ product is done).
+  static constexpr int kDQBoxCols = 32;
+  static constexpr int kDQBoxBytes = 32 * kDQBoxCols * 4;
   static constexpr int kDQBoxes = DH / kDQBoxCols;
-  static constexpr int kDQBoxesPerRound = kDSTileBytes / kDQBoxBytes;   // 2 (staging = dS buffer)
-  static constexpr int kDQRounds = kDQBoxes / kDQBoxesPerRound;
+  static constexpr int kDQWarpStage = kDQBoxes * kDQBoxBytes;
+  static_assert(2 * kDQWarpStage <= kDSTileBytes && 2 * kDQWarpStage <= kQTileBytes, "dQ staging");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
@@ -148,11 +150,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
 
-  // ---- work item: key tile blockIdx.x of (batch, KV head) blockIdx.y ----
-  const int bkv = blockIdx.y;
+  // ---- work item: key tile blockIdx.y of (batch, KV head) blockIdx.x.  The
+  // (batch, KV head) index runs fastest, so the first CTAs dispatched are the
+  // low key tiles, which under a causal mask see the most query tiles. ----
+  const int bkv = blockIdx.x;
   const int b = bkv / p.sh.Hkv;
   const int hkv = bkv - b * p.sh.Hkv;
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kTileN;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.y) * kTileN;
   const int64_t klen = key_len(p.mask, p.sh.n_k, b);
   const int64_t i_first = first_row_seeing_key(p.mask, p.sh.n_q, p.sh.n_k, b, j0);
   const int nqt = (p.sh.n_q + kTileM - 1) / kTileM;
@@ -166,7 +170,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarKV), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
-      mbar_init(bar(C::kBarQEmpty + s), 1);
+      mbar_init(bar(C::kBarQEmpty + s), 1 + 4);   // MMA commit + the four read-out warps
       mbar_init(bar(C::kBarQ16 + s), 128);
     }
     mbar_init(bar(C::kBarK16), 128);
@@ -179,8 +183,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDKDV), 1);
     mbar_init(bar(C::kBarLse), 128);
-    mbar_init(bar(C::kBarStageFull), 128);
-    mbar_init(bar(C::kBarStageFree), 1);
+    mbar_init(bar(C::kBarDSFree), 4);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
@@ -398,7 +401,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = ok && wait_all(C::kBarScale, 0);
       ds_scale = exp2_int(scale_exponent());
     }
-    uint32_t rr[32];
     uint32_t pw[64];
     // This thread's LSE and D entry (query q0 + tid) of a step, loaded one
     // step ahead so the global-memory latency is off the critical path.
@@ -420,7 +422,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (!ok) break;
       }
       lse_s[tid] = lse_next;
-      dd_s[tid] = d_next;
+      dd_s[tid] = d_next * ds_scale;
       if (s + 1 < total) load_row_terms(s + 1, lse_next, d_next);
       mbar_arrive(bar(C::kBarLse));
       ok = wait_all(C::kBarLse, static_cast<uint32_t>(s & 1));
@@ -433,56 +435,81 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarSFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
+      // P pass over 16-column chunks; the next chunk's load is in flight
+      // while this one is computed.  P^T (bf16) goes back into X behind the
+      // columns already read; P (fp16) stays in registers for the dS pass.
+      {
+        uint32_t ra[16], rb[16];
+        tmem_ld16_nowait(tX, ra);
+        tmem_wait_ld16(ra);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tX + cc * 32, rr);
-        uint32_t w[16];
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t (&cur)[16] = (ch & 1) ? rb : ra;
+          uint32_t (&nxt)[16] = (ch & 1) ? ra : rb;
+          if (ch + 1 < 8) tmem_ld16_nowait(tX + (ch + 1) * 16, nxt);
+          uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int c = cc * 32 + k;
-          float p0 = fast_exp2(fmaf(__uint_as_float(rr[k]), sl2, -lse_s[c]));
-          float p1 = fast_exp2(fmaf(__uint_as_float(rr[k + 1]), sl2, -lse_s[c + 1]));
-          if (need_mask) {
-            p0 = (!row_masked && c >= cmin) ? p0 : 0.f;
-            p1 = (!row_masked && c + 1 >= cmin) ? p1 : 0.f;
+          for (int k = 0; k < 16; k += 2) {
+            const int c = ch * 16 + k;
+            float p0 = fast_exp2(fmaf(__uint_as_float(cur[k]), sl2, -lse_s[c]));
+            float p1 = fast_exp2(fmaf(__uint_as_float(cur[k + 1]), sl2, -lse_s[c + 1]));
+            if (need_mask) {
+              p0 = (!row_masked && c >= cmin) ? p0 : 0.f;
+              p1 = (!row_masked && c + 1 >= cmin) ? p1 : 0.f;
+            }
+            w[k >> 1] = pack_bf16x2(p0, p1);
+            pw[ch * 8 + (k >> 1)] = pack_f16x2(p0, p1);
           }
-          w[k >> 1] = pack_bf16x2(p0, p1);
-          pw[cc * 16 + (k >> 1)] = pack_f16x2(p0, p1);
+          tmem_st8_nowait(tX + ch * 8, w);
+          if (ch + 1 < 8) tmem_wait_ld16(nxt);
         }
-        tmem_st16(tX + cc * 16, w);
+        tmem_wait_st();
       }
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarPReady));
       ok = wait_all(C::kBarDPFull, static_cast<uint32_t>(s & 1));
+      // The dS buffer doubles as dQ staging of the previous step.
+      if (ok && s > 0) ok = wait_all(C::kBarDSFree, static_cast<uint32_t>((s - 1) & 1));
       if (!ok) break;
       tc_fence_after_sync();
+      // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into Y (for dK) and
+      // into the dS buffer (for dQ); dd_s already holds D * 2^e.
+      {
+        uint32_t ra[16], rb[16];
+        tmem_ld16_nowait(tY, ra);
+        tmem_wait_ld16(ra);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tY + cc * 32, rr);
-        uint32_t w[16];
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t (&cur)[16] = (ch & 1) ? rb : ra;
+          uint32_t (&nxt)[16] = (ch & 1) ? ra : rb;
+          if (ch + 1 < 8) tmem_ld16_nowait(tY + (ch + 1) * 16, nxt);
+          uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int c = cc * 32 + k;
-          const uint32_t pp = pw[cc * 16 + (k >> 1)];
-          float d0 = f16_lo(pp) * (__uint_as_float(rr[k]) - dd_s[c]);
-          float d1 = f16_hi(pp) * (__uint_as_float(rr[k + 1]) - dd_s[c + 1]);
-          if (need_mask) {
-            d0 = (!row_masked && c >= cmin) ? d0 : 0.f;
-            d1 = (!row_masked && c + 1 >= cmin) ? d1 : 0.f;
+          for (int k = 0; k < 16; k += 2) {
+            const int c = ch * 16 + k;
+            const uint32_t pp = pw[ch * 8 + (k >> 1)];
+            float d0 = f16_lo(pp) * fmaf(__uint_as_float(cur[k]), ds_scale, -dd_s[c]);
+            float d1 = f16_hi(pp) * fmaf(__uint_as_float(cur[k + 1]), ds_scale, -dd_s[c + 1]);
+            if (need_mask) {
+              d0 = (!row_masked && c >= cmin) ? d0 : 0.f;
+              d1 = (!row_masked && c + 1 >= cmin) ? d1 : 0.f;
+            }
+            w[k >> 1] = pack_f16x2(d0, d1);
           }
-          w[k >> 1] = pack_f16x2(d0 * ds_scale, d1 * ds_scale);
-        }
-        tmem_st16(tY + cc * 16, w);
-        // dS (queries contiguous per key row) for the dQ = dS K product:
-        // block cc/2 holds queries [64*(cc/2), +64); 16-byte chunk index
-        // is XOR-swizzled with the key row (128-byte swizzle pattern).
-        uint8_t* blk = ds_row + (cc >> 1) * C::kBlockBytes;
+          tmem_st8_nowait(tY + ch * 8, w);
+          // dS (queries contiguous per key row) for the dQ = dS K product:
+          // block ch/4 holds queries [64*(ch/4), +64); 16-byte chunk index
+          // is XOR-swizzled with the key row (128-byte swizzle pattern).
+          uint8_t* blk = ds_row + (ch >> 2) * C::kBlockBytes;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int chunk = (cc & 1) * 4 + v;
-          *reinterpret_cast<uint4*>(blk + ((chunk ^ (jj & 7)) * 16)) =
-              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          for (int v = 0; v < 2; ++v) {
+            const int chunk = (ch & 3) * 2 + v;
+            *reinterpret_cast<uint4*>(blk + ((chunk ^ (jj & 7)) * 16)) =
+                make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+          if (ch + 1 < 8) tmem_wait_ld16(nxt);
         }
+        tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
@@ -527,14 +554,16 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (ok) ok = wait_all(C::kBarScale, 0);
       if (ok) inv_scale = exp2_int(-scale_exponent());
     }
-    // dQ read-out: the tile (128 query rows x DH fp32, in Y) is staged
-    // through the dS buffer, which no one uses between the dQ product and the
-    // next step's dS, in the 128-byte swizzle pattern (conflict-free stores),
-    // and added into the fp32 accumulator by TMA reduce-add boxes of
-    // 128 rows x 32 columns; rows past n_q are clipped by the tensor map.
+    // dQ read-out: each warp takes its 32 query rows of the tile (in Y),
+    // scales them back by 2^-e and stages them as 32 x 32 fp32 boxes in the
+    // 128-byte swizzle pattern (conflict-free stores), warps 0-1 in the dS
+    // buffer and warps 2-3 in the step's Q stage, both consumed once the dQ
+    // product has completed.  Y is released as soon as the tensor-memory
+    // reads are done; one lane then adds the boxes into the fp32 accumulator
+    // with TMA reduce-add and, once the boxes have been read, hands the Q
+    // stage back to the producer and the dS buffer back to the score warps.
+    // Rows past n_q are clipped by the tensor map.
     const uint32_t tY = tmem + lane_base + C::kTY;
-    uint8_t* stage = smem + C::kOffDS;
-    int rounds_done = 0;
     for (int s = 0; s < total && ok; ++s) {
       if (s + 1 < total) {
         const int st1 = (s + 1) & 1;
@@ -547,40 +576,37 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      for (int rd = 0; rd < C::kDQRounds && ok; ++rd) {
+      uint8_t* wstage = (quad < 2) ? smem + C::kOffDS + quad * C::kDQWarpStage
+                                   : smem + C::kOffQ + (s & 1) * C::kQTileBytes + (quad - 2) * C::kDQWarpStage;
 #pragma unroll
-        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
-          const int box = rd * C::kDQBoxesPerRound + bx;
-          tmem_ld32(tY + box * C::kDQBoxCols, rr);
-          uint8_t* dst = stage + bx * C::kDQBoxBytes + row * 128;
+      for (int bx = 0; bx < C::kDQBoxes; ++bx) {
+        tmem_ld32(tY + bx * C::kDQBoxCols, rr);
+        uint8_t* dst = wstage + bx * C::kDQBoxBytes + lane * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4*>(dst + ((c ^ (row & 7)) * 16)) =
-                make_float4(__uint_as_float(rr[4 * c]) * inv_scale, __uint_as_float(rr[4 * c + 1]) * inv_scale,
-                            __uint_as_float(rr[4 * c + 2]) * inv_scale, __uint_as_float(rr[4 * c + 3]) * inv_scale);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(C::kBarStageFull));
-        const uint32_t ph = static_cast<uint32_t>(rounds_done & 1);
-        if (tid2 == 0) {
-          ok = mbar_wait(bar(C::kBarStageFull), ph, abort_flag, limit);
-          if (ok) {
-#pragma unroll
-            for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
-              tma_reduce_add_3d(&tmdQ, smem_u32(stage + bx * C::kDQBoxBytes),
-                                (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, q0, bhq);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-          }
-          mbar_arrive(bar(C::kBarStageFree));
-        }
-        ok = wait_all(C::kBarStageFree, ph) && ok;
-        ++rounds_done;
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(dst + ((c ^ (lane & 7)) * 16)) =
+              make_float4(__uint_as_float(rr[4 * c]) * inv_scale, __uint_as_float(rr[4 * c + 1]) * inv_scale,
+                          __uint_as_float(rr[4 * c + 2]) * inv_scale, __uint_as_float(rr[4 * c + 3]) * inv_scale);
       }
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarDQFree));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = q0 + static_cast<int>(quad) * 32;
+        if (row0 < p.sh.n_q) {
+#pragma unroll
+          for (int bx = 0; bx < C::kDQBoxes; ++bx)
+            tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), bx * C::kDQBoxCols, row0, bhq);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(bar(C::kBarQEmpty + (s & 1)));
+        mbar_arrive(bar(C::kBarDSFree));
+      }
+      __syncwarp();
     }
-    if (tid2 == 0) bulk_wait_group0();
+    if (lane == 0) bulk_wait_group0();
     if (ok && total > 0) {
       ok = wait_all(C::kBarDKDV, 0);
       tc_fence_after_sync();
@@ -723,7 +749,7 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
   auto kern = attn_bwd_main_kernel<DH, DV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN), static_cast<unsigned>(p.sh.B * p.sh.Hkv));
+  dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN));
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, p);
   return cudaGetLastError();
 }

@@ -67,8 +67,8 @@ extern "C" {
 #define ATTN_OK               0
 #define ATTN_ERR_NULL         1  /* a required pointer is NULL                         */
 #define ATTN_ERR_SHAPE        2  /* non-positive size, Hq % Hkv != 0, kv_len out of   */
-                                 /* [1, n_k], B > ATTN_MAX_BATCH, B*Hkv > 65535,        */
-                                 /* n_q > 65535*128, size overflow                      */
+                                 /* [1, n_k], B > ATTN_MAX_BATCH, n_q or n_k above       */
+                                 /* 65535*128, size overflow                            */
 #define ATTN_ERR_UNSUPPORTED  3  /* (d_h, d_v) not one of the supported pairs          */
 #define ATTN_ERR_ALIGN        4  /* a tensor pointer is not 16-byte aligned            */
 #define ATTN_ERR_EMPTY_ROW    5  /* some query row has an empty visible set            */
