@@ -25,15 +25,16 @@
 //               accumulator with vector atomics.
 //   finalize    dQ = scale * accumulator, rounded to bf16.
 //
-// Main-kernel warp roles (384 threads):
+// Main-kernel warp roles (512 threads):
 //   warp 0      TMA producer: the K and V tile once, then Q and dO tiles
 //               of every step into a two-stage ring.
 //   warp 1      MMA issuer (lane 0 issues).
-//   warps 4-7   "score" warpgroup, thread = key row = TMEM lane:
+//   warps 4-11  two "score" warpgroups, one per 64-query half of the step,
+//               thread = key row = TMEM lane:
 //               P^T = exp2(S^T scale log2e - LSE log2e) and
 //               dS^T = P^T (dP^T - D), written back to tensor memory and
 //               dS to shared memory for the dQ product.
-//   warps 8-11  converts K and each Q tile to fp16 in shared memory, reads
+//   warps 12-15 converts K and each Q tile to fp16 in shared memory, reads
 //               dQ out (atomics) and writes the final dK, dV.
 //
 // Precision of the dS products.  dQ_i = scale sum_j dS_ij k_j sums terms
@@ -105,7 +106,7 @@ struct BwdCfg {
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemUsed = kOffAbort + 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;
-  static constexpr int kThreads = 384;
+  static constexpr int kThreads = 512;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
   // dQ read-out: each read-out warp stages its 32 query rows as DH/32 boxes
@@ -131,7 +132,7 @@ __device__ __forceinline__ int ds_scale_exponent(float bound) {
 }
 
 template <int DH, int DV>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ BwdParams p) {
@@ -177,12 +178,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarScale), 128);
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
-    mbar_init(bar(C::kBarPReady), 128);
-    mbar_init(bar(C::kBarDSReady), 128);
+    mbar_init(bar(C::kBarPReady), 256);
+    mbar_init(bar(C::kBarDSReady), 256);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDKDV), 1);
-    mbar_init(bar(C::kBarLse), 128);
+    mbar_init(bar(C::kBarLse), 256);
     mbar_init(bar(C::kBarDSFree), 4);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
@@ -281,10 +282,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         umma_commit(bar(C::kBarDPFull));
       };
-      // Order per step s:  dV(s) | dK(s), dQ(s) -> Y | S(s+1) -> X | [dQ read out] dP(s+1) -> Y.
+      // Order per step s:  dV(s) | S(s+1) -> X | dK(s), dQ(s) -> Y | [dQ read out] dP(s+1) -> Y.
       // S(s+1) only needs X, which dV(s) has finished reading (MMAs run in
-      // issue order), so the score warps start on step s+1 while dQ(s) is
-      // being read out of Y; dP(s+1) waits for that read-out.
+      // issue order), so the scores of step s+1 are ready when the score
+      // warps finish step s; dP(s+1) waits for dQ(s) to be read out of Y.
+      // The two score warpgroups leave P^T and dS^T for queries [0,64) in
+      // columns [0,32) and for queries [64,128) in columns [64,96) of X and Y.
+      auto half_col = [](int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); };
       if (ok) ok = wait_all(C::kBarQFull + 0, 0);
       if (ok) ok = wait_all(C::kBarQ16 + 0, 0);
       if (ok) {
@@ -303,24 +307,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts(tmem + C::kTdV, tmem + C::kTX + kk * 8,
+            umma_ts(tmem + C::kTdV, tmem + C::kTX + half_col(kk),
                     sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
-        }
-        __syncwarp();
-        ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
-        if (!ok) break;
-        tc_fence_after_sync();
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts(tmem + C::kTdK, tmem + C::kTY + kk * 8,
-                    sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            umma_ss(tmem + C::kTY, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
-                    sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
-          umma_commit(bar(C::kBarDQFull));
-          umma_commit(bar(C::kBarQEmpty + st));
         }
         __syncwarp();
         if (s + 1 < total) {
@@ -331,6 +319,24 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tc_fence_after_sync();
           if (lane == 0) issue_s(s + 1);
           __syncwarp();
+        }
+        ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            umma_ts(tmem + C::kTdK, tmem + C::kTY + half_col(kk),
+                    sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            umma_ss(tmem + C::kTY, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
+                    sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::kBarDQFull));
+          umma_commit(bar(C::kBarQEmpty + st));
+        }
+        __syncwarp();
+        if (s + 1 < total) {
           ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
           if (!ok) break;
           tc_fence_after_sync();
@@ -346,21 +352,24 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       }
       __syncwarp();
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ============================ score warps ===========================
+  } else if (warp >= 4 && warp < 12) {
+    // =========================== score warpgroups =======================
+    // Two warpgroups: h = 0 takes query columns [0, 64), h = 1 [64, 128);
+    // in both, thread = key row = TMEM lane.
+    const int h = static_cast<int>(warp - 4) / 4;
     const uint32_t quad = warp & 3;
     const int jj = static_cast<int>(quad * 32 + lane);
-    const int tid = static_cast<int>(threadIdx.x) - 128;
+    const int tid = static_cast<int>(threadIdx.x) - 128 - 128 * h;
     const int64_t j = j0 + jj;
     const bool row_masked = j >= klen;
     const uint32_t lane_base = (quad * 32u) << 16;
     const uint32_t tX = tmem + lane_base + C::kTX;
     const uint32_t tY = tmem + lane_base + C::kTY;
     const float sl2 = p.scale_log2;
-    uint8_t* ds_row = smem + C::kOffDS + jj * 128;
+    uint8_t* ds_row = smem + C::kOffDS + h * C::kBlockBytes + jj * 128;
     bool ok = *abort_flag == 0 && total > 0;
     float ds_scale = 1.f;
-    if (ok) {
+    if (ok && h == 0) {
       // ---- bound on |dS| for this CTA -> power-of-two scale ----
       ok = wait_all(C::kBarKV, 0);
       float vn2 = 0.f;
@@ -398,16 +407,19 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         red_s[4 * quad + 2] = md;
       }
       mbar_arrive(bar(C::kBarScale));
-      ok = ok && wait_all(C::kBarScale, 0);
+    }
+    if (ok) {
+      ok = wait_all(C::kBarScale, 0);
       ds_scale = exp2_int(scale_exponent());
     }
-    uint32_t pw[64];
-    // This thread's LSE and D entry (query q0 + tid) of a step, loaded one
-    // step ahead so the global-memory latency is off the critical path.
+    uint32_t pw[32];
+    // This thread's LSE and D entry (query q0 + 64h + tid, for tid < 64) of
+    // a step, loaded one step ahead so the global latency is off the
+    // critical path.
     auto load_row_terms = [&](int s, float& lse2, float& dd) {
-      const int64_t i = static_cast<int64_t>(step_q0(s)) + tid;
+      const int64_t i = static_cast<int64_t>(step_q0(s)) + 64 * h + tid;
       const int64_t r = static_cast<int64_t>(b * p.sh.Hq + step_head(s)) * p.sh.n_q + i;
-      const bool in = i < p.sh.n_q;
+      const bool in = tid < 64 && i < p.sh.n_q;
       lse2 = in ? p.LSE[r] * kLog2e : INFINITY;
       dd = in ? p.D[r] : 0.f;
     };
@@ -415,14 +427,16 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     if (ok) load_row_terms(0, lse_next, d_next);
     for (int s = 0; s < total && ok; ++s) {
       const int q0 = step_q0(s);
-      // The single LSE/D buffer is rewritten only after every score thread
-      // has finished the previous step (its dS-ready barrier completed).
+      // The LSE/D buffer is rewritten only after both warpgroups have
+      // finished the previous step (its dS-ready barrier completed).
       if (s > 0) {
         ok = wait_all(C::kBarDSReady, static_cast<uint32_t>((s - 1) & 1));
         if (!ok) break;
       }
-      lse_s[tid] = lse_next;
-      dd_s[tid] = d_next * ds_scale;
+      if (tid < 64) {
+        lse_s[64 * h + tid] = lse_next;
+        dd_s[64 * h + tid] = d_next * ds_scale;
+      }
       if (s + 1 < total) load_row_terms(s + 1, lse_next, d_next);
       mbar_arrive(bar(C::kBarLse));
       ok = wait_all(C::kBarLse, static_cast<uint32_t>(s & 1));
@@ -431,26 +445,26 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       // kv_len and, when causal, q0 + c >= j - offset.
       const int64_t cmin64 = p.mask.causal ? (j - p.mask.offset - q0) : INT64_MIN / 2;
       const int cmin = cmin64 > kTileM ? kTileM + 1 : (cmin64 < -1 ? -1 : static_cast<int>(cmin64));
-      const bool need_mask = __any_sync(0xffffffffu, row_masked || cmin > 0);
+      const bool need_mask = __any_sync(0xffffffffu, row_masked || cmin > 64 * h);
       ok = wait_all(C::kBarSFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      // P pass over 16-column chunks; the next chunk's load is in flight
-      // while this one is computed.  P^T (bf16) goes back into X behind the
-      // columns already read; P (fp16) stays in registers for the dS pass.
+      // P pass over this half's four 16-column chunks; the next chunk's load
+      // is in flight while this one is computed.  P^T (bf16) goes into X
+      // behind the columns already read; P (fp16) stays in registers.
       {
         uint32_t ra[16], rb[16];
-        tmem_ld16_nowait(tX, ra);
+        tmem_ld16_nowait(tX + 64 * h, ra);
         tmem_wait_ld16(ra);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t (&cur)[16] = (ch & 1) ? rb : ra;
-          uint32_t (&nxt)[16] = (ch & 1) ? ra : rb;
-          if (ch + 1 < 8) tmem_ld16_nowait(tX + (ch + 1) * 16, nxt);
+        for (int cq = 0; cq < 4; ++cq) {
+          uint32_t (&cur)[16] = (cq & 1) ? rb : ra;
+          uint32_t (&nxt)[16] = (cq & 1) ? ra : rb;
+          if (cq + 1 < 4) tmem_ld16_nowait(tX + 64 * h + (cq + 1) * 16, nxt);
           uint32_t w[8];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
-            const int c = ch * 16 + k;
+            const int c = 64 * h + cq * 16 + k;
             float p0 = fast_exp2(fmaf(__uint_as_float(cur[k]), sl2, -lse_s[c]));
             float p1 = fast_exp2(fmaf(__uint_as_float(cur[k + 1]), sl2, -lse_s[c + 1]));
             if (need_mask) {
@@ -458,10 +472,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
               p1 = (!row_masked && c + 1 >= cmin) ? p1 : 0.f;
             }
             w[k >> 1] = pack_bf16x2(p0, p1);
-            pw[ch * 8 + (k >> 1)] = pack_f16x2(p0, p1);
+            pw[cq * 8 + (k >> 1)] = pack_f16x2(p0, p1);
           }
-          tmem_st8_nowait(tX + ch * 8, w);
-          if (ch + 1 < 8) tmem_wait_ld16(nxt);
+          tmem_st8_nowait(tX + 64 * h + cq * 8, w);
+          if (cq + 1 < 4) tmem_wait_ld16(nxt);
         }
         tmem_wait_st();
       }
@@ -473,21 +487,21 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (!ok) break;
       tc_fence_after_sync();
       // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into Y (for dK) and
-      // into the dS buffer (for dQ); dd_s already holds D * 2^e.
+      // into this half's block of the dS buffer (for dQ); dd_s holds D 2^e.
       {
         uint32_t ra[16], rb[16];
-        tmem_ld16_nowait(tY, ra);
+        tmem_ld16_nowait(tY + 64 * h, ra);
         tmem_wait_ld16(ra);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t (&cur)[16] = (ch & 1) ? rb : ra;
-          uint32_t (&nxt)[16] = (ch & 1) ? ra : rb;
-          if (ch + 1 < 8) tmem_ld16_nowait(tY + (ch + 1) * 16, nxt);
+        for (int cq = 0; cq < 4; ++cq) {
+          uint32_t (&cur)[16] = (cq & 1) ? rb : ra;
+          uint32_t (&nxt)[16] = (cq & 1) ? ra : rb;
+          if (cq + 1 < 4) tmem_ld16_nowait(tY + 64 * h + (cq + 1) * 16, nxt);
           uint32_t w[8];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
-            const int c = ch * 16 + k;
-            const uint32_t pp = pw[ch * 8 + (k >> 1)];
+            const int c = 64 * h + cq * 16 + k;
+            const uint32_t pp = pw[cq * 8 + (k >> 1)];
             float d0 = f16_lo(pp) * fmaf(__uint_as_float(cur[k]), ds_scale, -dd_s[c]);
             float d1 = f16_hi(pp) * fmaf(__uint_as_float(cur[k + 1]), ds_scale, -dd_s[c + 1]);
             if (need_mask) {
@@ -496,18 +510,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             w[k >> 1] = pack_f16x2(d0, d1);
           }
-          tmem_st8_nowait(tY + ch * 8, w);
+          tmem_st8_nowait(tY + 64 * h + cq * 8, w);
           // dS (queries contiguous per key row) for the dQ = dS K product:
-          // block ch/4 holds queries [64*(ch/4), +64); 16-byte chunk index
-          // is XOR-swizzled with the key row (128-byte swizzle pattern).
-          uint8_t* blk = ds_row + (ch >> 2) * C::kBlockBytes;
+          // this half's 64 queries fill one 128-byte row of its block, the
+          // 16-byte chunk index XOR-swizzled with the key row.
 #pragma unroll
           for (int v = 0; v < 2; ++v) {
-            const int chunk = (ch & 3) * 2 + v;
-            *reinterpret_cast<uint4*>(blk + ((chunk ^ (jj & 7)) * 16)) =
+            const int chunk = cq * 2 + v;
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (jj & 7)) * 16)) =
                 make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
-          if (ch + 1 < 8) tmem_wait_ld16(nxt);
+          if (cq + 1 < 4) tmem_wait_ld16(nxt);
         }
         tmem_wait_st();
       }
@@ -515,11 +528,11 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarDSReady));
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ====== fp16 re-encoding of K and Q, dQ read-out, dK/dV epilogue ======
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
-    const int tid2 = static_cast<int>(threadIdx.x) - 256;
+    const int tid2 = static_cast<int>(threadIdx.x) - 384;
     const uint32_t lane_base = (quad * 32u) << 16;
     const uint32_t tX = tmem + lane_base + C::kTX;
     bool ok = *abort_flag == 0;
