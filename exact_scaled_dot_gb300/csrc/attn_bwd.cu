@@ -88,7 +88,9 @@ struct BwdCfg {
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;                 // [2]
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
-  static constexpr int kBarQ16 = kBarQEmpty + 2;      // [2] Q tile re-encoded as fp16
+  static constexpr int kBarDOFull = kBarQEmpty + 2;   // [2]
+  static constexpr int kBarDOEmpty = kBarDOFull + 2;  // [2]
+  static constexpr int kBarQ16 = kBarDOEmpty + 2;     // [2] Q tile re-encoded as fp16
   static constexpr int kBarK16 = kBarQ16 + 2;         // K tile re-encoded as fp16
   static constexpr int kBarScale = kBarK16 + 1;       // dS scale bound reduced
   static constexpr int kBarSFull = kBarScale + 1;
@@ -109,14 +111,21 @@ struct BwdCfg {
   static constexpr int kThreads = 512;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
-  // dQ read-out: each read-out warp stages its 32 query rows as DH/32 boxes
-  // of 32 rows x 32 fp32 (4 KB), warps 0-1 in the dS buffer and warps 2-3
-  // in the step's Q stage (both consumed once the dQ product is done).
+  // dQ read-out: each read-out warp stages its 32 query rows as boxes of 32
+  // rows x 32 fp32 (4 KB).  With d_h = d_v = 128 all four boxes of a warp
+  // fit at once, warps 0-1 in the dS buffer and warps 2-3 in the step's dO
+  // stage (both consumed once the dQ product is done); otherwise the dS
+  // buffer alone holds two boxes per warp and the read-out takes DH/64
+  // rounds.
   static constexpr int kDQBoxCols = 32;
   static constexpr int kDQBoxBytes = 32 * kDQBoxCols * 4;
   static constexpr int kDQBoxes = DH / kDQBoxCols;
-  static constexpr int kDQWarpStage = kDQBoxes * kDQBoxBytes;
-  static_assert(2 * kDQWarpStage <= kDSTileBytes && 2 * kDQWarpStage <= kQTileBytes, "dQ staging");
+  static constexpr bool kStageInDO = (DH == 128 && DV == 128);
+  static constexpr int kDQBoxesPerRound = kStageInDO ? 4 : 2;
+  static constexpr int kDQRounds = kDQBoxes / kDQBoxesPerRound;
+  static constexpr int kDQWarpStage = kDQBoxesPerRound * kDQBoxBytes;
+  static_assert(kStageInDO ? (2 * kDQWarpStage <= kDSTileBytes && 2 * kDQWarpStage <= kDOTileBytes)
+                           : (4 * kDQWarpStage <= kDSTileBytes), "dQ staging");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
@@ -171,10 +180,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarKV), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
-      mbar_init(bar(C::kBarQEmpty + s), 1 + 4);   // MMA commit + the four read-out warps
-      mbar_init(bar(C::kBarQ16 + s), 128);
+      mbar_init(bar(C::kBarQEmpty + s), 1);
+      mbar_init(bar(C::kBarDOFull + s), 1);
+      // MMA commit, plus the four read-out warps when the dO stage is staging.
+      mbar_init(bar(C::kBarDOEmpty + s), C::kStageInDO ? 1 + 4 : 1);
+      mbar_init(bar(C::kBarQ16 + s), 64);
     }
-    mbar_init(bar(C::kBarK16), 128);
+    mbar_init(bar(C::kBarK16), 64);
     mbar_init(bar(C::kBarScale), 128);
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
@@ -228,28 +240,32 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       for (int c = 0; c < DV / 64; ++c)
         tma_load_3d(sbase + C::kOffV + c * C::kBlockBytes, &tmV, bar(C::kBarKV), c * 64,
                     static_cast<int32_t>(j0), bkv);
-      int issued[2] = {0, 0};
+      int q_issued[2] = {0, 0}, do_issued[2] = {0, 0};
       for (int s = 0; s < total; ++s) {
         const int st = s & 1;
-        if (!mbar_wait(bar(C::kBarQEmpty + st), static_cast<uint32_t>(((s >> 1) & 1) ^ 1), abort_flag,
-                       limit))
-          break;
+        const uint32_t ph = static_cast<uint32_t>(((s >> 1) & 1) ^ 1);
         const int bhq = b * p.sh.Hq + step_head(s);
         const int q0 = step_q0(s);
-        mbar_arrive_expect_tx(bar(C::kBarQFull + st), C::kQTileBytes + C::kDOTileBytes);
+        if (!mbar_wait(bar(C::kBarQEmpty + st), ph, abort_flag, limit)) break;
+        mbar_arrive_expect_tx(bar(C::kBarQFull + st), C::kQTileBytes);
         for (int c = 0; c < DH / 64; ++c)
           tma_load_3d(sbase + C::kOffQ + st * C::kQTileBytes + c * C::kBlockBytes, &tmQ,
                       bar(C::kBarQFull + st), c * 64, q0, bhq);
+        ++q_issued[st];
+        if (!mbar_wait(bar(C::kBarDOEmpty + st), ph, abort_flag, limit)) break;
+        mbar_arrive_expect_tx(bar(C::kBarDOFull + st), C::kDOTileBytes);
         for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(sbase + C::kOffDO + st * C::kDOTileBytes + c * C::kBlockBytes, &tmdO,
-                      bar(C::kBarQFull + st), c * 64, q0, bhq);
-        ++issued[st];
+                      bar(C::kBarDOFull + st), c * 64, q0, bhq);
+        ++do_issued[st];
       }
       if (*abort_flag) {
         int no_abort = 0;
         mbar_wait(bar(C::kBarKV), 0, &no_abort, limit);
-        for (int st = 0; st < 2; ++st)
-          if (issued[st]) mbar_wait(bar(C::kBarQFull + st), (issued[st] - 1) & 1, &no_abort, limit);
+        for (int st = 0; st < 2; ++st) {
+          if (q_issued[st]) mbar_wait(bar(C::kBarQFull + st), (q_issued[st] - 1) & 1, &no_abort, limit);
+          if (do_issued[st]) mbar_wait(bar(C::kBarDOFull + st), (do_issued[st] - 1) & 1, &no_abort, limit);
+        }
       }
     }
   } else if (warp == 1) {
@@ -293,10 +309,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (ok) ok = wait_all(C::kBarQ16 + 0, 0);
       if (ok) {
         tc_fence_after_sync();
-        if (lane == 0) {
-          issue_s(0);
-          issue_dp(0);
-        }
+        if (lane == 0) issue_s(0);
+        __syncwarp();
+      }
+      if (ok) ok = wait_all(C::kBarDOFull + 0, 0);
+      if (ok) {
+        tc_fence_after_sync();
+        if (lane == 0) issue_dp(0);
         __syncwarp();
       }
       for (int s = 0; s < total && ok; ++s) {
@@ -334,10 +353,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
           umma_commit(bar(C::kBarDQFull));
           umma_commit(bar(C::kBarQEmpty + st));
+          umma_commit(bar(C::kBarDOEmpty + st));
         }
         __syncwarp();
         if (s + 1 < total) {
-          ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
+          ok = wait_all(C::kBarDOFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          if (ok) ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
           if (!ok) break;
           tc_fence_after_sync();
           if (lane == 0) issue_dp(s + 1);
@@ -351,6 +372,36 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
       }
       __syncwarp();
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ================= fp16 re-encoding of the K and Q tiles ================
+    // K once (rows in [kv_len, n_k) hold caller memory that may be anything,
+    // even NaN, and become zeros: their dS entries are 0, but 0 * NaN would
+    // still poison dQ; rows at or beyond n_k arrive as zeros from the TMA
+    // bounds check), then every Q tile as soon as it lands.
+    const int t64 = static_cast<int>(threadIdx.x) - 64;
+    auto to_f16 = [](uint4 u) {
+      return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+    };
+    bool ok = *abort_flag == 0 && total > 0;
+    if (ok) ok = wait_all(C::kBarKV, 0);
+    if (ok) {
+      uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
+      for (int k = t64; k < C::kKTileBytes / 16; k += 64) {
+        const int krow = (k % (C::kBlockBytes / 16)) / 8;
+        kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarK16));
+    }
+    for (int s = 0; s < total && ok; ++s) {
+      const int st = s & 1;
+      ok = wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1));
+      if (!ok) break;
+      uint4* q = reinterpret_cast<uint4*>(smem + C::kOffQ + st * C::kQTileBytes);
+      for (int k = t64; k < C::kQTileBytes / 16; k += 64) q[k] = to_f16(q[k]);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarQ16 + st));
     }
   } else if (warp >= 4 && warp < 12) {
     // =========================== score warpgroups =======================
@@ -529,92 +580,64 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_arrive(bar(C::kBarDSReady));
     }
   } else if (warp >= 12) {
-    // ====== fp16 re-encoding of K and Q, dQ read-out, dK/dV epilogue ======
+    // =================== dQ read-out and dK/dV epilogue ==================
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
-    const int tid2 = static_cast<int>(threadIdx.x) - 384;
     const uint32_t lane_base = (quad * 32u) << 16;
-    const uint32_t tX = tmem + lane_base + C::kTX;
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
-    auto to_f16 = [](uint4 u) {
-      return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-    };
-    auto convert_q = [&](int st) {
-      uint4* q = reinterpret_cast<uint4*>(smem + C::kOffQ + st * C::kQTileBytes);
-      for (int k = tid2; k < C::kQTileBytes / 16; k += 128) q[k] = to_f16(q[k]);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarQ16 + st));
-    };
     float inv_scale = 1.f;
     if (ok && total > 0) {
-      // K: re-encode as fp16; rows in [kv_len, n_k) hold caller memory that
-      // may be anything (even NaN) and become zeros -- their dS entries are
-      // 0, but 0 * NaN would still poison dQ.  Rows at or beyond n_k arrive
-      // as zeros from the TMA bounds check.
-      ok = wait_all(C::kBarKV, 0);
-      if (ok) {
-        uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
-        for (int k = tid2; k < C::kKTileBytes / 16; k += 128) {
-          const int krow = (k % (C::kBlockBytes / 16)) / 8;
-          kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(C::kBarK16));
-        ok = wait_all(C::kBarQFull + 0, 0);
-      }
-      if (ok) convert_q(0);
-      if (ok) ok = wait_all(C::kBarScale, 0);
+      ok = wait_all(C::kBarScale, 0);
       if (ok) inv_scale = exp2_int(-scale_exponent());
     }
     // dQ read-out: each warp takes its 32 query rows of the tile (in Y),
     // scales them back by 2^-e and stages them as 32 x 32 fp32 boxes in the
-    // 128-byte swizzle pattern (conflict-free stores), warps 0-1 in the dS
-    // buffer and warps 2-3 in the step's Q stage, both consumed once the dQ
-    // product has completed.  Y is released as soon as the tensor-memory
-    // reads are done; one lane then adds the boxes into the fp32 accumulator
-    // with TMA reduce-add and, once the boxes have been read, hands the Q
-    // stage back to the producer and the dS buffer back to the score warps.
-    // Rows past n_q are clipped by the tensor map.
+    // 128-byte swizzle pattern (conflict-free stores).  Y is released as soon
+    // as the tensor-memory reads are done; one lane then adds the boxes into
+    // the fp32 accumulator with TMA reduce-add and, once the boxes have been
+    // read, hands the staging memory back.  Rows past n_q are clipped by the
+    // tensor map.
     const uint32_t tY = tmem + lane_base + C::kTY;
     for (int s = 0; s < total && ok; ++s) {
-      if (s + 1 < total) {
-        const int st1 = (s + 1) & 1;
-        ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
-        if (!ok) break;
-        convert_q(st1);
-      }
       const int bhq = b * p.sh.Hq + step_head(s);
       const int q0 = step_q0(s);
+      const int row0 = q0 + static_cast<int>(quad) * 32;
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      uint8_t* wstage = (quad < 2) ? smem + C::kOffDS + quad * C::kDQWarpStage
-                                   : smem + C::kOffQ + (s & 1) * C::kQTileBytes + (quad - 2) * C::kDQWarpStage;
+      uint8_t* wstage = (!C::kStageInDO || quad < 2)
+                            ? smem + C::kOffDS + quad * C::kDQWarpStage
+                            : smem + C::kOffDO + (s & 1) * C::kDOTileBytes + (quad - 2) * C::kDQWarpStage;
+      for (int rd = 0; rd < C::kDQRounds; ++rd) {
 #pragma unroll
-      for (int bx = 0; bx < C::kDQBoxes; ++bx) {
-        tmem_ld32(tY + bx * C::kDQBoxCols, rr);
-        uint8_t* dst = wstage + bx * C::kDQBoxBytes + lane * 128;
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
+          tmem_ld32(tY + (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, rr);
+          uint8_t* dst = wstage + bx * C::kDQBoxBytes + lane * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(dst + ((c ^ (lane & 7)) * 16)) =
-              make_float4(__uint_as_float(rr[4 * c]) * inv_scale, __uint_as_float(rr[4 * c + 1]) * inv_scale,
-                          __uint_as_float(rr[4 * c + 2]) * inv_scale, __uint_as_float(rr[4 * c + 3]) * inv_scale);
-      }
-      tc_fence_before_sync();
-      mbar_arrive(bar(C::kBarDQFree));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int row0 = q0 + static_cast<int>(quad) * 32;
-        if (row0 < p.sh.n_q) {
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(dst + ((c ^ (lane & 7)) * 16)) =
+                make_float4(__uint_as_float(rr[4 * c]) * inv_scale, __uint_as_float(rr[4 * c + 1]) * inv_scale,
+                            __uint_as_float(rr[4 * c + 2]) * inv_scale, __uint_as_float(rr[4 * c + 3]) * inv_scale);
+        }
+        if (rd + 1 == C::kDQRounds) {
+          tc_fence_before_sync();
+          mbar_arrive(bar(C::kBarDQFree));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.sh.n_q) {
 #pragma unroll
-          for (int bx = 0; bx < C::kDQBoxes; ++bx)
-            tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), bx * C::kDQBoxCols, row0, bhq);
+          for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
+            tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes),
+                              (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, row0, bhq);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
-        mbar_arrive(bar(C::kBarQEmpty + (s & 1)));
+        __syncwarp();
+      }
+      if (lane == 0) {
+        if (C::kStageInDO) mbar_arrive(bar(C::kBarDOEmpty + (s & 1)));
         mbar_arrive(bar(C::kBarDSFree));
       }
       __syncwarp();
