@@ -112,19 +112,20 @@ struct BwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
   // dQ read-out: each read-out warp stages its 32 query rows as boxes of 32
-  // rows x 32 fp32 (4 KB).  With d_h = d_v = 128 all four boxes of a warp
-  // fit at once, warps 0-1 in the dS buffer and warps 2-3 in the step's dO
-  // stage (both consumed once the dQ product is done); otherwise the dS
-  // buffer alone holds two boxes per warp and the read-out takes DH/64
-  // rounds.
+  // rows x 32 fp32 (4 KB).  When d_h = d_v the staging is the step's dO
+  // stage (consumed once the dQ product is done), DV/64 boxes per warp per
+  // round, two rounds, the second round's boxes held in registers meanwhile
+  // so that tensor memory is released at once; the score warps never wait
+  // for it.  Otherwise (d_h = 128, d_v = 64) the staging is the dS buffer,
+  // two boxes per warp per round.
   static constexpr int kDQBoxCols = 32;
   static constexpr int kDQBoxBytes = 32 * kDQBoxCols * 4;
   static constexpr int kDQBoxes = DH / kDQBoxCols;
-  static constexpr bool kStageInDO = (DH == 128 && DV == 128);
-  static constexpr int kDQBoxesPerRound = kStageInDO ? 4 : 2;
+  static constexpr bool kStageInDO = (DH == DV);
+  static constexpr int kDQBoxesPerRound = kStageInDO ? DV / 64 : 2;
   static constexpr int kDQRounds = kDQBoxes / kDQBoxesPerRound;
   static constexpr int kDQWarpStage = kDQBoxesPerRound * kDQBoxBytes;
-  static_assert(kStageInDO ? (2 * kDQWarpStage <= kDSTileBytes && 2 * kDQWarpStage <= kDOTileBytes)
+  static_assert(kStageInDO ? (kDQRounds == 2 && 4 * kDQWarpStage <= kDOTileBytes)
                            : (4 * kDQWarpStage <= kDSTileBytes), "dQ staging");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
@@ -184,9 +185,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_init(bar(C::kBarDOFull + s), 1);
       // MMA commit, plus the four read-out warps when the dO stage is staging.
       mbar_init(bar(C::kBarDOEmpty + s), C::kStageInDO ? 1 + 4 : 1);
-      mbar_init(bar(C::kBarQ16 + s), 64);
+      mbar_init(bar(C::kBarQ16 + s), 128);
     }
-    mbar_init(bar(C::kBarK16), 64);
+    mbar_init(bar(C::kBarK16), 128);
     mbar_init(bar(C::kBarScale), 128);
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
@@ -373,36 +374,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       }
       __syncwarp();
     }
-  } else if (warp == 2 || warp == 3) {
-    // ================= fp16 re-encoding of the K and Q tiles ================
-    // K once (rows in [kv_len, n_k) hold caller memory that may be anything,
-    // even NaN, and become zeros: their dS entries are 0, but 0 * NaN would
-    // still poison dQ; rows at or beyond n_k arrive as zeros from the TMA
-    // bounds check), then every Q tile as soon as it lands.
-    const int t64 = static_cast<int>(threadIdx.x) - 64;
-    auto to_f16 = [](uint4 u) {
-      return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-    };
-    bool ok = *abort_flag == 0 && total > 0;
-    if (ok) ok = wait_all(C::kBarKV, 0);
-    if (ok) {
-      uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
-      for (int k = t64; k < C::kKTileBytes / 16; k += 64) {
-        const int krow = (k % (C::kBlockBytes / 16)) / 8;
-        kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarK16));
-    }
-    for (int s = 0; s < total && ok; ++s) {
-      const int st = s & 1;
-      ok = wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1));
-      if (!ok) break;
-      uint4* q = reinterpret_cast<uint4*>(smem + C::kOffQ + st * C::kQTileBytes);
-      for (int k = t64; k < C::kQTileBytes / 16; k += 64) q[k] = to_f16(q[k]);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarQ16 + st));
-    }
   } else if (warp >= 4 && warp < 12) {
     // =========================== score warpgroups =======================
     // Two warpgroups: h = 0 takes query columns [0, 64), h = 1 [64, 128);
@@ -533,8 +504,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarPReady));
       ok = wait_all(C::kBarDPFull, static_cast<uint32_t>(s & 1));
-      // The dS buffer doubles as dQ staging of the previous step.
-      if (ok && s > 0) ok = wait_all(C::kBarDSFree, static_cast<uint32_t>((s - 1) & 1));
+      // Without d_h = d_v the dS buffer doubles as dQ staging of the previous step.
+      if (!C::kStageInDO && ok && s > 0) ok = wait_all(C::kBarDSFree, static_cast<uint32_t>((s - 1) & 1));
       if (!ok) break;
       tc_fence_after_sync();
       // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into Y (for dK) and
@@ -580,15 +551,45 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_arrive(bar(C::kBarDSReady));
     }
   } else if (warp >= 12) {
-    // =================== dQ read-out and dK/dV epilogue ==================
+    // ===== fp16 re-encoding of K and Q, dQ read-out, dK/dV epilogue ======
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
+    const int tid2 = static_cast<int>(threadIdx.x) - 384;
     const uint32_t lane_base = (quad * 32u) << 16;
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
+    auto to_f16 = [](uint4 u) {
+      return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+    };
+    // Re-encode the Q tile of step s in place as fp16 once it has landed.
+    auto convert_q = [&](int s) -> bool {
+      const int st = s & 1;
+      if (!wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1))) return false;
+      uint4* q = reinterpret_cast<uint4*>(smem + C::kOffQ + st * C::kQTileBytes);
+      for (int k = tid2; k < C::kQTileBytes / 16; k += 128) q[k] = to_f16(q[k]);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarQ16 + st));
+      return true;
+    };
     float inv_scale = 1.f;
     if (ok && total > 0) {
-      ok = wait_all(C::kBarScale, 0);
+      // K once: rows in [kv_len, n_k) hold caller memory that may be anything
+      // (even NaN) and become zeros -- their dS entries are 0, but 0 * NaN
+      // would still poison dQ.  Rows at or beyond n_k arrive as zeros from
+      // the TMA bounds check.  Then the first two Q tiles.
+      ok = wait_all(C::kBarKV, 0);
+      if (ok) {
+        uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
+        for (int k = tid2; k < C::kKTileBytes / 16; k += 128) {
+          const int krow = (k % (C::kBlockBytes / 16)) / 8;
+          kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::kBarK16));
+      }
+      if (ok) ok = convert_q(0);
+      if (ok && total > 1) ok = convert_q(1);
+      if (ok) ok = wait_all(C::kBarScale, 0);
       if (ok) inv_scale = exp2_int(-scale_exponent());
     }
     // dQ read-out: each warp takes its 32 query rows of the tile (in Y),
@@ -597,8 +598,30 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // as the tensor-memory reads are done; one lane then adds the boxes into
     // the fp32 accumulator with TMA reduce-add and, once the boxes have been
     // read, hands the staging memory back.  Rows past n_q are clipped by the
-    // tensor map.
+    // tensor map.  After the read-out, the Q tile two steps ahead is
+    // re-encoded as fp16.
     const uint32_t tY = tmem + lane_base + C::kTY;
+    auto stage_box = [&](uint8_t* dst_box, const uint32_t (&v)[32]) {
+      uint8_t* dst = dst_box + lane * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(dst + ((c ^ (lane & 7)) * 16)) =
+            make_float4(__uint_as_float(v[4 * c]) * inv_scale, __uint_as_float(v[4 * c + 1]) * inv_scale,
+                        __uint_as_float(v[4 * c + 2]) * inv_scale, __uint_as_float(v[4 * c + 3]) * inv_scale);
+    };
+    auto reduce_round = [&](uint8_t* wstage, int first_box, int row0, int bhq) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && row0 < p.sh.n_q) {
+#pragma unroll
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
+          tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), (first_box + bx) * C::kDQBoxCols, row0,
+                            bhq);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      __syncwarp();
+    };
     for (int s = 0; s < total && ok; ++s) {
       const int bhq = b * p.sh.Hq + step_head(s);
       const int q0 = step_q0(s);
@@ -606,41 +629,42 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      uint8_t* wstage = (!C::kStageInDO || quad < 2)
-                            ? smem + C::kOffDS + quad * C::kDQWarpStage
-                            : smem + C::kOffDO + (s & 1) * C::kDOTileBytes + (quad - 2) * C::kDQWarpStage;
-      for (int rd = 0; rd < C::kDQRounds; ++rd) {
+      if constexpr (C::kStageInDO) {
+        uint8_t* wstage = smem + C::kOffDO + (s & 1) * C::kDOTileBytes + quad * C::kDQWarpStage;
+        uint32_t keep[C::kDQBoxesPerRound][32];
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
-          tmem_ld32(tY + (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, rr);
-          uint8_t* dst = wstage + bx * C::kDQBoxBytes + lane * 128;
+          tmem_ld32(tY + bx * C::kDQBoxCols, rr);
+          stage_box(wstage + bx * C::kDQBoxBytes, rr);
+        }
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4*>(dst + ((c ^ (lane & 7)) * 16)) =
-                make_float4(__uint_as_float(rr[4 * c]) * inv_scale, __uint_as_float(rr[4 * c + 1]) * inv_scale,
-                            __uint_as_float(rr[4 * c + 2]) * inv_scale, __uint_as_float(rr[4 * c + 3]) * inv_scale);
-        }
-        if (rd + 1 == C::kDQRounds) {
-          tc_fence_before_sync();
-          mbar_arrive(bar(C::kBarDQFree));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < p.sh.n_q) {
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
+          tmem_ld32(tY + (C::kDQBoxesPerRound + bx) * C::kDQBoxCols, keep[bx]);
+        tc_fence_before_sync();
+        mbar_arrive(bar(C::kBarDQFree));
+        reduce_round(wstage, 0, row0, bhq);
 #pragma unroll
-          for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
-            tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes),
-                              (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, row0, bhq);
-          bulk_commit_group();
-          bulk_wait_group_read0();
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, keep[bx]);
+        reduce_round(wstage, C::kDQBoxesPerRound, row0, bhq);
+        if (lane == 0) mbar_arrive(bar(C::kBarDOEmpty + (s & 1)));
+      } else {
+        uint8_t* wstage = smem + C::kOffDS + quad * C::kDQWarpStage;
+        for (int rd = 0; rd < C::kDQRounds; ++rd) {
+#pragma unroll
+          for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
+            tmem_ld32(tY + (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, rr);
+            stage_box(wstage + bx * C::kDQBoxBytes, rr);
+          }
+          if (rd + 1 == C::kDQRounds) {
+            tc_fence_before_sync();
+            mbar_arrive(bar(C::kBarDQFree));
+          }
+          reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, bhq);
         }
-        __syncwarp();
-      }
-      if (lane == 0) {
-        if (C::kStageInDO) mbar_arrive(bar(C::kBarDOEmpty + (s & 1)));
-        mbar_arrive(bar(C::kBarDSFree));
+        if (lane == 0) mbar_arrive(bar(C::kBarDSFree));
       }
       __syncwarp();
+      if (s + 2 < total) ok = convert_q(s + 2);
     }
     if (lane == 0) bulk_wait_group0();
     if (ok && total > 0) {
