@@ -234,6 +234,11 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
+      for (int s = 0; s < 2 && s < total; ++s) {
+        const int bhq2 = b * p.sh.Hq + step_head(s);
+        for (int c = 0; c < DH / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, step_q0(s), bhq2);
+        for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&tmdO, c * 64, step_q0(s), bhq2);
+      }
       mbar_arrive_expect_tx(bar(C::kBarKV), C::kKTileBytes + C::kVTileBytes);
       for (int c = 0; c < DH / 64; ++c)
         tma_load_3d(sbase + C::kOffK + c * C::kBlockBytes, &tmK, bar(C::kBarKV), c * 64,
@@ -259,6 +264,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tma_load_3d(sbase + C::kOffDO + st * C::kDOTileBytes + c * C::kBlockBytes, &tmdO,
                       bar(C::kBarDOFull + st), c * 64, q0, bhq);
         ++do_issued[st];
+        // Warm L2 with the tiles of step s + 2: their shared-memory stage is
+        // only free once step s has finished, which leaves too little time to
+        // hide a load from HBM.
+        if (s + 2 < total) {
+          const int bhq2 = b * p.sh.Hq + step_head(s + 2);
+          const int q02 = step_q0(s + 2);
+          for (int c = 0; c < DH / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, q02, bhq2);
+          for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&tmdO, c * 64, q02, bhq2);
+        }
       }
       if (*abort_flag) {
         int no_abort = 0;
@@ -331,14 +345,37 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
-        if (s + 1 < total) {
+        // S(s+1) goes in as soon as its fp16 Q tile is ready, but never
+        // holds up dK(s), dQ(s): poll both and take whichever comes first.
+        bool s_next_done = s + 1 >= total;
+        if (!s_next_done) {
           const int st1 = (s + 1) & 1;
-          ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
-          if (ok) ok = wait_all(C::kBarQ16 + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          const uint32_t ph1 = static_cast<uint32_t>(((s + 1) >> 1) & 1);
+          const uint64_t t0 = global_timer_ns();
+          for (;;) {
+            int q_ready = 0, ds_ready = 0;
+            if (lane == 0) {
+              q_ready = mbar_try_wait(bar(C::kBarQFull + st1), ph1) && mbar_try_wait(bar(C::kBarQ16 + st1), ph1);
+              ds_ready = mbar_try_wait(bar(C::kBarDSReady), static_cast<uint32_t>(s & 1));
+            }
+            q_ready = __shfl_sync(0xffffffffu, q_ready, 0);
+            ds_ready = __shfl_sync(0xffffffffu, ds_ready, 0);
+            if (q_ready) {
+              tc_fence_after_sync();
+              if (lane == 0) issue_s(s + 1);
+              __syncwarp();
+              s_next_done = true;
+              break;
+            }
+            if (ds_ready) break;
+            __nanosleep(32);
+            if (*abort_flag || global_timer_ns() - t0 > limit) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
           if (!ok) break;
-          tc_fence_after_sync();
-          if (lane == 0) issue_s(s + 1);
-          __syncwarp();
         }
         ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
         if (!ok) break;
@@ -357,6 +394,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           umma_commit(bar(C::kBarDOEmpty + st));
         }
         __syncwarp();
+        if (!s_next_done) {
+          const int st1 = (s + 1) & 1;
+          ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          if (ok) ok = wait_all(C::kBarQ16 + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after_sync();
+          if (lane == 0) issue_s(s + 1);
+          __syncwarp();
+        }
         if (s + 1 < total) {
           ok = wait_all(C::kBarDOFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
           if (ok) ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
