@@ -72,6 +72,8 @@ struct FwdCfg {
   static constexpr int kSmemUsed = kOffAbort + 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;   // slack for 1024-byte alignment
   static constexpr int kThreads = 384;
+  static constexpr int kRegsLaunch = 168;   // 65536 / 384, rounded down to a multiple of 8
+  static constexpr uint32_t kRegsLow = 56, kRegsHigh = 224;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(2 * 128 + 2 * DV <= 512, "tensor memory budget");
@@ -136,7 +138,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
+  // Registers: the producer/MMA warpgroup gives up most of its share to the
+  // two softmax warpgroups, which hold a whole 128-column score row each
+  // (128 x 56 + 256 x 224 = 384 x 168, the launch allocation).
+  static_assert(128 * C::kRegsLow + 256 * C::kRegsHigh <= C::kThreads * C::kRegsLaunch, "register split");
 
+  if (warp < 4) setmaxnreg_dec<C::kRegsLow>();
   if (warp == 0) {
     // =========================== TMA producer ===========================
     if (lane == 0 && *abort_flag == 0) {
@@ -298,6 +305,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
   } else if (warp >= 4) {
     // ============================== softmax =============================
+    setmaxnreg_inc<C::kRegsHigh>();
     const int t = (warp - 4) / 4;
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
@@ -321,22 +329,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const int lim_rel = lrel64 > kTileN ? kTileN : (lrel64 < 0 ? 0 : static_cast<int>(lrel64));
       const bool masked = __any_sync(0xffffffffu, lim_rel < kTileN);
 
-      // pass 1: row maximum of the visible scores
-      float mx = -INFINITY;
+      // The whole 128-column score row in registers: four loads, one wait.
+      uint32_t sc[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + c * 32, sc[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_wait_ld32(sc[c]);
+      // Scores outside the visible set become -inf, so their weights below
+      // are exp2(-inf) = 0 without a second test.
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            sc[c][k] = (c * 32 + k < lim_rel) ? sc[c][k] : __float_as_uint(-INFINITY);
+      }
+      // Row maximum: four independent chains of three-input maxima.
+      float mxc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tS + c * 32, rr);
-        if (masked) {
+        mxc[c] = fmaxf(__uint_as_float(sc[c][0]), __uint_as_float(sc[c][1]));
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float s = (c * 32 + k < lim_rel) ? __uint_as_float(rr[k]) : -INFINITY;
-            mx = fmaxf(mx, s);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(rr[k]));
-        }
+        for (int k = 2; k < 32; k += 2) mxc[c] = fmax3(mxc[c], __uint_as_float(sc[c][k]), __uint_as_float(sc[c][k + 1]));
       }
+      const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       if (j == 0) {
         m_ref = m_new;
@@ -358,27 +374,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
       }
-      const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // pass 2: P = exp2(S*scale*log2e - m_ref) -> bf16 into tensor memory
+      // P = exp2(S scale log2e - m_ref) -> bf16 pairs into tensor memory
+      // (over the first 64 columns of S, all of which are in registers).
+      float ls[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, lu[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tS + c * 32, rr);
         uint32_t pw[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          float p0 = fast_exp2(fmaf(__uint_as_float(rr[k]), sl2, -m_sub));
-          float p1 = fast_exp2(fmaf(__uint_as_float(rr[k + 1]), sl2, -m_sub));
-          if (masked) {
-            p0 = (c * 32 + k < lim_rel) ? p0 : 0.f;
-            p1 = (c * 32 + k + 1 < lim_rel) ? p1 : 0.f;
-          }
-          l_sum += p0 + p1;
-          pw[k >> 1] = pack_bf16x2(p0, p1);
-          l_used += bf16_lo(pw[k >> 1]) + bf16_hi(pw[k >> 1]);
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sc[c][k]), __uint_as_float(sc[c][k + 1]), sl2, sl2, nm, nm);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          fadd2(ls[c & 1][0], ls[c & 1][1], p0, p1);
+          fadd2(lu[c & 1][0], lu[c & 1][1], bf16_lo(w), bf16_hi(w));
+          pw[k >> 1] = w;
         }
-        tmem_st16(tS + c * 16, pw);
+        tmem_st16_nowait(tS + c * 16, pw);
       }
+      l_sum += (ls[0][0] + ls[0][1]) + (ls[1][0] + ls[1][1]);
+      l_used += (lu[0][0] + lu[0][1]) + (lu[1][0] + lu[1][1]);
+      tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarPReady + t));
     }
