@@ -125,9 +125,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D view [bh][n][d] of a contiguous bf16 tensor, read in 128-row x 64-col
-// boxes with the 128-byte swizzle the tensor-core operand layout expects.
-// Rows beyond n of a head read as zeros (bounds fill), never the next head.
+// 3-D view [bh][n][d] of a contiguous tensor of 2-byte elements (bf16, or
+// the backward's fp16 copy of Q: the copy does not interpret the values),
+// read in 128-row x 64-col boxes with the 128-byte swizzle the tensor-core
+// operand layout expects.  Rows beyond n of a head read as all-zero bits
+// (bounds fill, 0 in either type), never the next head.
 bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -204,11 +206,13 @@ ShapeParams shape_params(const attn_shape* s) {
 int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq * s->n_q; }
 
 // Backward workspace: D [rows] | per-query-tile maxima float2 [B*Hq*nqt] |
-// fp32 dQ accumulator [rows * d_h], each 256-byte aligned.
+// fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h], each
+// 256-byte aligned.
 struct Workspace {
   float* D;
   float2* tilemax;
   float* dQacc;
+  void* Q16;
   size_t bytes;
 };
 
@@ -218,12 +222,14 @@ Workspace workspace_layout(const attn_shape* s, void* base) {
   const size_t tiles = static_cast<size_t>(s->B) * s->Hq * nqt;
   const size_t off_t = round256(rows * sizeof(float));
   const size_t off_a = off_t + round256(tiles * sizeof(float2));
+  const size_t off_q = off_a + round256(rows * static_cast<size_t>(s->d_h) * sizeof(float));
   Workspace w;
   uint8_t* b = static_cast<uint8_t*>(base);
   w.D = reinterpret_cast<float*>(b);
   w.tilemax = reinterpret_cast<float2*>(b + off_t);
   w.dQacc = reinterpret_cast<float*>(b + off_a);
-  w.bytes = off_a + round256(rows * static_cast<size_t>(s->d_h) * sizeof(float));
+  w.Q16 = b + off_q;
+  w.bytes = off_q + round256(rows * static_cast<size_t>(s->d_h) * 2);
   return w;
 }
 
@@ -353,11 +359,11 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo, const void* dO, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O, const void* O_lo, const void* dO,
+                        void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
-  rc = check_ptrs({O, dO});
+  rc = check_ptrs({Q, O, dO});
   if (rc) return rc;
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   rc = check_workspace(shape, workspace, workspace_bytes);
@@ -367,14 +373,14 @@ int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo
   if (rc) return rc;
   const Workspace w = workspace_layout(shape, workspace);
   const cudaError_t e = launch_attn_bwd_preprocess(static_cast<int64_t>(shape->B) * shape->Hq, shape->n_q,
-                                                   shape->d_v, shape->d_h, O, O_lo, dO, w.D, w.tilemax, w.dQacc,
-                                                   static_cast<cudaStream_t>(stream));
+                                                   shape->d_v, shape->d_h, Q, O, O_lo, dO, w.D, w.tilemax, w.dQacc,
+                                                   w.Q16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-                  const void* V, const void* dO, const float* LSE, void* workspace, size_t workspace_bytes,
-                  void* dK, void* dV, void* stream) {
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, const void* K, const void* V,
+                  const void* dO, const float* LSE, void* workspace, size_t workspace_bytes, void* dK, void* dV,
+                  void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   BwdParams p;
@@ -382,7 +388,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
-  rc = check_ptrs({Q, K, V, dO, LSE, dK, dV});
+  rc = check_ptrs({K, V, dO, LSE, dK, dV});
   if (rc) return rc;
   rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
@@ -393,7 +399,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   CUtensorMap tq, tk, tv, tdo, tdq;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
-  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
+  if (!make_tmap(&tq, w.Q16, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
       !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, dO, shape->d_v, shape->n_q, bhq) ||
       !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
     return ATTN_ERR_CUDA;
@@ -448,9 +454,9 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
-  rc = attn_bwd_preprocess(shape, O, O_lo, dO, workspace, workspace_bytes, stream);
+  rc = attn_bwd_preprocess(shape, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
   if (rc) return rc;
-  rc = attn_bwd_main(shape, mask, scale, Q, K, V, dO, LSE, workspace, workspace_bytes, dK, dV, stream);
+  rc = attn_bwd_main(shape, mask, scale, K, V, dO, LSE, workspace, workspace_bytes, dK, dV, stream);
   if (rc) return rc;
   return attn_bwd_finalize(shape, scale, workspace, workspace_bytes, dQ, stream);
 }

@@ -13,7 +13,8 @@
 //
 // Three kernels:
 //   preprocess  D_i = sum_l dO_il O_il (equal to c_i of A.10.7 because
-//               O_i = sum_j A_ij v_j), and zeroes the fp32 dQ accumulator.
+//               O_i = sum_j A_ij v_j), zeroes the fp32 dQ accumulator and
+//               writes Q re-encoded as fp16 (the main kernel's operand).
 //               O is taken as the bf16 output plus, when given, the
 //               forward's bf16 rounding residual, so D is not limited by the
 //               bf16 rounding of O.  Per 128-row query tile it also records
@@ -22,20 +23,23 @@
 //               the query heads of its group and the query tiles that can
 //               see its keys, keeps dK and dV in tensor memory for the whole
 //               loop, and adds each tile's dS K product into the fp32 dQ
-//               accumulator with vector atomics.
+//               accumulator with TMA reduce-add.
 //   finalize    dQ = scale * accumulator, rounded to bf16.
 //
 // Main-kernel warp roles (512 threads):
-//   warp 0      TMA producer: the K and V tile once, then Q and dO tiles
-//               of every step into a two-stage ring.
+//   warp 0      TMA producer: the K and V tile once, then the fp16 Q and
+//               the dO tile of every step into two-stage rings.
 //   warp 1      MMA issuer (lane 0 issues).
 //   warps 4-11  two "score" warpgroups, one per 64-query half of the step,
 //               thread = key row = TMEM lane:
 //               P^T = exp2(S^T scale log2e - LSE log2e) and
 //               dS^T = P^T (dP^T - D), written back to tensor memory and
 //               dS to shared memory for the dQ product.
-//   warps 12-15 converts K and each Q tile to fp16 in shared memory, reads
-//               dQ out (atomics) and writes the final dK, dV.
+//   warps 12-15 converts K to fp16 in shared memory, reads dQ out of tensor
+//               memory into the accumulator and writes the final dK, dV.
+// The producer/MMA warpgroup hands most of its registers to the others
+// (setmaxnreg), so a score thread holds 64 scores and a read-out thread a
+// whole 128-column dQ row at once.
 //
 // Precision of the dS products.  dQ_i = scale sum_j dS_ij k_j sums terms
 // that largely cancel when a softmax row is sharply peaked, so rounding dS
@@ -47,7 +51,8 @@
 // from the fp16 subnormal range.  The scale is exact and undone exactly when
 // dQ is read out and when dK is written.  Q and K are re-encoded as fp16 in
 // shared memory (the MMA takes one type for both operands; the conversion
-// is exact for |x| up to 65504 and saturates beyond).  The weights P used
+// is exact for |x| up to 65504 and saturates beyond; Q arrives re-encoded
+// from the preprocess kernel, K is converted once per CTA).  The weights P used
 // inside dS are kept as fp16 too; dP = dO V^T and dV = P^T dO stay bf16.
 // Per step (query tile of 128 rows) the products are
 //   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dK += dS^T Q,
@@ -90,8 +95,7 @@ struct BwdCfg {
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
   static constexpr int kBarDOFull = kBarQEmpty + 2;   // [2]
   static constexpr int kBarDOEmpty = kBarDOFull + 2;  // [2]
-  static constexpr int kBarQ16 = kBarDOEmpty + 2;     // [2] Q tile re-encoded as fp16
-  static constexpr int kBarK16 = kBarQ16 + 2;         // K tile re-encoded as fp16
+  static constexpr int kBarK16 = kBarDOEmpty + 2;     // K tile re-encoded as fp16
   static constexpr int kBarScale = kBarK16 + 1;       // dS scale bound reduced
   static constexpr int kBarSFull = kBarScale + 1;
   static constexpr int kBarDPFull = kBarSFull + 1;
@@ -109,6 +113,11 @@ struct BwdCfg {
   static constexpr int kSmemUsed = kOffAbort + 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;
   static constexpr int kThreads = 512;
+  // Registers per thread: 128 at launch (65536 / 512); the producer/MMA
+  // warpgroup gives most of its share to the score and read-out warpgroups
+  // (128 x 80 + 256 x 136 + 128 x 144 = 63488 <= 512 x 128).
+  static constexpr uint32_t kRegsLow = 80, kRegsScore = 136, kRegsAux = 144;
+  static_assert(128 * kRegsLow + 256 * kRegsScore + 128 * kRegsAux <= 512 * 128, "register split");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
   // dQ read-out: each read-out warp stages its 32 query rows as boxes of 32
@@ -185,7 +194,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_init(bar(C::kBarDOFull + s), 1);
       // MMA commit, plus the four read-out warps when the dO stage is staging.
       mbar_init(bar(C::kBarDOEmpty + s), C::kStageInDO ? 1 + 4 : 1);
-      mbar_init(bar(C::kBarQ16 + s), 128);
     }
     mbar_init(bar(C::kBarK16), 128);
     mbar_init(bar(C::kBarScale), 128);
@@ -227,6 +235,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     return ds_scale_exponent(mdo * mv + md);
   };
 
+  if (warp < 4) setmaxnreg_dec<C::kRegsLow>();
   if (warp == 0) {
     // =========================== TMA producer ===========================
     if (lane == 0 && *abort_flag == 0 && total > 0) {
@@ -321,7 +330,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       // columns [0,32) and for queries [64,128) in columns [64,96) of X and Y.
       auto half_col = [](int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); };
       if (ok) ok = wait_all(C::kBarQFull + 0, 0);
-      if (ok) ok = wait_all(C::kBarQ16 + 0, 0);
       if (ok) {
         tc_fence_after_sync();
         if (lane == 0) issue_s(0);
@@ -345,8 +353,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
-        // S(s+1) goes in as soon as its fp16 Q tile is ready, but never
-        // holds up dK(s), dQ(s): poll both and take whichever comes first.
+        // S(s+1) goes in as soon as its Q tile has landed, but never holds
+        // up dK(s), dQ(s): poll both and take whichever comes first.
         bool s_next_done = s + 1 >= total;
         if (!s_next_done) {
           const int st1 = (s + 1) & 1;
@@ -355,7 +363,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           for (;;) {
             int q_ready = 0, ds_ready = 0;
             if (lane == 0) {
-              q_ready = mbar_try_wait(bar(C::kBarQFull + st1), ph1) && mbar_try_wait(bar(C::kBarQ16 + st1), ph1);
+              q_ready = mbar_try_wait(bar(C::kBarQFull + st1), ph1);
               ds_ready = mbar_try_wait(bar(C::kBarDSReady), static_cast<uint32_t>(s & 1));
             }
             q_ready = __shfl_sync(0xffffffffu, q_ready, 0);
@@ -397,7 +405,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (!s_next_done) {
           const int st1 = (s + 1) & 1;
           ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
-          if (ok) ok = wait_all(C::kBarQ16 + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
           if (!ok) break;
           tc_fence_after_sync();
           if (lane == 0) issue_s(s + 1);
@@ -424,6 +431,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // =========================== score warpgroups =======================
     // Two warpgroups: h = 0 takes query columns [0, 64), h = 1 [64, 128);
     // in both, thread = key row = TMEM lane.
+    setmaxnreg_inc<C::kRegsScore>();
     const int h = static_cast<int>(warp - 4) / 4;
     const uint32_t quad = warp & 3;
     const int jj = static_cast<int>(quad * 32 + lane);
@@ -481,15 +489,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ds_scale = exp2_int(scale_exponent());
     }
     uint32_t pw[32];
-    // This thread's LSE and D entry (query q0 + 64h + tid, for tid < 64) of
-    // a step, loaded one step ahead so the global latency is off the
-    // critical path.
-    auto load_row_terms = [&](int s, float& lse2, float& dd) {
+    // This thread's -LSE log2(e) and -D entries (query q0 + 64h + tid, for
+    // tid < 64) of a step, loaded one step ahead so the global latency is
+    // off the critical path.  Both are kept negated so that one paired
+    // fused multiply-add forms x log2(e) scale - LSE log2(e) and
+    // dP 2^e - D 2^e.
+    auto load_row_terms = [&](int s, float& nlse2, float& nd) {
       const int64_t i = static_cast<int64_t>(step_q0(s)) + 64 * h + tid;
       const int64_t r = static_cast<int64_t>(b * p.sh.Hq + step_head(s)) * p.sh.n_q + i;
       const bool in = tid < 64 && i < p.sh.n_q;
-      lse2 = in ? p.LSE[r] * kLog2e : INFINITY;
-      dd = in ? p.D[r] : 0.f;
+      nlse2 = in ? -p.LSE[r] * kLog2e : -INFINITY;
+      nd = in ? -p.D[r] : 0.f;
     };
     float lse_next = 0.f, d_next = 0.f;
     if (ok) load_row_terms(0, lse_next, d_next);
@@ -517,33 +527,44 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarSFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      // P pass over this half's four 16-column chunks; the next chunk's load
-      // is in flight while this one is computed.  P^T (bf16) goes into X
-      // behind the columns already read; P (fp16) stays in registers.
+      // P pass: this half's 64 scores in registers (two loads, one wait).
+      // P^T (bf16) goes into X over the columns already read; P (fp16)
+      // stays in registers for the dS pass.
       {
-        uint32_t ra[16], rb[16];
-        tmem_ld16_nowait(tX + 64 * h, ra);
-        tmem_wait_ld16(ra);
+        uint32_t sa[32], sb[32];
+        tmem_ld32_nowait(tX + 64 * h, sa);
+        tmem_ld32_nowait(tX + 64 * h + 32, sb);
+        tmem_wait_ld32(sa);
+        tmem_wait_ld32(sb);
 #pragma unroll
         for (int cq = 0; cq < 4; ++cq) {
-          uint32_t (&cur)[16] = (cq & 1) ? rb : ra;
-          uint32_t (&nxt)[16] = (cq & 1) ? ra : rb;
-          if (cq + 1 < 4) tmem_ld16_nowait(tX + 64 * h + (cq + 1) * 16, nxt);
+          float nl[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(lse_s + 64 * h + cq * 16 + 4 * q);
+            nl[4 * q] = v.x;
+            nl[4 * q + 1] = v.y;
+            nl[4 * q + 2] = v.z;
+            nl[4 * q + 3] = v.w;
+          }
           uint32_t w[8];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
             const int c = 64 * h + cq * 16 + k;
-            float p0 = fast_exp2(fmaf(__uint_as_float(cur[k]), sl2, -lse_s[c]));
-            float p1 = fast_exp2(fmaf(__uint_as_float(cur[k + 1]), sl2, -lse_s[c + 1]));
+            const int r = (cq & 1) * 16 + k;
+            const float s0 = __uint_as_float(cq < 2 ? sa[r] : sb[r]);
+            const float s1 = __uint_as_float(cq < 2 ? sa[r + 1] : sb[r + 1]);
+            float x0, x1;
+            ffma2(x0, x1, s0, s1, sl2, sl2, nl[k], nl[k + 1]);
             if (need_mask) {
-              p0 = (!row_masked && c >= cmin) ? p0 : 0.f;
-              p1 = (!row_masked && c + 1 >= cmin) ? p1 : 0.f;
+              x0 = (!row_masked && c >= cmin) ? x0 : -INFINITY;
+              x1 = (!row_masked && c + 1 >= cmin) ? x1 : -INFINITY;
             }
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             w[k >> 1] = pack_bf16x2(p0, p1);
             pw[cq * 8 + (k >> 1)] = pack_f16x2(p0, p1);
           }
           tmem_st8_nowait(tX + 64 * h + cq * 8, w);
-          if (cq + 1 < 4) tmem_wait_ld16(nxt);
         }
         tmem_wait_st();
       }
@@ -555,23 +576,35 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (!ok) break;
       tc_fence_after_sync();
       // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into Y (for dK) and
-      // into this half's block of the dS buffer (for dQ); dd_s holds D 2^e.
+      // into this half's block of the dS buffer (for dQ); dd_s holds -D 2^e.
       {
-        uint32_t ra[16], rb[16];
-        tmem_ld16_nowait(tY + 64 * h, ra);
-        tmem_wait_ld16(ra);
+        uint32_t da[32], db[32];
+        tmem_ld32_nowait(tY + 64 * h, da);
+        tmem_ld32_nowait(tY + 64 * h + 32, db);
+        tmem_wait_ld32(da);
+        tmem_wait_ld32(db);
 #pragma unroll
         for (int cq = 0; cq < 4; ++cq) {
-          uint32_t (&cur)[16] = (cq & 1) ? rb : ra;
-          uint32_t (&nxt)[16] = (cq & 1) ? ra : rb;
-          if (cq + 1 < 4) tmem_ld16_nowait(tY + 64 * h + (cq + 1) * 16, nxt);
+          float nd[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(dd_s + 64 * h + cq * 16 + 4 * q);
+            nd[4 * q] = v.x;
+            nd[4 * q + 1] = v.y;
+            nd[4 * q + 2] = v.z;
+            nd[4 * q + 3] = v.w;
+          }
           uint32_t w[8];
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
             const int c = 64 * h + cq * 16 + k;
+            const int r = (cq & 1) * 16 + k;
+            const float g0 = __uint_as_float(cq < 2 ? da[r] : db[r]);
+            const float g1 = __uint_as_float(cq < 2 ? da[r + 1] : db[r + 1]);
+            float t0, t1, d0, d1;
+            ffma2(t0, t1, g0, g1, ds_scale, ds_scale, nd[k], nd[k + 1]);
             const uint32_t pp = pw[cq * 8 + (k >> 1)];
-            float d0 = f16_lo(pp) * fmaf(__uint_as_float(cur[k]), ds_scale, -dd_s[c]);
-            float d1 = f16_hi(pp) * fmaf(__uint_as_float(cur[k + 1]), ds_scale, -dd_s[c + 1]);
+            fmul2(d0, d1, f16_lo(pp), f16_hi(pp), t0, t1);
             if (need_mask) {
               d0 = (!row_masked && c >= cmin) ? d0 : 0.f;
               d1 = (!row_masked && c + 1 >= cmin) ? d1 : 0.f;
@@ -588,7 +621,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (jj & 7)) * 16)) =
                 make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
-          if (cq + 1 < 4) tmem_wait_ld16(nxt);
         }
         tmem_wait_st();
       }
@@ -597,7 +629,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_arrive(bar(C::kBarDSReady));
     }
   } else if (warp >= 12) {
-    // ===== fp16 re-encoding of K and Q, dQ read-out, dK/dV epilogue ======
+    // ======== fp16 re-encoding of K, dQ read-out, dK/dV epilogue ========
+    setmaxnreg_inc<C::kRegsAux>();
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
     const int tid2 = static_cast<int>(threadIdx.x) - 384;
@@ -607,22 +640,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     auto to_f16 = [](uint4 u) {
       return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
     };
-    // Re-encode the Q tile of step s in place as fp16 once it has landed.
-    auto convert_q = [&](int s) -> bool {
-      const int st = s & 1;
-      if (!wait_all(C::kBarQFull + st, static_cast<uint32_t>((s >> 1) & 1))) return false;
-      uint4* q = reinterpret_cast<uint4*>(smem + C::kOffQ + st * C::kQTileBytes);
-      for (int k = tid2; k < C::kQTileBytes / 16; k += 128) q[k] = to_f16(q[k]);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarQ16 + st));
-      return true;
-    };
     float inv_scale = 1.f;
     if (ok && total > 0) {
       // K once: rows in [kv_len, n_k) hold caller memory that may be anything
       // (even NaN) and become zeros -- their dS entries are 0, but 0 * NaN
       // would still poison dQ.  Rows at or beyond n_k arrive as zeros from
-      // the TMA bounds check.  Then the first two Q tiles.
+      // the TMA bounds check.
       ok = wait_all(C::kBarKV, 0);
       if (ok) {
         uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
@@ -633,19 +656,16 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarK16));
       }
-      if (ok) ok = convert_q(0);
-      if (ok && total > 1) ok = convert_q(1);
       if (ok) ok = wait_all(C::kBarScale, 0);
       if (ok) inv_scale = exp2_int(-scale_exponent());
     }
-    // dQ read-out: each warp takes its 32 query rows of the tile (in Y),
-    // scales them back by 2^-e and stages them as 32 x 32 fp32 boxes in the
-    // 128-byte swizzle pattern (conflict-free stores).  Y is released as soon
-    // as the tensor-memory reads are done; one lane then adds the boxes into
-    // the fp32 accumulator with TMA reduce-add and, once the boxes have been
-    // read, hands the staging memory back.  Rows past n_q are clipped by the
-    // tensor map.  After the read-out, the Q tile two steps ahead is
-    // re-encoded as fp16.
+    // dQ read-out: each warp takes its 32 query rows of the tile (in Y) into
+    // registers at once (one wait) and releases Y; it then scales them back
+    // by 2^-e and stages them as 32 x 32 fp32 boxes in the 128-byte swizzle
+    // pattern (conflict-free stores), and one lane adds the boxes into the
+    // fp32 accumulator with TMA reduce-add, a round at a time, the staging
+    // memory being reused once a round's boxes have been read.  Rows past
+    // n_q are clipped by the tensor map.
     const uint32_t tY = tmem + lane_base + C::kTY;
     auto stage_box = [&](uint8_t* dst_box, const uint32_t (&v)[32]) {
       uint8_t* dst = dst_box + lane * 128;
@@ -675,42 +695,24 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      if constexpr (C::kStageInDO) {
-        uint8_t* wstage = smem + C::kOffDO + (s & 1) * C::kDOTileBytes + quad * C::kDQWarpStage;
-        uint32_t keep[C::kDQBoxesPerRound][32];
+      uint32_t v[C::kDQBoxes][32];
 #pragma unroll
-        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
-          tmem_ld32(tY + bx * C::kDQBoxCols, rr);
-          stage_box(wstage + bx * C::kDQBoxBytes, rr);
-        }
+      for (int bx = 0; bx < C::kDQBoxes; ++bx) tmem_ld32_nowait(tY + bx * C::kDQBoxCols, v[bx]);
+#pragma unroll
+      for (int bx = 0; bx < C::kDQBoxes; ++bx) tmem_wait_ld32(v[bx]);
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::kBarDQFree));
+      uint8_t* wstage = C::kStageInDO ? smem + C::kOffDO + (s & 1) * C::kDOTileBytes + quad * C::kDQWarpStage
+                                      : smem + C::kOffDS + quad * C::kDQWarpStage;
+#pragma unroll
+      for (int rd = 0; rd < C::kDQRounds; ++rd) {
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
-          tmem_ld32(tY + (C::kDQBoxesPerRound + bx) * C::kDQBoxCols, keep[bx]);
-        tc_fence_before_sync();
-        mbar_arrive(bar(C::kBarDQFree));
-        reduce_round(wstage, 0, row0, bhq);
-#pragma unroll
-        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, keep[bx]);
-        reduce_round(wstage, C::kDQBoxesPerRound, row0, bhq);
-        if (lane == 0) mbar_arrive(bar(C::kBarDOEmpty + (s & 1)));
-      } else {
-        uint8_t* wstage = smem + C::kOffDS + quad * C::kDQWarpStage;
-        for (int rd = 0; rd < C::kDQRounds; ++rd) {
-#pragma unroll
-          for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) {
-            tmem_ld32(tY + (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, rr);
-            stage_box(wstage + bx * C::kDQBoxBytes, rr);
-          }
-          if (rd + 1 == C::kDQRounds) {
-            tc_fence_before_sync();
-            mbar_arrive(bar(C::kBarDQFree));
-          }
-          reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, bhq);
-        }
-        if (lane == 0) mbar_arrive(bar(C::kBarDSFree));
+          stage_box(wstage + bx * C::kDQBoxBytes, v[rd * C::kDQBoxesPerRound + bx]);
+        reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, bhq);
       }
+      if (lane == 0) mbar_arrive(bar(C::kStageInDO ? C::kBarDOEmpty + (s & 1) : C::kBarDSFree));
       __syncwarp();
-      if (s + 2 < total) ok = convert_q(s + 2);
     }
     if (lane == 0) bulk_wait_group0();
     if (ok && total > 0) {
@@ -774,12 +776,14 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 // per row:
 //   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
 //   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
-// and the tile's rows of the fp32 dQ accumulator are zeroed.
+// the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
+// are re-encoded as fp16 for the main kernel (exact for |q| <= 65504,
+// saturating beyond).
 template <int DV, int DH>
 __global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
-                           const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
-                           float4* __restrict__ dQacc) {
+attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const uint4* __restrict__ O,
+                           const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
+                           float2* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16) {
   constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
   __shared__ float red[2][8];
   const int64_t bh = blockIdx.x;
@@ -831,8 +835,15 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ O, const 
   }
   const int64_t rows_here = (n_q - static_cast<int64_t>(qt) * kTileM) < kTileM ? (n_q - static_cast<int64_t>(qt) * kTileM)
                                                                                 : kTileM;
-  float4* acc_tile = dQacc + (bh * n_q + static_cast<int64_t>(qt) * kTileM) * (DH / 4);
+  const int64_t tile_row0 = bh * n_q + static_cast<int64_t>(qt) * kTileM;
+  float4* acc_tile = dQacc + tile_row0 * (DH / 4);
   for (int64_t k = threadIdx.x; k < rows_here * (DH / 4); k += 256) acc_tile[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint4* q_tile = Q + tile_row0 * (DH / 8);
+  uint4* q16_tile = Q16 + tile_row0 * (DH / 8);
+  for (int64_t k = threadIdx.x; k < rows_here * (DH / 8); k += 256) {
+    const uint4 u = q_tile[k];
+    q16_tile[k] = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+  }
 }
 
 // dQ = scale * acc, eight elements per thread per iteration.
@@ -868,12 +879,12 @@ int grid_for(int64_t work_threads) {
 }
 
 template <int DV, int DH>
-void launch_pre_t(int64_t bhq, int n_q, int nqt, const void* O, const void* O_lo, const void* dO, float* D,
-                  float2* tilemax, float* dQacc, cudaStream_t stream) {
+void launch_pre_t(int64_t bhq, int n_q, int nqt, const void* Q, const void* O, const void* O_lo, const void* dO,
+                  float* D, float2* tilemax, float* dQacc, void* Q16, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(bhq), static_cast<unsigned>(nqt));
   attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(
-      n_q, nqt, static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo), static_cast<const uint4*>(dO), D,
-      tilemax, reinterpret_cast<float4*>(dQacc));
+      n_q, nqt, static_cast<const uint4*>(Q), static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo),
+      static_cast<const uint4*>(dO), D, tilemax, reinterpret_cast<float4*>(dQacc), static_cast<uint4*>(Q16));
 }
 
 }  // namespace
@@ -887,16 +898,16 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* O, const void* O_lo,
-                                       const void* dO, float* D, float2* tilemax, float* dQacc,
-                                       cudaStream_t stream) {
+cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* Q, const void* O,
+                                       const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
+                                       void* Q16, cudaStream_t stream) {
   const int nqt = (n_q + kTileM - 1) / kTileM;
   if (dv == 128 && dh == 128)
-    launch_pre_t<128, 128>(bhq, n_q, nqt, O, O_lo, dO, D, tilemax, dQacc, stream);
+    launch_pre_t<128, 128>(bhq, n_q, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
   else if (dv == 64 && dh == 64)
-    launch_pre_t<64, 64>(bhq, n_q, nqt, O, O_lo, dO, D, tilemax, dQacc, stream);
+    launch_pre_t<64, 64>(bhq, n_q, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
   else if (dv == 64 && dh == 128)
-    launch_pre_t<64, 128>(bhq, n_q, nqt, O, O_lo, dO, D, tilemax, dQacc, stream);
+    launch_pre_t<64, 128>(bhq, n_q, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -108,9 +108,9 @@ cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtens
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* O, const void* O_lo,
-                                       const void* dO, float* D, float2* tilemax, float* dQacc,
-                                       cudaStream_t stream);
+cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* Q, const void* O,
+                                       const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
+                                       void* Q16, cudaStream_t stream);
 cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
                                      cudaStream_t stream);
 

@@ -76,7 +76,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 // Paired fp32 arithmetic (one instruction for two lanes of work, each
-// rounded to nearest like its scalar form): d = a * b + c and d = a + b.
+// rounded to nearest like its scalar form): d = a * b + c, d = a + b and
+// d = a * b.
 __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
                                       float c1) {
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
@@ -91,6 +92,14 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) 
       "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
+}
+
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // Per-warpgroup register budget (every warp of the warpgroup executes the

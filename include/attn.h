@@ -61,7 +61,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -117,9 +117,9 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
              void* O, float* LSE, void* O_lo, void* stream);
 
 /* Bytes of device workspace the backward needs (attn_bwd and its three
- * stages): row terms D, per-128-row-tile bounds used to scale dS, and an
- * fp32 dQ accumulator, about B*Hq*n_q*(4*d_h + 4) bytes.  The layout is
- * private to the library.  Returns 0 for an invalid shape. */
+ * stages): row terms D, per-128-row-tile bounds used to scale dS, an fp32
+ * dQ accumulator and an fp16 copy of Q, about B*Hq*n_q*(6*d_h + 4) bytes.
+ * The layout is private to the library.  Returns 0 for an invalid shape. */
 size_t attn_bwd_workspace_bytes(const attn_shape* shape);
 
 /* Backward pass (A.10.5-A.10.9).  Q, K, V, O, LSE must be those of the
@@ -143,17 +143,19 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Stage 1 of the backward: D_i = sum_l dO_il (O_il + O_lo_il) (= c_i of
- * A.10.7; O_lo may be NULL), per-tile bounds max ||dO_i|| and max |D_i|, and
- * a zeroed dQ accumulator, all in `workspace`. */
-int attn_bwd_preprocess(const attn_shape* shape, const void* O, const void* O_lo,
-                        const void* dO, void* workspace, size_t workspace_bytes,
-                        void* stream);
+ * A.10.7; O_lo may be NULL), per-tile bounds max ||dO_i|| and max |D_i|, a
+ * zeroed dQ accumulator and Q re-encoded as fp16 (see attn_bwd), all in
+ * `workspace`.  Q is the forward's bf16 query tensor. */
+int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O,
+                        const void* O_lo, const void* dO, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
-/* Stage 2: the key-tile-stationary main kernel.  Recomputes A from Q, K and
- * LSE, writes dK (scaled) and dV (bf16) and adds the dS K products into the
- * workspace's fp32 dQ accumulator (zeroed by stage 1). */
+/* Stage 2: the key-tile-stationary main kernel.  Recomputes A from the
+ * workspace's fp16 copy of Q (written by stage 1), K and LSE, writes dK
+ * (scaled) and dV (bf16) and adds the dS K products into the workspace's
+ * fp32 dQ accumulator (zeroed by stage 1). */
 int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale,
-                  const void* Q, const void* K, const void* V, const void* dO,
+                  const void* K, const void* V, const void* dO,
                   const float* LSE, void* workspace, size_t workspace_bytes,
                   void* dK, void* dV, void* stream);
 
