@@ -305,7 +305,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       auto qB = [&](int s) { return sbase + C::kOffQ + (s & 1) * C::kQTileBytes; };
       auto doB = [&](int s) { return sbase + C::kOffDO + (s & 1) * C::kDOTileBytes; };
       auto issue_s = [&](int s) {   // S^T = K Q^T -> X
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
           umma_ss(tmem + C::kTX, sw128_desc(kA + off, 16, 1024), sw128_desc(qB(s) + off, 16, 1024), kIdS,
@@ -314,7 +314,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         umma_commit(bar(C::kBarSFull));
       };
       auto issue_dp = [&](int s) {  // dP^T = V dO^T -> Y
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
           umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB(s) + off, 16, 1024), kIdDP,
@@ -322,6 +322,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         umma_commit(bar(C::kBarDPFull));
       };
+      // The MMA issue loops are not unrolled: issue is paced by the tensor
+      // pipe, and the smaller code leaves the instruction cache to the score
+      // and read-out warps.
       // Order per step s:  dV(s) | S(s+1) -> X | dK(s), dQ(s) -> Y | [dQ read out] dP(s+1) -> Y.
       // S(s+1) only needs X, which dV(s) has finished reading (MMAs run in
       // issue order), so the scores of step s+1 are ready when the score
@@ -347,7 +350,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (!ok) break;
         tc_fence_after_sync();
         if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ts(tmem + C::kTdV, tmem + C::kTX + half_col(kk),
                     sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
@@ -389,11 +392,11 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (!ok) break;
         tc_fence_after_sync();
         if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ts(tmem + C::kTdK, tmem + C::kTY + half_col(kk),
                     sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
+#pragma unroll 1
           for (int kk = 0; kk < kTileN / 16; ++kk)
             umma_ss(tmem + C::kTY, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
                     sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
