@@ -55,13 +55,14 @@
 // from the preprocess kernel, K is converted once per CTA).  The weights P used
 // inside dS are kept as fp16 too; dP = dO V^T and dV = P^T dO stay bf16.
 // Per step (query tile of 128 rows) the products are
-//   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dK += dS^T Q,
-//   dQ = dS K -> Y,
+//   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dQ = dS K -> Y,
+//   dK += dS^T Q,
 // where tensor memory holds X [0,128), Y [128,256), dK [256, 256+DH) and
-// dV [256+DH, 256+DH+DV).  P^T and dS^T overwrite the first 64 columns of X
-// and Y once their fp32 inputs are consumed; dQ reuses Y after the dK
-// product has read dS^T (MMAs run in issue order), which leaves X free for
-// the next step's scores while dQ is read out.
+// dV [256+DH, 256+DH+DV).  P^T (bf16) overwrites the first 64 columns of X
+// once the scores are consumed; dS goes to shared memory only, where it
+// serves both dQ and dK.  dQ reuses Y once the score warps have read dP^T
+// out of it, and is read out while dK runs, which leaves X free for the
+// next step's scores.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -106,7 +107,8 @@ struct BwdCfg {
   static constexpr int kBarDKDV = kBarDQFree + 1;
   static constexpr int kBarLse = kBarDKDV + 1;        // score warps loaded LSE, D
   static constexpr int kBarDSFree = kBarLse + 1;     // dS buffer no longer read by the dQ reduce
-  static constexpr int kBarDrain = kBarDSFree + 1;
+  static constexpr int kBarDSRead = kBarDSFree + 1;  // dK product has read the dS buffer
+  static constexpr int kBarDrain = kBarDSRead + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -206,6 +208,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDKDV), 1);
     mbar_init(bar(C::kBarLse), 256);
     mbar_init(bar(C::kBarDSFree), 4);
+    mbar_init(bar(C::kBarDSRead), 1);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
@@ -294,13 +297,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    if (*abort_flag == 0 && total > 0) {
+    // Lane 0 alone waits and issues (an MMA issue holds the thread for
+    // about as long as the MMA takes, so the issuer must never stall on a
+    // warp-wide vote); the other lanes go straight to the teardown.
+    if (lane == 0 && *abort_flag == 0 && total > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(128, 128, false, false);    // S^T = K Q^T (fp16)
       constexpr uint32_t kIdDP = idesc_bf16_f32(128, 128, false, false);  // dP^T = V dO^T
       constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV += P^T dO
       constexpr uint32_t kIdDK = idesc_f16_f32(128, DH, false, true);     // dK += dS^T Q
       constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
-      bool ok = wait_all(C::kBarK16, 0);
+      auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
+      bool ok = wait1(C::kBarK16, 0);
       const uint32_t kA = sbase + C::kOffK, vA = sbase + C::kOffV, dsA = sbase + C::kOffDS;
       auto qB = [&](int s) { return sbase + C::kOffQ + (s & 1) * C::kQTileBytes; };
       auto doB = [&](int s) { return sbase + C::kOffDO + (s & 1) * C::kDOTileBytes; };
@@ -325,37 +332,33 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       // The MMA issue loops are not unrolled: issue is paced by the tensor
       // pipe, and the smaller code leaves the instruction cache to the score
       // and read-out warps.
-      // Order per step s:  dV(s) | S(s+1) -> X | dK(s), dQ(s) -> Y | [dQ read out] dP(s+1) -> Y.
+      // Order per step s:  dV(s) | S(s+1) -> X | dQ(s) -> Y, dK(s) | [dQ read out] dP(s+1) -> Y.
       // S(s+1) only needs X, which dV(s) has finished reading (MMAs run in
       // issue order), so the scores of step s+1 are ready when the score
-      // warps finish step s; dP(s+1) waits for dQ(s) to be read out of Y.
-      // The two score warpgroups leave P^T and dS^T for queries [0,64) in
-      // columns [0,32) and for queries [64,128) in columns [64,96) of X and Y.
+      // warps finish step s; dP(s+1) waits for dQ(s) to be read out of Y,
+      // which happens while dK(s) runs.  The two score warpgroups leave P^T
+      // for queries [0,64) in columns [0,32) and for queries [64,128) in
+      // columns [64,96) of X.
       auto half_col = [](int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); };
-      if (ok) ok = wait_all(C::kBarQFull + 0, 0);
+      if (ok) ok = wait1(C::kBarQFull + 0, 0);
       if (ok) {
         tc_fence_after_sync();
-        if (lane == 0) issue_s(0);
-        __syncwarp();
+        issue_s(0);
       }
-      if (ok) ok = wait_all(C::kBarDOFull + 0, 0);
+      if (ok) ok = wait1(C::kBarDOFull + 0, 0);
       if (ok) {
         tc_fence_after_sync();
-        if (lane == 0) issue_dp(0);
-        __syncwarp();
+        issue_dp(0);
       }
       for (int s = 0; s < total && ok; ++s) {
         const int st = s & 1;
-        ok = wait_all(C::kBarPReady, static_cast<uint32_t>(s & 1));
+        ok = wait1(C::kBarPReady, static_cast<uint32_t>(s & 1));
         if (!ok) break;
         tc_fence_after_sync();
-        if (lane == 0) {
 #pragma unroll 1
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts(tmem + C::kTdV, tmem + C::kTX + half_col(kk),
-                    sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < kTileM / 16; ++kk)
+          umma_ts(tmem + C::kTdV, tmem + C::kTX + half_col(kk),
+                  sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
         // S(s+1) goes in as soon as its Q tile has landed, but never holds
         // up dK(s), dQ(s): poll both and take whichever comes first.
         bool s_next_done = s + 1 >= total;
@@ -363,24 +366,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           const int st1 = (s + 1) & 1;
           const uint32_t ph1 = static_cast<uint32_t>(((s + 1) >> 1) & 1);
           const uint64_t t0 = global_timer_ns();
-          for (;;) {
-            int q_ready = 0, ds_ready = 0;
-            if (lane == 0) {
-              q_ready = mbar_try_wait(bar(C::kBarQFull + st1), ph1);
-              ds_ready = mbar_try_wait(bar(C::kBarDSReady), static_cast<uint32_t>(s & 1));
-            }
-            q_ready = __shfl_sync(0xffffffffu, q_ready, 0);
-            ds_ready = __shfl_sync(0xffffffffu, ds_ready, 0);
-            if (q_ready) {
+          for (uint32_t it = 0;; ++it) {
+            if (mbar_test_wait(bar(C::kBarQFull + st1), ph1)) {
               tc_fence_after_sync();
-              if (lane == 0) issue_s(s + 1);
-              __syncwarp();
+              issue_s(s + 1);
               s_next_done = true;
               break;
             }
-            if (ds_ready) break;
-            __nanosleep(32);
-            if (*abort_flag || global_timer_ns() - t0 > limit) {
+            if (mbar_test_wait(bar(C::kBarDSReady), static_cast<uint32_t>(s & 1))) break;
+            if ((it & 63u) == 63u && (*abort_flag || global_timer_ns() - t0 > limit)) {
               *abort_flag = 1;
               ok = false;
               break;
@@ -388,48 +382,48 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           }
           if (!ok) break;
         }
-        ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
+        ok = wait1(C::kBarDSReady, static_cast<uint32_t>(s & 1));
         if (!ok) break;
         tc_fence_after_sync();
-        if (lane == 0) {
-#pragma unroll 1
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts(tmem + C::kTdK, tmem + C::kTY + half_col(kk),
-                    sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
+        {
+          // dQ(s) first, into Y (the score warps have read dP^T out of it),
+          // so that its read-out overlaps dK(s); both take dS from the
+          // shared-memory buffer, as the MN-major (dQ) and the K-major (dK)
+          // view of the same swizzled tile.
 #pragma unroll 1
           for (int kk = 0; kk < kTileN / 16; ++kk)
             umma_ss(tmem + C::kTY, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
                     sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
           umma_commit(bar(C::kBarDQFull));
+#pragma unroll 1
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            umma_ss(tmem + C::kTdK, sw128_desc(dsA + (kk >> 2) * C::kBlockBytes + (kk & 3) * 32, 16, 1024),
+                    sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(C::kBarQEmpty + st));
           umma_commit(bar(C::kBarDOEmpty + st));
+          if (!C::kStageInDO) umma_commit(bar(C::kBarDSRead));
         }
-        __syncwarp();
         if (!s_next_done) {
           const int st1 = (s + 1) & 1;
-          ok = wait_all(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          ok = wait1(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
           if (!ok) break;
           tc_fence_after_sync();
-          if (lane == 0) issue_s(s + 1);
-          __syncwarp();
+          issue_s(s + 1);
         }
         if (s + 1 < total) {
-          ok = wait_all(C::kBarDOFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
-          if (ok) ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
+          ok = wait1(C::kBarDOFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          if (ok) ok = wait1(C::kBarDQFree, static_cast<uint32_t>(s & 1));
           if (!ok) break;
           tc_fence_after_sync();
-          if (lane == 0) issue_dp(s + 1);
-          __syncwarp();
+          issue_dp(s + 1);
         }
       }
-      if (lane == 0) {
-        if (ok) umma_commit(bar(C::kBarDKDV));
-        int no_abort = 0;
-        umma_commit(bar(C::kBarDrain));
-        mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
-      }
-      __syncwarp();
+      if (ok) umma_commit(bar(C::kBarDKDV));
+      int no_abort = 0;
+      umma_commit(bar(C::kBarDrain));
+      mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
     }
+    __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     // =========================== score warpgroups =======================
     // Two warpgroups: h = 0 takes query columns [0, 64), h = 1 [64, 128);
@@ -578,8 +572,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (!C::kStageInDO && ok && s > 0) ok = wait_all(C::kBarDSFree, static_cast<uint32_t>((s - 1) & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into Y (for dK) and
-      // into this half's block of the dS buffer (for dQ); dd_s holds -D 2^e.
+      // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into this half's
+      // block of the dS buffer (for dQ and dK); dd_s holds -D 2^e.
       {
         uint32_t da[32], db[32];
         tmem_ld32_nowait(tY + 64 * h, da);
@@ -614,10 +608,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             w[k >> 1] = pack_f16x2(d0, d1);
           }
-          tmem_st8_nowait(tY + 64 * h + cq * 8, w);
-          // dS (queries contiguous per key row) for the dQ = dS K product:
-          // this half's 64 queries fill one 128-byte row of its block, the
-          // 16-byte chunk index XOR-swizzled with the key row.
+          // dS (queries contiguous per key row) for the dQ = dS K and
+          // dK = dS^T Q products: this half's 64 queries fill one 128-byte
+          // row of its block, the 16-byte chunk index XOR-swizzled with the
+          // key row.
 #pragma unroll
           for (int v = 0; v < 2; ++v) {
             const int chunk = cq * 2 + v;
@@ -625,7 +619,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
         }
-        tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
@@ -707,6 +700,11 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_arrive(bar(C::kBarDQFree));
       uint8_t* wstage = C::kStageInDO ? smem + C::kOffDO + (s & 1) * C::kDOTileBytes + quad * C::kDQWarpStage
                                       : smem + C::kOffDS + quad * C::kDQWarpStage;
+      // Staging in the dS buffer waits until the dK product has read it.
+      if (!C::kStageInDO && !wait_all(C::kBarDSRead, static_cast<uint32_t>(s & 1))) {
+        ok = false;
+        break;
+      }
 #pragma unroll
       for (int rd = 0; rd < C::kDQRounds; ++rd) {
 #pragma unroll
