@@ -51,6 +51,26 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest per-rank value over all ranks of the initialised process
+    group (the value itself when not distributed).  Used for the timed
+    region: the job takes as long as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank does one step's work per step (weak
+    scaling), so the job does `world` times the per-rank FLOPs in the
+    slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def flops_per_pair(dh: int, dv: int):
     return 2 * (dh + dv), 2 * (2 * dh + 3 * dv)
 
@@ -291,13 +311,9 @@ def run_cuda(args):
     if status != 0:
         raise RuntimeError(f"device status {status}: {esd.strerror(status)}")
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * (flops_fwd + flops_bwd) / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(flops_fwd + flops_bwd, world, ms_per_step)
 
     names = ["attn_fwd_kernel", "attn_bwd_preprocess_kernel", "attn_bwd_main_kernel", "attn_bwd_finalize_kernel"]
     per_kernel = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i, n in enumerate(names)}
@@ -380,13 +396,8 @@ def run_cuda(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b) / args.steps
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * (flops_fwd + flops_bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
+        e2e = {"value": job_throughput(flops_fwd + flops_bwd, world, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ---- parity spot check (oracle rows, forward and dQ) and CPU baseline ----
