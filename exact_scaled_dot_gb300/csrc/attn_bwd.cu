@@ -27,8 +27,9 @@
 //   finalize    dQ = scale * accumulator, rounded to bf16.
 //
 // Main-kernel warp roles (512 threads):
-//   warp 0      TMA producer: the K and V tile once, then the fp16 Q and
-//               the dO tile of every step into two-stage rings.
+//   warp 0      TMA producer: the K and V tile once, then the fp16 Q tile
+//               of every step into a two-stage ring and its dO tile into a
+//               single stage (dO(s) is dead once dV(s) is done).
 //   warp 1      MMA issuer (lane 0 issues).
 //   warps 4-11  two "score" warpgroups, one per 64-query half of the step,
 //               thread = key row = TMEM lane:
@@ -85,18 +86,19 @@ struct BwdCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKTileBytes;
   static constexpr int kOffQ = kOffV + kVTileBytes;
-  static constexpr int kOffDO = kOffQ + kStages * kQTileBytes;
-  static constexpr int kOffDS = kOffDO + kStages * kDOTileBytes;
-  static constexpr int kOffLse = kOffDS + kDSTileBytes;
+  static constexpr int kOffDO = kOffQ + kStages * kQTileBytes;   // one stage: dO(s) is dead after dV(s)
+  static constexpr int kOffDS = kOffDO + kDOTileBytes;
+  static constexpr int kOffStage = kOffDS + kDSTileBytes;          // dQ staging, 4 warps x 8 KB
+  static constexpr int kOffLse = kOffStage + 4 * 2 * 32 * 32 * 4;
   static constexpr int kOffDd = kOffLse + kTileM * 4;
   static constexpr int kOffRed = kOffDd + kTileM * 4;      // 4 warps x 4 floats
   static constexpr int kOffBar = kOffRed + 64;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;                 // [2]
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
-  static constexpr int kBarDOFull = kBarQEmpty + 2;   // [2]
-  static constexpr int kBarDOEmpty = kBarDOFull + 2;  // [2]
-  static constexpr int kBarK16 = kBarDOEmpty + 2;     // K tile re-encoded as fp16
+  static constexpr int kBarDOFull = kBarQEmpty + 2;
+  static constexpr int kBarDOEmpty = kBarDOFull + 1;
+  static constexpr int kBarK16 = kBarDOEmpty + 1;     // K tile re-encoded as fp16
   static constexpr int kBarScale = kBarK16 + 1;       // dS scale bound reduced
   static constexpr int kBarSFull = kBarScale + 1;
   static constexpr int kBarDPFull = kBarSFull + 1;
@@ -106,9 +108,7 @@ struct BwdCfg {
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKDV = kBarDQFree + 1;
   static constexpr int kBarLse = kBarDKDV + 1;        // score warps loaded LSE, D
-  static constexpr int kBarDSFree = kBarLse + 1;     // dS buffer no longer read by the dQ reduce
-  static constexpr int kBarDSRead = kBarDSFree + 1;  // dK product has read the dS buffer
-  static constexpr int kBarDrain = kBarDSRead + 1;
+  static constexpr int kBarDrain = kBarLse + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -123,21 +123,14 @@ struct BwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
   // dQ read-out: each read-out warp stages its 32 query rows as boxes of 32
-  // rows x 32 fp32 (4 KB).  When d_h = d_v the staging is the step's dO
-  // stage (consumed once the dQ product is done), DV/64 boxes per warp per
-  // round, two rounds, the second round's boxes held in registers meanwhile
-  // so that tensor memory is released at once; the score warps never wait
-  // for it.  Otherwise (d_h = 128, d_v = 64) the staging is the dS buffer,
-  // two boxes per warp per round.
+  // rows x 32 fp32 (4 KB) in its own 8 KB of a dedicated staging buffer,
+  // two boxes per round, DH / 64 rounds per step.
   static constexpr int kDQBoxCols = 32;
   static constexpr int kDQBoxBytes = 32 * kDQBoxCols * 4;
   static constexpr int kDQBoxes = DH / kDQBoxCols;
-  static constexpr bool kStageInDO = (DH == DV);
-  static constexpr int kDQBoxesPerRound = kStageInDO ? DV / 64 : 2;
+  static constexpr int kDQBoxesPerRound = 2;
   static constexpr int kDQRounds = kDQBoxes / kDQBoxesPerRound;
   static constexpr int kDQWarpStage = kDQBoxesPerRound * kDQBoxBytes;
-  static_assert(kStageInDO ? (kDQRounds == 2 && 4 * kDQWarpStage <= kDOTileBytes)
-                           : (4 * kDQWarpStage <= kDSTileBytes), "dQ staging");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
@@ -193,10 +186,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
       mbar_init(bar(C::kBarQEmpty + s), 1);
-      mbar_init(bar(C::kBarDOFull + s), 1);
-      // MMA commit, plus the four read-out warps when the dO stage is staging.
-      mbar_init(bar(C::kBarDOEmpty + s), C::kStageInDO ? 1 + 4 : 1);
     }
+    mbar_init(bar(C::kBarDOFull), 1);
+    mbar_init(bar(C::kBarDOEmpty), 1);
     mbar_init(bar(C::kBarK16), 128);
     mbar_init(bar(C::kBarScale), 128);
     mbar_init(bar(C::kBarSFull), 1);
@@ -207,8 +199,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDKDV), 1);
     mbar_init(bar(C::kBarLse), 256);
-    mbar_init(bar(C::kBarDSFree), 4);
-    mbar_init(bar(C::kBarDSRead), 1);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
@@ -258,7 +248,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       for (int c = 0; c < DV / 64; ++c)
         tma_load_3d(sbase + C::kOffV + c * C::kBlockBytes, &tmV, bar(C::kBarKV), c * 64,
                     static_cast<int32_t>(j0), bkv);
-      int q_issued[2] = {0, 0}, do_issued[2] = {0, 0};
+      int q_issued[2] = {0, 0}, do_issued = 0;
       for (int s = 0; s < total; ++s) {
         const int st = s & 1;
         const uint32_t ph = static_cast<uint32_t>(((s >> 1) & 1) ^ 1);
@@ -270,12 +260,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tma_load_3d(sbase + C::kOffQ + st * C::kQTileBytes + c * C::kBlockBytes, &tmQ,
                       bar(C::kBarQFull + st), c * 64, q0, bhq);
         ++q_issued[st];
-        if (!mbar_wait(bar(C::kBarDOEmpty + st), ph, abort_flag, limit)) break;
-        mbar_arrive_expect_tx(bar(C::kBarDOFull + st), C::kDOTileBytes);
+        // One dO stage: dO(s) is read by dP(s) and dV(s) only, so the next
+        // tile loads as soon as dV(s) is done, well before dP(s+1).
+        if (s > 0 && !mbar_wait(bar(C::kBarDOEmpty), static_cast<uint32_t>((s - 1) & 1), abort_flag, limit)) break;
+        mbar_arrive_expect_tx(bar(C::kBarDOFull), C::kDOTileBytes);
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sbase + C::kOffDO + st * C::kDOTileBytes + c * C::kBlockBytes, &tmdO,
-                      bar(C::kBarDOFull + st), c * 64, q0, bhq);
-        ++do_issued[st];
+          tma_load_3d(sbase + C::kOffDO + c * C::kBlockBytes, &tmdO, bar(C::kBarDOFull), c * 64, q0, bhq);
+        ++do_issued;
         // Warm L2 with the tiles of step s + 2: their shared-memory stage is
         // only free once step s has finished, which leaves too little time to
         // hide a load from HBM.
@@ -291,8 +282,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_wait(bar(C::kBarKV), 0, &no_abort, limit);
         for (int st = 0; st < 2; ++st) {
           if (q_issued[st]) mbar_wait(bar(C::kBarQFull + st), (q_issued[st] - 1) & 1, &no_abort, limit);
-          if (do_issued[st]) mbar_wait(bar(C::kBarDOFull + st), (do_issued[st] - 1) & 1, &no_abort, limit);
         }
+        if (do_issued) mbar_wait(bar(C::kBarDOFull), (do_issued - 1) & 1, &no_abort, limit);
       }
     }
   } else if (warp == 1) {
@@ -310,7 +301,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       bool ok = wait1(C::kBarK16, 0);
       const uint32_t kA = sbase + C::kOffK, vA = sbase + C::kOffV, dsA = sbase + C::kOffDS;
       auto qB = [&](int s) { return sbase + C::kOffQ + (s & 1) * C::kQTileBytes; };
-      auto doB = [&](int s) { return sbase + C::kOffDO + (s & 1) * C::kDOTileBytes; };
+      auto doB = [&](int) { return sbase + C::kOffDO; };
       auto issue_s = [&](int s) {   // S^T = K Q^T -> X
 #pragma unroll 1
         for (int kk = 0; kk < DH / 16; ++kk) {
@@ -345,7 +336,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tc_fence_after_sync();
         issue_s(0);
       }
-      if (ok) ok = wait1(C::kBarDOFull + 0, 0);
+      if (ok) ok = wait1(C::kBarDOFull, 0);
       if (ok) {
         tc_fence_after_sync();
         issue_dp(0);
@@ -359,6 +350,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int kk = 0; kk < kTileM / 16; ++kk)
           umma_ts(tmem + C::kTdV, tmem + C::kTX + half_col(kk),
                   sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::kBarDOEmpty));   // dP(s) and dV(s) were dO(s)'s only readers
         // S(s+1) goes in as soon as its Q tile has landed, but never holds
         // up dK(s), dQ(s): poll both and take whichever comes first.
         bool s_next_done = s + 1 >= total;
@@ -400,8 +392,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             umma_ss(tmem + C::kTdK, sw128_desc(dsA + (kk >> 2) * C::kBlockBytes + (kk & 3) * 32, 16, 1024),
                     sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(C::kBarQEmpty + st));
-          umma_commit(bar(C::kBarDOEmpty + st));
-          if (!C::kStageInDO) umma_commit(bar(C::kBarDSRead));
         }
         if (!s_next_done) {
           const int st1 = (s + 1) & 1;
@@ -411,7 +401,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           issue_s(s + 1);
         }
         if (s + 1 < total) {
-          ok = wait1(C::kBarDOFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
+          ok = wait1(C::kBarDOFull, static_cast<uint32_t>((s + 1) & 1));
           if (ok) ok = wait1(C::kBarDQFree, static_cast<uint32_t>(s & 1));
           if (!ok) break;
           tc_fence_after_sync();
@@ -568,8 +558,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarPReady));
       ok = wait_all(C::kBarDPFull, static_cast<uint32_t>(s & 1));
-      // Without d_h = d_v the dS buffer doubles as dQ staging of the previous step.
-      if (!C::kStageInDO && ok && s > 0) ok = wait_all(C::kBarDSFree, static_cast<uint32_t>((s - 1) & 1));
       if (!ok) break;
       tc_fence_after_sync();
       // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into this half's
@@ -680,8 +668,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), (first_box + bx) * C::kDQBoxCols, row0,
                             bhq);
         bulk_commit_group();
-        bulk_wait_group_read0();
       }
+    };
+    // The staging memory is rewritten only once the reduce-adds already
+    // issued from it have read it (the last round of a step completes while
+    // the next step's MMAs run).
+    auto staging_free = [&]() {
+      if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
     };
     for (int s = 0; s < total && ok; ++s) {
@@ -698,21 +691,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       for (int bx = 0; bx < C::kDQBoxes; ++bx) tmem_wait_ld32(v[bx]);
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarDQFree));
-      uint8_t* wstage = C::kStageInDO ? smem + C::kOffDO + (s & 1) * C::kDOTileBytes + quad * C::kDQWarpStage
-                                      : smem + C::kOffDS + quad * C::kDQWarpStage;
-      // Staging in the dS buffer waits until the dK product has read it.
-      if (!C::kStageInDO && !wait_all(C::kBarDSRead, static_cast<uint32_t>(s & 1))) {
-        ok = false;
-        break;
-      }
+      uint8_t* wstage = smem + C::kOffStage + quad * C::kDQWarpStage;
 #pragma unroll
       for (int rd = 0; rd < C::kDQRounds; ++rd) {
+        staging_free();
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
           stage_box(wstage + bx * C::kDQBoxBytes, v[rd * C::kDQBoxesPerRound + bx]);
         reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, bhq);
       }
-      if (lane == 0) mbar_arrive(bar(C::kStageInDO ? C::kBarDOEmpty + (s & 1) : C::kBarDSFree));
       __syncwarp();
     }
     if (lane == 0) bulk_wait_group0();
