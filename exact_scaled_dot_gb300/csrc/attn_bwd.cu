@@ -38,9 +38,9 @@
 //               dS to shared memory for the dQ product.
 //   warps 12-15 converts K to fp16 in shared memory, reads dQ out of tensor
 //               memory into the accumulator and writes the final dK, dV.
-// The producer/MMA warpgroup hands most of its registers to the others
-// (setmaxnreg), so a score thread holds 64 scores and a read-out thread a
-// whole 128-column dQ row at once.
+// The producer/MMA and read-out warpgroups hand registers to the score
+// warpgroups (setmaxnreg), which hold 64 scores and the fp16 weights of a
+// step at once.
 //
 // Precision of the dS products.  dQ_i = scale sum_j dS_ij k_j sums terms
 // that largely cancel when a softmax row is sharply peaked, so rounding dS
@@ -117,9 +117,10 @@ struct BwdCfg {
   static constexpr int kThreads = 512;
   // Registers per thread: 128 at launch (65536 / 512); the producer/MMA
   // warpgroup gives most of its share to the score and read-out warpgroups
-  // (128 x 80 + 256 x 136 + 128 x 144 = 63488 <= 512 x 128).
-  static constexpr uint32_t kRegsLow = 80, kRegsScore = 136, kRegsAux = 144;
-  static_assert(128 * kRegsLow + 256 * kRegsScore + 128 * kRegsAux <= 512 * 128, "register split");
+  // (128 x 56 + 256 x 176 + 128 x 96 = 64512 <= 512 x 128).
+  static constexpr uint32_t kRegsLaunch = 128;   // 65536 / 512
+  static constexpr uint32_t kRegsLow = 56, kRegsScore = 176, kRegsAux = 96;
+  static_assert(128 * kRegsLow + 256 * kRegsScore + 128 * kRegsAux <= 512 * kRegsLaunch, "register split");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
   // dQ read-out: each read-out warp stages its 32 query rows as boxes of 32
@@ -228,7 +229,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     return ds_scale_exponent(mdo * mv + md);
   };
 
-  if (warp < 4) setmaxnreg_dec<C::kRegsLow>();
+  if (warp < 4) setmaxnreg_to<C::kRegsLow, C::kRegsLaunch>();
   if (warp == 0) {
     // =========================== TMA producer ===========================
     if (lane == 0 && *abort_flag == 0 && total > 0) {
@@ -418,7 +419,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // =========================== score warpgroups =======================
     // Two warpgroups: h = 0 takes query columns [0, 64), h = 1 [64, 128);
     // in both, thread = key row = TMEM lane.
-    setmaxnreg_inc<C::kRegsScore>();
+    setmaxnreg_to<C::kRegsScore, C::kRegsLaunch>();
     const int h = static_cast<int>(warp - 4) / 4;
     const uint32_t quad = warp & 3;
     const int jj = static_cast<int>(quad * 32 + lane);
@@ -614,7 +615,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
   } else if (warp >= 12) {
     // ======== fp16 re-encoding of K, dQ read-out, dK/dV epilogue ========
-    setmaxnreg_inc<C::kRegsAux>();
+    setmaxnreg_to<C::kRegsAux, C::kRegsLaunch>();
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);
     const int tid2 = static_cast<int>(threadIdx.x) - 384;
@@ -644,7 +645,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (ok) inv_scale = exp2_int(-scale_exponent());
     }
     // dQ read-out: each warp takes its 32 query rows of the tile (in Y) into
-    // registers at once (one wait) and releases Y; it then scales them back
+    // registers a 64-column round at a time and releases Y after the last
+    // round's loads; it scales them back
     // by 2^-e and stages them as 32 x 32 fp32 boxes in the 128-byte swizzle
     // pattern (conflict-free stores), and one lane adds the boxes into the
     // fp32 accumulator with TMA reduce-add, a round at a time, the staging
@@ -684,20 +686,24 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t v[C::kDQBoxes][32];
-#pragma unroll
-      for (int bx = 0; bx < C::kDQBoxes; ++bx) tmem_ld32_nowait(tY + bx * C::kDQBoxCols, v[bx]);
-#pragma unroll
-      for (int bx = 0; bx < C::kDQBoxes; ++bx) tmem_wait_ld32(v[bx]);
-      tc_fence_before_sync();
-      mbar_arrive(bar(C::kBarDQFree));
       uint8_t* wstage = smem + C::kOffStage + quad * C::kDQWarpStage;
+      // A round at a time: two 32-column loads behind one wait; Y is handed
+      // back after the last round's loads.
 #pragma unroll
       for (int rd = 0; rd < C::kDQRounds; ++rd) {
-        staging_free();
+        uint32_t v[C::kDQBoxesPerRound][32];
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
-          stage_box(wstage + bx * C::kDQBoxBytes, v[rd * C::kDQBoxesPerRound + bx]);
+          tmem_ld32_nowait(tY + (rd * C::kDQBoxesPerRound + bx) * C::kDQBoxCols, v[bx]);
+#pragma unroll
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) tmem_wait_ld32(v[bx]);
+        if (rd + 1 == C::kDQRounds) {
+          tc_fence_before_sync();
+          mbar_arrive(bar(C::kBarDQFree));
+        }
+        staging_free();
+#pragma unroll
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, v[bx]);
         reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, bhq);
       }
       __syncwarp();

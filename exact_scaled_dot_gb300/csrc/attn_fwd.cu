@@ -72,7 +72,7 @@ struct FwdCfg {
   static constexpr int kSmemUsed = kOffAbort + 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;   // slack for 1024-byte alignment
   static constexpr int kThreads = 384;
-  static constexpr int kRegsLaunch = 168;   // 65536 / 384, rounded down to a multiple of 8
+  static constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384, rounded down to a multiple of 8
   static constexpr uint32_t kRegsLow = 56, kRegsHigh = 224;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -143,7 +143,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // (128 x 56 + 256 x 224 = 384 x 168, the launch allocation).
   static_assert(128 * C::kRegsLow + 256 * C::kRegsHigh <= C::kThreads * C::kRegsLaunch, "register split");
 
-  if (warp < 4) setmaxnreg_dec<C::kRegsLow>();
+  if (warp < 4) setmaxnreg_to<C::kRegsLow, C::kRegsLaunch>();
   if (warp == 0) {
     // =========================== TMA producer ===========================
     if (lane == 0 && *abort_flag == 0) {
@@ -305,7 +305,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
   } else if (warp >= 4) {
     // ============================== softmax =============================
-    setmaxnreg_inc<C::kRegsHigh>();
+    setmaxnreg_to<C::kRegsHigh, C::kRegsLaunch>();
     const int t = (warp - 4) / 4;
     const uint32_t quad = warp & 3;
     const int row = static_cast<int>(quad * 32 + lane);

@@ -114,6 +114,16 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegs));
 }
 
+// Move this warpgroup's budget from kLaunch (the launch allocation) to
+// kRegs: an increase where kRegs > kLaunch, a decrease where it is smaller
+// (an increase to a smaller count is an illegal instruction).
+template <uint32_t kRegs, uint32_t kLaunch>
+__device__ __forceinline__ void setmaxnreg_to() {
+  static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+  if constexpr (kRegs > kLaunch) setmaxnreg_inc<kRegs>();
+  else if constexpr (kRegs < kLaunch) setmaxnreg_dec<kRegs>();
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
