@@ -31,7 +31,7 @@ ATTN_MAX_BATCH = 512
 ATTN_OFFSET_DEFAULT = -(2 ** 63)
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+EXPORTS = ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
            "attn_bwd_finalize", "attn_visible_pairs", "attn_get_status", "attn_clear_status",
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes")
@@ -70,6 +70,9 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     S, M = ctypes.POINTER(AttnShape), ctypes.POINTER(AttnMask)
     f = ctypes.c_float
     lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_fwd_decode.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd_decode_workspace_bytes.argtypes = [S, M]
+    lib.attn_fwd_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [S]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
@@ -89,7 +92,7 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_bwd_noalloc.restype = ctypes.c_int
     lib.attn_bwd_noalloc_max_scratch_bytes.argtypes = []
     lib.attn_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
-    for name in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
+    for name in ("attn_fwd", "attn_fwd_decode", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
                  "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
@@ -204,6 +207,45 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool 
     rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
                          _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), _stream(dev, stream))
     _check(rc, "attn_fwd")
+    return O, LSE, O_lo
+
+
+def attn_fwd_decode_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, causal: bool = False,
+                                    causal_offset: Optional[int] = None, kv_len=None) -> int:
+    shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    return int(load().attn_fwd_decode_workspace_bytes(ctypes.byref(shape), ctypes.byref(m.mask)))
+
+
+def attn_fwd_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
+                    causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
+                    O: Optional[torch.Tensor] = None, LSE: Optional[torch.Tensor] = None,
+                    O_lo: Optional[torch.Tensor] = None, residual: bool = True, workspace=None, stream=None):
+    """Forward for short query blocks (n_q <= 128) over a long key cache: the
+    same outputs as attn_fwd, with the query heads of a KV head packed into
+    one tile and the key range split across CTAs (merged by log-sum-exp)."""
+    dims, dev = _check_qkv(Q, K, V)
+    B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
+    scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
+    if O is None:
+        O = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
+    if LSE is None:
+        LSE = torch.empty((B, Hq, n_q), dtype=torch.float32, device=dev)
+    if O_lo is None and residual:
+        O_lo = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
+    if O_lo is not None:
+        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    shape = make_shape(*dims)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    need = int(load().attn_fwd_decode_workspace_bytes(ctypes.byref(shape), ctypes.byref(m.mask)))
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_ptr, ws_bytes = (_ws(workspace) if workspace is not None else (None, ctypes.c_size_t(0)))
+    rc = load().attn_fwd_decode(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
+                                _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), ws_ptr, ws_bytes, _stream(dev, stream))
+    _check(rc, "attn_fwd_decode")
     return O, LSE, O_lo
 
 

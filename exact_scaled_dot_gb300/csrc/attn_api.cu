@@ -2,6 +2,7 @@
 // descriptors, launches, the device status word and the failure-detection
 // self test.  Every argument check runs before the first CUDA call, so an
 // invalid call returns its error code without touching the GPU.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -285,6 +286,41 @@ int static_scratch_ptr(void** out) {
   *out = g_scratch_ptr[dev];
   return ATTN_OK;
 }
+// Layout of the short-query forward: query heads packed per 128-row tile,
+// and the key range split so that the row tiles fill about two CTAs per SM.
+struct DecodePlan {
+  int heads_per_tile, chunks, nsplit;
+  size_t opart_bytes, bytes;   // workspace: range outputs | range log-sum-exps
+};
+
+DecodePlan decode_plan(const attn_shape* s, const MaskParams& m) {
+  constexpr int kTargetCtas = 2 * 152;
+  const int group = s->Hq / s->Hkv;
+  DecodePlan d;
+  d.heads_per_tile = std::min(group, std::max(1, 128 / s->n_q));
+  d.chunks = (group + d.heads_per_tile - 1) / d.heads_per_tile;
+  const int64_t row_tiles = static_cast<int64_t>(s->B) * s->Hkv * d.chunks;
+  int64_t max_tiles = 0;
+  for (int b = 0; b < s->B; ++b) {
+    const int64_t lim = row_key_limit(m, s->n_k, b, static_cast<int64_t>(s->n_q) - 1);
+    max_tiles = std::max<int64_t>(max_tiles, (lim + kTileN - 1) / kTileN);
+  }
+  int64_t ns = (kTargetCtas + row_tiles - 1) / row_tiles;
+  ns = std::min<int64_t>(ns, std::max<int64_t>(1, max_tiles / 2));   // at least two key tiles per range
+  ns = std::min<int64_t>(std::max<int64_t>(ns, 1), 64);
+  d.nsplit = static_cast<int>(ns);
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * s->n_q;
+  d.opart_bytes = d.nsplit > 1 ? round256(static_cast<size_t>(d.nsplit) * rows * s->d_v * sizeof(float)) : 0;
+  d.bytes = d.nsplit > 1 ? d.opart_bytes + round256(static_cast<size_t>(d.nsplit) * rows * sizeof(float)) : 0;
+  return d;
+}
+
+int check_decode_shape(const attn_shape* shape) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  return shape->n_q > 128 ? ATTN_ERR_UNSUPPORTED : ATTN_OK;
+}
+
 }  // namespace
 }  // namespace esd
 
@@ -356,6 +392,55 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   p.status = status;
   const cudaError_t e =
       launch_attn_fwd(shape->d_h, shape->d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_fwd_decode_workspace_bytes(const attn_shape* shape, const attn_mask* mask) {
+  if (check_decode_shape(shape) != ATTN_OK) return 0;
+  MaskParams m;
+  if (build_mask(shape, mask, &m) != ATTN_OK) return 0;
+  return decode_plan(shape, m).bytes;
+}
+
+int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
+                    const void* V, void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  int rc = check_decode_shape(shape);
+  if (rc) return rc;
+  DecParams p;
+  rc = build_mask(shape, mask, &p.mask);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_ptrs({Q, K, V, O, LSE});
+  if (rc) return rc;
+  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+  const DecodePlan plan = decode_plan(shape, p.mask);
+  if (plan.bytes > 0 &&
+      (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < plan.bytes))
+    return ATTN_ERR_WORKSPACE;
+  // ---- CUDA from here on ----
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tk, tv;
+  const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
+  if (!make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) || !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk))
+    return ATTN_ERR_CUDA;
+  p.sh = shape_params(shape);
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.Q = Q;
+  p.O = O;
+  p.O_lo = O_lo;
+  p.LSE = LSE;
+  p.Opart = plan.bytes > 0 ? static_cast<float*>(workspace) : nullptr;
+  p.Lpart = plan.bytes > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.opart_bytes) : nullptr;
+  p.heads_per_tile = plan.heads_per_tile;
+  p.chunks = plan.chunks;
+  p.nsplit = plan.nsplit;
+  p.status = status;
+  const cudaError_t e = launch_attn_decode(shape->d_h, shape->d_v, tk, tv, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -99,12 +99,31 @@ struct BwdParams {
   unsigned int* status;
 };
 
+struct DecParams {
+  ShapeParams sh;
+  MaskParams mask;
+  float scale_log2;            // scale * log2(e)
+  uint64_t wait_limit_ns;
+  const void* Q;               // bf16 [B][Hq][n_q][d_h], gathered by threads
+  void* O;                     // bf16 [B][Hq][n_q][d_v]
+  void* O_lo;                  // bf16 rounding residual of O, or nullptr
+  float* LSE;                  // fp32 [B][Hq][n_q]
+  float* Opart;                // fp32 [nsplit][B*Hq*n_q][d_v] range partials (nsplit > 1)
+  float* Lpart;                // fp32 [nsplit][B*Hq*n_q] range log-sum-exps (nsplit > 1)
+  int32_t heads_per_tile;      // query heads packed into one 128-row tile
+  int32_t chunks;              // row tiles per KV head
+  int32_t nsplit;              // key ranges per row tile
+  unsigned int* status;
+};
+
 // Default limit of every bounded wait inside the kernels.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 // Kernel launchers (defined next to their kernels).
 cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_attn_decode(int dh, int dv, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecParams& p,
+                               cudaStream_t stream);
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);

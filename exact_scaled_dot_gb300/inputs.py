@@ -69,7 +69,16 @@ WORKLOADS: Dict[str, Workload] = {
                                     seed=1004),
     "mqa_chunked_prefill": Workload("mqa_chunked_prefill", B=1, Hq=64, Hkv=1, nq=1024, nk=16384,
                                     dh=128, dv=128, causal=True, seed=1005),
+    # Short query blocks over a long key cache (decode and small chunks of new
+    # queries): causal with the bottom-right offset n_k - n_q, ragged cache
+    # lengths.  Forward only; HBM-bound (the K/V cache is read once).
+    "decode_gqa": Workload("decode_gqa", B=8, Hq=32, Hkv=8, nq=1, nk=32768, dh=128, dv=128, causal=True,
+                           kv_len_range=(16384, 32768), seed=1101),
+    "decode_mqa_chunk": Workload("decode_mqa_chunk", B=8, Hq=64, Hkv=1, nq=16, nk=65536, dh=128, dv=128,
+                                 causal=True, kv_len_range=(32768, 65536), seed=1102),
 }
+
+DECODE_WORKLOADS = ["decode_gqa", "decode_mqa_chunk"]
 
 WORKLOAD_ORDER = ["single_head_full", "mha_causal", "gqa_causal_padded",
                   "cross_padded_peaked", "mqa_chunked_prefill"]

@@ -61,7 +61,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -115,6 +115,23 @@ typedef struct {
 int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
              void* O, float* LSE, void* O_lo, void* stream);
+
+/* Forward for short query blocks over a long key cache (decode, small
+ * chunks of new queries: the new-queries-over-a-history shape of "Chapter
+ * 31", section 1), n_q <= 128.  Same function, arguments and outputs as
+ * attn_fwd (A.10.1-A.10.3, same visible sets); the work is laid out
+ * differently: the query heads that share a KV head are packed into one
+ * 128-row tile, so each K/V tile is read once per group, and the key range is
+ * split across CTAs, the partial results being merged by their log-sum-exp
+ * (O = sum_s exp(LSE_s - LSE) O_s, LSE = log sum_s exp(LSE_s)).
+ * `workspace`: device memory of at least attn_fwd_decode_workspace_bytes()
+ * bytes, 256-byte aligned (may be NULL when that is 0).  Returns
+ * ATTN_ERR_UNSUPPORTED for n_q > 128 (use attn_fwd). */
+size_t attn_fwd_decode_workspace_bytes(const attn_shape* shape, const attn_mask* mask);
+int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
+                    const void* Q, const void* K, const void* V,
+                    void* O, float* LSE, void* O_lo,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace the backward needs (attn_bwd and its three
  * stages): row terms D, per-128-row-tile bounds used to scale dS, an fp32

@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 2
+    assert esd.attn_abi_version() == 3
 
 
 def test_strerror_covers_every_code(lib):
@@ -145,3 +145,22 @@ def test_visible_pairs_closed_form(lib, orc):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         bnd.load(tmp_path / "nope.so")
+
+
+def test_decode_entry_point_checks(lib):
+    """attn_fwd_decode: n_q > 128 is unsupported (use attn_fwd); a needed
+    workspace must be present and 256-byte aligned; all before any CUDA call."""
+    m = _mask(causal=1)
+    p = ctypes.c_void_p(256)
+    big = _shape(n_q=129, n_k=1000)
+    assert lib.attn_fwd_decode(ctypes.byref(big), ctypes.byref(m), ctypes.c_float(0.1), p, p, p, p, p, None,
+                               None, ctypes.c_size_t(0), None) == bnd.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_decode_workspace_bytes(ctypes.byref(big), ctypes.byref(m)) == 0
+    small = _shape(B=1, Hq=8, Hkv=1, n_q=1, n_k=4096)
+    need = lib.attn_fwd_decode_workspace_bytes(ctypes.byref(small), ctypes.byref(m))
+    # one row tile of 8 heads x 1 query: the key range is split, partials need a workspace
+    assert need > 0 and need % 256 == 0
+    args = [ctypes.byref(small), ctypes.byref(m), ctypes.c_float(0.1), p, p, p, p, p, None]
+    assert lib.attn_fwd_decode(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_fwd_decode(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_fwd_decode(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
