@@ -235,7 +235,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       auto issue_qk = [&](int j) {   // S_{j&1} = Q K_j^T
         const int st = j & 1;
         const uint32_t kb = sbase + C::kOffK + st * C::kKTileBytes;
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
           umma_ss(tmem + 128 * st, sw128_desc(sbase + C::kOffQ + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
@@ -257,7 +257,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t vb = sbase + C::kOffV + st * C::kVTileBytes;
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
           umma_ts(tmem + C::kTO, tmem + 128 * st + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024), kIdPV,
                   (j > 0 || kk > 0) ? 1u : 0u);

@@ -14,8 +14,12 @@
 // CTA = two 128-row query tiles of one (batch, query head), sharing every
 // K/V tile the CTA loads.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K_j and V_j into rings.
-//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
-//               O_t += P_t V_j with P_t read back from tensor memory.
+//   warp 1      MMA issuer (lane 0 alone waits and issues): S_t = Q_t K_j^T
+//               into tensor memory, O_t += P_t V_j with P_t read back from
+//               tensor memory.
+//   warp 2      zeroes the padded key rows of a V tile before its PV product
+//               (only tiles that hold rows in [kv_len, n_k)), on request of
+//               the MMA thread once that tile has landed.
 //   warps 4-7   softmax for query tile 0 (thread = row = TMEM lane).
 //   warps 8-11  softmax for query tile 1.
 // While one tile's softmax runs, the tensor core works on the other tile.
@@ -62,7 +66,9 @@ struct FwdCfg {
   static constexpr int kBarKEmpty = kBarKFull + kKStages;
   static constexpr int kBarVFull = kBarKEmpty + kKStages;
   static constexpr int kBarVEmpty = kBarVFull + kVStages;
-  static constexpr int kBarSFull = kBarVEmpty + kVStages;   // [2]
+  static constexpr int kBarZeroReq = kBarVEmpty + kVStages;  // MMA thread: zero this V tile's padding
+  static constexpr int kBarZeroed = kBarZeroReq + 1;          // warp 2: done
+  static constexpr int kBarSFull = kBarZeroed + 1;            // [2]
   static constexpr int kBarPReady = kBarSFull + 2;          // [2]
   static constexpr int kBarOFull = kBarPReady + 2;          // [2]
   static constexpr int kBarDrain = kBarOFull + 2;
@@ -73,7 +79,7 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kSmemUsed + 1024;   // slack for 1024-byte alignment
   static constexpr int kThreads = 384;
   static constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384, rounded down to a multiple of 8
-  static constexpr uint32_t kRegsLow = 56, kRegsHigh = 224;
+  static constexpr uint32_t kRegsLow = 64, kRegsHigh = 216;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(2 * 128 + 2 * DV <= 512, "tensor memory budget");
@@ -120,6 +126,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarVEmpty + s), 1);
     }
+    mbar_init(bar(C::kBarZeroReq), 1);
+    mbar_init(bar(C::kBarZeroed), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
       mbar_init(bar(C::kBarPReady + t), 128);
@@ -188,11 +196,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           if (v_issued[s]) mbar_wait(bar(C::kBarVFull + s), (v_issued[s] - 1) & 1, &no_abort, limit);
       }
     }
+  } else if (warp == 2) {
+    // ===================== zero padded V rows =====================
+    // Key rows in [kv_len, n_k) hold caller memory that may be anything
+    // (even NaN); their weights are exactly 0, but 0 * NaN would still
+    // poison O, so those V rows are zeroed before the PV product.  Rows at
+    // or beyond n_k arrive as zeros from the TMA bounds check.
+    // The request comes from the MMA thread after it has seen the tile land,
+    // and it waits for the reply before it asks again, so the two barriers
+    // never run more than one phase apart.
+    if (*abort_flag == 0) {
+      uint32_t z = 0;
+      for (int j = 0; j < nkv; ++j) {
+        int r0, r1;
+        if (!padded_rows(p.mask, p.sh.n_k, b, j, r0, r1)) continue;
+        const int vs = j % C::kVStages;
+        const bool w = mbar_wait(bar(C::kBarZeroReq), z & 1u, abort_flag, limit);
+        if (!__all_sync(0xffffffffu, w)) break;
+        ++z;
+        uint8_t* vbase = smem + C::kOffV + vs * C::kVTileBytes;
+        const int chunks = (r1 - r0) * (DV / 64) * 8;   // 16-byte chunks
+        for (int q = static_cast<int>(lane); q < chunks; q += 32) {
+          const int row = r0 + q / ((DV / 64) * 8);
+          const int rem = q % ((DV / 64) * 8);
+          *reinterpret_cast<uint4*>(vbase + (rem / 8) * C::kBlockBytes + row * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarZeroed));
+      }
+    }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    // The whole warp follows the schedule; lane 0 issues the MMAs.  The
-    // other lanes help zero padded V rows in shared memory.
-    if (*abort_flag == 0) {
+    // Lane 0 alone follows the schedule: every wait and every MMA issue is
+    // on the critical path of the tensor core, so no warp-wide votes or
+    // reconvergence points sit between them.
+    if (lane == 0 && *abort_flag == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
       auto issue_qk = [&](int t, int ks) {
@@ -214,95 +254,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                   (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      auto wait_all = [&](int idx, uint32_t parity) -> bool {
-        const bool w = mbar_wait(bar(idx), parity, abort_flag, limit);
-        return __all_sync(0xffffffffu, w);
-      };
-      // Key rows in [kv_len, n_k) hold caller memory that may be anything
-      // (even NaN); their weights are exactly 0, but 0 * NaN would still
-      // poison O, so those V rows are zeroed before the PV product.  Rows
-      // at or beyond n_k arrive as zeros from the TMA bounds check.
-      const int64_t klen = key_len(p.mask, p.sh.n_k, b);
-      auto zero_padded_v = [&](int j, int vs) {
-        const int64_t j0 = static_cast<int64_t>(j) * kTileN;
-        int64_t r0 = klen - j0, r1 = static_cast<int64_t>(p.sh.n_k) - j0;
-        if (r0 < 0) r0 = 0;
-        if (r1 > kTileN) r1 = kTileN;
-        if (r0 >= r1) return;
-        uint8_t* vbase = smem + C::kOffV + vs * C::kVTileBytes;
-        const int chunks = static_cast<int>(r1 - r0) * (DV / 64) * 8;   // 16-byte chunks
-        for (int q = static_cast<int>(lane); q < chunks; q += 32) {
-          const int row = static_cast<int>(r0) + q / ((DV / 64) * 8);
-          const int rem = q % ((DV / 64) * 8);
-          *reinterpret_cast<uint4*>(vbase + (rem / 8) * C::kBlockBytes + row * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      };
-      bool ok = wait_all(C::kBarQFull, 0);
+      auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
+      bool ok = wait1(C::kBarQFull, 0);
       if (ok && nkv > 0) {
-        ok = wait_all(C::kBarKFull + 0, 0);
+        ok = wait1(C::kBarKFull + 0, 0);
         if (ok) {
           tc_fence_after_sync();
-          if (lane == 0) {
-            for (int t = 0; t < 2; ++t)
-              if (ntiles[t] > 0) {
-                issue_qk(t, 0);
-                umma_commit(bar(C::kBarSFull + t));
-              }
-            umma_commit(bar(C::kBarKEmpty + 0));
-          }
-          __syncwarp();
+          for (int t = 0; t < 2; ++t)
+            if (ntiles[t] > 0) {
+              issue_qk(t, 0);
+              umma_commit(bar(C::kBarSFull + t));
+            }
+          umma_commit(bar(C::kBarKEmpty + 0));
         }
       }
+      uint32_t z = 0;   // padded tiles handed to warp 2 so far
       for (int j = 0; j < nkv && ok; ++j) {
         const int vs = j % C::kVStages;
-        ok = wait_all(C::kBarVFull + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
+        ok = wait1(C::kBarVFull + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
+        int r0, r1;
+        if (ok && padded_rows(p.mask, p.sh.n_k, b, j, r0, r1)) {
+          mbar_arrive(bar(C::kBarZeroReq));
+          ok = wait1(C::kBarZeroed, z & 1u);
+          ++z;
+        }
         if (!ok) break;
-        if (static_cast<int64_t>(j + 1) * kTileN > klen) zero_padded_v(j, vs);
         const int kn = (j + 1) % C::kKStages;
         bool k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < ntiles[t]) {
-            ok = wait_all(C::kBarPReady + t, static_cast<uint32_t>(j & 1));
+            ok = wait1(C::kBarPReady + t, static_cast<uint32_t>(j & 1));
             if (!ok) break;
             tc_fence_after_sync();
-            if (lane == 0) {
-              issue_pv(t, vs, j > 0);
-              if (j == ntiles[t] - 1) umma_commit(bar(C::kBarOFull + t));
-            }
-            __syncwarp();
+            issue_pv(t, vs, j > 0);
+            if (j == ntiles[t] - 1) umma_commit(bar(C::kBarOFull + t));
           }
           if (j + 1 < ntiles[t]) {
             if (!k_next_ready) {
-              ok = wait_all(C::kBarKFull + kn, static_cast<uint32_t>(((j + 1) / C::kKStages) & 1));
+              ok = wait1(C::kBarKFull + kn, static_cast<uint32_t>(((j + 1) / C::kKStages) & 1));
               if (!ok) break;
               tc_fence_after_sync();
               k_next_ready = true;
             }
-            if (lane == 0) {
-              issue_qk(t, kn);
-              umma_commit(bar(C::kBarSFull + t));
-            }
-            __syncwarp();
+            issue_qk(t, kn);
+            umma_commit(bar(C::kBarSFull + t));
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          umma_commit(bar(C::kBarVEmpty + vs));
-          if (k_next_ready) umma_commit(bar(C::kBarKEmpty + kn));
-        }
-        __syncwarp();
+        umma_commit(bar(C::kBarVEmpty + vs));
+        if (k_next_ready) umma_commit(bar(C::kBarKEmpty + kn));
       }
       // Every MMA issued above must finish before tensor memory is freed.
-      if (lane == 0) {
-        int no_abort = 0;
-        umma_commit(bar(C::kBarDrain));
-        mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
-      }
-      __syncwarp();
+      int no_abort = 0;
+      umma_commit(bar(C::kBarDrain));
+      mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // ============================== softmax =============================
     setmaxnreg_to<C::kRegsHigh, C::kRegsLaunch>();

@@ -61,6 +61,20 @@ __host__ __device__ __forceinline__ int kv_tiles_for_q_tile(const MaskParams& m,
   return static_cast<int>((lim + kTileN - 1) / kTileN);
 }
 
+// Rows [r0, r1) of key tile j (tile-relative) lie in [kv_len, n_k): rows
+// that hold caller memory but no visible key.  False when there are none.
+__host__ __device__ __forceinline__ bool padded_rows(const MaskParams& m, int n_k, int b, int j, int& r0,
+                                                     int& r1) {
+  const int64_t j0 = static_cast<int64_t>(j) * kTileN;
+  int64_t lo = key_len(m, n_k, b) - j0, hi = static_cast<int64_t>(n_k) - j0;
+  if (lo < 0) lo = 0;
+  if (hi > kTileN) hi = kTileN;
+  if (lo >= hi) return false;
+  r0 = static_cast<int>(lo);
+  r1 = static_cast<int>(hi);
+  return true;
+}
+
 // First query row that sees key j0 (the smallest i with lim(i) > j0), or
 // n_q when no row does.
 __host__ __device__ __forceinline__ int64_t first_row_seeing_key(const MaskParams& m, int n_q,
