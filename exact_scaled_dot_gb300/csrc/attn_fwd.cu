@@ -235,24 +235,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (lane == 0 && *abort_flag == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
-      auto issue_qk = [&](int t, int ks) {
-        const uint32_t qa = sbase + C::kOffQ + t * C::kQTileBytes;
-        const uint32_t kb = sbase + C::kOffK + ks * C::kKTileBytes;
+      // Shared-memory descriptors as base words plus constant steps: the
+      // softmax warps sharing this sub-partition take most issue slots, so
+      // every instruction between two MMAs delays the tensor core.
+      const SmemDesc dq0 = sw128_desc_words(sbase + C::kOffQ, 16, 1024);
+      const SmemDesc dk0 = sw128_desc_words(sbase + C::kOffK, 16, 1024);
+      const SmemDesc dv0 = sw128_desc_words(sbase + C::kOffV, C::kBlockBytes, 1024);
+      auto issue_qk = [&](int t, int ks) {   // S_t = Q_t K^T
+        const SmemDesc dq = desc_step(dq0, t * C::kQTileBytes);
+        const SmemDesc dk = desc_step(dk0, ks * C::kKTileBytes);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * 128, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                  kIdescQK, kk > 0 ? 1u : 0u);
+          umma_ss_w(tmem + t * 128, desc_step(dq, off), desc_step(dk, off), kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int vs, bool accumulate) {
-        const uint32_t vb = sbase + C::kOffV + vs * C::kVTileBytes;
+      auto issue_pv = [&](int t, int vs, bool accumulate) {   // O_t += P_t V
+        const SmemDesc dv = desc_step(dv0, vs * C::kVTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          umma_ts(tmem + 256 + t * DV, tmem + t * 128 + kk * 8,
-                  sw128_desc(vb + kk * 16 * 128, C::kBlockBytes, 1024), kIdescPV,
-                  (accumulate || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          umma_ts_w(tmem + 256 + t * DV, tmem + t * 128 + kk * 8, desc_step(dv, kk * 16 * 128), kIdescPV,
+                    (accumulate || kk > 0) ? 1u : 0u);
       };
       auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
       bool ok = wait1(C::kBarQFull, 0);

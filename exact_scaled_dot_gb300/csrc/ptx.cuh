@@ -332,6 +332,41 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// The same two products with each shared-memory descriptor passed as its
+// two 32-bit words.  A descriptor's low word holds the start address >> 4
+// (bits 0-13) and the leading-byte offset; stepping the start address by a
+// constant is then a single 32-bit add on the low word (no carry leaves
+// bits 0-13 for addresses inside shared memory), which keeps the issuing
+// thread's instruction count per MMA small.
+struct SmemDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SmemDesc sw128_desc_words(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  const uint64_t d = sw128_desc(saddr, lbo, sbo);
+  return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+// Descriptor of the tile `bytes` further on (bytes a multiple of 16).
+__device__ __forceinline__ SmemDesc desc_step(SmemDesc d, uint32_t bytes) { return SmemDesc{d.lo + (bytes >> 4), d.hi}; }
+
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n"
+      :: "r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n"
+      :: "r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 MMA issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
