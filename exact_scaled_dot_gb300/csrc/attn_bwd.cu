@@ -119,7 +119,7 @@ struct BwdCfg {
   // warpgroup gives most of its share to the score and read-out warpgroups
   // (128 x 56 + 256 x 176 + 128 x 96 = 64512 <= 512 x 128).
   static constexpr uint32_t kRegsLaunch = 128;   // 65536 / 512
-  static constexpr uint32_t kRegsLow = 56, kRegsScore = 176, kRegsAux = 96;
+  static constexpr uint32_t kRegsLow = 64, kRegsScore = 176, kRegsAux = 96;
   static_assert(128 * kRegsLow + 256 * kRegsScore + 128 * kRegsAux <= 512 * kRegsLaunch, "register split");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTX = 0, kTY = 128, kTdK = 256, kTdV = 256 + DH;
@@ -300,30 +300,37 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
       auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
       bool ok = wait1(C::kBarK16, 0);
-      const uint32_t kA = sbase + C::kOffK, vA = sbase + C::kOffV, dsA = sbase + C::kOffDS;
-      auto qB = [&](int s) { return sbase + C::kOffQ + (s & 1) * C::kQTileBytes; };
-      auto doB = [&](int) { return sbase + C::kOffDO; };
+      // Shared-memory descriptors as base words plus constant steps (K-major
+      // operands: leading offset 16; MN-major: the next 64-column block).
+      // The score and read-out warps sharing this sub-partition take most
+      // issue slots, so every instruction between two MMAs delays the
+      // tensor core.
+      const SmemDesc dK_k = sw128_desc_words(sbase + C::kOffK, 16, 1024);
+      const SmemDesc dK_mn = sw128_desc_words(sbase + C::kOffK, C::kBlockBytes, 1024);
+      const SmemDesc dV_k = sw128_desc_words(sbase + C::kOffV, 16, 1024);
+      const SmemDesc dQ_k = sw128_desc_words(sbase + C::kOffQ, 16, 1024);
+      const SmemDesc dQ_mn = sw128_desc_words(sbase + C::kOffQ, C::kBlockBytes, 1024);
+      const SmemDesc dDO_k = sw128_desc_words(sbase + C::kOffDO, 16, 1024);
+      const SmemDesc dDO_mn = sw128_desc_words(sbase + C::kOffDO, C::kBlockBytes, 1024);
+      const SmemDesc dDS_k = sw128_desc_words(sbase + C::kOffDS, 16, 1024);
+      const SmemDesc dDS_mn = sw128_desc_words(sbase + C::kOffDS, C::kBlockBytes, 1024);
       auto issue_s = [&](int s) {   // S^T = K Q^T -> X
-#pragma unroll 1
+        const SmemDesc dq = desc_step(dQ_k, (s & 1) * C::kQTileBytes);
+#pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          umma_ss(tmem + C::kTX, sw128_desc(kA + off, 16, 1024), sw128_desc(qB(s) + off, 16, 1024), kIdS,
-                  kk > 0 ? 1u : 0u);
+          umma_ss_w(tmem + C::kTX, desc_step(dK_k, off), desc_step(dq, off), kIdS, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(C::kBarSFull));
       };
-      auto issue_dp = [&](int s) {  // dP^T = V dO^T -> Y
-#pragma unroll 1
+      auto issue_dp = [&](int) {  // dP^T = V dO^T -> Y
+#pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          umma_ss(tmem + C::kTY, sw128_desc(vA + off, 16, 1024), sw128_desc(doB(s) + off, 16, 1024), kIdDP,
-                  kk > 0 ? 1u : 0u);
+          umma_ss_w(tmem + C::kTY, desc_step(dV_k, off), desc_step(dDO_k, off), kIdDP, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(C::kBarDPFull));
       };
-      // The MMA issue loops are not unrolled: issue is paced by the tensor
-      // pipe, and the smaller code leaves the instruction cache to the score
-      // and read-out warps.
       // Order per step s:  dV(s) | S(s+1) -> X | dQ(s) -> Y, dK(s) | [dQ read out] dP(s+1) -> Y.
       // S(s+1) only needs X, which dV(s) has finished reading (MMAs run in
       // issue order), so the scores of step s+1 are ready when the score
@@ -347,10 +354,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         ok = wait1(C::kBarPReady, static_cast<uint32_t>(s & 1));
         if (!ok) break;
         tc_fence_after_sync();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)
-          umma_ts(tmem + C::kTdV, tmem + C::kTX + half_col(kk),
-                  sw128_desc(doB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDV, (s > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_w(tmem + C::kTdV, tmem + C::kTX + half_col(kk), desc_step(dDO_mn, kk * 2048), kIdDV,
+                    (s > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(C::kBarDOEmpty));   // dP(s) and dV(s) were dO(s)'s only readers
         // S(s+1) goes in as soon as its Q tile has landed, but never holds
         // up dK(s), dQ(s): poll both and take whichever comes first.
@@ -383,15 +390,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           // so that its read-out overlaps dK(s); both take dS from the
           // shared-memory buffer, as the MN-major (dQ) and the K-major (dK)
           // view of the same swizzled tile.
-#pragma unroll 1
+#pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            umma_ss(tmem + C::kTY, sw128_desc(dsA + kk * 2048, C::kBlockBytes, 1024),
-                    sw128_desc(kA + kk * 2048, C::kBlockBytes, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+            umma_ss_w(tmem + C::kTY, desc_step(dDS_mn, kk * 2048), desc_step(dK_mn, kk * 2048), kIdDQ,
+                      kk > 0 ? 1u : 0u);
           umma_commit(bar(C::kBarDQFull));
-#pragma unroll 1
+#pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ss(tmem + C::kTdK, sw128_desc(dsA + (kk >> 2) * C::kBlockBytes + (kk & 3) * 32, 16, 1024),
-                    sw128_desc(qB(s) + kk * 2048, C::kBlockBytes, 1024), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
+            umma_ss_w(tmem + C::kTdK, desc_step(dDS_k, (kk >> 2) * C::kBlockBytes + (kk & 3) * 32),
+                      desc_step(dQ_mn, (s & 1) * C::kQTileBytes + kk * 2048), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(C::kBarQEmpty + st));
         }
         if (!s_next_done) {
