@@ -107,8 +107,7 @@ struct BwdCfg {
   static constexpr int kBarDQFull = kBarDSReady + 1;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKDV = kBarDQFree + 1;
-  static constexpr int kBarLse = kBarDKDV + 1;        // score warps loaded LSE, D
-  static constexpr int kBarDrain = kBarLse + 1;
+  static constexpr int kBarDrain = kBarDKDV + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -199,7 +198,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDKDV), 1);
-    mbar_init(bar(C::kBarLse), 256);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
@@ -496,24 +494,28 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       nlse2 = in ? -p.LSE[r] * kLog2e : -INFINITY;
       nd = in ? -p.D[r] : 0.f;
     };
+    // Each warpgroup reads only its own 64 LSE/D entries, written by its own
+    // threads tid < 64, so the two warpgroups never wait for each other
+    // here: a 128-thread named barrier publishes the entries of step s
+    // before its passes, and a second one ends every reader of step s
+    // before the entries of step s+1 overwrite them.  Every thread passes
+    // both barriers of every step, even after an abort (the step's work is
+    // then skipped), so no warp can be left waiting at one.
     float lse_next = 0.f, d_next = 0.f;
-    if (ok) load_row_terms(0, lse_next, d_next);
-    for (int s = 0; s < total && ok; ++s) {
-      const int q0 = step_q0(s);
-      // The LSE/D buffer is rewritten only after both warpgroups have
-      // finished the previous step (its dS-ready barrier completed).
-      if (s > 0) {
-        ok = wait_all(C::kBarDSReady, static_cast<uint32_t>((s - 1) & 1));
-        if (!ok) break;
-      }
+    if (ok) {
+      load_row_terms(0, lse_next, d_next);
       if (tid < 64) {
         lse_s[64 * h + tid] = lse_next;
         dd_s[64 * h + tid] = d_next * ds_scale;
       }
-      if (s + 1 < total) load_row_terms(s + 1, lse_next, d_next);
-      mbar_arrive(bar(C::kBarLse));
-      ok = wait_all(C::kBarLse, static_cast<uint32_t>(s & 1));
+      if (total > 1) load_row_terms(1, lse_next, d_next);
+    }
+    const uint32_t wg_bar = 1 + static_cast<uint32_t>(h);
+    for (int s = 0; s < total; ++s) {
+      named_bar_sync(wg_bar, 128);
+      do {
       if (!ok) break;
+      const int q0 = step_q0(s);
       // Column c (query q0 + c) is visible iff this key row is inside
       // kv_len and, when causal, q0 + c >= j - offset.
       const int64_t cmin64 = p.mask.causal ? (j - p.mask.offset - q0) : INT64_MIN / 2;
@@ -619,6 +621,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarDSReady));
+      } while (false);
+      named_bar_sync(wg_bar, 128);
+      if (ok && tid < 64 && s + 1 < total) {
+        lse_s[64 * h + tid] = lse_next;
+        dd_s[64 * h + tid] = d_next * ds_scale;
+      }
+      if (ok && s + 2 < total) load_row_terms(s + 2, lse_next, d_next);
     }
   } else if (warp >= 12) {
     // ======== fp16 re-encoding of K, dQ read-out, dK/dV epilogue ========
