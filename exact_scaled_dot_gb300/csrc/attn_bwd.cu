@@ -298,11 +298,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
       auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
       bool ok = wait1(C::kBarK16, 0);
-      // Shared-memory descriptors as base words plus constant steps (K-major
-      // operands: leading offset 16; MN-major: the next 64-column block).
-      // The score and read-out warps sharing this sub-partition take most
-      // issue slots, so every instruction between two MMAs delays the
-      // tensor core.
+      // Shared-memory descriptors as base words plus steps (K-major operands:
+      // leading offset 16; MN-major: the next 64-column block).  The score
+      // and read-out warps sharing this sub-partition take most issue slots,
+      // so every instruction between two MMAs delays the tensor core; the
+      // loops stay rolled so that the kernel's code fits the instruction
+      // cache next to the score and read-out warps.
       const SmemDesc dK_k = sw128_desc_words(sbase + C::kOffK, 16, 1024);
       const SmemDesc dK_mn = sw128_desc_words(sbase + C::kOffK, C::kBlockBytes, 1024);
       const SmemDesc dV_k = sw128_desc_words(sbase + C::kOffV, 16, 1024);
@@ -314,7 +315,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const SmemDesc dDS_mn = sw128_desc_words(sbase + C::kOffDS, C::kBlockBytes, 1024);
       auto issue_s = [&](int s) {   // S^T = K Q^T -> X
         const SmemDesc dq = desc_step(dQ_k, (s & 1) * C::kQTileBytes);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
           umma_ss_w(tmem + C::kTX, desc_step(dK_k, off), desc_step(dq, off), kIdS, kk > 0 ? 1u : 0u);
@@ -322,7 +323,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         umma_commit(bar(C::kBarSFull));
       };
       auto issue_dp = [&](int) {  // dP^T = V dO^T -> Y
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
           umma_ss_w(tmem + C::kTY, desc_step(dV_k, off), desc_step(dDO_k, off), kIdDP, kk > 0 ? 1u : 0u);
@@ -352,7 +353,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         ok = wait1(C::kBarPReady, static_cast<uint32_t>(s & 1));
         if (!ok) break;
         tc_fence_after_sync();
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kTileM / 16; ++kk)
           umma_ts_w(tmem + C::kTdV, tmem + C::kTX + half_col(kk), desc_step(dDO_mn, kk * 2048), kIdDV,
                     (s > 0 || kk > 0) ? 1u : 0u);
@@ -388,12 +389,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           // so that its read-out overlaps dK(s); both take dS from the
           // shared-memory buffer, as the MN-major (dQ) and the K-major (dK)
           // view of the same swizzled tile.
-#pragma unroll
+#pragma unroll 1
           for (int kk = 0; kk < kTileN / 16; ++kk)
             umma_ss_w(tmem + C::kTY, desc_step(dDS_mn, kk * 2048), desc_step(dK_mn, kk * 2048), kIdDQ,
                       kk > 0 ? 1u : 0u);
           umma_commit(bar(C::kBarDQFull));
-#pragma unroll
+#pragma unroll 1
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ss_w(tmem + C::kTdK, desc_step(dDS_k, (kk >> 2) * C::kBlockBytes + (kk & 3) * 32),
                       desc_step(dQ_mn, (s & 1) * C::kQTileBytes + kk * 2048), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
