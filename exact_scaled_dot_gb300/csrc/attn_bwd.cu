@@ -106,7 +106,8 @@ struct BwdCfg {
   static constexpr int kBarDSReady = kBarPReady + 1;
   static constexpr int kBarDQFull = kBarDSReady + 1;
   static constexpr int kBarDQFree = kBarDQFull + 1;
-  static constexpr int kBarDKDV = kBarDQFree + 1;
+  static constexpr int kBarDKDone = kBarDQFree + 1;   // dK(s) done: dS tile free again
+  static constexpr int kBarDKDV = kBarDKDone + 1;
   static constexpr int kBarDrain = kBarDKDV + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -197,8 +198,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDSReady), 256);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
-    mbar_init(bar(C::kBarDKDV), 1);
-    mbar_init(bar(C::kBarDrain), 1);
+    mbar_init(bar(C::kBarDKDone), 1);
+    mbar_init(bar(C::kBarDKDV), 2);    // one commit from each MMA issuer
+    mbar_init(bar(C::kBarDrain), 2);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
   }
@@ -285,11 +287,24 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (do_issued) mbar_wait(bar(C::kBarDOFull), (do_issued - 1) & 1, &no_abort, limit);
       }
     }
-  } else if (warp == 1) {
-    // ============================ MMA issuer ============================
-    // Lane 0 alone waits and issues (an MMA issue holds the thread for
-    // about as long as the MMA takes, so the issuer must never stall on a
-    // warp-wide vote); the other lanes go straight to the teardown.
+  } else if (warp == 1 || warp == 3) {
+    // =========================== MMA issuers ============================
+    // Two issuers on two SM sub-partitions split each step's products:
+    //   warp 1 (A):  dV(s) | S(s+1) -> X | dP(s+1) -> Y
+    //   warp 3 (B):  dQ(s) -> Y, dK(s)
+    // An MMA issue takes several instructions of the issuing thread, and the
+    // score and read-out warps sharing a sub-partition leave it only part of
+    // the issue slots; two issuers halve the instructions each one needs.
+    // Lane 0 alone waits and issues.  Ordering across the two:
+    //   X: dV(s) reads P^T(s) before S(s+1) overwrites it (both A, in order).
+    //   Y: dP(s) [A] -> score warps read it -> dQ(s) [B, after dS ready]
+    //      -> read-out -> dP(s+1) [A, after dQ free].
+    //   dS tile: dQ(s), dK(s) [B] read it; the score warps rewrite it only
+    //      after dP(s+1) has landed, and A issues dP(s+1) after B's dK(s)
+    //      has completed.
+    //   Q(s) stage: S(s) [A] completed before the scores of step s were
+    //      seen, so B's commit after dK(s) releases it.
+    const bool issuer_a = warp == 1;
     if (lane == 0 && *abort_flag == 0 && total > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(128, 128, false, false);    // S^T = K Q^T (fp16)
       constexpr uint32_t kIdDP = idesc_bf16_f32(128, 128, false, false);  // dP^T = V dO^T
@@ -299,11 +314,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
       bool ok = wait1(C::kBarK16, 0);
       // Shared-memory descriptors as base words plus steps (K-major operands:
-      // leading offset 16; MN-major: the next 64-column block).  The score
-      // and read-out warps sharing this sub-partition take most issue slots,
-      // so every instruction between two MMAs delays the tensor core; the
-      // loops stay rolled so that the kernel's code fits the instruction
-      // cache next to the score and read-out warps.
+      // leading offset 16; MN-major: the next 64-column block), so that few
+      // instructions sit between two MMAs; the loops stay rolled so that the
+      // kernel's code fits the instruction cache next to the other warps.
       const SmemDesc dK_k = sw128_desc_words(sbase + C::kOffK, 16, 1024);
       const SmemDesc dK_mn = sw128_desc_words(sbase + C::kOffK, C::kBlockBytes, 1024);
       const SmemDesc dV_k = sw128_desc_words(sbase + C::kOffV, 16, 1024);
@@ -313,78 +326,64 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const SmemDesc dDO_mn = sw128_desc_words(sbase + C::kOffDO, C::kBlockBytes, 1024);
       const SmemDesc dDS_k = sw128_desc_words(sbase + C::kOffDS, 16, 1024);
       const SmemDesc dDS_mn = sw128_desc_words(sbase + C::kOffDS, C::kBlockBytes, 1024);
-      auto issue_s = [&](int s) {   // S^T = K Q^T -> X
-        const SmemDesc dq = desc_step(dQ_k, (s & 1) * C::kQTileBytes);
+      if (issuer_a) {
+        auto issue_s = [&](int s) {   // S^T = K Q^T -> X
+          const SmemDesc dq = desc_step(dQ_k, (s & 1) * C::kQTileBytes);
 #pragma unroll 1
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          umma_ss_w(tmem + C::kTX, desc_step(dK_k, off), desc_step(dq, off), kIdS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(C::kBarSFull));
-      };
-      auto issue_dp = [&](int) {  // dP^T = V dO^T -> Y
-#pragma unroll 1
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          umma_ss_w(tmem + C::kTY, desc_step(dV_k, off), desc_step(dDO_k, off), kIdDP, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(C::kBarDPFull));
-      };
-      // Order per step s:  dV(s) | S(s+1) -> X | dQ(s) -> Y, dK(s) | [dQ read out] dP(s+1) -> Y.
-      // S(s+1) only needs X, which dV(s) has finished reading (MMAs run in
-      // issue order), so the scores of step s+1 are ready when the score
-      // warps finish step s; dP(s+1) waits for dQ(s) to be read out of Y,
-      // which happens while dK(s) runs.  The two score warpgroups leave P^T
-      // for queries [0,64) in columns [0,32) and for queries [64,128) in
-      // columns [64,96) of X.
-      auto half_col = [](int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); };
-      if (ok) ok = wait1(C::kBarQFull + 0, 0);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0);
-      }
-      if (ok) ok = wait1(C::kBarDOFull, 0);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_dp(0);
-      }
-      for (int s = 0; s < total && ok; ++s) {
-        const int st = s & 1;
-        ok = wait1(C::kBarPReady, static_cast<uint32_t>(s & 1));
-        if (!ok) break;
-        tc_fence_after_sync();
-#pragma unroll 1
-        for (int kk = 0; kk < kTileM / 16; ++kk)
-          umma_ts_w(tmem + C::kTdV, tmem + C::kTX + half_col(kk), desc_step(dDO_mn, kk * 2048), kIdDV,
-                    (s > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::kBarDOEmpty));   // dP(s) and dV(s) were dO(s)'s only readers
-        // S(s+1) goes in as soon as its Q tile has landed, but never holds
-        // up dK(s), dQ(s): poll both and take whichever comes first.
-        bool s_next_done = s + 1 >= total;
-        if (!s_next_done) {
-          const int st1 = (s + 1) & 1;
-          const uint32_t ph1 = static_cast<uint32_t>(((s + 1) >> 1) & 1);
-          const uint64_t t0 = global_timer_ns();
-          for (uint32_t it = 0;; ++it) {
-            if (mbar_test_wait(bar(C::kBarQFull + st1), ph1)) {
-              tc_fence_after_sync();
-              issue_s(s + 1);
-              s_next_done = true;
-              break;
-            }
-            if (mbar_test_wait(bar(C::kBarDSReady), static_cast<uint32_t>(s & 1))) break;
-            if ((it & 63u) == 63u && (*abort_flag || global_timer_ns() - t0 > limit)) {
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            umma_ss_w(tmem + C::kTX, desc_step(dK_k, off), desc_step(dq, off), kIdS, kk > 0 ? 1u : 0u);
           }
-          if (!ok) break;
+          umma_commit(bar(C::kBarSFull));
+        };
+        auto issue_dp = [&]() {  // dP^T = V dO^T -> Y
+#pragma unroll 1
+          for (int kk = 0; kk < DV / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            umma_ss_w(tmem + C::kTY, desc_step(dV_k, off), desc_step(dDO_k, off), kIdDP, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::kBarDPFull));
+        };
+        // The two score warpgroups leave P^T for queries [0,64) in columns
+        // [0,32) and for queries [64,128) in columns [64,96) of X.
+        auto half_col = [](int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); };
+        if (ok) ok = wait1(C::kBarQFull + 0, 0);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_s(0);
         }
-        ok = wait1(C::kBarDSReady, static_cast<uint32_t>(s & 1));
-        if (!ok) break;
-        tc_fence_after_sync();
-        {
+        if (ok) ok = wait1(C::kBarDOFull, 0);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_dp();
+        }
+        for (int s = 0; s < total && ok; ++s) {
+          ok = wait1(C::kBarPReady, static_cast<uint32_t>(s & 1));
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            umma_ts_w(tmem + C::kTdV, tmem + C::kTX + half_col(kk), desc_step(dDO_mn, kk * 2048), kIdDV,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(C::kBarDOEmpty));   // dP(s) and dV(s) were dO(s)'s only readers
+          if (s + 1 < total) {
+            ok = wait1(C::kBarQFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_s(s + 1);
+            ok = wait1(C::kBarDOFull, static_cast<uint32_t>((s + 1) & 1));
+            if (ok) ok = wait1(C::kBarDQFree, static_cast<uint32_t>(s & 1));
+            if (ok) ok = wait1(C::kBarDKDone, static_cast<uint32_t>(s & 1));
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_dp();
+          }
+        }
+      } else {
+        for (int s = 0; s < total && ok; ++s) {
+          ok = wait1(C::kBarDSReady, static_cast<uint32_t>(s & 1));
+          if (!ok) break;
+          tc_fence_after_sync();
           // dQ(s) first, into Y (the score warps have read dP^T out of it),
           // so that its read-out overlaps dK(s); both take dS from the
           // shared-memory buffer, as the MN-major (dQ) and the K-major (dK)
@@ -398,21 +397,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           for (int kk = 0; kk < kTileM / 16; ++kk)
             umma_ss_w(tmem + C::kTdK, desc_step(dDS_k, (kk >> 2) * C::kBlockBytes + (kk & 3) * 32),
                       desc_step(dQ_mn, (s & 1) * C::kQTileBytes + kk * 2048), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(C::kBarQEmpty + st));
-        }
-        if (!s_next_done) {
-          const int st1 = (s + 1) & 1;
-          ok = wait1(C::kBarQFull + st1, static_cast<uint32_t>(((s + 1) >> 1) & 1));
-          if (!ok) break;
-          tc_fence_after_sync();
-          issue_s(s + 1);
-        }
-        if (s + 1 < total) {
-          ok = wait1(C::kBarDOFull, static_cast<uint32_t>((s + 1) & 1));
-          if (ok) ok = wait1(C::kBarDQFree, static_cast<uint32_t>(s & 1));
-          if (!ok) break;
-          tc_fence_after_sync();
-          issue_dp(s + 1);
+          umma_commit(bar(C::kBarQEmpty + (s & 1)));
+          umma_commit(bar(C::kBarDKDone));
         }
       }
       if (ok) umma_commit(bar(C::kBarDKDV));
