@@ -9,4 +9,5 @@ from ._binding import (  # noqa: F401
     AttnError, AttnShape, attn_abi_version, attn_bwd, attn_bwd_finalize, attn_bwd_main, attn_bwd_noalloc,
     attn_bwd_noalloc_max_scratch_bytes, attn_bwd_preprocess, attn_bwd_workspace_bytes, attn_clear_status, attn_fwd, attn_fwd_decode, attn_fwd_decode_workspace_bytes,
     attn_get_status, attn_selftest_wait_timeout, attn_visible_pairs, load, make_shape, strerror,
+    AttnVarlen, attn_bwd_varlen, attn_bwd_varlen_workspace_bytes, attn_fwd_varlen, attn_varlen_visible_pairs,
 )

@@ -34,7 +34,8 @@ ATTN_OFFSET_DEFAULT = -(2 ** 63)
 EXPORTS = ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
            "attn_bwd_finalize", "attn_visible_pairs", "attn_get_status", "attn_clear_status",
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
-           "attn_bwd_noalloc_max_scratch_bytes")
+           "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
+           "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen")
 
 
 class AttnError(RuntimeError):
@@ -52,6 +53,12 @@ class AttnShape(ctypes.Structure):
 class AttnMask(ctypes.Structure):
     _fields_ = [("causal", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("causal_offset", ctypes.c_int64), ("kv_len", ctypes.POINTER(ctypes.c_int32))]
+
+
+class AttnVarlen(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d_h", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)), ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32))]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -92,8 +99,16 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_bwd_noalloc.restype = ctypes.c_int
     lib.attn_bwd_noalloc_max_scratch_bytes.argtypes = []
     lib.attn_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
+    VL = ctypes.POINTER(AttnVarlen)
+    lib.attn_varlen_visible_pairs.argtypes = [VL]
+    lib.attn_varlen_visible_pairs.restype = ctypes.c_int64
+    lib.attn_fwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_varlen_workspace_bytes.argtypes = [VL]
+    lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_bwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     for name in ("attn_fwd", "attn_fwd_decode", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
-                 "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout"):
+                 "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout", "attn_fwd_varlen",
+                 "attn_bwd_varlen"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -385,3 +400,102 @@ def attn_bwd_noalloc_max_scratch_bytes() -> int:
 
 def attn_abi_version() -> int:
     return int(load().attn_abi_version())
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length sequences (token-major tensors, per-sequence lengths)
+# ---------------------------------------------------------------------------
+class _VarlenArg:
+    """ctypes description of packed sequences; keeps the host offset arrays alive."""
+
+    def __init__(self, Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal):
+        cq = [int(x) for x in (cu_seqlens_q.tolist() if hasattr(cu_seqlens_q, "tolist") else cu_seqlens_q)]
+        ck = [int(x) for x in (cu_seqlens_k.tolist() if hasattr(cu_seqlens_k, "tolist") else cu_seqlens_k)]
+        if len(cq) != len(ck) or len(cq) < 2:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 >= 2 entries")
+        self._q = (ctypes.c_int32 * len(cq))(*cq)
+        self._k = (ctypes.c_int32 * len(ck))(*ck)
+        self.B = len(cq) - 1
+        self.total_q, self.total_k = cq[-1], ck[-1]
+        self.v = AttnVarlen(self.B, int(Hq), int(Hkv), int(d_h), int(d_v), 1 if causal else 0,
+                            ctypes.cast(self._q, ctypes.POINTER(ctypes.c_int32)),
+                            ctypes.cast(self._k, ctypes.POINTER(ctypes.c_int32)))
+
+
+def _varlen_dims(Q, K, V):
+    if Q.dim() != 3 or K.dim() != 3 or V.dim() != 3:
+        raise ValueError("packed Q, K, V must be 3-D [tokens, heads, d]")
+    Tq, Hq, d_h = (int(x) for x in Q.shape)
+    Tk, Hkv, _ = (int(x) for x in K.shape)
+    d_v = int(V.shape[2])
+    dev = Q.device
+    _check_tensor(Q, "Q", torch.bfloat16, (Tq, Hq, d_h), dev)
+    _check_tensor(K, "K", torch.bfloat16, (Tk, Hkv, d_h), dev)
+    _check_tensor(V, "V", torch.bfloat16, (Tk, Hkv, d_v), dev)
+    return (Tq, Tk, Hq, Hkv, d_h, d_v), dev
+
+
+def attn_varlen_visible_pairs(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False) -> int:
+    a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
+    return int(load().attn_varlen_visible_pairs(ctypes.byref(a.v)))
+
+
+def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False, scale: Optional[float] = None,
+                    O=None, LSE=None, O_lo=None, residual: bool = True, stream=None):
+    """Forward over packed sequences: Q [T_q, Hq, d_h], K [T_k, Hkv, d_h], V [T_k, Hkv, d_v] (bf16);
+    cu_seqlens_* are host offsets [B + 1].  Returns (O [T_q, Hq, d_v], LSE [Hq, T_q] fp32, O_lo)."""
+    (Tq, Tk, Hq, Hkv, d_h, d_v), dev = _varlen_dims(Q, K, V)
+    a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
+    if a.total_q != Tq or a.total_k != Tk:
+        raise ValueError("cu_seqlens_q[-1] / cu_seqlens_k[-1] must equal the token counts of Q / K")
+    scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
+    if O is None:
+        O = torch.empty((Tq, Hq, d_v), dtype=torch.bfloat16, device=dev)
+    if LSE is None:
+        LSE = torch.empty((Hq, Tq), dtype=torch.float32, device=dev)
+    if O_lo is None and residual:
+        O_lo = torch.empty((Tq, Hq, d_v), dtype=torch.bfloat16, device=dev)
+    _check_tensor(O, "O", torch.bfloat16, (Tq, Hq, d_v), dev)
+    _check_tensor(LSE, "LSE", torch.float32, (Hq, Tq), dev)
+    if O_lo is not None:
+        _check_tensor(O_lo, "O_lo", torch.bfloat16, (Tq, Hq, d_v), dev)
+    rc = load().attn_fwd_varlen(ctypes.byref(a.v), ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                _ptr(LSE), _ptr(O_lo), _stream(dev, stream))
+    _check(rc, "attn_fwd_varlen")
+    return O, LSE, O_lo
+
+
+def attn_bwd_varlen_workspace_bytes(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False) -> int:
+    a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
+    return int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+
+
+def attn_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens_q, cu_seqlens_k, *, O_lo=None, causal: bool = False,
+                    scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+    """Backward over packed sequences: returns (dQ, dK, dV), laid out like Q, K, V."""
+    (Tq, Tk, Hq, Hkv, d_h, d_v), dev = _varlen_dims(Q, K, V)
+    a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
+    if a.total_q != Tq or a.total_k != Tk:
+        raise ValueError("cu_seqlens_q[-1] / cu_seqlens_k[-1] must equal the token counts of Q / K")
+    scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
+    _check_tensor(O, "O", torch.bfloat16, (Tq, Hq, d_v), dev)
+    _check_tensor(dO, "dO", torch.bfloat16, (Tq, Hq, d_v), dev)
+    _check_tensor(LSE, "LSE", torch.float32, (Hq, Tq), dev)
+    if O_lo is not None:
+        _check_tensor(O_lo, "O_lo", torch.bfloat16, (Tq, Hq, d_v), dev)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev)
+    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev)
+    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev)
+    need = int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must hold at least {need} bytes")
+    rc = load().attn_bwd_varlen(ctypes.byref(a.v), ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                                ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
+    _check(rc, "attn_bwd_varlen")
+    return dQ, dK, dV

@@ -95,13 +95,65 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Sum over query rows of max(0, lim(b, i)) for one batch element.
 int64_t pairs_one_batch(const MaskParams& m, int n_q, int n_k, int b) {
   const int64_t L = key_len(m, n_k, b);
-  if (!m.causal) return L * n_q;
+  const int64_t nq = query_len(m, n_q, b);
+  if (!m.causal) return L * nq;
   // Rows with i + offset + 1 < L see i + offset + 1 keys; the rest see L.
-  int64_t split = L - m.offset - 1;        // rows i < split are causal-bound
+  const int64_t off = causal_offset(m, b);
+  int64_t split = L - off - 1;             // rows i < split are causal-bound
   if (split < 0) split = 0;
-  if (split > n_q) split = n_q;
-  const int64_t head = split * (m.offset + 1) + split * (split - 1) / 2;
-  return head + (n_q - split) * L;
+  if (split > nq) split = nq;
+  const int64_t head = split * (off + 1) + split * (split - 1) / 2;
+  return head + (nq - split) * L;
+}
+
+// A packed variable-length description turned into the kernels' terms: the
+// shape's n_q, n_k are the longest sequence (grid extents), the mask carries
+// every sequence's lengths and its own bottom-right causal offset, and the
+// layout its token offsets.
+struct Varlen {
+  attn_shape shape;
+  MaskParams mask;
+  LayoutParams lay;
+  int64_t total_q, total_k;
+};
+
+int build_varlen(const attn_varlen* v, Varlen* out) {
+  if (!v || !v->cu_seqlens_q || !v->cu_seqlens_k) return ATTN_ERR_NULL;
+  if (v->B <= 0 || v->B > ATTN_MAX_BATCH || v->Hq <= 0 || v->Hkv <= 0 || v->d_h <= 0 || v->d_v <= 0)
+    return ATTN_ERR_SHAPE;
+  if (v->Hq % v->Hkv != 0 || (v->causal != 0 && v->causal != 1)) return ATTN_ERR_SHAPE;
+  if (!supported_dims(v->d_h, v->d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (v->cu_seqlens_q[0] != 0 || v->cu_seqlens_k[0] != 0) return ATTN_ERR_SHAPE;
+  std::memset(out, 0, sizeof(*out));
+  int32_t max_q = 0, max_k = 0;
+  for (int b = 0; b < v->B; ++b) {
+    const int64_t lq = static_cast<int64_t>(v->cu_seqlens_q[b + 1]) - v->cu_seqlens_q[b];
+    const int64_t lk = static_cast<int64_t>(v->cu_seqlens_k[b + 1]) - v->cu_seqlens_k[b];
+    if (lq < 0 || lk < 0) return ATTN_ERR_SHAPE;
+    if (lq > 0 && lk == 0) return ATTN_ERR_EMPTY_ROW;
+    if (v->causal && lq > lk) return ATTN_ERR_EMPTY_ROW;   // row 0 would see keys j <= lk - lq < 0
+    out->mask.kv_len[b] = static_cast<int32_t>(lk);
+    out->mask.q_len[b] = static_cast<int32_t>(lq);
+    max_q = std::max<int32_t>(max_q, static_cast<int32_t>(lq));
+    max_k = std::max<int32_t>(max_k, static_cast<int32_t>(lk));
+  }
+  out->mask.causal = v->causal;
+  out->mask.has_kv_len = 1;
+  out->mask.has_q_len = 1;
+  out->mask.offset_from_lengths = 1;
+  out->lay.packed = 1;
+  for (int b = 0; b <= v->B; ++b) {
+    out->lay.cu_q[b] = v->cu_seqlens_q[b];
+    out->lay.cu_k[b] = v->cu_seqlens_k[b];
+  }
+  out->total_q = v->cu_seqlens_q[v->B];
+  out->total_k = v->cu_seqlens_k[v->B];
+  out->lay.total_q = out->total_q;
+  // Grid extents from the longest sequence (at least one tile).
+  out->shape = attn_shape{v->B, v->Hq, v->Hkv, std::max(max_q, 1), std::max(max_k, 1), v->d_h, v->d_v};
+  if ((static_cast<int64_t>(out->shape.n_k) + 127) / 128 > 65535) return ATTN_ERR_SHAPE;
+  if ((static_cast<int64_t>(out->shape.n_q) + 127) / 128 > 65535) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -146,6 +198,36 @@ bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
 // 3-D view [bh][n][d] of the fp32 dQ accumulator for TMA reduce-add in
 // 32-row x 32-column boxes (128-byte rows, 128-byte swizzle); rows beyond n
 // of a head are clipped.
+// Token-major view [T][H][d] (packed sequences) of a 2-byte tensor: dims
+// (d, H, T), boxes of 64 columns x 1 head x 128 tokens, which land in
+// shared memory exactly like the padded view's 128-row x 64-col boxes.
+// Tokens past T read as zeros.
+bool make_tmap_packed(CUtensorMap* map, const void* ptr, int d, int H, int64_t T) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same token-major view of the fp32 dQ accumulator, in boxes of 32
+// columns x 1 head x 32 tokens for TMA reduce-add.
+bool make_tmap_acc_packed(CUtensorMap* map, const void* ptr, int d, int H, int64_t T) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_acc(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -217,8 +299,9 @@ struct Workspace {
   size_t bytes;
 };
 
-Workspace workspace_layout(const attn_shape* s, void* base) {
-  const size_t rows = static_cast<size_t>(q_rows(s));
+// rows: query rows over all heads (B Hq n_q padded, T_q Hq packed); the
+// tile bounds are indexed [B Hq][ceil(n_q / 128)] in both layouts.
+Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base) {
   const size_t nqt = (static_cast<size_t>(s->n_q) + 127) / 128;
   const size_t tiles = static_cast<size_t>(s->B) * s->Hq * nqt;
   const size_t off_t = round256(rows * sizeof(float));
@@ -232,6 +315,14 @@ Workspace workspace_layout(const attn_shape* s, void* base) {
   w.Q16 = b + off_q;
   w.bytes = off_q + round256(rows * static_cast<size_t>(s->d_h) * 2);
   return w;
+}
+
+Workspace workspace_layout(const attn_shape* s, void* base) {
+  return workspace_layout_rows(s, static_cast<size_t>(q_rows(s)), base);
+}
+
+Workspace workspace_layout_varlen(const Varlen& v, void* base) {
+  return workspace_layout_rows(&v.shape, static_cast<size_t>(v.total_q) * v.shape.Hq, base);
 }
 
 int check_workspace(const attn_shape* s, const void* ws, size_t bytes) {
@@ -384,6 +475,7 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
       !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk))
     return ATTN_ERR_CUDA;
   p.sh = shape_params(shape);
+  std::memset(&p.lay, 0, sizeof(p.lay));
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
   p.O = O;
@@ -457,9 +549,13 @@ int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O, c
   rc = device_status_ptr(&status);
   if (rc) return rc;
   const Workspace w = workspace_layout(shape, workspace);
-  const cudaError_t e = launch_attn_bwd_preprocess(static_cast<int64_t>(shape->B) * shape->Hq, shape->n_q,
-                                                   shape->d_v, shape->d_h, Q, O, O_lo, dO, w.D, w.tilemax, w.dQacc,
-                                                   w.Q16, static_cast<cudaStream_t>(stream));
+  MaskParams no_mask;
+  LayoutParams padded;
+  std::memset(&no_mask, 0, sizeof(no_mask));
+  std::memset(&padded, 0, sizeof(padded));
+  const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), no_mask, padded, shape->d_v, shape->d_h, Q,
+                                                   O, O_lo, dO, w.D, w.tilemax, w.dQacc, w.Q16,
+                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -489,6 +585,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
       !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
     return ATTN_ERR_CUDA;
   p.sh = shape_params(shape);
+  std::memset(&p.lay, 0, sizeof(p.lay));
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
@@ -598,5 +695,121 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale
 }
 
 size_t attn_bwd_noalloc_max_scratch_bytes(void) { return kStaticBwdScratchBytes; }
+
+// ---------------------------------------------------------------------------
+// Packed variable-length sequences: the same kernels, addressing rows through
+// the token offsets (LayoutParams) and the per-sequence lengths (MaskParams).
+// ---------------------------------------------------------------------------
+int64_t attn_varlen_visible_pairs(const attn_varlen* v) {
+  Varlen d;
+  if (build_varlen(v, &d) != ATTN_OK) return -1;
+  int64_t total = 0;
+  for (int b = 0; b < v->B; ++b) total += pairs_one_batch(d.mask, d.shape.n_q, d.shape.n_k, b);
+  return total * v->Hq;
+}
+
+int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V, void* O,
+                    float* LSE, void* O_lo, void* stream) {
+  Varlen d;
+  int rc = build_varlen(v, &d);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  if (d.total_q == 0) return ATTN_OK;   // no query rows: nothing to write
+  rc = check_ptrs({Q, K, V, O, LSE});
+  if (rc) return rc;
+  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+  // ---- CUDA from here on ----
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q) || !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k) ||
+      !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k))
+    return ATTN_ERR_CUDA;
+  FwdParams p;
+  p.sh = shape_params(&d.shape);
+  p.mask = d.mask;
+  p.lay = d.lay;
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.O = O;
+  p.O_lo = O_lo;
+  p.LSE = LSE;
+  p.status = status;
+  const cudaError_t e = launch_attn_fwd(v->d_h, v->d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v) {
+  Varlen d;
+  if (build_varlen(v, &d) != ATTN_OK) return 0;
+  return workspace_layout_varlen(d, nullptr).bytes;
+}
+
+int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
+                    const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ, void* dK,
+                    void* dV, void* workspace, size_t workspace_bytes, void* stream) {
+  Varlen d;
+  int rc = build_varlen(v, &d);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  if (d.total_k > 0) {
+    rc = check_ptrs({K, V, dK, dV});
+    if (rc) return rc;
+  }
+  if (d.total_q > 0) {
+    rc = check_ptrs({Q, O, dO, LSE, dQ});
+    if (rc) return rc;
+    if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+    const Workspace need = workspace_layout_varlen(d, nullptr);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need.bytes)
+      return ATTN_ERR_WORKSPACE;
+  }
+  // ---- CUDA from here on ----
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d.total_k == 0) return ATTN_OK;
+  if (d.total_q == 0) {
+    // No query sees any key: the gradients of K and V are zero.
+    if (cudaMemsetAsync(dK, 0, static_cast<size_t>(d.total_k) * v->Hkv * v->d_h * 2, st) != cudaSuccess ||
+        cudaMemsetAsync(dV, 0, static_cast<size_t>(d.total_k) * v->Hkv * v->d_v * 2, st) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  const Workspace w = workspace_layout_varlen(d, workspace);
+  const ShapeParams sh = shape_params(&d.shape);
+  cudaError_t e = launch_attn_bwd_preprocess(sh, d.mask, d.lay, v->d_v, v->d_h, Q, O, O_lo, dO, w.D, w.tilemax,
+                                             w.dQacc, w.Q16, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_tmap_packed(&tq, w.Q16, v->d_h, v->Hq, d.total_q) ||
+      !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k) || !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k) ||
+      !make_tmap_packed(&tdo, dO, v->d_v, v->Hq, d.total_q) ||
+      !make_tmap_acc_packed(&tdq, w.dQacc, v->d_h, v->Hq, d.total_q))
+    return ATTN_ERR_CUDA;
+  BwdParams p;
+  p.sh = sh;
+  p.mask = d.mask;
+  p.lay = d.lay;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.LSE = LSE;
+  p.D = w.D;
+  p.tilemax = w.tilemax;
+  p.nqt = (d.shape.n_q + 127) / 128;
+  p.dQacc = w.dQacc;
+  p.dK = dK;
+  p.dV = dV;
+  p.status = status;
+  e = launch_attn_bwd_main(v->d_h, v->d_v, tq, tk, tv, tdo, tdq, p, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = launch_attn_bwd_finalize(d.total_q * v->Hq * v->d_h, scale, w.dQacc, dQ, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 }  // extern "C"

@@ -146,7 +146,7 @@ __device__ __forceinline__ int ds_scale_exponent(float bound) {
   return e < -120 ? -120 : (e > 120 ? 120 : e);
 }
 
-template <int DH, int DV>
+template <int DH, int DV, bool PACKED>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -174,10 +174,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   const int hkv = bkv - b * p.sh.Hkv;
   const int64_t j0 = static_cast<int64_t>(blockIdx.y) * kTileN;
   const int64_t klen = key_len(p.mask, p.sh.n_k, b);
+  const int64_t nq_b = query_len(p.mask, p.sh.n_q, b);
   const int64_t i_first = first_row_seeing_key(p.mask, p.sh.n_q, p.sh.n_k, b, j0);
-  const int nqt = (p.sh.n_q + kTileM - 1) / kTileM;
+  const int nqt = static_cast<int>((nq_b + kTileM - 1) / kTileM);
   const int qt_first = static_cast<int>(i_first / kTileM);
-  const int per_head = (i_first < p.sh.n_q) ? (nqt - qt_first) : 0;
+  const int per_head = (i_first < nq_b) ? (nqt - qt_first) : 0;
+  // dK/dV rows this CTA writes: up to n_k in the padded layout (rows past
+  // kv_len get zeros); in the packed layout rows past the sequence belong to
+  // another one.
+  const int64_t k_row_end = PACKED ? klen : p.sh.n_k;
   const int total = per_head * p.sh.group;
   auto step_head = [&](int s) { return hkv * p.sh.group + s / per_head; };
   auto step_q0 = [&](int s) { return (qt_first + s % per_head) * kTileM; };
@@ -238,44 +243,43 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
       for (int s = 0; s < 2 && s < total; ++s) {
-        const int bhq2 = b * p.sh.Hq + step_head(s);
-        for (int c = 0; c < DH / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, step_q0(s), bhq2);
-        for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&tmdO, c * 64, step_q0(s), bhq2);
+        const TmaYZ yz = q_tma(PACKED, p.lay, p.sh.Hq, b, step_head(s), step_q0(s));
+        for (int c = 0; c < DH / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, yz.y, yz.z);
+        for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&tmdO, c * 64, yz.y, yz.z);
       }
+      const TmaYZ kyz = k_tma(PACKED, p.lay, p.sh.Hkv, b, hkv, static_cast<int>(j0));
       mbar_arrive_expect_tx(bar(C::kBarKV), C::kKTileBytes + C::kVTileBytes);
       for (int c = 0; c < DH / 64; ++c)
         tma_load_3d(sbase + C::kOffK + c * C::kBlockBytes, &tmK, bar(C::kBarKV), c * 64,
-                    static_cast<int32_t>(j0), bkv);
+                    kyz.y, kyz.z);
       for (int c = 0; c < DV / 64; ++c)
         tma_load_3d(sbase + C::kOffV + c * C::kBlockBytes, &tmV, bar(C::kBarKV), c * 64,
-                    static_cast<int32_t>(j0), bkv);
+                    kyz.y, kyz.z);
       int q_issued[2] = {0, 0}, do_issued = 0;
       for (int s = 0; s < total; ++s) {
         const int st = s & 1;
         const uint32_t ph = static_cast<uint32_t>(((s >> 1) & 1) ^ 1);
-        const int bhq = b * p.sh.Hq + step_head(s);
-        const int q0 = step_q0(s);
+        const TmaYZ yz = q_tma(PACKED, p.lay, p.sh.Hq, b, step_head(s), step_q0(s));
         if (!mbar_wait(bar(C::kBarQEmpty + st), ph, abort_flag, limit)) break;
         mbar_arrive_expect_tx(bar(C::kBarQFull + st), C::kQTileBytes);
         for (int c = 0; c < DH / 64; ++c)
           tma_load_3d(sbase + C::kOffQ + st * C::kQTileBytes + c * C::kBlockBytes, &tmQ,
-                      bar(C::kBarQFull + st), c * 64, q0, bhq);
+                      bar(C::kBarQFull + st), c * 64, yz.y, yz.z);
         ++q_issued[st];
         // One dO stage: dO(s) is read by dP(s) and dV(s) only, so the next
         // tile loads as soon as dV(s) is done, well before dP(s+1).
         if (s > 0 && !mbar_wait(bar(C::kBarDOEmpty), static_cast<uint32_t>((s - 1) & 1), abort_flag, limit)) break;
         mbar_arrive_expect_tx(bar(C::kBarDOFull), C::kDOTileBytes);
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sbase + C::kOffDO + c * C::kBlockBytes, &tmdO, bar(C::kBarDOFull), c * 64, q0, bhq);
+          tma_load_3d(sbase + C::kOffDO + c * C::kBlockBytes, &tmdO, bar(C::kBarDOFull), c * 64, yz.y, yz.z);
         ++do_issued;
         // Warm L2 with the tiles of step s + 2: their shared-memory stage is
         // only free once step s has finished, which leaves too little time to
         // hide a load from HBM.
         if (s + 2 < total) {
-          const int bhq2 = b * p.sh.Hq + step_head(s + 2);
-          const int q02 = step_q0(s + 2);
-          for (int c = 0; c < DH / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, q02, bhq2);
-          for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&tmdO, c * 64, q02, bhq2);
+          const TmaYZ yz2 = q_tma(PACKED, p.lay, p.sh.Hq, b, step_head(s + 2), step_q0(s + 2));
+          for (int c = 0; c < DH / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, yz2.y, yz2.z);
+          for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_3d(&tmdO, c * 64, yz2.y, yz2.z);
         }
       }
       if (*abort_flag) {
@@ -476,8 +480,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // dP 2^e - D 2^e.
     auto load_row_terms = [&](int s, float& nlse2, float& nd) {
       const int64_t i = static_cast<int64_t>(step_q0(s)) + 64 * h + tid;
-      const int64_t r = static_cast<int64_t>(b * p.sh.Hq + step_head(s)) * p.sh.n_q + i;
-      const bool in = tid < 64 && i < p.sh.n_q;
+      // Query rows past the sequence get LSE = -inf: their weights P, and so
+      // their dS and contributions to dK, dV, dQ, are exactly 0.
+      const bool in = tid < 64 && i < nq_b;
+      const int64_t r = in ? q_vec(PACKED, p.lay, p.sh.Hq, p.sh.n_q, b, step_head(s), i) : 0;
       nlse2 = in ? -p.LSE[r] * kLog2e : -INFINITY;
       nd = in ? -p.D[r] : 0.f;
     };
@@ -505,9 +511,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const int q0 = step_q0(s);
       // Column c (query q0 + c) is visible iff this key row is inside
       // kv_len and, when causal, q0 + c >= j - offset.
-      const int64_t cmin64 = p.mask.causal ? (j - p.mask.offset - q0) : INT64_MIN / 2;
+      const int64_t cmin64 = p.mask.causal ? (j - causal_offset(p.mask, b) - q0) : INT64_MIN / 2;
       const int cmin = cmin64 > kTileM ? kTileM + 1 : (cmin64 < -1 ? -1 : static_cast<int>(cmin64));
-      const bool need_mask = __any_sync(0xffffffffu, row_masked || cmin > 64 * h);
+      // Packed sequences: columns c >= cmax are query rows of the next
+      // sequence; their weights and dS are set to 0 outright.  (In the padded
+      // layout the rows past n_q read as zeros and carry LSE = -inf.)
+      const int64_t cmax64 = nq_b - q0;
+      const int cmax = (!PACKED || cmax64 > kTileM) ? kTileM : static_cast<int>(cmax64);
+      const bool need_mask =
+          __any_sync(0xffffffffu, row_masked || cmin > 64 * h || (PACKED && cmax < 64 * h + 64));
       ok = wait_all(C::kBarSFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
@@ -541,8 +553,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             float x0, x1;
             ffma2(x0, x1, s0, s1, sl2, sl2, nl[k], nl[k + 1]);
             if (need_mask) {
-              x0 = (!row_masked && c >= cmin) ? x0 : -INFINITY;
-              x1 = (!row_masked && c + 1 >= cmin) ? x1 : -INFINITY;
+              x0 = (!row_masked && c >= cmin && (!PACKED || c < cmax)) ? x0 : -INFINITY;
+              x1 = (!row_masked && c + 1 >= cmin && (!PACKED || c + 1 < cmax)) ? x1 : -INFINITY;
             }
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             w[k >> 1] = pack_bf16x2(p0, p1);
@@ -588,8 +600,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint32_t pp = pw[cq * 8 + (k >> 1)];
             fmul2(d0, d1, f16_lo(pp), f16_hi(pp), t0, t1);
             if (need_mask) {
-              d0 = (!row_masked && c >= cmin) ? d0 : 0.f;
-              d1 = (!row_masked && c + 1 >= cmin) ? d1 : 0.f;
+              d0 = (!row_masked && c >= cmin && (!PACKED || c < cmax)) ? d0 : 0.f;
+              d1 = (!row_masked && c + 1 >= cmin && (!PACKED || c + 1 < cmax)) ? d1 : 0.f;
             }
             w[k >> 1] = pack_f16x2(d0, d1);
           }
@@ -664,14 +676,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             make_float4(__uint_as_float(v[4 * c]) * inv_scale, __uint_as_float(v[4 * c + 1]) * inv_scale,
                         __uint_as_float(v[4 * c + 2]) * inv_scale, __uint_as_float(v[4 * c + 3]) * inv_scale);
     };
-    auto reduce_round = [&](uint8_t* wstage, int first_box, int row0, int bhq) {
+    auto reduce_round = [&](uint8_t* wstage, int first_box, int row0, int head) {
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && row0 < p.sh.n_q) {
+      if (lane == 0 && row0 < nq_b) {
+        // (Rows of the box past the sequence hold zeros: adding them is a
+        // no-op on whatever rows lie there.)
+        const TmaYZ yz = q_tma(PACKED, p.lay, p.sh.Hq, b, head, row0);
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
-          tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), (first_box + bx) * C::kDQBoxCols, row0,
-                            bhq);
+          tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), (first_box + bx) * C::kDQBoxCols, yz.y,
+                            yz.z);
         bulk_commit_group();
       }
     };
@@ -683,7 +698,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       __syncwarp();
     };
     for (int s = 0; s < total && ok; ++s) {
-      const int bhq = b * p.sh.Hq + step_head(s);
+      const int head = step_head(s);
       const int q0 = step_q0(s);
       const int row0 = q0 + static_cast<int>(quad) * 32;
       ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(s & 1));
@@ -707,7 +722,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         staging_free();
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, v[bx]);
-        reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, bhq);
+        reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, head);
       }
       __syncwarp();
     }
@@ -718,8 +733,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     if (ok) {
       const int64_t j = j0 + row;
-      const bool in = j < p.sh.n_k;
-      const int64_t krow = static_cast<int64_t>(bkv) * p.sh.n_k + j;
+      const bool in = j < k_row_end;
+      const int64_t krow = k_row(PACKED, p.lay, p.sh.Hkv, p.sh.n_k, b, hkv, j);
       uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + krow * DH);
       uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + krow * DV);
       const float dk_scale = p.scale * inv_scale;
@@ -843,6 +858,105 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
   }
 }
 
+// The same for packed sequences (token-major rows, per-sequence lengths):
+// one block per 128-row query tile of one (sequence, query head), two threads
+// per row:
+//   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
+//   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
+// the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
+// are re-encoded as fp16 for the main kernel (exact for |q| <= 65504,
+// saturating beyond).
+// Row addressing for packed sequences: row i of (b, h) is token cu_q[b] + i;
+// rows past the sequence's length are left alone.
+struct PrepPacked {
+  int32_t n_q, Hq;
+  int64_t total_q;
+  int32_t cu_q[ATTN_MAX_BATCH + 1];
+  static constexpr bool kPacked = true;
+  __device__ __forceinline__ int64_t len(int b) const { return static_cast<int64_t>(cu_q[b + 1]) - cu_q[b]; }
+  __device__ __forceinline__ int64_t row(int b, int h, int64_t i) const {
+    return (static_cast<int64_t>(cu_q[b]) + i) * Hq + h;
+  }
+  __device__ __forceinline__ int64_t vec(int b, int h, int64_t i) const {
+    return static_cast<int64_t>(h) * total_q + cu_q[b] + i;
+  }
+};
+
+template <int DV, int DH>
+__global__ void __launch_bounds__(256)
+attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt, const uint4* __restrict__ Q,
+                           const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
+                           const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
+                           float4* __restrict__ dQacc, uint4* __restrict__ Q16) {
+  constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
+  __shared__ float red[2][8];
+  const int64_t bh = blockIdx.x;
+  const int b = static_cast<int>(bh / rm.Hq);
+  const int h = static_cast<int>(bh - static_cast<int64_t>(b) * rm.Hq);
+  const int qt = blockIdx.y;
+  const int64_t nq_b = rm.len(b);
+  const int r = static_cast<int>(threadIdx.x >> 1), half = static_cast<int>(threadIdx.x & 1);
+  const int64_t i = static_cast<int64_t>(qt) * kTileM + r;
+  const bool valid = i < nq_b;
+  const int64_t row = valid ? rm.row(b, h, i) : 0;
+  float acc = 0.f, nrm = 0.f;
+  if (valid) {
+    const int64_t base = row * (DV / 8) + half * kChunks;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 a = O[base + c];
+      const uint4 g = dO[base + c];
+      const uint4 lo = O_lo ? O_lo[base + c] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+        acc = fmaf(bf16_lo(aw[k]) + bf16_lo(lw[k]), g0, acc);
+        acc = fmaf(bf16_hi(aw[k]) + bf16_hi(lw[k]), g1, acc);
+        nrm = fmaf(g0, g0, nrm);
+        nrm = fmaf(g1, g1, nrm);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  nrm += __shfl_xor_sync(0xffffffffu, nrm, 1);
+  if (valid && half == 0) D[rm.vec(b, h, i)] = acc;
+  float mn = valid ? sqrtf(nrm) : 0.f, md = valid ? fabsf(acc) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = mn;
+    red[1][threadIdx.x >> 5] = md;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.f, c = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      a = fmaxf(a, red[0][w]);
+      c = fmaxf(c, red[1][w]);
+    }
+    tilemax[bh * nqt + qt] = make_float2(a, c);
+  }
+  const int64_t i0 = static_cast<int64_t>(qt) * kTileM;
+  const int rows_here = static_cast<int>(nq_b - i0 < kTileM ? (nq_b - i0 < 0 ? 0 : nq_b - i0) : kTileM);
+  {
+    for (int k = threadIdx.x; k < rows_here * (DH / 4); k += 256) {
+      const int rr = k / (DH / 4), cc = k - rr * (DH / 4);
+      dQacc[rm.row(b, h, i0 + rr) * (DH / 4) + cc] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k = threadIdx.x; k < rows_here * (DH / 8); k += 256) {
+      const int rr = k / (DH / 8), cc = k - rr * (DH / 8);
+      const int64_t at = rm.row(b, h, i0 + rr) * (DH / 8) + cc;
+      const uint4 u = Q[at];
+      Q16[at] =
+          make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+    }
+  }
+}
+
 // dQ = scale * acc, eight elements per thread per iteration.
 __global__ void __launch_bounds__(256)
 attn_bwd_finalize_kernel(int64_t n8, float scale, const float4* __restrict__ acc, uint4* __restrict__ dQ) {
@@ -860,7 +974,7 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
                               const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdParams& p,
                               cudaStream_t stream) {
   using C = BwdCfg<DH, DV>;
-  auto kern = attn_bwd_main_kernel<DH, DV>;
+  auto kern = p.lay.packed ? attn_bwd_main_kernel<DH, DV, true> : attn_bwd_main_kernel<DH, DV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN));
@@ -876,12 +990,26 @@ int grid_for(int64_t work_threads) {
 }
 
 template <int DV, int DH>
-void launch_pre_t(int64_t bhq, int n_q, int nqt, const void* Q, const void* O, const void* O_lo, const void* dO,
-                  float* D, float2* tilemax, float* dQacc, void* Q16, cudaStream_t stream) {
-  dim3 grid(static_cast<unsigned>(bhq), static_cast<unsigned>(nqt));
-  attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(
-      n_q, nqt, static_cast<const uint4*>(Q), static_cast<const uint4*>(O), static_cast<const uint4*>(O_lo),
-      static_cast<const uint4*>(dO), D, tilemax, reinterpret_cast<float4*>(dQacc), static_cast<uint4*>(Q16));
+void launch_pre_t(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay, int nqt, const void* Q,
+                  const void* O, const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
+                  void* Q16, cudaStream_t stream) {
+  (void)mask;
+  dim3 grid(static_cast<unsigned>(static_cast<int64_t>(sh.B) * sh.Hq), static_cast<unsigned>(nqt));
+  const uint4 *q = static_cast<const uint4*>(Q), *o = static_cast<const uint4*>(O);
+  const uint4 *olo = static_cast<const uint4*>(O_lo), *g = static_cast<const uint4*>(dO);
+  float4* acc = reinterpret_cast<float4*>(dQacc);
+  uint4* q16 = static_cast<uint4*>(Q16);
+  if (!lay.packed) {
+    attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, q, o, olo, g, D, tilemax, acc, q16);
+  } else {
+    PrepPacked rm;
+    rm.n_q = sh.n_q;
+    rm.Hq = sh.Hq;
+    rm.total_q = lay.total_q;
+    for (int b = 0; b <= sh.B; ++b) rm.cu_q[b] = lay.cu_q[b];
+    attn_bwd_preprocess_packed_kernel<DV, DH><<<grid, 256, 0, stream>>>(rm, nqt, q, o, olo, g, D, tilemax, acc,
+                                                                        q16);
+  }
 }
 
 }  // namespace
@@ -895,16 +1023,17 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* Q, const void* O,
-                                       const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
-                                       void* Q16, cudaStream_t stream) {
-  const int nqt = (n_q + kTileM - 1) / kTileM;
+cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay,
+                                       int dv, int dh, const void* Q, const void* O, const void* O_lo,
+                                       const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
+                                       cudaStream_t stream) {
+  const int nqt = (sh.n_q + kTileM - 1) / kTileM;
   if (dv == 128 && dh == 128)
-    launch_pre_t<128, 128>(bhq, n_q, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
+    launch_pre_t<128, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
   else if (dv == 64 && dh == 64)
-    launch_pre_t<64, 64>(bhq, n_q, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
+    launch_pre_t<64, 64>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
   else if (dv == 64 && dh == 128)
-    launch_pre_t<64, 128>(bhq, n_q, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
+    launch_pre_t<64, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -17,15 +17,14 @@
 //   warp 1      MMA issuer (lane 0 alone waits and issues): S_t = Q_t K_j^T
 //               into tensor memory, O_t += P_t V_j with P_t read back from
 //               tensor memory.
-//   warp 2      zeroes the padded key rows of a V tile before its PV product
-//               (only tiles that hold rows in [kv_len, n_k)), on request of
-//               the MMA thread once that tile has landed.
+//   warps 2, 3  re-encode every V tile as fp16 in place once it has landed,
+//               zeroing its padded key rows (rows in [kv_len, n_k)).
 //   warps 4-7   softmax for query tile 0 (thread = row = TMEM lane).
 //   warps 8-11  softmax for query tile 1.
 // While one tile's softmax runs, the tensor core works on the other tile.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
-//   [t*128, t*128+128)   S_t (fp32); P_t (bf16 pairs) overwrites its first
+//   [t*128, t*128+128)   S_t (fp32); P_t (fp16 pairs) overwrites its first
 //                        64 columns once the scores are consumed.
 //   [256 + t*DV, ...)    O_t accumulator (fp32).
 //
@@ -35,8 +34,16 @@
 // always use the same reference, so the result is unchanged in real
 // arithmetic and no term exceeds 2^8 before normalisation.  The weight of
 // the dominant key is then 2^d with d in [0, 8) rather than exactly 1, and
-// its bf16 rounding would leave a 2^-9 relative error in O; normalising by
-// the sum of the rounded weights removes it (the LSE keeps the exact sum).
+// its rounding would leave a relative error in O; normalising by the sum of
+// the rounded weights removes it (the LSE keeps the exact sum).
+//
+// The PV product runs in fp16 (weights P and V both re-encoded; V exactly
+// for |v| <= 65504, P <= 2^8 by the lazy maximum): the backward rebuilds the
+// weights exactly and takes its row term from this O (c_i = sum_l dO_il O_il,
+// eq. A.10.7), so O must be the product of nearly exact weights.  With bf16
+// weights (8 significant bits) the two differ by about 2^-9 of
+// sum_j P_ij |dP_ij|, which for a sharply peaked row moved dQ past the
+// tolerance; fp16 (11 bits) shrinks that eightfold.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -66,9 +73,8 @@ struct FwdCfg {
   static constexpr int kBarKEmpty = kBarKFull + kKStages;
   static constexpr int kBarVFull = kBarKEmpty + kKStages;
   static constexpr int kBarVEmpty = kBarVFull + kVStages;
-  static constexpr int kBarZeroReq = kBarVEmpty + kVStages;  // MMA thread: zero this V tile's padding
-  static constexpr int kBarZeroed = kBarZeroReq + 1;          // warp 2: done
-  static constexpr int kBarSFull = kBarZeroed + 1;            // [2]
+  static constexpr int kBarVReady = kBarVEmpty + kVStages;   // [kVStages] V tile re-encoded as fp16
+  static constexpr int kBarSFull = kBarVReady + kVStages;    // [2]
   static constexpr int kBarPReady = kBarSFull + 2;          // [2]
   static constexpr int kBarOFull = kBarPReady + 2;          // [2]
   static constexpr int kBarDrain = kBarOFull + 2;
@@ -85,7 +91,7 @@ struct FwdCfg {
   static_assert(2 * 128 + 2 * DV <= 512, "tensor memory budget");
 };
 
-template <int DH, int DV>
+template <int DH, int DV, bool PACKED>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
@@ -105,7 +111,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int bh = blockIdx.x;                        // b * Hq + r
   const int b = bh / p.sh.Hq;
   const int r = bh - b * p.sh.Hq;
-  const int bkv = b * p.sh.Hkv + r / p.sh.group;    // g(r) = r / (Hq / Hkv)
+  const int hkv = r / p.sh.group;                   // g(r) = r / (Hq / Hkv)
+  // Key rows past the sequence: up to n_k in the padded layout; in the packed
+  // layout every row of a tile past kv_len belongs to another sequence.
+  const int row_end = PACKED ? INT32_MAX : p.sh.n_k;
   const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy first
   int q0[2], ntiles[2];
 #pragma unroll
@@ -126,8 +135,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarVEmpty + s), 1);
     }
-    mbar_init(bar(C::kBarZeroReq), 1);
-    mbar_init(bar(C::kBarZeroed), 1);
+    for (int s = 0; s < C::kVStages; ++s) mbar_init(bar(C::kBarVReady + s), 2);   // warps 2 and 3
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
       mbar_init(bar(C::kBarPReady + t), 128);
@@ -158,11 +166,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
+      TmaYZ qyz[2];
+      for (int t = 0; t < C::kQTiles; ++t) qyz[t] = q_tma(PACKED, p.lay, p.sh.Hq, b, r, q0[t]);
       mbar_arrive_expect_tx(bar(C::kBarQFull), C::kQTiles * C::kQTileBytes);
       for (int t = 0; t < C::kQTiles; ++t)
         for (int c = 0; c < DH / 64; ++c)
           tma_load_3d(sbase + C::kOffQ + t * C::kQTileBytes + c * C::kBlockBytes, &tmQ,
-                      bar(C::kBarQFull), c * 64, q0[t], bh);
+                      bar(C::kBarQFull), c * 64, qyz[t].y, qyz[t].z);
       int k_issued[C::kKStages > C::kVStages ? C::kKStages : C::kVStages] = {};
       int v_issued[C::kKStages > C::kVStages ? C::kKStages : C::kVStages] = {};
       bool ok = true;
@@ -172,9 +182,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = mbar_wait(bar(C::kBarKEmpty + ks), kph ^ 1u, abort_flag, limit);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kKTileBytes);
+        const TmaYZ kyz = k_tma(PACKED, p.lay, p.sh.Hkv, b, hkv, j * kTileN);
         for (int c = 0; c < DH / 64; ++c)
           tma_load_3d(sbase + C::kOffK + ks * C::kKTileBytes + c * C::kBlockBytes, &tmK,
-                      bar(C::kBarKFull + ks), c * 64, j * kTileN, bkv);
+                      bar(C::kBarKFull + ks), c * 64, kyz.y, kyz.z);
         ++k_issued[ks];
         const int vs = j % C::kVStages;
         const uint32_t vph = static_cast<uint32_t>((j / C::kVStages) & 1);
@@ -183,7 +194,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kVTileBytes);
         for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(sbase + C::kOffV + vs * C::kVTileBytes + c * C::kBlockBytes, &tmV,
-                      bar(C::kBarVFull + vs), c * 64, j * kTileN, bkv);
+                      bar(C::kBarVFull + vs), c * 64, kyz.y, kyz.z);
         ++v_issued[vs];
       }
       if (*abort_flag) {
@@ -196,36 +207,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           if (v_issued[s]) mbar_wait(bar(C::kBarVFull + s), (v_issued[s] - 1) & 1, &no_abort, limit);
       }
     }
-  } else if (warp == 2) {
-    // ===================== zero padded V rows =====================
-    // Key rows in [kv_len, n_k) hold caller memory that may be anything
-    // (even NaN); their weights are exactly 0, but 0 * NaN would still
-    // poison O, so those V rows are zeroed before the PV product.  Rows at
-    // or beyond n_k arrive as zeros from the TMA bounds check.
-    // The request comes from the MMA thread after it has seen the tile land,
-    // and it waits for the reply before it asks again, so the two barriers
-    // never run more than one phase apart.
-    if (*abort_flag == 0) {
-      uint32_t z = 0;
-      for (int j = 0; j < nkv; ++j) {
-        int r0, r1;
-        if (!padded_rows(p.mask, p.sh.n_k, b, j, r0, r1)) continue;
-        const int vs = j % C::kVStages;
-        const bool w = mbar_wait(bar(C::kBarZeroReq), z & 1u, abort_flag, limit);
-        if (!__all_sync(0xffffffffu, w)) break;
-        ++z;
-        uint8_t* vbase = smem + C::kOffV + vs * C::kVTileBytes;
-        const int chunks = (r1 - r0) * (DV / 64) * 8;   // 16-byte chunks
-        for (int q = static_cast<int>(lane); q < chunks; q += 32) {
-          const int row = r0 + q / ((DV / 64) * 8);
-          const int rem = q % ((DV / 64) * 8);
-          *reinterpret_cast<uint4*>(vbase + (rem / 8) * C::kBlockBytes + row * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBarZeroed));
+  } else if (warp == 2 || warp == 3) {
+    // =================== V tiles to fp16 (in place) ===================
+    // Every V tile, in order: the next load into a stage waits for the PV
+    // product that follows this conversion, so the full barrier cannot run a
+    // phase ahead of these warps.  Key rows in [kv_len, n_k) hold caller
+    // memory that may be anything (even NaN): their weights are exactly 0,
+    // but 0 * NaN would still poison O, so they become zeros.  Rows at or
+    // beyond n_k arrive as zeros from the TMA bounds check.
+    const int t64 = static_cast<int>(threadIdx.x) - 64;   // 0..63
+    bool ok = *abort_flag == 0;
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int vs = j % C::kVStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVFull + vs), static_cast<uint32_t>((j / C::kVStages) & 1),
+                                             abort_flag, limit));
+      if (!ok) break;
+      int r0 = kTileN, r1 = kTileN;
+      padded_rows(p.mask, row_end, b, j, r0, r1);
+      uint4* vt = reinterpret_cast<uint4*>(smem + C::kOffV + vs * C::kVTileBytes);
+#pragma unroll 4
+      for (int q = t64; q < C::kVTileBytes / 16; q += 64) {
+        const int row = (q % (C::kBlockBytes / 16)) / 8;   // 8 chunks of 16 bytes per 128-byte row
+        const uint4 u = vt[q];
+        vt[q] = (row >= r0 && row < r1)
+                    ? make_uint4(0u, 0u, 0u, 0u)
+                    : make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z),
+                                 bf16x2_to_f16x2(u.w));
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarVReady + vs));
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
@@ -234,7 +245,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // reconvergence points sit between them.
     if (lane == 0 && *abort_flag == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, false, true);
+      constexpr uint32_t kIdescPV = idesc_f16_f32(128, DV, false, true);   // fp16 P and V
       // Shared-memory descriptors as base words plus constant steps: the
       // softmax warps sharing this sub-partition take most issue slots, so
       // every instruction between two MMAs delays the tensor core.
@@ -271,16 +282,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           umma_commit(bar(C::kBarKEmpty + 0));
         }
       }
-      uint32_t z = 0;   // padded tiles handed to warp 2 so far
       for (int j = 0; j < nkv && ok; ++j) {
         const int vs = j % C::kVStages;
-        ok = wait1(C::kBarVFull + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
-        int r0, r1;
-        if (ok && padded_rows(p.mask, p.sh.n_k, b, j, r0, r1)) {
-          mbar_arrive(bar(C::kBarZeroReq));
-          ok = wait1(C::kBarZeroed, z & 1u);
-          ++z;
-        }
+        ok = wait1(C::kBarVReady + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
         if (!ok) break;
         const int kn = (j + 1) % C::kKStages;
         bool k_next_ready = false;
@@ -327,7 +331,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;   // reference maximum, exp2 domain
     float l_sum = 0.f;         // sum of the weights p (for the LSE)
-    float l_used = 0.f;        // sum of the bf16-rounded weights the PV product used
+    float l_used = 0.f;        // sum of the fp16-rounded weights the PV product used
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
     for (int j = 0; j < ntiles[t] && ok; ++j) {
@@ -386,7 +390,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // P = exp2(S scale log2e - m_ref) -> bf16 pairs into tensor memory
+      // P = exp2(S scale log2e - m_ref) -> fp16 pairs into tensor memory
       // (over the first 64 columns of S, all of which are in registers).
       float ls[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, lu[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
@@ -397,9 +401,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           float x0, x1;
           ffma2(x0, x1, __uint_as_float(sc[c][k]), __uint_as_float(sc[c][k + 1]), sl2, sl2, nm, nm);
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          const uint32_t w = pack_bf16x2(p0, p1);
+          const uint32_t w = pack_f16x2(p0, p1);
           fadd2(ls[c & 1][0], ls[c & 1][1], p0, p1);
-          fadd2(lu[c & 1][0], lu[c & 1][1], bf16_lo(w), bf16_hi(w));
+          fadd2(lu[c & 1][0], lu[c & 1][1], f16_lo(w), f16_hi(w));
           pw[k >> 1] = w;
         }
         tmem_st16_nowait(tS + c * 16, pw);
@@ -417,12 +421,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after_sync();
       if (ok) {
         // O is normalised by the sum of the weights the PV product actually
-        // used (their bf16 roundings), so each output row is an exact convex
+        // used (their fp16 roundings), so each output row is an exact convex
         // combination of V rows up to fp32 accumulation; the LSE keeps the
         // unrounded sum.
         const float inv_l = l_used > 0.f ? 1.0f / l_used : 0.f;
-        const bool in_range = i < p.sh.n_q;
-        const int64_t row_off = (static_cast<int64_t>(bh) * p.sh.n_q + i) * DV;
+        const bool in_range = i < query_len(p.mask, p.sh.n_q, b);
+        const int64_t row_off = q_row(PACKED, p.lay, p.sh.Hq, p.sh.n_q, b, r, i) * DV;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + row_off);
         uint4* lorow = p.O_lo ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O_lo) + row_off) : nullptr;
 #pragma unroll
@@ -447,7 +451,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
         if (in_range)
-          p.LSE[static_cast<int64_t>(bh) * p.sh.n_q + i] = (m_ref + fast_log2(l_sum)) * kLn2;
+          p.LSE[q_vec(PACKED, p.lay, p.sh.Hq, p.sh.n_q, b, r, i)] = (m_ref + fast_log2(l_sum)) * kLn2;
       }
     }
   }
@@ -466,7 +470,7 @@ template <int DH, int DV>
 cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<DH, DV>;
-  auto kern = attn_fwd_kernel<DH, DV>;
+  auto kern = p.lay.packed ? attn_fwd_kernel<DH, DV, true> : attn_fwd_kernel<DH, DV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int pairs = (p.sh.n_q + 2 * kTileM - 1) / (2 * kTileM);

@@ -4,9 +4,12 @@
 // Visible set ("Appendix A.10 -- Attention matrices and backpropagation",
 // eq. A.10.1 and section A.10.6; "Chapter 31 -- attention backprop",
 // section 1 for n_q != n_k): key j is visible to query row i of batch b iff
-//     j < kv_len[b]   and, when causal,   j <= i + offset.
-// Both conditions are upper bounds on j, so each row has a single key limit
-//     lim(b, i) = min(kv_len[b], causal ? i + offset + 1 : n_k)
+//     j < kv_len[b]   and, when causal,   j <= i + offset(b),
+// for the rows i < q_len(b) that exist.  offset(b) is one offset for the
+// whole batch, or, for packed variable-length sequences, kv_len[b] - q_len[b]
+// (each sequence's last query aligned with its last key).  Both conditions
+// are upper bounds on j, so each row has a single key limit
+//     lim(b, i) = min(kv_len[b], causal ? i + offset(b) + 1 : n_k)
 // and j is visible iff j < lim(b, i).  lim is non-decreasing in i, which
 // makes whole-tile classification a pair of comparisons.
 #pragma once
@@ -28,6 +31,9 @@ struct MaskParams {
   int32_t has_kv_len;
   int64_t offset;                  // effective causal offset, clamped to [0, n_k]
   int32_t kv_len[ATTN_MAX_BATCH];  // valid when has_kv_len
+  int32_t has_q_len;               // rows i >= q_len[b] do not exist (packed sequences)
+  int32_t offset_from_lengths;     // causal offset(b) = kv_len[b] - q_len[b]
+  int32_t q_len[ATTN_MAX_BATCH];   // valid when has_q_len
 };
 
 struct ShapeParams {
@@ -38,12 +44,21 @@ __host__ __device__ __forceinline__ int64_t key_len(const MaskParams& m, int n_k
   return m.has_kv_len ? static_cast<int64_t>(m.kv_len[b]) : static_cast<int64_t>(n_k);
 }
 
+// Query rows of batch element b (n_q unless the rows are per-sequence).
+__host__ __device__ __forceinline__ int64_t query_len(const MaskParams& m, int n_q, int b) {
+  return m.has_q_len ? static_cast<int64_t>(m.q_len[b]) : static_cast<int64_t>(n_q);
+}
+
+__host__ __device__ __forceinline__ int64_t causal_offset(const MaskParams& m, int b) {
+  return m.offset_from_lengths ? static_cast<int64_t>(m.kv_len[b]) - m.q_len[b] : m.offset;
+}
+
 // lim(b, i): keys j < lim are visible to row i.
 __host__ __device__ __forceinline__ int64_t row_key_limit(const MaskParams& m, int n_k, int b,
                                                           int64_t i) {
   int64_t lim = key_len(m, n_k, b);
   if (m.causal) {
-    const int64_t c = i + m.offset + 1;
+    const int64_t c = i + causal_offset(m, b) + 1;
     lim = c < lim ? c : lim;
   }
   return lim;
@@ -53,20 +68,23 @@ __host__ __device__ __forceinline__ int64_t row_key_limit(const MaskParams& m, i
 // below the last row's limit is non-empty, every tile above is empty.
 __host__ __device__ __forceinline__ int kv_tiles_for_q_tile(const MaskParams& m, int n_q, int n_k,
                                                             int b, int64_t i0) {
-  if (i0 >= n_q) return 0;
+  const int64_t nq_b = query_len(m, n_q, b);
+  if (i0 >= nq_b) return 0;
   int64_t i_last = i0 + kTileM - 1;
-  if (i_last > n_q - 1) i_last = n_q - 1;
+  if (i_last > nq_b - 1) i_last = nq_b - 1;
   const int64_t lim = row_key_limit(m, n_k, b, i_last);
   if (lim <= 0) return 0;
   return static_cast<int>((lim + kTileN - 1) / kTileN);
 }
 
-// Rows [r0, r1) of key tile j (tile-relative) lie in [kv_len, n_k): rows
-// that hold caller memory but no visible key.  False when there are none.
-__host__ __device__ __forceinline__ bool padded_rows(const MaskParams& m, int n_k, int b, int j, int& r0,
+// Rows [r0, r1) of key tile j (tile-relative) lie in [kv_len, row_end):
+// rows that hold caller memory but no visible key (row_end = n_k for the
+// padded layout; for packed sequences the tile's rows past the sequence
+// belong to the next one, row_end = INT32_MAX).  False when there are none.
+__host__ __device__ __forceinline__ bool padded_rows(const MaskParams& m, int row_end, int b, int j, int& r0,
                                                      int& r1) {
   const int64_t j0 = static_cast<int64_t>(j) * kTileN;
-  int64_t lo = key_len(m, n_k, b) - j0, hi = static_cast<int64_t>(n_k) - j0;
+  int64_t lo = key_len(m, row_end, b) - j0, hi = static_cast<int64_t>(row_end) - j0;
   if (lo < 0) lo = 0;
   if (hi > kTileN) hi = kTileN;
   if (lo >= hi) return false;
@@ -79,16 +97,61 @@ __host__ __device__ __forceinline__ bool padded_rows(const MaskParams& m, int n_
 // n_q when no row does.
 __host__ __device__ __forceinline__ int64_t first_row_seeing_key(const MaskParams& m, int n_q,
                                                                  int n_k, int b, int64_t j0) {
-  if (j0 >= key_len(m, n_k, b)) return n_q;
+  const int64_t nq_b = query_len(m, n_q, b);
+  if (j0 >= key_len(m, n_k, b)) return nq_b;
   if (!m.causal) return 0;
-  int64_t i = j0 - m.offset;
+  int64_t i = j0 - causal_offset(m, b);
   if (i < 0) i = 0;
-  return i < n_q ? i : n_q;
+  return i < nq_b ? i : nq_b;
+}
+
+// Where the rows of a tensor live.  Padded layout: [B][H][n][d], row i of
+// (b, h) at (b H + h) n + i.  Packed variable-length sequences: [T][H][d]
+// with the tokens of sequence b at cu[b] .. cu[b+1] - 1, row i of (b, h) at
+// (cu[b] + i) H + h.  The backward's fp16 copy of Q and its fp32 dQ
+// accumulator follow the layout of Q; LSE and D are [B][H][n] (padded) or
+// [H][T] (packed).
+struct LayoutParams {
+  int32_t packed;
+  int32_t cu_q[ATTN_MAX_BATCH + 1];   // packed: first query token of sequence b
+  int32_t cu_k[ATTN_MAX_BATCH + 1];   // packed: first key token of sequence b
+  int64_t total_q;                    // packed: query tokens
+};
+
+// The helpers take the layout kind as their first argument: the kernels are
+// compiled once per kind and pass it as a constant, so the padded layout's
+// index arithmetic carries no trace of the packed one.
+// Element row (in units of the row width) of query row i of (b, h).
+__host__ __device__ __forceinline__ int64_t q_row(bool packed, const LayoutParams& L, int Hq, int n_q, int b, int h,
+                                                  int64_t i) {
+  return packed ? (static_cast<int64_t>(L.cu_q[b]) + i) * Hq + h : (static_cast<int64_t>(b) * Hq + h) * n_q + i;
+}
+__host__ __device__ __forceinline__ int64_t k_row(bool packed, const LayoutParams& L, int Hkv, int n_k, int b, int h,
+                                                  int64_t j) {
+  return packed ? (static_cast<int64_t>(L.cu_k[b]) + j) * Hkv + h : (static_cast<int64_t>(b) * Hkv + h) * n_k + j;
+}
+// Index of the LSE / D entry of query row i of (b, h).
+__host__ __device__ __forceinline__ int64_t q_vec(bool packed, const LayoutParams& L, int Hq, int n_q, int b, int h,
+                                                  int64_t i) {
+  return packed ? static_cast<int64_t>(h) * L.total_q + L.cu_q[b] + i : (static_cast<int64_t>(b) * Hq + h) * n_q + i;
+}
+// TMA coordinates (y, z) of row i of (b, h) in the 3-D view of a tensor:
+// padded views are [B H][n][d] (y = row, z = b H + h), packed views
+// [T][H][d] (y = head, z = token).
+struct TmaYZ {
+  int32_t y, z;
+};
+__device__ __forceinline__ TmaYZ q_tma(bool packed, const LayoutParams& L, int Hq, int b, int h, int i) {
+  return packed ? TmaYZ{h, L.cu_q[b] + i} : TmaYZ{i, b * Hq + h};
+}
+__device__ __forceinline__ TmaYZ k_tma(bool packed, const LayoutParams& L, int Hkv, int b, int h, int j) {
+  return packed ? TmaYZ{h, L.cu_k[b] + j} : TmaYZ{j, b * Hkv + h};
 }
 
 struct FwdParams {
   ShapeParams sh;
   MaskParams mask;
+  LayoutParams lay;
   float scale_log2;            // scale * log2(e)
   uint64_t wait_limit_ns;
   void* O;                     // bf16 [B][Hq][n_q][d_v]
@@ -100,13 +163,14 @@ struct FwdParams {
 struct BwdParams {
   ShapeParams sh;
   MaskParams mask;
+  LayoutParams lay;
   float scale;                 // raw scale (dK epilogue)
   float scale_log2;            // scale * log2(e)
   uint64_t wait_limit_ns;
   const float* LSE;            // fp32 [B][Hq][n_q]
   const float* D;              // fp32 [B][Hq][n_q]
-  const float2* tilemax;       // per 128-row query tile: (max ||dO_i||, max |D_i|)
-  int32_t nqt;                 // query tiles per head
+  const float2* tilemax;       // per 128-row query tile: (max ||dO_i||, max |D_i|), [B Hq][nqt]
+  int32_t nqt;                 // query tiles per head (of the longest sequence)
   float* dQacc;                // fp32 [B][Hq][n_q][d_h]
   void* dK;                    // bf16 [B][Hkv][n_k][d_h]
   void* dV;                    // bf16 [B][Hkv][n_k][d_v]
@@ -141,9 +205,10 @@ cudaError_t launch_attn_decode(int dh, int dv, const CUtensorMap& tmK, const CUt
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_attn_bwd_preprocess(int64_t bhq, int n_q, int dv, int dh, const void* Q, const void* O,
-                                       const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
-                                       void* Q16, cudaStream_t stream);
+cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay,
+                                       int dv, int dh, const void* Q, const void* O, const void* O_lo,
+                                       const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
+                                       cudaStream_t stream);
 cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
                                      cudaStream_t stream);
 

@@ -18,7 +18,7 @@ backpropagation").
 from __future__ import annotations
 
 from dataclasses import dataclass, replace
-from typing import Dict, Optional, Tuple
+from typing import Dict, List, Optional, Tuple
 
 import torch
 
@@ -115,3 +115,78 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> Inputs:
         kv_len = torch.randint(int(lo), int(hi) + 1, (w.B,), generator=g, dtype=torch.int64)
         kv_len = kv_len.to(torch.int32)
     return Inputs(Q, K, V, dO, kv_len)
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length sequences (token-major tensors)
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """Packed sequences: per-sequence query and key lengths, token-major
+    tensors Q [T_q, Hq, d_h], K [T_k, Hkv, d_h], V [T_k, Hkv, d_v],
+    dO [T_q, Hq, d_v].  With ``len_range`` set, lengths are drawn uniformly
+    on that inclusive range (the same length for queries and keys of a
+    sequence: packed self-attention); explicit ``lens_q`` / ``lens_k`` take
+    precedence."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    dh: int
+    dv: int
+    causal: bool = False
+    len_range: Optional[Tuple[int, int]] = None
+    lens_q: Optional[Tuple[int, ...]] = None
+    lens_k: Optional[Tuple[int, ...]] = None
+    sigma_qk: float = 1.0
+    sigma_v: float = 1.0
+    seed: int = 0
+
+
+@dataclass
+class VarlenInputs:
+    Q: torch.Tensor
+    K: torch.Tensor
+    V: torch.Tensor
+    dO: torch.Tensor
+    lens_q: List[int]
+    lens_k: List[int]
+    cu_q: List[int]
+    cu_k: List[int]
+
+
+def make_varlen_inputs(w: VarlenWorkload, seed: Optional[int] = None) -> VarlenInputs:
+    """Draw the lengths first (when drawn), then Q, K, V, dO as in make_inputs."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed if seed is None else seed))
+    if w.lens_q is not None:
+        lq = [int(x) for x in w.lens_q]
+        lk = [int(x) for x in (w.lens_k if w.lens_k is not None else w.lens_q)]
+    else:
+        lo, hi = w.len_range
+        lq = torch.randint(int(lo), int(hi) + 1, (w.B,), generator=g, dtype=torch.int64).tolist()
+        lk = list(lq)
+    cu_q, cu_k = [0], [0]
+    for a, b in zip(lq, lk):
+        cu_q.append(cu_q[-1] + a)
+        cu_k.append(cu_k[-1] + b)
+
+    def draw(shape, sigma):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x.mul_(sigma)
+        return x.to(torch.bfloat16).contiguous()
+
+    Q = draw((cu_q[-1], w.Hq, w.dh), w.sigma_qk)
+    K = draw((cu_k[-1], w.Hkv, w.dh), w.sigma_qk)
+    V = draw((cu_k[-1], w.Hkv, w.dv), w.sigma_v)
+    dO = draw((cu_q[-1], w.Hq, w.dv), w.sigma_v)
+    return VarlenInputs(Q, K, V, dO, lq, lk, cu_q, cu_k)
+
+
+# Packed causal GQA sequences of mixed lengths (a training batch without
+# padding): 16 sequences of 256..4096 tokens, 32 query heads over 8 KV heads.
+VARLEN_WORKLOADS: Dict[str, VarlenWorkload] = {
+    "varlen_gqa_causal": VarlenWorkload("varlen_gqa_causal", B=16, Hq=32, Hkv=8, dh=128, dv=128, causal=True,
+                                        len_range=(256, 4096), seed=1201),
+}

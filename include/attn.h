@@ -33,6 +33,7 @@
  *   Q, dQ   [B][Hq ][n_q][d_h]  bf16        K, dK [B][Hkv][n_k][d_h] bf16
  *   O, dO   [B][Hq ][n_q][d_v]  bf16        V, dV [B][Hkv][n_k][d_v] bf16
  *   LSE, D  [B][Hq ][n_q]       fp32
+ * (the packed variable-length entry points below use token-major tensors).
  * Supported head widths (d_h, d_v): (64, 64), (128, 128), (128, 64).
  * Every tensor pointer must be 16-byte aligned.
  *
@@ -61,7 +62,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -210,6 +211,50 @@ size_t attn_bwd_noalloc_max_scratch_bytes(void);
  * from the same closed form the kernels use to classify tiles; -1 on an
  * invalid shape or mask.  Host only. */
 int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask);
+
+/* Packed variable-length sequences: padding removed on both axes ("Appendix
+ * A.10", section A.10.6 removes padding positions from the keys; here the
+ * queries of each sequence are only its own).  Sequence b has
+ * len_q(b) = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries and
+ * len_k(b) = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys, stored token-major:
+ *   Q, dQ       [T_q][Hq ][d_h]  bf16     K, dK [T_k][Hkv][d_h] bf16
+ *   O, O_lo, dO [T_q][Hq ][d_v]  bf16     V, dV [T_k][Hkv][d_v] bf16
+ *   LSE         [Hq][T_q]        fp32
+ * with T_q = cu_seqlens_q[B], T_k = cu_seqlens_k[B]; query token cu_q[b] + i
+ * is row i of sequence b (the same for keys).  A single sequence with
+ * equal lengths is the [S][H][d] layout.  Visible set of row i of sequence
+ * b: V_i = { j < len_k(b) }, and when causal j <= i + len_k(b) - len_q(b)
+ * (each sequence's last query aligned with its last key).  A sequence with
+ * len_q(b) > 0 needs len_k(b) >= 1, and when causal len_k(b) >= len_q(b)
+ * (else its first rows are empty: ATTN_ERR_EMPTY_ROW); len_q(b) = 0 is
+ * allowed (that sequence's keys then get dK = dV = 0).  Same functions,
+ * precision, workspace rules and errors as attn_fwd / attn_bwd. */
+typedef struct {
+  int32_t B;                    /* sequences, 1..ATTN_MAX_BATCH                     */
+  int32_t Hq;                   /* query heads                                      */
+  int32_t Hkv;                  /* key/value heads; Hq % Hkv == 0                   */
+  int32_t d_h;                  /* query/key width                                  */
+  int32_t d_v;                  /* value width                                      */
+  int32_t causal;               /* 0 or 1 (bottom-right aligned per sequence)       */
+  const int32_t* cu_seqlens_q;  /* HOST [B+1]: 0 = cu[0] <= cu[1] <= ... <= cu[B]    */
+  const int32_t* cu_seqlens_k;  /* HOST [B+1], same rules                           */
+} attn_varlen;
+
+/* Visible (query, key) pairs over all sequences and query heads, -1 when
+ * the description is invalid. */
+int64_t attn_varlen_visible_pairs(const attn_varlen* v);
+
+int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
+                    void* O, float* LSE, void* O_lo, void* stream);
+
+/* Workspace of attn_bwd_varlen, about T_q*Hq*(6*d_h + 4) bytes; 0 when the
+ * description is invalid. */
+size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v);
+
+int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
+                    const void* O, const void* O_lo, const void* dO, const float* LSE,
+                    void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                    void* stream);
 
 /* Device status word of the current device: ATTN_OK, or the first failure a
  * kernel recorded (ATTN_ERR_TIMEOUT).  Synchronises the device.  Writes the

@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 3
+    assert esd.attn_abi_version() == 4
 
 
 def test_strerror_covers_every_code(lib):
@@ -164,3 +164,62 @@ def test_decode_entry_point_checks(lib):
     assert lib.attn_fwd_decode(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_fwd_decode(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_fwd_decode(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
+
+
+def _varlen(cq, ck, causal=0, Hq=4, Hkv=2, d_h=128, d_v=128, B=None):
+    B = len(cq) - 1 if B is None else B
+    aq = (ctypes.c_int32 * len(cq))(*cq)
+    ak = (ctypes.c_int32 * len(ck))(*ck)
+    v = bnd.AttnVarlen(B, Hq, Hkv, d_h, d_v, causal, ctypes.cast(aq, ctypes.POINTER(ctypes.c_int32)),
+                       ctypes.cast(ak, ctypes.POINTER(ctypes.c_int32)))
+    v._keep = (aq, ak)
+    return v
+
+
+def test_varlen_checks(lib):
+    """Packed sequences: offsets must start at 0 and not decrease; a sequence
+    with queries needs keys, and under the causal (bottom-right) mask at least
+    as many keys as queries; zero-query sequences are allowed.  All checked
+    before any CUDA call."""
+    p = ctypes.c_void_p(256)
+    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), ctypes.c_float(0.1), p, p, p, p, p, None, None)  # noqa: E731
+    assert fwd(_varlen([1, 3], [0, 3])) == bnd.ATTN_ERR_SHAPE          # cu[0] != 0
+    assert fwd(_varlen([0, 5, 3], [0, 5, 6])) == bnd.ATTN_ERR_SHAPE    # decreasing
+    assert fwd(_varlen([0, 3], [0, 0])) == bnd.ATTN_ERR_EMPTY_ROW      # queries, no keys
+    assert fwd(_varlen([0, 4], [0, 3], causal=1)) == bnd.ATTN_ERR_EMPTY_ROW
+    assert fwd(_varlen([0, 3], [0, 3], causal=2)) == bnd.ATTN_ERR_SHAPE
+    assert fwd(_varlen([0, 3], [0, 3], Hq=3)) == bnd.ATTN_ERR_SHAPE
+    assert fwd(_varlen([0, 3], [0, 3], d_h=96, d_v=96)) == bnd.ATTN_ERR_UNSUPPORTED
+    assert fwd(_varlen([0, 3], [0, 3], B=0)) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_fwd_varlen(None, ctypes.c_float(0.1), p, p, p, p, p, None, None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), ctypes.c_float(0.0), p, p, p, p, p, None,
+                               None) == bnd.ATTN_ERR_SCALE
+    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), ctypes.c_float(0.1), p, p, p,
+                               ctypes.c_void_p(0x1008), p, None, None) == bnd.ATTN_ERR_ALIGN
+    # no query rows at all: nothing to compute, OK without touching the GPU
+    assert fwd(_varlen([0, 0, 0], [0, 4, 9])) == bnd.ATTN_OK
+
+
+def test_varlen_workspace_and_pairs(lib):
+    cq, ck = [0, 100, 100, 357], [0, 150, 170, 600]
+    v = _varlen(cq, ck, causal=1, Hq=4, Hkv=2, d_h=128, d_v=64)
+    need = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v))
+    rows = cq[-1] * 4
+    nqt = (257 + 127) // 128
+    r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
+    assert need == r256(rows * 4) + r256(3 * 4 * nqt * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
+    p = ctypes.c_void_p(512)
+    args = [ctypes.byref(v), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5
+    assert lib.attn_bwd_varlen(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd_varlen(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd_varlen(*args, p, ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
+    # visible pairs against a brute-force count of the per-sequence masks
+    brute = 0
+    for b in range(3):
+        lq, lk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+        for i in range(lq):
+            brute += sum(1 for j in range(lk) if j <= i + lk - lq)
+    assert lib.attn_varlen_visible_pairs(ctypes.byref(v)) == brute * 4
+    v2 = _varlen(cq, ck, causal=0)
+    assert lib.attn_varlen_visible_pairs(ctypes.byref(v2)) == sum(
+        (cq[b + 1] - cq[b]) * (ck[b + 1] - ck[b]) for b in range(3)) * 4
