@@ -597,6 +597,116 @@ def run_decode(args):
     return 0
 
 
+def run_varlen(args):
+    """Packed variable-length sequences (attn_fwd_varlen + attn_bwd_varlen):
+    one step is the forward and the backward over the whole packed batch;
+    the metric counts visible pairs like the padded workloads.  Sampled rows
+    of two sequences are checked against the oracle (run per sequence)."""
+    import numpy as np
+    import torch
+    import exact_scaled_dot_gb300 as esd
+    from exact_scaled_dot_gb300 import build as lib_build
+    from exact_scaled_dot_gb300.inputs import VARLEN_WORKLOADS, make_varlen_inputs
+
+    lib_build.build()
+    w = VARLEN_WORKLOADS[args.workload]
+    inp = make_varlen_inputs(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Q, K, V, dO = (x.to(dev) for x in (inp.Q, inp.K, inp.V, inp.dO))
+    Tq, Tk = Q.shape[0], K.shape[0]
+    O = torch.empty((Tq, w.Hq, w.dv), dtype=torch.bfloat16, device=dev)
+    O_lo = torch.empty_like(O)
+    LSE = torch.empty((w.Hq, Tq), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    need = esd.attn_bwd_varlen_workspace_bytes(w.Hq, w.Hkv, w.dh, w.dv, inp.cu_q, inp.cu_k, causal=w.causal)
+    ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    pairs = esd.attn_varlen_visible_pairs(w.Hq, w.Hkv, w.dh, w.dv, inp.cu_q, inp.cu_k, causal=w.causal)
+    flops_fwd = pairs * 2 * (w.dh + w.dv)
+    flops_bwd = pairs * 2 * (2 * w.dh + 3 * w.dv)
+    esd.attn_clear_status()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        esd.attn_fwd_varlen(Q, K, V, inp.cu_q, inp.cu_k, causal=w.causal, O=O, LSE=LSE, O_lo=O_lo)
+        if ev is not None:
+            ev[1].record(stream)
+        esd.attn_bwd_varlen(Q, K, V, O, dO, LSE, inp.cu_q, inp.cu_k, O_lo=O_lo, causal=w.causal, dQ=dQ, dK=dK,
+                            dV=dV, workspace=ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    status = esd.attn_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {esd.strerror(status)}")
+    ms = a.elapsed_time(b) / args.steps
+    ms_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    ms_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    tflops = (flops_fwd + flops_bwd) / (ms * 1e-3) / 1e12
+
+    parity = None
+    if not args.no_oracle:
+        import oracle
+        orc = oracle.default()
+        rng = np.random.default_rng(0)
+        order = np.argsort(inp.lens_q)
+        checks, ok, errs = 0, True, {"O": 0.0, "LSE": 0.0, "dQ": 0.0}
+        for bi in (int(order[0]), int(order[-1])):
+            lq, lk = inp.lens_q[bi], inp.lens_k[bi]
+            q0, q1, k0, k1 = inp.cu_q[bi], inp.cu_q[bi + 1], inp.cu_k[bi], inp.cu_k[bi + 1]
+            p = oracle.Problem(1, w.Hq, w.Hkv, lq, lk, w.dh, w.dv, causal=w.causal)
+            f = lambda x: np.ascontiguousarray(x.double().numpy().transpose(1, 0, 2)[None])  # noqa: E731
+            Qb, Kb, Vb, Gb = f(inp.Q[q0:q1]), f(inp.K[k0:k1]), f(inp.V[k0:k1]), f(inp.dO[q0:q1])
+            rows = np.sort(rng.choice(w.Hq * lq, size=min(8, w.Hq * lq), replace=False))
+            Oref, Lref = orc.forward(p, Qb, Kb, Vb, rows=rows)
+            dQref, _dK, _dV, _D, _C = orc.backward(p, Qb, Kb, Vb, Gb, q_rows=rows, want_dkdv=False)
+            h, i = rows // lq, rows % lq
+            Og = O[q0:q1].double().cpu().numpy()[i, h]
+            Lg = LSE[:, q0:q1].double().cpu().numpy()[h, i]
+            dQg = dQ[q0:q1].double().cpu().numpy()[i, h]
+            ok &= bool(np.all(np.abs(Og - Oref) <= 1e-2 + 2e-2 * np.abs(Oref)))
+            ok &= bool(np.all(np.abs(Lg - Lref) <= 1e-3))
+            ok &= bool(np.all(np.abs(dQg - dQref) <= 1e-2 + 2e-2 * np.abs(dQref)))
+            errs = {"O": max(errs["O"], float(np.abs(Og - Oref).max())),
+                    "LSE": max(errs["LSE"], float(np.abs(Lg - Lref).max())),
+                    "dQ": max(errs["dQ"], float(np.abs(dQg - dQref).max()))}
+            checks += len(rows)
+        parity = {"rows_checked": checks, "ok": ok, "max_abs_err": errs}
+
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) draws rounded to bf16, drawn sequence lengths)",
+        "config": {"workload": w.name, "sequences": len(inp.lens_q), "Hq": w.Hq, "Hkv": w.Hkv, "d_h": w.dh,
+                   "d_v": w.dv, "causal": w.causal, "tokens": Tq, "lens": inp.lens_q, "visible_pairs": pairs,
+                   "l2": "inputs larger than L2"},
+        "kernels": {"forward": {"ms": ms_fwd}, "backward (preprocess + main + finalize)": {"ms": ms_bwd}},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
+                     "frac": tflops / peaks.get("bf16_tflops"), "peak_kind": f"bf16_tflops burst ({peak_src})",
+                     "traffic": None},
+        "clocks": clocks, "parity": parity, "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -614,9 +724,11 @@ def main(argv=None):
         ap.error("need --steps >= 1 and --warmup >= 0")
     if args.impl == "reference":
         return run_reference(args)
-    from exact_scaled_dot_gb300.inputs import DECODE_WORKLOADS
+    from exact_scaled_dot_gb300.inputs import DECODE_WORKLOADS, VARLEN_WORKLOADS
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args)
+    if args.workload in VARLEN_WORKLOADS:
+        return run_varlen(args)
     return run_cuda(args)
 
 
