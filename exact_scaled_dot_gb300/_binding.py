@@ -35,7 +35,8 @@ EXPORTS = ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "at
            "attn_bwd_finalize", "attn_visible_pairs", "attn_get_status", "attn_clear_status",
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
-           "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen")
+           "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight",
+           "attn_proj_bwd_input")
 
 
 class AttnError(RuntimeError):
@@ -106,9 +107,14 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_bwd_varlen_workspace_bytes.argtypes = [VL]
     lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    i64, i32 = ctypes.c_int64, ctypes.c_int32
+    lib.attn_proj_fwd.argtypes = [i64, i32, i32, _vp, _vp, _vp, _vp]
+    lib.attn_proj_bwd_weight.argtypes = [i64, i32, i32, _vp, _vp, _vp, _vp]
+    lib.attn_proj_bwd_input.argtypes = [i64, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(_vp),
+                                        ctypes.POINTER(_vp), _vp, _vp]
     for name in ("attn_fwd", "attn_fwd_decode", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
                  "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout", "attn_fwd_varlen",
-                 "attn_bwd_varlen"):
+                 "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight", "attn_proj_bwd_input"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -499,3 +505,60 @@ def attn_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens_q, cu_seqlens_k, *, O_lo=Non
                                 ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
     _check(rc, "attn_bwd_varlen")
     return dQ, dK, dV
+
+
+# ---------------------------------------------------------------------------
+# Projections on either side of attention (row-major bf16 matrices)
+# ---------------------------------------------------------------------------
+def _mat(t, name, dtype, shape, dev):
+    _check_tensor(t, name, dtype, shape, dev)
+    return _ptr(t)
+
+
+def attn_proj_fwd(X, W, *, Y=None, stream=None):
+    """Y [T, N] = X [T, D] W [D, N] (bf16 in and out, fp32 accumulation)."""
+    if X.dim() != 2 or W.dim() != 2:
+        raise ValueError("X and W must be 2-D")
+    T, D = (int(x) for x in X.shape)
+    N = int(W.shape[1])
+    dev = X.device
+    Y = torch.empty((T, N), dtype=torch.bfloat16, device=dev) if Y is None else Y
+    rc = load().attn_proj_fwd(T, D, N, _mat(X, "X", torch.bfloat16, (T, D), dev),
+                              _mat(W, "W", torch.bfloat16, (D, N), dev), _mat(Y, "Y", torch.bfloat16, (T, N), dev),
+                              _stream(dev, stream))
+    _check(rc, "attn_proj_fwd")
+    return Y
+
+
+def attn_proj_bwd_weight(X, G, *, dW=None, stream=None):
+    """dW [D, N] = X^T G (fp32 out)."""
+    T, D = (int(x) for x in X.shape)
+    N = int(G.shape[1])
+    dev = X.device
+    dW = torch.empty((D, N), dtype=torch.float32, device=dev) if dW is None else dW
+    rc = load().attn_proj_bwd_weight(T, D, N, _mat(X, "X", torch.bfloat16, (T, D), dev),
+                                     _mat(G, "G", torch.bfloat16, (T, N), dev),
+                                     _mat(dW, "dW", torch.float32, (D, N), dev), _stream(dev, stream))
+    _check(rc, "attn_proj_bwd_weight")
+    return dW
+
+
+def attn_proj_bwd_input(Gs, Ws, *, dX=None, stream=None):
+    """dX [T, D] = sum_s G_s [T, N_s] W_s[D, N_s]^T over 1..3 branches that share X (bf16 out)."""
+    if not 1 <= len(Gs) == len(Ws) <= 3:
+        raise ValueError("1 to 3 (G, W) pairs")
+    T = int(Gs[0].shape[0])
+    D = int(Ws[0].shape[0])
+    dev = Gs[0].device
+    Ns = [int(g.shape[1]) for g in Gs]
+    for k, (g, w) in enumerate(zip(Gs, Ws)):
+        _check_tensor(g, f"G[{k}]", torch.bfloat16, (T, Ns[k]), dev)
+        _check_tensor(w, f"W[{k}]", torch.bfloat16, (D, Ns[k]), dev)
+    dX = torch.empty((T, D), dtype=torch.bfloat16, device=dev) if dX is None else dX
+    _check_tensor(dX, "dX", torch.bfloat16, (T, D), dev)
+    n_arr = (ctypes.c_int32 * len(Ns))(*Ns)
+    g_arr = (_vp * len(Gs))(*[g.data_ptr() for g in Gs])
+    w_arr = (_vp * len(Ws))(*[w.data_ptr() for w in Ws])
+    rc = load().attn_proj_bwd_input(T, D, len(Gs), n_arr, g_arr, w_arr, _ptr(dX), _stream(dev, stream))
+    _check(rc, "attn_proj_bwd_input")
+    return dX

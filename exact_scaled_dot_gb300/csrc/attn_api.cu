@@ -240,6 +240,29 @@ bool make_tmap_acc(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D view of a row-major [rows][cols] bf16 matrix, boxes of box_cols x
+// box_rows with the 128-byte swizzle; rows and columns past the edges read as
+// zeros.
+bool make_tmap_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int check_proj_dims(int64_t T, int32_t D, int32_t N) {
+  if (T <= 0 || D <= 0 || N <= 0) return ATTN_ERR_SHAPE;
+  if (D % 8 != 0 || N % 8 != 0) return ATTN_ERR_SHAPE;                 // 16-byte rows
+  if (T > (int64_t{1} << 31) - 1) return ATTN_ERR_SHAPE;               // TMA coordinates are int32
+  if ((T + 127) / 128 > 65535 || (static_cast<int64_t>(D) + 127) / 128 > 65535) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
 struct DeviceInfo {
   bool probed = false;
   bool ok = false;
@@ -695,6 +718,97 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale
 }
 
 size_t attn_bwd_noalloc_max_scratch_bytes(void) { return kStaticBwdScratchBytes; }
+
+// ---------------------------------------------------------------------------
+// Projections on either side of attention (A.10.10-A.10.11)
+// ---------------------------------------------------------------------------
+int attn_proj_fwd(int64_t T, int32_t D, int32_t N, const void* X, const void* W, void* Y, void* stream) {
+  int rc = check_proj_dims(T, D, N);
+  if (rc) return rc;
+  rc = check_ptrs({X, W, Y});
+  if (rc) return rc;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tA[3], tB[3];
+  // A = X [T][D] K-major (boxes 64 x 128), B = W [D][N] MN-major (boxes 64 x 64).
+  if (!make_tmap_2d(&tA[0], X, T, D, 64, 128) || !make_tmap_2d(&tB[0], W, D, N, 64, 64)) return ATTN_ERR_CUDA;
+  tA[1] = tA[2] = tA[0];
+  tB[1] = tB[2] = tB[0];
+  GemmParams p{};
+  p.M = T;
+  p.N = N;
+  p.nsrc = 1;
+  p.K[0] = D;
+  p.ldc = N;
+  p.C = Y;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.status = status;
+  return launch_proj_gemm(kGemmXW, tA, tB, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                                : ATTN_ERR_CUDA;
+}
+
+int attn_proj_bwd_weight(int64_t T, int32_t D, int32_t N, const void* X, const void* G, float* dW, void* stream) {
+  int rc = check_proj_dims(T, D, N);
+  if (rc) return rc;
+  rc = check_ptrs({X, G, dW});
+  if (rc) return rc;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tA[3], tB[3];
+  // A = X^T: X [T][D] read MN-major (boxes 64 x 64); B = G [T][N] MN-major.
+  if (!make_tmap_2d(&tA[0], X, T, D, 64, 64) || !make_tmap_2d(&tB[0], G, T, N, 64, 64)) return ATTN_ERR_CUDA;
+  tA[1] = tA[2] = tA[0];
+  tB[1] = tB[2] = tB[0];
+  GemmParams p{};
+  p.M = D;
+  p.N = N;
+  p.nsrc = 1;
+  p.K[0] = static_cast<int32_t>(T);
+  p.ldc = N;
+  p.C = dW;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.status = status;
+  return launch_proj_gemm(kGemmXtG, tA, tB, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                                 : ATTN_ERR_CUDA;
+}
+
+int attn_proj_bwd_input(int64_t T, int32_t D, int32_t nsrc, const int32_t* N, const void* const* G,
+                        const void* const* W, void* dX, void* stream) {
+  if (!N || !G || !W) return ATTN_ERR_NULL;
+  if (nsrc < 1 || nsrc > 3) return ATTN_ERR_SHAPE;
+  int rc = ATTN_OK;
+  for (int s = 0; s < nsrc; ++s) {
+    rc = check_proj_dims(T, D, N[s]);
+    if (rc) return rc;
+    rc = check_ptrs({G[s], W[s]});
+    if (rc) return rc;
+  }
+  rc = check_ptrs({dX});
+  if (rc) return rc;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tA[3], tB[3];
+  GemmParams p{};
+  for (int s = 0; s < 3; ++s) {
+    const int k = s < nsrc ? s : 0;
+    // A = G_s [T][N_s] K-major (boxes 64 x 128); B = W_s^T: W_s [D][N_s] K-major (boxes 64 x 256).
+    if (!make_tmap_2d(&tA[s], G[k], T, N[k], 64, 128) || !make_tmap_2d(&tB[s], W[k], D, N[k], 64, 256))
+      return ATTN_ERR_CUDA;
+    p.K[s] = s < nsrc ? N[s] : 0;
+  }
+  p.M = T;
+  p.N = D;
+  p.nsrc = nsrc;
+  p.ldc = D;
+  p.C = dX;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.status = status;
+  return launch_proj_gemm(kGemmGWt, tA, tB, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                                 : ATTN_ERR_CUDA;
+}
 
 // ---------------------------------------------------------------------------
 // Packed variable-length sequences: the same kernels, addressing rows through

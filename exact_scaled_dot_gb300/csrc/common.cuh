@@ -194,6 +194,24 @@ struct DecParams {
   unsigned int* status;
 };
 
+// The projection products (A.10.10-A.10.11): C = sum_s A_s B_s, row-major
+// bf16 operands through TMA maps, C row-major with leading dimension ldc.
+enum GemmKind : int {
+  kGemmXW = 0,    // Y = X W:     A [M][K] K-major, B [K][N] MN-major, C bf16
+  kGemmXtG = 1,   // dW = X^T G:  A [K][M] MN-major, B [K][N] MN-major, C fp32
+  kGemmGWt = 2,   // dX = G W^T:  A [M][K] K-major, B [N][K] K-major, C bf16 (up to 3 sources)
+};
+struct GemmParams {
+  int64_t M;                   // output rows
+  int32_t N;                   // output columns
+  int32_t nsrc;                // products summed (1..3)
+  int32_t K[3];                // contraction length of each product
+  int32_t ldc;
+  void* C;
+  uint64_t wait_limit_ns;
+  unsigned int* status;
+};
+
 // Default limit of every bounded wait inside the kernels.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -209,6 +227,8 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& 
                                        int dv, int dh, const void* Q, const void* O, const void* O_lo,
                                        const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
                                        cudaStream_t stream);
+cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap* tB, const GemmParams& p,
+                             cudaStream_t stream);
 cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
                                      cudaStream_t stream);
 

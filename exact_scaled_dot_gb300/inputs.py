@@ -190,3 +190,38 @@ VARLEN_WORKLOADS: Dict[str, VarlenWorkload] = {
     "varlen_gqa_causal": VarlenWorkload("varlen_gqa_causal", B=16, Hq=32, Hkv=8, dh=128, dv=128, causal=True,
                                         len_range=(256, 4096), seed=1201),
 }
+
+
+# ---------------------------------------------------------------------------
+# Projections on either side of attention
+# ---------------------------------------------------------------------------
+@dataclass
+class ProjInputs:
+    X: torch.Tensor          # [T, D]
+    Ws: List[torch.Tensor]   # [D, N_s]
+    Gs: List[torch.Tensor]   # [T, N_s] upstream gradients of the projections' outputs
+
+
+def make_proj_inputs(T: int, D: int, Ns, seed: int) -> ProjInputs:
+    """X ~ N(0, 1), W_s ~ N(0, 1/D) (so X W_s has unit variance), G_s ~ N(0, 1),
+    drawn in that order from a seeded CPU generator and rounded to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+
+    def draw(shape, sigma):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x.mul_(sigma)
+        return x.to(torch.bfloat16).contiguous()
+
+    X = draw((T, D), 1.0)
+    Ws = [draw((D, int(n)), 1.0 / float(D) ** 0.5) for n in Ns]
+    Gs = [draw((T, int(n)), 1.0) for n in Ns]
+    return ProjInputs(X, Ws, Gs)
+
+
+# The projections of the causal GQA workload: 8192 tokens (2 x 4096) of width
+# 4096 into Q (32 heads x 128), K and V (8 heads x 128 each).
+PROJ_WORKLOADS = {
+    "proj_qkv_gqa": dict(T=8192, D=4096, Ns=(4096, 1024, 1024), seed=1301),
+}

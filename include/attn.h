@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -255,6 +255,26 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
                     const void* O, const void* O_lo, const void* dO, const float* LSE,
                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
                     void* stream);
+
+/* Linear projections on either side of attention ("Appendix A.10", eqs.
+ * A.10.10-A.10.11), on the tensor cores.  Row-major matrices, bf16 in, fp32
+ * accumulation; T rows (tokens), D input width, N output width (for example
+ * Hq * d_h: the output [T][Hq*d_h] is the packed [T][Hq][d_h] layout the
+ * variable-length entry points take).
+ *   attn_proj_fwd:        Y [T][N] = X [T][D] W [D][N]                 bf16 out
+ *   attn_proj_bwd_weight: dW [D][N] = X^T G,  G [T][N]                 fp32 out
+ *   attn_proj_bwd_input:  dX [T][D] = sum_s G_s [T][N_s] W_s[D][N_s]^T bf16 out,
+ *                         over 1..3 sources: the branches that share X (all
+ *                         three for self-attention; only the shared ones for
+ *                         cross-attention, A.10.11).  N, G, W are host arrays
+ *                         of nsrc entries (G[s], W[s] device pointers).
+ * D and every N must be multiples of 8 (16-byte rows): ATTN_ERR_SHAPE
+ * otherwise; pointers 16-byte aligned.  Outputs are fully overwritten. */
+int attn_proj_fwd(int64_t T, int32_t D, int32_t N, const void* X, const void* W, void* Y, void* stream);
+int attn_proj_bwd_weight(int64_t T, int32_t D, int32_t N, const void* X, const void* G, float* dW,
+                         void* stream);
+int attn_proj_bwd_input(int64_t T, int32_t D, int32_t nsrc, const int32_t* N, const void* const* G,
+                        const void* const* W, void* dX, void* stream);
 
 /* Device status word of the current device: ATTN_OK, or the first failure a
  * kernel recorded (ATTN_ERR_TIMEOUT).  Synchronises the device.  Writes the

@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 4
+    assert esd.attn_abi_version() == 5
 
 
 def test_strerror_covers_every_code(lib):
@@ -223,3 +223,22 @@ def test_varlen_workspace_and_pairs(lib):
     v2 = _varlen(cq, ck, causal=0)
     assert lib.attn_varlen_visible_pairs(ctypes.byref(v2)) == sum(
         (cq[b + 1] - cq[b]) * (ck[b + 1] - ck[b]) for b in range(3)) * 4
+
+
+def test_proj_checks(lib):
+    """Projection entry points: widths must be multiples of 8 (16-byte rows),
+    1..3 sources for the input gradient; all checked before any CUDA call."""
+    p = ctypes.c_void_p(256)
+    assert lib.attn_proj_fwd(100, 60, 64, p, p, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_proj_fwd(100, 64, 60, p, p, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_proj_fwd(0, 64, 64, p, p, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_proj_fwd(100, 64, 64, None, p, p, None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_proj_fwd(100, 64, 64, p, ctypes.c_void_p(0x1008), p, None) == bnd.ATTN_ERR_ALIGN
+    assert lib.attn_proj_bwd_weight(100, 64, 12, p, p, p, None) == bnd.ATTN_ERR_SHAPE
+    n = (ctypes.c_int32 * 4)(64, 64, 64, 64)
+    ptrs = (ctypes.c_void_p * 4)(256, 256, 256, 256)
+    assert lib.attn_proj_bwd_input(100, 64, 4, n, ptrs, ptrs, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_proj_bwd_input(100, 64, 0, n, ptrs, ptrs, p, None) == bnd.ATTN_ERR_SHAPE
+    n2 = (ctypes.c_int32 * 2)(64, 20)
+    assert lib.attn_proj_bwd_input(100, 64, 2, n2, ptrs, ptrs, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_proj_bwd_input(100, 64, 2, None, ptrs, ptrs, p, None) == bnd.ATTN_ERR_NULL
