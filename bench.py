@@ -707,6 +707,104 @@ def run_varlen(args):
     return 0
 
 
+def run_proj(args):
+    """The projections on either side of attention (A.10.10-A.10.11) at the
+    GQA workload's shapes: one step is the three forward products
+    Q, K, V = X W_Q, X W_K, X W_V, the three weight gradients X^T G and the
+    input gradient sum_s G_s W_s^T.  Dense products: TFLOP/s against the
+    measured bf16 peak."""
+    import numpy as np
+    import torch
+    import exact_scaled_dot_gb300 as esd
+    from exact_scaled_dot_gb300 import build as lib_build
+    from exact_scaled_dot_gb300.inputs import PROJ_WORKLOADS, make_proj_inputs
+
+    lib_build.build()
+    cfg = PROJ_WORKLOADS[args.workload]
+    T, D, Ns = cfg["T"], cfg["D"], cfg["Ns"]
+    inp = make_proj_inputs(T, D, Ns, cfg["seed"])
+    dev = torch.device("cuda", torch.cuda.current_device())
+    X = inp.X.to(dev)
+    Ws = [w.to(dev) for w in inp.Ws]
+    Gs = [g.to(dev) for g in inp.Gs]
+    Ys = [torch.empty((T, n), dtype=torch.bfloat16, device=dev) for n in Ns]
+    dWs = [torch.empty((D, n), dtype=torch.float32, device=dev) for n in Ns]
+    dX = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops_each = 2 * T * D * sum(Ns)
+    esd.attn_clear_status()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for W, Y in zip(Ws, Ys):
+            esd.attn_proj_fwd(X, W, Y=Y)
+        if ev is not None:
+            ev[1].record(stream)
+        for G, dW in zip(Gs, dWs):
+            esd.attn_proj_bwd_weight(X, G, dW=dW)
+        if ev is not None:
+            ev[2].record(stream)
+        esd.attn_proj_bwd_input(Gs, Ws, dX=dX)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    status = esd.attn_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {esd.strerror(status)}")
+    ms = a.elapsed_time(b) / args.steps
+    part = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(3)]
+    tflops = 3 * flops_each / (ms * 1e-3) / 1e12
+    parity = None
+    if not args.no_oracle:
+        rng = np.random.default_rng(0)
+        rows = rng.integers(0, T, 8)
+        Xn = inp.X.double().numpy()
+        ok, err = True, 0.0
+        for k in range(3):
+            ref = Xn[rows] @ inp.Ws[k].double().numpy()
+            got = Ys[k].double().cpu().numpy()[rows]
+            ok &= bool(np.all(np.abs(got - ref) <= 1e-2 + 2e-2 * np.abs(ref)))
+            err = max(err, float(np.abs(got - ref).max()))
+        ref = sum(inp.Gs[k].double().numpy()[rows] @ inp.Ws[k].double().numpy().T for k in range(3))
+        got = dX.double().cpu().numpy()[rows]
+        ok &= bool(np.all(np.abs(got - ref) <= 1e-2 + 2e-2 * np.abs(ref)))
+        parity = {"rows_checked": int(len(rows)), "ok": ok,
+                  "max_abs_err": max(err, float(np.abs(got - ref).max()))}
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": "projections on either side of attention, fwd + bwd TFLOP/s", "value": tflops,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) draws, weights N(0,1/D), rounded to bf16)",
+        "config": {"workload": args.workload, "T": T, "D": D, "N": list(Ns), "l2": "inputs larger than L2"},
+        "kernels": {"X W (3 products)": {"ms": part[0], "tflops": flops_each / (part[0] * 1e-3) / 1e12},
+                    "X^T G (3 products)": {"ms": part[1], "tflops": flops_each / (part[1] * 1e-3) / 1e12},
+                    "sum G W^T": {"ms": part[2], "tflops": flops_each / (part[2] * 1e-3) / 1e12}},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
+                     "frac": tflops / peaks.get("bf16_tflops"), "peak_kind": f"bf16_tflops burst ({peak_src})",
+                     "kernel": "proj_gemm_kernel", "traffic": None},
+        "clocks": clocks, "parity": parity, "gpu_launches": 7 * args.steps,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -724,11 +822,13 @@ def main(argv=None):
         ap.error("need --steps >= 1 and --warmup >= 0")
     if args.impl == "reference":
         return run_reference(args)
-    from exact_scaled_dot_gb300.inputs import DECODE_WORKLOADS, VARLEN_WORKLOADS
+    from exact_scaled_dot_gb300.inputs import DECODE_WORKLOADS, PROJ_WORKLOADS, VARLEN_WORKLOADS
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args)
     if args.workload in VARLEN_WORKLOADS:
         return run_varlen(args)
+    if args.workload in PROJ_WORKLOADS:
+        return run_proj(args)
     return run_cuda(args)
 
 
