@@ -36,7 +36,7 @@ EXPORTS = ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "at
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight",
-           "attn_proj_bwd_input")
+           "attn_proj_bwd_input", "attn_rope")
 
 
 class AttnError(RuntimeError):
@@ -112,9 +112,11 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_proj_bwd_weight.argtypes = [i64, i32, i32, _vp, _vp, _vp, _vp]
     lib.attn_proj_bwd_input.argtypes = [i64, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(_vp),
                                         ctypes.POINTER(_vp), _vp, _vp]
+    lib.attn_rope.argtypes = [i64, i32, i32, f, _vp, i32, _vp, _vp, _vp]
     for name in ("attn_fwd", "attn_fwd_decode", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
                  "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout", "attn_fwd_varlen",
-                 "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight", "attn_proj_bwd_input"):
+                 "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight", "attn_proj_bwd_input",
+                 "attn_rope"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -562,3 +564,21 @@ def attn_proj_bwd_input(Gs, Ws, *, dX=None, stream=None):
     rc = load().attn_proj_bwd_input(T, D, len(Gs), n_arr, g_arr, w_arr, _ptr(dX), _stream(dev, stream))
     _check(rc, "attn_proj_bwd_input")
     return dX
+
+
+def attn_rope(X, positions, *, base: float = 10000.0, inverse: bool = False, Y=None, stream=None):
+    """Rotary position embedding of token-major rows X [tokens, heads, d] (bf16)
+    at int32 positions [tokens] (device); inverse=True rotates back (the
+    gradient map).  Y may be X (in place)."""
+    if X.dim() != 3:
+        raise ValueError("X must be [tokens, heads, d]")
+    T, H, d = (int(x) for x in X.shape)
+    dev = X.device
+    _check_tensor(X, "X", torch.bfloat16, (T, H, d), dev)
+    _check_tensor(positions, "positions", torch.int32, (T,), dev)
+    Y = torch.empty_like(X) if Y is None else Y
+    _check_tensor(Y, "Y", torch.bfloat16, (T, H, d), dev)
+    rc = load().attn_rope(T, H, d, ctypes.c_float(base), _ptr(positions), 1 if inverse else 0, _ptr(X), _ptr(Y),
+                          _stream(dev, stream))
+    _check(rc, "attn_rope")
+    return Y

@@ -722,6 +722,24 @@ size_t attn_bwd_noalloc_max_scratch_bytes(void) { return kStaticBwdScratchBytes;
 // ---------------------------------------------------------------------------
 // Projections on either side of attention (A.10.10-A.10.11)
 // ---------------------------------------------------------------------------
+int attn_rope(int64_t tokens, int32_t heads, int32_t d, float base, const int32_t* positions, int32_t inverse,
+              const void* X, void* Y, void* stream) {
+  if (tokens <= 0 || heads <= 0 || d <= 0 || d % 8 != 0 || d > 128) return ATTN_ERR_SHAPE;
+  if (inverse != 0 && inverse != 1) return ATTN_ERR_SHAPE;
+  if (!std::isfinite(base) || !(base > 1.f)) return ATTN_ERR_SCALE;
+  int rc = check_ptrs({X, Y});
+  if (rc) return rc;
+  if (!positions) return ATTN_ERR_NULL;
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  float w[64];
+  for (int k = 0; k < d / 2; ++k) w[k] = static_cast<float>(std::pow(static_cast<double>(base), -2.0 * k / d));
+  const cudaError_t e = launch_rope(tokens * heads, d, heads, positions, w, inverse, X, Y,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_proj_fwd(int64_t T, int32_t D, int32_t N, const void* X, const void* W, void* Y, void* stream) {
   int rc = check_proj_dims(T, D, N);
   if (rc) return rc;

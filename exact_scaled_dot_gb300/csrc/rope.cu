@@ -1,0 +1,99 @@
+// rope.cu -- rotary position embedding of query and key rows, and its
+// inverse for their gradients ("Chapter 15 -- matrix formulas", section
+// 15.6; "Chapter 31 -- attention backprop", section 5).
+//
+// Each row x of width d is split into 2-D blocks (x_2k, x_2k+1), k < d/2, and
+// block k is rotated by the angle a = pos * w_k, w_k = base^(-2k/d):
+//   x'_2k   = x_2k cos a - x_2k+1 sin a
+//   x'_2k+1 = x_2k sin a + x_2k+1 cos a          (column-vector rotation R(a)).
+// Then R_i^T R_j = R((j - i) w): the rotated dot product depends on the
+// position difference only.  The map is orthogonal for a fixed position, so
+// the gradient of a rotated row is the upstream gradient rotated back by -a
+// (inverse = 1).
+//
+// Memory-bound: every thread rotates 8 elements (four blocks) of one row,
+// 16 bytes in and out.  The angle is formed without losing the product's low
+// bits: a = p w is split exactly into hi + lo (an fma gives the rounding
+// residual), hi is reduced modulo 2 pi by the two-constant Cody-Waite scheme,
+// lo added back, and the sine and cosine of the reduced angle come from
+// sincosf.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace esd {
+namespace {
+
+// 2 pi split into a leading part with trailing zero bits (so k * kTwoPiHi is
+// exact for the k that occur) and the remainder.
+constexpr float kTwoPiHi = 6.28125f;
+constexpr float kTwoPiLo = 1.9353071795864769e-3f;
+constexpr float kInvTwoPi = 0.15915494309189535f;
+
+__device__ __forceinline__ float reduced_angle(int32_t pos, float w) {
+  const float p = static_cast<float>(pos);      // exact for |pos| < 2^24
+  const float hi = p * w;
+  const float lo = fmaf(p, w, -hi);             // p w = hi + lo exactly
+  const float k = rintf(hi * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiHi, hi);
+  r = fmaf(-k, kTwoPiLo, r);
+  return r + lo;
+}
+
+struct RopeParams {
+  int64_t rows;          // rows of the tensor (tokens x heads)
+  int32_t d;             // row width (even)
+  int32_t heads;         // rows per token: row r is token r / heads
+  int32_t inverse;       // rotate by -a
+  float w[64];           // w_k = base^(-2k/d), k < d/2
+  const int32_t* pos;    // [rows / heads] token positions
+  const uint4* x;        // bf16 rows, 8 elements per uint4
+  uint4* y;
+};
+
+__global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeParams p) {
+  const int per_row = p.d / 8;
+  const int64_t total = p.rows * per_row;
+  const float sgn = p.inverse ? -1.f : 1.f;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = u / per_row;
+    const int c = static_cast<int>(u - row * per_row);   // 8-element chunk: blocks 4c .. 4c+3
+    const int32_t pos = p.pos[row / p.heads];
+    const uint4 v = p.x[u];
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float s, co;
+      sincosf(sgn * reduced_angle(pos, p.w[4 * c + q]), &s, &co);
+      const float a = bf16_lo(in[q]), b = bf16_hi(in[q]);
+      out[q] = pack_bf16x2(a * co - b * s, a * s + b * co);
+    }
+    p.y[u] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rope(int64_t rows, int d, int heads, const int32_t* pos, const float* w, int inverse,
+                        const void* x, void* y, cudaStream_t stream) {
+  RopeParams p{};
+  p.rows = rows;
+  p.d = d;
+  p.heads = heads;
+  p.inverse = inverse;
+  for (int k = 0; k < d / 2; ++k) p.w[k] = w[k];
+  p.pos = pos;
+  p.x = static_cast<const uint4*>(x);
+  p.y = static_cast<uint4*>(y);
+  int64_t blocks = (rows * (d / 8) + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  rope_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace esd

@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 5
+#define ATTN_ABI_VERSION 6
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -275,6 +275,23 @@ int attn_proj_bwd_weight(int64_t T, int32_t D, int32_t N, const void* X, const v
                          void* stream);
 int attn_proj_bwd_input(int64_t T, int32_t D, int32_t nsrc, const int32_t* N, const void* const* G,
                         const void* const* W, void* dX, void* stream);
+
+/* Rotary position embedding of query or key rows ("Chapter 15 -- matrix
+ * formulas", section 15.6): every row x of width d is split into 2-D blocks
+ * (x_2k, x_2k+1), k < d/2, and block k is rotated by a = pos * w_k with
+ * w_k = base^(-2k/d) (column-vector rotation: x'_2k = x_2k cos a - x_2k+1
+ * sin a, x'_2k+1 = x_2k sin a + x_2k+1 cos a), so that the score of a rotated
+ * query and key depends only on their position difference.  inverse = 1
+ * rotates by -a: the transpose, which maps the gradient of a rotated row back
+ * to the row ("Chapter 31 -- attention backprop", section 5).
+ * X, Y: device bf16 [tokens][heads][d] (token-major, the packed layout; Y may
+ * equal X); positions: device int32 [tokens], the position of each token.
+ * d a multiple of 8 and <= 128; base finite and > 1 (ATTN_ERR_SCALE
+ * otherwise).  Angles are reduced modulo 2 pi in single precision with the
+ * product's rounding residual kept, so the rotation stays accurate for
+ * positions well beyond 10^5. */
+int attn_rope(int64_t tokens, int32_t heads, int32_t d, float base, const int32_t* positions, int32_t inverse,
+              const void* X, void* Y, void* stream);
 
 /* Device status word of the current device: ATTN_OK, or the first failure a
  * kernel recorded (ATTN_ERR_TIMEOUT).  Synchronises the device.  Writes the

@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 5
+    assert esd.attn_abi_version() == 6
 
 
 def test_strerror_covers_every_code(lib):
@@ -242,3 +242,16 @@ def test_proj_checks(lib):
     n2 = (ctypes.c_int32 * 2)(64, 20)
     assert lib.attn_proj_bwd_input(100, 64, 2, n2, ptrs, ptrs, p, None) == bnd.ATTN_ERR_SHAPE
     assert lib.attn_proj_bwd_input(100, 64, 2, None, ptrs, ptrs, p, None) == bnd.ATTN_ERR_NULL
+
+
+def test_rope_checks(lib):
+    p = ctypes.c_void_p(256)
+    f = ctypes.c_float
+    assert lib.attn_rope(10, 2, 12, f(10000.0), p, 0, p, p, None) == bnd.ATTN_ERR_SHAPE    # d % 8
+    assert lib.attn_rope(10, 2, 256, f(10000.0), p, 0, p, p, None) == bnd.ATTN_ERR_SHAPE   # d > 128
+    assert lib.attn_rope(10, 2, 64, f(10000.0), p, 2, p, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_rope(0, 2, 64, f(10000.0), p, 0, p, p, None) == bnd.ATTN_ERR_SHAPE
+    assert lib.attn_rope(10, 2, 64, f(1.0), p, 0, p, p, None) == bnd.ATTN_ERR_SCALE
+    assert lib.attn_rope(10, 2, 64, f(float("nan")), p, 0, p, p, None) == bnd.ATTN_ERR_SCALE
+    assert lib.attn_rope(10, 2, 64, f(10000.0), None, 0, p, p, None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_rope(10, 2, 64, f(10000.0), p, 0, ctypes.c_void_p(0x1008), p, None) == bnd.ATTN_ERR_ALIGN

@@ -1,0 +1,77 @@
+"""GPU-vs-oracle parity of the rotary embedding (attn_rope) and of attention
+over rotated queries and keys: the rotation within 1e-2 + 2e-2 |ref| of the
+fp64 rotation with exact angles (positions up to 10^5), the inverse undoing
+it, and packed causal attention over GPU-rotated Q, K matching the oracle's
+rotation (rounded to bf16, the precision of the rotated tensors) followed by
+the oracle's attention."""
+import numpy as np
+import pytest
+import torch
+
+from exact_scaled_dot_gb300.inputs import VarlenWorkload, make_varlen_inputs
+
+from _attn_cases import LSE_ATOL, assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    from exact_scaled_dot_gb300 import build as b
+    b.build()
+    import exact_scaled_dot_gb300 as esd
+    esd.load()
+    assert torch.cuda.is_available(), "a CUDA device is required"
+    esd.attn_clear_status()
+    yield
+    assert esd.attn_get_status() == 0
+
+
+@pytest.mark.parametrize("T,H,d,base,maxpos", [(1000, 4, 128, 10000.0, 65535), (333, 2, 64, 500000.0, 4096),
+                                                (64, 1, 8, 10.0, 100000)])
+def test_rope_matches_oracle(T, H, d, base, maxpos):
+    from oracle.rope import rope
+    import exact_scaled_dot_gb300 as esd
+    g = torch.Generator().manual_seed(T + d)
+    X = torch.randn((T, H, d), generator=g).to(torch.bfloat16)
+    pos = torch.randint(0, maxpos + 1, (T,), generator=g, dtype=torch.int32)
+    Xd, Pd = X.cuda(), pos.cuda()
+    Y = esd.attn_rope(Xd, Pd, base=base)
+    Z = esd.attn_rope(Y, Pd, base=base, inverse=True)
+    torch.cuda.synchronize()
+    ref = rope(f64(X), pos.numpy(), base=base)
+    assert_close(f64(Y), ref, "rotated")
+    assert_close(f64(Z), f64(X), "rotated back")
+    W = Xd.clone()
+    esd.attn_rope(W, Pd, base=base, Y=W)   # in place
+    torch.cuda.synchronize()
+    assert torch.equal(W, Y)
+
+
+def test_attention_over_rotated_queries_and_keys(orc):
+    import oracle
+    from oracle.rope import rope
+    import exact_scaled_dot_gb300 as esd
+    w = VarlenWorkload("rope", B=2, Hq=4, Hkv=2, dh=128, dv=128, causal=True, lens_q=(300, 129), seed=71)
+    inp = make_varlen_inputs(w)
+    # positions restart at 0 in every sequence
+    pos = np.concatenate([np.arange(n) for n in inp.lens_q]).astype(np.int32)
+    d = "cuda:0"
+    P = torch.from_numpy(pos).to(d)
+    Qr = esd.attn_rope(inp.Q.to(d), P)
+    Kr = esd.attn_rope(inp.K.to(d), P)
+    O, LSE, _ = esd.attn_fwd_varlen(Qr, Kr, inp.V.to(d), inp.cu_q, inp.cu_k, causal=True)
+    torch.cuda.synchronize()
+    # The rotated rows are stored in bf16 (the precision of the tensors the
+    # attention reads), so the reference rounds its exact rotation the same way.
+    bf16 = lambda x: torch.from_numpy(x).to(torch.bfloat16).double().numpy()  # noqa: E731
+    Qn, Kn = bf16(rope(f64(inp.Q), pos)), bf16(rope(f64(inp.K), pos))
+    Vn = f64(inp.V)
+    for b in range(2):
+        q0, q1 = inp.cu_q[b], inp.cu_q[b + 1]
+        n = q1 - q0
+        p = oracle.Problem(1, 4, 2, n, n, 128, 128, causal=True)
+        tr = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2)[None])  # noqa: E731
+        Oref, Lref = orc.forward(p, tr(Qn[q0:q1]), tr(Kn[q0:q1]), tr(Vn[q0:q1]))
+        assert_close(f64(O[q0:q1]), Oref[0].transpose(1, 0, 2), f"O[{b}]")
+        assert_close(f64(LSE[:, q0:q1]), Lref[0], f"LSE[{b}]", atol=LSE_ATOL, rtol=0.0)
