@@ -805,6 +805,72 @@ def run_proj(args):
     return 0
 
 
+def run_rope(args):
+    """Rotary embedding of the GQA workload's queries and keys (8192 tokens,
+    32 + 8 heads of 128): memory-bound, GB/s of rows read and written against
+    the measured copy bandwidth; the inverse (gradient) pass is the same
+    kernel."""
+    import numpy as np
+    import torch
+    import exact_scaled_dot_gb300 as esd
+    from exact_scaled_dot_gb300 import build as lib_build
+
+    lib_build.build()
+    T, Hq, Hkv, d = 8192, 32, 8, 128
+    g = torch.Generator().manual_seed(1401)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Q = torch.randn((T, Hq, d), generator=g).to(torch.bfloat16).to(dev)
+    K = torch.randn((T, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    pos = (torch.arange(T, dtype=torch.int32) % 4096).to(dev)
+    Qr, Kr = torch.empty_like(Q), torch.empty_like(K)
+    stream = torch.cuda.current_stream(dev)
+    esd.attn_clear_status()
+
+    def step():
+        esd.attn_rope(Q, pos, Y=Qr)
+        esd.attn_rope(K, pos, Y=Kr)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if esd.attn_get_status() != 0:
+        raise RuntimeError("device status set")
+    ms = a.elapsed_time(b) / args.steps
+    nbytes = 2 * (Q.numel() + K.numel()) * 2 + T * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    parity = None
+    if not args.no_oracle:
+        from oracle.rope import rope
+        rows = np.random.default_rng(0).integers(0, T, 16)
+        ref = rope(Q[rows].double().cpu().numpy(), pos[rows].cpu().numpy())
+        got = Qr[rows].double().cpu().numpy()
+        parity = {"rows_checked": 16, "ok": bool(np.all(np.abs(got - ref) <= 1e-2 + 2e-2 * np.abs(ref))),
+                  "max_abs_err": float(np.abs(got - ref).max())}
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": "rotary embedding of queries and keys (GB/s)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
+        "config": {"workload": "rope_gqa", "tokens": T, "Hq": Hq, "Hkv": Hkv, "d": d, "bytes_per_step": nbytes},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
+                     "frac": gbs / peaks.get("hbm_gbs"), "peak_kind": f"hbm_gbs ({peak_src})", "kernel": "rope_kernel",
+                     "traffic": None},
+        "clocks": clocks, "parity": parity, "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -829,6 +895,8 @@ def main(argv=None):
         return run_varlen(args)
     if args.workload in PROJ_WORKLOADS:
         return run_proj(args)
+    if args.workload == "rope_gqa":
+        return run_rope(args)
     return run_cuda(args)
 
 

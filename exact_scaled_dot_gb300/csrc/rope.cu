@@ -11,8 +11,10 @@
 // the gradient of a rotated row is the upstream gradient rotated back by -a
 // (inverse = 1).
 //
-// Memory-bound: every thread rotates 8 elements (four blocks) of one row,
-// 16 bytes in and out.  The angle is formed without losing the product's low
+// Memory-bound: every thread takes 8 elements (four blocks) of one token,
+// computes their four angles once and rotates those 16 bytes in a group of
+// up to 8 heads of the token (the angle depends on the position and the
+// block only).  The angle is formed without losing the product's low
 // bits: a = p w is split exactly into hi + lo (an fma gives the rounding
 // residual), hi is reduced modulo 2 pi by the two-constant Cody-Waite scheme,
 // lo added back, and the sine and cosine of the reduced angle come from
@@ -54,25 +56,36 @@ struct RopeParams {
 };
 
 __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeParams p) {
+  constexpr int kHeadGroup = 8;
   const int per_row = p.d / 8;
-  const int64_t total = p.rows * per_row;
+  const int groups = (p.heads + kHeadGroup - 1) / kHeadGroup;
+  const int64_t tokens = p.rows / p.heads;
+  const int64_t total = tokens * groups * per_row;
   const float sgn = p.inverse ? -1.f : 1.f;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
        u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = u / per_row;
-    const int c = static_cast<int>(u - row * per_row);   // 8-element chunk: blocks 4c .. 4c+3
-    const int32_t pos = p.pos[row / p.heads];
-    const uint4 v = p.x[u];
-    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[4];
+    const int64_t tg = u / per_row;                      // (token, head group)
+    const int c = static_cast<int>(u - tg * per_row);    // 8-element chunk: blocks 4c .. 4c+3
+    const int64_t tok = tg / groups;
+    const int h0 = static_cast<int>(tg - tok * groups) * kHeadGroup;
+    const int h1 = h0 + kHeadGroup < p.heads ? h0 + kHeadGroup : p.heads;
+    const int32_t pos = p.pos[tok];
+    float sn[4], cs[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float s, co;
-      sincosf(sgn * reduced_angle(pos, p.w[4 * c + q]), &s, &co);
-      const float a = bf16_lo(in[q]), b = bf16_hi(in[q]);
-      out[q] = pack_bf16x2(a * co - b * s, a * s + b * co);
+    for (int q = 0; q < 4; ++q) sincosf(sgn * reduced_angle(pos, p.w[4 * c + q]), &sn[q], &cs[q]);
+    const int64_t base = tok * p.heads * per_row + c;
+#pragma unroll 4
+    for (int h = h0; h < h1; ++h) {
+      const uint4 v = p.x[base + static_cast<int64_t>(h) * per_row];
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = bf16_lo(in[q]), b = bf16_hi(in[q]);
+        out[q] = pack_bf16x2(a * cs[q] - b * sn[q], a * sn[q] + b * cs[q]);
+      }
+      p.y[base + static_cast<int64_t>(h) * per_row] = make_uint4(out[0], out[1], out[2], out[3]);
     }
-    p.y[u] = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
@@ -89,7 +102,7 @@ cudaError_t launch_rope(int64_t rows, int d, int heads, const int32_t* pos, cons
   p.pos = pos;
   p.x = static_cast<const uint4*>(x);
   p.y = static_cast<uint4*>(y);
-  int64_t blocks = (rows * (d / 8) + 255) / 256;
+  int64_t blocks = ((rows / heads) * ((heads + 7) / 8) * (d / 8) + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   rope_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
