@@ -299,7 +299,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // An MMA issue takes several instructions of the issuing thread, and the
     // score and read-out warps sharing a sub-partition leave it only part of
     // the issue slots; two issuers halve the instructions each one needs.
-    // Lane 0 alone waits and issues.  Ordering across the two:
+    // Ordering across the two:
     //   X: dV(s) reads P^T(s) before S(s+1) overwrites it (both A, in order).
     //   Y: dP(s) [A] -> score warps read it -> dQ(s) [B, after dS ready]
     //      -> read-out -> dP(s+1) [A, after dQ free].
@@ -308,15 +308,18 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     //      has completed.
     //   Q(s) stage: S(s) [A] completed before the scores of step s were
     //      seen, so B's commit after dK(s) releases it.
+    // Each issuer warp runs converged: all lanes wait (with a vote) and one
+    // elected lane issues, so that descriptors and tensor-memory addresses
+    // stay warp-uniform and the issue keeps its rate under the score warps'
+    // pressure.
     const bool issuer_a = warp == 1;
-    if (lane == 0 && *abort_flag == 0 && total > 0) {
+    if (__all_sync(0xffffffffu, *abort_flag == 0) && total > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(128, 128, false, false);    // S^T = K Q^T (fp16)
       constexpr uint32_t kIdDP = idesc_bf16_f32(128, 128, false, false);  // dP^T = V dO^T
       constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV += P^T dO
       constexpr uint32_t kIdDK = idesc_f16_f32(128, DH, false, true);     // dK += dS^T Q
       constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
-      auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
-      bool ok = wait1(C::kBarK16, 0);
+      bool ok = wait_all(C::kBarK16, 0);
       // Shared-memory descriptors as base words plus steps (K-major operands:
       // leading offset 16; MN-major: the next 64-column block), so that few
       // instructions sit between two MMAs; the loops stay rolled so that the
@@ -336,48 +339,48 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll 1
           for (int kk = 0; kk < DH / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            umma_ss_w(tmem + C::kTX, desc_step(dK_k, off), desc_step(dq, off), kIdS, kk > 0 ? 1u : 0u);
+            umma_ss_we(tmem + C::kTX, desc_step(dK_k, off), desc_step(dq, off), kIdS, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(C::kBarSFull));
+          umma_commit_we(bar(C::kBarSFull));
         };
         auto issue_dp = [&]() {  // dP^T = V dO^T -> Y
 #pragma unroll 1
           for (int kk = 0; kk < DV / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            umma_ss_w(tmem + C::kTY, desc_step(dV_k, off), desc_step(dDO_k, off), kIdDP, kk > 0 ? 1u : 0u);
+            umma_ss_we(tmem + C::kTY, desc_step(dV_k, off), desc_step(dDO_k, off), kIdDP, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(C::kBarDPFull));
+          umma_commit_we(bar(C::kBarDPFull));
         };
         // The two score warpgroups leave P^T for queries [0,64) in columns
         // [0,32) and for queries [64,128) in columns [64,96) of X.
         auto half_col = [](int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); };
-        if (ok) ok = wait1(C::kBarQFull + 0, 0);
+        if (ok) ok = wait_all(C::kBarQFull + 0, 0);
         if (ok) {
           tc_fence_after_sync();
           issue_s(0);
         }
-        if (ok) ok = wait1(C::kBarDOFull, 0);
+        if (ok) ok = wait_all(C::kBarDOFull, 0);
         if (ok) {
           tc_fence_after_sync();
           issue_dp();
         }
         for (int s = 0; s < total && ok; ++s) {
-          ok = wait1(C::kBarPReady, static_cast<uint32_t>(s & 1));
+          ok = wait_all(C::kBarPReady, static_cast<uint32_t>(s & 1));
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll 1
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ts_w(tmem + C::kTdV, tmem + C::kTX + half_col(kk), desc_step(dDO_mn, kk * 2048), kIdDV,
+            umma_ts_we(tmem + C::kTdV, tmem + C::kTX + half_col(kk), desc_step(dDO_mn, kk * 2048), kIdDV,
                       (s > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(C::kBarDOEmpty));   // dP(s) and dV(s) were dO(s)'s only readers
+          umma_commit_we(bar(C::kBarDOEmpty));   // dP(s) and dV(s) were dO(s)'s only readers
           if (s + 1 < total) {
-            ok = wait1(C::kBarQFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
+            ok = wait_all(C::kBarQFull + ((s + 1) & 1), static_cast<uint32_t>(((s + 1) >> 1) & 1));
             if (!ok) break;
             tc_fence_after_sync();
             issue_s(s + 1);
-            ok = wait1(C::kBarDOFull, static_cast<uint32_t>((s + 1) & 1));
-            if (ok) ok = wait1(C::kBarDQFree, static_cast<uint32_t>(s & 1));
-            if (ok) ok = wait1(C::kBarDKDone, static_cast<uint32_t>(s & 1));
+            ok = wait_all(C::kBarDOFull, static_cast<uint32_t>((s + 1) & 1));
+            if (ok) ok = wait_all(C::kBarDQFree, static_cast<uint32_t>(s & 1));
+            if (ok) ok = wait_all(C::kBarDKDone, static_cast<uint32_t>(s & 1));
             if (!ok) break;
             tc_fence_after_sync();
             issue_dp();
@@ -385,7 +388,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
       } else {
         for (int s = 0; s < total && ok; ++s) {
-          ok = wait1(C::kBarDSReady, static_cast<uint32_t>(s & 1));
+          ok = wait_all(C::kBarDSReady, static_cast<uint32_t>(s & 1));
           if (!ok) break;
           tc_fence_after_sync();
           // dQ(s) first, into Y (the score warps have read dP^T out of it),
@@ -394,20 +397,20 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           // view of the same swizzled tile.
 #pragma unroll 1
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            umma_ss_w(tmem + C::kTY, desc_step(dDS_mn, kk * 2048), desc_step(dK_mn, kk * 2048), kIdDQ,
+            umma_ss_we(tmem + C::kTY, desc_step(dDS_mn, kk * 2048), desc_step(dK_mn, kk * 2048), kIdDQ,
                       kk > 0 ? 1u : 0u);
-          umma_commit(bar(C::kBarDQFull));
+          umma_commit_we(bar(C::kBarDQFull));
 #pragma unroll 1
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            umma_ss_w(tmem + C::kTdK, desc_step(dDS_k, (kk >> 2) * C::kBlockBytes + (kk & 3) * 32),
+            umma_ss_we(tmem + C::kTdK, desc_step(dDS_k, (kk >> 2) * C::kBlockBytes + (kk & 3) * 32),
                       desc_step(dQ_mn, (s & 1) * C::kQTileBytes + kk * 2048), kIdDK, (s > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(C::kBarQEmpty + (s & 1)));
-          umma_commit(bar(C::kBarDKDone));
+          umma_commit_we(bar(C::kBarQEmpty + (s & 1)));
+          umma_commit_we(bar(C::kBarDKDone));
         }
       }
-      if (ok) umma_commit(bar(C::kBarDKDV));
+      if (ok) umma_commit_we(bar(C::kBarDKDV));
       int no_abort = 0;
-      umma_commit(bar(C::kBarDrain));
+      umma_commit_we(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
     }
     __syncwarp();

@@ -228,21 +228,27 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    if (lane == 0 && *abort_flag == 0 && n > 0) {
+    // The whole warp follows the schedule (waits end in a vote) and one
+    // elected lane issues, so that descriptors stay warp-uniform.
+    if (__all_sync(0xffffffffu, *abort_flag == 0) && n > 0) {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, DV, false, true);
-      auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
+      auto wait1 = [&](int idx, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar(idx), parity, abort_flag, limit));
+      };
+      const SmemDesc dq0 = sw128_desc_words(sbase + C::kOffQ, 16, 1024);
+      const SmemDesc dk0 = sw128_desc_words(sbase + C::kOffK, 16, 1024);
+      const SmemDesc dv0 = sw128_desc_words(sbase + C::kOffV, C::kBoxBytes, 1024);
       auto issue_qk = [&](int j) {   // S_{j&1} = Q K_j^T
         const int st = j & 1;
-        const uint32_t kb = sbase + C::kOffK + st * C::kKTileBytes;
+        const SmemDesc dk = desc_step(dk0, st * C::kKTileBytes);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          umma_ss(tmem + 128 * st, sw128_desc(sbase + C::kOffQ + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                  kIdQK, kk > 0 ? 1u : 0u);
+          umma_ss_we(tmem + 128 * st, desc_step(dq0, off), desc_step(dk, off), kIdQK, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(C::kBarSFull + st));
-        umma_commit(bar(C::kBarKEmpty + st));
+        umma_commit_we(bar(C::kBarSFull + st));
+        umma_commit_we(bar(C::kBarKEmpty + st));
       };
       bool ok = wait1(C::kBarQReady, 0);
       if (ok && n > 0) ok = wait1(C::kBarKFull + 0, 0);
@@ -256,13 +262,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
              wait1(C::kBarVReady + st, static_cast<uint32_t>((j >> 1) & 1));
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t vb = sbase + C::kOffV + st * C::kVTileBytes;
+        const SmemDesc dv = desc_step(dv0, st * C::kVTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          umma_ts(tmem + C::kTO, tmem + 128 * st + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024), kIdPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::kBarVEmpty + st));
-        umma_commit(bar(C::kBarPVDone));
+          umma_ts_we(tmem + C::kTO, tmem + 128 * st + kk * 8, desc_step(dv, kk * 2048), kIdPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_we(bar(C::kBarVEmpty + st));
+        umma_commit_we(bar(C::kBarPVDone));
         // The next key tile's scores go in right behind PV(j).
         if (j + 1 < n) {
           ok = wait1(C::kBarKFull + (st ^ 1), static_cast<uint32_t>(((j + 1) >> 1) & 1));
@@ -272,7 +278,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
       }
       int no_abort = 0;
-      umma_commit(bar(C::kBarDrain));
+      umma_commit_we(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
     }
     __syncwarp();

@@ -240,15 +240,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    // Lane 0 alone follows the schedule: every wait and every MMA issue is
-    // on the critical path of the tensor core, so no warp-wide votes or
-    // reconvergence points sit between them.
-    if (lane == 0 && *abort_flag == 0) {
+    // The whole warp follows the schedule and one elected lane issues: the
+    // descriptors and tensor-memory addresses stay warp-uniform, which keeps
+    // the issue rate while the softmax warps sharing this sub-partition take
+    // most issue slots.  Waits end in a vote, so the warp stays converged.
+    if (__all_sync(0xffffffffu, *abort_flag == 0)) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32(128, DV, false, true);   // fp16 P and V
-      // Shared-memory descriptors as base words plus constant steps: the
-      // softmax warps sharing this sub-partition take most issue slots, so
-      // every instruction between two MMAs delays the tensor core.
+      // Shared-memory descriptors as base words plus constant steps: every
+      // instruction between two MMAs delays the tensor core.
       const SmemDesc dq0 = sw128_desc_words(sbase + C::kOffQ, 16, 1024);
       const SmemDesc dk0 = sw128_desc_words(sbase + C::kOffK, 16, 1024);
       const SmemDesc dv0 = sw128_desc_words(sbase + C::kOffV, C::kBlockBytes, 1024);
@@ -258,17 +258,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          umma_ss_w(tmem + t * 128, desc_step(dq, off), desc_step(dk, off), kIdescQK, kk > 0 ? 1u : 0u);
+          umma_ss_we(tmem + t * 128, desc_step(dq, off), desc_step(dk, off), kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int vs, bool accumulate) {   // O_t += P_t V
         const SmemDesc dv = desc_step(dv0, vs * C::kVTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          umma_ts_w(tmem + 256 + t * DV, tmem + t * 128 + kk * 8, desc_step(dv, kk * 16 * 128), kIdescPV,
+          umma_ts_we(tmem + 256 + t * DV, tmem + t * 128 + kk * 8, desc_step(dv, kk * 16 * 128), kIdescPV,
                     (accumulate || kk > 0) ? 1u : 0u);
       };
-      auto wait1 = [&](int idx, uint32_t parity) -> bool { return mbar_wait(bar(idx), parity, abort_flag, limit); };
+      auto wait1 = [&](int idx, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar(idx), parity, abort_flag, limit));
+      };
       bool ok = wait1(C::kBarQFull, 0);
       if (ok && nkv > 0) {
         ok = wait1(C::kBarKFull + 0, 0);
@@ -277,9 +279,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           for (int t = 0; t < 2; ++t)
             if (ntiles[t] > 0) {
               issue_qk(t, 0);
-              umma_commit(bar(C::kBarSFull + t));
+              umma_commit_we(bar(C::kBarSFull + t));
             }
-          umma_commit(bar(C::kBarKEmpty + 0));
+          umma_commit_we(bar(C::kBarKEmpty + 0));
         }
       }
       for (int j = 0; j < nkv && ok; ++j) {
@@ -294,7 +296,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ok) break;
             tc_fence_after_sync();
             issue_pv(t, vs, j > 0);
-            if (j == ntiles[t] - 1) umma_commit(bar(C::kBarOFull + t));
+            if (j == ntiles[t] - 1) umma_commit_we(bar(C::kBarOFull + t));
           }
           if (j + 1 < ntiles[t]) {
             if (!k_next_ready) {
@@ -304,16 +306,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               k_next_ready = true;
             }
             issue_qk(t, kn);
-            umma_commit(bar(C::kBarSFull + t));
+            umma_commit_we(bar(C::kBarSFull + t));
           }
         }
         if (!ok) break;
-        umma_commit(bar(C::kBarVEmpty + vs));
-        if (k_next_ready) umma_commit(bar(C::kBarKEmpty + kn));
+        umma_commit_we(bar(C::kBarVEmpty + vs));
+        if (k_next_ready) umma_commit_we(bar(C::kBarKEmpty + kn));
       }
       // Every MMA issued above must finish before tensor memory is freed.
       int no_abort = 0;
-      umma_commit(bar(C::kBarDrain));
+      umma_commit_we(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
     }
     __syncwarp();

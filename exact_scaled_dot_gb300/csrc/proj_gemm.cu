@@ -137,7 +137,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant_
     }
   } else if (warp == 1) {
     // ============================ MMA issuer =============================
-    if (lane == 0 && *abort_flag == 0 && total > 0) {
+    // The whole warp follows the schedule (waits end in a vote) and one
+    // elected lane issues, so that descriptors stay warp-uniform.
+    if (__all_sync(0xffffffffu, *abort_flag == 0) && total > 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(kGM, kGN, AMN, BMN);
       // K-major tiles step 32 bytes per K=16 product inside the 128-byte
       // swizzle row; MN-major tiles step 16 rows (2048 bytes), their 64-wide
@@ -149,20 +151,21 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant_
       bool ok = true;
       for (int it = 0; it < total && ok; ++it) {
         const int st = it % kGStages;
-        ok = mbar_wait(bar(C::kBarFull + st), static_cast<uint32_t>((it / kGStages) & 1), abort_flag, limit);
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(C::kBarFull + st), static_cast<uint32_t>((it / kGStages) & 1), abort_flag, limit));
         if (!ok) break;
         tc_fence_after_sync();
         const SmemDesc da = desc_step(da0, st * C::kStageBytes), db = desc_step(db0, st * C::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < kGK / 16; ++kk)
-          umma_ss_w(tmem, desc_step(da, kk * kStepA), desc_step(db, kk * kStepB), kIdesc,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::kBarEmpty + st));
+          umma_ss_we(tmem, desc_step(da, kk * kStepA), desc_step(db, kk * kStepB), kIdesc,
+                     (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_we(bar(C::kBarEmpty + st));
       }
-      if (ok) umma_commit(bar(C::kBarAcc));
+      if (ok) umma_commit_we(bar(C::kBarAcc));
       // Every product issued above must finish before tensor memory is freed.
       int no_abort = 0;
-      umma_commit(bar(C::kBarDrain));
+      umma_commit_we(bar(C::kBarDrain));
       mbar_wait(bar(C::kBarDrain), 0, &no_abort, limit);
     }
     __syncwarp();

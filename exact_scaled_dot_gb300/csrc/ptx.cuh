@@ -26,7 +26,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
+// Warp index, broadcast from lane 0 so that the compiler knows it is the
+// same in every lane: branches on it (the warp roles) are then warp-uniform,
+// and code under them keeps warp-uniform values (descriptors, tensor-memory
+// addresses) in uniform registers instead of re-deriving them lane by lane
+// at every tcgen05 instruction.  Call from converged code.
+__device__ __forceinline__ uint32_t warp_id() { return __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0); }
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
 // 2^x with the MUFU unit (ex2.approx, flush-to-zero).  exp2(-inf) = +0.
@@ -374,6 +379,42 @@ __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, Smem
       "mov.b64 db, {%2, %3};\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n"
       :: "r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The same two products and the commit issued by a converged warp: every
+// lane executes them and `elect.sync` lets one lane (the lowest active one,
+// lane 0 of a converged warp) issue.  Kept warp-uniform, the descriptors and
+// addresses live in uniform registers, and the issue holds its rate while the
+// other warps of the sub-partition take most issue slots (measured: 67
+// cycles per 128x128x16 product against 123 for a lane-0-only issuer, under
+// two full-rate FMA warps per sub-partition).  All lanes must call them, and
+// a commit must come from the same warp as the products it tracks.
+__device__ __forceinline__ void umma_ss_we(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 r;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n"
+      :: "r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void umma_ts_we(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t.reg .b32 r;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n"
+      :: "r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void umma_commit_we(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n"
+      :: "r"(bar) : "memory");
 }
 
 // Arrive (once) on `bar` when every tcgen05 MMA issued so far by this
