@@ -276,7 +276,7 @@ def run_cuda(args):
         esd.attn_bwd_preprocess(Q, O, dO, ws, shape=shape, O_lo=O_lo)
         if ev is not None:
             ev[2].record(stream)
-        esd.attn_bwd_main(K, V, dO, LSE, ws, dK, dV, shape=shape, scale=scale, **mask)
+        esd.attn_bwd_main(K, V, LSE, ws, dK, dV, shape=shape, scale=scale, **mask)
         if ev is not None:
             ev[3].record(stream)
         esd.attn_bwd_finalize(ws, dQ, shape=shape, scale=scale)
@@ -322,7 +322,7 @@ def run_cuda(args):
     peaks, peak_src = load_peaks()
     bhq = w.B * w.Hq
     bytes_io = {
-        "attn_bwd_preprocess_kernel": (rows * w.dv * 2 * 3 + rows * 4 + rows * w.dh * 4 + bhq * (w.nq // 128 + 1) * 8
+        "attn_bwd_preprocess_kernel": (rows * w.dv * 2 * 4 + rows * 4 + rows * w.dh * 4 + bhq * (w.nq // 128 + 1) * 8
                                        + rows * w.dh * 2 * 2),
         "attn_bwd_finalize_kernel": rows * w.dh * 4 + rows * w.dh * 2,
     }

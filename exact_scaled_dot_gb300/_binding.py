@@ -86,7 +86,7 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                              _vp]
     lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
+    lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
     lib.attn_bwd_finalize.argtypes = [S, f, _vp, ctypes.c_size_t, _vp, _vp]
     lib.attn_visible_pairs.argtypes = [S, M]
     lib.attn_visible_pairs.restype = ctypes.c_int64
@@ -323,14 +323,14 @@ def attn_bwd_preprocess(Q, O, dO, workspace, *, shape: AttnShape, O_lo=None, str
     _check(rc, "attn_bwd_preprocess")
 
 
-def attn_bwd_main(K, V, dO, LSE, workspace, dK, dV, *, shape: AttnShape, causal=False, causal_offset=None,
+def attn_bwd_main(K, V, LSE, workspace, dK, dV, *, shape: AttnShape, causal=False, causal_offset=None,
                   kv_len=None, scale: Optional[float] = None, stream=None):
-    """Stage 2 of the backward (the key-tile-stationary main kernel; Q comes
-    from the fp16 copy stage 1 left in the workspace)."""
+    """Stage 2 of the backward (the key-tile-stationary main kernel; Q and dO
+    come from the fp16 copies stage 1 left in the workspace)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
     m = _MaskArg(causal, causal_offset, kv_len)
     rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(K), _ptr(V),
-                              _ptr(dO), _ptr(LSE), *_ws(workspace), _ptr(dK), _ptr(dV), _stream(K.device, stream))
+                              _ptr(LSE), *_ws(workspace), _ptr(dK), _ptr(dV), _stream(K.device, stream))
     _check(rc, "attn_bwd_main")
 
 

@@ -312,13 +312,14 @@ ShapeParams shape_params(const attn_shape* s) {
 int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq * s->n_q; }
 
 // Backward workspace: D [rows] | per-query-tile maxima float2 [B*Hq*nqt] |
-// fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h], each
-// 256-byte aligned.
+// fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h] | fp16 copy
+// of dO [rows * d_v], each 256-byte aligned.
 struct Workspace {
   float* D;
   float2* tilemax;
   float* dQacc;
   void* Q16;
+  void* dO16;
   size_t bytes;
 };
 
@@ -330,13 +331,15 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base) {
   const size_t off_t = round256(rows * sizeof(float));
   const size_t off_a = off_t + round256(tiles * sizeof(float2));
   const size_t off_q = off_a + round256(rows * static_cast<size_t>(s->d_h) * sizeof(float));
+  const size_t off_o = off_q + round256(rows * static_cast<size_t>(s->d_h) * 2);
   Workspace w;
   uint8_t* b = static_cast<uint8_t*>(base);
   w.D = reinterpret_cast<float*>(b);
   w.tilemax = reinterpret_cast<float2*>(b + off_t);
   w.dQacc = reinterpret_cast<float*>(b + off_a);
   w.Q16 = b + off_q;
-  w.bytes = off_q + round256(rows * static_cast<size_t>(s->d_h) * 2);
+  w.dO16 = b + off_o;
+  w.bytes = off_o + round256(rows * static_cast<size_t>(s->d_v) * 2);
   return w;
 }
 
@@ -577,14 +580,13 @@ int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O, c
   std::memset(&no_mask, 0, sizeof(no_mask));
   std::memset(&padded, 0, sizeof(padded));
   const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), no_mask, padded, shape->d_v, shape->d_h, Q,
-                                                   O, O_lo, dO, w.D, w.tilemax, w.dQacc, w.Q16,
+                                                   O, O_lo, dO, w.D, w.tilemax, w.dQacc, w.Q16, w.dO16,
                                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, const void* K, const void* V,
-                  const void* dO, const float* LSE, void* workspace, size_t workspace_bytes, void* dK, void* dV,
-                  void* stream) {
+                  const float* LSE, void* workspace, size_t workspace_bytes, void* dK, void* dV, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   BwdParams p;
@@ -592,7 +594,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
-  rc = check_ptrs({K, V, dO, LSE, dK, dV});
+  rc = check_ptrs({K, V, LSE, dK, dV});
   if (rc) return rc;
   rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
@@ -604,7 +606,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
   if (!make_tmap(&tq, w.Q16, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
-      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, dO, shape->d_v, shape->n_q, bhq) ||
+      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, w.dO16, shape->d_v, shape->n_q, bhq) ||
       !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
     return ATTN_ERR_CUDA;
   p.sh = shape_params(shape);
@@ -661,7 +663,7 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   if (rc) return rc;
   rc = attn_bwd_preprocess(shape, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
   if (rc) return rc;
-  rc = attn_bwd_main(shape, mask, scale, K, V, dO, LSE, workspace, workspace_bytes, dK, dV, stream);
+  rc = attn_bwd_main(shape, mask, scale, K, V, LSE, workspace, workspace_bytes, dK, dV, stream);
   if (rc) return rc;
   return attn_bwd_finalize(shape, scale, workspace, workspace_bytes, dQ, stream);
 }
@@ -915,12 +917,12 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   const Workspace w = workspace_layout_varlen(d, workspace);
   const ShapeParams sh = shape_params(&d.shape);
   cudaError_t e = launch_attn_bwd_preprocess(sh, d.mask, d.lay, v->d_v, v->d_h, Q, O, O_lo, dO, w.D, w.tilemax,
-                                             w.dQacc, w.Q16, st);
+                                             w.dQacc, w.Q16, w.dO16, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_packed(&tq, w.Q16, v->d_h, v->Hq, d.total_q) ||
       !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k) || !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k) ||
-      !make_tmap_packed(&tdo, dO, v->d_v, v->Hq, d.total_q) ||
+      !make_tmap_packed(&tdo, w.dO16, v->d_v, v->Hq, d.total_q) ||
       !make_tmap_acc_packed(&tdq, w.dQacc, v->d_h, v->Hq, d.total_q))
     return ATTN_ERR_CUDA;
   BwdParams p;

@@ -14,7 +14,8 @@
 // Three kernels:
 //   preprocess  D_i = sum_l dO_il O_il (equal to c_i of A.10.7 because
 //               O_i = sum_j A_ij v_j), zeroes the fp32 dQ accumulator and
-//               writes Q re-encoded as fp16 (the main kernel's operand).
+//               writes Q and dO re-encoded as fp16 (the main kernel's
+//               operands).
 //               O is taken as the bf16 output plus, when given, the
 //               forward's bf16 rounding residual, so D is not limited by the
 //               bf16 rounding of O.  Per 128-row query tile it also records
@@ -28,16 +29,17 @@
 //
 // Main-kernel warp roles (512 threads):
 //   warp 0      TMA producer: the K and V tile once, then the fp16 Q tile
-//               of every step into a two-stage ring and its dO tile into a
-//               single stage (dO(s) is dead once dV(s) is done).
-//   warp 1      MMA issuer (lane 0 issues).
+//               of every step into a two-stage ring and its fp16 dO tile
+//               into a single stage (dO(s) is dead once dV(s) is done).
+//   warps 1, 3  MMA issuers (one elected lane issues).
 //   warps 4-11  two "score" warpgroups, one per 64-query half of the step,
 //               thread = key row = TMEM lane:
 //               P^T = exp2(S^T scale log2e - LSE log2e) and
-//               dS^T = P^T (dP^T - D), written back to tensor memory and
-//               dS to shared memory for the dQ product.
-//   warps 12-15 converts K to fp16 in shared memory, reads dQ out of tensor
-//               memory into the accumulator and writes the final dK, dV.
+//               dS = P (dP - D), P^T written back to tensor memory (for
+//               dV) and dS to shared memory (for dQ and dK).
+//   warps 12-15 convert K and V to fp16 in shared memory, read dQ out of
+//               tensor memory into the accumulator and write the final dK,
+//               dV.
 // The producer/MMA and read-out warpgroups hand registers to the score
 // warpgroups (setmaxnreg), which hold 64 scores and the fp16 weights of a
 // step at once.
@@ -50,16 +52,19 @@
 //   |dS_ij| <= P_ij |dP_ij - D_i| <= max_i ||dO_i|| max_j ||v_j|| + max_i |D_i|
 // so that |2^e dS| <= 2^14: no fp16 overflow, and small gradients stay far
 // from the fp16 subnormal range.  The scale is exact and undone exactly when
-// dQ is read out and when dK is written.  Q and K are re-encoded as fp16 in
-// shared memory (the MMA takes one type for both operands; the conversion
-// is exact for |x| up to 65504 and saturates beyond; Q arrives re-encoded
-// from the preprocess kernel, K is converted once per CTA).  The weights P used
-// inside dS are kept as fp16 too; dP = dO V^T and dV = P^T dO stay bf16.
+// dQ is read out and when dK is written.  Every product runs in fp16 (the
+// MMA takes one type for both operands; the conversion of the bf16 inputs
+// is exact for |x| up to 65504 and saturates beyond): Q and dO arrive
+// re-encoded from the preprocess kernel, K and V are converted once per
+// CTA, and the weights P -- one fp16 rounding, used both in dS and as P^T in
+// dV = P^T dO -- keep 11 significant bits, where bf16 weights left dV
+// errors near the tolerance for keys whose gradient sums a few hundred
+// comparable terms.
 // Per step (query tile of 128 rows) the products are
 //   S^T = K Q^T -> X, dP^T = V dO^T -> Y, dV += P^T dO, dQ = dS K -> Y,
 //   dK += dS^T Q,
 // where tensor memory holds X [0,128), Y [128,256), dK [256, 256+DH) and
-// dV [256+DH, 256+DH+DV).  P^T (bf16) overwrites the first 64 columns of X
+// dV [256+DH, 256+DH+DV).  P^T (fp16) overwrites the first 64 columns of X
 // once the scores are consumed; dS goes to shared memory only, where it
 // serves both dQ and dK.  dQ reuses Y once the score warps have read dP^T
 // out of it, and is read out while dK runs, which leaves X free for the
@@ -98,7 +103,7 @@ struct BwdCfg {
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
   static constexpr int kBarDOFull = kBarQEmpty + 2;
   static constexpr int kBarDOEmpty = kBarDOFull + 1;
-  static constexpr int kBarK16 = kBarDOEmpty + 1;     // K tile re-encoded as fp16
+  static constexpr int kBarK16 = kBarDOEmpty + 1;     // K and V tiles re-encoded as fp16
   static constexpr int kBarScale = kBarK16 + 1;       // dS scale bound reduced
   static constexpr int kBarSFull = kBarScale + 1;
   static constexpr int kBarDPFull = kBarSFull + 1;
@@ -315,8 +320,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const bool issuer_a = warp == 1;
     if (__all_sync(0xffffffffu, *abort_flag == 0) && total > 0) {
       constexpr uint32_t kIdS = idesc_f16_f32(128, 128, false, false);    // S^T = K Q^T (fp16)
-      constexpr uint32_t kIdDP = idesc_bf16_f32(128, 128, false, false);  // dP^T = V dO^T
-      constexpr uint32_t kIdDV = idesc_bf16_f32(128, DV, false, true);    // dV += P^T dO
+      constexpr uint32_t kIdDP = idesc_f16_f32(128, 128, false, false);   // dP^T = V dO^T (fp16)
+      constexpr uint32_t kIdDV = idesc_f16_f32(128, DV, false, true);     // dV += P^T dO (fp16)
       constexpr uint32_t kIdDK = idesc_f16_f32(128, DH, false, true);     // dK += dS^T Q
       constexpr uint32_t kIdDQ = idesc_f16_f32(128, DH, true, true);      // dQ = dS K
       bool ok = wait_all(C::kBarK16, 0);
@@ -434,7 +439,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     float ds_scale = 1.f;
     if (ok && h == 0) {
       // ---- bound on |dS| for this CTA -> power-of-two scale ----
-      ok = wait_all(C::kBarKV, 0);
+      // (V is read once the read-out warps have re-encoded it as fp16.)
+      ok = wait_all(C::kBarK16, 0);
       float vn2 = 0.f;
       if (ok && !row_masked) {
 #pragma unroll
@@ -445,8 +451,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              vn2 = fmaf(bf16_lo(wv[k]), bf16_lo(wv[k]), vn2);
-              vn2 = fmaf(bf16_hi(wv[k]), bf16_hi(wv[k]), vn2);
+              vn2 = fmaf(f16_lo(wv[k]), f16_lo(wv[k]), vn2);
+              vn2 = fmaf(f16_hi(wv[k]), f16_hi(wv[k]), vn2);
             }
           }
         }
@@ -527,8 +533,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (!ok) break;
       tc_fence_after_sync();
       // P pass: this half's 64 scores in registers (two loads, one wait).
-      // P^T (bf16) goes into X over the columns already read; P (fp16)
-      // stays in registers for the dS pass.
+      // P^T (fp16) goes into X over the columns already read; the same
+      // words stay in registers for the dS pass.
       {
         uint32_t sa[32], sb[32];
         tmem_ld32_nowait(tX + 64 * h, sa);
@@ -560,8 +566,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
               x1 = (!row_masked && c + 1 >= cmin && (!PACKED || c + 1 < cmax)) ? x1 : -INFINITY;
             }
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            w[k >> 1] = pack_bf16x2(p0, p1);
-            pw[cq * 8 + (k >> 1)] = pack_f16x2(p0, p1);
+            const uint32_t pk = pack_f16x2(p0, p1);
+            w[k >> 1] = pk;
+            pw[cq * 8 + (k >> 1)] = pk;
           }
           tmem_st8_nowait(tX + 64 * h + cq * 8, w);
         }
@@ -645,16 +652,21 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     };
     float inv_scale = 1.f;
     if (ok && total > 0) {
-      // K once: rows in [kv_len, n_k) hold caller memory that may be anything
-      // (even NaN) and become zeros -- their dS entries are 0, but 0 * NaN
-      // would still poison dQ.  Rows at or beyond n_k arrive as zeros from
-      // the TMA bounds check.
+      // K and V once: rows in [kv_len, n_k) hold caller memory that may be
+      // anything (even NaN) and become zeros -- their dS entries are 0, but
+      // 0 * NaN would still poison dQ.  Rows at or beyond n_k arrive as
+      // zeros from the TMA bounds check.
       ok = wait_all(C::kBarKV, 0);
       if (ok) {
         uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
         for (int k = tid2; k < C::kKTileBytes / 16; k += 128) {
           const int krow = (k % (C::kBlockBytes / 16)) / 8;
           kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
+        }
+        uint4* vt = reinterpret_cast<uint4*>(smem + C::kOffV);
+        for (int k = tid2; k < C::kVTileBytes / 16; k += 128) {
+          const int vrow = (k % (C::kBlockBytes / 16)) / 8;
+          vt[k] = (j0 + vrow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(vt[k]);
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarK16));
@@ -792,13 +804,14 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 //   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
 //   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
 // the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
-// are re-encoded as fp16 for the main kernel (exact for |q| <= 65504,
+// and dO are re-encoded as fp16 for the main kernel (exact for |x| <= 65504,
 // saturating beyond).
 template <int DV, int DH>
 __global__ void __launch_bounds__(256)
 attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const uint4* __restrict__ O,
                            const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
-                           float2* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16) {
+                           float2* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
+                           uint4* __restrict__ dO16) {
   constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
   __shared__ float red[2][8];
   const int64_t bh = blockIdx.x;
@@ -859,6 +872,14 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
     const uint4 u = q_tile[k];
     q16_tile[k] = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
   }
+  // dO again, now warp-contiguous (the tile was just read, so this hits the
+  // caches), so that the fp16 copy is written in whole lines.
+  const uint4* g_tile = dO + tile_row0 * (DV / 8);
+  uint4* g16_tile = dO16 + tile_row0 * (DV / 8);
+  for (int64_t k = threadIdx.x; k < rows_here * (DV / 8); k += 256) {
+    const uint4 u = g_tile[k];
+    g16_tile[k] = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+  }
 }
 
 // The same for packed sequences (token-major rows, per-sequence lengths):
@@ -867,7 +888,7 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
 //   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
 //   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
 // the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
-// are re-encoded as fp16 for the main kernel (exact for |q| <= 65504,
+// and dO are re-encoded as fp16 for the main kernel (exact for |x| <= 65504,
 // saturating beyond).
 // Row addressing for packed sequences: row i of (b, h) is token cu_q[b] + i;
 // rows past the sequence's length are left alone.
@@ -890,7 +911,7 @@ __global__ void __launch_bounds__(256)
 attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt, const uint4* __restrict__ Q,
                            const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
                            const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
-                           float4* __restrict__ dQacc, uint4* __restrict__ Q16) {
+                           float4* __restrict__ dQacc, uint4* __restrict__ Q16, uint4* __restrict__ dO16) {
   constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
   __shared__ float red[2][8];
   const int64_t bh = blockIdx.x;
@@ -957,6 +978,13 @@ attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt
       Q16[at] =
           make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
     }
+    for (int k = threadIdx.x; k < rows_here * (DV / 8); k += 256) {
+      const int rr = k / (DV / 8), cc = k - rr * (DV / 8);
+      const int64_t at = rm.row(b, h, i0 + rr) * (DV / 8) + cc;
+      const uint4 u = dO[at];
+      dO16[at] =
+          make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+    }
   }
 }
 
@@ -995,15 +1023,17 @@ int grid_for(int64_t work_threads) {
 template <int DV, int DH>
 void launch_pre_t(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay, int nqt, const void* Q,
                   const void* O, const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
-                  void* Q16, cudaStream_t stream) {
+                  void* Q16, void* dO16, cudaStream_t stream) {
   (void)mask;
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(sh.B) * sh.Hq), static_cast<unsigned>(nqt));
   const uint4 *q = static_cast<const uint4*>(Q), *o = static_cast<const uint4*>(O);
   const uint4 *olo = static_cast<const uint4*>(O_lo), *g = static_cast<const uint4*>(dO);
   float4* acc = reinterpret_cast<float4*>(dQacc);
   uint4* q16 = static_cast<uint4*>(Q16);
+  uint4* do16 = static_cast<uint4*>(dO16);
   if (!lay.packed) {
-    attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, q, o, olo, g, D, tilemax, acc, q16);
+    attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, q, o, olo, g, D, tilemax, acc, q16,
+                                                                  do16);
   } else {
     PrepPacked rm;
     rm.n_q = sh.n_q;
@@ -1011,7 +1041,7 @@ void launch_pre_t(const ShapeParams& sh, const MaskParams& mask, const LayoutPar
     rm.total_q = lay.total_q;
     for (int b = 0; b <= sh.B; ++b) rm.cu_q[b] = lay.cu_q[b];
     attn_bwd_preprocess_packed_kernel<DV, DH><<<grid, 256, 0, stream>>>(rm, nqt, q, o, olo, g, D, tilemax, acc,
-                                                                        q16);
+                                                                        q16, do16);
   }
 }
 
@@ -1029,14 +1059,14 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
 cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay,
                                        int dv, int dh, const void* Q, const void* O, const void* O_lo,
                                        const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
-                                       cudaStream_t stream) {
+                                       void* dO16, cudaStream_t stream) {
   const int nqt = (sh.n_q + kTileM - 1) / kTileM;
   if (dv == 128 && dh == 128)
-    launch_pre_t<128, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
+    launch_pre_t<128, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, stream);
   else if (dv == 64 && dh == 64)
-    launch_pre_t<64, 64>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
+    launch_pre_t<64, 64>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, stream);
   else if (dv == 64 && dh == 128)
-    launch_pre_t<64, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, stream);
+    launch_pre_t<64, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, stream);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

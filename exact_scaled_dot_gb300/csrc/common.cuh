@@ -226,7 +226,7 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
 cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay,
                                        int dv, int dh, const void* Q, const void* O, const void* O_lo,
                                        const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
-                                       cudaStream_t stream);
+                                       void* dO16, cudaStream_t stream);
 cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap* tB, const GemmParams& p,
                              cudaStream_t stream);
 cudaError_t launch_rope(int64_t rows, int d, int heads, const int32_t* pos, const float* w, int inverse,

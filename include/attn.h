@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 6
+#define ATTN_ABI_VERSION 7
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -136,7 +136,8 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
 
 /* Bytes of device workspace the backward needs (attn_bwd and its three
  * stages): row terms D, per-128-row-tile bounds used to scale dS, an fp32
- * dQ accumulator and an fp16 copy of Q, about B*Hq*n_q*(6*d_h + 4) bytes.
+ * dQ accumulator and fp16 copies of Q and dO, about
+ * B*Hq*n_q*(6*d_h + 2*d_v + 4) bytes.
  * The layout is private to the library.  Returns 0 for an invalid shape. */
 size_t attn_bwd_workspace_bytes(const attn_shape* shape);
 
@@ -151,9 +152,10 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * its contents on entry do not matter.  Equivalent to the three stage calls
  * below, in order, on the same workspace.
  *
- * Precision: the products with dS (dK and dQ) take dS in fp16 scaled by a
- * power of two derived from a bound on |dS|, with Q and K re-encoded as fp16
- * (exact for |x| <= 65504; larger entries saturate). */
+ * Precision: every product runs in fp16 with fp32 accumulation: Q, K, V
+ * and dO are re-encoded as fp16 (exact for |x| <= 65504; larger entries
+ * saturate), the weights A are rounded once to fp16, and dS enters dK and
+ * dQ in fp16 scaled by a power of two derived from a bound on |dS|. */
 int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
              const void* O, const void* O_lo, const void* dO, const float* LSE,
@@ -162,19 +164,21 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
 
 /* Stage 1 of the backward: D_i = sum_l dO_il (O_il + O_lo_il) (= c_i of
  * A.10.7; O_lo may be NULL), per-tile bounds max ||dO_i|| and max |D_i|, a
- * zeroed dQ accumulator and Q re-encoded as fp16 (see attn_bwd), all in
- * `workspace`.  Q is the forward's bf16 query tensor. */
+ * zeroed dQ accumulator and Q and dO re-encoded as fp16 (see attn_bwd), all
+ * in `workspace`.  Q is the forward's bf16 query tensor, dO the bf16
+ * upstream gradient. */
 int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O,
                         const void* O_lo, const void* dO, void* workspace,
                         size_t workspace_bytes, void* stream);
 
 /* Stage 2: the key-tile-stationary main kernel.  Recomputes A from the
- * workspace's fp16 copy of Q (written by stage 1), K and LSE, writes dK
- * (scaled) and dV (bf16) and adds the dS K products into the workspace's
- * fp32 dQ accumulator (zeroed by stage 1). */
+ * workspace's fp16 copy of Q (written by stage 1), K and LSE, takes dO from
+ * the workspace's fp16 copy (also written by stage 1), writes dK (scaled)
+ * and dV (bf16) and adds the dS K products into the workspace's fp32 dQ
+ * accumulator (zeroed by stage 1). */
 int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale,
-                  const void* K, const void* V, const void* dO,
-                  const float* LSE, void* workspace, size_t workspace_bytes,
+                  const void* K, const void* V, const float* LSE,
+                  void* workspace, size_t workspace_bytes,
                   void* dK, void* dV, void* stream);
 
 /* Stage 3: dQ = scale * accumulator, rounded to bf16. */
@@ -247,7 +251,7 @@ int64_t attn_varlen_visible_pairs(const attn_varlen* v);
 int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
                     void* O, float* LSE, void* O_lo, void* stream);
 
-/* Workspace of attn_bwd_varlen, about T_q*Hq*(6*d_h + 4) bytes; 0 when the
+/* Workspace of attn_bwd_varlen, about T_q*Hq*(6*d_h + 2*d_v + 4) bytes; 0 when the
  * description is invalid. */
 size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v);
 

@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 6
+    assert esd.attn_abi_version() == 7
 
 
 def test_strerror_covers_every_code(lib):
@@ -113,8 +113,9 @@ def test_bwd_workspace_checks(lib):
     need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
     rows = 2 * 4 * 100
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
-    # D | tile bounds | fp32 dQ accumulator | fp16 copy of Q
-    assert need == r256(rows * 4) + r256(2 * 4 * 1 * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
+    # D | tile bounds | fp32 dQ accumulator | fp16 copies of Q and dO
+    assert need == (r256(rows * 4) + r256(2 * 4 * 1 * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
+                    + r256(rows * s.d_v * 2))
     p = ctypes.c_void_p(256)
     m = _mask()
     args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5
@@ -207,7 +208,8 @@ def test_varlen_workspace_and_pairs(lib):
     rows = cq[-1] * 4
     nqt = (257 + 127) // 128
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
-    assert need == r256(rows * 4) + r256(3 * 4 * nqt * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
+    assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
+                    + r256(rows * 64 * 2))
     p = ctypes.c_void_p(512)
     args = [ctypes.byref(v), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5
     assert lib.attn_bwd_varlen(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE

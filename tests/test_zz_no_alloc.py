@@ -64,7 +64,7 @@ def test_noalloc_refuses_problems_beyond_its_buffer():
     import exact_scaled_dot_gb300 as esd
     from exact_scaled_dot_gb300 import _binding as bnd
     lib = esd.load()
-    shape = bnd.make_shape(4, 16, 16, 2048, 2048, 128, 128)   # about 68 MB of scratch
+    shape = bnd.make_shape(4, 16, 16, 2048, 2048, 128, 128)   # about 135 MB of scratch
     assert esd.attn_bwd_workspace_bytes(4, 16, 16, 2048, 2048, 128, 128) > esd.attn_bwd_noalloc_max_scratch_bytes()
     mask = bnd.AttnMask(1, 0, bnd.ATTN_OFFSET_DEFAULT, ctypes.POINTER(ctypes.c_int32)())
     p = ctypes.c_void_p(256)
