@@ -103,8 +103,9 @@ struct BwdCfg {
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
   static constexpr int kBarDOFull = kBarQEmpty + 2;
   static constexpr int kBarDOEmpty = kBarDOFull + 1;
-  static constexpr int kBarK16 = kBarDOEmpty + 1;     // K and V tiles re-encoded as fp16
-  static constexpr int kBarScale = kBarK16 + 1;       // dS scale bound reduced
+  static constexpr int kBarK16 = kBarDOEmpty + 1;     // K tile re-encoded as fp16
+  static constexpr int kBarV16 = kBarK16 + 1;         // V tile re-encoded as fp16 (after the bound read it)
+  static constexpr int kBarScale = kBarV16 + 1;       // dS scale bound reduced
   static constexpr int kBarSFull = kBarScale + 1;
   static constexpr int kBarDPFull = kBarSFull + 1;
   static constexpr int kBarPReady = kBarDPFull + 1;
@@ -201,6 +202,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDOFull), 1);
     mbar_init(bar(C::kBarDOEmpty), 1);
     mbar_init(bar(C::kBarK16), 128);
+    mbar_init(bar(C::kBarV16), 128);
     mbar_init(bar(C::kBarScale), 128);
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
@@ -365,6 +367,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           issue_s(0);
         }
         if (ok) ok = wait_all(C::kBarDOFull, 0);
+        if (ok) ok = wait_all(C::kBarV16, 0);
         if (ok) {
           tc_fence_after_sync();
           issue_dp();
@@ -439,8 +442,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     float ds_scale = 1.f;
     if (ok && h == 0) {
       // ---- bound on |dS| for this CTA -> power-of-two scale ----
-      // (V is read once the read-out warps have re-encoded it as fp16.)
-      ok = wait_all(C::kBarK16, 0);
+      // (from the bf16 V tile; the read-out warps re-encode it only after
+      // this bound is published)
+      ok = wait_all(C::kBarKV, 0);
       float vn2 = 0.f;
       if (ok && !row_masked) {
 #pragma unroll
@@ -451,8 +455,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              vn2 = fmaf(f16_lo(wv[k]), f16_lo(wv[k]), vn2);
-              vn2 = fmaf(f16_hi(wv[k]), f16_hi(wv[k]), vn2);
+              vn2 = fmaf(bf16_lo(wv[k]), bf16_lo(wv[k]), vn2);
+              vn2 = fmaf(bf16_hi(wv[k]), bf16_hi(wv[k]), vn2);
             }
           }
         }
@@ -655,7 +659,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       // K and V once: rows in [kv_len, n_k) hold caller memory that may be
       // anything (even NaN) and become zeros -- their dS entries are 0, but
       // 0 * NaN would still poison dQ.  Rows at or beyond n_k arrive as
-      // zeros from the TMA bounds check.
+      // zeros from the TMA bounds check.  K first (the first product needs
+      // it); V once the score warps have taken the |dS| bound from it.
       ok = wait_all(C::kBarKV, 0);
       if (ok) {
         uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
@@ -663,16 +668,20 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           const int krow = (k % (C::kBlockBytes / 16)) / 8;
           kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
         }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::kBarK16));
+      }
+      if (ok) ok = wait_all(C::kBarScale, 0);
+      if (ok) {
+        inv_scale = exp2_int(-scale_exponent());
         uint4* vt = reinterpret_cast<uint4*>(smem + C::kOffV);
         for (int k = tid2; k < C::kVTileBytes / 16; k += 128) {
           const int vrow = (k % (C::kBlockBytes / 16)) / 8;
           vt[k] = (j0 + vrow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(vt[k]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(C::kBarK16));
+        mbar_arrive(bar(C::kBarV16));
       }
-      if (ok) ok = wait_all(C::kBarScale, 0);
-      if (ok) inv_scale = exp2_int(-scale_exponent());
     }
     // dQ read-out: each warp takes its 32 query rows of the tile (in Y) into
     // registers a 64-column round at a time and releases Y after the last
