@@ -473,6 +473,12 @@ def run_cuda(args):
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n_q": w.nq, "n_k": w.nk,
                        "d_h": w.dh, "d_v": w.dv, "causal": w.causal, "kv_len": kv, "seed": w.seed,
                        "visible_pairs": pairs, "flops_per_step": flops_fwd + flops_bwd,
+                       # The backward's five products cost 2(3 d_h + 2 d_v) per pair; the metric counts
+                       # 2(2 d_h + 3 d_v).  Equal for d_h = d_v.
+                       "tflops_five_product_count": job_throughput(pairs * (ff + 2 * (3 * w.dh + 2 * w.dv)), world,
+                                                                   ms_per_step),
+                       "arithmetic": "bf16 inputs and outputs; Q K^T in bf16, P V and every backward product in "
+                                     "fp16 (exact re-encoding of the bf16 operands), fp32 accumulation",
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (about %.0f MB touched per step)" % (
                            sum(x.numel() * x.element_size() for x in (Q, K, V, dO, O, O_lo, LSE, dQ, dK, dV, ws))
