@@ -654,6 +654,23 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     auto to_f16 = [](uint4 u) {
       return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
     };
+    // A K or V tile (`n16` 16-byte chunks, a multiple of 1024) re-encoded
+    // as fp16 in place, rows past kv_len zeroed: eight loads in flight per
+    // thread before their stores (one load-store round trip per chunk would
+    // take several thousand cycles for a tile).
+    auto tile_to_f16 = [&](uint4* t, int n16) {
+      for (int i0 = 0; i0 < n16 / 128; i0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = t[tid2 + 128 * (i0 + i)];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int k = tid2 + 128 * (i0 + i);
+          const int row = (k % (C::kBlockBytes / 16)) / 8;
+          t[k] = (j0 + row >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(v[i]);
+        }
+      }
+    };
     float inv_scale = 1.f;
     if (ok && total > 0) {
       // K and V once: rows in [kv_len, n_k) hold caller memory that may be
@@ -663,22 +680,14 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       // it); V once the score warps have taken the |dS| bound from it.
       ok = wait_all(C::kBarKV, 0);
       if (ok) {
-        uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
-        for (int k = tid2; k < C::kKTileBytes / 16; k += 128) {
-          const int krow = (k % (C::kBlockBytes / 16)) / 8;
-          kt[k] = (j0 + krow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(kt[k]);
-        }
+        tile_to_f16(reinterpret_cast<uint4*>(smem + C::kOffK), C::kKTileBytes / 16);
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarK16));
       }
       if (ok) ok = wait_all(C::kBarScale, 0);
       if (ok) {
         inv_scale = exp2_int(-scale_exponent());
-        uint4* vt = reinterpret_cast<uint4*>(smem + C::kOffV);
-        for (int k = tid2; k < C::kVTileBytes / 16; k += 128) {
-          const int vrow = (k % (C::kBlockBytes / 16)) / 8;
-          vt[k] = (j0 + vrow >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(vt[k]);
-        }
+        tile_to_f16(reinterpret_cast<uint4*>(smem + C::kOffV), C::kVTileBytes / 16);
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarV16));
       }
