@@ -317,7 +317,7 @@ def _ws(workspace):
 
 
 def attn_bwd_preprocess(Q, O, dO, workspace, *, shape: AttnShape, O_lo=None, stream=None):
-    """Stage 1 of the backward (row terms, tile bounds, zeroed dQ accumulator, fp16 copy of Q)."""
+    """Stage 1 of the backward (row terms, tile bounds, zeroed dQ accumulator, fp16 copies of Q and dO)."""
     rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(Q), _ptr(O), _ptr(O_lo), _ptr(dO), *_ws(workspace),
                                     _stream(O.device, stream))
     _check(rc, "attn_bwd_preprocess")
