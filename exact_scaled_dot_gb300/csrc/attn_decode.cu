@@ -18,12 +18,15 @@
 //   normalised within the range and its log-sum-exp; the merge kernel
 //   combines them, O = sum_s exp(LSE_s - LSE) O_s with LSE = log sum_s
 //   exp(LSE_s), which is the same softmax in real arithmetic.
-// * One row tile per CTA; per key tile QK(j), the softmax, then PV(j), with
-//   QK(j+1) issued right behind PV(j).  (Issuing the next tile's scores
-//   before P(j) was complete, into the second score buffer, gave wrong
-//   products for the second half of a tile's weights in tests with more
-//   than 32 rows; the serial order is exact, and a decode step is bound by
-//   streaming K and V from memory rather than by the tensor core.)
+// * One row tile per CTA; the scores run one key tile ahead of the softmax
+//   in two buffers: QK(j+1) is computed while the softmax works on tile j,
+//   and QK(j+2) is issued right behind PV(j), which has read P(j) out of the
+//   buffer QK(j+2) overwrites (the tensor core runs one thread's products
+//   in order).  A softmax warp can then be one tile ahead of the others,
+//   which is why the P-ready barriers are per buffer, and a warp that has
+//   finished its last tile may find two PV products still pending, which is
+//   why the last one completes a barrier of its own (a parity wait on the
+//   PV-done barrier would match the phase before them).
 //
 // CTA: 256 threads.  warp 0 TMA producer (K and V tiles, two-stage rings),
 // warp 1 MMA issuer (lane 0), warp 2 gathers Q and then zeroes padded V rows
@@ -63,7 +66,8 @@ struct DecCfg {
   // its arrival for tile j+1 must not count towards tile j.
   static constexpr int kBarPReady = kBarSFull + 2;
   static constexpr int kBarPVDone = kBarPReady + 2;
-  static constexpr int kBarDrain = kBarPVDone + 1;
+  static constexpr int kBarOFull = kBarPVDone + 1;     // the last PV product done (single use)
+  static constexpr int kBarDrain = kBarOFull + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -127,6 +131,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     mbar_init(bar(C::kBarPReady + 0), 128);
     mbar_init(bar(C::kBarPReady + 1), 128);
     mbar_init(bar(C::kBarPVDone), 1);
+    mbar_init(bar(C::kBarOFull), 1);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
     *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
@@ -250,11 +255,15 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         umma_commit_we(bar(C::kBarSFull + st));
         umma_commit_we(bar(C::kBarKEmpty + st));
       };
+      // Scores run one key tile ahead: QK(j+1) is in its own buffer while
+      // the softmax works on tile j, and QK(j+2) goes in right behind PV(j),
+      // which has read P(j) out of the buffer QK(j+2) overwrites.
       bool ok = wait1(C::kBarQReady, 0);
-      if (ok && n > 0) ok = wait1(C::kBarKFull + 0, 0);
-      if (ok && n > 0) {
+      for (int j = 0; j < 2 && j < n && ok; ++j) {
+        ok = wait1(C::kBarKFull + j, 0);
+        if (!ok) break;
         tc_fence_after_sync();
-        issue_qk(0);
+        issue_qk(j);
       }
       for (int j = 0; j < n && ok; ++j) {
         const int st = j & 1;
@@ -269,12 +278,12 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                      (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit_we(bar(C::kBarVEmpty + st));
         umma_commit_we(bar(C::kBarPVDone));
-        // The next key tile's scores go in right behind PV(j).
-        if (j + 1 < n) {
-          ok = wait1(C::kBarKFull + (st ^ 1), static_cast<uint32_t>(((j + 1) >> 1) & 1));
+        if (j == n - 1) umma_commit_we(bar(C::kBarOFull));
+        if (j + 2 < n) {
+          ok = wait1(C::kBarKFull + st, static_cast<uint32_t>(((j + 2) >> 1) & 1));
           if (!ok) break;
           tc_fence_after_sync();
-          issue_qk(j + 1);
+          issue_qk(j + 2);
         }
       }
       int no_abort = 0;
@@ -382,8 +391,11 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
     // ---- epilogue ----
     if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::kBarPVDone), static_cast<uint32_t>((n - 1) & 1), abort_flag, limit));
+      // The scores of tile n-1 imply only PV(n-3) done (QK(n-1) followed it),
+      // so PV(n-2) and PV(n-1) may both be pending, and a parity wait on the
+      // PV-done barrier could match the phase before them: the last product
+      // has a barrier of its own.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull), 0, abort_flag, limit));
       tc_fence_after_sync();
     }
     if (ok) {
