@@ -50,17 +50,20 @@ struct DecCfg {
   static constexpr int kQTileBytes = 128 * DH * 2;
   static constexpr int kKTileBytes = 128 * DH * 2;
   static constexpr int kVTileBytes = 128 * DV * 2;
+  // K and V rings of three stages: a CTA streams its key range once, so
+  // the more tiles in flight, the more of the HBM latency is hidden.
+  static constexpr int kStages = 3;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQTileBytes;
-  static constexpr int kOffV = kOffK + 2 * kKTileBytes;
-  static constexpr int kOffBar = kOffV + 2 * kVTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kKTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kVTileBytes;
   static constexpr int kBarQReady = 0;
-  static constexpr int kBarKFull = 1;                  // [2]
-  static constexpr int kBarKEmpty = kBarKFull + 2;     // [2]
-  static constexpr int kBarVFull = kBarKEmpty + 2;     // [2]
-  static constexpr int kBarVReady = kBarVFull + 2;     // [2]
-  static constexpr int kBarVEmpty = kBarVReady + 2;    // [2]
-  static constexpr int kBarSFull = kBarVEmpty + 2;     // [2]
+  static constexpr int kBarKFull = 1;                        // [kStages]
+  static constexpr int kBarKEmpty = kBarKFull + kStages;     // [kStages]
+  static constexpr int kBarVFull = kBarKEmpty + kStages;     // [kStages]
+  static constexpr int kBarVReady = kBarVFull + kStages;     // [kStages]
+  static constexpr int kBarVEmpty = kBarVReady + kStages;    // [kStages]
+  static constexpr int kBarSFull = kBarVEmpty + kStages;     // [2], one per score buffer
   // [2], one per score buffer: a softmax warp may run one tile ahead of the
   // others (the scores of tile j+1 are computed before P(j) is complete), so
   // its arrival for tile j+1 must not count towards tile j.
@@ -120,14 +123,14 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   // ---- setup ----
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQReady), 64);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
       mbar_init(bar(C::kBarKEmpty + s), 1);
       mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarVReady + s), 1);
       mbar_init(bar(C::kBarVEmpty + s), 1);
-      mbar_init(bar(C::kBarSFull + s), 1);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(C::kBarSFull + s), 1);
     mbar_init(bar(C::kBarPReady + 0), 128);
     mbar_init(bar(C::kBarPReady + 1), 128);
     mbar_init(bar(C::kBarPVDone), 1);
@@ -152,18 +155,18 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     if (lane == 0 && *abort_flag == 0 && n > 0) {
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
+      int k_issued[C::kStages] = {}, v_issued[C::kStages] = {};
       for (int j = 0; j < n; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = static_cast<uint32_t>(((j >> 1) - 1) & 1);
+        const int st = j % C::kStages;
+        const uint32_t ph = static_cast<uint32_t>((j / C::kStages - 1) & 1);
         const int32_t row = (t0 + j) * kTileN;
-        if (j >= 2 && !mbar_wait(bar(C::kBarKEmpty + st), ph, abort_flag, limit)) break;
+        if (j >= C::kStages && !mbar_wait(bar(C::kBarKEmpty + st), ph, abort_flag, limit)) break;
         mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kKTileBytes);
         for (int c = 0; c < DH / 64; ++c)
           tma_load_3d(sbase + C::kOffK + st * C::kKTileBytes + c * C::kBoxBytes, &tmK, bar(C::kBarKFull + st),
                       c * 64, row, bkv);
         ++k_issued[st];
-        if (j >= 2 && !mbar_wait(bar(C::kBarVEmpty + st), ph, abort_flag, limit)) break;
+        if (j >= C::kStages && !mbar_wait(bar(C::kBarVEmpty + st), ph, abort_flag, limit)) break;
         mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kVTileBytes);
         for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(sbase + C::kOffV + st * C::kVTileBytes + c * C::kBoxBytes, &tmV, bar(C::kBarVFull + st),
@@ -172,7 +175,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       }
       if (*abort_flag) {
         int no_abort = 0;
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
           if (k_issued[s]) mbar_wait(bar(C::kBarKFull + s), (k_issued[s] - 1) & 1, &no_abort, limit);
           if (v_issued[s]) mbar_wait(bar(C::kBarVFull + s), (v_issued[s] - 1) & 1, &no_abort, limit);
         }
@@ -208,9 +211,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       // poison O, so those V rows are zeroed before the PV product.
       bool ok = *abort_flag == 0;
       for (int j = 0; j < n && ok; ++j) {
-        const int st = j & 1;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(C::kBarVFull + st), static_cast<uint32_t>((j >> 1) & 1), abort_flag, limit));
+        const int st = j % C::kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVFull + st), static_cast<uint32_t>((j / C::kStages) & 1),
+                                               abort_flag, limit));
         if (!ok) break;
         const int64_t base = static_cast<int64_t>(t0 + j) * kTileN;
         int64_t r0 = klen - base, r1 = static_cast<int64_t>(p.sh.n_k) - base;
@@ -244,43 +247,43 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       const SmemDesc dq0 = sw128_desc_words(sbase + C::kOffQ, 16, 1024);
       const SmemDesc dk0 = sw128_desc_words(sbase + C::kOffK, 16, 1024);
       const SmemDesc dv0 = sw128_desc_words(sbase + C::kOffV, C::kBoxBytes, 1024);
-      auto issue_qk = [&](int j) {   // S_{j&1} = Q K_j^T
-        const int st = j & 1;
-        const SmemDesc dk = desc_step(dk0, st * C::kKTileBytes);
+      auto issue_qk = [&](int j) {   // S_{j&1} = Q K_j^T, K_j in stage j % kStages
+        const int sb = j & 1, kst = j % C::kStages;
+        const SmemDesc dk = desc_step(dk0, kst * C::kKTileBytes);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          umma_ss_we(tmem + 128 * st, desc_step(dq0, off), desc_step(dk, off), kIdQK, kk > 0 ? 1u : 0u);
+          umma_ss_we(tmem + 128 * sb, desc_step(dq0, off), desc_step(dk, off), kIdQK, kk > 0 ? 1u : 0u);
         }
-        umma_commit_we(bar(C::kBarSFull + st));
-        umma_commit_we(bar(C::kBarKEmpty + st));
+        umma_commit_we(bar(C::kBarSFull + sb));
+        umma_commit_we(bar(C::kBarKEmpty + kst));
       };
       // Scores run one key tile ahead: QK(j+1) is in its own buffer while
       // the softmax works on tile j, and QK(j+2) goes in right behind PV(j),
       // which has read P(j) out of the buffer QK(j+2) overwrites.
       bool ok = wait1(C::kBarQReady, 0);
       for (int j = 0; j < 2 && j < n && ok; ++j) {
-        ok = wait1(C::kBarKFull + j, 0);
+        ok = wait1(C::kBarKFull + j % C::kStages, static_cast<uint32_t>((j / C::kStages) & 1));
         if (!ok) break;
         tc_fence_after_sync();
         issue_qk(j);
       }
       for (int j = 0; j < n && ok; ++j) {
-        const int st = j & 1;
-        ok = wait1(C::kBarPReady + st, static_cast<uint32_t>((j >> 1) & 1)) &&
-             wait1(C::kBarVReady + st, static_cast<uint32_t>((j >> 1) & 1));
+        const int sb = j & 1, vst = j % C::kStages;
+        ok = wait1(C::kBarPReady + sb, static_cast<uint32_t>((j >> 1) & 1)) &&
+             wait1(C::kBarVReady + vst, static_cast<uint32_t>((j / C::kStages) & 1));
         if (!ok) break;
         tc_fence_after_sync();
-        const SmemDesc dv = desc_step(dv0, st * C::kVTileBytes);
+        const SmemDesc dv = desc_step(dv0, vst * C::kVTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          umma_ts_we(tmem + C::kTO, tmem + 128 * st + kk * 8, desc_step(dv, kk * 2048), kIdPV,
+          umma_ts_we(tmem + C::kTO, tmem + 128 * sb + kk * 8, desc_step(dv, kk * 2048), kIdPV,
                      (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_we(bar(C::kBarVEmpty + st));
+        umma_commit_we(bar(C::kBarVEmpty + vst));
         umma_commit_we(bar(C::kBarPVDone));
         if (j == n - 1) umma_commit_we(bar(C::kBarOFull));
         if (j + 2 < n) {
-          ok = wait1(C::kBarKFull + st, static_cast<uint32_t>(((j + 2) >> 1) & 1));
+          ok = wait1(C::kBarKFull + (j + 2) % C::kStages, static_cast<uint32_t>(((j + 2) / C::kStages) & 1));
           if (!ok) break;
           tc_fence_after_sync();
           issue_qk(j + 2);
