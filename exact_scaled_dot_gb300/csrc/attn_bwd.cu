@@ -914,7 +914,6 @@ struct PrepPacked {
   int32_t n_q, Hq;
   int64_t total_q;
   int32_t cu_q[ATTN_MAX_BATCH + 1];
-  static constexpr bool kPacked = true;
   __device__ __forceinline__ int64_t len(int b) const { return static_cast<int64_t>(cu_q[b + 1]) - cu_q[b]; }
   __device__ __forceinline__ int64_t row(int b, int h, int64_t i) const {
     return (static_cast<int64_t>(cu_q[b]) + i) * Hq + h;

@@ -28,9 +28,10 @@
 //   why the last one completes a barrier of its own (a parity wait on the
 //   PV-done barrier would match the phase before them).
 //
-// CTA: 256 threads.  warp 0 TMA producer (K and V tiles, two-stage rings),
-// warp 1 MMA issuer (lane 0), warp 2 gathers Q and then zeroes padded V rows
-// as tiles land, warp 3 helps gather Q, warps 4-7 softmax (thread = row).
+// CTA: 256 threads.  warp 0 TMA producer (K and V tiles, three-stage
+// rings), warp 1 MMA issuer (converged, one elected lane issues), warp 2
+// gathers Q and then zeroes padded V rows as tiles land, warp 3 helps gather
+// Q, warps 4-7 softmax (thread = row).
 // Tensor memory: scores of even and odd key tiles in S_0 [0,128) and
 // S_1 [128,256) (P as bf16 pairs over the first 64 columns of its buffer),
 // O [256, 256 + DV).

@@ -14,7 +14,7 @@
 // CTA = two 128-row query tiles of one (batch, query head), sharing every
 // K/V tile the CTA loads.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K_j and V_j into rings.
-//   warp 1      MMA issuer (lane 0 alone waits and issues): S_t = Q_t K_j^T
+//   warp 1      MMA issuer (converged; one elected lane issues): S_t = Q_t K_j^T
 //               into tensor memory, O_t += P_t V_j with P_t read back from
 //               tensor memory.
 //   warps 2, 3  re-encode every V tile as fp16 in place once it has landed,

@@ -15,8 +15,8 @@
 //
 // CTA: one 128 x 256 output tile, 256 threads.  warp 0 TMA producer (two
 // stages of 64 contraction steps: A 16 KB + B 32 KB), warp 1 MMA issuer
-// (lane 0; M=128, N=256, four K=16 products per stage), warps 4-7 epilogue
-// (thread = output row = TMEM lane).  96 KB of shared memory and 256 tensor
+// (converged, one elected lane issues; M=128, N=256, four K=16 products per
+// stage), warps 4-7 epilogue (thread = output row = TMEM lane).  96 KB of shared memory and 256 tensor
 // memory columns, so two CTAs share an SM and one's epilogue overlaps the
 // other's products.  Contraction tails, rows and columns past the matrix
 // edges read as zeros (TMA bounds fill); the epilogue writes only inside C.

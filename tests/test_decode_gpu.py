@@ -6,7 +6,8 @@ Every case is compared element by element with the fp64 oracle (O within
 same inputs.  The shapes cover single-query decode (MQA, GQA), small chunks
 of new queries over a history (the causal offset n_k - n_q), a chunk that
 spans two row tiles, full tiles, no split, d = 64 and d_v = 64, key padding
-with NaN in the padded rows, and a peaked softmax.
+with NaN in the padded rows, a peaked softmax, and full 128-row tiles over
+key ranges of one, two, three and five tiles.
 """
 import numpy as np
 import pytest
@@ -49,6 +50,17 @@ CASES = {
                              seed=48),
     "explicit_offset": Workload("explicit_offset", B=1, Hq=8, Hkv=1, nq=3, nk=1200, dh=128, dv=128, causal=True,
                                 offset=700, seed=49),
+    # Full 128-row tiles over key ranges of one, two, three and (split) five
+    # tiles: the scores run one tile ahead of the softmax, so the first and
+    # last tiles of a range and the wait for the last PV product are edge
+    # cases, with four softmax warps in play.
+    "rows128_one_tile": Workload("rows128_one_tile", B=2, Hq=16, Hkv=2, nq=16, nk=100, dh=128, dv=128, causal=True,
+                                 seed=50),
+    "rows128_two_tiles": Workload("rows128_two_tiles", B=2, Hq=16, Hkv=2, nq=16, nk=250, dh=128, dv=128, seed=51),
+    "rows128_three_tiles": Workload("rows128_three_tiles", B=2, Hq=16, Hkv=2, nq=16, nk=300, dh=128, dv=64,
+                                    causal=True, kv_len_range=(260, 300), seed=52),
+    "rows128_five_tiles_split": Workload("rows128_five_tiles_split", B=1, Hq=16, Hkv=2, nq=16, nk=600, dh=128,
+                                         dv=128, causal=True, seed=53),
 }
 
 
