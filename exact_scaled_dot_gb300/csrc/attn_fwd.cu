@@ -61,7 +61,10 @@ template <int DH, int DV>
 struct FwdCfg {
   static constexpr int kQTiles = 2;
   static constexpr int kKStages = (DH == 128) ? 2 : 3;
-  static constexpr int kVStages = (DV == 128) ? 2 : 3;
+  // Three V stages at every width: a V tile then lands a period earlier,
+  // and its fp16 re-encoding (slow: its shared-memory reads wait behind the
+  // QK products' operand reads) is finished before its PV product is due.
+  static constexpr int kVStages = 3;
   static constexpr int kQTileBytes = kTileM * DH * 2;
   static constexpr int kKTileBytes = kTileN * DH * 2;
   static constexpr int kVTileBytes = kTileN * DV * 2;
