@@ -817,36 +817,53 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
 }
 
-// One block per 128-row query tile of one (batch, query head), two threads
-// per row:
+// Per-tile work of the backward preprocess, for a 128-row query tile:
 //   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
 //   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
 // the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
 // and dO are re-encoded as fp16 for the main kernel (exact for |x| <= 65504,
-// saturating beyond).
-template <int DV, int DH>
-__global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const uint4* __restrict__ O,
-                           const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
-                           float2* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
-                           uint4* __restrict__ dO16) {
-  constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
+// saturating beyond).  In the D pass each row has DV/8 consecutive threads,
+// one 16-byte chunk each, so every warp load covers whole rows; the fp16 copy
+// of dO is written from the registers that chunk was loaded into.
+// row_at(rr) is the storage row of the tile's row rr, d_at(rr) its index in D.
+template <int DV, int DH, class RowAt, class DAt>
+__device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at, const DAt& d_at,
+                                              const uint4* __restrict__ Q, const uint4* __restrict__ O,
+                                              const uint4* __restrict__ O_lo, const uint4* __restrict__ dO,
+                                              float* __restrict__ D, float2* __restrict__ tm,
+                                              float4* __restrict__ dQacc, uint4* __restrict__ Q16,
+                                              uint4* __restrict__ dO16) {
+  constexpr int kTpr = DV / 8;                 // threads per row in the D pass
+  constexpr int kRows = 256 / kTpr;            // rows per pass
+  constexpr int kPasses = kTileM / kRows;
+  constexpr int kBatch = 2;                    // passes whose loads are in flight together
+  static_assert(kPasses % kBatch == 0, "pass count");
   __shared__ float red[2][8];
-  const int64_t bh = blockIdx.x;
-  const int qt = blockIdx.y;
-  const int r = static_cast<int>(threadIdx.x >> 1), half = static_cast<int>(threadIdx.x & 1);
-  const int64_t i = static_cast<int64_t>(qt) * kTileM + r;
-  const bool valid = i < n_q;
-  const int64_t row = bh * n_q + i;
-  float acc = 0.f, nrm = 0.f;
-  if (valid) {
-    const int64_t base = row * (DV / 8) + half * kChunks;
+  const int c = static_cast<int>(threadIdx.x) % kTpr, r0 = static_cast<int>(threadIdx.x) / kTpr;
+  float mn = 0.f, md = 0.f;
+  for (int p0 = 0; p0 < kPasses; p0 += kBatch) {
+    uint4 a[kBatch], g[kBatch], lo[kBatch];
+    int64_t at[kBatch];
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const uint4 a = O[base + c];
-      const uint4 g = dO[base + c];
-      const uint4 lo = O_lo ? O_lo[base + c] : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
+    for (int u = 0; u < kBatch; ++u) {
+      const int rr = (p0 + u) * kRows + r0;
+      a[u] = g[u] = lo[u] = make_uint4(0u, 0u, 0u, 0u);
+      at[u] = 0;
+      if (rr < rows_here) {
+        at[u] = row_at(rr) * (DV / 8) + c;
+        a[u] = O[at[u]];
+        g[u] = dO[at[u]];
+        if (O_lo) lo[u] = O_lo[at[u]];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int rr = (p0 + u) * kRows + r0;
+      const bool valid = rr < rows_here;
+      const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+      const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      const uint32_t lw[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
+      float acc = 0.f, nrm = 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
@@ -855,14 +872,23 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
         nrm = fmaf(g0, g0, nrm);
         nrm = fmaf(g1, g1, nrm);
       }
+      if (valid)
+        dO16[at[u]] = make_uint4(bf16x2_to_f16x2(gw[0]), bf16x2_to_f16x2(gw[1]), bf16x2_to_f16x2(gw[2]),
+                                 bf16x2_to_f16x2(gw[3]));
+#pragma unroll
+      for (int off = kTpr / 2; off > 0; off >>= 1) {
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        nrm += __shfl_xor_sync(0xffffffffu, nrm, off);
+      }
+      if (valid) {
+        if (c == 0) D[d_at(rr)] = acc;
+        mn = fmaxf(mn, sqrtf(nrm));
+        md = fmaxf(md, fabsf(acc));
+      }
     }
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  nrm += __shfl_xor_sync(0xffffffffu, nrm, 1);
-  if (valid && half == 0) D[row] = acc;
-  float mn = valid ? sqrtf(nrm) : 0.f, md = valid ? fabsf(acc) : 0.f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
+  for (int off = 16; off >= kTpr; off >>= 1) {
     mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
     md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
   }
@@ -872,44 +898,56 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    float a = 0.f, c = 0.f;
+    float x = 0.f, y = 0.f;
     for (int w = 0; w < 8; ++w) {
-      a = fmaxf(a, red[0][w]);
-      c = fmaxf(c, red[1][w]);
+      x = fmaxf(x, red[0][w]);
+      y = fmaxf(y, red[1][w]);
     }
-    tilemax[bh * nqt + qt] = make_float2(a, c);
+    *tm = make_float2(x, y);
   }
-  const int64_t rows_here = (n_q - static_cast<int64_t>(qt) * kTileM) < kTileM ? (n_q - static_cast<int64_t>(qt) * kTileM)
-                                                                                : kTileM;
-  const int64_t tile_row0 = bh * n_q + static_cast<int64_t>(qt) * kTileM;
-  float4* acc_tile = dQacc + tile_row0 * (DH / 4);
-  for (int64_t k = threadIdx.x; k < rows_here * (DH / 4); k += 256) acc_tile[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const uint4* q_tile = Q + tile_row0 * (DH / 8);
-  uint4* q16_tile = Q16 + tile_row0 * (DH / 8);
-  for (int64_t k = threadIdx.x; k < rows_here * (DH / 8); k += 256) {
-    const uint4 u = q_tile[k];
-    q16_tile[k] = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+  // Q to fp16 and the accumulator zeroed, with every thread's Q loads issued
+  // before its first store.
+  constexpr int kQ = kTileM * (DH / 8) / 256, kZ = kTileM * (DH / 4) / 256;
+  uint4 q[kQ];
+#pragma unroll
+  for (int j = 0; j < kQ; ++j) {
+    const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
+    q[j] = rr < rows_here ? Q[row_at(rr) * (DH / 8) + k % (DH / 8)] : make_uint4(0u, 0u, 0u, 0u);
   }
-  // dO again, now warp-contiguous (the tile was just read, so this hits the
-  // caches), so that the fp16 copy is written in whole lines.
-  const uint4* g_tile = dO + tile_row0 * (DV / 8);
-  uint4* g16_tile = dO16 + tile_row0 * (DV / 8);
-  for (int64_t k = threadIdx.x; k < rows_here * (DV / 8); k += 256) {
-    const uint4 u = g_tile[k];
-    g16_tile[k] = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+#pragma unroll
+  for (int j = 0; j < kZ; ++j) {
+    const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 4);
+    if (rr < rows_here) dQacc[row_at(rr) * (DH / 4) + k % (DH / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < kQ; ++j) {
+    const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
+    if (rr < rows_here)
+      Q16[row_at(rr) * (DH / 8) + k % (DH / 8)] = make_uint4(bf16x2_to_f16x2(q[j].x), bf16x2_to_f16x2(q[j].y),
+                                                             bf16x2_to_f16x2(q[j].z), bf16x2_to_f16x2(q[j].w));
   }
 }
 
+// One block per 128-row query tile of one (batch, query head); rows of
+// (b, h) are contiguous, n_q of them.
+template <int DV, int DH>
+__global__ void __launch_bounds__(256)
+attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const uint4* __restrict__ O,
+                           const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
+                           float2* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
+                           uint4* __restrict__ dO16) {
+  const int64_t bh = blockIdx.x;
+  const int qt = blockIdx.y;
+  const int64_t i0 = static_cast<int64_t>(qt) * kTileM;
+  const int rows_here = static_cast<int>(n_q - i0 < kTileM ? n_q - i0 : kTileM);
+  const int64_t row0 = bh * n_q + i0;
+  const auto row_at = [row0](int rr) { return row0 + rr; };
+  bwd_prep_tile<DV, DH>(rows_here, row_at, row_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16);
+}
+
 // The same for packed sequences (token-major rows, per-sequence lengths):
-// one block per 128-row query tile of one (sequence, query head), two threads
-// per row:
-//   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
-//   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
-// the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
-// and dO are re-encoded as fp16 for the main kernel (exact for |x| <= 65504,
-// saturating beyond).
-// Row addressing for packed sequences: row i of (b, h) is token cu_q[b] + i;
-// rows past the sequence's length are left alone.
+// row i of (b, h) is token cu_q[b] + i; rows past the sequence's length are
+// left alone.
 struct PrepPacked {
   int32_t n_q, Hq;
   int64_t total_q;
@@ -926,83 +964,19 @@ struct PrepPacked {
 template <int DV, int DH>
 __global__ void __launch_bounds__(256)
 attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt, const uint4* __restrict__ Q,
-                           const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
-                           const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
-                           float4* __restrict__ dQacc, uint4* __restrict__ Q16, uint4* __restrict__ dO16) {
-  constexpr int kChunks = DV / 16;          // 16-byte chunks per half row
-  __shared__ float red[2][8];
+                                  const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
+                                  const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
+                                  float4* __restrict__ dQacc, uint4* __restrict__ Q16, uint4* __restrict__ dO16) {
   const int64_t bh = blockIdx.x;
   const int b = static_cast<int>(bh / rm.Hq);
   const int h = static_cast<int>(bh - static_cast<int64_t>(b) * rm.Hq);
   const int qt = blockIdx.y;
-  const int64_t nq_b = rm.len(b);
-  const int r = static_cast<int>(threadIdx.x >> 1), half = static_cast<int>(threadIdx.x & 1);
-  const int64_t i = static_cast<int64_t>(qt) * kTileM + r;
-  const bool valid = i < nq_b;
-  const int64_t row = valid ? rm.row(b, h, i) : 0;
-  float acc = 0.f, nrm = 0.f;
-  if (valid) {
-    const int64_t base = row * (DV / 8) + half * kChunks;
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const uint4 a = O[base + c];
-      const uint4 g = dO[base + c];
-      const uint4 lo = O_lo ? O_lo[base + c] : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
-        acc = fmaf(bf16_lo(aw[k]) + bf16_lo(lw[k]), g0, acc);
-        acc = fmaf(bf16_hi(aw[k]) + bf16_hi(lw[k]), g1, acc);
-        nrm = fmaf(g0, g0, nrm);
-        nrm = fmaf(g1, g1, nrm);
-      }
-    }
-  }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  nrm += __shfl_xor_sync(0xffffffffu, nrm, 1);
-  if (valid && half == 0) D[rm.vec(b, h, i)] = acc;
-  float mn = valid ? sqrtf(nrm) : 0.f, md = valid ? fabsf(acc) : 0.f;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = mn;
-    red[1][threadIdx.x >> 5] = md;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float a = 0.f, c = 0.f;
-    for (int w = 0; w < 8; ++w) {
-      a = fmaxf(a, red[0][w]);
-      c = fmaxf(c, red[1][w]);
-    }
-    tilemax[bh * nqt + qt] = make_float2(a, c);
-  }
   const int64_t i0 = static_cast<int64_t>(qt) * kTileM;
-  const int rows_here = static_cast<int>(nq_b - i0 < kTileM ? (nq_b - i0 < 0 ? 0 : nq_b - i0) : kTileM);
-  {
-    for (int k = threadIdx.x; k < rows_here * (DH / 4); k += 256) {
-      const int rr = k / (DH / 4), cc = k - rr * (DH / 4);
-      dQacc[rm.row(b, h, i0 + rr) * (DH / 4) + cc] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int k = threadIdx.x; k < rows_here * (DH / 8); k += 256) {
-      const int rr = k / (DH / 8), cc = k - rr * (DH / 8);
-      const int64_t at = rm.row(b, h, i0 + rr) * (DH / 8) + cc;
-      const uint4 u = Q[at];
-      Q16[at] =
-          make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-    }
-    for (int k = threadIdx.x; k < rows_here * (DV / 8); k += 256) {
-      const int rr = k / (DV / 8), cc = k - rr * (DV / 8);
-      const int64_t at = rm.row(b, h, i0 + rr) * (DV / 8) + cc;
-      const uint4 u = dO[at];
-      dO16[at] =
-          make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-    }
-  }
+  const int64_t left = rm.len(b) - i0;
+  const int rows_here = static_cast<int>(left < kTileM ? (left < 0 ? 0 : left) : kTileM);
+  const auto row_at = [&rm, b, h, i0](int rr) { return rm.row(b, h, i0 + rr); };
+  const auto d_at = [&rm, b, h, i0](int rr) { return rm.vec(b, h, i0 + rr); };
+  bwd_prep_tile<DV, DH>(rows_here, row_at, d_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16);
 }
 
 // dQ = scale * acc, eight elements per thread per iteration.
