@@ -12,9 +12,9 @@
 // (inverse = 1).
 //
 // Memory-bound: every thread takes 8 elements (four blocks) of one token,
-// computes their four angles once and rotates those 16 bytes in a group of
-// up to 8 heads of the token (the angle depends on the position and the
-// block only).  The angle is formed without losing the product's low
+// loads those 16 bytes from a group of up to 8 heads of the token, computes
+// the four angles once (they depend on the position and the block only) and
+// rotates and stores the group.  The angle is formed without losing the product's low
 // bits: a = p w is split exactly into hi + lo (an fma gives the rounding
 // residual), hi is reduced modulo 2 pi by the two-constant Cody-Waite scheme,
 // lo added back, and the sine and cosine of the reduced angle come from
@@ -69,22 +69,28 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
     const int64_t tok = tg / groups;
     const int h0 = static_cast<int>(tg - tok * groups) * kHeadGroup;
     const int h1 = h0 + kHeadGroup < p.heads ? h0 + kHeadGroup : p.heads;
+    // Every row of the group is requested before the angles are formed, so
+    // a thread keeps up to 8 x 16 bytes in flight.
+    const int64_t base = tok * p.heads * per_row + c;
     const int32_t pos = p.pos[tok];
+    uint4 v[kHeadGroup];
+#pragma unroll
+    for (int j = 0; j < kHeadGroup; ++j)
+      if (h0 + j < h1) v[j] = p.x[base + static_cast<int64_t>(h0 + j) * per_row];
     float sn[4], cs[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) sincosf(sgn * reduced_angle(pos, p.w[4 * c + q]), &sn[q], &cs[q]);
-    const int64_t base = tok * p.heads * per_row + c;
-#pragma unroll 4
-    for (int h = h0; h < h1; ++h) {
-      const uint4 v = p.x[base + static_cast<int64_t>(h) * per_row];
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < kHeadGroup; ++j) {
+      if (h0 + j >= h1) break;
+      const uint32_t in[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
       uint32_t out[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float a = bf16_lo(in[q]), b = bf16_hi(in[q]);
         out[q] = pack_bf16x2(a * cs[q] - b * sn[q], a * sn[q] + b * cs[q]);
       }
-      p.y[base + static_cast<int64_t>(h) * per_row] = make_uint4(out[0], out[1], out[2], out[3]);
+      p.y[base + static_cast<int64_t>(h0 + j) * per_row] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
 }
