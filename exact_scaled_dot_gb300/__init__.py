@@ -10,5 +10,5 @@ from ._binding import (  # noqa: F401
     attn_bwd_noalloc_max_scratch_bytes, attn_bwd_preprocess, attn_bwd_workspace_bytes, attn_clear_status, attn_fwd, attn_fwd_decode, attn_fwd_decode_workspace_bytes,
     attn_get_status, attn_selftest_wait_timeout, attn_visible_pairs, load, make_shape, strerror,
     AttnVarlen, attn_bwd_varlen, attn_bwd_varlen_workspace_bytes, attn_fwd_varlen, attn_varlen_visible_pairs,
-    attn_proj_bwd_input, attn_proj_bwd_weight, attn_proj_fwd, attn_rope,
+    attn_proj_bwd_input, attn_proj_bwd_weight, attn_proj_fwd, attn_rope, attn_rope_qk,
 )

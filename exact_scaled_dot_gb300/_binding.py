@@ -36,7 +36,7 @@ EXPORTS = ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "at
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight",
-           "attn_proj_bwd_input", "attn_rope")
+           "attn_proj_bwd_input", "attn_rope", "attn_rope_qk")
 
 
 class AttnError(RuntimeError):
@@ -113,10 +113,11 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_proj_bwd_input.argtypes = [i64, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(_vp),
                                         ctypes.POINTER(_vp), _vp, _vp]
     lib.attn_rope.argtypes = [i64, i32, i32, f, _vp, i32, _vp, _vp, _vp]
+    lib.attn_rope_qk.argtypes = [i64, i32, i32, i32, f, _vp, i32, _vp, _vp, _vp, _vp, _vp]
     for name in ("attn_fwd", "attn_fwd_decode", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_finalize",
                  "attn_get_status", "attn_clear_status", "attn_selftest_wait_timeout", "attn_fwd_varlen",
                  "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight", "attn_proj_bwd_input",
-                 "attn_rope"):
+                 "attn_rope", "attn_rope_qk"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -582,3 +583,25 @@ def attn_rope(X, positions, *, base: float = 10000.0, inverse: bool = False, Y=N
                           _stream(dev, stream))
     _check(rc, "attn_rope")
     return Y
+
+
+def attn_rope_qk(Q, K, positions, *, base: float = 10000.0, inverse: bool = False, Yq=None, Yk=None, stream=None):
+    """attn_rope of queries Q [tokens, Hq, d] and keys K [tokens, Hkv, d] at
+    the same positions, in one launch; returns (Yq, Yk).  Yq may be Q and Yk
+    may be K (in place)."""
+    if Q.dim() != 3 or K.dim() != 3:
+        raise ValueError("Q and K must be [tokens, heads, d]")
+    T, Hq, d = (int(x) for x in Q.shape)
+    Hk = int(K.shape[1])
+    dev = Q.device
+    _check_tensor(Q, "Q", torch.bfloat16, (T, Hq, d), dev)
+    _check_tensor(K, "K", torch.bfloat16, (T, Hk, d), dev)
+    _check_tensor(positions, "positions", torch.int32, (T,), dev)
+    Yq = torch.empty_like(Q) if Yq is None else Yq
+    Yk = torch.empty_like(K) if Yk is None else Yk
+    _check_tensor(Yq, "Yq", torch.bfloat16, (T, Hq, d), dev)
+    _check_tensor(Yk, "Yk", torch.bfloat16, (T, Hk, d), dev)
+    rc = load().attn_rope_qk(T, Hq, Hk, d, ctypes.c_float(base), _ptr(positions), 1 if inverse else 0, _ptr(Q),
+                             _ptr(Yq), _ptr(K), _ptr(Yk), _stream(dev, stream))
+    _check(rc, "attn_rope_qk")
+    return Yq, Yk

@@ -438,6 +438,27 @@ int check_decode_shape(const attn_shape* shape) {
   return shape->n_q > 128 ? ATTN_ERR_UNSUPPORTED : ATTN_OK;
 }
 
+int check_rope(int64_t tokens, int32_t d, float base, const int32_t* positions, int32_t inverse) {
+  if (tokens <= 0 || d <= 0 || d % 8 != 0 || d > 128) return ATTN_ERR_SHAPE;
+  if (inverse != 0 && inverse != 1) return ATTN_ERR_SHAPE;
+  if (!std::isfinite(base) || !(base > 1.f)) return ATTN_ERR_SCALE;
+  if (!positions) return ATTN_ERR_NULL;
+  return ATTN_OK;
+}
+
+int rope_launch(int64_t tokens, int32_t heads_a, int32_t heads_b, int32_t d, float base,
+                const int32_t* positions, int32_t inverse, const void* Xa, void* Ya, const void* Xb, void* Yb,
+                void* stream) {
+  unsigned int* status = nullptr;
+  int rc = device_status_ptr(&status);
+  if (rc) return rc;
+  float w[64];
+  for (int k = 0; k < d / 2; ++k) w[k] = static_cast<float>(std::pow(static_cast<double>(base), -2.0 * k / d));
+  const cudaError_t e = launch_rope(tokens, d, heads_a, heads_b, positions, w, inverse, Xa, Ya, Xb, Yb,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace esd
 
@@ -726,20 +747,23 @@ size_t attn_bwd_noalloc_max_scratch_bytes(void) { return kStaticBwdScratchBytes;
 // ---------------------------------------------------------------------------
 int attn_rope(int64_t tokens, int32_t heads, int32_t d, float base, const int32_t* positions, int32_t inverse,
               const void* X, void* Y, void* stream) {
-  if (tokens <= 0 || heads <= 0 || d <= 0 || d % 8 != 0 || d > 128) return ATTN_ERR_SHAPE;
-  if (inverse != 0 && inverse != 1) return ATTN_ERR_SHAPE;
-  if (!std::isfinite(base) || !(base > 1.f)) return ATTN_ERR_SCALE;
-  int rc = check_ptrs({X, Y});
+  if (heads <= 0) return ATTN_ERR_SHAPE;
+  int rc = check_rope(tokens, d, base, positions, inverse);
   if (rc) return rc;
-  if (!positions) return ATTN_ERR_NULL;
-  unsigned int* status = nullptr;
-  rc = device_status_ptr(&status);
+  rc = check_ptrs({X, Y});
   if (rc) return rc;
-  float w[64];
-  for (int k = 0; k < d / 2; ++k) w[k] = static_cast<float>(std::pow(static_cast<double>(base), -2.0 * k / d));
-  const cudaError_t e = launch_rope(tokens * heads, d, heads, positions, w, inverse, X, Y,
-                                    static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return rope_launch(tokens, heads, 0, d, base, positions, inverse, X, Y, nullptr, nullptr, stream);
+}
+
+int attn_rope_qk(int64_t tokens, int32_t heads_q, int32_t heads_k, int32_t d, float base,
+                 const int32_t* positions, int32_t inverse, const void* Xq, void* Yq, const void* Xk, void* Yk,
+                 void* stream) {
+  if (heads_q <= 0 || heads_k <= 0) return ATTN_ERR_SHAPE;
+  int rc = check_rope(tokens, d, base, positions, inverse);
+  if (rc) return rc;
+  rc = check_ptrs({Xq, Yq, Xk, Yk});
+  if (rc) return rc;
+  return rope_launch(tokens, heads_q, heads_k, d, base, positions, inverse, Xq, Yq, Xk, Yk, stream);
 }
 
 int attn_proj_fwd(int64_t T, int32_t D, int32_t N, const void* X, const void* W, void* Y, void* stream) {

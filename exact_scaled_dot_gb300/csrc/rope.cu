@@ -11,14 +11,15 @@
 // the gradient of a rotated row is the upstream gradient rotated back by -a
 // (inverse = 1).
 //
-// Memory-bound: every thread takes 8 elements (four blocks) of one token,
-// loads those 16 bytes from a group of up to 8 heads of the token, computes
-// the four angles once (they depend on the position and the block only) and
-// rotates and stores the group.  The angle is formed without losing the product's low
-// bits: a = p w is split exactly into hi + lo (an fma gives the rounding
-// residual), hi is reduced modulo 2 pi by the two-constant Cody-Waite scheme,
-// lo added back, and the sine and cosine of the reduced angle come from
-// sincosf.
+// Memory-bound: one launch rotates one tensor, or two that share tokens and
+// positions (queries and keys).  Every thread takes 8 elements (four blocks)
+// of one token, loads those 16 bytes from a group of up to 8 heads of the
+// token, computes the four angles once (they depend on the position and the
+// block only) and rotates and stores the group.  The angle is formed without
+// losing the product's low bits: a = p w is split exactly into hi + lo (an
+// fma gives the rounding residual), hi is reduced modulo 2 pi by the
+// two-constant Cody-Waite scheme, lo added back, and the sine and cosine of
+// the reduced angle come from sincosf.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -44,39 +45,52 @@ __device__ __forceinline__ float reduced_angle(int32_t pos, float w) {
   return r + lo;
 }
 
+// One or two token-major tensors that share tokens and positions (the
+// queries and keys of a batch), rotated in one launch: the work items of
+// tensor 0 come first, then those of tensor 1.
 struct RopeParams {
-  int64_t rows;          // rows of the tensor (tokens x heads)
-  int32_t d;             // row width (even)
-  int32_t heads;         // rows per token: row r is token r / heads
+  int64_t tokens;
+  int32_t d;             // row width (a multiple of 8)
   int32_t inverse;       // rotate by -a
+  int32_t heads[2];      // rows per token of each tensor (0: no second tensor)
+  const uint4* x[2];     // bf16 rows, 8 elements per uint4
+  uint4* y[2];
+  const int32_t* pos;    // [tokens] token positions
   float w[64];           // w_k = base^(-2k/d), k < d/2
-  const int32_t* pos;    // [rows / heads] token positions
-  const uint4* x;        // bf16 rows, 8 elements per uint4
-  uint4* y;
 };
 
+constexpr int kHeadGroup = 8;
+
+__host__ __device__ __forceinline__ int64_t rope_items(int64_t tokens, int heads, int d) {
+  return tokens * ((heads + kHeadGroup - 1) / kHeadGroup) * (d / 8);
+}
+
 __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeParams p) {
-  constexpr int kHeadGroup = 8;
   const int per_row = p.d / 8;
-  const int groups = (p.heads + kHeadGroup - 1) / kHeadGroup;
-  const int64_t tokens = p.rows / p.heads;
-  const int64_t total = tokens * groups * per_row;
+  const int64_t items0 = rope_items(p.tokens, p.heads[0], p.d);
+  const int64_t total = items0 + rope_items(p.tokens, p.heads[1], p.d);
   const float sgn = p.inverse ? -1.f : 1.f;
-  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
-       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u0 < total;
+       u0 += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool second = u0 >= items0;
+    const int64_t u = second ? u0 - items0 : u0;
+    const int heads = second ? p.heads[1] : p.heads[0];
+    const uint4* __restrict__ x = second ? p.x[1] : p.x[0];
+    uint4* __restrict__ y = second ? p.y[1] : p.y[0];
+    const int groups = (heads + kHeadGroup - 1) / kHeadGroup;
     const int64_t tg = u / per_row;                      // (token, head group)
     const int c = static_cast<int>(u - tg * per_row);    // 8-element chunk: blocks 4c .. 4c+3
     const int64_t tok = tg / groups;
     const int h0 = static_cast<int>(tg - tok * groups) * kHeadGroup;
-    const int h1 = h0 + kHeadGroup < p.heads ? h0 + kHeadGroup : p.heads;
+    const int h1 = h0 + kHeadGroup < heads ? h0 + kHeadGroup : heads;
     // Every row of the group is requested before the angles are formed, so
     // a thread keeps up to 8 x 16 bytes in flight.
-    const int64_t base = tok * p.heads * per_row + c;
+    const int64_t base = tok * heads * per_row + c;
     const int32_t pos = p.pos[tok];
     uint4 v[kHeadGroup];
 #pragma unroll
     for (int j = 0; j < kHeadGroup; ++j)
-      if (h0 + j < h1) v[j] = p.x[base + static_cast<int64_t>(h0 + j) * per_row];
+      if (h0 + j < h1) v[j] = x[base + static_cast<int64_t>(h0 + j) * per_row];
     float sn[4], cs[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) sincosf(sgn * reduced_angle(pos, p.w[4 * c + q]), &sn[q], &cs[q]);
@@ -90,25 +104,28 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
         const float a = bf16_lo(in[q]), b = bf16_hi(in[q]);
         out[q] = pack_bf16x2(a * cs[q] - b * sn[q], a * sn[q] + b * cs[q]);
       }
-      p.y[base + static_cast<int64_t>(h0 + j) * per_row] = make_uint4(out[0], out[1], out[2], out[3]);
+      y[base + static_cast<int64_t>(h0 + j) * per_row] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_rope(int64_t rows, int d, int heads, const int32_t* pos, const float* w, int inverse,
-                        const void* x, void* y, cudaStream_t stream) {
+cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w,
+                        int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream) {
   RopeParams p{};
-  p.rows = rows;
+  p.tokens = tokens;
   p.d = d;
-  p.heads = heads;
   p.inverse = inverse;
-  for (int k = 0; k < d / 2; ++k) p.w[k] = w[k];
+  p.heads[0] = heads_a;
+  p.heads[1] = heads_b;
+  p.x[0] = static_cast<const uint4*>(xa);
+  p.y[0] = static_cast<uint4*>(ya);
+  p.x[1] = static_cast<const uint4*>(xb);
+  p.y[1] = static_cast<uint4*>(yb);
   p.pos = pos;
-  p.x = static_cast<const uint4*>(x);
-  p.y = static_cast<uint4*>(y);
-  int64_t blocks = ((rows / heads) * ((heads + 7) / 8) * (d / 8) + 255) / 256;
+  for (int k = 0; k < d / 2; ++k) p.w[k] = w[k];
+  int64_t blocks = (rope_items(tokens, heads_a, d) + rope_items(tokens, heads_b, d) + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   rope_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);

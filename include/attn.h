@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 7
+#define ATTN_ABI_VERSION 8
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -296,6 +296,18 @@ int attn_proj_bwd_input(int64_t T, int32_t D, int32_t nsrc, const int32_t* N, co
  * positions well beyond 10^5. */
 int attn_rope(int64_t tokens, int32_t heads, int32_t d, float base, const int32_t* positions, int32_t inverse,
               const void* X, void* Y, void* stream);
+
+/* The rotation of a batch's queries and keys in one launch: Xq, Yq are
+ * [tokens][heads_q][d], Xk, Yk [tokens][heads_k][d], both at the same
+ * positions.  Equal, bit for bit, to attn_rope on Xq followed by attn_rope
+ * on Xk with the same tokens, d, base, positions and inverse; the argument
+ * rules and errors are those of attn_rope, for both tensors (Yq may equal Xq
+ * and Yk may equal Xk; no other overlap is allowed).  One launch instead of
+ * two: the keys' short pass does not pay a launch, a ramp and a tail of its
+ * own. */
+int attn_rope_qk(int64_t tokens, int32_t heads_q, int32_t heads_k, int32_t d, float base,
+                 const int32_t* positions, int32_t inverse, const void* Xq, void* Yq, const void* Xk, void* Yk,
+                 void* stream);
 
 /* Device status word of the current device: ATTN_OK, or the first failure a
  * kernel recorded (ATTN_ERR_TIMEOUT).  Synchronises the device.  Writes the

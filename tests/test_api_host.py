@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 7
+    assert esd.attn_abi_version() == 8
 
 
 def test_strerror_covers_every_code(lib):
@@ -257,3 +257,25 @@ def test_rope_checks(lib):
     assert lib.attn_rope(10, 2, 64, f(float("nan")), p, 0, p, p, None) == bnd.ATTN_ERR_SCALE
     assert lib.attn_rope(10, 2, 64, f(10000.0), None, 0, p, p, None) == bnd.ATTN_ERR_NULL
     assert lib.attn_rope(10, 2, 64, f(10000.0), p, 0, ctypes.c_void_p(0x1008), p, None) == bnd.ATTN_ERR_ALIGN
+
+
+def test_rope_qk_checks(lib):
+    p = ctypes.c_void_p(256)
+    f = ctypes.c_float
+    ok = dict(tokens=10, hq=4, hk=2, d=64, base=f(10000.0), pos=p, inv=0, xq=p, yq=p, xk=p, yk=p)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.attn_rope_qk(a["tokens"], a["hq"], a["hk"], a["d"], a["base"], a["pos"], a["inv"],
+                                a["xq"], a["yq"], a["xk"], a["yk"], None)
+
+    assert call(hk=0) == bnd.ATTN_ERR_SHAPE
+    assert call(hq=-1) == bnd.ATTN_ERR_SHAPE
+    assert call(d=12) == bnd.ATTN_ERR_SHAPE
+    assert call(d=256) == bnd.ATTN_ERR_SHAPE
+    assert call(tokens=0) == bnd.ATTN_ERR_SHAPE
+    assert call(inv=2) == bnd.ATTN_ERR_SHAPE
+    assert call(base=f(0.5)) == bnd.ATTN_ERR_SCALE
+    assert call(pos=None) == bnd.ATTN_ERR_NULL
+    assert call(yk=None) == bnd.ATTN_ERR_NULL
+    assert call(xk=ctypes.c_void_p(0x1008)) == bnd.ATTN_ERR_ALIGN

@@ -75,3 +75,27 @@ def test_attention_over_rotated_queries_and_keys(orc):
         Oref, Lref = orc.forward(p, tr(Qn[q0:q1]), tr(Kn[q0:q1]), tr(Vn[q0:q1]))
         assert_close(f64(O[q0:q1]), Oref[0].transpose(1, 0, 2), f"O[{b}]")
         assert_close(f64(LSE[:, q0:q1]), Lref[0], f"LSE[{b}]", atol=LSE_ATOL, rtol=0.0)
+
+
+@pytest.mark.parametrize("T,Hq,Hk,d,inverse", [(1000, 32, 8, 128, False), (333, 5, 3, 64, True),
+                                               (64, 1, 9, 8, False)])
+def test_rope_qk_equals_two_calls(T, Hq, Hk, d, inverse):
+    """One launch for queries and keys gives the two single-tensor results bit
+    for bit (the kernel is the same; only the work items are concatenated),
+    head counts that are not multiples of the kernel's 8-head groups
+    included, and in place as well."""
+    import exact_scaled_dot_gb300 as esd
+    g = torch.Generator().manual_seed(T + Hq + Hk)
+    Q = torch.randn((T, Hq, d), generator=g).to(torch.bfloat16).cuda()
+    K = torch.randn((T, Hk, d), generator=g).to(torch.bfloat16).cuda()
+    pos = torch.randint(0, 70000, (T,), generator=g, dtype=torch.int32).cuda()
+    Yq, Yk = esd.attn_rope_qk(Q, K, pos, base=10000.0, inverse=inverse)
+    Rq = esd.attn_rope(Q, pos, base=10000.0, inverse=inverse)
+    Rk = esd.attn_rope(K, pos, base=10000.0, inverse=inverse)
+    Q2, K2 = Q.clone(), K.clone()
+    esd.attn_rope_qk(Q2, K2, pos, base=10000.0, inverse=inverse, Yq=Q2, Yk=K2)
+    torch.cuda.synchronize()
+    assert torch.equal(Yq.view(torch.int16), Rq.view(torch.int16))
+    assert torch.equal(Yk.view(torch.int16), Rk.view(torch.int16))
+    assert torch.equal(Q2.view(torch.int16), Rq.view(torch.int16))
+    assert torch.equal(K2.view(torch.int16), Rk.view(torch.int16))
