@@ -579,6 +579,21 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
   p.chunks = plan.chunks;
   p.nsplit = plan.nsplit;
   p.status = status;
+  // Longest key range first: a CTA's work is proportional to its batch's
+  // key tiles, and dispatching the long ones first keeps short ones for the
+  // tail (the longest-processing-time-first list schedule).
+  {
+    int64_t ntiles[ATTN_MAX_BATCH];
+    int16_t order[ATTN_MAX_BATCH];
+    for (int b = 0; b < shape->B; ++b) {
+      const int64_t lim = row_key_limit(p.mask, shape->n_k, b, static_cast<int64_t>(shape->n_q) - 1);
+      ntiles[b] = lim > 0 ? (lim + kTileN - 1) / kTileN : 0;
+      order[b] = static_cast<int16_t>(b);
+    }
+    std::stable_sort(order, order + shape->B, [&ntiles](int16_t x, int16_t y) { return ntiles[x] > ntiles[y]; });
+    std::memset(p.batch_order, 0, sizeof(p.batch_order));
+    for (int b = 0; b < shape->B; ++b) p.batch_order[b] = order[b];
+  }
   const cudaError_t e = launch_attn_decode(shape->d_h, shape->d_v, tk, tv, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

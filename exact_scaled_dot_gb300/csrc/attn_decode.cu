@@ -101,12 +101,17 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   const uint32_t lane = lane_id();
 
   // ---- work item: row tile (batch, KV head, head chunk) and key range ----
+  // Row tiles run fastest in the dispatch order, batch by batch in
+  // batch_order (the longest key range first), so that the last CTAs to
+  // start are the short batches' last key ranges.
   const int chunks = p.chunks;
   const int tile = blockIdx.x;
-  const int bkv = tile / chunks;                      // b * Hkv + hkv
-  const int chunk = tile - bkv * chunks;
-  const int b = bkv / p.sh.Hkv;
-  const int hkv = bkv - b * p.sh.Hkv;
+  const int rkv = tile / chunks;                      // rank * Hkv + hkv
+  const int chunk = tile - rkv * chunks;
+  const int b_rank = rkv / p.sh.Hkv;
+  const int hkv = rkv - b_rank * p.sh.Hkv;
+  const int b = p.batch_order[b_rank];
+  const int bkv = b * p.sh.Hkv + hkv;
   const int split = blockIdx.y;
   const int n_q = p.sh.n_q;
   // Rows r < rows_valid hold (head h0 + r / n_q, query r % n_q).

@@ -192,6 +192,7 @@ struct DecParams {
   int32_t chunks;              // row tiles per KV head
   int32_t nsplit;              // key ranges per row tile
   unsigned int* status;
+  int16_t batch_order[ATTN_MAX_BATCH];  // batches by descending key range: CTA dispatch order
 };
 
 // The projection products (A.10.10-A.10.11): C = sum_s A_s B_s, row-major
