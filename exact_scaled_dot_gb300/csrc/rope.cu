@@ -126,7 +126,7 @@ cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const i
   p.pos = pos;
   for (int k = 0; k < d / 2; ++k) p.w[k] = w[k];
   int64_t blocks = (rope_items(tokens, heads_a, d) + rope_items(tokens, heads_b, d) + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > 152 * 64) blocks = 152 * 64;
   if (blocks < 1) blocks = 1;
   rope_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
