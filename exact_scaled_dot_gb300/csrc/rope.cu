@@ -75,8 +75,8 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
     const bool second = u0 >= items0;
     const int64_t u = second ? u0 - items0 : u0;
     const int heads = second ? p.heads[1] : p.heads[0];
-    const uint4* __restrict__ x = second ? p.x[1] : p.x[0];
-    uint4* __restrict__ y = second ? p.y[1] : p.y[0];
+    const uint4* x = second ? p.x[1] : p.x[0];   // y may equal x (in place)
+    uint4* y = second ? p.y[1] : p.y[0];
     const int groups = (heads + kHeadGroup - 1) / kHeadGroup;
     const int64_t tg = u / per_row;                      // (token, head group)
     const int c = static_cast<int>(u - tg * per_row);    // 8-element chunk: blocks 4c .. 4c+3
