@@ -452,9 +452,15 @@ int rope_launch(int64_t tokens, int32_t heads_a, int32_t heads_b, int32_t d, flo
   unsigned int* status = nullptr;
   int rc = device_status_ptr(&status);
   if (rc) return rc;
-  float w[64];
-  for (int k = 0; k < d / 2; ++k) w[k] = static_cast<float>(std::pow(static_cast<double>(base), -2.0 * k / d));
-  const cudaError_t e = launch_rope(tokens, d, heads_a, heads_b, positions, w, inverse, Xa, Ya, Xb, Yb,
+  // Frequencies in double, passed as fp32 pairs w_hi + w_lo so that the
+  // rounding of w does not grow with the position.
+  float w_hi[64], w_lo[64];
+  for (int k = 0; k < d / 2; ++k) {
+    const double w = std::pow(static_cast<double>(base), -2.0 * k / d);
+    w_hi[k] = static_cast<float>(w);
+    w_lo[k] = static_cast<float>(w - static_cast<double>(w_hi[k]));
+  }
+  const cudaError_t e = launch_rope(tokens, d, heads_a, heads_b, positions, w_hi, w_lo, inverse, Xa, Ya, Xb, Yb,
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

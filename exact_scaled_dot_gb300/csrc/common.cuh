@@ -231,8 +231,8 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& 
 cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap* tB, const GemmParams& p,
                              cudaStream_t stream);
 // heads_b = 0: one tensor (xb, yb unused).
-cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w,
-                        int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream);
+cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w_hi,
+                        const float* w_lo, int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream);
 cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
                                      cudaStream_t stream);
 

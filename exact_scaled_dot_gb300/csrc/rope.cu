@@ -15,11 +15,22 @@
 // positions (queries and keys).  Every thread takes 8 elements (four blocks)
 // of one token, loads those 16 bytes from a group of up to 8 heads of the
 // token, computes the four angles once (they depend on the position and the
-// block only) and rotates and stores the group.  The angle is formed without
-// losing the product's low bits: a = p w is split exactly into hi + lo (an
-// fma gives the rounding residual), hi is reduced modulo 2 pi by the
-// two-constant Cody-Waite scheme, lo added back, and the sine and cosine of
-// the reduced angle come from sincosf.
+// block only) and rotates and stores the group.
+//
+// The angle a = p w is formed to about single-precision accuracy of the
+// reduced angle for every |p| < 2^24 (the positions an fp32 holds exactly).
+// Two errors would otherwise grow with p: the rounding of w itself, whose
+// 2^-24 relative error is worth 0.06 rad at p = 10^6 for w = 1, and the
+// reduction modulo 2 pi.  So w arrives as w_hi + w_lo (w_lo the rounding
+// residual of w_hi, both from the double-precision frequency), the product
+// p w_hi is split exactly into hi + lo with an fma, lo collects p w_lo, and
+// hi is reduced by a three-constant Cody-Waite scheme: 2 pi = C1 + C2 + C3
+// where C1 = 6.28125 has 8 significant bits.  For |hi| < 2^24 the quotient k
+// is below 2^22 and fmaf(-k, C1, hi) is exact (the difference is at most a
+// few thousand and lies on the grid of the finer of hi's unit in the last
+// place and C1's 2^-5, so it is representable); the C2 and C3 steps and the
+// final additions round a few times near |r| <= pi, which leaves a few
+// 10^-7 rad.  sincosf then takes the reduced angle.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -29,19 +40,22 @@
 namespace esd {
 namespace {
 
-// 2 pi split into a leading part with trailing zero bits (so k * kTwoPiHi is
-// exact for the k that occur) and the remainder.
-constexpr float kTwoPiHi = 6.28125f;
-constexpr float kTwoPiLo = 1.9353071795864769e-3f;
+// 2 pi = C1 + C2 + C3: C1 with trailing zero bits, C2 the fp32 rounding of
+// the rest, C3 that rounding's residual.
+constexpr float kTwoPiC1 = 6.28125f;
+constexpr float kTwoPiC2 = static_cast<float>(6.283185307179586476925 - 6.28125);
+constexpr float kTwoPiC3 = static_cast<float>(6.283185307179586476925 - 6.28125 - static_cast<double>(kTwoPiC2));
 constexpr float kInvTwoPi = 0.15915494309189535f;
 
-__device__ __forceinline__ float reduced_angle(int32_t pos, float w) {
+// p (w_hi + w_lo) reduced modulo 2 pi.
+__device__ __forceinline__ float reduced_angle(int32_t pos, float w_hi, float w_lo) {
   const float p = static_cast<float>(pos);      // exact for |pos| < 2^24
-  const float hi = p * w;
-  const float lo = fmaf(p, w, -hi);             // p w = hi + lo exactly
+  const float hi = p * w_hi;
+  const float lo = fmaf(p, w_lo, fmaf(p, w_hi, -hi));   // p w_hi = hi + its residual, plus p w_lo
   const float k = rintf(hi * kInvTwoPi);
-  float r = fmaf(-k, kTwoPiHi, hi);
-  r = fmaf(-k, kTwoPiLo, r);
+  float r = fmaf(-k, kTwoPiC1, hi);
+  r = fmaf(-k, kTwoPiC2, r);
+  r = fmaf(-k, kTwoPiC3, r);
   return r + lo;
 }
 
@@ -56,7 +70,8 @@ struct RopeParams {
   const uint4* x[2];     // bf16 rows, 8 elements per uint4
   uint4* y[2];
   const int32_t* pos;    // [tokens] token positions
-  float w[64];           // w_k = base^(-2k/d), k < d/2
+  float w_hi[64];        // w_k = base^(-2k/d), k < d/2, rounded to fp32
+  float w_lo[64];        // w_k - w_hi[k], rounded to fp32
 };
 
 constexpr int kHeadGroup = 8;
@@ -93,7 +108,7 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
       if (h0 + j < h1) v[j] = x[base + static_cast<int64_t>(h0 + j) * per_row];
     float sn[4], cs[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) sincosf(sgn * reduced_angle(pos, p.w[4 * c + q]), &sn[q], &cs[q]);
+    for (int q = 0; q < 4; ++q) sincosf(sgn * reduced_angle(pos, p.w_hi[4 * c + q], p.w_lo[4 * c + q]), &sn[q], &cs[q]);
 #pragma unroll
     for (int j = 0; j < kHeadGroup; ++j) {
       if (h0 + j >= h1) break;
@@ -111,8 +126,8 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
 
 }  // namespace
 
-cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w,
-                        int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream) {
+cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w_hi,
+                        const float* w_lo, int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream) {
   RopeParams p{};
   p.tokens = tokens;
   p.d = d;
@@ -124,7 +139,10 @@ cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const i
   p.x[1] = static_cast<const uint4*>(xb);
   p.y[1] = static_cast<uint4*>(yb);
   p.pos = pos;
-  for (int k = 0; k < d / 2; ++k) p.w[k] = w[k];
+  for (int k = 0; k < d / 2; ++k) {
+    p.w_hi[k] = w_hi[k];
+    p.w_lo[k] = w_lo[k];
+  }
   int64_t blocks = (rope_items(tokens, heads_a, d) + rope_items(tokens, heads_b, d) + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
   if (blocks < 1) blocks = 1;

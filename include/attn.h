@@ -291,9 +291,12 @@ int attn_proj_bwd_input(int64_t T, int32_t D, int32_t nsrc, const int32_t* N, co
  * X, Y: device bf16 [tokens][heads][d] (token-major, the packed layout; Y may
  * equal X); positions: device int32 [tokens], the position of each token.
  * d a multiple of 8 and <= 128; base finite and > 1 (ATTN_ERR_SCALE
- * otherwise).  Angles are reduced modulo 2 pi in single precision with the
- * product's rounding residual kept, so the rotation stays accurate for
- * positions well beyond 10^5. */
+ * otherwise).  Positions must satisfy |pos| < 2^24 (the integers an fp32
+ * holds exactly).  Each frequency reaches the kernel as an fp32 value plus
+ * its rounding residual, the product pos * w keeps its own rounding
+ * residual, and the angle is reduced modulo 2 pi in three steps, so the
+ * angle is accurate to a few 1e-7 rad over that whole range (tested against
+ * exact fp64 angles for positions up to 2^24 - 1). */
 int attn_rope(int64_t tokens, int32_t heads, int32_t d, float base, const int32_t* positions, int32_t inverse,
               const void* X, void* Y, void* stream);
 

@@ -1,6 +1,8 @@
 """GPU-vs-oracle parity of the rotary embedding (attn_rope) and of attention
 over rotated queries and keys: the rotation within 1e-2 + 2e-2 |ref| of the
-fp64 rotation with exact angles (positions up to 10^5), the inverse undoing
+fp64 rotation with exact angles (positions up to 2^24 - 1, the largest the
+kernel takes; a frequency rounded to fp32 alone would be off by 0.06 rad at
+10^6), the inverse undoing
 it, and packed causal attention over GPU-rotated Q, K matching the oracle's
 rotation (rounded to bf16, the precision of the rotated tensors) followed by
 the oracle's attention."""
@@ -28,7 +30,8 @@ def built_library():
 
 
 @pytest.mark.parametrize("T,H,d,base,maxpos", [(1000, 4, 128, 10000.0, 65535), (333, 2, 64, 500000.0, 4096),
-                                                (64, 1, 8, 10.0, 100000)])
+                                                (64, 1, 8, 10.0, 100000), (777, 2, 128, 10000.0, 1_000_000),
+                                                (512, 3, 64, 10000.0, (1 << 24) - 1)])
 def test_rope_matches_oracle(T, H, d, base, maxpos):
     from oracle.rope import rope
     import exact_scaled_dot_gb300 as esd
