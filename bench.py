@@ -223,6 +223,172 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # CUDA arm
 # ---------------------------------------------------------------------------
+KERNEL_STAGES = ["attn_fwd (V pre-pass + forward kernel)", "attn_bwd_preprocess_kernel", "attn_bwd_main_kernel",
+                 "attn_bwd_finalize_kernel"]
+LAUNCHES_PER_STEP = 5   # attn_v16_kernel, attn_fwd_kernel, preprocess, main, finalize
+
+
+class AttnStep:
+    """Device buffers of one workload and its fwd+bwd step through the public
+    calls (the forward, then the backward's three stages), with optional
+    CUDA events between the calls."""
+
+    def __init__(self, esd, w, inp, dev):
+        import torch
+        self.esd, self.w = esd, w
+        self.kv = None if inp.kv_len is None else inp.kv_len.tolist()
+        off = w.causal_offset if w.causal else None
+        self.mask = dict(causal=w.causal, causal_offset=off, kv_len=self.kv)
+        self.shape = esd.make_shape(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv)
+        self.pairs = esd.attn_visible_pairs(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv, **self.mask)
+        ff, fb = flops_per_pair(w.dh, w.dv)
+        self.flops_fwd, self.flops_bwd = self.pairs * ff, self.pairs * fb
+        self.scale = 1.0 / math.sqrt(w.dh)
+        self.Q, self.K, self.V, self.dO = (x.to(dev) for x in (inp.Q, inp.K, inp.V, inp.dO))
+        self.O = torch.empty((w.B, w.Hq, w.nq, w.dv), dtype=torch.bfloat16, device=dev)
+        self.LSE = torch.empty((w.B, w.Hq, w.nq), dtype=torch.float32, device=dev)
+        self.O_lo = torch.empty_like(self.O)
+        self.dQ, self.dK, self.dV = torch.empty_like(self.Q), torch.empty_like(self.K), torch.empty_like(self.V)
+        dims = (w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv)
+        self.fws = torch.empty((esd.attn_fwd_workspace_bytes(*dims),), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty((esd.attn_bwd_workspace_bytes(*dims),), dtype=torch.uint8, device=dev)
+        self.rows = w.B * w.Hq * w.nq
+
+    def tensors(self):
+        return (self.Q, self.K, self.V, self.dO, self.O, self.O_lo, self.LSE, self.dQ, self.dK, self.dV, self.ws,
+                self.fws)
+
+    def bytes_touched(self):
+        return sum(x.numel() * x.element_size() for x in self.tensors())
+
+    def __call__(self, stream, ev=None):
+        esd = self.esd
+        if ev is not None:
+            ev[0].record(stream)
+        esd.attn_fwd(self.Q, self.K, self.V, scale=self.scale, O=self.O, LSE=self.LSE, O_lo=self.O_lo,
+                     workspace=self.fws, stream=stream, **self.mask)
+        if ev is not None:
+            ev[1].record(stream)
+        esd.attn_bwd_preprocess(self.Q, self.O, self.dO, self.ws, shape=self.shape, O_lo=self.O_lo, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        esd.attn_bwd_main(self.K, self.V, self.LSE, self.ws, self.dK, self.dV, shape=self.shape, scale=self.scale,
+                          stream=stream, **self.mask)
+        if ev is not None:
+            ev[3].record(stream)
+        esd.attn_bwd_finalize(self.ws, self.dQ, shape=self.shape, scale=self.scale, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def io_bytes(self):
+        """Algorithmic bytes of the two memory-bound backward kernels: one read
+        of each input, one write of each output."""
+        w, rows = self.w, self.rows
+        bhq = w.B * w.Hq
+        return {
+            "attn_bwd_preprocess_kernel": (rows * w.dv * 2 * 3 + rows * w.dh * 2 + rows * 4 + rows * w.dh * 4
+                                           + bhq * ((w.nq + 127) // 128) * 16 + rows * w.dh * 2 + rows * w.dv * 2),
+            "attn_bwd_finalize_kernel": rows * w.dh * 4 + rows * w.dh * 2,
+        }
+
+    def compulsory_bytes(self):
+        """One read of Q, K, V, dO and one write of O, LSE, dQ, dK, dV: the HBM
+        floor of a whole fwd+bwd step."""
+        return sum(x.numel() * x.element_size() for x in (self.Q, self.K, self.V, self.dO, self.O, self.LSE,
+                                                          self.dQ, self.dK, self.dV))
+
+
+def time_steps(step, stream, dev, steps, flush=None):
+    """Per-call CUDA-event times (ms, averaged over `steps`) of `step`; when
+    `flush` is given it is written between steps, outside the timed events,
+    so that every step starts with a cold L2."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for k in range(steps):
+        if flush is not None:
+            flush.add_(1)
+        step(stream, evs[k])
+    torch.cuda.synchronize(dev)
+    per = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / steps for i in range(4)]
+    total = sum(e[0].elapsed_time(e[4]) for e in evs) / steps
+    return per, total
+
+
+def config_line(esd, name, dev, steps, warmup, peaks):
+    """One configuration timed on its own: per-stage times, TFLOP/s, fraction
+    of the measured bf16 burst peak (the stages are timed in sub-second
+    regions), and for the tiny single-head case the HBM view and a CUDA-graph
+    replay of the step."""
+    import torch
+    from exact_scaled_dot_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    st = AttnStep(esd, w, make_inputs(w), dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        st(stream)
+    torch.cuda.synchronize(dev)
+    small = st.bytes_touched() < 2 * 129e6
+    flush = torch.empty((64 * 1024 * 1024,), dtype=torch.float32, device=dev) if small else None
+    per, total = time_steps(st, stream, dev, steps, flush)
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    value = (st.flops_fwd + st.flops_bwd) / (total * 1e-3) / 1e12
+    out = {"workload": name, "steps": steps, "ms_per_step": total, "tflops": value, "frac": value / peak,
+           "peak_kind": "bf16_tflops burst", "visible_pairs": st.pairs,
+           "l2": "flushed between steps" if small else "inputs larger than L2",
+           "stages": {}}
+    io = st.io_bytes()
+    for stage, ms in zip(KERNEL_STAGES, per):
+        ent = {"ms": ms}
+        if stage.startswith("attn_fwd"):
+            ent["tflops"] = st.flops_fwd / (ms * 1e-3) / 1e12
+            ent["frac"] = ent["tflops"] / peak
+        elif stage == "attn_bwd_main_kernel":
+            ent["tflops"] = st.flops_bwd / (ms * 1e-3) / 1e12
+            ent["frac"] = ent["tflops"] / peak
+        else:
+            ent["gbs"] = io[stage] / (ms * 1e-3) / 1e9
+            ent["frac_hbm"] = ent["gbs"] / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        out["stages"][stage] = ent
+    if small:
+        # Launch-bound: the HBM floor of the step against its time, and the
+        # same step replayed from a CUDA graph (no host work between launches).
+        cb = st.compulsory_bytes()
+        out["hbm"] = {"compulsory_bytes": cb, "ideal_us": cb / (peaks.get("hbm_gbs", 6800.0) * 1e9) * 1e6,
+                      "achieved_gbs": cb / (total * 1e-3) / 1e9}
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                st(side)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g):
+                st(torch.cuda.current_stream(dev))
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ms = 0.0
+            for _ in range(steps):
+                flush.add_(1)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                ms += a.elapsed_time(b)
+            ms /= steps
+            out["graph_replay"] = {"ms_per_step": ms, "tflops": (st.flops_fwd + st.flops_bwd) / (ms * 1e-3) / 1e12,
+                                   "achieved_gbs": cb / (ms * 1e-3) / 1e9}
+        except Exception as e:  # noqa: BLE001 - report, do not fail the line
+            out["graph_replay"] = {"error": f"{type(e).__name__}: {e}"}
+    status = esd.attn_get_status()
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status}: {esd.strerror(status)}")
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_cuda(args):
     import numpy as np
     import torch
@@ -247,43 +413,20 @@ def run_cuda(args):
     if args.batch is not None:
         w = w.scaled(B=args.batch)
     inp = make_inputs(w)
-    kv = None if inp.kv_len is None else inp.kv_len.tolist()
-    off = w.causal_offset if w.causal else None
-    mask = dict(causal=w.causal, causal_offset=off, kv_len=kv)
-    shape = esd.make_shape(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv)
-    pairs = esd.attn_visible_pairs(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv, **mask)
+    st = AttnStep(esd, w, inp, dev)
+    kv, mask, scale, shape = st.kv, st.mask, st.scale, st.shape
+    off = mask["causal_offset"]
+    pairs, flops_fwd, flops_bwd = st.pairs, st.flops_fwd, st.flops_bwd
     ff, fb = flops_per_pair(w.dh, w.dv)
-    flops_fwd, flops_bwd = pairs * ff, pairs * fb
-    scale = 1.0 / math.sqrt(w.dh)
-
-    Q, K, V, dO = (x.to(dev) for x in (inp.Q, inp.K, inp.V, inp.dO))
-    O = torch.empty((w.B, w.Hq, w.nq, w.dv), dtype=torch.bfloat16, device=dev)
-    LSE = torch.empty((w.B, w.Hq, w.nq), dtype=torch.float32, device=dev)
-    O_lo = torch.empty_like(O)
-    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    rows = w.B * w.Hq * w.nq
-    ws = torch.empty((esd.attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv),),
-                     dtype=torch.uint8, device=dev)
+    Q, K, V, dO, O, O_lo, LSE, dQ, dK, dV, ws, fws = st.tensors()
+    rows = st.rows
     stream = torch.cuda.current_stream(dev)
     esd.attn_clear_status()
 
     def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        esd.attn_fwd(Q, K, V, scale=scale, O=O, LSE=LSE, O_lo=O_lo, **mask)
-        if ev is not None:
-            ev[1].record(stream)
-        esd.attn_bwd_preprocess(Q, O, dO, ws, shape=shape, O_lo=O_lo)
-        if ev is not None:
-            ev[2].record(stream)
-        esd.attn_bwd_main(K, V, LSE, ws, dK, dV, shape=shape, scale=scale, **mask)
-        if ev is not None:
-            ev[3].record(stream)
-        esd.attn_bwd_finalize(ws, dQ, shape=shape, scale=scale)
-        if ev is not None:
-            ev[4].record(stream)
+        st(stream, ev)
 
-    launches_per_step = 4
+    launches_per_step = LAUNCHES_PER_STEP
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -315,24 +458,22 @@ def run_cuda(args):
     ms_per_step = elapsed_ms / args.steps
     value = job_throughput(flops_fwd + flops_bwd, world, ms_per_step)
 
-    names = ["attn_fwd_kernel", "attn_bwd_preprocess_kernel", "attn_bwd_main_kernel", "attn_bwd_finalize_kernel"]
+    names = KERNEL_STAGES
     per_kernel = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i, n in enumerate(names)}
 
     # ---- roofline of the dominant kernel ----
+    # Every stage is timed inside a region of well under a second, so the
+    # measured burst bf16 peak is the denominator (the sustained one is for
+    # seconds-long loops under the power cap).
     peaks, peak_src = load_peaks()
-    bhq = w.B * w.Hq
-    bytes_io = {
-        "attn_bwd_preprocess_kernel": (rows * w.dv * 2 * 4 + rows * 4 + rows * w.dh * 4 + bhq * (w.nq // 128 + 1) * 8
-                                       + rows * w.dh * 2 * 2),
-        "attn_bwd_finalize_kernel": rows * w.dh * 4 + rows * w.dh * 2,
-    }
+    bytes_io = st.io_bytes()
     dominant = max(per_kernel, key=per_kernel.get)
-    if dominant in ("attn_fwd_kernel", "attn_bwd_main_kernel"):
-        work = flops_fwd if dominant == "attn_fwd_kernel" else flops_bwd
+    if dominant in (names[0], "attn_bwd_main_kernel"):
+        work = flops_fwd if dominant == names[0] else flops_bwd
         achieved = work / (per_kernel[dominant] * 1e-3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_kind": f"bf16_tflops_sustained ({peak_src})"}
+                "frac": achieved / peak, "peak_kind": f"bf16_tflops burst ({peak_src})"}
     else:
         achieved = bytes_io[dominant] / (per_kernel[dominant] * 1e-3) / 1e9
         peak = peaks.get("hbm_gbs")
@@ -352,7 +493,7 @@ def run_cuda(args):
     for n in names:
         ms = per_kernel[n]
         ent = {"ms": ms, "share": ms / sum(per_kernel.values())}
-        if n == "attn_fwd_kernel":
+        if n == names[0]:
             ent["tflops"] = flops_fwd / (ms * 1e-3) / 1e12
         elif n == "attn_bwd_main_kernel":
             ent["tflops"] = flops_bwd / (ms * 1e-3) / 1e12
@@ -378,7 +519,7 @@ def run_cuda(args):
             dsets.append({"Q": torch.empty_like(Q), "K": torch.empty_like(K), "V": torch.empty_like(V),
                           "dO": torch.empty_like(dO), "O": torch.empty_like(O), "LSE": torch.empty_like(LSE),
                           "O_lo": torch.empty_like(O_lo), "dQ": torch.empty_like(dQ), "dK": torch.empty_like(dK),
-                          "dV": torch.empty_like(dV), "ws": torch.empty_like(ws)})
+                          "dV": torch.empty_like(dV), "ws": torch.empty_like(ws), "fws": torch.empty_like(fws)})
             hsets.append({k: torch.empty(dsets[-1][k].shape, dtype=dsets[-1][k].dtype).pin_memory()
                           for k in ("O", "LSE", "dQ", "dK", "dV")})
         h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hdO))
@@ -404,7 +545,7 @@ def run_cuda(args):
                 if k_step >= nbuf:
                     s_cmp.wait_event(ev_out[k])      # the set's previous results have been read back
                 esd.attn_fwd(d["Q"], d["K"], d["V"], scale=scale, O=d["O"], LSE=d["LSE"], O_lo=d["O_lo"],
-                             stream=s_cmp, **mask)
+                             workspace=d["fws"], stream=s_cmp, **mask)
                 esd.attn_bwd(d["Q"], d["K"], d["V"], d["O"], d["dO"], d["LSE"], O_lo=d["O_lo"], scale=scale,
                              dQ=d["dQ"], dK=d["dK"], dV=d["dV"], workspace=d["ws"], stream=s_cmp, **mask)
                 ev_cmp[k].record(s_cmp)
@@ -439,6 +580,8 @@ def run_cuda(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "pipeline": "uploads, kernels and downloads of consecutive steps on three streams, two buffer sets"}
 
+    bytes_touched = st.bytes_touched()
+
     # ---- parity spot check (oracle rows, forward and dQ) and CPU baseline ----
     parity = None
     cpu = None
@@ -464,6 +607,18 @@ def run_cuda(args):
         v, desc, threads, _dt = oracle_cpu_sample(w, inp, args.cpu_rows)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
 
+    # ---- the other configurations, each timed on its own after the headline ----
+    configs = None
+    if not args.no_configs and args.batch is None:
+        from exact_scaled_dot_gb300.inputs import WORKLOAD_ORDER
+        del st, Q, K, V, dO, O, LSE, O_lo, dQ, dK, dV, ws, fws
+        torch.cuda.empty_cache()
+        configs = {}
+        for name in WORKLOAD_ORDER:
+            if name == w.name:
+                continue
+            configs[name] = config_line(esd, name, dev, args.config_steps, 3, peaks)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -480,9 +635,7 @@ def run_cuda(args):
                        "arithmetic": "bf16 inputs and outputs; Q K^T in bf16, P V and every backward product in "
                                      "fp16 (exact re-encoding of the bf16 operands), fp32 accumulation",
                        "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (about %.0f MB touched per step)" % (
-                           sum(x.numel() * x.element_size() for x in (Q, K, V, dO, O, O_lo, LSE, dQ, dK, dV, ws))
-                           / 1e6)},
+                       "l2": "inputs larger than L2 (about %.0f MB touched per step)" % (bytes_touched / 1e6)},
             "peak_fraction": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
             "roofline": roof,
             "kernels": kernels,
@@ -491,6 +644,7 @@ def run_cuda(args):
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "parity": parity,
+            "configs": configs,
         }
         print(json.dumps(line))
     if world > 1:
@@ -547,7 +701,10 @@ def run_decode(args):
     status = esd.attn_get_status()
     if status != 0:
         raise RuntimeError(f"device status {status}: {esd.strerror(status)}")
-    ms_regular = timed(lambda: esd.attn_fwd(Q, K, V, O=O, LSE=LSE, O_lo=O_lo, **mask), max(5, args.steps // 4))
+    fws = torch.empty((esd.attn_fwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv),), dtype=torch.uint8,
+                      device=dev)
+    ms_regular = timed(lambda: esd.attn_fwd(Q, K, V, O=O, LSE=LSE, O_lo=O_lo, workspace=fws, **mask),
+                       max(5, args.steps // 4))
     esd.attn_fwd_decode(Q, K, V, O=O, LSE=LSE, O_lo=O_lo, workspace=ws, **mask)
     torch.cuda.synchronize(dev)
 
@@ -626,6 +783,8 @@ def run_varlen(args):
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     need = esd.attn_bwd_varlen_workspace_bytes(w.Hq, w.Hkv, w.dh, w.dv, inp.cu_q, inp.cu_k, causal=w.causal)
     ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    fneed = esd.attn_fwd_varlen_workspace_bytes(w.Hq, w.Hkv, w.dh, w.dv, inp.cu_q, inp.cu_k, causal=w.causal)
+    fws = torch.empty((max(fneed, 256),), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     pairs = esd.attn_varlen_visible_pairs(w.Hq, w.Hkv, w.dh, w.dv, inp.cu_q, inp.cu_k, causal=w.causal)
     flops_fwd = pairs * 2 * (w.dh + w.dv)
@@ -635,7 +794,7 @@ def run_varlen(args):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        esd.attn_fwd_varlen(Q, K, V, inp.cu_q, inp.cu_k, causal=w.causal, O=O, LSE=LSE, O_lo=O_lo)
+        esd.attn_fwd_varlen(Q, K, V, inp.cu_q, inp.cu_k, causal=w.causal, O=O, LSE=LSE, O_lo=O_lo, workspace=fws)
         if ev is not None:
             ev[1].record(stream)
         esd.attn_bwd_varlen(Q, K, V, O, dO, LSE, inp.cu_q, inp.cu_k, O_lo=O_lo, causal=w.causal, dQ=dQ, dK=dK,
@@ -707,7 +866,7 @@ def run_varlen(args):
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
                      "frac": tflops / peaks.get("bf16_tflops"), "peak_kind": f"bf16_tflops burst ({peak_src})",
                      "traffic": None},
-        "clocks": clocks, "parity": parity, "gpu_launches": 4 * args.steps,
+        "clocks": clocks, "parity": parity, "gpu_launches": 5 * args.steps,
     }
     print(json.dumps(line))
     return 0
@@ -889,6 +1048,8 @@ def main(argv=None):
     ap.add_argument("--reference-rows", type=int, default=384, help="query rows per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-oracle", action="store_true", help="skip the parity spot check and CPU baseline")
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the other configurations")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps per other configuration")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("need --steps >= 1 and --warmup >= 0")

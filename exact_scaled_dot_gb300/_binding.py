@@ -27,11 +27,12 @@ ATTN_ERR_WORKSPACE = 7
 ATTN_ERR_CUDA = 8
 ATTN_ERR_TIMEOUT = 9
 ATTN_ERR_DEVICE = 10
+ATTN_ERR_RANGE = 11
 ATTN_MAX_BATCH = 512
 ATTN_OFFSET_DEFAULT = -(2 ** 63)
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+EXPORTS = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_varlen_workspace_bytes", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
            "attn_bwd_finalize", "attn_visible_pairs", "attn_get_status", "attn_clear_status",
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
@@ -77,7 +78,9 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(str(p))
     S, M = ctypes.POINTER(AttnShape), ctypes.POINTER(AttnMask)
     f = ctypes.c_float
-    lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd_workspace_bytes.argtypes = [S]
+    lib.attn_fwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_decode.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.attn_fwd_decode_workspace_bytes.argtypes = [S, M]
     lib.attn_fwd_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -103,7 +106,9 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     VL = ctypes.POINTER(AttnVarlen)
     lib.attn_varlen_visible_pairs.argtypes = [VL]
     lib.attn_varlen_visible_pairs.restype = ctypes.c_int64
-    lib.attn_fwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_fwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd_varlen_workspace_bytes.argtypes = [VL]
+    lib.attn_fwd_varlen_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_varlen_workspace_bytes.argtypes = [VL]
     lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -204,15 +209,21 @@ def _check_qkv(Q, K, V):
 # ---------------------------------------------------------------------------
 # Public functions (names follow the C ABI)
 # ---------------------------------------------------------------------------
+def attn_fwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
+    shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
+    return int(load().attn_fwd_workspace_bytes(ctypes.byref(shape)))
+
+
 def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
              causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
              O: Optional[torch.Tensor] = None, LSE: Optional[torch.Tensor] = None,
-             O_lo: Optional[torch.Tensor] = None, residual: bool = True, stream=None):
+             O_lo: Optional[torch.Tensor] = None, residual: bool = True, workspace=None, stream=None):
     """Forward pass: returns (O [B,Hq,n_q,d_v] bf16, LSE [B,Hq,n_q] fp32, O_lo).
 
-    O_lo is the bf16 rounding residual of O (O + O_lo ~ the fp32 result), for
-    the backward's row term; it is None when ``residual`` is False and no
-    O_lo tensor is given."""
+    O_lo is the bf16 rounding residual of O (O + O_lo ~ the fp32 result), which
+    the backward requires for its row term; it is None when ``residual`` is
+    False and no O_lo tensor is given.  ``workspace`` (uint8, at least
+    attn_fwd_workspace_bytes) is created here by torch when not given."""
     dims, dev = _check_qkv(Q, K, V)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
@@ -228,8 +239,11 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool 
         _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
+    if workspace is None:
+        need = int(load().attn_fwd_workspace_bytes(ctypes.byref(shape)))
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
-                         _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), _stream(dev, stream))
+                         _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), *_ws(workspace), _stream(dev, stream))
     _check(rc, "attn_fwd")
     return O, LSE, O_lo
 
@@ -280,7 +294,10 @@ def attn_bwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
 
 def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_offset: Optional[int] = None,
              kv_len=None, scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
-    """Backward pass: returns (dQ, dK, dV) in bf16; dK, dV summed over each KV head's group."""
+    """Backward pass: returns (dQ, dK, dV) in bf16; dK, dV summed over each KV head's group.
+
+    O_lo (the forward's residual) is required; without it the library
+    returns ATTN_ERR_NULL, raised here as AttnError."""
     dims, dev = _check_qkv(Q, K, V)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
@@ -449,8 +466,13 @@ def attn_varlen_visible_pairs(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, 
     return int(load().attn_varlen_visible_pairs(ctypes.byref(a.v)))
 
 
+def attn_fwd_varlen_workspace_bytes(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False) -> int:
+    a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
+    return int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+
+
 def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False, scale: Optional[float] = None,
-                    O=None, LSE=None, O_lo=None, residual: bool = True, stream=None):
+                    O=None, LSE=None, O_lo=None, residual: bool = True, workspace=None, stream=None):
     """Forward over packed sequences: Q [T_q, Hq, d_h], K [T_k, Hkv, d_h], V [T_k, Hkv, d_v] (bf16);
     cu_seqlens_* are host offsets [B + 1].  Returns (O [T_q, Hq, d_v], LSE [Hq, T_q] fp32, O_lo)."""
     (Tq, Tk, Hq, Hkv, d_h, d_v), dev = _varlen_dims(Q, K, V)
@@ -468,8 +490,11 @@ def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False
     _check_tensor(LSE, "LSE", torch.float32, (Hq, Tq), dev)
     if O_lo is not None:
         _check_tensor(O_lo, "O_lo", torch.bfloat16, (Tq, Hq, d_v), dev)
+    if workspace is None:
+        need = int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     rc = load().attn_fwd_varlen(ctypes.byref(a.v), ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
-                                _ptr(LSE), _ptr(O_lo), _stream(dev, stream))
+                                _ptr(LSE), _ptr(O_lo), *_ws(workspace), _stream(dev, stream))
     _check(rc, "attn_fwd_varlen")
     return O, LSE, O_lo
 

@@ -13,6 +13,7 @@
 
 #include "../../include/attn.h"
 #include "common.cuh"
+#include "f16range.cuh"
 #include "ptx.cuh"
 
 namespace esd {
@@ -311,12 +312,14 @@ ShapeParams shape_params(const attn_shape* s) {
 
 int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq * s->n_q; }
 
-// Backward workspace: D [rows] | per-query-tile maxima float2 [B*Hq*nqt] |
+// Backward workspace: D [rows] | per-query-tile maxima and fp16 exponents
+// float4 [B*Hq*nqt] | per-group fp16 exponents float2 [B*Hkv] |
 // fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h] | fp16 copy
 // of dO [rows * d_v], each 256-byte aligned.
 struct Workspace {
   float* D;
-  float2* tilemax;
+  float4* tilemax;
+  float2* grpexp;
   float* dQacc;
   void* Q16;
   void* dO16;
@@ -329,13 +332,15 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base) {
   const size_t nqt = (static_cast<size_t>(s->n_q) + 127) / 128;
   const size_t tiles = static_cast<size_t>(s->B) * s->Hq * nqt;
   const size_t off_t = round256(rows * sizeof(float));
-  const size_t off_a = off_t + round256(tiles * sizeof(float2));
+  const size_t off_g = off_t + round256(tiles * sizeof(float4));
+  const size_t off_a = off_g + round256(static_cast<size_t>(s->B) * s->Hkv * sizeof(float2));
   const size_t off_q = off_a + round256(rows * static_cast<size_t>(s->d_h) * sizeof(float));
   const size_t off_o = off_q + round256(rows * static_cast<size_t>(s->d_h) * 2);
   Workspace w;
   uint8_t* b = static_cast<uint8_t*>(base);
   w.D = reinterpret_cast<float*>(b);
-  w.tilemax = reinterpret_cast<float2*>(b + off_t);
+  w.tilemax = reinterpret_cast<float4*>(b + off_t);
+  w.grpexp = reinterpret_cast<float2*>(b + off_g);
   w.dQacc = reinterpret_cast<float*>(b + off_a);
   w.Q16 = b + off_q;
   w.dO16 = b + off_o;
@@ -349,6 +354,65 @@ Workspace workspace_layout(const attn_shape* s, void* base) {
 
 Workspace workspace_layout_varlen(const Varlen& v, void* base) {
   return workspace_layout_rows(&v.shape, static_cast<size_t>(v.total_q) * v.shape.Hq, base);
+}
+
+// Forward workspace: the fp16 V tiles [B Hkv][nkt 128][d_v] | their
+// exponents int32 [B Hkv][nkt], each 256-byte aligned.
+struct FwdWorkspace {
+  void* V16;
+  int32_t* vexp;
+  int nkt;
+  size_t bytes;
+};
+
+FwdWorkspace fwd_workspace_layout(const attn_shape* s, void* base) {
+  FwdWorkspace w;
+  w.nkt = (s->n_k + kTileN - 1) / kTileN;
+  const size_t tiles = static_cast<size_t>(s->B) * s->Hkv * w.nkt;
+  const size_t v16 = round256(tiles * kTileN * static_cast<size_t>(s->d_v) * 2);
+  uint8_t* b = static_cast<uint8_t*>(base);
+  w.V16 = b;
+  w.vexp = reinterpret_cast<int32_t*>(b + v16);
+  w.bytes = v16 + round256(tiles * sizeof(int32_t));
+  return w;
+}
+
+int check_fwd_workspace(const attn_shape* s, const void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_WORKSPACE;
+  if (bytes < fwd_workspace_layout(s, nullptr).bytes) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+// The fp16 V pre-pass and the forward kernel, both on `stream`.
+int launch_forward(const attn_shape* shape, const MaskParams& mask, const LayoutParams& lay, float scale,
+                   const CUtensorMap& tq, const CUtensorMap& tk, const void* V, const FwdWorkspace& w, void* O,
+                   float* LSE, void* O_lo, unsigned int* status, cudaStream_t st) {
+  CUtensorMap tv;
+  if (!make_tmap(&tv, w.V16, shape->d_v, w.nkt * kTileN, static_cast<int64_t>(shape->B) * shape->Hkv))
+    return ATTN_ERR_CUDA;
+  V16Params vp;
+  vp.sh = shape_params(shape);
+  vp.mask = mask;
+  vp.lay = lay;
+  vp.nkt = w.nkt;
+  vp.V = V;
+  vp.V16 = w.V16;
+  vp.vexp = w.vexp;
+  vp.status = status;
+  if (launch_attn_v16(shape->d_v, vp, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  FwdParams p;
+  p.sh = vp.sh;
+  p.mask = mask;
+  p.lay = lay;
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.O = O;
+  p.O_lo = O_lo;
+  p.LSE = LSE;
+  p.vexp = w.vexp;
+  p.nkt = w.nkt;
+  p.status = status;
+  return launch_attn_fwd(shape->d_h, shape->d_v, tq, tk, tv, p, st) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int check_workspace(const attn_shape* s, const void* ws, size_t bytes) {
@@ -368,7 +432,7 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* status) {
   __syncthreads();
   // Nothing ever arrives on this barrier: the wait has to give up by itself.
   const bool ok = mbar_wait(smem_u32(&never), 0, &abort_flag, limit_ns);
-  if (!ok && threadIdx.x == 0) atomicCAS(status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+  if (!ok && threadIdx.x == 0) record_status(status, ATTN_ERR_TIMEOUT);
 }
 
 }  // namespace
@@ -487,6 +551,7 @@ const char* attn_strerror(int status) {
     case ATTN_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case ATTN_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
     case ATTN_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case ATTN_ERR_RANGE: return "an input tile's magnitude (2^46 or more) was beyond the fp16 operands";
     default: return "unknown status";
   }
 }
@@ -505,39 +570,39 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
   return workspace_layout(shape, nullptr).bytes;
 }
 
+size_t attn_fwd_workspace_bytes(const attn_shape* shape) {
+  if (check_shape(shape) != ATTN_OK) return 0;
+  return fwd_workspace_layout(shape, nullptr).bytes;
+}
+
 int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-             const void* V, void* O, float* LSE, void* O_lo, void* stream) {
+             const void* V, void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes,
+             void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
-  FwdParams p;
-  rc = build_mask(shape, mask, &p.mask);
+  MaskParams m;
+  rc = build_mask(shape, mask, &m);
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, LSE});
   if (rc) return rc;
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+  rc = check_fwd_workspace(shape, workspace, workspace_bytes);
+  if (rc) return rc;
   // ---- CUDA from here on ----
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
-  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
-      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk))
+  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk))
     return ATTN_ERR_CUDA;
-  p.sh = shape_params(shape);
-  std::memset(&p.lay, 0, sizeof(p.lay));
-  p.scale_log2 = scale * kLog2e;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
-  p.O = O;
-  p.O_lo = O_lo;
-  p.LSE = LSE;
-  p.status = status;
-  const cudaError_t e =
-      launch_attn_fwd(shape->d_h, shape->d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  LayoutParams lay;
+  std::memset(&lay, 0, sizeof(lay));
+  return launch_forward(shape, m, lay, scale, tq, tk, V, fwd_workspace_layout(shape, workspace), O, LSE, O_lo,
+                        status, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_fwd_decode_workspace_bytes(const attn_shape* shape, const attn_mask* mask) {
@@ -608,21 +673,18 @@ int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O, c
                         void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
-  rc = check_ptrs({Q, O, dO});
+  rc = check_ptrs({Q, O, O_lo, dO});
   if (rc) return rc;
-  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
   const Workspace w = workspace_layout(shape, workspace);
-  MaskParams no_mask;
   LayoutParams padded;
-  std::memset(&no_mask, 0, sizeof(no_mask));
   std::memset(&padded, 0, sizeof(padded));
-  const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), no_mask, padded, shape->d_v, shape->d_h, Q,
-                                                   O, O_lo, dO, w.D, w.tilemax, w.dQacc, w.Q16, w.dO16,
+  const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), padded, shape->d_v, shape->d_h, Q, O, O_lo,
+                                                   dO, w.D, w.tilemax, w.grpexp, w.dQacc, w.Q16, w.dO16, status,
                                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -659,6 +721,7 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   p.LSE = LSE;
   p.D = w.D;
   p.tilemax = w.tilemax;
+  p.grpexp = w.grpexp;
   p.nqt = (shape->n_q + 127) / 128;
   p.dQacc = w.dQacc;
   p.dK = dK;
@@ -698,9 +761,8 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
-  rc = check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV});
+  rc = check_ptrs({Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV});
   if (rc) return rc;
-  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
   rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
   rc = attn_bwd_preprocess(shape, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
@@ -754,6 +816,14 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale
   int rc = check_shape(shape);
   if (rc) return rc;
   if (workspace_layout(shape, nullptr).bytes > kStaticBwdScratchBytes) return ATTN_ERR_WORKSPACE;
+  // Every argument check before the first CUDA call (the symbol lookup).
+  MaskParams m;
+  rc = build_mask(shape, mask, &m);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_ptrs({Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV});
+  if (rc) return rc;
   void* scratch = nullptr;
   rc = static_scratch_ptr(&scratch);
   if (rc) return rc;
@@ -887,8 +957,14 @@ int64_t attn_varlen_visible_pairs(const attn_varlen* v) {
   return total * v->Hq;
 }
 
+size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v) {
+  Varlen d;
+  if (build_varlen(v, &d) != ATTN_OK) return 0;
+  return fwd_workspace_layout(&d.shape, nullptr).bytes;
+}
+
 int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V, void* O,
-                    float* LSE, void* O_lo, void* stream) {
+                    float* LSE, void* O_lo, void* workspace, size_t workspace_bytes, void* stream) {
   Varlen d;
   int rc = build_varlen(v, &d);
   if (rc) return rc;
@@ -898,26 +974,17 @@ int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   rc = check_ptrs({Q, K, V, O, LSE});
   if (rc) return rc;
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+  rc = check_fwd_workspace(&d.shape, workspace, workspace_bytes);
+  if (rc) return rc;
   // ---- CUDA from here on ----
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q) || !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k) ||
-      !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k))
+  CUtensorMap tq, tk;
+  if (!make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q) || !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k))
     return ATTN_ERR_CUDA;
-  FwdParams p;
-  p.sh = shape_params(&d.shape);
-  p.mask = d.mask;
-  p.lay = d.lay;
-  p.scale_log2 = scale * kLog2e;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
-  p.O = O;
-  p.O_lo = O_lo;
-  p.LSE = LSE;
-  p.status = status;
-  const cudaError_t e = launch_attn_fwd(v->d_h, v->d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return launch_forward(&d.shape, d.mask, d.lay, scale, tq, tk, V, fwd_workspace_layout(&d.shape, workspace), O, LSE,
+                        O_lo, status, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v) {
@@ -939,9 +1006,8 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
     if (rc) return rc;
   }
   if (d.total_q > 0) {
-    rc = check_ptrs({Q, O, dO, LSE, dQ});
+    rc = check_ptrs({Q, O, O_lo, dO, LSE, dQ});
     if (rc) return rc;
-    if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
     const Workspace need = workspace_layout_varlen(d, nullptr);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need.bytes)
       return ATTN_ERR_WORKSPACE;
@@ -961,8 +1027,8 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   if (rc) return rc;
   const Workspace w = workspace_layout_varlen(d, workspace);
   const ShapeParams sh = shape_params(&d.shape);
-  cudaError_t e = launch_attn_bwd_preprocess(sh, d.mask, d.lay, v->d_v, v->d_h, Q, O, O_lo, dO, w.D, w.tilemax,
-                                             w.dQacc, w.Q16, w.dO16, st);
+  cudaError_t e = launch_attn_bwd_preprocess(sh, d.lay, v->d_v, v->d_h, Q, O, O_lo, dO, w.D, w.tilemax, w.grpexp,
+                                             w.dQacc, w.Q16, w.dO16, status, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_packed(&tq, w.Q16, v->d_h, v->Hq, d.total_q) ||
@@ -980,6 +1046,7 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   p.LSE = LSE;
   p.D = w.D;
   p.tilemax = w.tilemax;
+  p.grpexp = w.grpexp;
   p.nqt = (d.shape.n_q + 127) / 128;
   p.dQacc = w.dQacc;
   p.dK = dK;

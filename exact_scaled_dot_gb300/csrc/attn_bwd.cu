@@ -11,15 +11,20 @@
 // scores and the forward's log-sum-exp, A_ij = exp(scale q_i.k_j - LSE_i)
 // (the recomputation the appendix names in section A.10.6).
 //
-// Three kernels:
+// Four kernels:
 //   preprocess  D_i = sum_l dO_il O_il (equal to c_i of A.10.7 because
 //               O_i = sum_j A_ij v_j), zeroes the fp32 dQ accumulator and
 //               writes Q and dO re-encoded as fp16 (the main kernel's
-//               operands).
-//               O is taken as the bf16 output plus, when given, the
-//               forward's bf16 rounding residual, so D is not limited by the
-//               bf16 rounding of O.  Per 128-row query tile it also records
-//               max ||dO_i|| and max |D_i|, which bound |dS| (below).
+//               operands), each query tile scaled by a power of two from its
+//               largest magnitude (f16range.cuh).
+//               O is taken as the bf16 output plus the forward's bf16
+//               rounding residual, so D is not limited by the bf16 rounding
+//               of O.  Per 128-row query tile it also records max ||dO_i||
+//               and max |D_i|, which bound |dS| (below).
+//   group exp   brings the fp16 query tiles of each (batch, KV head) group to
+//               one exponent for Q and one for dO (usually they agree and
+//               nothing is rewritten), so the main kernel's steps share one
+//               scale.
 //   main        one CTA per (batch, KV head, 128-key tile).  It loops over
 //               the query heads of its group and the query tiles that can
 //               see its keys, keeps dK and dV in tensor memory for the whole
@@ -37,9 +42,9 @@
 //               P^T = exp2(S^T scale log2e - LSE log2e) and
 //               dS = P (dP - D), P^T written back to tensor memory (for
 //               dV) and dS to shared memory (for dQ and dK).
-//   warps 12-15 convert K and V to fp16 in shared memory, read dQ out of
-//               tensor memory into the accumulator and write the final dK,
-//               dV.
+//   warps 12-15 convert K and V to fp16 in shared memory (each scaled by a
+//               power of two of its own), read dQ out of tensor memory into
+//               the accumulator and write the final dK, dV.
 // The producer/MMA and read-out warpgroups hand registers to the score
 // warpgroups (setmaxnreg), which hold 64 scores and the fp16 weights of a
 // step at once.
@@ -48,15 +53,16 @@
 // that largely cancel when a softmax row is sharply peaked, so rounding dS
 // to bf16 (8 significant bits) alone can use up most of a 1e-2 error
 // budget.  dS therefore enters the dK and dQ products as fp16 (11 bits),
-// multiplied by a per-CTA power of two 2^e chosen from the bound
+// multiplied by a per-CTA power of two 2^g chosen from the bound
 //   |dS_ij| <= P_ij |dP_ij - D_i| <= max_i ||dO_i|| max_j ||v_j|| + max_i |D_i|
-// so that |2^e dS| <= 2^14: no fp16 overflow, and small gradients stay far
+// so that |2^g dS| <= 2^14: no fp16 overflow, and small gradients stay far
 // from the fp16 subnormal range.  The scale is exact and undone exactly when
 // dQ is read out and when dK is written.  Every product runs in fp16 (the
-// MMA takes one type for both operands; the conversion of the bf16 inputs
-// is exact for |x| up to 65504 and saturates beyond): Q and dO arrive
-// re-encoded from the preprocess kernel, K and V are converted once per
-// CTA, and the weights P -- one fp16 rounding, used both in dS and as P^T in
+// MMA takes one type for both operands): Q and dO arrive re-encoded by the
+// preprocess, K and V are converted once per CTA, each operand multiplied by
+// a power of two that brings its largest magnitude to the top of the fp16
+// range (CtaScale), so the re-encoding is exact at any input scale; the
+// weights P -- one fp16 rounding, used both in dS and as P^T in
 // dV = P^T dO -- keep 11 significant bits, where bf16 weights left dV
 // errors near the tolerance for keys whose gradient sums a few hundred
 // comparable terms.
@@ -74,6 +80,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "f16range.cuh"
 #include "ptx.cuh"
 
 namespace esd {
@@ -96,8 +103,12 @@ struct BwdCfg {
   static constexpr int kOffStage = kOffDS + kDSTileBytes;          // dQ staging, 4 warps x 8 KB
   static constexpr int kOffLse = kOffStage + 4 * 2 * 32 * 32 * 4;
   static constexpr int kOffDd = kOffLse + kTileM * 4;
-  static constexpr int kOffRed = kOffDd + kTileM * 4;      // 4 warps x 4 floats
-  static constexpr int kOffBar = kOffRed + 64;
+  // Reductions: the score warps' per-warp maxima and exponent extremes
+  // (4 warps x 8 floats), the read-out warps' K-tile maxima (4) and the K
+  // tile's exponent.
+  static constexpr int kOffRed = kOffDd + kTileM * 4;
+  static constexpr int kRedK = 32, kRedKExp = 36;
+  static constexpr int kOffBar = kOffRed + 256;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;                 // [2]
   static constexpr int kBarQEmpty = kBarQFull + 2;    // [2]
@@ -142,14 +153,52 @@ struct BwdCfg {
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
 
-// Power-of-two exponent e with 2^e * bound <= 2^14 (0 for a zero or
-// non-finite bound), clamped so that 2^e and 2^-e are normal floats.
-__device__ __forceinline__ int ds_scale_exponent(float bound) {
-  if (!(bound > 0.f) || !(bound < INFINITY)) return 0;
-  int E;
-  frexpf(bound, &E);           // bound = m 2^E, m in [0.5, 1)
-  int e = 14 - E;
-  return e < -120 ? -120 : (e > 120 ? 120 : e);
+// The CTA's fp16 operand exponents (f16range.cuh): K16 = K 2^k and
+// V16 = V 2^v for its key tile, and Q16 = Q 2^q, dO16 = dO 2^o for every
+// query tile of its (batch, KV head) group (attn_bwd_group_exp_kernel gives
+// all of a group's tiles one q and one o, so no step needs a scale of its
+// own).  The products then carry
+//   S^T = K16 Q16^T = 2^(k + q) S_raw^T,   dP^T = V16 dO16^T = 2^(v + o) dP^T,
+//   dV_acc = P^T dO16 = 2^o dV,
+// and dS enters dQ and dK as fp16 dS' = 2^g dS, with g chosen from the bound
+// |dS_ij| <= max ||dO_i|| max ||v_j|| + max |D_i| (the preprocess's tile
+// maxima and the V tile's row norms) so that |dS'| < 2^14: no fp16
+// overflow, and small gradients stay far from the fp16 subnormals.  Then
+//   dQ_acc = dS' K16 = 2^(g + k) dS K,   dK_acc = dS'^T Q16 = 2^(g + q) dS^T Q,
+// all unscaled exactly.  Every exponent lies in [-30, 30], so each derived
+// multiplier is a normal fp32 power of two.
+struct CtaScale {
+  float mv;        // max_j ||v_j|| over the key tile
+  int v, q, o, g;
+  bool overflow;   // the bound needed g < -30: dS' may saturate
+};
+
+// From the score warps' reduction (per warp w: red[4w .. 4w+2] = max
+// ||v_j||, max ||dO_i||, max |D_i|) and the group's exponents (q, o).
+__device__ __noinline__ CtaScale cta_scale(const float* red, float2 qo) {
+  CtaScale c;
+  float mdo = 0.f, md = 0.f;
+  c.mv = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    c.mv = fmaxf(c.mv, red[4 * w]);
+    mdo = fmaxf(mdo, red[4 * w + 1]);
+    md = fmaxf(md, red[4 * w + 2]);
+  }
+  c.v = f16_tile_exponent(c.mv);
+  if (c.v == kExpZero) c.v = 0;
+  c.q = static_cast<int>(qo.x);
+  c.o = static_cast<int>(qo.y);
+  int g = kExpLimit;
+  const float bound = mdo * c.mv + md;
+  if (bound > 0.f && bound < INFINITY) {
+    int E;
+    frexpf(bound, &E);   // bound < 2^E, so |dS| 2^(14 - E) < 2^14
+    g = min(g, 14 - E);
+  }
+  c.overflow = g < -kExpLimit;
+  c.g = c.overflow ? -kExpLimit : g;
+  return c;
 }
 
 template <int DH, int DV, bool PACKED>
@@ -214,7 +263,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     mbar_init(bar(C::kBarDKDV), 2);    // one commit from each MMA issuer
     mbar_init(bar(C::kBarDrain), 2);
     fence_mbar_init();
-    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
+    *abort_flag = status_blocks(p.status) ? 2 : 0;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -229,17 +278,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const bool w = mbar_wait(bar(idx), parity, abort_flag, limit);
     return __all_sync(0xffffffffu, w);
   };
-  // e of the dS scale, from the four score warps' partial maxima.
-  auto scale_exponent = [&]() -> int {
-    float mv = 0.f, mdo = 0.f, md = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      mv = fmaxf(mv, red_s[4 * w]);
-      mdo = fmaxf(mdo, red_s[4 * w + 1]);
-      md = fmaxf(md, red_s[4 * w + 2]);
-    }
-    return ds_scale_exponent(mdo * mv + md);
-  };
+  // The group's exponents (q, o) (attn_bwd_group_exp_kernel).
+  auto group_exps = [&]() -> float2 { return p.grpexp[bkv]; };
 
   if (warp < 4) setmaxnreg_to<C::kRegsLow, C::kRegsLaunch>();
   if (warp == 0) {
@@ -436,14 +476,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t lane_base = (quad * 32u) << 16;
     const uint32_t tX = tmem + lane_base + C::kTX;
     const uint32_t tY = tmem + lane_base + C::kTY;
-    const float sl2 = p.scale_log2;
     uint8_t* ds_row = smem + C::kOffDS + h * C::kBlockBytes + jj * 128;
     bool ok = *abort_flag == 0 && total > 0;
-    float ds_scale = 1.f;
     if (ok && h == 0) {
-      // ---- bound on |dS| for this CTA -> power-of-two scale ----
-      // (from the bf16 V tile; the read-out warps re-encode it only after
-      // this bound is published)
+      // ---- the bound on |dS| for this CTA (CtaScale) ----
+      // From the bf16 V tile's row norms (the read-out warps re-encode it
+      // only after this reduction is published) and every step's tile
+      // maxima.
       ok = wait_all(C::kBarKV, 0);
       float vn2 = 0.f;
       if (ok && !row_masked) {
@@ -464,7 +503,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       float mv = sqrtf(vn2), mdo = 0.f, md = 0.f;
       for (int idx = tid; idx < total; idx += 128) {
         const int bhq = b * p.sh.Hq + step_head(idx);
-        const float2 t = p.tilemax[static_cast<int64_t>(bhq) * p.nqt + step_q0(idx) / kTileM];
+        const float4 t = p.tilemax[static_cast<int64_t>(bhq) * p.nqt + step_q0(idx) / kTileM];
         mdo = fmaxf(mdo, t.x);
         md = fmaxf(md, t.y);
       }
@@ -481,16 +520,19 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       }
       mbar_arrive(bar(C::kBarScale));
     }
-    if (ok) {
-      ok = wait_all(C::kBarScale, 0);
-      ds_scale = exp2_int(scale_exponent());
-    }
+    CtaScale cs{};
+    const float2 qo = ok ? group_exps() : make_float2(0.f, 0.f);
+    if (ok) ok = wait_all(C::kBarScale, 0);
+    // The CTA's multipliers (CtaScale): the scores come out of S^T = K16
+    // Q16^T as 2^(k + q) S_raw, so P = exp2(S_acc sl2 - LSE log2e) with
+    // sl2 = scale log2e 2^-(k + q); and dS' = 2^g dS =
+    // P (dP_acc cp + (-D) dmul) with cp = 2^(g - o - v), dmul = 2^g.
+    float sl2 = p.scale_log2, cp = 1.f, dmul = 1.f;
     uint32_t pw[32];
     // This thread's -LSE log2(e) and -D entries (query q0 + 64h + tid, for
     // tid < 64) of a step, loaded one step ahead so the global latency is
     // off the critical path.  Both are kept negated so that one paired
-    // fused multiply-add forms x log2(e) scale - LSE log2(e) and
-    // dP 2^e - D 2^e.
+    // fused multiply-add forms x sl2 - LSE log2(e) and dP_acc cp - D dmul.
     auto load_row_terms = [&](int s, float& nlse2, float& nd) {
       const int64_t i = static_cast<int64_t>(step_q0(s)) + 64 * h + tid;
       // Query rows past the sequence get LSE = -inf: their weights P, and so
@@ -508,11 +550,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // both barriers of every step, even after an abort (the step's work is
     // then skipped), so no warp can be left waiting at one.
     float lse_next = 0.f, d_next = 0.f;
+    if (ok) load_row_terms(0, lse_next, d_next);
+    if (ok) ok = wait_all(C::kBarK16, 0);   // the read-out warps publish the K exponent with it
     if (ok) {
-      load_row_terms(0, lse_next, d_next);
+      cs = cta_scale(red_s, qo);
+      const int kexp = static_cast<int>(red_s[C::kRedKExp]);
+      sl2 = p.scale_log2 * exp2_int(-kexp - cs.q);
+      cp = exp2_int(cs.g - cs.o - cs.v);
+      dmul = exp2_int(cs.g);
       if (tid < 64) {
         lse_s[64 * h + tid] = lse_next;
-        dd_s[64 * h + tid] = d_next * ds_scale;
+        dd_s[64 * h + tid] = d_next * dmul;
       }
       if (total > 1) load_row_terms(1, lse_next, d_next);
     }
@@ -583,8 +631,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarDPFull, static_cast<uint32_t>(s & 1));
       if (!ok) break;
       tc_fence_after_sync();
-      // dS pass: dS = P (dP - D), scaled by 2^e, as fp16 into this half's
-      // block of the dS buffer (for dQ and dK); dd_s holds -D 2^e.
+      // dS pass: dS' = dS 2^g (CtaScale) as fp16 into this half's block of
+      // the dS buffer (for dQ and dK).
       {
         uint32_t da[32], db[32];
         tmem_ld32_nowait(tY + 64 * h, da);
@@ -610,7 +658,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const float g0 = __uint_as_float(cq < 2 ? da[r] : db[r]);
             const float g1 = __uint_as_float(cq < 2 ? da[r + 1] : db[r + 1]);
             float t0, t1, d0, d1;
-            ffma2(t0, t1, g0, g1, ds_scale, ds_scale, nd[k], nd[k + 1]);
+            ffma2(t0, t1, g0, g1, cp, cp, nd[k], nd[k + 1]);
             const uint32_t pp = pw[cq * 8 + (k >> 1)];
             fmul2(d0, d1, f16_lo(pp), f16_hi(pp), t0, t1);
             if (need_mask) {
@@ -638,7 +686,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       named_bar_sync(wg_bar, 128);
       if (ok && tid < 64 && s + 1 < total) {
         lse_s[64 * h + tid] = lse_next;
-        dd_s[64 * h + tid] = d_next * ds_scale;
+        dd_s[64 * h + tid] = d_next * dmul;
       }
       if (ok && s + 2 < total) load_row_terms(s + 2, lse_next, d_next);
     }
@@ -651,63 +699,92 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t lane_base = (quad * 32u) << 16;
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
-    auto to_f16 = [](uint4 u) {
-      return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-    };
-    // A K or V tile (`n16` 16-byte chunks, a multiple of 1024) re-encoded
-    // as fp16 in place, rows past kv_len zeroed: eight loads in flight per
-    // thread before their stores (one load-store round trip per chunk would
-    // take several thousand cycles for a tile).
-    auto tile_to_f16 = [&](uint4* t, int n16) {
-      for (int i0 = 0; i0 < n16 / 128; i0 += 8) {
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = t[tid2 + 128 * (i0 + i)];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k = tid2 + 128 * (i0 + i);
-          const int row = (k % (C::kBlockBytes / 16)) / 8;
-          t[k] = (j0 + row >= klen) ? make_uint4(0u, 0u, 0u, 0u) : to_f16(v[i]);
+    CtaScale cs{};
+    int kexp = 0;
+    const float2 qo = (ok && total > 0) ? group_exps() : make_float2(0.f, 0.f);
+    if (total > 0) {
+      // K and V once, as fp16 x 2^k and x 2^v (CtaScale): rows in
+      // [kv_len, n_k) hold caller memory that may be anything (even NaN) and
+      // become zeros -- their dS entries are 0, but 0 * NaN would still
+      // poison dQ.  Rows at or beyond n_k arrive as zeros from the TMA
+      // bounds check.  K first (the first product needs it): the whole tile
+      // is held in registers while the four warps agree on its largest
+      // magnitude; V once the score warps have published the reduction its
+      // exponent comes from.
+      constexpr int kKc = C::kKTileBytes / 16 / 128;
+      uint4* kt = reinterpret_cast<uint4*>(smem + C::kOffK);
+      auto tile_row = [](int k) { return (k % (C::kBlockBytes / 16)) / 8; };   // 8 chunks per 128-byte row
+      if (ok) ok = wait_all(C::kBarKV, 0);
+      uint32_t km = 0u;
+      if (ok) {
+#pragma unroll 8
+        for (int i = 0; i < kKc; ++i) {
+          const uint4 u = kt[tid2 + 128 * i];
+          if (j0 + tile_row(tid2 + 128 * i) < klen) km = bf16_absmax_fold(km, u);
         }
       }
-    };
-    float inv_scale = 1.f;
-    if (ok && total > 0) {
-      // K and V once: rows in [kv_len, n_k) hold caller memory that may be
-      // anything (even NaN) and become zeros -- their dS entries are 0, but
-      // 0 * NaN would still poison dQ.  Rows at or beyond n_k arrive as
-      // zeros from the TMA bounds check.  K first (the first product needs
-      // it); V once the score warps have taken the |dS| bound from it.
-      ok = wait_all(C::kBarKV, 0);
+      float kmax = bf16_absmax_value(km);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+      if (lane == 0) red_s[C::kRedK + quad] = kmax;
+      named_bar_sync(3, 128);   // passed by all four warps, even after an abort
+      kmax = fmaxf(fmaxf(red_s[C::kRedK], red_s[C::kRedK + 1]), fmaxf(red_s[C::kRedK + 2], red_s[C::kRedK + 3]));
+      kexp = f16_tile_exponent(kmax);
+      if (kexp == kExpZero) kexp = 0;
       if (ok) {
-        tile_to_f16(reinterpret_cast<uint4*>(smem + C::kOffK), C::kKTileBytes / 16);
+        const float ks = exp2_int(kexp);
+        for (int i0 = 0; i0 < kKc; i0 += 8) {
+          uint4 kv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) kv[i] = kt[tid2 + 128 * (i0 + i)];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = tid2 + 128 * (i0 + i);
+            kt[k] = (j0 + tile_row(k) >= klen) ? make_uint4(0u, 0u, 0u, 0u) : bf16x8_to_f16x8_scaled(kv[i], ks);
+          }
+        }
+        if (tid2 == 0) red_s[C::kRedKExp] = static_cast<float>(kexp);
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarK16));
       }
       if (ok) ok = wait_all(C::kBarScale, 0);
       if (ok) {
-        inv_scale = exp2_int(-scale_exponent());
-        tile_to_f16(reinterpret_cast<uint4*>(smem + C::kOffV), C::kVTileBytes / 16);
+        cs = cta_scale(red_s, qo);
+        if (tid2 == 0 && (f16_saturates(kmax, kexp) || f16_saturates(cs.mv, cs.v) || cs.overflow))
+          record_status(p.status, ATTN_ERR_RANGE);
+        // V in place, eight loads in flight per thread before their stores.
+        const float vs = exp2_int(cs.v);
+        uint4* vt = reinterpret_cast<uint4*>(smem + C::kOffV);
+        for (int i0 = 0; i0 < C::kVTileBytes / 16 / 128; i0 += 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = vt[tid2 + 128 * (i0 + i)];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = tid2 + 128 * (i0 + i);
+            vt[k] = (j0 + tile_row(k) >= klen) ? make_uint4(0u, 0u, 0u, 0u) : bf16x8_to_f16x8_scaled(v[i], vs);
+          }
+        }
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarV16));
       }
     }
     // dQ read-out: each warp takes its 32 query rows of the tile (in Y) into
     // registers a 64-column round at a time and releases Y after the last
-    // round's loads; it scales them back
-    // by 2^-e and stages them as 32 x 32 fp32 boxes in the 128-byte swizzle
+    // round's loads; it scales them back by 2^-(g + k) (dQ_acc = dS' K16,
+    // CtaScale) and stages them as 32 x 32 fp32 boxes in the 128-byte swizzle
     // pattern (conflict-free stores), and one lane adds the boxes into the
     // fp32 accumulator with TMA reduce-add, a round at a time, the staging
     // memory being reused once a round's boxes have been read.  Rows past
     // n_q are clipped by the tensor map.
     const uint32_t tY = tmem + lane_base + C::kTY;
-    auto stage_box = [&](uint8_t* dst_box, const uint32_t (&v)[32]) {
+    auto stage_box = [&](uint8_t* dst_box, const uint32_t (&v)[32], float inv) {
       uint8_t* dst = dst_box + lane * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<float4*>(dst + ((c ^ (lane & 7)) * 16)) =
-            make_float4(__uint_as_float(v[4 * c]) * inv_scale, __uint_as_float(v[4 * c + 1]) * inv_scale,
-                        __uint_as_float(v[4 * c + 2]) * inv_scale, __uint_as_float(v[4 * c + 3]) * inv_scale);
+            make_float4(__uint_as_float(v[4 * c]) * inv, __uint_as_float(v[4 * c + 1]) * inv,
+                        __uint_as_float(v[4 * c + 2]) * inv, __uint_as_float(v[4 * c + 3]) * inv);
     };
     auto reduce_round = [&](uint8_t* wstage, int first_box, int row0, int head) {
       fence_proxy_async_smem();
@@ -730,6 +807,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
     };
+    const float inv = exp2_int(-cs.g - kexp);
     for (int s = 0; s < total && ok; ++s) {
       const int head = step_head(s);
       const int q0 = step_q0(s);
@@ -754,7 +832,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         staging_free();
 #pragma unroll
-        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, v[bx]);
+        for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, v[bx], inv);
         reduce_round(wstage, rd * C::kDQBoxesPerRound, row0, head);
       }
       __syncwarp();
@@ -770,7 +848,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const int64_t krow = k_row(PACKED, p.lay, p.sh.Hkv, p.sh.n_k, b, hkv, j);
       uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + krow * DH);
       uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + krow * DV);
-      const float dk_scale = p.scale * inv_scale;
+      const float dk_scale = p.scale * exp2_int(-cs.g - cs.q);   // dK_acc = 2^(g + q) dS^T Q (CtaScale)
+      const float dv_scale = exp2_int(-cs.o);                    // dV_acc = 2^o P^T dO
 #pragma unroll
       for (int cc = 0; cc < DH / 32; ++cc) {
         uint32_t w[16];
@@ -795,7 +874,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tmem_ld32(tmem + lane_base + C::kTdV + cc * 32, rr);
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
-            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1]));
+            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * dv_scale, __uint_as_float(rr[k + 1]) * dv_scale);
         } else {
 #pragma unroll
           for (int k = 0; k < 16; ++k) w[k] = 0u;
@@ -814,54 +893,65 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+  if (threadIdx.x == 0 && *abort_flag == 1) record_status(p.status, ATTN_ERR_TIMEOUT);
 }
 
 // Per-tile work of the backward preprocess, for a 128-row query tile:
 //   D_i = sum_l dO_il (O_il + O_lo_il)   (O_lo may be absent),
-//   tilemax = (max_i ||dO_i||_2, max_i |D_i|) over the tile's rows,
+//   tilemax = (max_i ||dO_i||_2, max_i |D_i|, e_Q, e_dO) over the tile's rows,
 // the tile's rows of the fp32 dQ accumulator are zeroed, and its rows of Q
-// and dO are re-encoded as fp16 for the main kernel (exact for |x| <= 65504,
-// saturating beyond).  In the D pass each row has DV/8 consecutive threads,
-// one 16-byte chunk each, so every warp load covers whole rows; the fp16 copy
-// of dO is written from the registers that chunk was loaded into.
+// and dO are re-encoded as fp16 for the main kernel, scaled by 2^e_Q and
+// 2^e_dO (f16range.cuh: the exponents come from the tile's largest
+// magnitudes, so the re-encoding is exact whatever the inputs' scale).  The
+// whole tile's Q and dO therefore stay in registers until the block has
+// reduced its maxima.  In the D pass each row has DV/8 consecutive threads,
+// one 16-byte chunk each, so every warp load covers whole rows.
 // row_at(rr) is the storage row of the tile's row rr, d_at(rr) its index in D.
 template <int DV, int DH, class RowAt, class DAt>
 __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at, const DAt& d_at,
                                               const uint4* __restrict__ Q, const uint4* __restrict__ O,
                                               const uint4* __restrict__ O_lo, const uint4* __restrict__ dO,
-                                              float* __restrict__ D, float2* __restrict__ tm,
+                                              float* __restrict__ D, float4* __restrict__ tm,
                                               float4* __restrict__ dQacc, uint4* __restrict__ Q16,
-                                              uint4* __restrict__ dO16) {
+                                              uint4* __restrict__ dO16, unsigned int* status) {
   constexpr int kTpr = DV / 8;                 // threads per row in the D pass
   constexpr int kRows = 256 / kTpr;            // rows per pass
   constexpr int kPasses = kTileM / kRows;
-  constexpr int kBatch = 2;                    // passes whose loads are in flight together
+  constexpr int kBatch = 2;                    // passes whose O loads are in flight together
   static_assert(kPasses % kBatch == 0, "pass count");
-  __shared__ float red[2][8];
+  constexpr int kQ = kTileM * (DH / 8) / 256, kZ = kTileM * (DH / 4) / 256;
+  __shared__ float red[4][8];
   const int c = static_cast<int>(threadIdx.x) % kTpr, r0 = static_cast<int>(threadIdx.x) / kTpr;
+  // Q first: its loads stay in flight through the D pass.
+  uint4 q[kQ];
+#pragma unroll
+  for (int j = 0; j < kQ; ++j) {
+    const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
+    q[j] = rr < rows_here ? Q[row_at(rr) * (DH / 8) + k % (DH / 8)] : make_uint4(0u, 0u, 0u, 0u);
+  }
   float mn = 0.f, md = 0.f;
+  uint32_t gmax = 0u, qmax = 0u;
+  uint4 g[kPasses];
+#pragma unroll
   for (int p0 = 0; p0 < kPasses; p0 += kBatch) {
-    uint4 a[kBatch], g[kBatch], lo[kBatch];
-    int64_t at[kBatch];
+    uint4 a[kBatch], lo[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int rr = (p0 + u) * kRows + r0;
-      a[u] = g[u] = lo[u] = make_uint4(0u, 0u, 0u, 0u);
-      at[u] = 0;
+      a[u] = g[p0 + u] = lo[u] = make_uint4(0u, 0u, 0u, 0u);
       if (rr < rows_here) {
-        at[u] = row_at(rr) * (DV / 8) + c;
-        a[u] = O[at[u]];
-        g[u] = dO[at[u]];
-        if (O_lo) lo[u] = O_lo[at[u]];
+        const int64_t at = row_at(rr) * (DV / 8) + c;
+        a[u] = O[at];
+        g[p0 + u] = dO[at];
+        if (O_lo) lo[u] = O_lo[at];
       }
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int rr = (p0 + u) * kRows + r0;
-      const bool valid = rr < rows_here;
+      const uint4 gu = g[p0 + u];
       const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
-      const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
       const uint32_t lw[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
       float acc = 0.f, nrm = 0.f;
 #pragma unroll
@@ -872,15 +962,13 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
         nrm = fmaf(g0, g0, nrm);
         nrm = fmaf(g1, g1, nrm);
       }
-      if (valid)
-        dO16[at[u]] = make_uint4(bf16x2_to_f16x2(gw[0]), bf16x2_to_f16x2(gw[1]), bf16x2_to_f16x2(gw[2]),
-                                 bf16x2_to_f16x2(gw[3]));
+      gmax = bf16_absmax_fold(gmax, gu);
 #pragma unroll
       for (int off = kTpr / 2; off > 0; off >>= 1) {
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
         nrm += __shfl_xor_sync(0xffffffffu, nrm, off);
       }
-      if (valid) {
+      if (rr < rows_here) {
         if (c == 0) D[d_at(rr)] = acc;
         mn = fmaxf(mn, sqrtf(nrm));
         md = fmaxf(md, fabsf(acc));
@@ -888,31 +976,45 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
     }
   }
 #pragma unroll
-  for (int off = 16; off >= kTpr; off >>= 1) {
-    mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
+  for (int j = 0; j < kQ; ++j) qmax = bf16_absmax_fold(qmax, q[j]);
+  // Block maxima: row norms and |D| agree across a row's kTpr lanes already;
+  // the magnitude maxima differ per thread.
+  float gm = bf16_absmax_value(gmax), qm = bf16_absmax_value(qmax);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    if (off >= kTpr) {
+      mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
+    }
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, off));
+    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, off));
   }
   if ((threadIdx.x & 31) == 0) {
     red[0][threadIdx.x >> 5] = mn;
     red[1][threadIdx.x >> 5] = md;
+    red[2][threadIdx.x >> 5] = gm;
+    red[3][threadIdx.x >> 5] = qm;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float x = 0.f, y = 0.f;
-    for (int w = 0; w < 8; ++w) {
-      x = fmaxf(x, red[0][w]);
-      y = fmaxf(y, red[1][w]);
-    }
-    *tm = make_float2(x, y);
-  }
-  // Q to fp16 and the accumulator zeroed, with every thread's Q loads issued
-  // before its first store.
-  constexpr int kQ = kTileM * (DH / 8) / 256, kZ = kTileM * (DH / 4) / 256;
-  uint4 q[kQ];
+  float x = 0.f, y = 0.f;
+  gm = qm = 0.f;
 #pragma unroll
-  for (int j = 0; j < kQ; ++j) {
-    const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
-    q[j] = rr < rows_here ? Q[row_at(rr) * (DH / 8) + k % (DH / 8)] : make_uint4(0u, 0u, 0u, 0u);
+  for (int w = 0; w < 8; ++w) {
+    x = fmaxf(x, red[0][w]);
+    y = fmaxf(y, red[1][w]);
+    gm = fmaxf(gm, red[2][w]);
+    qm = fmaxf(qm, red[3][w]);
+  }
+  const int eq = f16_tile_exponent(qm), eo = f16_tile_exponent(gm);
+  if (threadIdx.x == 0) {
+    *tm = make_float4(x, y, static_cast<float>(eq), static_cast<float>(eo));
+    if (f16_saturates(qm, eq) || f16_saturates(gm, eo)) record_status(status, ATTN_ERR_RANGE);
+  }
+  const float so = exp2_int(eo == kExpZero ? 0 : eo), sq = exp2_int(eq == kExpZero ? 0 : eq);
+#pragma unroll
+  for (int p0 = 0; p0 < kPasses; ++p0) {
+    const int rr = p0 * kRows + r0;
+    if (rr < rows_here) dO16[row_at(rr) * (DV / 8) + c] = bf16x8_to_f16x8_scaled(g[p0], so);
   }
 #pragma unroll
   for (int j = 0; j < kZ; ++j) {
@@ -922,9 +1024,7 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
 #pragma unroll
   for (int j = 0; j < kQ; ++j) {
     const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
-    if (rr < rows_here)
-      Q16[row_at(rr) * (DH / 8) + k % (DH / 8)] = make_uint4(bf16x2_to_f16x2(q[j].x), bf16x2_to_f16x2(q[j].y),
-                                                             bf16x2_to_f16x2(q[j].z), bf16x2_to_f16x2(q[j].w));
+    if (rr < rows_here) Q16[row_at(rr) * (DH / 8) + k % (DH / 8)] = bf16x8_to_f16x8_scaled(q[j], sq);
   }
 }
 
@@ -934,15 +1034,16 @@ template <int DV, int DH>
 __global__ void __launch_bounds__(256)
 attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const uint4* __restrict__ O,
                            const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
-                           float2* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
-                           uint4* __restrict__ dO16) {
+                           float4* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
+                           uint4* __restrict__ dO16, unsigned int* status) {
   const int64_t bh = blockIdx.x;
   const int qt = blockIdx.y;
   const int64_t i0 = static_cast<int64_t>(qt) * kTileM;
   const int rows_here = static_cast<int>(n_q - i0 < kTileM ? n_q - i0 : kTileM);
   const int64_t row0 = bh * n_q + i0;
   const auto row_at = [row0](int rr) { return row0 + rr; };
-  bwd_prep_tile<DV, DH>(rows_here, row_at, row_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16);
+  bwd_prep_tile<DV, DH>(rows_here, row_at, row_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16,
+                        status);
 }
 
 // The same for packed sequences (token-major rows, per-sequence lengths):
@@ -965,8 +1066,9 @@ template <int DV, int DH>
 __global__ void __launch_bounds__(256)
 attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt, const uint4* __restrict__ Q,
                                   const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
-                                  const uint4* __restrict__ dO, float* __restrict__ D, float2* __restrict__ tilemax,
-                                  float4* __restrict__ dQacc, uint4* __restrict__ Q16, uint4* __restrict__ dO16) {
+                                  const uint4* __restrict__ dO, float* __restrict__ D, float4* __restrict__ tilemax,
+                                  float4* __restrict__ dQacc, uint4* __restrict__ Q16, uint4* __restrict__ dO16,
+                                  unsigned int* status) {
   const int64_t bh = blockIdx.x;
   const int b = static_cast<int>(bh / rm.Hq);
   const int h = static_cast<int>(bh - static_cast<int64_t>(b) * rm.Hq);
@@ -976,7 +1078,101 @@ attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt
   const int rows_here = static_cast<int>(left < kTileM ? (left < 0 ? 0 : left) : kTileM);
   const auto row_at = [&rm, b, h, i0](int rr) { return rm.row(b, h, i0 + rr); };
   const auto d_at = [&rm, b, h, i0](int rr) { return rm.vec(b, h, i0 + rr); };
-  bwd_prep_tile<DV, DH>(rows_here, row_at, d_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16);
+  bwd_prep_tile<DV, DH>(rows_here, row_at, d_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16,
+                        status);
+}
+
+// Every query tile of a (batch, KV head) group brought to one exponent for
+// its fp16 Q and one for its fp16 dO, the smallest among the group's tiles
+// that hold a non-zero entry (f16range.cuh), so that the main kernel's loop
+// over the group's steps needs no scale of its own per step.  A tile whose
+// own exponent is larger is rescaled in place by the exact power of two
+// 2^(e_group - e_tile) < 1: its largest entry lies that many binades below
+// the group's largest, and its entries keep full precision down to about
+// 2^-28 of the group's largest entry.  The group's exponents go to grpexp
+// (0 for a group without any non-zero entry); the tile records are only
+// read.  One block per query tile: it reduces its group's records (a few
+// hundred bytes from L2) and rescales its own tile if it has to, which
+// tiles of similar scale (one exponent, f16range.cuh) never need.
+struct GroupExpParams {
+  int32_t Hq, Hkv, group, n_q, nqt, packed;
+  int32_t cu_q[ATTN_MAX_BATCH + 1];   // packed: first query token of sequence b
+  const float4* tilemax;              // [B Hq][nqt]: (.., .., e_Q, e_dO) per tile
+  float2* grpexp;                     // [B Hkv]: the group's (e_Q, e_dO)
+  uint4* Q16;
+  uint4* dO16;
+};
+
+__device__ __forceinline__ uint4 f16x8_scaled(uint4 u, float sc) {
+  return make_uint4(pack_f16x2(f16_lo(u.x) * sc, f16_hi(u.x) * sc), pack_f16x2(f16_lo(u.y) * sc, f16_hi(u.y) * sc),
+                    pack_f16x2(f16_lo(u.z) * sc, f16_hi(u.z) * sc), pack_f16x2(f16_lo(u.w) * sc, f16_hi(u.w) * sc));
+}
+
+// grid (B Hkv, up to group nqt): block (bk, y) takes the tiles idx = y,
+// y + gridDim.y, ... of its group, idx naming head hk group + idx / nt and
+// query tile idx % nt (nt = the sequence's query tiles).
+template <int DH, int DV>
+__global__ void __launch_bounds__(256) attn_bwd_group_exp_kernel(const __grid_constant__ GroupExpParams p) {
+  const int b = static_cast<int>(blockIdx.x) / p.Hkv;
+  const int hk = static_cast<int>(blockIdx.x) - b * p.Hkv;
+  const int64_t nq_b = p.packed ? static_cast<int64_t>(p.cu_q[b + 1]) - p.cu_q[b] : p.n_q;
+  const int nt = static_cast<int>((nq_b + kTileM - 1) / kTileM);
+  const int items = p.group * nt;
+  if (static_cast<int>(blockIdx.y) >= items) return;   // past the sequence (packed): no tile
+  auto rec_of = [&](int idx) -> const float4* {
+    return p.tilemax + static_cast<int64_t>(b * p.Hq + hk * p.group + idx / nt) * p.nqt + idx % nt;
+  };
+  int qmin = kExpZero, omin = kExpZero;
+  for (int idx = static_cast<int>(threadIdx.x); idx < items; idx += 256) {
+    const float2 e = reinterpret_cast<const float2*>(rec_of(idx))[1];
+    const int q = static_cast<int>(e.x), o = static_cast<int>(e.y);
+    if (q != kExpZero) qmin = min(qmin, q);
+    if (o != kExpZero) omin = min(omin, o);
+  }
+  __shared__ int red[2][8];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    qmin = min(qmin, __shfl_xor_sync(0xffffffffu, qmin, off));
+    omin = min(omin, __shfl_xor_sync(0xffffffffu, omin, off));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = qmin;
+    red[1][threadIdx.x >> 5] = omin;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    qmin = min(qmin, red[0][w]);
+    omin = min(omin, red[1][w]);
+  }
+  const int qg = qmin == kExpZero ? 0 : qmin, og = omin == kExpZero ? 0 : omin;
+  if (blockIdx.y == 0 && threadIdx.x == 0)
+    p.grpexp[blockIdx.x] = make_float2(static_cast<float>(qg), static_cast<float>(og));
+  for (int self = static_cast<int>(blockIdx.y); self < items; self += static_cast<int>(gridDim.y)) {
+  const float2 e = reinterpret_cast<const float2*>(rec_of(self))[1];
+  const int q = static_cast<int>(e.x), o = static_cast<int>(e.y);
+  const int r = hk * p.group + self / nt;
+  const int64_t i0 = static_cast<int64_t>(self % nt) * kTileM;
+  const int rows = static_cast<int>(nq_b - i0 < kTileM ? nq_b - i0 : kTileM);
+  auto row_at = [&](int rr) -> int64_t {
+    return p.packed ? (static_cast<int64_t>(p.cu_q[b]) + i0 + rr) * p.Hq + r
+                    : (static_cast<int64_t>(b) * p.Hq + r) * p.n_q + i0 + rr;
+  };
+  if (q != kExpZero && q != qg) {
+    const float sc = exp2_int(qg - q);
+    for (int k = static_cast<int>(threadIdx.x); k < rows * (DH / 8); k += 256) {
+      uint4* at = p.Q16 + row_at(k / (DH / 8)) * (DH / 8) + k % (DH / 8);
+      *at = f16x8_scaled(*at, sc);
+    }
+  }
+  if (o != kExpZero && o != og) {
+    const float sc = exp2_int(og - o);
+    for (int k = static_cast<int>(threadIdx.x); k < rows * (DV / 8); k += 256) {
+      uint4* at = p.dO16 + row_at(k / (DV / 8)) * (DV / 8) + k % (DV / 8);
+      *at = f16x8_scaled(*at, sc);
+    }
+  }
+  }
 }
 
 // dQ = scale * acc, eight elements per thread per iteration.
@@ -1012,10 +1208,9 @@ int grid_for(int64_t work_threads) {
 }
 
 template <int DV, int DH>
-void launch_pre_t(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay, int nqt, const void* Q,
-                  const void* O, const void* O_lo, const void* dO, float* D, float2* tilemax, float* dQacc,
-                  void* Q16, void* dO16, cudaStream_t stream) {
-  (void)mask;
+void launch_pre_t(const ShapeParams& sh, const LayoutParams& lay, int nqt, const void* Q, const void* O,
+                  const void* O_lo, const void* dO, float* D, float4* tilemax, float* dQacc, void* Q16, void* dO16,
+                  unsigned int* status, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(sh.B) * sh.Hq), static_cast<unsigned>(nqt));
   const uint4 *q = static_cast<const uint4*>(Q), *o = static_cast<const uint4*>(O);
   const uint4 *olo = static_cast<const uint4*>(O_lo), *g = static_cast<const uint4*>(dO);
@@ -1024,7 +1219,7 @@ void launch_pre_t(const ShapeParams& sh, const MaskParams& mask, const LayoutPar
   uint4* do16 = static_cast<uint4*>(dO16);
   if (!lay.packed) {
     attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, q, o, olo, g, D, tilemax, acc, q16,
-                                                                  do16);
+                                                                  do16, status);
   } else {
     PrepPacked rm;
     rm.n_q = sh.n_q;
@@ -1032,7 +1227,7 @@ void launch_pre_t(const ShapeParams& sh, const MaskParams& mask, const LayoutPar
     rm.total_q = lay.total_q;
     for (int b = 0; b <= sh.B; ++b) rm.cu_q[b] = lay.cu_q[b];
     attn_bwd_preprocess_packed_kernel<DV, DH><<<grid, 256, 0, stream>>>(rm, nqt, q, o, olo, g, D, tilemax, acc,
-                                                                        q16, do16);
+                                                                        q16, do16, status);
   }
 }
 
@@ -1047,19 +1242,37 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay,
-                                       int dv, int dh, const void* Q, const void* O, const void* O_lo,
-                                       const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
-                                       void* dO16, cudaStream_t stream) {
+cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams& lay, int dv, int dh,
+                                       const void* Q, const void* O, const void* O_lo, const void* dO, float* D,
+                                       float4* tilemax, float2* grpexp, float* dQacc, void* Q16, void* dO16,
+                                       unsigned int* status, cudaStream_t stream) {
   const int nqt = (sh.n_q + kTileM - 1) / kTileM;
-  if (dv == 128 && dh == 128)
-    launch_pre_t<128, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, stream);
-  else if (dv == 64 && dh == 64)
-    launch_pre_t<64, 64>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, stream);
-  else if (dv == 64 && dh == 128)
-    launch_pre_t<64, 128>(sh, mask, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, stream);
-  else
+  GroupExpParams g;
+  g.Hq = sh.Hq;
+  g.Hkv = sh.Hkv;
+  g.group = sh.group;
+  g.n_q = sh.n_q;
+  g.nqt = nqt;
+  g.packed = lay.packed;
+  for (int b = 0; b <= sh.B; ++b) g.cu_q[b] = lay.packed ? lay.cu_q[b] : 0;
+  g.tilemax = tilemax;
+  g.grpexp = grpexp;
+  g.Q16 = static_cast<uint4*>(Q16);
+  g.dO16 = static_cast<uint4*>(dO16);
+  const int64_t gy = static_cast<int64_t>(sh.group) * nqt;
+  const dim3 ggrid(static_cast<unsigned>(sh.B * sh.Hkv), static_cast<unsigned>(gy < 65535 ? gy : 65535));
+  if (dv == 128 && dh == 128) {
+    launch_pre_t<128, 128>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, status, stream);
+    attn_bwd_group_exp_kernel<128, 128><<<ggrid, 256, 0, stream>>>(g);
+  } else if (dv == 64 && dh == 64) {
+    launch_pre_t<64, 64>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, status, stream);
+    attn_bwd_group_exp_kernel<64, 64><<<ggrid, 256, 0, stream>>>(g);
+  } else if (dv == 64 && dh == 128) {
+    launch_pre_t<64, 128>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, status, stream);
+    attn_bwd_group_exp_kernel<128, 64><<<ggrid, 256, 0, stream>>>(g);
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

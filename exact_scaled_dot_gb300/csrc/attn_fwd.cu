@@ -17,10 +17,18 @@
 //   warp 1      MMA issuer (converged; one elected lane issues): S_t = Q_t K_j^T
 //               into tensor memory, O_t += P_t V_j with P_t read back from
 //               tensor memory.
-//   warps 2, 3  re-encode every V tile as fp16 in place once it has landed,
-//               zeroing its padded key rows (rows in [kv_len, n_k)).
+//   warps 2, 3  idle.
 //   warps 4-7   softmax for query tile 0 (thread = row = TMEM lane).
 //   warps 8-11  softmax for query tile 1.
+// V arrives as fp16 from a pre-pass (attn_v16_kernel): every 128-key tile j
+// scaled by its own power of two 2^v_j (f16range.cuh), padded key rows
+// zeroed.  The softmax writes the weights of tile j as P 2^(E - v_j) with
+// one reference E per query tile, so every PV product adds 2^E P V into
+// the accumulator and the epilogue divides 2^E out with the row sum.  The
+// weights are at most 2^8 (the lazy maximum below), so E may lie up to 7
+// above the smallest v_j without overflowing fp16: E = min(vmin + 7, vmax)
+// over the tiles the query tile sees, which keeps the weights of tiles with
+// up to 2^7 smaller values at full precision.
 // While one tile's softmax runs, the tensor core works on the other tile.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
@@ -40,8 +48,9 @@
 // tolerance).  Summing the rounded weights as well would remove it, at three
 // more instructions per pair of weights in the hot loop.
 //
-// The PV product runs in fp16 (weights P and V both re-encoded; V exactly
-// for |v| <= 65504, P <= 2^8 by the lazy maximum): the backward rebuilds the
+// The PV product runs in fp16 (weights P and V both re-encoded; V exactly at
+// any scale through its tile exponent, P <= 2^8 by the lazy maximum): the
+// backward rebuilds the
 // weights exactly and takes its row term from this O (c_i = sum_l dO_il O_il,
 // eq. A.10.7), so O must be the product of nearly exact weights.  With bf16
 // weights (8 significant bits) the two differ by about 2^-9 of
@@ -52,6 +61,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "f16range.cuh"
 #include "ptx.cuh"
 
 namespace esd {
@@ -61,9 +71,6 @@ template <int DH, int DV>
 struct FwdCfg {
   static constexpr int kQTiles = 2;
   static constexpr int kKStages = (DH == 128) ? 2 : 3;
-  // Three V stages at every width: a V tile then lands a period earlier,
-  // and its fp16 re-encoding (slow: its shared-memory reads wait behind the
-  // QK products' operand reads) is finished before its PV product is due.
   static constexpr int kVStages = 3;
   static constexpr int kQTileBytes = kTileM * DH * 2;
   static constexpr int kKTileBytes = kTileN * DH * 2;
@@ -79,8 +86,7 @@ struct FwdCfg {
   static constexpr int kBarKEmpty = kBarKFull + kKStages;
   static constexpr int kBarVFull = kBarKEmpty + kKStages;
   static constexpr int kBarVEmpty = kBarVFull + kVStages;
-  static constexpr int kBarVReady = kBarVEmpty + kVStages;   // [kVStages] V tile re-encoded as fp16
-  static constexpr int kBarSFull = kBarVReady + kVStages;    // [2]
+  static constexpr int kBarSFull = kBarVEmpty + kVStages;    // [2]
   static constexpr int kBarPReady = kBarSFull + 2;          // [2]
   static constexpr int kBarOFull = kBarPReady + 2;          // [2]
   static constexpr int kBarDrain = kBarOFull + 2;
@@ -118,9 +124,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int b = bh / p.sh.Hq;
   const int r = bh - b * p.sh.Hq;
   const int hkv = r / p.sh.group;                   // g(r) = r / (Hq / Hkv)
-  // Key rows past the sequence: up to n_k in the padded layout; in the packed
-  // layout every row of a tile past kv_len belongs to another sequence.
-  const int row_end = PACKED ? INT32_MAX : p.sh.n_k;
   const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy first
   int q0[2], ntiles[2];
 #pragma unroll
@@ -141,7 +144,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarVEmpty + s), 1);
     }
-    for (int s = 0; s < C::kVStages; ++s) mbar_init(bar(C::kBarVReady + s), 2);   // warps 2 and 3
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
       mbar_init(bar(C::kBarPReady + t), 128);
@@ -149,7 +151,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
-    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
+    *abort_flag = status_blocks(p.status) ? 2 : 0;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -198,9 +200,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = mbar_wait(bar(C::kBarVEmpty + vs), vph ^ 1u, abort_flag, limit);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kVTileBytes);
+        // V16 is [B Hkv][nkt 128][DV] in both layouts.
         for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(sbase + C::kOffV + vs * C::kVTileBytes + c * C::kBlockBytes, &tmV,
-                      bar(C::kBarVFull + vs), c * 64, kyz.y, kyz.z);
+                      bar(C::kBarVFull + vs), c * 64, j * kTileN, b * p.sh.Hkv + hkv);
         ++v_issued[vs];
       }
       if (*abort_flag) {
@@ -212,37 +215,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int s = 0; s < C::kVStages; ++s)
           if (v_issued[s]) mbar_wait(bar(C::kBarVFull + s), (v_issued[s] - 1) & 1, &no_abort, limit);
       }
-    }
-  } else if (warp == 2 || warp == 3) {
-    // =================== V tiles to fp16 (in place) ===================
-    // Every V tile, in order: the next load into a stage waits for the PV
-    // product that follows this conversion, so the full barrier cannot run a
-    // phase ahead of these warps.  Key rows in [kv_len, n_k) hold caller
-    // memory that may be anything (even NaN): their weights are exactly 0,
-    // but 0 * NaN would still poison O, so they become zeros.  Rows at or
-    // beyond n_k arrive as zeros from the TMA bounds check.
-    const int t64 = static_cast<int>(threadIdx.x) - 64;   // 0..63
-    bool ok = *abort_flag == 0;
-    for (int j = 0; j < nkv && ok; ++j) {
-      const int vs = j % C::kVStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVFull + vs), static_cast<uint32_t>((j / C::kVStages) & 1),
-                                             abort_flag, limit));
-      if (!ok) break;
-      int r0 = kTileN, r1 = kTileN;
-      padded_rows(p.mask, row_end, b, j, r0, r1);
-      uint4* vt = reinterpret_cast<uint4*>(smem + C::kOffV + vs * C::kVTileBytes);
-#pragma unroll 4
-      for (int q = t64; q < C::kVTileBytes / 16; q += 64) {
-        const int row = (q % (C::kBlockBytes / 16)) / 8;   // 8 chunks of 16 bytes per 128-byte row
-        const uint4 u = vt[q];
-        vt[q] = (row >= r0 && row < r1)
-                    ? make_uint4(0u, 0u, 0u, 0u)
-                    : make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z),
-                                 bf16x2_to_f16x2(u.w));
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kBarVReady + vs));
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
@@ -292,7 +264,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       for (int j = 0; j < nkv && ok; ++j) {
         const int vs = j % C::kVStages;
-        ok = wait1(C::kBarVReady + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
+        ok = wait1(C::kBarVFull + vs, static_cast<uint32_t>((j / C::kVStages) & 1));
         if (!ok) break;
         const int kn = (j + 1) % C::kKStages;
         bool k_next_ready = false;
@@ -341,7 +313,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     float l_sum = 0.f;         // sum of the weights p
     bool ok = *abort_flag == 0;
     uint32_t rr[32];
+    // The reference E of this query tile's V exponents (all-zero tiles left
+    // out), and each tile's offset E - v_j <= 7 for its weights.
+    const int* vexp = p.vexp + static_cast<int64_t>(b * p.sh.Hkv + hkv) * p.nkt;
+    int vmin = kExpZero, vmax = -kExpZero;
+    for (int jt = static_cast<int>(lane); jt < ntiles[t]; jt += 32) {
+      const int e = vexp[jt];
+      if (e != kExpZero) {
+        vmin = min(vmin, e);
+        vmax = max(vmax, e);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, off));
+      vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+    }
+    const int vref = vmin == kExpZero ? 0 : min(vmin + 7, vmax);
+    int v_next = ntiles[t] > 0 ? vexp[0] : 0;
     for (int j = 0; j < ntiles[t] && ok; ++j) {
+      const int v_j = v_next;
+      if (j + 1 < ntiles[t]) v_next = vexp[j + 1];
+      const int voff = v_j == kExpZero ? 0 : vref - v_j;
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::kBarSFull + t), static_cast<uint32_t>(j & 1), abort_flag, limit));
       if (!ok) break;
@@ -394,10 +387,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
       }
-      const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const float nm = ((m_ref == -INFINITY) ? 0.f : -m_ref) + static_cast<float>(voff);
 
-      // P = exp2(S scale log2e - m_ref) -> fp16 pairs into tensor memory
-      // (over the first 64 columns of S, all of which are in registers).
+      // P' = exp2(S scale log2e - m_ref + E - v_j) -> fp16 pairs into
+      // tensor memory (over the first 64 columns of S, all of which are in
+      // registers); the row sum takes P = P' 2^(v_j - vmin).
       float ls[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -413,7 +407,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         tmem_st16_nowait(tS + c * 16, pw);
       }
-      l_sum += (ls[0][0] + ls[0][1]) + (ls[1][0] + ls[1][1]);
+      l_sum += ((ls[0][0] + ls[0][1]) + (ls[1][0] + ls[1][1])) * exp2_int(-voff);
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarPReady + t));
@@ -424,7 +418,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull + t), 0, abort_flag, limit));
       tc_fence_after_sync();
       if (ok) {
-        const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+        // O = 2^-E acc / l (the weights of tile j were scaled by 2^(E - v_j)).
+        const float inv_l = l_sum > 0.f ? exp2_int(-vref) / l_sum : 0.f;
         const bool in_range = i < query_len(p.mask, p.sh.n_q, b);
         const int64_t row_off = q_row(PACKED, p.lay, p.sh.Hq, p.sh.n_q, b, r, i) * DV;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + row_off);
@@ -463,7 +458,57 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+  if (threadIdx.x == 0 && *abort_flag == 1) record_status(p.status, ATTN_ERR_TIMEOUT);
+}
+
+// V for the forward's P V product: every 128-key tile of (b, h) re-encoded
+// as fp16 x 2^e, e from the tile's largest magnitude (f16range.cuh), rows
+// past the key length zero, and e recorded in vexp.  One block per tile;
+// the whole tile stays in registers while the block agrees on e.  Tiles that
+// start past the key length are never read by the forward and are skipped.
+template <int DV, bool PACKED>
+__global__ void __launch_bounds__(256) attn_v16_kernel(const __grid_constant__ V16Params p) {
+  constexpr int kCpr = DV / 8;                    // 16-byte chunks per row
+  constexpr int kChunks = kTileN * kCpr / 256;    // per thread
+  const int bh = blockIdx.x;
+  const int b = bh / p.sh.Hkv;
+  const int h = bh - b * p.sh.Hkv;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.y) * kTileN;
+  const int64_t klen = key_len(p.mask, p.sh.n_k, b);
+  if (j0 >= klen) return;
+  __shared__ float red[8];
+  const uint4* V = static_cast<const uint4*>(p.V);
+  uint4 v[kChunks];
+  uint32_t m = 0u;
+#pragma unroll
+  for (int i = 0; i < kChunks; ++i) {
+    const int k = static_cast<int>(threadIdx.x) + 256 * i;
+    const int64_t jr = j0 + k / kCpr;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (jr < klen) {
+      v[i] = V[k_row(PACKED, p.lay, p.sh.Hkv, p.sh.n_k, b, h, jr) * kCpr + k % kCpr];
+      m = bf16_absmax_fold(m, v[i]);
+    }
+  }
+  float mx = bf16_absmax_value(m);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mx = fmaxf(mx, red[w]);
+  const int e = f16_tile_exponent(mx);
+  const float sc = exp2_int(e == kExpZero ? 0 : e);
+  uint4* dst = static_cast<uint4*>(p.V16) + (static_cast<int64_t>(bh) * p.nkt * kTileN + j0) * kCpr;
+#pragma unroll
+  for (int i = 0; i < kChunks; ++i) {
+    const int k = static_cast<int>(threadIdx.x) + 256 * i;
+    dst[k] = (j0 + k / kCpr < klen) ? bf16x8_to_f16x8_scaled(v[i], sc) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (threadIdx.x == 0) {
+    p.vexp[static_cast<int64_t>(bh) * p.nkt + blockIdx.y] = e;
+    if (f16_saturates(mx, e)) record_status(p.status, ATTN_ERR_RANGE);
+  }
 }
 
 template <int DH, int DV>
@@ -480,6 +525,20 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
 }
 
 }  // namespace
+
+cudaError_t launch_attn_v16(int dv, const V16Params& p, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>(p.nkt));
+  if (dv == 128) {
+    if (p.lay.packed) attn_v16_kernel<128, true><<<grid, 256, 0, stream>>>(p);
+    else attn_v16_kernel<128, false><<<grid, 256, 0, stream>>>(p);
+  } else if (dv == 64) {
+    if (p.lay.packed) attn_v16_kernel<64, true><<<grid, 256, 0, stream>>>(p);
+    else attn_v16_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream) {

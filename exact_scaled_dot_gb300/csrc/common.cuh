@@ -157,7 +157,23 @@ struct FwdParams {
   void* O;                     // bf16 [B][Hq][n_q][d_v]
   void* O_lo;                  // bf16 rounding residual of O, or nullptr
   float* LSE;                  // fp32 [B][Hq][n_q]
+  const int32_t* vexp;         // [B Hkv][nkt] exponents of the fp16 V tiles (attn_v16_kernel)
+  int32_t nkt;                 // key tiles per head of the fp16 V buffer
   unsigned int* status;        // device status word
+};
+
+// The forward's fp16 copy of V: tile j of (b, h) re-encoded as V 2^vexp
+// (f16range.cuh), rows past the key length zero, in a [B Hkv][nkt 128][d_v]
+// buffer in both layouts.
+struct V16Params {
+  ShapeParams sh;
+  MaskParams mask;
+  LayoutParams lay;
+  int32_t nkt;
+  const void* V;               // bf16, the caller's layout
+  void* V16;                   // fp16 [B Hkv][nkt 128][d_v]
+  int32_t* vexp;               // [B Hkv][nkt]; tiles past the key length are not written
+  unsigned int* status;
 };
 
 struct BwdParams {
@@ -169,8 +185,9 @@ struct BwdParams {
   uint64_t wait_limit_ns;
   const float* LSE;            // fp32 [B][Hq][n_q]
   const float* D;              // fp32 [B][Hq][n_q]
-  const float2* tilemax;       // per 128-row query tile: (max ||dO_i||, max |D_i|), [B Hq][nqt]
+  const float4* tilemax;       // per 128-row query tile: (max ||dO_i||, max |D_i|, e_Q, e_dO), [B Hq][nqt]
   int32_t nqt;                 // query tiles per head (of the longest sequence)
+  const float2* grpexp;        // [B Hkv]: the exponents of the group's fp16 Q and dO tiles
   float* dQacc;                // fp32 [B][Hq][n_q][d_h]
   void* dK;                    // bf16 [B][Hkv][n_k][d_h]
   void* dV;                    // bf16 [B][Hkv][n_k][d_v]
@@ -219,15 +236,16 @@ constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 // Kernel launchers (defined next to their kernels).
 cudaError_t launch_attn_fwd(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_attn_v16(int dv, const V16Params& p, cudaStream_t stream);
 cudaError_t launch_attn_decode(int dh, int dv, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecParams& p,
                                cudaStream_t stream);
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const MaskParams& mask, const LayoutParams& lay,
-                                       int dv, int dh, const void* Q, const void* O, const void* O_lo,
-                                       const void* dO, float* D, float2* tilemax, float* dQacc, void* Q16,
-                                       void* dO16, cudaStream_t stream);
+cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams& lay, int dv, int dh,
+                                       const void* Q, const void* O, const void* O_lo, const void* dO, float* D,
+                                       float4* tilemax, float2* grpexp, float* dQacc, void* Q16, void* dO16,
+                                       unsigned int* status, cudaStream_t stream);
 cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap* tB, const GemmParams& p,
                              cudaStream_t stream);
 // heads_b = 0: one tensor (xb, yb unused).

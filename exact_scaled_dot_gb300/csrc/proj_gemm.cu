@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "f16range.cuh"
 #include "ptx.cuh"
 
 namespace esd {
@@ -81,7 +82,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant_
     mbar_init(bar(C::kBarAcc), 1);
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
-    *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.status) != 0u) ? 2 : 0;
+    *abort_flag = status_blocks(p.status) ? 2 : 0;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -222,7 +223,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant_
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (threadIdx.x == 0 && *abort_flag == 1) atomicCAS(p.status, 0u, static_cast<unsigned int>(ATTN_ERR_TIMEOUT));
+  if (threadIdx.x == 0 && *abort_flag == 1) record_status(p.status, ATTN_ERR_TIMEOUT);
 }
 
 template <bool AMN, bool BMN, bool OUTF32>

@@ -74,10 +74,19 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
-// A packed bf16x2 word re-encoded as f16x2 (exact for |x| in the normal
-// half range, saturating above it).
+// A packed bf16x2 word re-encoded as f16x2 (exact for 2^-17 <= |x| <= 65504,
+// saturating above; f16range.cuh scales operands into that range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(bf16_lo(w), bf16_hi(w));
+}
+
+// The same for x s, s an exact power of two (the fp16 operand x 2^e).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
+  return pack_f16x2(bf16_lo(w) * s, bf16_hi(w) * s);
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 u, float s) {
+  return make_uint4(bf16x2_to_f16x2_scaled(u.x, s), bf16x2_to_f16x2_scaled(u.y, s),
+                    bf16x2_to_f16x2_scaled(u.z, s), bf16x2_to_f16x2_scaled(u.w, s));
 }
 
 // Paired fp32 arithmetic (one instruction for two lanes of work, each

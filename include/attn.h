@@ -38,7 +38,8 @@
  * Every tensor pointer must be 16-byte aligned.
  *
  * Ownership and execution.  The caller allocates and owns every buffer,
- * including the backward workspace; the library allocates no device memory
+ * including the forward and backward workspaces; the library allocates no
+ * device memory
  * and keeps no state between calls other than a cached driver entry point.
  * Device pointers refer to memory of the current CUDA device.  `stream` is a
  * cudaStream_t (NULL = the legacy default stream); every call only enqueues
@@ -47,10 +48,26 @@
  *
  * Errors.  Every function returns ATTN_OK (0) or one of the codes below; no
  * exception or abort crosses the ABI.  Argument checks happen before any
- * CUDA call.  Device-side failures (a bounded wait that ran out) are recorded
- * in a device status word: attn_get_status() reads it; while it is set, the
- * kernels return immediately without writing outputs, until
- * attn_clear_status() resets it.
+ * CUDA call.  Device-side conditions are recorded in a device status word
+ * that attn_get_status() reads and attn_clear_status() resets:
+ * ATTN_ERR_TIMEOUT (a bounded wait ran out; while it is set, the kernels
+ * return immediately without writing outputs) or ATTN_ERR_RANGE (an input
+ * tile was too large for the fp16 operands, below; the outputs of that call
+ * are not to be trusted, later calls run normally).
+ *
+ * Precision.  Inputs and outputs are bf16 with fp32 accumulation.  Q K^T in
+ * the forward runs on bf16 operands; P V and every backward product run on
+ * fp16 operands (11 significant bits, so that the weights and dS keep more
+ * precision than bf16 gives them).  Each fp16 operand is the bf16 input
+ * times a power of two 2^e chosen from the largest magnitude M it holds, so
+ * that 2^11 <= M 2^e < 2^15 (e a multiple of 4), and the products are
+ * unscaled exactly.  The unit that shares one e is a 128-key tile of V in
+ * the forward, a 128-key tile of K and of V in the backward, and all query
+ * rows of Q (and of dO) that share a KV head in the backward.  The
+ * re-encoding is therefore exact at any input scale: every value down to
+ * about 2^-28 M is kept, for any M below 2^46; a tile with M >= 2^46
+ * saturates and sets ATTN_ERR_RANGE.  (e is clamped to [-30, 30]: a unit
+ * whose M is below 2^-16 still keeps every value down to 2^-47.)
  */
 #ifndef EXACT_SCALED_DOT_GB300_ATTN_H
 #define EXACT_SCALED_DOT_GB300_ATTN_H
@@ -62,7 +79,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 8
+#define ATTN_ABI_VERSION 9
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -78,6 +95,8 @@ extern "C" {
 #define ATTN_ERR_CUDA         8  /* a CUDA runtime/driver call or launch failed        */
 #define ATTN_ERR_TIMEOUT      9  /* a kernel's bounded wait ran out (device status)    */
 #define ATTN_ERR_DEVICE      10  /* the current device is not an sm_103 GPU            */
+#define ATTN_ERR_RANGE       11  /* an input tile held a magnitude of 2^46 or more,    */
+                                 /* beyond the scaled fp16 operands (device status)    */
 
 /* Largest batch whose per-batch key lengths travel with the launch. */
 #define ATTN_MAX_BATCH 512
@@ -103,19 +122,31 @@ typedef struct {
   const int32_t* kv_len;   /* NULL (= n_k for all) or HOST array [B], each in [1,n_k] */
 } attn_mask;
 
+/* Bytes of device workspace attn_fwd needs: an fp16 copy of V in 128-key
+ * tiles with one exponent per tile, about B*Hkv*ceil(n_k/128)*128*(2*d_v)
+ * bytes.  The layout is private to the library.  Returns 0 for an invalid
+ * shape. */
+size_t attn_fwd_workspace_bytes(const attn_shape* shape);
+
 /* Forward pass (A.10.1-A.10.3).  Inputs Q, K, V (bf16, device); outputs
  * O (bf16) and LSE (fp32, natural log), both device, fully overwritten.
+ * `workspace`: caller-owned device memory of at least
+ * attn_fwd_workspace_bytes(shape) bytes, 256-byte aligned (ATTN_ERR_WORKSPACE
+ * otherwise); its contents on entry do not matter.  Two launches on
+ * `stream`: V re-encoded into the workspace, then the forward kernel.
  *
- * O_lo (optional, NULL to skip): bf16 [B][Hq][n_q][d_v] receiving the
- * rounding residual of O, so that O + O_lo carries the fp32 result to about
- * 16 significant bits.  The backward's row term c_i = sum_l dO_il O_il
- * (A.10.7) feeds dQ_i with weight -scale * sum_j A_ij k_j, which for a
- * sharply peaked softmax row is a whole key row; bf16 rounding of O alone
- * then moves dQ and dK by a few 1e-2.  Passing O_lo on to the backward
- * removes that error. */
+ * O_lo (optional here, NULL to skip; required by the backward): bf16
+ * [B][Hq][n_q][d_v] receiving the rounding residual of O, so that O + O_lo
+ * carries the fp32 result to about 16 significant bits.  The backward's row
+ * term c_i = sum_l dO_il O_il (A.10.7) feeds dQ_i with weight
+ * -scale * sum_j A_ij k_j, which for a sharply peaked softmax row is a whole
+ * key row; bf16 rounding of O alone then moves dQ and dK beyond the stated
+ * tolerance (measured: up to 2.2x on the peaked cross-attention workload,
+ * 4x on smaller peaked cases). */
 int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
-             void* O, float* LSE, void* O_lo, void* stream);
+             void* O, float* LSE, void* O_lo,
+             void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward for short query blocks over a long key cache (decode, small
  * chunks of new queries: the new-queries-over-a-history shape of "Chapter
@@ -141,11 +172,12 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
  * The layout is private to the library.  Returns 0 for an invalid shape. */
 size_t attn_bwd_workspace_bytes(const attn_shape* shape);
 
-/* Backward pass (A.10.5-A.10.9).  Q, K, V, O, LSE must be those of the
- * forward call with the same mask and scale ("Chapter 31", section 3: the
- * backward must use the forward's semantics); O_lo is the forward's residual
- * output or NULL (then D is computed from the bf16 O alone).  dO is the
- * upstream gradient.
+/* Backward pass (A.10.5-A.10.9).  Q, K, V, O, O_lo, LSE must be those of
+ * the forward call with the same mask and scale ("Chapter 31", section 3:
+ * the backward must use the forward's semantics).  O_lo, the forward's
+ * rounding residual of O, is required (ATTN_ERR_NULL when NULL): the row
+ * terms c_i are formed from O + O_lo (see attn_fwd).  dO is the upstream
+ * gradient.
  * Outputs dQ, dK, dV (bf16, device) are fully overwritten; dK and dV hold the
  * sums over each KV head's query heads.  `workspace` is caller-owned device
  * memory of at least attn_bwd_workspace_bytes(shape) bytes, 256-byte aligned;
@@ -153,9 +185,10 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * below, in order, on the same workspace.
  *
  * Precision: every product runs in fp16 with fp32 accumulation: Q, K, V
- * and dO are re-encoded as fp16 (exact for |x| <= 65504; larger entries
- * saturate), the weights A are rounded once to fp16, and dS enters dK and
- * dQ in fp16 scaled by a power of two derived from a bound on |dS|. */
+ * and dO are re-encoded as fp16 tile by tile with their own powers of two
+ * (exact at any scale, see Precision above), the weights A are rounded once
+ * to fp16, and dS enters dK and dQ in fp16 scaled by a power of two derived
+ * from a bound on |dS|. */
 int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              const void* Q, const void* K, const void* V,
              const void* O, const void* O_lo, const void* dO, const float* LSE,
@@ -163,10 +196,10 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Stage 1 of the backward: D_i = sum_l dO_il (O_il + O_lo_il) (= c_i of
- * A.10.7; O_lo may be NULL), per-tile bounds max ||dO_i|| and max |D_i|, a
- * zeroed dQ accumulator and Q and dO re-encoded as fp16 (see attn_bwd), all
- * in `workspace`.  Q is the forward's bf16 query tensor, dO the bf16
- * upstream gradient. */
+ * A.10.7; O_lo required), per-tile bounds max ||dO_i|| and max |D_i|, a
+ * zeroed dQ accumulator and Q and dO re-encoded as fp16 with per-tile
+ * exponents (see attn_bwd), all in `workspace`.  Q is the forward's bf16
+ * query tensor, dO the bf16 upstream gradient. */
 int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O,
                         const void* O_lo, const void* dO, void* workspace,
                         size_t workspace_bytes, void* stream);
@@ -248,8 +281,13 @@ typedef struct {
  * the description is invalid. */
 int64_t attn_varlen_visible_pairs(const attn_varlen* v);
 
+/* Workspace of attn_fwd_varlen, about B*Hkv*ceil(max len_k/128)*128*(2*d_v)
+ * bytes (the fp16 V tiles are laid out per sequence); 0 when the
+ * description is invalid. */
+size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v);
+
 int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
-                    void* O, float* LSE, void* O_lo, void* stream);
+                    void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace of attn_bwd_varlen, about T_q*Hq*(6*d_h + 2*d_v + 4) bytes; 0 when the
  * description is invalid. */

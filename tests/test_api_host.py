@@ -34,7 +34,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 8
+    assert esd.attn_abi_version() == 9
 
 
 def test_strerror_covers_every_code(lib):
@@ -44,11 +44,12 @@ def test_strerror_covers_every_code(lib):
     assert lib.attn_strerror(999).decode() == "unknown status"
 
 
-def _call_fwd(lib, shape, mask, scale=None, ptr=256):
+def _call_fwd(lib, shape, mask, scale=None, ptr=256, ws=256, ws_bytes=1 << 40):
     p = ctypes.c_void_p(ptr)
     scale = 1.0 / math.sqrt(max(shape.d_h, 1)) if scale is None else scale
     return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None,
-                        ctypes.c_float(scale), p, p, p, p, p, None, None)
+                        ctypes.c_float(scale), p, p, p, p, p, None, ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes),
+                        None)
 
 
 def _mask(causal=0, offset=bnd.ATTN_OFFSET_DEFAULT, kv=None, reserved=0):
@@ -108,21 +109,56 @@ def test_bad_scale_and_pointers_rejected(lib):
     assert _call_fwd(lib, _shape(), _mask(), ptr=0x1008) == bnd.ATTN_ERR_ALIGN
 
 
+def test_fwd_workspace_checks(lib):
+    """The forward's workspace (fp16 V tiles and their exponents) must be
+    present, 256-byte aligned and large enough; checked before any CUDA call."""
+    s = _shape(n_k=300, d_v=64, d_h=128)
+    need = lib.attn_fwd_workspace_bytes(ctypes.byref(s))
+    r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
+    tiles = 2 * 2 * 3     # B * Hkv * ceil(300 / 128)
+    assert need == r256(tiles * 128 * 64 * 2) + r256(tiles * 4)
+    assert _call_fwd(lib, s, _mask(), ws=0, ws_bytes=need) == bnd.ATTN_ERR_WORKSPACE
+    assert _call_fwd(lib, s, _mask(), ws=512 + 16, ws_bytes=need) == bnd.ATTN_ERR_WORKSPACE
+    assert _call_fwd(lib, s, _mask(), ws=512, ws_bytes=need - 1) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_fwd_workspace_bytes(ctypes.byref(_shape(B=0))) == 0
+
+
 def test_bwd_workspace_checks(lib):
     s = _shape()
     need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
     rows = 2 * 4 * 100
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
-    # D | tile bounds | fp32 dQ accumulator | fp16 copies of Q and dO
-    assert need == (r256(rows * 4) + r256(2 * 4 * 1 * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
-                    + r256(rows * s.d_v * 2))
+    # D | tile bounds and exponents | group exponents | fp32 dQ accumulator | fp16 copies of Q and dO
+    assert need == (r256(rows * 4) + r256(2 * 4 * 1 * 16) + r256(2 * 2 * 8) + r256(rows * 128 * 4)
+                    + r256(rows * 128 * 2) + r256(rows * s.d_v * 2))
     p = ctypes.c_void_p(256)
     m = _mask()
-    args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5
+    args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 10
     assert lib.attn_bwd(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(_shape(B=0))) == 0
+
+
+def test_bwd_requires_the_output_residual(lib):
+    """The backward's row terms come from O + O_lo: without O_lo the peaked
+    cross-attention gradients miss the tolerance, so every backward entry
+    point refuses a NULL O_lo with ATTN_ERR_NULL before any CUDA call."""
+    s = _shape()
+    need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
+    p = ctypes.c_void_p(256)
+    m = _mask()
+    head = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)]
+    # Q, K, V, O, O_lo = NULL, dO, LSE, dQ, dK, dV
+    assert lib.attn_bwd(*head, p, p, p, p, None, p, p, p, p, p, p, ctypes.c_size_t(need),
+                        None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_bwd_preprocess(ctypes.byref(s), p, p, None, p, p, ctypes.c_size_t(need),
+                                   None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_bwd_noalloc(*head, p, p, p, p, None, p, p, p, p, p, None) == bnd.ATTN_ERR_NULL
+    v = _varlen([0, 100], [0, 100])
+    vneed = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v))
+    assert lib.attn_bwd_varlen(ctypes.byref(v), ctypes.c_float(0.1), p, p, p, p, None, p, p, p, p, p, p,
+                               ctypes.c_size_t(vneed), None) == bnd.ATTN_ERR_NULL
 
 
 def test_visible_pairs_closed_form(lib, orc):
@@ -183,7 +219,9 @@ def test_varlen_checks(lib):
     as many keys as queries; zero-query sequences are allowed.  All checked
     before any CUDA call."""
     p = ctypes.c_void_p(256)
-    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), ctypes.c_float(0.1), p, p, p, p, p, None, None)  # noqa: E731
+    big = ctypes.c_size_t(1 << 40)
+    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), ctypes.c_float(0.1), p, p, p, p, p, None, p, big,  # noqa: E731
+                                        None)
     assert fwd(_varlen([1, 3], [0, 3])) == bnd.ATTN_ERR_SHAPE          # cu[0] != 0
     assert fwd(_varlen([0, 5, 3], [0, 5, 6])) == bnd.ATTN_ERR_SHAPE    # decreasing
     assert fwd(_varlen([0, 3], [0, 0])) == bnd.ATTN_ERR_EMPTY_ROW      # queries, no keys
@@ -192,11 +230,20 @@ def test_varlen_checks(lib):
     assert fwd(_varlen([0, 3], [0, 3], Hq=3)) == bnd.ATTN_ERR_SHAPE
     assert fwd(_varlen([0, 3], [0, 3], d_h=96, d_v=96)) == bnd.ATTN_ERR_UNSUPPORTED
     assert fwd(_varlen([0, 3], [0, 3], B=0)) == bnd.ATTN_ERR_SHAPE
-    assert lib.attn_fwd_varlen(None, ctypes.c_float(0.1), p, p, p, p, p, None, None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_fwd_varlen(None, ctypes.c_float(0.1), p, p, p, p, p, None, p, big, None) == bnd.ATTN_ERR_NULL
     assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), ctypes.c_float(0.0), p, p, p, p, p, None,
-                               None) == bnd.ATTN_ERR_SCALE
+                               p, big, None) == bnd.ATTN_ERR_SCALE
     assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), ctypes.c_float(0.1), p, p, p,
-                               ctypes.c_void_p(0x1008), p, None, None) == bnd.ATTN_ERR_ALIGN
+                               ctypes.c_void_p(0x1008), p, None, p, big, None) == bnd.ATTN_ERR_ALIGN
+    # the forward workspace: present, aligned, large enough
+    v3 = _varlen([0, 3, 200], [0, 3, 300])
+    need = lib.attn_fwd_varlen_workspace_bytes(ctypes.byref(v3))
+    r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
+    assert need == r256(2 * 2 * 3 * 128 * 128 * 2) + r256(2 * 2 * 3 * 4)   # B Hkv ceil(297/128) tiles
+    assert lib.attn_fwd_varlen(ctypes.byref(v3), ctypes.c_float(0.1), p, p, p, p, p, None, None, ctypes.c_size_t(need),
+                               None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_fwd_varlen(ctypes.byref(v3), ctypes.c_float(0.1), p, p, p, p, p, None, p,
+                               ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     # no query rows at all: nothing to compute, OK without touching the GPU
     assert fwd(_varlen([0, 0, 0], [0, 4, 9])) == bnd.ATTN_OK
 
@@ -208,10 +255,10 @@ def test_varlen_workspace_and_pairs(lib):
     rows = cq[-1] * 4
     nqt = (257 + 127) // 128
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
-    assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 8) + r256(rows * 128 * 4) + r256(rows * 128 * 2)
-                    + r256(rows * 64 * 2))
+    assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 16) + r256(3 * 2 * 8) + r256(rows * 128 * 4)
+                    + r256(rows * 128 * 2) + r256(rows * 64 * 2))
     p = ctypes.c_void_p(512)
-    args = [ctypes.byref(v), ctypes.c_float(0.1)] + [p] * 4 + [None] + [p] * 5
+    args = [ctypes.byref(v), ctypes.c_float(0.1)] + [p] * 10
     assert lib.attn_bwd_varlen(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_varlen(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_varlen(*args, p, ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE

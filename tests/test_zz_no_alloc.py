@@ -5,9 +5,9 @@ Some callers cannot allocate device memory where they run the backward pass
 an allocation's device-wide synchronisation).  attn_bwd_noalloc serves them
 from a static buffer inside the library.  This test calls it through the C
 ABI twice in a row and compares each result with the ordinary attn_bwd on
-the same inputs, within the parity tolerance the other GPU tests use.  The
-file is named so that pytest collects it last; it also runs on its own in a
-fresh process.
+the same inputs, and with the fp64 oracle, within the parity tolerance the
+other GPU tests use.  The file is named so that pytest collects it last; it
+also runs on its own in a fresh process.
 """
 import ctypes
 
@@ -15,6 +15,8 @@ import pytest
 import torch
 
 from exact_scaled_dot_gb300.inputs import Workload, make_inputs
+
+from _attn_cases import assert_close, f64, problem_of
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +39,7 @@ def _close(got, ref, what):
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} elements outside tolerance"
 
 
-def test_noalloc_backward_matches_workspace_backward_twice():
+def test_noalloc_backward_matches_workspace_backward_twice(orc):
     import exact_scaled_dot_gb300 as esd
     w = Workload("noalloc", B=2, Hq=4, Hkv=2, nq=200, nk=256, dh=128, dv=128, causal=True,
                  kv_len_range=(120, 256), seed=41)
@@ -50,14 +52,16 @@ def test_noalloc_backward_matches_workspace_backward_twice():
 
     O, LSE, O_lo = esd.attn_fwd(Q, K, V, causal=True, kv_len=kv)
     ref = esd.attn_bwd(Q, K, V, O, dO, LSE, O_lo=O_lo, causal=True, kv_len=kv)
+    rdQ, rdK, rdV, _D, _C = orc.backward(problem_of(w, inp), *(f64(x) for x in (inp.Q, inp.K, inp.V, inp.dO)))
     for call in range(2):
         outs = [torch.full_like(t, float("nan")) for t in ref]
         esd.attn_bwd_noalloc(Q, K, V, O, dO, LSE, O_lo=O_lo, causal=True, kv_len=kv,
                              dQ=outs[0], dK=outs[1], dV=outs[2])
         torch.cuda.synchronize()
         assert esd.attn_get_status() == esd.ATTN_OK
-        for name, got, want in zip(("dQ", "dK", "dV"), outs, ref):
+        for name, got, want, orc_ref in zip(("dQ", "dK", "dV"), outs, ref, (rdQ, rdK, rdV)):
             _close(got, want, f"call {call}: {name}")
+            assert_close(f64(got), orc_ref, f"call {call}: {name} vs oracle")
 
 
 def test_noalloc_refuses_problems_beyond_its_buffer():
