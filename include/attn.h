@@ -39,9 +39,13 @@
  *
  * Ownership and execution.  The caller allocates and owns every buffer,
  * including the forward and backward workspaces; the library allocates no
- * device memory
- * and keeps no state between calls other than a cached driver entry point.
- * Device pointers refer to memory of the current CUDA device.  `stream` is a
+ * device memory.  It keeps a little state between calls: a cached driver
+ * entry point and, per device, the device addresses of its status word and
+ * of attn_bwd_noalloc's static buffer, looked up on the first call there.
+ * Those addresses belong to the device's primary context: after
+ * cudaDeviceReset (or anything else that destroys and recreates that
+ * context) the library must not be called on that device again in the same
+ * process.  Device pointers refer to memory of the current CUDA device.  `stream` is a
  * cudaStream_t (NULL = the legacy default stream); every call only enqueues
  * work on it and returns without synchronising.  Host arrays (kv_len) are
  * read during the call only.
