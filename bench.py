@@ -225,7 +225,7 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 KERNEL_STAGES = ["attn_fwd (V pre-pass + forward kernel)", "attn_bwd_preprocess_kernel", "attn_bwd_main_kernel",
                  "attn_bwd_finalize_kernel"]
-LAUNCHES_PER_STEP = 5   # attn_v16_kernel, attn_fwd_kernel, preprocess, main, finalize
+LAUNCHES_PER_STEP = 6   # attn_v16_kernel, attn_fwd_kernel, preprocess, group exponents, main, finalize
 
 
 class AttnStep:
@@ -866,7 +866,7 @@ def run_varlen(args):
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
                      "frac": tflops / peaks.get("bf16_tflops"), "peak_kind": f"bf16_tflops burst ({peak_src})",
                      "traffic": None},
-        "clocks": clocks, "parity": parity, "gpu_launches": 5 * args.steps,
+        "clocks": clocks, "parity": parity, "gpu_launches": 6 * args.steps,
     }
     print(json.dumps(line))
     return 0

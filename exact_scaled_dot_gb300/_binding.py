@@ -3,6 +3,13 @@
 Argument marshalling only: shapes, masks, pointers and the current torch
 stream go in; every step of the computation runs in the CUDA library.  There
 is no fallback: if the compiled library is missing, every call raises.
+
+The prefill forward, the backward and its stages take strided views for Q,
+K, V, O (with O_lo), dO and the gradients: any tensor whose innermost index
+is contiguous, e.g. Q, K, V sliced out of one fused projection output, with
+their element strides passed through attn_strides.  Padded [B, H, n, d]
+views additionally need a batch stride of H times their head stride.  The
+decode forward takes contiguous tensors only.
 """
 from __future__ import annotations
 
@@ -57,6 +64,14 @@ class AttnMask(ctypes.Structure):
                 ("causal_offset", ctypes.c_int64), ("kv_len", ctypes.POINTER(ctypes.c_int32))]
 
 
+class AttnTensorStrides(ctypes.Structure):
+    _fields_ = [("row", ctypes.c_int64), ("head", ctypes.c_int64)]
+
+
+class AttnStrides(ctypes.Structure):
+    _fields_ = [(n, AttnTensorStrides) for n in ("q", "k", "v", "o", "dO", "dq", "dk", "dv")]
+
+
 class AttnVarlen(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d_h", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("causal", ctypes.c_int32),
@@ -77,8 +92,9 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
         raise RuntimeError(f"CUDA library {p} not found; build it with exact_scaled_dot_gb300.build.build()")
     lib = ctypes.CDLL(str(p))
     S, M = ctypes.POINTER(AttnShape), ctypes.POINTER(AttnMask)
+    ST = ctypes.POINTER(AttnStrides)
     f = ctypes.c_float
-    lib.attn_fwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.attn_fwd_workspace_bytes.argtypes = [S]
     lib.attn_fwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_decode.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -86,11 +102,11 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_fwd_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_workspace_bytes.argtypes = [S]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+    lib.attn_bwd.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                              _vp]
-    lib.attn_bwd_preprocess.argtypes = [S, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    lib.attn_bwd_main.argtypes = [S, M, f, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
-    lib.attn_bwd_finalize.argtypes = [S, f, _vp, ctypes.c_size_t, _vp, _vp]
+    lib.attn_bwd_preprocess.argtypes = [S, ST, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd_main.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
+    lib.attn_bwd_finalize.argtypes = [S, ST, f, _vp, ctypes.c_size_t, _vp, _vp]
     lib.attn_visible_pairs.argtypes = [S, M]
     lib.attn_visible_pairs.restype = ctypes.c_int64
     lib.attn_get_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -99,19 +115,20 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_strerror.argtypes = [ctypes.c_int]
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_abi_version.restype = ctypes.c_int
-    lib.attn_bwd_noalloc.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_noalloc.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.attn_bwd_noalloc.restype = ctypes.c_int
     lib.attn_bwd_noalloc_max_scratch_bytes.argtypes = []
     lib.attn_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
     VL = ctypes.POINTER(AttnVarlen)
     lib.attn_varlen_visible_pairs.argtypes = [VL]
     lib.attn_varlen_visible_pairs.restype = ctypes.c_int64
-    lib.attn_fwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd_varlen.argtypes = [VL, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.attn_fwd_varlen_workspace_bytes.argtypes = [VL]
     lib.attn_fwd_varlen_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd_varlen_workspace_bytes.argtypes = [VL]
     lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd_varlen.argtypes = [VL, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd_varlen.argtypes = [VL, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                                    _vp]
     i64, i32 = ctypes.c_int64, ctypes.c_int32
     lib.attn_proj_fwd.argtypes = [i64, i32, i32, _vp, _vp, _vp, _vp]
     lib.attn_proj_bwd_weight.argtypes = [i64, i32, i32, _vp, _vp, _vp, _vp]
@@ -175,7 +192,9 @@ def _stream(device: torch.device, stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _check_tensor(t: torch.Tensor, name: str, dtype, shape: Tuple[int, ...], device):
+def _check_tensor(t: torch.Tensor, name: str, dtype, shape: Tuple[int, ...], device, strided: bool = False):
+    """strided: the tensor may be a view whose innermost index is contiguous
+    (its other strides go to the library through attn_strides)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
@@ -184,8 +203,58 @@ def _check_tensor(t: torch.Tensor, name: str, dtype, shape: Tuple[int, ...], dev
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda or (device is not None and t.device != device):
         raise ValueError(f"{name} must be a CUDA tensor on {device}")
-    if not t.is_contiguous():
+    if strided:
+        if t.shape[-1] > 1 and t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a contiguous innermost dimension")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _padded_strides(t: torch.Tensor, name: str) -> Tuple[int, int]:
+    """(row, head) element strides of a [B, H, n, d] view; its batch stride
+    must be H times its head stride (size-1 dimensions are free)."""
+    B, H, n, d = (int(x) for x in t.shape)
+    sB, sH, sR = (int(x) for x in t.stride()[:3])
+    row = sR if n > 1 else d
+    head = sH if H > 1 else (sB if B > 1 else n * row)
+    if B > 1 and sB != H * head:
+        raise ValueError(f"{name}: the batch stride must be H times the head stride (use the packed entry points "
+                         f"for sequence-major tensors)")
+    return row, head
+
+
+def _packed_strides(t: torch.Tensor) -> Tuple[int, int]:
+    """(row = token, head) element strides of a [T, H, d] view."""
+    T, H, d = (int(x) for x in t.shape)
+    return (int(t.stride(0)) if T > 1 else H * d), (int(t.stride(1)) if H > 1 else d)
+
+
+def _strides_arg(packed: bool, **tensors):
+    """attn_strides for the given tensors (q=, k=, ... by ABI field name), or
+    None when every one of them is contiguous.  Missing tensors keep the
+    contiguous default ({0, 0})."""
+    st = AttnStrides()
+    any_strided = False
+    for field, t in tensors.items():
+        if t is None:
+            continue
+        if t.is_contiguous():
+            continue
+        row, head = _packed_strides(t) if packed else _padded_strides(t, field)
+        setattr(st, field, AttnTensorStrides(row, head))
+        any_strided = True
+    return ctypes.pointer(st) if any_strided else None
+
+
+def _check_o_lo(O_lo, O, shape, dev):
+    _check_tensor(O_lo, "O_lo", torch.bfloat16, shape, dev, strided=True)
+    if O_lo.stride() != O.stride():
+        raise ValueError("O_lo must have the same strides as O")
+
+
+def _like_o(O):
+    """A residual tensor with O's strides (O may be a view into a larger buffer)."""
+    return torch.empty_strided(O.shape, O.stride(), dtype=O.dtype, device=O.device)
 
 
 def _qkv_shape(Q, K, V):
@@ -197,12 +266,12 @@ def _qkv_shape(Q, K, V):
     return int(B), int(Hq), int(Hkv), int(n_q), int(n_k), int(d_h), int(d_v)
 
 
-def _check_qkv(Q, K, V):
+def _check_qkv(Q, K, V, strided: bool = True):
     B, Hq, Hkv, n_q, n_k, d_h, d_v = _qkv_shape(Q, K, V)
     dev = Q.device
-    _check_tensor(Q, "Q", torch.bfloat16, (B, Hq, n_q, d_h), dev)
-    _check_tensor(K, "K", torch.bfloat16, (B, Hkv, n_k, d_h), dev)
-    _check_tensor(V, "V", torch.bfloat16, (B, Hkv, n_k, d_v), dev)
+    _check_tensor(Q, "Q", torch.bfloat16, (B, Hq, n_q, d_h), dev, strided=strided)
+    _check_tensor(K, "K", torch.bfloat16, (B, Hkv, n_k, d_h), dev, strided=strided)
+    _check_tensor(V, "V", torch.bfloat16, (B, Hkv, n_k, d_v), dev, strided=strided)
     return (B, Hq, Hkv, n_q, n_k, d_h, d_v), dev
 
 
@@ -231,18 +300,19 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool 
         O = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
     if LSE is None:
         LSE = torch.empty((B, Hq, n_q), dtype=torch.float32, device=dev)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev, strided=True)
     if O_lo is None and residual:
-        O_lo = torch.empty((B, Hq, n_q, d_v), dtype=torch.bfloat16, device=dev)
-    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+        O_lo = _like_o(O)
     _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
     if O_lo is not None:
-        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+        _check_o_lo(O_lo, O, (B, Hq, n_q, d_v), dev)
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
     if workspace is None:
         need = int(load().attn_fwd_workspace_bytes(ctypes.byref(shape)))
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
-    rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
+    st = _strides_arg(False, q=Q, k=K, v=V, o=O)
+    rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(Q), _ptr(K),
                          _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), *_ws(workspace), _stream(dev, stream))
     _check(rc, "attn_fwd")
     return O, LSE, O_lo
@@ -262,7 +332,7 @@ def attn_fwd_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal
     """Forward for short query blocks (n_q <= 128) over a long key cache: the
     same outputs as attn_fwd, with the query heads of a KV head packed into
     one tile and the key range split across CTAs (merged by log-sum-exp)."""
-    dims, dev = _check_qkv(Q, K, V)
+    dims, dev = _check_qkv(Q, K, V, strided=False)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
     if O is None:
@@ -301,20 +371,20 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_off
     dims, dev = _check_qkv(Q, K, V)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
-    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
-    _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev, strided=True)
+    _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev, strided=True)
     _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
     if O_lo is not None:
-        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+        _check_o_lo(O_lo, O, (B, Hq, n_q, d_v), dev)
     if dQ is None:
         dQ = torch.empty_like(Q)
     if dK is None:
         dK = torch.empty_like(K)
     if dV is None:
         dV = torch.empty_like(V)
-    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev)
-    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev)
-    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev)
+    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev, strided=True)
+    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev, strided=True)
+    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev, strided=True)
     need = attn_bwd_workspace_bytes(*dims)
     if workspace is None:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
@@ -322,7 +392,8 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_off
         raise ValueError(f"workspace must hold at least {need} bytes")
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
-    rc = load().attn_bwd(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q), _ptr(K),
+    st = _strides_arg(False, q=Q, k=K, v=V, o=O, dO=dO, dq=dQ, dk=dK, dv=dV)
+    rc = load().attn_bwd(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(Q), _ptr(K),
                          _ptr(V), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
                          _ptr(workspace),
                          ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
@@ -336,8 +407,11 @@ def _ws(workspace):
 
 def attn_bwd_preprocess(Q, O, dO, workspace, *, shape: AttnShape, O_lo=None, stream=None):
     """Stage 1 of the backward (row terms, tile bounds, zeroed dQ accumulator, fp16 copies of Q and dO)."""
-    rc = load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(Q), _ptr(O), _ptr(O_lo), _ptr(dO), *_ws(workspace),
-                                    _stream(O.device, stream))
+    if O_lo is not None and O_lo.stride() != O.stride():
+        raise ValueError("O_lo must have the same strides as O")
+    st = _strides_arg(False, q=Q, o=O, dO=dO)
+    rc = load().attn_bwd_preprocess(ctypes.byref(shape), st, _ptr(Q), _ptr(O), _ptr(O_lo), _ptr(dO),
+                                    *_ws(workspace), _stream(O.device, stream))
     _check(rc, "attn_bwd_preprocess")
 
 
@@ -347,15 +421,17 @@ def attn_bwd_main(K, V, LSE, workspace, dK, dV, *, shape: AttnShape, causal=Fals
     come from the fp16 copies stage 1 left in the workspace)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
     m = _MaskArg(causal, causal_offset, kv_len)
-    rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(K), _ptr(V),
-                              _ptr(LSE), *_ws(workspace), _ptr(dK), _ptr(dV), _stream(K.device, stream))
+    st = _strides_arg(False, k=K, v=V, dk=dK, dv=dV)
+    rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(K),
+                              _ptr(V), _ptr(LSE), *_ws(workspace), _ptr(dK), _ptr(dV), _stream(K.device, stream))
     _check(rc, "attn_bwd_main")
 
 
 def attn_bwd_finalize(workspace, dQ, *, shape: AttnShape, scale: Optional[float] = None, stream=None):
     """Stage 3 of the backward (dQ = scale * accumulator in bf16)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
-    rc = load().attn_bwd_finalize(ctypes.byref(shape), ctypes.c_float(scale), *_ws(workspace), _ptr(dQ),
+    st = _strides_arg(False, dq=dQ)
+    rc = load().attn_bwd_finalize(ctypes.byref(shape), st, ctypes.c_float(scale), *_ws(workspace), _ptr(dQ),
                                   _stream(dQ.device, stream))
     _check(rc, "attn_bwd_finalize")
 
@@ -400,20 +476,21 @@ def attn_bwd_noalloc(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False,
     dims, dev = _check_qkv(Q, K, V)
     B, Hq, Hkv, n_q, n_k, d_h, d_v = dims
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
-    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev)
-    _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+    _check_tensor(O, "O", torch.bfloat16, (B, Hq, n_q, d_v), dev, strided=True)
+    _check_tensor(dO, "dO", torch.bfloat16, (B, Hq, n_q, d_v), dev, strided=True)
     _check_tensor(LSE, "LSE", torch.float32, (B, Hq, n_q), dev)
     if O_lo is not None:
-        _check_tensor(O_lo, "O_lo", torch.bfloat16, (B, Hq, n_q, d_v), dev)
+        _check_o_lo(O_lo, O, (B, Hq, n_q, d_v), dev)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
-    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev)
-    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev)
-    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev)
+    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev, strided=True)
+    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev, strided=True)
+    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev, strided=True)
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
-    rc = load().attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(m.mask), ctypes.c_float(scale), _ptr(Q),
+    st = _strides_arg(False, q=Q, k=K, v=V, o=O, dO=dO, dq=dQ, dk=dK, dv=dV)
+    rc = load().attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(Q),
                                  _ptr(K), _ptr(V), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
                                  _ptr(dV), _stream(dev, stream))
     _check(rc, "attn_bwd_noalloc")
@@ -455,9 +532,9 @@ def _varlen_dims(Q, K, V):
     Tk, Hkv, _ = (int(x) for x in K.shape)
     d_v = int(V.shape[2])
     dev = Q.device
-    _check_tensor(Q, "Q", torch.bfloat16, (Tq, Hq, d_h), dev)
-    _check_tensor(K, "K", torch.bfloat16, (Tk, Hkv, d_h), dev)
-    _check_tensor(V, "V", torch.bfloat16, (Tk, Hkv, d_v), dev)
+    _check_tensor(Q, "Q", torch.bfloat16, (Tq, Hq, d_h), dev, strided=True)
+    _check_tensor(K, "K", torch.bfloat16, (Tk, Hkv, d_h), dev, strided=True)
+    _check_tensor(V, "V", torch.bfloat16, (Tk, Hkv, d_v), dev, strided=True)
     return (Tq, Tk, Hq, Hkv, d_h, d_v), dev
 
 
@@ -484,16 +561,17 @@ def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False
         O = torch.empty((Tq, Hq, d_v), dtype=torch.bfloat16, device=dev)
     if LSE is None:
         LSE = torch.empty((Hq, Tq), dtype=torch.float32, device=dev)
+    _check_tensor(O, "O", torch.bfloat16, (Tq, Hq, d_v), dev, strided=True)
     if O_lo is None and residual:
-        O_lo = torch.empty((Tq, Hq, d_v), dtype=torch.bfloat16, device=dev)
-    _check_tensor(O, "O", torch.bfloat16, (Tq, Hq, d_v), dev)
+        O_lo = _like_o(O)
     _check_tensor(LSE, "LSE", torch.float32, (Hq, Tq), dev)
     if O_lo is not None:
-        _check_tensor(O_lo, "O_lo", torch.bfloat16, (Tq, Hq, d_v), dev)
+        _check_o_lo(O_lo, O, (Tq, Hq, d_v), dev)
     if workspace is None:
         need = int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v)))
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
-    rc = load().attn_fwd_varlen(ctypes.byref(a.v), ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+    st = _strides_arg(True, q=Q, k=K, v=V, o=O)
+    rc = load().attn_fwd_varlen(ctypes.byref(a.v), st, ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                 _ptr(LSE), _ptr(O_lo), *_ws(workspace), _stream(dev, stream))
     _check(rc, "attn_fwd_varlen")
     return O, LSE, O_lo
@@ -512,23 +590,24 @@ def attn_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens_q, cu_seqlens_k, *, O_lo=Non
     if a.total_q != Tq or a.total_k != Tk:
         raise ValueError("cu_seqlens_q[-1] / cu_seqlens_k[-1] must equal the token counts of Q / K")
     scale = 1.0 / math.sqrt(d_h) if scale is None else float(scale)
-    _check_tensor(O, "O", torch.bfloat16, (Tq, Hq, d_v), dev)
-    _check_tensor(dO, "dO", torch.bfloat16, (Tq, Hq, d_v), dev)
+    _check_tensor(O, "O", torch.bfloat16, (Tq, Hq, d_v), dev, strided=True)
+    _check_tensor(dO, "dO", torch.bfloat16, (Tq, Hq, d_v), dev, strided=True)
     _check_tensor(LSE, "LSE", torch.float32, (Hq, Tq), dev)
     if O_lo is not None:
-        _check_tensor(O_lo, "O_lo", torch.bfloat16, (Tq, Hq, d_v), dev)
+        _check_o_lo(O_lo, O, (Tq, Hq, d_v), dev)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
-    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev)
-    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev)
-    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev)
+    _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev, strided=True)
+    _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev, strided=True)
+    _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev, strided=True)
     need = int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v)))
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace must hold at least {need} bytes")
-    rc = load().attn_bwd_varlen(ctypes.byref(a.v), ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+    st = _strides_arg(True, q=Q, k=K, v=V, o=O, dO=dO, dq=dQ, dk=dK, dv=dV)
+    rc = load().attn_bwd_varlen(ctypes.byref(a.v), st, ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                 _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
                                 ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
     _check(rc, "attn_bwd_varlen")

@@ -93,6 +93,51 @@ int check_ptrs(std::initializer_list<const void*> ptrs) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// One tensor's strides: the caller's ({0, 0} = contiguous), checked.
+int one_strides(const attn_tensor_strides* user, int64_t row0, int64_t head0, int d, TensorStrides* out) {
+  if (!user || (user->row == 0 && user->head == 0)) {
+    *out = TensorStrides{row0, head0};
+    return ATTN_OK;
+  }
+  if (user->row % 8 != 0 || user->head % 8 != 0) return ATTN_ERR_ALIGN;
+  if (user->row < d || user->head < d || user->row > (int64_t{1} << 36) || user->head > (int64_t{1} << 36))
+    return ATTN_ERR_SHAPE;
+  *out = TensorStrides{user->row, user->head};
+  return ATTN_OK;
+}
+
+// Every user tensor's strides into `lay` (whose `packed` is set): padded
+// [B][H][n][d] defaults row = d, head = n d; packed [T][H][d] defaults
+// row = H d, head = d.
+int build_strides(const attn_strides* st, int Hq, int Hkv, int n_q, int n_k, int dh, int dv, LayoutParams* lay) {
+  const bool pk = lay->packed != 0;
+  auto def = [&](int H, int n, int d, int64_t& row, int64_t& head) {
+    row = pk ? static_cast<int64_t>(H) * d : d;
+    head = pk ? d : static_cast<int64_t>(n) * d;
+  };
+  struct Item {
+    const attn_tensor_strides* user;
+    TensorStrides* out;
+    int H, n, d;
+  } items[8] = {{st ? &st->q : nullptr, &lay->sq, Hq, n_q, dh},   {st ? &st->k : nullptr, &lay->sk, Hkv, n_k, dh},
+                {st ? &st->v : nullptr, &lay->sv, Hkv, n_k, dv},  {st ? &st->o : nullptr, &lay->so, Hq, n_q, dv},
+                {st ? &st->dO : nullptr, &lay->sdo, Hq, n_q, dv}, {st ? &st->dq : nullptr, &lay->sdq, Hq, n_q, dh},
+                {st ? &st->dk : nullptr, &lay->sdk, Hkv, n_k, dh}, {st ? &st->dv : nullptr, &lay->sdv, Hkv, n_k, dv}};
+  for (const Item& it : items) {
+    int64_t row, head;
+    def(it.H, it.n, it.d, row, head);
+    const int rc = one_strides(it.user, row, head, it.d, it.out);
+    if (rc) return rc;
+  }
+  return ATTN_OK;
+}
+
+// Whether a tensor has its layout's contiguous strides.
+bool contiguous_strides(const LayoutParams& lay, const TensorStrides& s, int H, int n, int d) {
+  return lay.packed ? (s.row == static_cast<int64_t>(H) * d && s.head == d)
+                    : (s.row == d && s.head == static_cast<int64_t>(n) * d);
+}
+
 // Sum over query rows of max(0, lim(b, i)) for one batch element.
 int64_t pairs_one_batch(const MaskParams& m, int n_q, int n_k, int b) {
   const int64_t L = key_len(m, n_k, b);
@@ -179,16 +224,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D view [bh][n][d] of a contiguous tensor of 2-byte elements (bf16, or
-// the backward's fp16 copy of Q: the copy does not interpret the values),
-// read in 128-row x 64-col boxes with the 128-byte swizzle the tensor-core
-// operand layout expects.  Rows beyond n of a head read as all-zero bits
-// (bounds fill, 0 in either type), never the next head.
-bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
+// 3-D view [bh][n][d] of a tensor of 2-byte elements (bf16, or the
+// backward's fp16 copy of Q: the copy does not interpret the values) with
+// element strides row (default d) and head (default n d), read in 128-row x
+// 64-col boxes with the 128-byte swizzle the tensor-core operand layout
+// expects.  Rows beyond n of a head read as all-zero bits (bounds fill, 0 in
+// either type), never the next head.
+bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh, int64_t row_stride = 0,
+               int64_t head_stride = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  if (row_stride == 0) row_stride = d;
+  if (head_stride == 0) head_stride = static_cast<int64_t>(n) * d;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride) * 2, static_cast<cuuint64_t>(head_stride) * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -199,15 +248,19 @@ bool make_tmap(CUtensorMap* map, const void* ptr, int d, int n, int64_t bh) {
 // 3-D view [bh][n][d] of the fp32 dQ accumulator for TMA reduce-add in
 // 32-row x 32-column boxes (128-byte rows, 128-byte swizzle); rows beyond n
 // of a head are clipped.
-// Token-major view [T][H][d] (packed sequences) of a 2-byte tensor: dims
-// (d, H, T), boxes of 64 columns x 1 head x 128 tokens, which land in
+// Token-major view [T][H][d] (packed sequences) of a 2-byte tensor with
+// element strides row (between tokens, default H d) and head (default d):
+// dims (d, H, T), boxes of 64 columns x 1 head x 128 tokens, which land in
 // shared memory exactly like the padded view's 128-row x 64-col boxes.
 // Tokens past T read as zeros.
-bool make_tmap_packed(CUtensorMap* map, const void* ptr, int d, int H, int64_t T) {
+bool make_tmap_packed(CUtensorMap* map, const void* ptr, int d, int H, int64_t T, int64_t row_stride = 0,
+                      int64_t head_stride = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  if (row_stride == 0) row_stride = static_cast<int64_t>(H) * d;
+  if (head_stride == 0) head_stride = d;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_stride) * 2, static_cast<cuuint64_t>(row_stride) * 2};
   cuuint32_t box[3] = {64, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -575,15 +628,19 @@ size_t attn_fwd_workspace_bytes(const attn_shape* shape) {
   return fwd_workspace_layout(shape, nullptr).bytes;
 }
 
-int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-             const void* V, void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes,
-             void* stream) {
+int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+             const void* Q, const void* K, const void* V, void* O, float* LSE, void* O_lo, void* workspace,
+             size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   MaskParams m;
   rc = build_mask(shape, mask, &m);
   if (rc) return rc;
   rc = check_scale(scale);
+  if (rc) return rc;
+  LayoutParams lay;
+  std::memset(&lay, 0, sizeof(lay));
+  rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &lay);
   if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, LSE});
   if (rc) return rc;
@@ -597,10 +654,9 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale, const 
   CUtensorMap tq, tk;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
-  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk))
+  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq, lay.sq.row, lay.sq.head) ||
+      !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk, lay.sk.row, lay.sk.head))
     return ATTN_ERR_CUDA;
-  LayoutParams lay;
-  std::memset(&lay, 0, sizeof(lay));
   return launch_forward(shape, m, lay, scale, tq, tk, V, fwd_workspace_layout(shape, workspace), O, LSE, O_lo,
                         status, static_cast<cudaStream_t>(stream));
 }
@@ -669,9 +725,13 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O, const void* O_lo, const void* dO,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const void* Q, const void* O,
+                        const void* O_lo, const void* dO, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
+  if (rc) return rc;
+  LayoutParams padded;
+  std::memset(&padded, 0, sizeof(padded));
+  rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &padded);
   if (rc) return rc;
   rc = check_ptrs({Q, O, O_lo, dO});
   if (rc) return rc;
@@ -681,20 +741,22 @@ int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O, c
   rc = device_status_ptr(&status);
   if (rc) return rc;
   const Workspace w = workspace_layout(shape, workspace);
-  LayoutParams padded;
-  std::memset(&padded, 0, sizeof(padded));
   const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), padded, shape->d_v, shape->d_h, Q, O, O_lo,
                                                    dO, w.D, w.tilemax, w.grpexp, w.dQacc, w.Q16, w.dO16, status,
                                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, const void* K, const void* V,
-                  const float* LSE, void* workspace, size_t workspace_bytes, void* dK, void* dV, void* stream) {
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+                  const void* K, const void* V, const float* LSE, void* workspace, size_t workspace_bytes, void* dK,
+                  void* dV, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   BwdParams p;
   rc = build_mask(shape, mask, &p.mask);
+  if (rc) return rc;
+  std::memset(&p.lay, 0, sizeof(p.lay));
+  rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &p.lay);
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
@@ -709,12 +771,12 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   CUtensorMap tq, tk, tv, tdo, tdq;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
-  if (!make_tmap(&tq, w.Q16, shape->d_h, shape->n_q, bhq) || !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk) ||
-      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk) || !make_tmap(&tdo, w.dO16, shape->d_v, shape->n_q, bhq) ||
-      !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
+  if (!make_tmap(&tq, w.Q16, shape->d_h, shape->n_q, bhq) ||
+      !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk, p.lay.sk.row, p.lay.sk.head) ||
+      !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk, p.lay.sv.row, p.lay.sv.head) ||
+      !make_tmap(&tdo, w.dO16, shape->d_v, shape->n_q, bhq) || !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
     return ATTN_ERR_CUDA;
   p.sh = shape_params(shape);
-  std::memset(&p.lay, 0, sizeof(p.lay));
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
@@ -732,9 +794,13 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale, c
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspace, size_t workspace_bytes,
-                      void* dQ, void* stream) {
+int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, float scale, const void* workspace,
+                      size_t workspace_bytes, void* dQ, void* stream) {
   int rc = check_shape(shape);
+  if (rc) return rc;
+  LayoutParams lay;
+  std::memset(&lay, 0, sizeof(lay));
+  rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &lay);
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
@@ -746,30 +812,39 @@ int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspac
   rc = device_status_ptr(&status);
   if (rc) return rc;
   const Workspace w = workspace_layout(shape, const_cast<void*>(workspace));
-  const cudaError_t e = launch_attn_bwd_finalize(q_rows(shape) * shape->d_h, scale, w.dQacc, dQ,
-                                                 static_cast<cudaStream_t>(stream));
+  // Padded accumulator rows: heads of n_q rows.
+  const cudaError_t e = launch_attn_bwd_finalize(
+      q_rows(shape) * shape->d_h, shape->d_h, shape->n_q, lay.sdq.head, lay.sdq.row,
+      contiguous_strides(lay, lay.sdq, shape->Hq, shape->n_q, shape->d_h), scale, w.dQacc, dQ,
+      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-             const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
+int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale, const void* Q,
+             const void* K, const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
              void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   MaskParams m;
   rc = build_mask(shape, mask, &m);
   if (rc) return rc;
+  {
+    LayoutParams lay;
+    std::memset(&lay, 0, sizeof(lay));
+    rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &lay);
+    if (rc) return rc;
+  }
   rc = check_scale(scale);
   if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV});
   if (rc) return rc;
   rc = check_workspace(shape, workspace, workspace_bytes);
   if (rc) return rc;
-  rc = attn_bwd_preprocess(shape, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
+  rc = attn_bwd_preprocess(shape, strides, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
   if (rc) return rc;
-  rc = attn_bwd_main(shape, mask, scale, K, V, LSE, workspace, workspace_bytes, dK, dV, stream);
+  rc = attn_bwd_main(shape, mask, strides, scale, K, V, LSE, workspace, workspace_bytes, dK, dV, stream);
   if (rc) return rc;
-  return attn_bwd_finalize(shape, scale, workspace, workspace_bytes, dQ, stream);
+  return attn_bwd_finalize(shape, strides, scale, workspace, workspace_bytes, dQ, stream);
 }
 
 int attn_get_status(int* status) {
@@ -810,9 +885,9 @@ int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 // the preprocess stage), so leftovers from an earlier call do not matter; but
 // all calls share the one buffer, so calls that overlap on the GPU (other
 // streams, other host threads) race and must be serialised by the caller.
-int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale, const void* Q, const void* K,
-                     const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
-                     void* dK, void* dV, void* stream) {
+int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+                     const void* Q, const void* K, const void* V, const void* O, const void* O_lo, const void* dO,
+                     const float* LSE, void* dQ, void* dK, void* dV, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   if (workspace_layout(shape, nullptr).bytes > kStaticBwdScratchBytes) return ATTN_ERR_WORKSPACE;
@@ -820,6 +895,12 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale
   MaskParams m;
   rc = build_mask(shape, mask, &m);
   if (rc) return rc;
+  {
+    LayoutParams lay;
+    std::memset(&lay, 0, sizeof(lay));
+    rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &lay);
+    if (rc) return rc;
+  }
   rc = check_scale(scale);
   if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV});
@@ -827,8 +908,8 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale
   void* scratch = nullptr;
   rc = static_scratch_ptr(&scratch);
   if (rc) return rc;
-  return attn_bwd(shape, mask, scale, Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV, scratch, kStaticBwdScratchBytes,
-                  stream);
+  return attn_bwd(shape, mask, strides, scale, Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV, scratch,
+                  kStaticBwdScratchBytes, stream);
 }
 
 size_t attn_bwd_noalloc_max_scratch_bytes(void) { return kStaticBwdScratchBytes; }
@@ -963,10 +1044,13 @@ size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v) {
   return fwd_workspace_layout(&d.shape, nullptr).bytes;
 }
 
-int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V, void* O,
-                    float* LSE, void* O_lo, void* workspace, size_t workspace_bytes, void* stream) {
+int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
+                    const void* V, void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes,
+                    void* stream) {
   Varlen d;
   int rc = build_varlen(v, &d);
+  if (rc) return rc;
+  rc = build_strides(strides, v->Hq, v->Hkv, 0, 0, v->d_h, v->d_v, &d.lay);
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
@@ -981,7 +1065,8 @@ int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   rc = device_status_ptr(&status);
   if (rc) return rc;
   CUtensorMap tq, tk;
-  if (!make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q) || !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k))
+  if (!make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q, d.lay.sq.row, d.lay.sq.head) ||
+      !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k, d.lay.sk.row, d.lay.sk.head))
     return ATTN_ERR_CUDA;
   return launch_forward(&d.shape, d.mask, d.lay, scale, tq, tk, V, fwd_workspace_layout(&d.shape, workspace), O, LSE,
                         O_lo, status, static_cast<cudaStream_t>(stream));
@@ -993,11 +1078,13 @@ size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v) {
   return workspace_layout_varlen(d, nullptr).bytes;
 }
 
-int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
-                    const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ, void* dK,
-                    void* dV, void* workspace, size_t workspace_bytes, void* stream) {
+int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
+                    const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
+                    void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream) {
   Varlen d;
   int rc = build_varlen(v, &d);
+  if (rc) return rc;
+  rc = build_strides(strides, v->Hq, v->Hkv, 0, 0, v->d_h, v->d_v, &d.lay);
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
@@ -1016,10 +1103,17 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (d.total_k == 0) return ATTN_OK;
   if (d.total_q == 0) {
-    // No query sees any key: the gradients of K and V are zero.
-    if (cudaMemsetAsync(dK, 0, static_cast<size_t>(d.total_k) * v->Hkv * v->d_h * 2, st) != cudaSuccess ||
-        cudaMemsetAsync(dV, 0, static_cast<size_t>(d.total_k) * v->Hkv * v->d_v * 2, st) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    // No query sees any key: the gradients of K and V are zero (each head's
+    // rows as one pitched block: tokens at the row stride, d elements each).
+    auto zero = [&](void* t, const TensorStrides& s, int d_) {
+      for (int h = 0; h < v->Hkv; ++h)
+        if (cudaMemset2DAsync(static_cast<__nv_bfloat16*>(t) + static_cast<int64_t>(h) * s.head,
+                              static_cast<size_t>(s.row) * 2, 0, static_cast<size_t>(d_) * 2,
+                              static_cast<size_t>(d.total_k), st) != cudaSuccess)
+          return false;
+      return true;
+    };
+    if (!zero(dK, d.lay.sdk, v->d_h) || !zero(dV, d.lay.sdv, v->d_v)) return ATTN_ERR_CUDA;
     return ATTN_OK;
   }
   unsigned int* status = nullptr;
@@ -1032,7 +1126,8 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_packed(&tq, w.Q16, v->d_h, v->Hq, d.total_q) ||
-      !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k) || !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k) ||
+      !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k, d.lay.sk.row, d.lay.sk.head) ||
+      !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k, d.lay.sv.row, d.lay.sv.head) ||
       !make_tmap_packed(&tdo, w.dO16, v->d_v, v->Hq, d.total_q) ||
       !make_tmap_acc_packed(&tdq, w.dQacc, v->d_h, v->Hq, d.total_q))
     return ATTN_ERR_CUDA;
@@ -1054,7 +1149,9 @@ int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void
   p.status = status;
   e = launch_attn_bwd_main(v->d_h, v->d_v, tq, tk, tv, tdo, tdq, p, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  e = launch_attn_bwd_finalize(d.total_q * v->Hq * v->d_h, scale, w.dQacc, dQ, st);
+  // Packed accumulator rows: tokens of Hq heads.
+  e = launch_attn_bwd_finalize(d.total_q * v->Hq * v->d_h, v->d_h, v->Hq, d.lay.sdq.row, d.lay.sdq.head,
+                               contiguous_strides(d.lay, d.lay.sdq, v->Hq, 0, v->d_h), scale, w.dQacc, dQ, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

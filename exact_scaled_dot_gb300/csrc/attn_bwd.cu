@@ -845,9 +845,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     if (ok) {
       const int64_t j = j0 + row;
       const bool in = j < k_row_end;
-      const int64_t krow = k_row(PACKED, p.lay, p.sh.Hkv, p.sh.n_k, b, hkv, j);
-      uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + krow * DH);
-      uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + krow * DV);
+      uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) +
+                                           strided_off(PACKED, p.lay.sdk, p.sh.Hkv, p.lay.cu_k[b], b, hkv, j));
+      uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) +
+                                           strided_off(PACKED, p.lay.sdv, p.sh.Hkv, p.lay.cu_k[b], b, hkv, j));
       const float dk_scale = p.scale * exp2_int(-cs.g - cs.q);   // dK_acc = 2^(g + q) dS^T Q (CtaScale)
       const float dv_scale = exp2_int(-cs.o);                    // dV_acc = 2^o P^T dO
 #pragma unroll
@@ -906,9 +907,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 // whole tile's Q and dO therefore stay in registers until the block has
 // reduced its maxima.  In the D pass each row has DV/8 consecutive threads,
 // one 16-byte chunk each, so every warp load covers whole rows.
-// row_at(rr) is the storage row of the tile's row rr, d_at(rr) its index in D.
-template <int DV, int DH, class RowAt, class DAt>
+// row_at(rr) is the workspace row of the tile's row rr (the contiguous
+// layout of Q), d_at(rr) its index in D, and user_at(s, rr) its element
+// offset in a user tensor with strides s.
+template <int DV, int DH, class RowAt, class DAt, class UserAt>
 __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at, const DAt& d_at,
+                                              const UserAt& user_at, const TensorStrides& sq,
+                                              const TensorStrides& so, const TensorStrides& sdo,
                                               const uint4* __restrict__ Q, const uint4* __restrict__ O,
                                               const uint4* __restrict__ O_lo, const uint4* __restrict__ dO,
                                               float* __restrict__ D, float4* __restrict__ tm,
@@ -927,7 +932,7 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
 #pragma unroll
   for (int j = 0; j < kQ; ++j) {
     const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
-    q[j] = rr < rows_here ? Q[row_at(rr) * (DH / 8) + k % (DH / 8)] : make_uint4(0u, 0u, 0u, 0u);
+    q[j] = rr < rows_here ? Q[user_at(sq, rr) / 8 + k % (DH / 8)] : make_uint4(0u, 0u, 0u, 0u);
   }
   float mn = 0.f, md = 0.f;
   uint32_t gmax = 0u, qmax = 0u;
@@ -940,9 +945,9 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
       const int rr = (p0 + u) * kRows + r0;
       a[u] = g[p0 + u] = lo[u] = make_uint4(0u, 0u, 0u, 0u);
       if (rr < rows_here) {
-        const int64_t at = row_at(rr) * (DV / 8) + c;
+        const int64_t at = user_at(so, rr) / 8 + c;
         a[u] = O[at];
-        g[p0 + u] = dO[at];
+        g[p0 + u] = dO[user_at(sdo, rr) / 8 + c];
         if (O_lo) lo[u] = O_lo[at];
       }
     }
@@ -1010,11 +1015,11 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
     *tm = make_float4(x, y, static_cast<float>(eq), static_cast<float>(eo));
     if (f16_saturates(qm, eq) || f16_saturates(gm, eo)) record_status(status, ATTN_ERR_RANGE);
   }
-  const float so = exp2_int(eo == kExpZero ? 0 : eo), sq = exp2_int(eq == kExpZero ? 0 : eq);
+  const float sco = exp2_int(eo == kExpZero ? 0 : eo), scq = exp2_int(eq == kExpZero ? 0 : eq);
 #pragma unroll
   for (int p0 = 0; p0 < kPasses; ++p0) {
     const int rr = p0 * kRows + r0;
-    if (rr < rows_here) dO16[row_at(rr) * (DV / 8) + c] = bf16x8_to_f16x8_scaled(g[p0], so);
+    if (rr < rows_here) dO16[row_at(rr) * (DV / 8) + c] = bf16x8_to_f16x8_scaled(g[p0], sco);
   }
 #pragma unroll
   for (int j = 0; j < kZ; ++j) {
@@ -1024,7 +1029,7 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
 #pragma unroll
   for (int j = 0; j < kQ; ++j) {
     const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
-    if (rr < rows_here) Q16[row_at(rr) * (DH / 8) + k % (DH / 8)] = bf16x8_to_f16x8_scaled(q[j], sq);
+    if (rr < rows_here) Q16[row_at(rr) * (DH / 8) + k % (DH / 8)] = bf16x8_to_f16x8_scaled(q[j], scq);
   }
 }
 
@@ -1032,7 +1037,8 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
 // (b, h) are contiguous, n_q of them.
 template <int DV, int DH>
 __global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const uint4* __restrict__ O,
+attn_bwd_preprocess_kernel(int n_q, int nqt, TensorStrides sq, TensorStrides so, TensorStrides sdo,
+                           const uint4* __restrict__ Q, const uint4* __restrict__ O,
                            const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
                            float4* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
                            uint4* __restrict__ dO16, unsigned int* status) {
@@ -1042,8 +1048,9 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
   const int rows_here = static_cast<int>(n_q - i0 < kTileM ? n_q - i0 : kTileM);
   const int64_t row0 = bh * n_q + i0;
   const auto row_at = [row0](int rr) { return row0 + rr; };
-  bwd_prep_tile<DV, DH>(rows_here, row_at, row_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16,
-                        status);
+  const auto user_at = [bh, i0](const TensorStrides& s, int rr) { return bh * s.head + (i0 + rr) * s.row; };
+  bwd_prep_tile<DV, DH>(rows_here, row_at, row_at, user_at, sq, so, sdo, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt,
+                        dQacc, Q16, dO16, status);
 }
 
 // The same for packed sequences (token-major rows, per-sequence lengths):
@@ -1052,6 +1059,7 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, const uint4* __restrict__ Q, const 
 struct PrepPacked {
   int32_t n_q, Hq;
   int64_t total_q;
+  TensorStrides sq, so, sdo;
   int32_t cu_q[ATTN_MAX_BATCH + 1];
   __device__ __forceinline__ int64_t len(int b) const { return static_cast<int64_t>(cu_q[b + 1]) - cu_q[b]; }
   __device__ __forceinline__ int64_t row(int b, int h, int64_t i) const {
@@ -1078,8 +1086,10 @@ attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt
   const int rows_here = static_cast<int>(left < kTileM ? (left < 0 ? 0 : left) : kTileM);
   const auto row_at = [&rm, b, h, i0](int rr) { return rm.row(b, h, i0 + rr); };
   const auto d_at = [&rm, b, h, i0](int rr) { return rm.vec(b, h, i0 + rr); };
-  bwd_prep_tile<DV, DH>(rows_here, row_at, d_at, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt, dQacc, Q16, dO16,
-                        status);
+  const int64_t t0 = static_cast<int64_t>(rm.cu_q[b]) + i0;
+  const auto user_at = [t0, h](const TensorStrides& s, int rr) { return (t0 + rr) * s.row + h * s.head; };
+  bwd_prep_tile<DV, DH>(rows_here, row_at, d_at, user_at, rm.sq, rm.so, rm.sdo, Q, O, O_lo, dO, D,
+                        tilemax + bh * nqt + qt, dQacc, Q16, dO16, status);
 }
 
 // Every query tile of a (batch, KV head) group brought to one exponent for
@@ -1175,7 +1185,26 @@ __global__ void __launch_bounds__(256) attn_bwd_group_exp_kernel(const __grid_co
   }
 }
 
-// dQ = scale * acc, eight elements per thread per iteration.
+// dQ = scale * acc into a strided dQ: the accumulator row r (d_h / 8 chunks of
+// 8) is row r % n_inner of group r / n_inner, at element offset
+// (r / n_inner) s_outer + (r % n_inner) s_inner (padded: heads of n_q rows;
+// packed: tokens of Hq heads).
+__global__ void __launch_bounds__(256)
+attn_bwd_finalize_strided_kernel(int64_t n8, int c8, int n_inner, int64_t s_outer, int64_t s_inner, float scale,
+                                 const float4* __restrict__ acc, uint4* __restrict__ dQ) {
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n8; k += nthreads) {
+    const int64_t r = k / c8;
+    const int64_t outer = r / n_inner;
+    const int64_t off = outer * s_outer + (r - outer * n_inner) * s_inner;
+    const float4 a = acc[2 * k];
+    const float4 c = acc[2 * k + 1];
+    dQ[off / 8 + (k - r * c8)] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                                            pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+  }
+}
+
+// dQ = scale * acc, eight elements per thread per iteration (contiguous dQ).
 __global__ void __launch_bounds__(256)
 attn_bwd_finalize_kernel(int64_t n8, float scale, const float4* __restrict__ acc, uint4* __restrict__ dQ) {
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -1218,13 +1247,16 @@ void launch_pre_t(const ShapeParams& sh, const LayoutParams& lay, int nqt, const
   uint4* q16 = static_cast<uint4*>(Q16);
   uint4* do16 = static_cast<uint4*>(dO16);
   if (!lay.packed) {
-    attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, q, o, olo, g, D, tilemax, acc, q16,
-                                                                  do16, status);
+    attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, lay.sq, lay.so, lay.sdo, q, o, olo, g,
+                                                                  D, tilemax, acc, q16, do16, status);
   } else {
     PrepPacked rm;
     rm.n_q = sh.n_q;
     rm.Hq = sh.Hq;
     rm.total_q = lay.total_q;
+    rm.sq = lay.sq;
+    rm.so = lay.so;
+    rm.sdo = lay.sdo;
     for (int b = 0; b <= sh.B; ++b) rm.cu_q[b] = lay.cu_q[b];
     attn_bwd_preprocess_packed_kernel<DV, DH><<<grid, 256, 0, stream>>>(rm, nqt, q, o, olo, g, D, tilemax, acc,
                                                                         q16, do16, status);
@@ -1276,11 +1308,15 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
-                                     cudaStream_t stream) {
+cudaError_t launch_attn_bwd_finalize(int64_t elems, int dh, int n_inner, int64_t s_outer, int64_t s_inner,
+                                     bool contiguous, float scale, const float* dQacc, void* dQ, cudaStream_t stream) {
   const int64_t n8 = elems / 8;
-  attn_bwd_finalize_kernel<<<grid_for(n8), 256, 0, stream>>>(n8, scale, reinterpret_cast<const float4*>(dQacc),
-                                                           static_cast<uint4*>(dQ));
+  if (contiguous)
+    attn_bwd_finalize_kernel<<<grid_for(n8), 256, 0, stream>>>(n8, scale, reinterpret_cast<const float4*>(dQacc),
+                                                             static_cast<uint4*>(dQ));
+  else
+    attn_bwd_finalize_strided_kernel<<<grid_for(n8), 256, 0, stream>>>(
+        n8, dh / 8, n_inner, s_outer, s_inner, scale, reinterpret_cast<const float4*>(dQacc), static_cast<uint4*>(dQ));
   return cudaGetLastError();
 }
 

@@ -421,7 +421,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // O = 2^-E acc / l (the weights of tile j were scaled by 2^(E - v_j)).
         const float inv_l = l_sum > 0.f ? exp2_int(-vref) / l_sum : 0.f;
         const bool in_range = i < query_len(p.mask, p.sh.n_q, b);
-        const int64_t row_off = q_row(PACKED, p.lay, p.sh.Hq, p.sh.n_q, b, r, i) * DV;
+        const int64_t row_off = strided_off(PACKED, p.lay.so, p.sh.Hq, p.lay.cu_q[b], b, r, i);
         uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + row_off);
         uint4* lorow = p.O_lo ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O_lo) + row_off) : nullptr;
 #pragma unroll
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(256) attn_v16_kernel(const __grid_constant__ V
     const int64_t jr = j0 + k / kCpr;
     v[i] = make_uint4(0u, 0u, 0u, 0u);
     if (jr < klen) {
-      v[i] = V[k_row(PACKED, p.lay, p.sh.Hkv, p.sh.n_k, b, h, jr) * kCpr + k % kCpr];
+      v[i] = V[strided_off(PACKED, p.lay.sv, p.sh.Hkv, p.lay.cu_k[b], b, h, jr) / 8 + k % kCpr];
       m = bf16_absmax_fold(m, v[i]);
     }
   }

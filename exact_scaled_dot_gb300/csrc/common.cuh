@@ -111,12 +111,31 @@ __host__ __device__ __forceinline__ int64_t first_row_seeing_key(const MaskParam
 // (cu[b] + i) H + h.  The backward's fp16 copy of Q and its fp32 dQ
 // accumulator follow the layout of Q; LSE and D are [B][H][n] (padded) or
 // [H][T] (packed).
+// Element strides of one user tensor (its innermost index, d, has stride 1):
+// `row` between consecutive rows of a head (tokens in the packed layout),
+// `head` between consecutive heads; in the padded layout the batch stride is
+// H head.  The workspace copies (fp16 Q and dO, the dQ accumulator) always use
+// the contiguous strides of the layout.
+struct TensorStrides {
+  int64_t row, head;
+};
+
 struct LayoutParams {
   int32_t packed;
   int32_t cu_q[ATTN_MAX_BATCH + 1];   // packed: first query token of sequence b
   int32_t cu_k[ATTN_MAX_BATCH + 1];   // packed: first key token of sequence b
   int64_t total_q;                    // packed: query tokens
+  // User tensors: Q, K, V, O (and O_lo), dO, dQ, dK, dV.
+  TensorStrides sq, sk, sv, so, sdo, sdq, sdk, sdv;
 };
+
+// Element offset of row i of (b, h) in a user tensor with strides `s` and H
+// heads (cu: the packed layout's first token of sequence b).
+__host__ __device__ __forceinline__ int64_t strided_off(bool packed, const TensorStrides& s, int H, int32_t cu, int b,
+                                                        int h, int64_t i) {
+  return packed ? (static_cast<int64_t>(cu) + i) * s.row + static_cast<int64_t>(h) * s.head
+                : (static_cast<int64_t>(b) * H + h) * s.head + i * s.row;
+}
 
 // The helpers take the layout kind as their first argument: the kernels are
 // compiled once per kind and pass it as a constant, so the padded layout's
@@ -251,7 +270,9 @@ cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap*
 // heads_b = 0: one tensor (xb, yb unused).
 cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w_hi,
                         const float* w_lo, int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream);
-cudaError_t launch_attn_bwd_finalize(int64_t elems, float scale, const float* dQacc, void* dQ,
-                                     cudaStream_t stream);
+// dQ = scale * accumulator (elems elements of rows of dh); contiguous dQ, or
+// row r at (r / n_inner) s_outer + (r % n_inner) s_inner.
+cudaError_t launch_attn_bwd_finalize(int64_t elems, int dh, int n_inner, int64_t s_outer, int64_t s_inner,
+                                     bool contiguous, float scale, const float* dQacc, void* dQ, cudaStream_t stream);
 
 }  // namespace esd

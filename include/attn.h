@@ -29,13 +29,14 @@
  * ("Chapter 31", section 3): every call checks this in closed form on the
  * host and returns ATTN_ERR_EMPTY_ROW before launching anything.
  *
- * Layout.  All tensors are contiguous, row-major, innermost index last:
+ * Layout.  Tensors are row-major with the innermost index last:
  *   Q, dQ   [B][Hq ][n_q][d_h]  bf16        K, dK [B][Hkv][n_k][d_h] bf16
  *   O, dO   [B][Hq ][n_q][d_v]  bf16        V, dV [B][Hkv][n_k][d_v] bf16
  *   LSE, D  [B][Hq ][n_q]       fp32
  * (the packed variable-length entry points below use token-major tensors).
- * Supported head widths (d_h, d_v): (64, 64), (128, 128), (128, 64).
- * Every tensor pointer must be 16-byte aligned.
+ * They are contiguous unless the call's attn_strides say otherwise (below);
+ * LSE is always contiguous.  Supported head widths (d_h, d_v): (64, 64),
+ * (128, 128), (128, 64).  Every tensor pointer must be 16-byte aligned.
  *
  * Ownership and execution.  The caller allocates and owns every buffer,
  * including the forward and backward workspaces; the library allocates no
@@ -83,7 +84,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 9
+#define ATTN_ABI_VERSION 10
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -132,6 +133,32 @@ typedef struct {
  * shape. */
 size_t attn_fwd_workspace_bytes(const attn_shape* shape);
 
+/* Element strides of one tensor whose innermost index (d) is contiguous:
+ * `row` = elements between consecutive rows of one head (between
+ * consecutive tokens in the packed layout), `head` = elements between
+ * consecutive heads.  In the padded layout [B][H][n][d] the batch stride is
+ * H * head: a tensor sliced along d, or with padded rows or heads, fits; a
+ * sequence-major [B][n][H][d] tensor does not and goes through the packed
+ * entry points (one sequence per batch element).  Both strides must be
+ * multiples of 8 (16-byte rows; ATTN_ERR_ALIGN otherwise) and at least d
+ * (ATTN_ERR_SHAPE).  {0, 0} means the contiguous strides of the layout. */
+typedef struct {
+  int64_t row, head;
+} attn_tensor_strides;
+
+/* Strides of a call's tensors ("Appendix A.10", section A.10.5: the
+ * B x H x n x d tensors and their head concatenation); NULL = every tensor
+ * contiguous.  O_lo has O's strides.  Every entry is checked, also those of
+ * tensors the call does not take ({0, 0} passes).  A Q, K or V that is a
+ * slice of one fused projection output [T][(Hq + 2 Hkv) d] (token stride
+ * (Hq + 2 Hkv) d, head stride d) is read in place by the packed entry
+ * points, and dQ, dK, dV may be written into the matching slices of one
+ * fused gradient buffer.  Output views must not overlap one another or an
+ * input; nothing outside a view is written. */
+typedef struct {
+  attn_tensor_strides q, k, v, o, dO, dq, dk, dv;
+} attn_strides;
+
 /* Forward pass (A.10.1-A.10.3).  Inputs Q, K, V (bf16, device); outputs
  * O (bf16) and LSE (fp32, natural log), both device, fully overwritten.
  * `workspace`: caller-owned device memory of at least
@@ -147,7 +174,7 @@ size_t attn_fwd_workspace_bytes(const attn_shape* shape);
  * key row; bf16 rounding of O alone then moves dQ and dK beyond the stated
  * tolerance (measured: up to 2.2x on the peaked cross-attention workload,
  * 4x on smaller peaked cases). */
-int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
+int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
              const void* Q, const void* K, const void* V,
              void* O, float* LSE, void* O_lo,
              void* workspace, size_t workspace_bytes, void* stream);
@@ -162,7 +189,7 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, float scale,
  * (O = sum_s exp(LSE_s - LSE) O_s, LSE = log sum_s exp(LSE_s)).
  * `workspace`: device memory of at least attn_fwd_decode_workspace_bytes()
  * bytes, 256-byte aligned (may be NULL when that is 0).  Returns
- * ATTN_ERR_UNSUPPORTED for n_q > 128 (use attn_fwd). */
+ * ATTN_ERR_UNSUPPORTED for n_q > 128 (use attn_fwd).  Tensors contiguous. */
 size_t attn_fwd_decode_workspace_bytes(const attn_shape* shape, const attn_mask* mask);
 int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
                     const void* Q, const void* K, const void* V,
@@ -193,7 +220,7 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * (exact at any scale, see Precision above), the weights A are rounded once
  * to fp16, and dS enters dK and dQ in fp16 scaled by a power of two derived
  * from a bound on |dS|. */
-int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
+int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
              const void* Q, const void* K, const void* V,
              const void* O, const void* O_lo, const void* dO, const float* LSE,
              void* dQ, void* dK, void* dV,
@@ -204,7 +231,7 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, float scale,
  * zeroed dQ accumulator and Q and dO re-encoded as fp16 with per-tile
  * exponents (see attn_bwd), all in `workspace`.  Q is the forward's bf16
  * query tensor, dO the bf16 upstream gradient. */
-int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O,
+int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const void* Q, const void* O,
                         const void* O_lo, const void* dO, void* workspace,
                         size_t workspace_bytes, void* stream);
 
@@ -213,13 +240,13 @@ int attn_bwd_preprocess(const attn_shape* shape, const void* Q, const void* O,
  * the workspace's fp16 copy (also written by stage 1), writes dK (scaled)
  * and dV (bf16) and adds the dS K products into the workspace's fp32 dQ
  * accumulator (zeroed by stage 1). */
-int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, float scale,
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
                   const void* K, const void* V, const float* LSE,
                   void* workspace, size_t workspace_bytes,
                   void* dK, void* dV, void* stream);
 
 /* Stage 3: dQ = scale * accumulator, rounded to bf16. */
-int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspace,
+int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, float scale, const void* workspace,
                       size_t workspace_bytes, void* dQ, void* stream);
 
 /* The backward pass without any device allocation, for callers that cannot
@@ -240,7 +267,7 @@ int attn_bwd_finalize(const attn_shape* shape, float scale, const void* workspac
  * buffer, whose contents persist between calls: the kernels clear what must
  * start at zero, but calls that overlap on the GPU race and must be
  * serialised by the caller. */
-int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, float scale,
+int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
                      const void* Q, const void* K, const void* V,
                      const void* O, const void* O_lo, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, void* stream);
@@ -290,14 +317,16 @@ int64_t attn_varlen_visible_pairs(const attn_varlen* v);
  * description is invalid. */
 size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v);
 
-int attn_fwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
+int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
+                    const void* V,
                     void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace of attn_bwd_varlen, about T_q*Hq*(6*d_h + 2*d_v + 4) bytes; 0 when the
  * description is invalid. */
 size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v);
 
-int attn_bwd_varlen(const attn_varlen* v, float scale, const void* Q, const void* K, const void* V,
+int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
+                    const void* V,
                     const void* O, const void* O_lo, const void* dO, const float* LSE,
                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
                     void* stream);

@@ -122,3 +122,31 @@ def compare_sampled(w: Workload, inp: Inputs, res: GpuResult, orc, n_rows=192, n
     for name in ("O", "LSE", "dQ", "dK", "dV"):
         t = getattr(res, name)
         assert bool(torch.isfinite(t).all()), f"{name} has non-finite entries"
+
+
+def varlen_reference(w, inp, orc):
+    """Oracle outputs packed token-major: O, LSE [Hq, T_q], dQ, dK, dV."""
+    import oracle
+    Q, K, V, G = (f64(x) for x in (inp.Q, inp.K, inp.V, inp.dO))
+    Tq, Tk = Q.shape[0], K.shape[0]
+    O = np.zeros((Tq, w.Hq, w.dv))
+    LSE = np.zeros((w.Hq, Tq))
+    dQ = np.zeros((Tq, w.Hq, w.dh))
+    dK = np.zeros((Tk, w.Hkv, w.dh))
+    dV = np.zeros((Tk, w.Hkv, w.dv))
+    for b in range(len(inp.lens_q)):
+        lq, lk = inp.lens_q[b], inp.lens_k[b]
+        q0, q1, k0, k1 = inp.cu_q[b], inp.cu_q[b + 1], inp.cu_k[b], inp.cu_k[b + 1]
+        if lq == 0:
+            continue            # no query sees these keys: dK = dV = 0
+        p = oracle.Problem(1, w.Hq, w.Hkv, lq, lk, w.dh, w.dv, causal=w.causal, offset=None, kv_len=None)
+        to_bhnd = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2)[None])  # noqa: E731  [n,H,d] -> [1,H,n,d]
+        Qb, Kb, Vb, Gb = to_bhnd(Q[q0:q1]), to_bhnd(K[k0:k1]), to_bhnd(V[k0:k1]), to_bhnd(G[q0:q1])
+        Ob, Lb = orc.forward(p, Qb, Kb, Vb)
+        dQb, dKb, dVb, _D, _C = orc.backward(p, Qb, Kb, Vb, Gb)
+        O[q0:q1] = Ob[0].transpose(1, 0, 2)
+        LSE[:, q0:q1] = Lb[0]
+        dQ[q0:q1] = dQb[0].transpose(1, 0, 2)
+        dK[k0:k1] = dKb[0].transpose(1, 0, 2)
+        dV[k0:k1] = dVb[0].transpose(1, 0, 2)
+    return O, LSE, dQ, dK, dV

@@ -7,6 +7,7 @@ import re
 from pathlib import Path
 
 import pytest
+import torch
 
 import exact_scaled_dot_gb300 as esd
 from exact_scaled_dot_gb300 import _binding as bnd
@@ -34,7 +35,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 9
+    assert esd.attn_abi_version() == 10
 
 
 def test_strerror_covers_every_code(lib):
@@ -44,10 +45,10 @@ def test_strerror_covers_every_code(lib):
     assert lib.attn_strerror(999).decode() == "unknown status"
 
 
-def _call_fwd(lib, shape, mask, scale=None, ptr=256, ws=256, ws_bytes=1 << 40):
+def _call_fwd(lib, shape, mask, scale=None, ptr=256, ws=256, ws_bytes=1 << 40, strides=None):
     p = ctypes.c_void_p(ptr)
     scale = 1.0 / math.sqrt(max(shape.d_h, 1)) if scale is None else scale
-    return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None,
+    return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None, strides,
                         ctypes.c_float(scale), p, p, p, p, p, None, ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes),
                         None)
 
@@ -133,7 +134,7 @@ def test_bwd_workspace_checks(lib):
                     + r256(rows * 128 * 2) + r256(rows * s.d_v * 2))
     p = ctypes.c_void_p(256)
     m = _mask()
-    args = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)] + [p] * 10
+    args = [ctypes.byref(s), ctypes.byref(m), None, ctypes.c_float(0.1)] + [p] * 10
     assert lib.attn_bwd(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
@@ -148,16 +149,16 @@ def test_bwd_requires_the_output_residual(lib):
     need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
     p = ctypes.c_void_p(256)
     m = _mask()
-    head = [ctypes.byref(s), ctypes.byref(m), ctypes.c_float(0.1)]
+    head = [ctypes.byref(s), ctypes.byref(m), None, ctypes.c_float(0.1)]
     # Q, K, V, O, O_lo = NULL, dO, LSE, dQ, dK, dV
     assert lib.attn_bwd(*head, p, p, p, p, None, p, p, p, p, p, p, ctypes.c_size_t(need),
                         None) == bnd.ATTN_ERR_NULL
-    assert lib.attn_bwd_preprocess(ctypes.byref(s), p, p, None, p, p, ctypes.c_size_t(need),
+    assert lib.attn_bwd_preprocess(ctypes.byref(s), None, p, p, None, p, p, ctypes.c_size_t(need),
                                    None) == bnd.ATTN_ERR_NULL
     assert lib.attn_bwd_noalloc(*head, p, p, p, p, None, p, p, p, p, p, None) == bnd.ATTN_ERR_NULL
     v = _varlen([0, 100], [0, 100])
     vneed = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v))
-    assert lib.attn_bwd_varlen(ctypes.byref(v), ctypes.c_float(0.1), p, p, p, p, None, p, p, p, p, p, p,
+    assert lib.attn_bwd_varlen(ctypes.byref(v), None, ctypes.c_float(0.1), p, p, p, p, None, p, p, p, p, p, p,
                                ctypes.c_size_t(vneed), None) == bnd.ATTN_ERR_NULL
 
 
@@ -220,8 +221,8 @@ def test_varlen_checks(lib):
     before any CUDA call."""
     p = ctypes.c_void_p(256)
     big = ctypes.c_size_t(1 << 40)
-    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), ctypes.c_float(0.1), p, p, p, p, p, None, p, big,  # noqa: E731
-                                        None)
+    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), None, ctypes.c_float(0.1), p, p, p, p, p, None, p,  # noqa: E731
+                                        big, None)
     assert fwd(_varlen([1, 3], [0, 3])) == bnd.ATTN_ERR_SHAPE          # cu[0] != 0
     assert fwd(_varlen([0, 5, 3], [0, 5, 6])) == bnd.ATTN_ERR_SHAPE    # decreasing
     assert fwd(_varlen([0, 3], [0, 0])) == bnd.ATTN_ERR_EMPTY_ROW      # queries, no keys
@@ -230,19 +231,19 @@ def test_varlen_checks(lib):
     assert fwd(_varlen([0, 3], [0, 3], Hq=3)) == bnd.ATTN_ERR_SHAPE
     assert fwd(_varlen([0, 3], [0, 3], d_h=96, d_v=96)) == bnd.ATTN_ERR_UNSUPPORTED
     assert fwd(_varlen([0, 3], [0, 3], B=0)) == bnd.ATTN_ERR_SHAPE
-    assert lib.attn_fwd_varlen(None, ctypes.c_float(0.1), p, p, p, p, p, None, p, big, None) == bnd.ATTN_ERR_NULL
-    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), ctypes.c_float(0.0), p, p, p, p, p, None,
+    assert lib.attn_fwd_varlen(None, None, ctypes.c_float(0.1), p, p, p, p, p, None, p, big, None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), None, ctypes.c_float(0.0), p, p, p, p, p, None,
                                p, big, None) == bnd.ATTN_ERR_SCALE
-    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), ctypes.c_float(0.1), p, p, p,
+    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), None, ctypes.c_float(0.1), p, p, p,
                                ctypes.c_void_p(0x1008), p, None, p, big, None) == bnd.ATTN_ERR_ALIGN
     # the forward workspace: present, aligned, large enough
     v3 = _varlen([0, 3, 200], [0, 3, 300])
     need = lib.attn_fwd_varlen_workspace_bytes(ctypes.byref(v3))
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
     assert need == r256(2 * 2 * 3 * 128 * 128 * 2) + r256(2 * 2 * 3 * 4)   # B Hkv ceil(297/128) tiles
-    assert lib.attn_fwd_varlen(ctypes.byref(v3), ctypes.c_float(0.1), p, p, p, p, p, None, None, ctypes.c_size_t(need),
-                               None) == bnd.ATTN_ERR_WORKSPACE
-    assert lib.attn_fwd_varlen(ctypes.byref(v3), ctypes.c_float(0.1), p, p, p, p, p, None, p,
+    assert lib.attn_fwd_varlen(ctypes.byref(v3), None, ctypes.c_float(0.1), p, p, p, p, p, None, None,
+                               ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
+    assert lib.attn_fwd_varlen(ctypes.byref(v3), None, ctypes.c_float(0.1), p, p, p, p, p, None, p,
                                ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     # no query rows at all: nothing to compute, OK without touching the GPU
     assert fwd(_varlen([0, 0, 0], [0, 4, 9])) == bnd.ATTN_OK
@@ -258,7 +259,7 @@ def test_varlen_workspace_and_pairs(lib):
     assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 16) + r256(3 * 2 * 8) + r256(rows * 128 * 4)
                     + r256(rows * 128 * 2) + r256(rows * 64 * 2))
     p = ctypes.c_void_p(512)
-    args = [ctypes.byref(v), ctypes.c_float(0.1)] + [p] * 10
+    args = [ctypes.byref(v), None, ctypes.c_float(0.1)] + [p] * 10
     assert lib.attn_bwd_varlen(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_varlen(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_varlen(*args, p, ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
@@ -326,3 +327,59 @@ def test_rope_qk_checks(lib):
     assert call(pos=None) == bnd.ATTN_ERR_NULL
     assert call(yk=None) == bnd.ATTN_ERR_NULL
     assert call(xk=ctypes.c_void_p(0x1008)) == bnd.ATTN_ERR_ALIGN
+
+
+def _strides(**kw):
+    st = bnd.AttnStrides()
+    for name, (row, head) in kw.items():
+        setattr(st, name, bnd.AttnTensorStrides(row, head))
+    return st
+
+
+def test_strides_validated(lib):
+    """attn_strides: element strides that are multiples of 8 (16-byte rows for
+    the tensor-memory copies) and at least d; {0, 0} is the contiguous
+    default.  Checked before any CUDA call."""
+    s = _shape()
+    bad_align = _strides(q=(136, 100 * 136 + 4))
+    assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(bad_align)) == bnd.ATTN_ERR_ALIGN
+    assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(_strides(k=(12, 1200)))) == bnd.ATTN_ERR_ALIGN
+    assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(_strides(v=(64, 64 * 100)))) == bnd.ATTN_ERR_SHAPE
+    assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(_strides(o=(128, 64)))) == bnd.ATTN_ERR_SHAPE
+    assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(_strides(q=(128, 1 << 40)))) == bnd.ATTN_ERR_SHAPE
+    # a bad stride of a tensor the forward does not take is still a bad argument
+    assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(_strides(dk=(8, 8)))) == bnd.ATTN_ERR_SHAPE
+    v = _varlen([0, 100], [0, 100])
+    p = ctypes.c_void_p(256)
+    rc = lib.attn_fwd_varlen(ctypes.byref(v), ctypes.byref(_strides(q=(3 * 128 + 4, 128))), ctypes.c_float(0.1),
+                             p, p, p, p, p, None, p, ctypes.c_size_t(1 << 40), None)
+    assert rc == bnd.ATTN_ERR_ALIGN
+
+
+def test_binding_reads_view_strides():
+    """The binding passes a view's element strides: Q, K, V sliced out of one
+    fused [T, (Hq + 2 Hkv) d] projection output (packed), and head-major
+    views with a padded row (padded); contiguous tensors give NULL."""
+    T, Hq, Hkv, d = 10, 4, 2, 128
+    qkv = torch.empty((T, (Hq + 2 * Hkv) * d), dtype=torch.bfloat16)
+    Q = qkv[:, :Hq * d].view(T, Hq, d)
+    K = qkv[:, Hq * d:(Hq + Hkv) * d].view(T, Hkv, d)
+    V = qkv[:, (Hq + Hkv) * d:].view(T, Hkv, d)
+    ref = bnd._strides_arg(True, q=Q, k=K, v=V).contents
+    for t in (ref.q, ref.k, ref.v):
+        assert (t.row, t.head) == ((Hq + 2 * Hkv) * d, d)
+    assert (ref.o.row, ref.o.head) == (0, 0)
+    assert bnd._strides_arg(True, q=Q.contiguous()) is None
+    B, H, n = 2, 3, 50
+    big = torch.empty((B, H, n, 192), dtype=torch.bfloat16)
+    X = big[..., :128]
+    pst = bnd._strides_arg(False, dO=X).contents
+    assert (pst.dO.row, pst.dO.head) == (192, n * 192)
+    # sequence-major [B, n, H, d] seen as [B, H, n, d]: head-major batch stride fails
+    seq = torch.empty((B, n, H, 128), dtype=torch.bfloat16).transpose(1, 2)
+    with pytest.raises(ValueError):
+        bnd._strides_arg(False, q=seq)
+    # ... but one batch element of it is a valid padded view
+    one = torch.empty((1, n, H, 128), dtype=torch.bfloat16).transpose(1, 2)
+    pst = bnd._strides_arg(False, q=one).contents
+    assert (pst.q.row, pst.q.head) == (H * 128, 128)

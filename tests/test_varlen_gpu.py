@@ -12,13 +12,12 @@ chunks over a history, a sequence with no queries (its keys get dK = dV = 0),
 d_v = 64 with a peaked softmax, and a single sequence checked against the
 padded [B][H][n][d] entry points.
 """
-import numpy as np
 import pytest
 import torch
 
 from exact_scaled_dot_gb300.inputs import VarlenWorkload, make_varlen_inputs
 
-from _attn_cases import LSE_ATOL, assert_close, f64
+from _attn_cases import LSE_ATOL, assert_close, f64, varlen_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -51,34 +50,6 @@ CASES = {
 }
 
 
-def _reference(w: VarlenWorkload, inp, orc):
-    """Oracle outputs packed token-major: O, LSE [Hq, T_q], dQ, dK, dV."""
-    import oracle
-    Q, K, V, G = (f64(x) for x in (inp.Q, inp.K, inp.V, inp.dO))
-    Tq, Tk = Q.shape[0], K.shape[0]
-    O = np.zeros((Tq, w.Hq, w.dv))
-    LSE = np.zeros((w.Hq, Tq))
-    dQ = np.zeros((Tq, w.Hq, w.dh))
-    dK = np.zeros((Tk, w.Hkv, w.dh))
-    dV = np.zeros((Tk, w.Hkv, w.dv))
-    for b in range(len(inp.lens_q)):
-        lq, lk = inp.lens_q[b], inp.lens_k[b]
-        q0, q1, k0, k1 = inp.cu_q[b], inp.cu_q[b + 1], inp.cu_k[b], inp.cu_k[b + 1]
-        if lq == 0:
-            continue            # no query sees these keys: dK = dV = 0
-        p = oracle.Problem(1, w.Hq, w.Hkv, lq, lk, w.dh, w.dv, causal=w.causal, offset=None, kv_len=None)
-        to_bhnd = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2)[None])  # noqa: E731  [n,H,d] -> [1,H,n,d]
-        Qb, Kb, Vb, Gb = to_bhnd(Q[q0:q1]), to_bhnd(K[k0:k1]), to_bhnd(V[k0:k1]), to_bhnd(G[q0:q1])
-        Ob, Lb = orc.forward(p, Qb, Kb, Vb)
-        dQb, dKb, dVb, _D, _C = orc.backward(p, Qb, Kb, Vb, Gb)
-        O[q0:q1] = Ob[0].transpose(1, 0, 2)
-        LSE[:, q0:q1] = Lb[0]
-        dQ[q0:q1] = dQb[0].transpose(1, 0, 2)
-        dK[k0:k1] = dKb[0].transpose(1, 0, 2)
-        dV[k0:k1] = dVb[0].transpose(1, 0, 2)
-    return O, LSE, dQ, dK, dV
-
-
 def _run(w: VarlenWorkload, inp, dev="cuda:0"):
     import exact_scaled_dot_gb300 as esd
     Q, K, V, G = (x.to(dev) for x in (inp.Q, inp.K, inp.V, inp.dO))
@@ -99,7 +70,7 @@ def test_varlen_matches_oracle(orc, name):
     w = CASES[name]
     inp = make_varlen_inputs(w)
     O, LSE, dQ, dK, dV = _run(w, inp)
-    rO, rL, rdQ, rdK, rdV = _reference(w, inp, orc)
+    rO, rL, rdQ, rdK, rdV = varlen_reference(w, inp, orc)
     assert_close(f64(O), rO, "O")
     assert_close(f64(LSE), rL, "LSE", atol=LSE_ATOL, rtol=0.0)
     assert_close(f64(dQ), rdQ, "dQ")
