@@ -233,7 +233,7 @@ class AttnStep:
     calls (the forward, then the backward's three stages), with optional
     CUDA events between the calls."""
 
-    def __init__(self, esd, w, inp, dev):
+    def __init__(self, esd, w, inp, dev, rotary=False, keep_rotated=False):
         import torch
         self.esd, self.w = esd, w
         self.kv = None if inp.kv_len is None else inp.kv_len.tolist()
@@ -250,8 +250,15 @@ class AttnStep:
         self.O_lo = torch.empty_like(self.O)
         self.dQ, self.dK, self.dV = torch.empty_like(self.Q), torch.empty_like(self.K), torch.empty_like(self.V)
         dims = (w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv)
-        self.fws = torch.empty((esd.attn_fwd_workspace_bytes(*dims),), dtype=torch.uint8, device=dev)
-        self.ws = torch.empty((esd.attn_bwd_workspace_bytes(*dims),), dtype=torch.uint8, device=dev)
+        # Rotary: every row at its sequence position (queries at the end of
+        # the keys when n_q < n_k), the rotation fused into the calls.
+        self.rot = None
+        if rotary:
+            pk = torch.arange(w.nk, dtype=torch.int32, device=dev).expand(w.B, w.nk).contiguous()
+            kept = (torch.empty_like(self.Q), torch.empty_like(self.K)) if keep_rotated else (None, None)
+            self.rot = esd.Rotary(pk[:, w.nk - w.nq:].contiguous(), pk, base=10000.0, q_rot=kept[0], k_rot=kept[1])
+        self.fws = torch.empty((esd.attn_fwd_workspace_bytes(*dims, rotary=self.rot),), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty((esd.attn_bwd_workspace_bytes(*dims, rotary=self.rot),), dtype=torch.uint8, device=dev)
         self.rows = w.B * w.Hq * w.nq
 
     def tensors(self):
@@ -266,19 +273,31 @@ class AttnStep:
         if ev is not None:
             ev[0].record(stream)
         esd.attn_fwd(self.Q, self.K, self.V, scale=self.scale, O=self.O, LSE=self.LSE, O_lo=self.O_lo,
-                     workspace=self.fws, stream=stream, **self.mask)
+                     rotary=self.rot, workspace=self.fws, stream=stream, **self.mask)
         if ev is not None:
             ev[1].record(stream)
-        esd.attn_bwd_preprocess(self.Q, self.O, self.dO, self.ws, shape=self.shape, O_lo=self.O_lo, stream=stream)
+        esd.attn_bwd_preprocess(self.Q, self.O, self.dO, self.ws, shape=self.shape, O_lo=self.O_lo, rotary=self.rot,
+                                stream=stream)
         if ev is not None:
             ev[2].record(stream)
         esd.attn_bwd_main(self.K, self.V, self.LSE, self.ws, self.dK, self.dV, shape=self.shape, scale=self.scale,
-                          stream=stream, **self.mask)
+                          rotary=self.rot, stream=stream, **self.mask)
         if ev is not None:
             ev[3].record(stream)
-        esd.attn_bwd_finalize(self.ws, self.dQ, shape=self.shape, scale=self.scale, stream=stream)
+        esd.attn_bwd_finalize(self.ws, self.dQ, shape=self.shape, scale=self.scale, rotary=self.rot, stream=stream)
         if ev is not None:
             ev[4].record(stream)
+
+    def composite(self, stream):
+        """The same step through the composite backward call (one call for
+        the three stages; with a rotary, one preparation launch for both
+        tables and the rotated keys instead of one per stage)."""
+        esd = self.esd
+        esd.attn_fwd(self.Q, self.K, self.V, scale=self.scale, O=self.O, LSE=self.LSE, O_lo=self.O_lo,
+                     rotary=self.rot, workspace=self.fws, stream=stream, **self.mask)
+        esd.attn_bwd(self.Q, self.K, self.V, self.O, self.dO, self.LSE, O_lo=self.O_lo, scale=self.scale,
+                     dQ=self.dQ, dK=self.dK, dV=self.dV, rotary=self.rot, workspace=self.ws, stream=stream,
+                     **self.mask)
 
     def io_bytes(self):
         """Algorithmic bytes of the two memory-bound backward kernels: one read
@@ -314,7 +333,7 @@ def time_steps(step, stream, dev, steps, flush=None):
     return per, total
 
 
-def config_line(esd, name, dev, steps, warmup, peaks):
+def config_line(esd, name, dev, steps, warmup, peaks, rotary=False):
     """One configuration timed on its own: per-stage times, TFLOP/s, fraction
     of the measured bf16 burst peak (the stages are timed in sub-second
     regions), and for the tiny single-head case the HBM view and a CUDA-graph
@@ -322,7 +341,7 @@ def config_line(esd, name, dev, steps, warmup, peaks):
     import torch
     from exact_scaled_dot_gb300.inputs import WORKLOADS, make_inputs
     w = WORKLOADS[name]
-    st = AttnStep(esd, w, make_inputs(w), dev)
+    st = AttnStep(esd, w, make_inputs(w), dev, rotary=rotary)
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
         st(stream)
@@ -332,7 +351,8 @@ def config_line(esd, name, dev, steps, warmup, peaks):
     per, total = time_steps(st, stream, dev, steps, flush)
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     value = (st.flops_fwd + st.flops_bwd) / (total * 1e-3) / 1e12
-    out = {"workload": name, "steps": steps, "ms_per_step": total, "tflops": value, "frac": value / peak,
+    out = {"workload": name + ("+rotary" if rotary else ""), "steps": steps, "ms_per_step": total, "tflops": value,
+           "frac": value / peak,
            "peak_kind": "bf16_tflops burst", "visible_pairs": st.pairs,
            "l2": "flushed between steps" if small else "inputs larger than L2",
            "stages": {}}
@@ -389,6 +409,49 @@ def config_line(esd, name, dev, steps, warmup, peaks):
     return out
 
 
+def rotary_cost(esd, name, dev, steps, reps=3):
+    """The same workload without and with the fused rotary embedding, each a
+    forward and the composite backward call, timed alternately (reps rounds
+    of `steps` steps, the fastest round kept): the step-time overhead of
+    rotating Q and K inside the calls, with the forward's rotated rows kept
+    for the backward (q_rot, k_rot) and without them (the backward rotates
+    again)."""
+    import torch
+    from exact_scaled_dot_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    stream = torch.cuda.current_stream(dev)
+    best = {}
+    modes = {"plain": dict(rotary=False), "kept": dict(rotary=True, keep_rotated=True),
+             "recomputed": dict(rotary=True)}
+    for _ in range(reps):
+        for rot, kw in modes.items():
+            st = AttnStep(esd, w, inp, dev, **kw)
+            for _ in range(3):
+                st.composite(stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            for _ in range(steps):
+                st.composite(stream)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = a.elapsed_time(b) / steps
+            best[rot] = min(best.get(rot, float("inf")), ms)
+            del st
+            torch.cuda.empty_cache()
+    status = esd.attn_get_status()
+    if status != 0:
+        raise RuntimeError(f"rotary cost: device status {status}: {esd.strerror(status)}")
+    return {"workload": name, "calls": "attn_fwd + attn_bwd (composite)", "steps": steps, "rounds": reps,
+            "plain_ms_per_step": best["plain"], "rotary_ms_per_step": best["kept"],
+            "overhead": best["kept"] / best["plain"] - 1.0,
+            "recomputed_ms_per_step": best["recomputed"],
+            "overhead_recomputed": best["recomputed"] / best["plain"] - 1.0,
+            "launches_per_step": {"plain": LAUNCHES_PER_STEP, "kept": LAUNCHES_PER_STEP,
+                                  "recomputed": LAUNCHES_PER_STEP + 1}}
+
+
 def run_cuda(args):
     import numpy as np
     import torch
@@ -413,7 +476,7 @@ def run_cuda(args):
     if args.batch is not None:
         w = w.scaled(B=args.batch)
     inp = make_inputs(w)
-    st = AttnStep(esd, w, inp, dev)
+    st = AttnStep(esd, w, inp, dev, rotary=args.rotary)
     kv, mask, scale, shape = st.kv, st.mask, st.scale, st.shape
     off = mask["causal_offset"]
     pairs, flops_fwd, flops_bwd = st.pairs, st.flops_fwd, st.flops_bwd
@@ -426,7 +489,7 @@ def run_cuda(args):
     def step(ev=None):
         st(stream, ev)
 
-    launches_per_step = LAUNCHES_PER_STEP
+    launches_per_step = LAUNCHES_PER_STEP + (3 if args.rotary else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -618,6 +681,7 @@ def run_cuda(args):
             if name == w.name:
                 continue
             configs[name] = config_line(esd, name, dev, args.config_steps, 3, peaks)
+        configs["rotary_cost"] = rotary_cost(esd, w.name, dev, args.config_steps)
 
     if rank == 0:
         line = {
@@ -627,6 +691,7 @@ def run_cuda(args):
             "data": "synthetic (seeded N(0,1) draws rounded to bf16; random key lengths)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "n_q": w.nq, "n_k": w.nk,
                        "d_h": w.dh, "d_v": w.dv, "causal": w.causal, "kv_len": kv, "seed": w.seed,
+                       "rotary": bool(args.rotary),
                        "visible_pairs": pairs, "flops_per_step": flops_fwd + flops_bwd,
                        # The backward's five products cost 2(3 d_h + 2 d_v) per pair; the metric counts
                        # 2(2 d_h + 3 d_v).  Equal for d_h = d_v.
@@ -1049,6 +1114,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-oracle", action="store_true", help="skip the parity spot check and CPU baseline")
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other configurations")
+    ap.add_argument("--rotary", action="store_true",
+                    help="headline step with the rotary embedding fused into the calls")
     ap.add_argument("--config-steps", type=int, default=20, help="timed steps per other configuration")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:

@@ -72,6 +72,11 @@ class AttnStrides(ctypes.Structure):
     _fields_ = [(n, AttnTensorStrides) for n in ("q", "k", "v", "o", "dO", "dq", "dk", "dv")]
 
 
+class AttnRotary(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_float), ("pos_q", ctypes.c_void_p), ("pos_k", ctypes.c_void_p),
+                ("q_rot", ctypes.c_void_p), ("k_rot", ctypes.c_void_p)]
+
+
 class AttnVarlen(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d_h", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("causal", ctypes.c_int32),
@@ -93,20 +98,21 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(str(p))
     S, M = ctypes.POINTER(AttnShape), ctypes.POINTER(AttnMask)
     ST = ctypes.POINTER(AttnStrides)
+    RT = ctypes.POINTER(AttnRotary)
     f = ctypes.c_float
-    lib.attn_fwd.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    lib.attn_fwd_workspace_bytes.argtypes = [S]
+    lib.attn_fwd.argtypes = [S, M, ST, RT, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd_workspace_bytes.argtypes = [S, RT]
     lib.attn_fwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_decode.argtypes = [S, M, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.attn_fwd_decode_workspace_bytes.argtypes = [S, M]
     lib.attn_fwd_decode_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd_workspace_bytes.argtypes = [S]
+    lib.attn_bwd_workspace_bytes.argtypes = [S, RT]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+    lib.attn_bwd.argtypes = [S, M, ST, RT, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                              _vp]
-    lib.attn_bwd_preprocess.argtypes = [S, ST, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    lib.attn_bwd_main.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
-    lib.attn_bwd_finalize.argtypes = [S, ST, f, _vp, ctypes.c_size_t, _vp, _vp]
+    lib.attn_bwd_preprocess.argtypes = [S, ST, RT, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd_main.argtypes = [S, M, ST, RT, f, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
+    lib.attn_bwd_finalize.argtypes = [S, ST, RT, f, _vp, ctypes.c_size_t, _vp, _vp]
     lib.attn_visible_pairs.argtypes = [S, M]
     lib.attn_visible_pairs.restype = ctypes.c_int64
     lib.attn_get_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -115,19 +121,19 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_strerror.argtypes = [ctypes.c_int]
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_abi_version.restype = ctypes.c_int
-    lib.attn_bwd_noalloc.argtypes = [S, M, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.attn_bwd_noalloc.argtypes = [S, M, ST, RT, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.attn_bwd_noalloc.restype = ctypes.c_int
     lib.attn_bwd_noalloc_max_scratch_bytes.argtypes = []
     lib.attn_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
     VL = ctypes.POINTER(AttnVarlen)
     lib.attn_varlen_visible_pairs.argtypes = [VL]
     lib.attn_varlen_visible_pairs.restype = ctypes.c_int64
-    lib.attn_fwd_varlen.argtypes = [VL, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    lib.attn_fwd_varlen_workspace_bytes.argtypes = [VL]
+    lib.attn_fwd_varlen.argtypes = [VL, ST, RT, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd_varlen_workspace_bytes.argtypes = [VL, RT]
     lib.attn_fwd_varlen_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd_varlen_workspace_bytes.argtypes = [VL]
+    lib.attn_bwd_varlen_workspace_bytes.argtypes = [VL, RT]
     lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
-    lib.attn_bwd_varlen.argtypes = [VL, ST, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+    lib.attn_bwd_varlen.argtypes = [VL, ST, RT, f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                     _vp]
     i64, i32 = ctypes.c_int64, ctypes.c_int32
     lib.attn_proj_fwd.argtypes = [i64, i32, i32, _vp, _vp, _vp, _vp]
@@ -181,6 +187,46 @@ class _MaskArg:
             kv = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
         off = ATTN_OFFSET_DEFAULT if causal_offset is None else int(causal_offset)
         self.mask = AttnMask(1 if causal else 0, 0, off, kv)
+
+
+class Rotary:
+    """Rotary position embedding fused into the attention calls (attn_rotary):
+    pos_q, pos_k are int32 device tensors with the position of every query /
+    key row ([B, n_q] and [B, n_k] for the padded calls, [T_q] and [T_k] for
+    the packed ones); base sets the frequencies base^(-2k/d_h).
+
+    q_rot, k_rot (optional): bf16 tensors shaped like contiguous Q and K
+    that the forward fills with the rotated rows and the backward then reads
+    instead of rotating again (keep them between the two calls)."""
+
+    def __init__(self, pos_q: torch.Tensor, pos_k: torch.Tensor, base: float = 10000.0,
+                 q_rot: Optional[torch.Tensor] = None, k_rot: Optional[torch.Tensor] = None):
+        self.pos_q, self.pos_k, self.base = pos_q, pos_k, float(base)
+        self.q_rot, self.k_rot = q_rot, k_rot
+
+    def check(self, q_shape, k_shape, device, Q=None, K=None):
+        for t, name, shp in ((self.pos_q, "pos_q", q_shape), (self.pos_k, "pos_k", k_shape)):
+            _check_tensor(t, name, torch.int32, shp, device)
+        for t, name, ref in ((self.q_rot, "q_rot", Q), (self.k_rot, "k_rot", K)):
+            if t is not None and ref is not None:
+                _check_tensor(t, name, torch.bfloat16, tuple(ref.shape), device)
+
+    def arg(self):
+        r = AttnRotary(self.base, self.pos_q.data_ptr(), self.pos_k.data_ptr(),
+                       None if self.q_rot is None else self.q_rot.data_ptr(),
+                       None if self.k_rot is None else self.k_rot.data_ptr())
+        return ctypes.pointer(r)
+
+
+# Stands in for a Rotary without caller buffers where only its presence
+# matters (workspace sizes).
+_SIZE_ONLY_ROTARY = AttnRotary(10000.0, 4, 4, None, None)
+
+
+def _rot_size_arg(rotary):
+    if isinstance(rotary, Rotary):
+        return rotary.arg()
+    return ctypes.pointer(_SIZE_ONLY_ROTARY) if rotary else None
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -278,16 +324,20 @@ def _check_qkv(Q, K, V, strided: bool = True):
 # ---------------------------------------------------------------------------
 # Public functions (names follow the C ABI)
 # ---------------------------------------------------------------------------
-def attn_fwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
+def attn_fwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, rotary=None) -> int:
+    """rotary: a Rotary (or True) when the forward will rotate; only its presence matters."""
     shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
-    return int(load().attn_fwd_workspace_bytes(ctypes.byref(shape)))
+    return int(load().attn_fwd_workspace_bytes(ctypes.byref(shape), _rot_size_arg(rotary)))
 
 
 def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
              causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
              O: Optional[torch.Tensor] = None, LSE: Optional[torch.Tensor] = None,
-             O_lo: Optional[torch.Tensor] = None, residual: bool = True, workspace=None, stream=None):
+             O_lo: Optional[torch.Tensor] = None, residual: bool = True, rotary: Optional[Rotary] = None,
+             workspace=None, stream=None):
     """Forward pass: returns (O [B,Hq,n_q,d_v] bf16, LSE [B,Hq,n_q] fp32, O_lo).
+
+    rotary: a Rotary to rotate Q and K by their positions inside the call.
 
     O_lo is the bf16 rounding residual of O (O + O_lo ~ the fp32 result), which
     the backward requires for its row term; it is None when ``residual`` is
@@ -308,11 +358,14 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool 
         _check_o_lo(O_lo, O, (B, Hq, n_q, d_v), dev)
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
+    if rotary is not None:
+        rotary.check((B, n_q), (B, n_k), dev, Q, K)
     if workspace is None:
-        need = int(load().attn_fwd_workspace_bytes(ctypes.byref(shape)))
+        need = int(load().attn_fwd_workspace_bytes(ctypes.byref(shape), _rot_size_arg(rotary)))
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     st = _strides_arg(False, q=Q, k=K, v=V, o=O)
-    rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(Q), _ptr(K),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_fwd(ctypes.byref(shape), ctypes.byref(m.mask), st, rt, ctypes.c_float(scale), _ptr(Q), _ptr(K),
                          _ptr(V), _ptr(O), _ptr(LSE), _ptr(O_lo), *_ws(workspace), _stream(dev, stream))
     _check(rc, "attn_fwd")
     return O, LSE, O_lo
@@ -357,13 +410,14 @@ def attn_fwd_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal
     return O, LSE, O_lo
 
 
-def attn_bwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v) -> int:
+def attn_bwd_workspace_bytes(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, rotary=None) -> int:
     shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
-    return int(load().attn_bwd_workspace_bytes(ctypes.byref(shape)))
+    return int(load().attn_bwd_workspace_bytes(ctypes.byref(shape), _rot_size_arg(rotary)))
 
 
 def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_offset: Optional[int] = None,
-             kv_len=None, scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+             kv_len=None, scale: Optional[float] = None, dQ=None, dK=None, dV=None, rotary: Optional[Rotary] = None,
+             workspace=None, stream=None):
     """Backward pass: returns (dQ, dK, dV) in bf16; dK, dV summed over each KV head's group.
 
     O_lo (the forward's residual) is required; without it the library
@@ -385,7 +439,9 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_off
     _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev, strided=True)
     _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev, strided=True)
     _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev, strided=True)
-    need = attn_bwd_workspace_bytes(*dims)
+    if rotary is not None:
+        rotary.check((B, n_q), (B, n_k), dev, Q, K)
+    need = attn_bwd_workspace_bytes(*dims, rotary=rotary)
     if workspace is None:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     if workspace.numel() * workspace.element_size() < need:
@@ -393,7 +449,8 @@ def attn_bwd(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False, causal_off
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
     st = _strides_arg(False, q=Q, k=K, v=V, o=O, dO=dO, dq=dQ, dk=dK, dv=dV)
-    rc = load().attn_bwd(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(Q), _ptr(K),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_bwd(ctypes.byref(shape), ctypes.byref(m.mask), st, rt, ctypes.c_float(scale), _ptr(Q), _ptr(K),
                          _ptr(V), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
                          _ptr(workspace),
                          ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
@@ -405,33 +462,38 @@ def _ws(workspace):
     return _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size())
 
 
-def attn_bwd_preprocess(Q, O, dO, workspace, *, shape: AttnShape, O_lo=None, stream=None):
+def attn_bwd_preprocess(Q, O, dO, workspace, *, shape: AttnShape, O_lo=None, rotary: Optional[Rotary] = None,
+                        stream=None):
     """Stage 1 of the backward (row terms, tile bounds, zeroed dQ accumulator, fp16 copies of Q and dO)."""
     if O_lo is not None and O_lo.stride() != O.stride():
         raise ValueError("O_lo must have the same strides as O")
     st = _strides_arg(False, q=Q, o=O, dO=dO)
-    rc = load().attn_bwd_preprocess(ctypes.byref(shape), st, _ptr(Q), _ptr(O), _ptr(O_lo), _ptr(dO),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_bwd_preprocess(ctypes.byref(shape), st, rt, _ptr(Q), _ptr(O), _ptr(O_lo), _ptr(dO),
                                     *_ws(workspace), _stream(O.device, stream))
     _check(rc, "attn_bwd_preprocess")
 
 
 def attn_bwd_main(K, V, LSE, workspace, dK, dV, *, shape: AttnShape, causal=False, causal_offset=None,
-                  kv_len=None, scale: Optional[float] = None, stream=None):
+                  kv_len=None, scale: Optional[float] = None, rotary: Optional[Rotary] = None, stream=None):
     """Stage 2 of the backward (the key-tile-stationary main kernel; Q and dO
     come from the fp16 copies stage 1 left in the workspace)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
     m = _MaskArg(causal, causal_offset, kv_len)
     st = _strides_arg(False, k=K, v=V, dk=dK, dv=dV)
-    rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(K),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_bwd_main(ctypes.byref(shape), ctypes.byref(m.mask), st, rt, ctypes.c_float(scale), _ptr(K),
                               _ptr(V), _ptr(LSE), *_ws(workspace), _ptr(dK), _ptr(dV), _stream(K.device, stream))
     _check(rc, "attn_bwd_main")
 
 
-def attn_bwd_finalize(workspace, dQ, *, shape: AttnShape, scale: Optional[float] = None, stream=None):
+def attn_bwd_finalize(workspace, dQ, *, shape: AttnShape, scale: Optional[float] = None,
+                      rotary: Optional[Rotary] = None, stream=None):
     """Stage 3 of the backward (dQ = scale * accumulator in bf16)."""
     scale = 1.0 / math.sqrt(shape.d_h) if scale is None else float(scale)
     st = _strides_arg(False, dq=dQ)
-    rc = load().attn_bwd_finalize(ctypes.byref(shape), st, ctypes.c_float(scale), *_ws(workspace), _ptr(dQ),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_bwd_finalize(ctypes.byref(shape), st, rt, ctypes.c_float(scale), *_ws(workspace), _ptr(dQ),
                                   _stream(dQ.device, stream))
     _check(rc, "attn_bwd_finalize")
 
@@ -461,7 +523,7 @@ def attn_selftest_wait_timeout(limit_ns: int, stream=None, device=None) -> None:
 
 def attn_bwd_noalloc(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False,
                      causal_offset: Optional[int] = None, kv_len=None, scale: Optional[float] = None,
-                     dQ=None, dK=None, dV=None, stream=None):
+                     dQ=None, dK=None, dV=None, rotary: Optional[Rotary] = None, stream=None):
     """Backward pass that allocates no device memory in the library.
 
     For callers that cannot allocate where they run the backward (memory owned
@@ -490,7 +552,10 @@ def attn_bwd_noalloc(Q, K, V, O, dO, LSE, *, O_lo=None, causal: bool = False,
     shape = make_shape(*dims)
     m = _MaskArg(causal, causal_offset, kv_len)
     st = _strides_arg(False, q=Q, k=K, v=V, o=O, dO=dO, dq=dQ, dk=dK, dv=dV)
-    rc = load().attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(m.mask), st, ctypes.c_float(scale), _ptr(Q),
+    if rotary is not None:
+        rotary.check((B, n_q), (B, n_k), dev, Q, K)
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(m.mask), st, rt, ctypes.c_float(scale), _ptr(Q),
                                  _ptr(K), _ptr(V), _ptr(O), _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
                                  _ptr(dV), _stream(dev, stream))
     _check(rc, "attn_bwd_noalloc")
@@ -543,13 +608,15 @@ def attn_varlen_visible_pairs(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, 
     return int(load().attn_varlen_visible_pairs(ctypes.byref(a.v)))
 
 
-def attn_fwd_varlen_workspace_bytes(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False) -> int:
+def attn_fwd_varlen_workspace_bytes(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False,
+                                    rotary=None) -> int:
     a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
-    return int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+    return int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v), _rot_size_arg(rotary)))
 
 
 def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False, scale: Optional[float] = None,
-                    O=None, LSE=None, O_lo=None, residual: bool = True, workspace=None, stream=None):
+                    O=None, LSE=None, O_lo=None, residual: bool = True, rotary: Optional[Rotary] = None,
+                    workspace=None, stream=None):
     """Forward over packed sequences: Q [T_q, Hq, d_h], K [T_k, Hkv, d_h], V [T_k, Hkv, d_v] (bf16);
     cu_seqlens_* are host offsets [B + 1].  Returns (O [T_q, Hq, d_v], LSE [Hq, T_q] fp32, O_lo)."""
     (Tq, Tk, Hq, Hkv, d_h, d_v), dev = _varlen_dims(Q, K, V)
@@ -567,23 +634,28 @@ def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False
     _check_tensor(LSE, "LSE", torch.float32, (Hq, Tq), dev)
     if O_lo is not None:
         _check_o_lo(O_lo, O, (Tq, Hq, d_v), dev)
+    if rotary is not None:
+        rotary.check((Tq,), (Tk,), dev, Q, K)
     if workspace is None:
-        need = int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+        need = int(load().attn_fwd_varlen_workspace_bytes(ctypes.byref(a.v), _rot_size_arg(rotary)))
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     st = _strides_arg(True, q=Q, k=K, v=V, o=O)
-    rc = load().attn_fwd_varlen(ctypes.byref(a.v), st, ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_fwd_varlen(ctypes.byref(a.v), st, rt, ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                 _ptr(LSE), _ptr(O_lo), *_ws(workspace), _stream(dev, stream))
     _check(rc, "attn_fwd_varlen")
     return O, LSE, O_lo
 
 
-def attn_bwd_varlen_workspace_bytes(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False) -> int:
+def attn_bwd_varlen_workspace_bytes(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, *, causal=False,
+                                    rotary=None) -> int:
     a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
-    return int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+    return int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v), _rot_size_arg(rotary)))
 
 
 def attn_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens_q, cu_seqlens_k, *, O_lo=None, causal: bool = False,
-                    scale: Optional[float] = None, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+                    scale: Optional[float] = None, dQ=None, dK=None, dV=None, rotary: Optional[Rotary] = None,
+                    workspace=None, stream=None):
     """Backward over packed sequences: returns (dQ, dK, dV), laid out like Q, K, V."""
     (Tq, Tk, Hq, Hkv, d_h, d_v), dev = _varlen_dims(Q, K, V)
     a = _VarlenArg(Hq, Hkv, d_h, d_v, cu_seqlens_q, cu_seqlens_k, causal)
@@ -601,13 +673,16 @@ def attn_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens_q, cu_seqlens_k, *, O_lo=Non
     _check_tensor(dQ, "dQ", torch.bfloat16, tuple(Q.shape), dev, strided=True)
     _check_tensor(dK, "dK", torch.bfloat16, tuple(K.shape), dev, strided=True)
     _check_tensor(dV, "dV", torch.bfloat16, tuple(V.shape), dev, strided=True)
-    need = int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v)))
+    if rotary is not None:
+        rotary.check((Tq,), (Tk,), dev, Q, K)
+    need = int(load().attn_bwd_varlen_workspace_bytes(ctypes.byref(a.v), _rot_size_arg(rotary)))
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace must hold at least {need} bytes")
     st = _strides_arg(True, q=Q, k=K, v=V, o=O, dO=dO, dq=dQ, dk=dK, dv=dV)
-    rc = load().attn_bwd_varlen(ctypes.byref(a.v), st, ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+    rt = None if rotary is None else rotary.arg()
+    rc = load().attn_bwd_varlen(ctypes.byref(a.v), st, rt, ctypes.c_float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                 _ptr(O_lo), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
                                 ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev, stream))
     _check(rc, "attn_bwd_varlen")

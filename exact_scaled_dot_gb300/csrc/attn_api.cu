@@ -369,6 +369,8 @@ int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq 
 // float4 [B*Hq*nqt] | per-group fp16 exponents float2 [B*Hkv] |
 // fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h] | fp16 copy
 // of dO [rows * d_v], each 256-byte aligned.
+// With a rotary, then the rotated keys bf16 [tokens_k Hkv][d_h]
+// (contiguous in the keys' layout).
 struct Workspace {
   float* D;
   float4* tilemax;
@@ -376,12 +378,22 @@ struct Workspace {
   float* dQacc;
   void* Q16;
   void* dO16;
+  void* Kr;
   size_t bytes;
+};
+
+// The rotary part of a workspace: tokens of the queries and keys (padded
+// B n, packed T), and which rotated rows live in the workspace (those
+// without a caller buffer).
+struct RotaryTokens {
+  bool on;
+  int64_t q, k;
+  bool q_ws, k_ws;
 };
 
 // rows: query rows over all heads (B Hq n_q padded, T_q Hq packed); the
 // tile bounds are indexed [B Hq][ceil(n_q / 128)] in both layouts.
-Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base) {
+Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base, const RotaryTokens& rt) {
   const size_t nqt = (static_cast<size_t>(s->n_q) + 127) / 128;
   const size_t tiles = static_cast<size_t>(s->B) * s->Hq * nqt;
   const size_t off_t = round256(rows * sizeof(float));
@@ -397,28 +409,49 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base) {
   w.dQacc = reinterpret_cast<float*>(b + off_a);
   w.Q16 = b + off_q;
   w.dO16 = b + off_o;
-  w.bytes = off_o + round256(rows * static_cast<size_t>(s->d_v) * 2);
+  size_t end = off_o + round256(rows * static_cast<size_t>(s->d_v) * 2);
+  w.Kr = nullptr;
+  if (rt.on && rt.k_ws) {
+    w.Kr = b + end;
+    end += round256(static_cast<size_t>(rt.k) * s->Hkv * s->d_h * 2);
+  }
+  w.bytes = end;
   return w;
 }
 
-Workspace workspace_layout(const attn_shape* s, void* base) {
-  return workspace_layout_rows(s, static_cast<size_t>(q_rows(s)), base);
+RotaryTokens rotary_tokens(const attn_rotary* r, int64_t q, int64_t k) {
+  return RotaryTokens{r != nullptr, q, k, r != nullptr && r->q_rot == nullptr, r != nullptr && r->k_rot == nullptr};
 }
 
-Workspace workspace_layout_varlen(const Varlen& v, void* base) {
-  return workspace_layout_rows(&v.shape, static_cast<size_t>(v.total_q) * v.shape.Hq, base);
+RotaryTokens padded_tokens(const attn_shape* s, const attn_rotary* r) {
+  return rotary_tokens(r, static_cast<int64_t>(s->B) * s->n_q, static_cast<int64_t>(s->B) * s->n_k);
+}
+
+RotaryTokens varlen_tokens(const Varlen& v, const attn_rotary* r) { return rotary_tokens(r, v.total_q, v.total_k); }
+
+Workspace workspace_layout(const attn_shape* s, void* base, const attn_rotary* r) {
+  return workspace_layout_rows(s, static_cast<size_t>(q_rows(s)), base, padded_tokens(s, r));
+}
+
+Workspace workspace_layout_varlen(const Varlen& v, void* base, const attn_rotary* r) {
+  return workspace_layout_rows(&v.shape, static_cast<size_t>(v.total_q) * v.shape.Hq, base, varlen_tokens(v, r));
 }
 
 // Forward workspace: the fp16 V tiles [B Hkv][nkt 128][d_v] | their
-// exponents int32 [B Hkv][nkt], each 256-byte aligned.
+// exponents int32 [B Hkv][nkt] | with a rotary, the rotated queries bf16
+// [tokens_q Hq][d_h] and keys [tokens_k Hkv][d_h] (contiguous in their
+// layouts) that have no caller buffer; each 256-byte aligned.  Qr, Kr point
+// at wherever the rotated rows go (a caller buffer or the workspace).
 struct FwdWorkspace {
   void* V16;
   int32_t* vexp;
+  void* Qr;
+  void* Kr;
   int nkt;
   size_t bytes;
 };
 
-FwdWorkspace fwd_workspace_layout(const attn_shape* s, void* base) {
+FwdWorkspace fwd_workspace_layout(const attn_shape* s, void* base, const RotaryTokens& rt) {
   FwdWorkspace w;
   w.nkt = (s->n_k + kTileN - 1) / kTileN;
   const size_t tiles = static_cast<size_t>(s->B) * s->Hkv * w.nkt;
@@ -426,20 +459,96 @@ FwdWorkspace fwd_workspace_layout(const attn_shape* s, void* base) {
   uint8_t* b = static_cast<uint8_t*>(base);
   w.V16 = b;
   w.vexp = reinterpret_cast<int32_t*>(b + v16);
-  w.bytes = v16 + round256(tiles * sizeof(int32_t));
+  size_t end = v16 + round256(tiles * sizeof(int32_t));
+  w.Qr = w.Kr = nullptr;
+  if (rt.on && rt.q_ws) {
+    w.Qr = b + end;
+    end += round256(static_cast<size_t>(rt.q) * s->Hq * s->d_h * 2);
+  }
+  if (rt.on && rt.k_ws) {
+    w.Kr = b + end;
+    end += round256(static_cast<size_t>(rt.k) * s->Hkv * s->d_h * 2);
+  }
+  w.bytes = end;
   return w;
 }
 
-int check_fwd_workspace(const attn_shape* s, const void* ws, size_t bytes) {
+int check_fwd_workspace(const attn_shape* s, const RotaryTokens& rt, const void* ws, size_t bytes) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_WORKSPACE;
-  if (bytes < fwd_workspace_layout(s, nullptr).bytes) return ATTN_ERR_WORKSPACE;
+  if (bytes < fwd_workspace_layout(s, nullptr, rt).bytes) return ATTN_ERR_WORKSPACE;
   return ATTN_OK;
 }
 
-// The fp16 V pre-pass and the forward kernel, both on `stream`.
+// A rotary description: base finite and > 1, both position arrays present
+// and 4-byte aligned.  NULL (no rotary) passes.
+int check_rotary(const attn_rotary* r) {
+  if (!r) return ATTN_OK;
+  if (!std::isfinite(r->base) || !(r->base > 1.f)) return ATTN_ERR_SCALE;
+  if (!r->pos_q || !r->pos_k) return ATTN_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(r->pos_q) & 3u) != 0 || (reinterpret_cast<uintptr_t>(r->pos_k) & 3u) != 0)
+    return ATTN_ERR_ALIGN;
+  if ((r->q_rot && !aligned16(r->q_rot)) || (r->k_rot && !aligned16(r->k_rot))) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+// Frequencies w_k = base^(-2k/d) in double, passed as fp32 pairs w_hi + w_lo
+// so that the rounding of w does not grow with the position.
+void rope_frequencies(float base, int d, float* w_hi, float* w_lo) {
+  for (int k = 0; k < d / 2; ++k) {
+    const double w = std::pow(static_cast<double>(base), -2.0 * k / d);
+    w_hi[k] = static_cast<float>(w);
+    w_lo[k] = static_cast<float>(w - static_cast<double>(w_hi[k]));
+  }
+}
+
+// One segment of rotated rows ahead of the attention kernels: `tokens`
+// rows of X's H heads at positions pos, written contiguous into Y (an empty
+// segment when Y is nullptr).
+RopeSegment rope_segment(int64_t tokens, int n, int H, const int32_t* pos, const void* X, const TensorStrides& sx,
+                         void* Y) {
+  RopeSegment g;
+  std::memset(&g, 0, sizeof(g));
+  g.tokens = Y ? tokens : 0;
+  g.n = n;
+  g.H = H;
+  g.pos = pos;
+  g.X = X;
+  g.sx = sx;
+  g.Y = Y;
+  return g;
+}
+
+RopePrepParams rotary_prep(const attn_rotary* r, int d, bool packed, const RopeSegment& a, const RopeSegment& b) {
+  RopePrepParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.d = d;
+  p.packed = packed ? 1 : 0;
+  p.seg[0] = a;
+  p.seg[1] = b;
+  rope_frequencies(r->base, d, p.w_hi, p.w_lo);
+  return p;
+}
+
+// Positions and frequencies for a kernel that turns rows itself.
+RotaryAngles rotary_angles(const attn_rotary* r, const int32_t* pos, int d) {
+  RotaryAngles a;
+  std::memset(&a, 0, sizeof(a));
+  a.pos = pos;
+  rope_frequencies(r->base, d, a.w_hi, a.w_lo);
+  return a;
+}
+
+int launch_rotary_prep(const RopePrepParams& p, cudaStream_t st) {
+  if (p.seg[0].tokens == 0 && p.seg[1].tokens == 0) return ATTN_OK;
+  return launch_rope_prep(p, st) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// The fp16 V pre-pass and the forward kernel, both on `stream`.  With a
+// rotary, the V pre-pass launch also writes the rotated queries and keys
+// (rp; tq and tk then describe those copies), in extra rows of blocks.
 int launch_forward(const attn_shape* shape, const MaskParams& mask, const LayoutParams& lay, float scale,
                    const CUtensorMap& tq, const CUtensorMap& tk, const void* V, const FwdWorkspace& w, void* O,
-                   float* LSE, void* O_lo, unsigned int* status, cudaStream_t st) {
+                   float* LSE, void* O_lo, const RopePrepParams* rp, unsigned int* status, cudaStream_t st) {
   CUtensorMap tv;
   if (!make_tmap(&tv, w.V16, shape->d_v, w.nkt * kTileN, static_cast<int64_t>(shape->B) * shape->Hkv))
     return ATTN_ERR_CUDA;
@@ -452,6 +561,17 @@ int launch_forward(const attn_shape* shape, const MaskParams& mask, const Layout
   vp.V16 = w.V16;
   vp.vexp = w.vexp;
   vp.status = status;
+  vp.prep_rows = 0;
+  std::memset(&vp.rp, 0, sizeof(vp.rp));
+  if (rp) {
+    // About two work items per prep thread, spread over whole rows of
+    // B Hkv blocks.
+    const int64_t items = (rp->seg[0].tokens + rp->seg[1].tokens) * (rp->d / 8);   // key rows (segment 0)
+    const int64_t per_row = static_cast<int64_t>(shape->B) * shape->Hkv * 256 * 2;
+    vp.prep_rows = static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>((items + per_row - 1) / per_row, 1),
+                                                          1024));
+    vp.rp = *rp;
+  }
   if (launch_attn_v16(shape->d_v, vp, st) != cudaSuccess) return ATTN_ERR_CUDA;
   FwdParams p;
   p.sh = vp.sh;
@@ -468,9 +588,9 @@ int launch_forward(const attn_shape* shape, const MaskParams& mask, const Layout
   return launch_attn_fwd(shape->d_h, shape->d_v, tq, tk, tv, p, st) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int check_workspace(const attn_shape* s, const void* ws, size_t bytes) {
+int check_workspace(const attn_shape* s, const attn_rotary* r, const void* ws, size_t bytes) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_WORKSPACE;
-  if (bytes < workspace_layout(s, nullptr).bytes) return ATTN_ERR_WORKSPACE;
+  if (bytes < workspace_layout(s, nullptr, r).bytes) return ATTN_ERR_WORKSPACE;
   return ATTN_OK;
 }
 
@@ -569,14 +689,8 @@ int rope_launch(int64_t tokens, int32_t heads_a, int32_t heads_b, int32_t d, flo
   unsigned int* status = nullptr;
   int rc = device_status_ptr(&status);
   if (rc) return rc;
-  // Frequencies in double, passed as fp32 pairs w_hi + w_lo so that the
-  // rounding of w does not grow with the position.
   float w_hi[64], w_lo[64];
-  for (int k = 0; k < d / 2; ++k) {
-    const double w = std::pow(static_cast<double>(base), -2.0 * k / d);
-    w_hi[k] = static_cast<float>(w);
-    w_lo[k] = static_cast<float>(w - static_cast<double>(w_hi[k]));
-  }
+  rope_frequencies(base, d, w_hi, w_lo);
   const cudaError_t e = launch_rope(tokens, d, heads_a, heads_b, positions, w_hi, w_lo, inverse, Xa, Ya, Xb, Yb,
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -618,19 +732,19 @@ int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask) {
   return total * shape->Hq;
 }
 
-size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
-  if (check_shape(shape) != ATTN_OK) return 0;
-  return workspace_layout(shape, nullptr).bytes;
+size_t attn_bwd_workspace_bytes(const attn_shape* shape, const attn_rotary* rotary) {
+  if (check_shape(shape) != ATTN_OK || check_rotary(rotary) != ATTN_OK) return 0;
+  return workspace_layout(shape, nullptr, rotary).bytes;
 }
 
-size_t attn_fwd_workspace_bytes(const attn_shape* shape) {
-  if (check_shape(shape) != ATTN_OK) return 0;
-  return fwd_workspace_layout(shape, nullptr).bytes;
+size_t attn_fwd_workspace_bytes(const attn_shape* shape, const attn_rotary* rotary) {
+  if (check_shape(shape) != ATTN_OK || check_rotary(rotary) != ATTN_OK) return 0;
+  return fwd_workspace_layout(shape, nullptr, padded_tokens(shape, rotary)).bytes;
 }
 
-int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
-             const void* Q, const void* K, const void* V, void* O, float* LSE, void* O_lo, void* workspace,
-             size_t workspace_bytes, void* stream) {
+int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, const attn_rotary* rotary,
+             float scale, const void* Q, const void* K, const void* V, void* O, float* LSE, void* O_lo,
+             void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   MaskParams m;
@@ -642,23 +756,39 @@ int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides*
   std::memset(&lay, 0, sizeof(lay));
   rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &lay);
   if (rc) return rc;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, LSE});
   if (rc) return rc;
   if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
-  rc = check_fwd_workspace(shape, workspace, workspace_bytes);
+  const RotaryTokens rt = padded_tokens(shape, rotary);
+  rc = check_fwd_workspace(shape, rt, workspace, workspace_bytes);
   if (rc) return rc;
   // ---- CUDA from here on ----
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FwdWorkspace w = fwd_workspace_layout(shape, workspace, rt);
+  RopePrepParams rp;
+  const void* Qa = Q;
+  const void* Ka = K;
+  if (rotary) {
+    Qa = rotary->q_rot ? rotary->q_rot : w.Qr;
+    Ka = rotary->k_rot ? rotary->k_rot : w.Kr;
+    rp = rotary_prep(rotary, shape->d_h, false,
+                     rope_segment(rt.q, shape->n_q, shape->Hq, rotary->pos_q, Q, lay.sq, const_cast<void*>(Qa)),
+                     rope_segment(rt.k, shape->n_k, shape->Hkv, rotary->pos_k, K, lay.sk, const_cast<void*>(Ka)));
+  }
   CUtensorMap tq, tk;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
-  if (!make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq, lay.sq.row, lay.sq.head) ||
-      !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk, lay.sk.row, lay.sk.head))
-    return ATTN_ERR_CUDA;
-  return launch_forward(shape, m, lay, scale, tq, tk, V, fwd_workspace_layout(shape, workspace), O, LSE, O_lo,
-                        status, static_cast<cudaStream_t>(stream));
+  const bool ok = rotary ? make_tmap(&tq, Qa, shape->d_h, shape->n_q, bhq) &&
+                               make_tmap(&tk, Ka, shape->d_h, shape->n_k, bhk)
+                         : make_tmap(&tq, Q, shape->d_h, shape->n_q, bhq, lay.sq.row, lay.sq.head) &&
+                               make_tmap(&tk, K, shape->d_h, shape->n_k, bhk, lay.sk.row, lay.sk.head);
+  if (!ok) return ATTN_ERR_CUDA;
+  return launch_forward(shape, m, lay, scale, tq, tk, V, w, O, LSE, O_lo, rotary ? &rp : nullptr, status, st);
 }
 
 size_t attn_fwd_decode_workspace_bytes(const attn_shape* shape, const attn_mask* mask) {
@@ -725,31 +855,46 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const void* Q, const void* O,
-                        const void* O_lo, const void* dO, void* workspace, size_t workspace_bytes, void* stream) {
+// Stage 1.  With a rotary, Q is turned as it is read, or the forward's
+// rotated queries (q_rot) are read instead.
+int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const attn_rotary* rotary,
+                        const void* Q, const void* O, const void* O_lo, const void* dO, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   LayoutParams padded;
   std::memset(&padded, 0, sizeof(padded));
   rc = build_strides(strides, shape->Hq, shape->Hkv, shape->n_q, shape->n_k, shape->d_h, shape->d_v, &padded);
   if (rc) return rc;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
   rc = check_ptrs({Q, O, O_lo, dO});
   if (rc) return rc;
-  rc = check_workspace(shape, workspace, workspace_bytes);
+  rc = check_workspace(shape, rotary, workspace, workspace_bytes);
   if (rc) return rc;
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  const Workspace w = workspace_layout(shape, workspace);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(shape, workspace, rotary);
+  RotaryAngles ra;
+  const bool turn = rotary && !rotary->q_rot;
+  if (turn) ra = rotary_angles(rotary, rotary->pos_q, shape->d_h);
+  if (rotary && rotary->q_rot) {
+    Q = rotary->q_rot;   // contiguous rows
+    padded.sq = TensorStrides{shape->d_h, static_cast<int64_t>(shape->n_q) * shape->d_h};
+  }
   const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), padded, shape->d_v, shape->d_h, Q, O, O_lo,
-                                                   dO, w.D, w.tilemax, w.grpexp, w.dQacc, w.Q16, w.dO16, status,
-                                                   static_cast<cudaStream_t>(stream));
+                                                   dO, w.D, w.tilemax, w.grpexp, w.dQacc, w.Q16, w.dO16,
+                                                   turn ? &ra : nullptr, status, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
-                  const void* K, const void* V, const float* LSE, void* workspace, size_t workspace_bytes, void* dK,
-                  void* dV, void* stream) {
+// Stage 2.  With a rotary, the keys are the forward's rotated keys (k_rot)
+// or a rotated copy written into the workspace first; dK is turned back.
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
+                  const attn_rotary* rotary, float scale, const void* K, const void* V, const float* LSE,
+                  void* workspace, size_t workspace_bytes, void* dK, void* dV, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   BwdParams p;
@@ -760,19 +905,37 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_str
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
   rc = check_ptrs({K, V, LSE, dK, dV});
   if (rc) return rc;
-  rc = check_workspace(shape, workspace, workspace_bytes);
+  rc = check_workspace(shape, rotary, workspace, workspace_bytes);
   if (rc) return rc;
-  const Workspace w = workspace_layout(shape, workspace);
+  const Workspace w = workspace_layout(shape, workspace, rotary);
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void* Ka = K;
+  if (rotary) {
+    Ka = rotary->k_rot ? rotary->k_rot : w.Kr;
+    if (!rotary->k_rot) {
+      const RotaryTokens rt = padded_tokens(shape, rotary);
+      const RopeSegment none = rope_segment(0, 0, 0, nullptr, nullptr, TensorStrides{0, 0}, nullptr);
+      rc = launch_rotary_prep(rotary_prep(rotary, shape->d_h, false,
+                                          rope_segment(rt.k, shape->n_k, shape->Hkv, rotary->pos_k, K, p.lay.sk,
+                                                       w.Kr),
+                                          none),
+                              st);
+      if (rc) return rc;
+    }
+  }
   CUtensorMap tq, tk, tv, tdo, tdq;
   const int64_t bhq = static_cast<int64_t>(shape->B) * shape->Hq;
   const int64_t bhk = static_cast<int64_t>(shape->B) * shape->Hkv;
-  if (!make_tmap(&tq, w.Q16, shape->d_h, shape->n_q, bhq) ||
-      !make_tmap(&tk, K, shape->d_h, shape->n_k, bhk, p.lay.sk.row, p.lay.sk.head) ||
+  const bool k_ok = rotary ? make_tmap(&tk, Ka, shape->d_h, shape->n_k, bhk)
+                           : make_tmap(&tk, K, shape->d_h, shape->n_k, bhk, p.lay.sk.row, p.lay.sk.head);
+  if (!make_tmap(&tq, w.Q16, shape->d_h, shape->n_q, bhq) || !k_ok ||
       !make_tmap(&tv, V, shape->d_v, shape->n_k, bhk, p.lay.sv.row, p.lay.sv.head) ||
       !make_tmap(&tdo, w.dO16, shape->d_v, shape->n_q, bhq) || !make_tmap_acc(&tdq, w.dQacc, shape->d_h, shape->n_q, bhq))
     return ATTN_ERR_CUDA;
@@ -788,14 +951,15 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_str
   p.dQacc = w.dQacc;
   p.dK = dK;
   p.dV = dV;
+  if (rotary) p.rot = rotary_angles(rotary, rotary->pos_k, shape->d_h);
+  else p.rot.pos = nullptr;
   p.status = status;
-  const cudaError_t e =
-      launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, tdq, p, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, float scale, const void* workspace,
-                      size_t workspace_bytes, void* dQ, void* stream) {
+int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, const attn_rotary* rotary, float scale,
+                      const void* workspace, size_t workspace_bytes, void* dQ, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   LayoutParams lay;
@@ -804,25 +968,29 @@ int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, floa
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
   rc = check_ptrs({dQ});
   if (rc) return rc;
-  rc = check_workspace(shape, workspace, workspace_bytes);
+  rc = check_workspace(shape, rotary, workspace, workspace_bytes);
   if (rc) return rc;
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  const Workspace w = workspace_layout(shape, const_cast<void*>(workspace));
+  const Workspace w = workspace_layout(shape, const_cast<void*>(workspace), rotary);
+  RotaryAngles ra;
+  if (rotary) ra = rotary_angles(rotary, rotary->pos_q, shape->d_h);
   // Padded accumulator rows: heads of n_q rows.
   const cudaError_t e = launch_attn_bwd_finalize(
       q_rows(shape) * shape->d_h, shape->d_h, shape->n_q, lay.sdq.head, lay.sdq.row,
       contiguous_strides(lay, lay.sdq, shape->Hq, shape->n_q, shape->d_h), scale, w.dQacc, dQ,
-      static_cast<cudaStream_t>(stream));
+      rotary ? &ra : nullptr, false, shape->Hq, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale, const void* Q,
-             const void* K, const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
-             void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream) {
+int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, const attn_rotary* rotary,
+             float scale, const void* Q, const void* K, const void* V, const void* O, const void* O_lo, const void* dO,
+             const float* LSE, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   MaskParams m;
@@ -836,15 +1004,17 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides*
   }
   rc = check_scale(scale);
   if (rc) return rc;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
   rc = check_ptrs({Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV});
   if (rc) return rc;
-  rc = check_workspace(shape, workspace, workspace_bytes);
+  rc = check_workspace(shape, rotary, workspace, workspace_bytes);
   if (rc) return rc;
-  rc = attn_bwd_preprocess(shape, strides, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
+  rc = attn_bwd_preprocess(shape, strides, rotary, Q, O, O_lo, dO, workspace, workspace_bytes, stream);
   if (rc) return rc;
-  rc = attn_bwd_main(shape, mask, strides, scale, K, V, LSE, workspace, workspace_bytes, dK, dV, stream);
+  rc = attn_bwd_main(shape, mask, strides, rotary, scale, K, V, LSE, workspace, workspace_bytes, dK, dV, stream);
   if (rc) return rc;
-  return attn_bwd_finalize(shape, strides, scale, workspace, workspace_bytes, dQ, stream);
+  return attn_bwd_finalize(shape, strides, rotary, scale, workspace, workspace_bytes, dQ, stream);
 }
 
 int attn_get_status(int* status) {
@@ -885,12 +1055,15 @@ int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 // the preprocess stage), so leftovers from an earlier call do not matter; but
 // all calls share the one buffer, so calls that overlap on the GPU (other
 // streams, other host threads) race and must be serialised by the caller.
-int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
-                     const void* Q, const void* K, const void* V, const void* O, const void* O_lo, const void* dO,
-                     const float* LSE, void* dQ, void* dK, void* dV, void* stream) {
+int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
+                     const attn_rotary* rotary, float scale, const void* Q, const void* K, const void* V,
+                     const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                     void* stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
-  if (workspace_layout(shape, nullptr).bytes > kStaticBwdScratchBytes) return ATTN_ERR_WORKSPACE;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
+  if (workspace_layout(shape, nullptr, rotary).bytes > kStaticBwdScratchBytes) return ATTN_ERR_WORKSPACE;
   // Every argument check before the first CUDA call (the symbol lookup).
   MaskParams m;
   rc = build_mask(shape, mask, &m);
@@ -908,7 +1081,7 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_
   void* scratch = nullptr;
   rc = static_scratch_ptr(&scratch);
   if (rc) return rc;
-  return attn_bwd(shape, mask, strides, scale, Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV, scratch,
+  return attn_bwd(shape, mask, strides, rotary, scale, Q, K, V, O, O_lo, dO, LSE, dQ, dK, dV, scratch,
                   kStaticBwdScratchBytes, stream);
 }
 
@@ -1038,14 +1211,66 @@ int64_t attn_varlen_visible_pairs(const attn_varlen* v) {
   return total * v->Hq;
 }
 
-size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v) {
+size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v, const attn_rotary* rotary) {
   Varlen d;
-  if (build_varlen(v, &d) != ATTN_OK) return 0;
-  return fwd_workspace_layout(&d.shape, nullptr).bytes;
+  if (build_varlen(v, &d) != ATTN_OK || check_rotary(rotary) != ATTN_OK) return 0;
+  return fwd_workspace_layout(&d.shape, nullptr, varlen_tokens(d, rotary)).bytes;
 }
 
-int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
-                    const void* V, void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes,
+int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, const attn_rotary* rotary, float scale,
+                    const void* Q, const void* K, const void* V, void* O, float* LSE, void* O_lo, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  Varlen d;
+  int rc = build_varlen(v, &d);
+  if (rc) return rc;
+  rc = build_strides(strides, v->Hq, v->Hkv, 0, 0, v->d_h, v->d_v, &d.lay);
+  if (rc) return rc;
+  rc = check_scale(scale);
+  if (rc) return rc;
+  rc = check_rotary(rotary);
+  if (rc) return rc;
+  if (d.total_q == 0) return ATTN_OK;   // no query rows: nothing to write
+  rc = check_ptrs({Q, K, V, O, LSE});
+  if (rc) return rc;
+  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
+  const RotaryTokens rt = varlen_tokens(d, rotary);
+  rc = check_fwd_workspace(&d.shape, rt, workspace, workspace_bytes);
+  if (rc) return rc;
+  // ---- CUDA from here on ----
+  unsigned int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FwdWorkspace w = fwd_workspace_layout(&d.shape, workspace, rt);
+  RopePrepParams rp;
+  const void* Qa = Q;
+  const void* Ka = K;
+  if (rotary) {
+    Qa = rotary->q_rot ? rotary->q_rot : w.Qr;
+    Ka = rotary->k_rot ? rotary->k_rot : w.Kr;
+    rp = rotary_prep(rotary, v->d_h, true,
+                     rope_segment(rt.q, 0, v->Hq, rotary->pos_q, Q, d.lay.sq, const_cast<void*>(Qa)),
+                     rope_segment(rt.k, 0, v->Hkv, rotary->pos_k, K, d.lay.sk, const_cast<void*>(Ka)));
+  }
+  CUtensorMap tq, tk;
+  const bool ok = rotary ? make_tmap_packed(&tq, Qa, v->d_h, v->Hq, d.total_q) &&
+                               make_tmap_packed(&tk, Ka, v->d_h, v->Hkv, d.total_k)
+                         : make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q, d.lay.sq.row, d.lay.sq.head) &&
+                               make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k, d.lay.sk.row, d.lay.sk.head);
+  if (!ok) return ATTN_ERR_CUDA;
+  return launch_forward(&d.shape, d.mask, d.lay, scale, tq, tk, V, w, O, LSE, O_lo, rotary ? &rp : nullptr, status,
+                        st);
+}
+
+size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v, const attn_rotary* rotary) {
+  Varlen d;
+  if (build_varlen(v, &d) != ATTN_OK || check_rotary(rotary) != ATTN_OK) return 0;
+  return workspace_layout_varlen(d, nullptr, rotary).bytes;
+}
+
+int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, const attn_rotary* rotary, float scale,
+                    const void* Q, const void* K, const void* V, const void* O, const void* O_lo, const void* dO,
+                    const float* LSE, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
                     void* stream) {
   Varlen d;
   int rc = build_varlen(v, &d);
@@ -1054,39 +1279,7 @@ int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, float sca
   if (rc) return rc;
   rc = check_scale(scale);
   if (rc) return rc;
-  if (d.total_q == 0) return ATTN_OK;   // no query rows: nothing to write
-  rc = check_ptrs({Q, K, V, O, LSE});
-  if (rc) return rc;
-  if (O_lo && !aligned16(O_lo)) return ATTN_ERR_ALIGN;
-  rc = check_fwd_workspace(&d.shape, workspace, workspace_bytes);
-  if (rc) return rc;
-  // ---- CUDA from here on ----
-  unsigned int* status = nullptr;
-  rc = device_status_ptr(&status);
-  if (rc) return rc;
-  CUtensorMap tq, tk;
-  if (!make_tmap_packed(&tq, Q, v->d_h, v->Hq, d.total_q, d.lay.sq.row, d.lay.sq.head) ||
-      !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k, d.lay.sk.row, d.lay.sk.head))
-    return ATTN_ERR_CUDA;
-  return launch_forward(&d.shape, d.mask, d.lay, scale, tq, tk, V, fwd_workspace_layout(&d.shape, workspace), O, LSE,
-                        O_lo, status, static_cast<cudaStream_t>(stream));
-}
-
-size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v) {
-  Varlen d;
-  if (build_varlen(v, &d) != ATTN_OK) return 0;
-  return workspace_layout_varlen(d, nullptr).bytes;
-}
-
-int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
-                    const void* V, const void* O, const void* O_lo, const void* dO, const float* LSE, void* dQ,
-                    void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream) {
-  Varlen d;
-  int rc = build_varlen(v, &d);
-  if (rc) return rc;
-  rc = build_strides(strides, v->Hq, v->Hkv, 0, 0, v->d_h, v->d_v, &d.lay);
-  if (rc) return rc;
-  rc = check_scale(scale);
+  rc = check_rotary(rotary);
   if (rc) return rc;
   if (d.total_k > 0) {
     rc = check_ptrs({K, V, dK, dV});
@@ -1095,7 +1288,7 @@ int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float sca
   if (d.total_q > 0) {
     rc = check_ptrs({Q, O, O_lo, dO, LSE, dQ});
     if (rc) return rc;
-    const Workspace need = workspace_layout_varlen(d, nullptr);
+    const Workspace need = workspace_layout_varlen(d, nullptr, rotary);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need.bytes)
       return ATTN_ERR_WORKSPACE;
   }
@@ -1119,14 +1312,39 @@ int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float sca
   unsigned int* status = nullptr;
   rc = device_status_ptr(&status);
   if (rc) return rc;
-  const Workspace w = workspace_layout_varlen(d, workspace);
+  const Workspace w = workspace_layout_varlen(d, workspace, rotary);
   const ShapeParams sh = shape_params(&d.shape);
-  cudaError_t e = launch_attn_bwd_preprocess(sh, d.lay, v->d_v, v->d_h, Q, O, O_lo, dO, w.D, w.tilemax, w.grpexp,
-                                             w.dQacc, w.Q16, w.dO16, status, st);
+  if (rotary) {
+    // The rotated keys, unless the forward's are given.
+    if (!rotary->k_rot) {
+      const RopeSegment none = rope_segment(0, 0, 0, nullptr, nullptr, TensorStrides{0, 0}, nullptr);
+      rc = launch_rotary_prep(
+          rotary_prep(rotary, v->d_h, true, rope_segment(d.total_k, 0, v->Hkv, rotary->pos_k, K, d.lay.sk, w.Kr),
+                      none),
+          st);
+      if (rc) return rc;
+    }
+  }
+  RotaryAngles rq, rk;
+  LayoutParams play = d.lay;   // the preprocess's view of Q
+  const void* Qa = Q;
+  const bool turn_q = rotary && !rotary->q_rot;
+  if (rotary) {
+    rq = rotary_angles(rotary, rotary->pos_q, v->d_h);
+    rk = rotary_angles(rotary, rotary->pos_k, v->d_h);
+    if (rotary->q_rot) {
+      Qa = rotary->q_rot;
+      play.sq = TensorStrides{static_cast<int64_t>(v->Hq) * v->d_h, v->d_h};
+    }
+  }
+  cudaError_t e = launch_attn_bwd_preprocess(sh, play, v->d_v, v->d_h, Qa, O, O_lo, dO, w.D, w.tilemax, w.grpexp,
+                                             w.dQacc, w.Q16, w.dO16, turn_q ? &rq : nullptr, status, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_tmap_packed(&tq, w.Q16, v->d_h, v->Hq, d.total_q) ||
-      !make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k, d.lay.sk.row, d.lay.sk.head) ||
+  const bool k_ok =
+      rotary ? make_tmap_packed(&tk, rotary->k_rot ? rotary->k_rot : w.Kr, v->d_h, v->Hkv, d.total_k)
+             : make_tmap_packed(&tk, K, v->d_h, v->Hkv, d.total_k, d.lay.sk.row, d.lay.sk.head);
+  if (!make_tmap_packed(&tq, w.Q16, v->d_h, v->Hq, d.total_q) || !k_ok ||
       !make_tmap_packed(&tv, V, v->d_v, v->Hkv, d.total_k, d.lay.sv.row, d.lay.sv.head) ||
       !make_tmap_packed(&tdo, w.dO16, v->d_v, v->Hq, d.total_q) ||
       !make_tmap_acc_packed(&tdq, w.dQacc, v->d_h, v->Hq, d.total_q))
@@ -1146,12 +1364,15 @@ int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float sca
   p.dQacc = w.dQacc;
   p.dK = dK;
   p.dV = dV;
+  if (rotary) p.rot = rk;
+  else p.rot.pos = nullptr;
   p.status = status;
   e = launch_attn_bwd_main(v->d_h, v->d_v, tq, tk, tv, tdo, tdq, p, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   // Packed accumulator rows: tokens of Hq heads.
   e = launch_attn_bwd_finalize(d.total_q * v->Hq * v->d_h, v->d_h, v->Hq, d.lay.sdq.row, d.lay.sdq.head,
-                               contiguous_strides(d.lay, d.lay.sdq, v->Hq, 0, v->d_h), scale, w.dQacc, dQ, st);
+                               contiguous_strides(d.lay, d.lay.sdq, v->Hq, 0, v->d_h), scale, w.dQacc, dQ,
+                               rotary ? &rq : nullptr, true, v->Hq, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -82,6 +82,7 @@
 #include "common.cuh"
 #include "f16range.cuh"
 #include "ptx.cuh"
+#include "rotary.cuh"
 
 namespace esd {
 namespace {
@@ -201,7 +202,7 @@ __device__ __noinline__ CtaScale cta_scale(const float* red, float2 qo) {
   return c;
 }
 
-template <int DH, int DV, bool PACKED>
+template <int DH, int DV, bool PACKED, bool ROPE>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -851,14 +852,39 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                            strided_off(PACKED, p.lay.sdv, p.sh.Hkv, p.lay.cu_k[b], b, hkv, j));
       const float dk_scale = p.scale * exp2_int(-cs.g - cs.q);   // dK_acc = 2^(g + q) dS^T Q (CtaScale)
       const float dv_scale = exp2_int(-cs.o);                    // dV_acc = 2^o P^T dO
+      // Rotary: the accumulated gradient is that of the rotated key; the
+      // key's own gradient is it turned back by the key's angles (the
+      // transpose of the rotation), formed here per 4-block chunk.
+      int32_t kpos = 0;
+      if constexpr (ROPE) kpos = in ? p.rot.pos[k_token(PACKED, p.lay, p.sh.n_k, b, j)] : 0;
 #pragma unroll
       for (int cc = 0; cc < DH / 32; ++cc) {
         uint32_t w[16];
         if (total > 0) {
           tmem_ld32(tmem + lane_base + C::kTdK + cc * 32, rr);
+          if constexpr (ROPE) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * dk_scale, __uint_as_float(rr[k + 1]) * dk_scale);
+            for (int q4 = 0; q4 < 4; ++q4) {   // chunk 4 cc + q4: columns 32 cc + 8 q4 ..
+              float wh[4], wl[4];
+              rope_freqs4(p.rot.w_hi, p.rot.w_lo, 4 * cc + q4, wh, wl);
+              float4 t0, t1;
+              rope_angles4(kpos, wh, wl, t0, t1);
+              rope_transpose(t0, t1);
+              const float cs4[4] = {t0.x, t0.z, t1.x, t1.z}, sn4[4] = {t0.y, t0.w, t1.y, t1.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int k = 8 * q4 + 2 * q;
+                float y0, y1;
+                rot_block(__uint_as_float(rr[k]) * dk_scale, __uint_as_float(rr[k + 1]) * dk_scale, cs4[q], sn4[q],
+                          y0, y1);
+                w[k >> 1] = pack_bf16x2(y0, y1);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; k += 2)
+              w[k >> 1] = pack_bf16x2(__uint_as_float(rr[k]) * dk_scale, __uint_as_float(rr[k + 1]) * dk_scale);
+          }
         } else {
 #pragma unroll
           for (int k = 0; k < 16; ++k) w[k] = 0u;
@@ -909,10 +935,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 // one 16-byte chunk each, so every warp load covers whole rows.
 // row_at(rr) is the workspace row of the tile's row rr (the contiguous
 // layout of Q), d_at(rr) its index in D, and user_at(s, rr) its element
-// offset in a user tensor with strides s.
-template <int DV, int DH, class RowAt, class DAt, class UserAt>
+// offset in a user tensor with strides s.  ROPE: Q is the rotated query,
+// each row turned by the angles of its token tok_at(rr) (positions and
+// frequencies rot) and rounded to bf16 as the forward's rotation rounds it.
+template <int DV, int DH, bool ROPE, class RowAt, class DAt, class UserAt, class TokAt>
 __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at, const DAt& d_at,
-                                              const UserAt& user_at, const TensorStrides& sq,
+                                              const UserAt& user_at, const TokAt& tok_at, const RotaryAngles& rot,
+                                              const TensorStrides& sq,
                                               const TensorStrides& so, const TensorStrides& sdo,
                                               const uint4* __restrict__ Q, const uint4* __restrict__ O,
                                               const uint4* __restrict__ O_lo, const uint4* __restrict__ dO,
@@ -933,6 +962,28 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
   for (int j = 0; j < kQ; ++j) {
     const int k = j * 256 + static_cast<int>(threadIdx.x), rr = k / (DH / 8);
     q[j] = rr < rows_here ? Q[user_at(sq, rr) / 8 + k % (DH / 8)] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if constexpr (ROPE) {
+    // A thread keeps one chunk (256 is a multiple of the row's DH / 8
+    // chunks), so its four frequencies serve all its rows; the positions are
+    // requested right behind the rows, which are turned before the D pass.
+    float wh[4], wl[4];
+    rope_freqs4(rot.w_hi, rot.w_lo, static_cast<int>(threadIdx.x) % (DH / 8), wh, wl);
+    int32_t pos[kQ];
+#pragma unroll
+    for (int j = 0; j < kQ; ++j) {
+      const int rr = (j * 256 + static_cast<int>(threadIdx.x)) / (DH / 8);
+      pos[j] = rr < rows_here ? rot.pos[tok_at(rr)] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kQ; ++j) {
+      const int rr = (j * 256 + static_cast<int>(threadIdx.x)) / (DH / 8);
+      if (rr < rows_here) {
+        float4 t0, t1;
+        rope_angles4(pos[j], wh, wl, t0, t1);
+        q[j] = rot_bf16x8(q[j], t0, t1);
+      }
+    }
   }
   float mn = 0.f, md = 0.f;
   uint32_t gmax = 0u, qmax = 0u;
@@ -1035,9 +1086,10 @@ __device__ __forceinline__ void bwd_prep_tile(int rows_here, const RowAt& row_at
 
 // One block per 128-row query tile of one (batch, query head); rows of
 // (b, h) are contiguous, n_q of them.
-template <int DV, int DH>
+template <int DV, int DH, bool ROPE>
 __global__ void __launch_bounds__(256)
-attn_bwd_preprocess_kernel(int n_q, int nqt, TensorStrides sq, TensorStrides so, TensorStrides sdo,
+attn_bwd_preprocess_kernel(int n_q, int nqt, int Hq, const __grid_constant__ RotaryAngles rot, TensorStrides sq,
+                           TensorStrides so, TensorStrides sdo,
                            const uint4* __restrict__ Q, const uint4* __restrict__ O,
                            const uint4* __restrict__ O_lo, const uint4* __restrict__ dO, float* __restrict__ D,
                            float4* __restrict__ tilemax, float4* __restrict__ dQacc, uint4* __restrict__ Q16,
@@ -1049,8 +1101,9 @@ attn_bwd_preprocess_kernel(int n_q, int nqt, TensorStrides sq, TensorStrides so,
   const int64_t row0 = bh * n_q + i0;
   const auto row_at = [row0](int rr) { return row0 + rr; };
   const auto user_at = [bh, i0](const TensorStrides& s, int rr) { return bh * s.head + (i0 + rr) * s.row; };
-  bwd_prep_tile<DV, DH>(rows_here, row_at, row_at, user_at, sq, so, sdo, Q, O, O_lo, dO, D, tilemax + bh * nqt + qt,
-                        dQacc, Q16, dO16, status);
+  const auto tok_at = [bh, Hq, n_q, i0](int rr) { return (bh / Hq) * n_q + i0 + rr; };
+  bwd_prep_tile<DV, DH, ROPE>(rows_here, row_at, row_at, user_at, tok_at, rot, sq, so, sdo, Q, O, O_lo, dO, D,
+                              tilemax + bh * nqt + qt, dQacc, Q16, dO16, status);
 }
 
 // The same for packed sequences (token-major rows, per-sequence lengths):
@@ -1070,9 +1123,10 @@ struct PrepPacked {
   }
 };
 
-template <int DV, int DH>
+template <int DV, int DH, bool ROPE>
 __global__ void __launch_bounds__(256)
-attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt, const uint4* __restrict__ Q,
+attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt,
+                                  const __grid_constant__ RotaryAngles rot, const uint4* __restrict__ Q,
                                   const uint4* __restrict__ O, const uint4* __restrict__ O_lo,
                                   const uint4* __restrict__ dO, float* __restrict__ D, float4* __restrict__ tilemax,
                                   float4* __restrict__ dQacc, uint4* __restrict__ Q16, uint4* __restrict__ dO16,
@@ -1088,8 +1142,9 @@ attn_bwd_preprocess_packed_kernel(const __grid_constant__ PrepPacked rm, int nqt
   const auto d_at = [&rm, b, h, i0](int rr) { return rm.vec(b, h, i0 + rr); };
   const int64_t t0 = static_cast<int64_t>(rm.cu_q[b]) + i0;
   const auto user_at = [t0, h](const TensorStrides& s, int rr) { return (t0 + rr) * s.row + h * s.head; };
-  bwd_prep_tile<DV, DH>(rows_here, row_at, d_at, user_at, rm.sq, rm.so, rm.sdo, Q, O, O_lo, dO, D,
-                        tilemax + bh * nqt + qt, dQacc, Q16, dO16, status);
+  const auto tok_at = [t0](int rr) { return t0 + rr; };
+  bwd_prep_tile<DV, DH, ROPE>(rows_here, row_at, d_at, user_at, tok_at, rot, rm.sq, rm.so, rm.sdo, Q, O, O_lo, dO, D,
+                              tilemax + bh * nqt + qt, dQacc, Q16, dO16, status);
 }
 
 // Every query tile of a (batch, KV head) group brought to one exponent for
@@ -1204,6 +1259,70 @@ attn_bwd_finalize_strided_kernel(int64_t n8, int c8, int n_inner, int64_t s_oute
   }
 }
 
+// The same with the rotary embedding: each 8-element chunk of the rotated
+// query's gradient turned back by its token's angles (the transpose of the
+// rotation) before it is rounded.  A work item is one chunk of one token for
+// a group of up to 8 query heads, so that the token's table entries are read
+// once per group.  Accumulator row and dQ offset of (token, h): padded
+// (token = b n_q + i) row (b Hq + h) n_q + i at (b Hq + h) s_head + i s_row;
+// packed row token Hq + h at token s_row + h s_head.
+__global__ void __launch_bounds__(256)
+attn_bwd_finalize_rope_kernel(int64_t tokens, int c8, int Hq, int n_q, int packed, int64_t s_row, int64_t s_head,
+                              float scale, const float4* __restrict__ acc, const __grid_constant__ RotaryAngles rot,
+                              uint4* __restrict__ dQ) {
+  constexpr int kG = 8;
+  const int groups = (Hq + kG - 1) / kG;
+  const int64_t items = tokens * c8 * groups;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < items; u += nthreads) {
+    const int64_t tg = u / c8;
+    const int c = static_cast<int>(u - tg * c8);
+    const int64_t tok = tg / groups;
+    const int h0 = static_cast<int>(tg - tok * groups) * kG;
+    int64_t row0, rstep, off0, ostep;
+    if (packed) {
+      row0 = tok * Hq;
+      rstep = 1;
+      off0 = tok * s_row;
+      ostep = s_head;
+    } else {
+      const int64_t b = tok / n_q, i = tok - b * n_q;
+      row0 = b * Hq * n_q + i;
+      rstep = n_q;
+      off0 = b * Hq * s_head + i * s_row;
+      ostep = s_head;
+    }
+    float4 a[kG], bb[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g)
+      if (h0 + g < Hq) {
+        const int64_t k = (row0 + (h0 + g) * rstep) * c8 + c;
+        a[g] = acc[2 * k];
+        bb[g] = acc[2 * k + 1];
+      }
+    float wh[4], wl[4];
+    rope_freqs4(rot.w_hi, rot.w_lo, c, wh, wl);
+    float4 t0, t1;
+    rope_angles4(rot.pos[tok], wh, wl, t0, t1);
+    rope_transpose(t0, t1);
+    const float cs[4] = {t0.x, t0.z, t1.x, t1.z}, sn[4] = {t0.y, t0.w, t1.y, t1.w};
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      if (h0 + g >= Hq) break;
+      const float x[8] = {a[g].x * scale, a[g].y * scale, a[g].z * scale, a[g].w * scale,
+                          bb[g].x * scale, bb[g].y * scale, bb[g].z * scale, bb[g].w * scale};
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float y0, y1;
+        rot_block(x[2 * q], x[2 * q + 1], cs[q], sn[q], y0, y1);
+        w[q] = pack_bf16x2(y0, y1);
+      }
+      dQ[(off0 + (h0 + g) * ostep) / 8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // dQ = scale * acc, eight elements per thread per iteration (contiguous dQ).
 __global__ void __launch_bounds__(256)
 attn_bwd_finalize_kernel(int64_t n8, float scale, const float4* __restrict__ acc, uint4* __restrict__ dQ) {
@@ -1221,7 +1340,10 @@ cudaError_t launch_bwd_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
                               const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdParams& p,
                               cudaStream_t stream) {
   using C = BwdCfg<DH, DV>;
-  auto kern = p.lay.packed ? attn_bwd_main_kernel<DH, DV, true> : attn_bwd_main_kernel<DH, DV, false>;
+  auto kern = p.rot.pos ? (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, true>
+                                      : attn_bwd_main_kernel<DH, DV, false, true>)
+                      : (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, false>
+                                      : attn_bwd_main_kernel<DH, DV, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN));
@@ -1239,7 +1361,10 @@ int grid_for(int64_t work_threads) {
 template <int DV, int DH>
 void launch_pre_t(const ShapeParams& sh, const LayoutParams& lay, int nqt, const void* Q, const void* O,
                   const void* O_lo, const void* dO, float* D, float4* tilemax, float* dQacc, void* Q16, void* dO16,
-                  unsigned int* status, cudaStream_t stream) {
+                  const RotaryAngles* rot, unsigned int* status, cudaStream_t stream) {
+  RotaryAngles none;
+  none.pos = nullptr;
+  const RotaryAngles& ra = rot ? *rot : none;
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(sh.B) * sh.Hq), static_cast<unsigned>(nqt));
   const uint4 *q = static_cast<const uint4*>(Q), *o = static_cast<const uint4*>(O);
   const uint4 *olo = static_cast<const uint4*>(O_lo), *g = static_cast<const uint4*>(dO);
@@ -1247,8 +1372,9 @@ void launch_pre_t(const ShapeParams& sh, const LayoutParams& lay, int nqt, const
   uint4* q16 = static_cast<uint4*>(Q16);
   uint4* do16 = static_cast<uint4*>(dO16);
   if (!lay.packed) {
-    attn_bwd_preprocess_kernel<DV, DH><<<grid, 256, 0, stream>>>(sh.n_q, nqt, lay.sq, lay.so, lay.sdo, q, o, olo, g,
-                                                                  D, tilemax, acc, q16, do16, status);
+    auto kern = rot ? attn_bwd_preprocess_kernel<DV, DH, true> : attn_bwd_preprocess_kernel<DV, DH, false>;
+    kern<<<grid, 256, 0, stream>>>(sh.n_q, nqt, sh.Hq, ra, lay.sq, lay.so, lay.sdo, q, o, olo, g, D, tilemax, acc,
+                                   q16, do16, status);
   } else {
     PrepPacked rm;
     rm.n_q = sh.n_q;
@@ -1258,8 +1384,8 @@ void launch_pre_t(const ShapeParams& sh, const LayoutParams& lay, int nqt, const
     rm.so = lay.so;
     rm.sdo = lay.sdo;
     for (int b = 0; b <= sh.B; ++b) rm.cu_q[b] = lay.cu_q[b];
-    attn_bwd_preprocess_packed_kernel<DV, DH><<<grid, 256, 0, stream>>>(rm, nqt, q, o, olo, g, D, tilemax, acc,
-                                                                        q16, do16, status);
+    auto kern = rot ? attn_bwd_preprocess_packed_kernel<DV, DH, true> : attn_bwd_preprocess_packed_kernel<DV, DH, false>;
+    kern<<<grid, 256, 0, stream>>>(rm, nqt, ra, q, o, olo, g, D, tilemax, acc, q16, do16, status);
   }
 }
 
@@ -1277,7 +1403,7 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
 cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams& lay, int dv, int dh,
                                        const void* Q, const void* O, const void* O_lo, const void* dO, float* D,
                                        float4* tilemax, float2* grpexp, float* dQacc, void* Q16, void* dO16,
-                                       unsigned int* status, cudaStream_t stream) {
+                                       const RotaryAngles* rot_q, unsigned int* status, cudaStream_t stream) {
   const int nqt = (sh.n_q + kTileM - 1) / kTileM;
   GroupExpParams g;
   g.Hq = sh.Hq;
@@ -1294,13 +1420,13 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams
   const int64_t gy = static_cast<int64_t>(sh.group) * nqt;
   const dim3 ggrid(static_cast<unsigned>(sh.B * sh.Hkv), static_cast<unsigned>(gy < 65535 ? gy : 65535));
   if (dv == 128 && dh == 128) {
-    launch_pre_t<128, 128>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, status, stream);
+    launch_pre_t<128, 128>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, rot_q, status, stream);
     attn_bwd_group_exp_kernel<128, 128><<<ggrid, 256, 0, stream>>>(g);
   } else if (dv == 64 && dh == 64) {
-    launch_pre_t<64, 64>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, status, stream);
+    launch_pre_t<64, 64>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, rot_q, status, stream);
     attn_bwd_group_exp_kernel<64, 64><<<ggrid, 256, 0, stream>>>(g);
   } else if (dv == 64 && dh == 128) {
-    launch_pre_t<64, 128>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, status, stream);
+    launch_pre_t<64, 128>(sh, lay, nqt, Q, O, O_lo, dO, D, tilemax, dQacc, Q16, dO16, rot_q, status, stream);
     attn_bwd_group_exp_kernel<128, 64><<<ggrid, 256, 0, stream>>>(g);
   } else {
     return cudaErrorInvalidValue;
@@ -1309,9 +1435,18 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams
 }
 
 cudaError_t launch_attn_bwd_finalize(int64_t elems, int dh, int n_inner, int64_t s_outer, int64_t s_inner,
-                                     bool contiguous, float scale, const float* dQacc, void* dQ, cudaStream_t stream) {
+                                     bool contiguous, float scale, const float* dQacc, void* dQ,
+                                     const RotaryAngles* rot_q, bool packed, int Hq, cudaStream_t stream) {
   const int64_t n8 = elems / 8;
-  if (contiguous)
+  if (rot_q) {
+    // Padded rows are heads of n_inner = n_q rows (s_outer the head stride);
+    // packed rows are tokens of n_inner = Hq heads (s_outer the token stride).
+    const int64_t tokens = elems / (static_cast<int64_t>(Hq) * dh);
+    const int64_t items = tokens * (dh / 8) * ((Hq + 7) / 8);
+    attn_bwd_finalize_rope_kernel<<<grid_for(items), 256, 0, stream>>>(
+        tokens, dh / 8, Hq, packed ? 0 : n_inner, packed ? 1 : 0, packed ? s_outer : s_inner,
+        packed ? s_inner : s_outer, scale, reinterpret_cast<const float4*>(dQacc), *rot_q, static_cast<uint4*>(dQ));
+  } else if (contiguous)
     attn_bwd_finalize_kernel<<<grid_for(n8), 256, 0, stream>>>(n8, scale, reinterpret_cast<const float4*>(dQacc),
                                                              static_cast<uint4*>(dQ));
   else

@@ -63,6 +63,7 @@
 #include "common.cuh"
 #include "f16range.cuh"
 #include "ptx.cuh"
+#include "rotary.cuh"
 
 namespace esd {
 namespace {
@@ -466,10 +467,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // past the key length zero, and e recorded in vexp.  One block per tile;
 // the whole tile stays in registers while the block agrees on e.  Tiles that
 // start past the key length are never read by the forward and are skipped.
-template <int DV, bool PACKED>
+template <int DV, bool PACKED, bool ROPE>
 __global__ void __launch_bounds__(256) attn_v16_kernel(const __grid_constant__ V16Params p) {
   constexpr int kCpr = DV / 8;                    // 16-byte chunks per row
   constexpr int kChunks = kTileN * kCpr / 256;    // per thread
+  if (ROPE && static_cast<int>(blockIdx.y) >= p.nkt) {
+    // Rotary: the rotated queries and keys, in the same launch.
+    const int64_t blk = static_cast<int64_t>(blockIdx.y - p.nkt) * gridDim.x + blockIdx.x;
+    rope_prep_range(p.rp, blk * 256 + threadIdx.x, static_cast<int64_t>(p.prep_rows) * gridDim.x * 256);
+    return;
+  }
   const int bh = blockIdx.x;
   const int b = bh / p.sh.Hkv;
   const int h = bh - b * p.sh.Hkv;
@@ -527,16 +534,18 @@ cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const C
 }  // namespace
 
 cudaError_t launch_attn_v16(int dv, const V16Params& p, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>(p.nkt));
-  if (dv == 128) {
-    if (p.lay.packed) attn_v16_kernel<128, true><<<grid, 256, 0, stream>>>(p);
-    else attn_v16_kernel<128, false><<<grid, 256, 0, stream>>>(p);
-  } else if (dv == 64) {
-    if (p.lay.packed) attn_v16_kernel<64, true><<<grid, 256, 0, stream>>>(p);
-    else attn_v16_kernel<64, false><<<grid, 256, 0, stream>>>(p);
-  } else {
+  const dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>(p.nkt + p.prep_rows));
+  const bool rope = p.prep_rows > 0;
+  decltype(&attn_v16_kernel<128, true, true>) kern;
+  if (dv == 128)
+    kern = p.lay.packed ? (rope ? attn_v16_kernel<128, true, true> : attn_v16_kernel<128, true, false>)
+                        : (rope ? attn_v16_kernel<128, false, true> : attn_v16_kernel<128, false, false>);
+  else if (dv == 64)
+    kern = p.lay.packed ? (rope ? attn_v16_kernel<64, true, true> : attn_v16_kernel<64, true, false>)
+                        : (rope ? attn_v16_kernel<64, false, true> : attn_v16_kernel<64, false, false>);
+  else
     return cudaErrorInvalidValue;
-  }
+  kern<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

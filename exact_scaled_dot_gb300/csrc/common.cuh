@@ -167,6 +167,45 @@ __device__ __forceinline__ TmaYZ k_tma(bool packed, const LayoutParams& L, int H
   return packed ? TmaYZ{h, L.cu_k[b] + j} : TmaYZ{j, b * Hkv + h};
 }
 
+// Token of query row i / key row j of batch element b: the row of its
+// positions and of its cos/sin table (padded b n + i, packed cu[b] + i).
+__host__ __device__ __forceinline__ int64_t q_token(bool packed, const LayoutParams& L, int n_q, int b, int64_t i) {
+  return packed ? static_cast<int64_t>(L.cu_q[b]) + i : static_cast<int64_t>(b) * n_q + i;
+}
+__host__ __device__ __forceinline__ int64_t k_token(bool packed, const LayoutParams& L, int n_k, int b, int64_t j) {
+  return packed ? static_cast<int64_t>(L.cu_k[b]) + j : static_cast<int64_t>(b) * n_k + j;
+}
+
+// Rotary embedding: the positions of the rows a kernel turns and the
+// frequencies w_k = base^(-2k/d), k < d/2, as fp32 pairs w_hi + w_lo (w_lo
+// the rounding residual of w_hi, so that the rounding of w does not grow
+// with the position).  pos == nullptr: no rotation.
+struct RotaryAngles {
+  const int32_t* pos;
+  float w_hi[64];
+  float w_lo[64];
+};
+
+// Rotated copies ahead of the attention kernels, over two segments (the
+// query and the key tokens): each writes its tokens' rows rotated, read from
+// the caller's strided tensor X and written contiguous in X's layout (padded
+// [B H][n][d], packed [T][H][d]).
+struct RopeSegment {
+  int64_t tokens;              // padded: B n; packed: T (0: empty segment)
+  int32_t n;                   // padded: rows per (b, h)
+  int32_t H;                   // heads of X
+  const int32_t* pos;          // [tokens]
+  const void* X;               // bf16 rows to rotate (strides sx)
+  TensorStrides sx;
+  void* Y;                     // rotated rows, contiguous
+};
+struct RopePrepParams {
+  int32_t d, packed;
+  RopeSegment seg[2];
+  float w_hi[64];              // as in RotaryAngles
+  float w_lo[64];
+};
+
 struct FwdParams {
   ShapeParams sh;
   MaskParams mask;
@@ -181,6 +220,7 @@ struct FwdParams {
   unsigned int* status;        // device status word
 };
 
+
 // The forward's fp16 copy of V: tile j of (b, h) re-encoded as V 2^vexp
 // (f16range.cuh), rows past the key length zero, in a [B Hkv][nkt 128][d_v]
 // buffer in both layouts.
@@ -193,6 +233,10 @@ struct V16Params {
   void* V16;                   // fp16 [B Hkv][nkt 128][d_v]
   int32_t* vexp;               // [B Hkv][nkt]; tiles past the key length are not written
   unsigned int* status;
+  // Rotary: prep_rows extra rows of blocks in the same launch work through
+  // rp (the rotated queries and keys); 0 without a rotary.
+  int32_t prep_rows;
+  RopePrepParams rp;
 };
 
 struct BwdParams {
@@ -211,7 +255,9 @@ struct BwdParams {
   void* dK;                    // bf16 [B][Hkv][n_k][d_h]
   void* dV;                    // bf16 [B][Hkv][n_k][d_v]
   unsigned int* status;
+  RotaryAngles rot;            // rotary: the keys' positions (dK turned back in the epilogue)
 };
+
 
 struct DecParams {
   ShapeParams sh;
@@ -261,18 +307,24 @@ cudaError_t launch_attn_decode(int dh, int dv, const CUtensorMap& tmK, const CUt
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);
+// rot_q: the queries' positions (rotary: Q is rotated as it is read), or nullptr.
 cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams& lay, int dv, int dh,
                                        const void* Q, const void* O, const void* O_lo, const void* dO, float* D,
                                        float4* tilemax, float2* grpexp, float* dQacc, void* Q16, void* dO16,
-                                       unsigned int* status, cudaStream_t stream);
+                                       const RotaryAngles* rot_q, unsigned int* status, cudaStream_t stream);
 cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap* tB, const GemmParams& p,
                              cudaStream_t stream);
+cudaError_t launch_rope_prep(const RopePrepParams& p, cudaStream_t stream);
 // heads_b = 0: one tensor (xb, yb unused).
 cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w_hi,
                         const float* w_lo, int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream);
 // dQ = scale * accumulator (elems elements of rows of dh); contiguous dQ, or
-// row r at (r / n_inner) s_outer + (r % n_inner) s_inner.
+// row r at (r / n_inner) s_outer + (r % n_inner) s_inner.  With rot_q (the
+// queries' positions) each row is turned back by its token's angles: the
+// token of row r is r / n_inner when packed (rows are tokens of Hq heads),
+// else (r / n_inner / Hq) n_inner + r % n_inner (rows are heads of n_q rows).
 cudaError_t launch_attn_bwd_finalize(int64_t elems, int dh, int n_inner, int64_t s_outer, int64_t s_inner,
-                                     bool contiguous, float scale, const float* dQacc, void* dQ, cudaStream_t stream);
+                                     bool contiguous, float scale, const float* dQacc, void* dQ,
+                                     const RotaryAngles* rot_q, bool packed, int Hq, cudaStream_t stream);
 
 }  // namespace esd

@@ -17,47 +17,17 @@
 // token, computes the four angles once (they depend on the position and the
 // block only) and rotates and stores the group.
 //
-// The angle a = p w is formed to about single-precision accuracy of the
-// reduced angle for every |p| < 2^24 (the positions an fp32 holds exactly).
-// Two errors would otherwise grow with p: the rounding of w itself, whose
-// 2^-24 relative error is worth 0.06 rad at p = 10^6 for w = 1, and the
-// reduction modulo 2 pi.  So w arrives as w_hi + w_lo (w_lo the rounding
-// residual of w_hi, both from the double-precision frequency), the product
-// p w_hi is split exactly into hi + lo with an fma, lo collects p w_lo, and
-// hi is reduced by a three-constant Cody-Waite scheme: 2 pi = C1 + C2 + C3
-// where C1 = 6.28125 has 8 significant bits.  For |hi| < 2^24 the quotient k
-// is below 2^22 and fmaf(-k, C1, hi) is exact (the difference is at most a
-// few thousand and lies on the grid of the finer of hi's unit in the last
-// place and C1's 2^-5, so it is representable); the C2 and C3 steps and the
-// final additions round a few times near |r| <= pi, which leaves a few
-// 10^-7 rad.  sincosf then takes the reduced angle.
+// The angle and the products come from rotary.cuh, shared with the cos/sin
+// tables and the rotations fused into the attention kernels.
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "rotary.cuh"
 
 namespace esd {
 namespace {
-
-// 2 pi = C1 + C2 + C3: C1 with trailing zero bits, C2 the fp32 rounding of
-// the rest, C3 that rounding's residual.
-constexpr float kTwoPiC1 = 6.28125f;
-constexpr float kTwoPiC2 = static_cast<float>(6.283185307179586476925 - 6.28125);
-constexpr float kTwoPiC3 = static_cast<float>(6.283185307179586476925 - 6.28125 - static_cast<double>(kTwoPiC2));
-constexpr float kInvTwoPi = 0.15915494309189535f;
-
-// p (w_hi + w_lo) reduced modulo 2 pi.
-__device__ __forceinline__ float reduced_angle(int32_t pos, float w_hi, float w_lo) {
-  const float p = static_cast<float>(pos);      // exact for |pos| < 2^24
-  const float hi = p * w_hi;
-  const float lo = fmaf(p, w_lo, fmaf(p, w_hi, -hi));   // p w_hi = hi + its residual, plus p w_lo
-  const float k = rintf(hi * kInvTwoPi);
-  float r = fmaf(-k, kTwoPiC1, hi);
-  r = fmaf(-k, kTwoPiC2, r);
-  r = fmaf(-k, kTwoPiC3, r);
-  return r + lo;
-}
 
 // One or two token-major tensors that share tokens and positions (the
 // queries and keys of a batch), rotated in one launch: the work items of
@@ -84,7 +54,6 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
   const int per_row = p.d / 8;
   const int64_t items0 = rope_items(p.tokens, p.heads[0], p.d);
   const int64_t total = items0 + rope_items(p.tokens, p.heads[1], p.d);
-  const float sgn = p.inverse ? -1.f : 1.f;
   for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u0 < total;
        u0 += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const bool second = u0 >= items0;
@@ -106,25 +75,33 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
 #pragma unroll
     for (int j = 0; j < kHeadGroup; ++j)
       if (h0 + j < h1) v[j] = x[base + static_cast<int64_t>(h0 + j) * per_row];
-    float sn[4], cs[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) sincosf(sgn * reduced_angle(pos, p.w_hi[4 * c + q], p.w_lo[4 * c + q]), &sn[q], &cs[q]);
+    float wh[4], wl[4];
+    rope_freqs4(p.w_hi, p.w_lo, c, wh, wl);
+    float4 t0, t1;
+    rope_angles4(pos, wh, wl, t0, t1);
+    if (p.inverse) rope_transpose(t0, t1);
 #pragma unroll
     for (int j = 0; j < kHeadGroup; ++j) {
       if (h0 + j >= h1) break;
-      const uint32_t in[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      uint32_t out[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float a = bf16_lo(in[q]), b = bf16_hi(in[q]);
-        out[q] = pack_bf16x2(a * cs[q] - b * sn[q], a * sn[q] + b * cs[q]);
-      }
-      y[base + static_cast<int64_t>(h0 + j) * per_row] = make_uint4(out[0], out[1], out[2], out[3]);
+      y[base + static_cast<int64_t>(h0 + j) * per_row] = rot_bf16x8(v[j], t0, t1);
     }
   }
 }
 
+__global__ void __launch_bounds__(256) rope_prep_kernel(const __grid_constant__ RopePrepParams p) {
+  rope_prep_range(p, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                  static_cast<int64_t>(gridDim.x) * blockDim.x);
+}
+
 }  // namespace
+
+cudaError_t launch_rope_prep(const RopePrepParams& p, cudaStream_t stream) {
+  int64_t blocks = ((p.seg[0].tokens + p.seg[1].tokens) * (p.d / 8) + 255) / 256;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  if (blocks < 1) blocks = 1;
+  rope_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w_hi,
                         const float* w_lo, int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream) {

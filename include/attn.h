@@ -84,7 +84,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 10
+#define ATTN_ABI_VERSION 11
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -127,11 +127,6 @@ typedef struct {
   const int32_t* kv_len;   /* NULL (= n_k for all) or HOST array [B], each in [1,n_k] */
 } attn_mask;
 
-/* Bytes of device workspace attn_fwd needs: an fp16 copy of V in 128-key
- * tiles with one exponent per tile, about B*Hkv*ceil(n_k/128)*128*(2*d_v)
- * bytes.  The layout is private to the library.  Returns 0 for an invalid
- * shape. */
-size_t attn_fwd_workspace_bytes(const attn_shape* shape);
 
 /* Element strides of one tensor whose innermost index (d) is contiguous:
  * `row` = elements between consecutive rows of one head (between
@@ -159,12 +154,57 @@ typedef struct {
   attn_tensor_strides q, k, v, o, dO, dq, dk, dv;
 } attn_strides;
 
+/* Rotary position embedding fused into the attention entry points
+ * ("Chapter 15 -- matrix formulas", section 15.6: the scores are those of
+ * the rotated rows q~_i = R_i q_i, k~_j = R_j k_j; "Chapter 31 -- attention
+ * backprop", section 5: the gradients of q and k are those of q~ and k~
+ * turned back by the opposite angles).  NULL = no rotation.  The rotation is
+ * attn_rope's (same angles, same bf16 rounding of each rotated row), over
+ * the whole width d_h of Q and K; V is not rotated.  The forward with a
+ * rotary equals, bit for bit, attn_rope on Q and K followed by the forward
+ * without one.  The backward takes the un-rotated Q and K and returns the
+ * gradients of the un-rotated Q and K; their turn back happens in fp32,
+ * before the one rounding to bf16.
+ * pos_q, pos_k: device int32 positions of every query / key row: padded
+ * [B][n_q] and [B][n_k] (row i of batch element b at b * n + i), packed
+ * [T_q] and [T_k]; |pos| < 2^24 (see attn_rope).  base finite and > 1
+ * (ATTN_ERR_SCALE); NULL positions give ATTN_ERR_NULL.
+ * q_rot, k_rot (optional, 16-byte aligned, device): the rotated rows, bf16
+ * in Q's and K's contiguous layouts ([B][Hq][n_q][d_h] and
+ * [B][Hkv][n_k][d_h]; packed [T_q][Hq][d_h] and [T_k][Hkv][d_h]).  The
+ * forward writes its rotated queries and keys there (else into its
+ * workspace); a backward given them reads them instead of rotating Q and K
+ * again (they must hold what the forward wrote for the same Q, K and
+ * positions; the backward's Q and K arguments are then not read for the
+ * rows' values).  Keeping them is the trade an unfused rotation makes, which
+ * keeps the rotated rows for the attention's backward.  Without them the
+ * backward turns Q as it reads it and writes a rotated copy of K into its
+ * workspace.  Pass the same rotary to the workspace-size functions: a
+ * workspace holds the rotated rows that have no caller buffer.  The decode
+ * forward takes no rotary (rotate its few queries with attn_rope; a key
+ * cache holds rotated keys). */
+typedef struct {
+  float base;             /* w_k = base^(-2k/d_h), k < d_h/2                     */
+  const int32_t* pos_q;   /* DEVICE positions of the query rows                   */
+  const int32_t* pos_k;   /* DEVICE positions of the key rows                     */
+  void* q_rot;            /* DEVICE rotated queries, or NULL                      */
+  void* k_rot;            /* DEVICE rotated keys, or NULL                         */
+} attn_rotary;
+
+/* Bytes of device workspace attn_fwd needs: an fp16 copy of V in 128-key
+ * tiles with one exponent per tile, about B*Hkv*ceil(n_k/128)*128*(2*d_v)
+ * bytes, plus with a rotary the rotated rows it has no buffer for
+ * (B*Hq*n_q*2*d_h bytes of queries, B*Hkv*n_k*2*d_h of keys).  The layout
+ * is private to the library.  Returns 0 for an invalid shape or rotary. */
+size_t attn_fwd_workspace_bytes(const attn_shape* shape, const attn_rotary* rotary);
+
 /* Forward pass (A.10.1-A.10.3).  Inputs Q, K, V (bf16, device); outputs
  * O (bf16) and LSE (fp32, natural log), both device, fully overwritten.
  * `workspace`: caller-owned device memory of at least
  * attn_fwd_workspace_bytes(shape) bytes, 256-byte aligned (ATTN_ERR_WORKSPACE
  * otherwise); its contents on entry do not matter.  Two launches on
- * `stream`: V re-encoded into the workspace, then the forward kernel.
+ * `stream`: V re-encoded into the workspace (with a rotary, the same launch
+ * writes the rotated queries and keys), then the forward kernel.
  *
  * O_lo (optional here, NULL to skip; required by the backward): bf16
  * [B][Hq][n_q][d_v] receiving the rounding residual of O, so that O + O_lo
@@ -174,7 +214,8 @@ typedef struct {
  * key row; bf16 rounding of O alone then moves dQ and dK beyond the stated
  * tolerance (measured: up to 2.2x on the peaked cross-attention workload,
  * 4x on smaller peaked cases). */
-int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+int attn_fwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
+             const attn_rotary* rotary, float scale,
              const void* Q, const void* K, const void* V,
              void* O, float* LSE, void* O_lo,
              void* workspace, size_t workspace_bytes, void* stream);
@@ -199,9 +240,11 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
 /* Bytes of device workspace the backward needs (attn_bwd and its three
  * stages): row terms D, per-128-row-tile bounds used to scale dS, an fp32
  * dQ accumulator and fp16 copies of Q and dO, about
- * B*Hq*n_q*(6*d_h + 2*d_v + 4) bytes.
- * The layout is private to the library.  Returns 0 for an invalid shape. */
-size_t attn_bwd_workspace_bytes(const attn_shape* shape);
+ * B*Hq*n_q*(6*d_h + 2*d_v + 4) bytes, plus with a rotary and no k_rot a
+ * rotated copy of K, B*Hkv*n_k*2*d_h bytes.
+ * The layout is private to the library.  Returns 0 for an invalid shape or
+ * rotary. */
+size_t attn_bwd_workspace_bytes(const attn_shape* shape, const attn_rotary* rotary);
 
 /* Backward pass (A.10.5-A.10.9).  Q, K, V, O, O_lo, LSE must be those of
  * the forward call with the same mask and scale ("Chapter 31", section 3:
@@ -220,7 +263,8 @@ size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * (exact at any scale, see Precision above), the weights A are rounded once
  * to fp16, and dS enters dK and dQ in fp16 scaled by a power of two derived
  * from a bound on |dS|. */
-int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
+             const attn_rotary* rotary, float scale,
              const void* Q, const void* K, const void* V,
              const void* O, const void* O_lo, const void* dO, const float* LSE,
              void* dQ, void* dK, void* dV,
@@ -231,7 +275,8 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides*
  * zeroed dQ accumulator and Q and dO re-encoded as fp16 with per-tile
  * exponents (see attn_bwd), all in `workspace`.  Q is the forward's bf16
  * query tensor, dO the bf16 upstream gradient. */
-int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const void* Q, const void* O,
+int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const attn_rotary* rotary,
+                        const void* Q, const void* O,
                         const void* O_lo, const void* dO, void* workspace,
                         size_t workspace_bytes, void* stream);
 
@@ -240,13 +285,20 @@ int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, co
  * the workspace's fp16 copy (also written by stage 1), writes dK (scaled)
  * and dV (bf16) and adds the dS K products into the workspace's fp32 dQ
  * accumulator (zeroed by stage 1). */
-int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
+                  const attn_rotary* rotary, float scale,
                   const void* K, const void* V, const float* LSE,
                   void* workspace, size_t workspace_bytes,
                   void* dK, void* dV, void* stream);
 
-/* Stage 3: dQ = scale * accumulator, rounded to bf16. */
-int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, float scale, const void* workspace,
+/* Stage 3: dQ = scale * accumulator, rounded to bf16.
+ *
+ * With a rotary, the three stages take the same one: stage 1 rotates Q as
+ * it reads it (or reads q_rot), stage 2 writes the rotated keys into the
+ * workspace (one extra launch; or reads k_rot) and turns dK back, stage 3
+ * turns dQ back. */
+int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, const attn_rotary* rotary,
+                      float scale, const void* workspace,
                       size_t workspace_bytes, void* dQ, void* stream);
 
 /* The backward pass without any device allocation, for callers that cannot
@@ -267,7 +319,8 @@ int attn_bwd_finalize(const attn_shape* shape, const attn_strides* strides, floa
  * buffer, whose contents persist between calls: the kernels clear what must
  * start at zero, but calls that overlap on the GPU race and must be
  * serialised by the caller. */
-int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides, float scale,
+int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
+                     const attn_rotary* rotary, float scale,
                      const void* Q, const void* K, const void* V,
                      const void* O, const void* O_lo, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, void* stream);
@@ -313,19 +366,22 @@ typedef struct {
 int64_t attn_varlen_visible_pairs(const attn_varlen* v);
 
 /* Workspace of attn_fwd_varlen, about B*Hkv*ceil(max len_k/128)*128*(2*d_v)
- * bytes (the fp16 V tiles are laid out per sequence); 0 when the
- * description is invalid. */
-size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v);
+ * bytes (the fp16 V tiles are laid out per sequence), plus with a rotary
+ * the rotated rows without a caller buffer ((T_q*Hq + T_k*Hkv)*2*d_h bytes
+ * at most); 0 when the description is invalid. */
+size_t attn_fwd_varlen_workspace_bytes(const attn_varlen* v, const attn_rotary* rotary);
 
-int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
+int attn_fwd_varlen(const attn_varlen* v, const attn_strides* strides, const attn_rotary* rotary, float scale,
+                    const void* Q, const void* K,
                     const void* V,
                     void* O, float* LSE, void* O_lo, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace of attn_bwd_varlen, about T_q*Hq*(6*d_h + 2*d_v + 4) bytes; 0 when the
  * description is invalid. */
-size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v);
+size_t attn_bwd_varlen_workspace_bytes(const attn_varlen* v, const attn_rotary* rotary);
 
-int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, float scale, const void* Q, const void* K,
+int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, const attn_rotary* rotary, float scale,
+                    const void* Q, const void* K,
                     const void* V,
                     const void* O, const void* O_lo, const void* dO, const float* LSE,
                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,

@@ -35,7 +35,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 10
+    assert esd.attn_abi_version() == 11
 
 
 def test_strerror_covers_every_code(lib):
@@ -45,10 +45,10 @@ def test_strerror_covers_every_code(lib):
     assert lib.attn_strerror(999).decode() == "unknown status"
 
 
-def _call_fwd(lib, shape, mask, scale=None, ptr=256, ws=256, ws_bytes=1 << 40, strides=None):
+def _call_fwd(lib, shape, mask, scale=None, ptr=256, ws=256, ws_bytes=1 << 40, strides=None, rotary=None):
     p = ctypes.c_void_p(ptr)
     scale = 1.0 / math.sqrt(max(shape.d_h, 1)) if scale is None else scale
-    return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None, strides,
+    return lib.attn_fwd(ctypes.byref(shape), ctypes.byref(mask) if mask is not None else None, strides, rotary,
                         ctypes.c_float(scale), p, p, p, p, p, None, ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes),
                         None)
 
@@ -114,19 +114,19 @@ def test_fwd_workspace_checks(lib):
     """The forward's workspace (fp16 V tiles and their exponents) must be
     present, 256-byte aligned and large enough; checked before any CUDA call."""
     s = _shape(n_k=300, d_v=64, d_h=128)
-    need = lib.attn_fwd_workspace_bytes(ctypes.byref(s))
+    need = lib.attn_fwd_workspace_bytes(ctypes.byref(s), None)
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
     tiles = 2 * 2 * 3     # B * Hkv * ceil(300 / 128)
     assert need == r256(tiles * 128 * 64 * 2) + r256(tiles * 4)
     assert _call_fwd(lib, s, _mask(), ws=0, ws_bytes=need) == bnd.ATTN_ERR_WORKSPACE
     assert _call_fwd(lib, s, _mask(), ws=512 + 16, ws_bytes=need) == bnd.ATTN_ERR_WORKSPACE
     assert _call_fwd(lib, s, _mask(), ws=512, ws_bytes=need - 1) == bnd.ATTN_ERR_WORKSPACE
-    assert lib.attn_fwd_workspace_bytes(ctypes.byref(_shape(B=0))) == 0
+    assert lib.attn_fwd_workspace_bytes(ctypes.byref(_shape(B=0)), None) == 0
 
 
 def test_bwd_workspace_checks(lib):
     s = _shape()
-    need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
+    need = lib.attn_bwd_workspace_bytes(ctypes.byref(s), None)
     rows = 2 * 4 * 100
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
     # D | tile bounds and exponents | group exponents | fp32 dQ accumulator | fp16 copies of Q and dO
@@ -134,11 +134,11 @@ def test_bwd_workspace_checks(lib):
                     + r256(rows * 128 * 2) + r256(rows * s.d_v * 2))
     p = ctypes.c_void_p(256)
     m = _mask()
-    args = [ctypes.byref(s), ctypes.byref(m), None, ctypes.c_float(0.1)] + [p] * 10
+    args = [ctypes.byref(s), ctypes.byref(m), None, None, ctypes.c_float(0.1)] + [p] * 10
     assert lib.attn_bwd(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512), ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
-    assert lib.attn_bwd_workspace_bytes(ctypes.byref(_shape(B=0))) == 0
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(_shape(B=0)), None) == 0
 
 
 def test_bwd_requires_the_output_residual(lib):
@@ -146,19 +146,19 @@ def test_bwd_requires_the_output_residual(lib):
     cross-attention gradients miss the tolerance, so every backward entry
     point refuses a NULL O_lo with ATTN_ERR_NULL before any CUDA call."""
     s = _shape()
-    need = lib.attn_bwd_workspace_bytes(ctypes.byref(s))
+    need = lib.attn_bwd_workspace_bytes(ctypes.byref(s), None)
     p = ctypes.c_void_p(256)
     m = _mask()
-    head = [ctypes.byref(s), ctypes.byref(m), None, ctypes.c_float(0.1)]
+    head = [ctypes.byref(s), ctypes.byref(m), None, None, ctypes.c_float(0.1)]
     # Q, K, V, O, O_lo = NULL, dO, LSE, dQ, dK, dV
     assert lib.attn_bwd(*head, p, p, p, p, None, p, p, p, p, p, p, ctypes.c_size_t(need),
                         None) == bnd.ATTN_ERR_NULL
-    assert lib.attn_bwd_preprocess(ctypes.byref(s), None, p, p, None, p, p, ctypes.c_size_t(need),
+    assert lib.attn_bwd_preprocess(ctypes.byref(s), None, None, p, p, None, p, p, ctypes.c_size_t(need),
                                    None) == bnd.ATTN_ERR_NULL
     assert lib.attn_bwd_noalloc(*head, p, p, p, p, None, p, p, p, p, p, None) == bnd.ATTN_ERR_NULL
     v = _varlen([0, 100], [0, 100])
-    vneed = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v))
-    assert lib.attn_bwd_varlen(ctypes.byref(v), None, ctypes.c_float(0.1), p, p, p, p, None, p, p, p, p, p, p,
+    vneed = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v), None)
+    assert lib.attn_bwd_varlen(ctypes.byref(v), None, None, ctypes.c_float(0.1), p, p, p, p, None, p, p, p, p, p, p,
                                ctypes.c_size_t(vneed), None) == bnd.ATTN_ERR_NULL
 
 
@@ -221,8 +221,8 @@ def test_varlen_checks(lib):
     before any CUDA call."""
     p = ctypes.c_void_p(256)
     big = ctypes.c_size_t(1 << 40)
-    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), None, ctypes.c_float(0.1), p, p, p, p, p, None, p,  # noqa: E731
-                                        big, None)
+    fwd = lambda v: lib.attn_fwd_varlen(ctypes.byref(v), None, None, ctypes.c_float(0.1), p, p, p, p, p, None,  # noqa: E731
+                                        p, big, None)
     assert fwd(_varlen([1, 3], [0, 3])) == bnd.ATTN_ERR_SHAPE          # cu[0] != 0
     assert fwd(_varlen([0, 5, 3], [0, 5, 6])) == bnd.ATTN_ERR_SHAPE    # decreasing
     assert fwd(_varlen([0, 3], [0, 0])) == bnd.ATTN_ERR_EMPTY_ROW      # queries, no keys
@@ -231,19 +231,19 @@ def test_varlen_checks(lib):
     assert fwd(_varlen([0, 3], [0, 3], Hq=3)) == bnd.ATTN_ERR_SHAPE
     assert fwd(_varlen([0, 3], [0, 3], d_h=96, d_v=96)) == bnd.ATTN_ERR_UNSUPPORTED
     assert fwd(_varlen([0, 3], [0, 3], B=0)) == bnd.ATTN_ERR_SHAPE
-    assert lib.attn_fwd_varlen(None, None, ctypes.c_float(0.1), p, p, p, p, p, None, p, big, None) == bnd.ATTN_ERR_NULL
-    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), None, ctypes.c_float(0.0), p, p, p, p, p, None,
+    assert lib.attn_fwd_varlen(None, None, None, ctypes.c_float(0.1), p, p, p, p, p, None, p, big, None) == bnd.ATTN_ERR_NULL
+    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), None, None, ctypes.c_float(0.0), p, p, p, p, p, None,
                                p, big, None) == bnd.ATTN_ERR_SCALE
-    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), None, ctypes.c_float(0.1), p, p, p,
+    assert lib.attn_fwd_varlen(ctypes.byref(_varlen([0, 3], [0, 3])), None, None, ctypes.c_float(0.1), p, p, p,
                                ctypes.c_void_p(0x1008), p, None, p, big, None) == bnd.ATTN_ERR_ALIGN
     # the forward workspace: present, aligned, large enough
     v3 = _varlen([0, 3, 200], [0, 3, 300])
-    need = lib.attn_fwd_varlen_workspace_bytes(ctypes.byref(v3))
+    need = lib.attn_fwd_varlen_workspace_bytes(ctypes.byref(v3), None)
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
     assert need == r256(2 * 2 * 3 * 128 * 128 * 2) + r256(2 * 2 * 3 * 4)   # B Hkv ceil(297/128) tiles
-    assert lib.attn_fwd_varlen(ctypes.byref(v3), None, ctypes.c_float(0.1), p, p, p, p, p, None, None,
+    assert lib.attn_fwd_varlen(ctypes.byref(v3), None, None, ctypes.c_float(0.1), p, p, p, p, p, None, None,
                                ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
-    assert lib.attn_fwd_varlen(ctypes.byref(v3), None, ctypes.c_float(0.1), p, p, p, p, p, None, p,
+    assert lib.attn_fwd_varlen(ctypes.byref(v3), None, None, ctypes.c_float(0.1), p, p, p, p, p, None, p,
                                ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
     # no query rows at all: nothing to compute, OK without touching the GPU
     assert fwd(_varlen([0, 0, 0], [0, 4, 9])) == bnd.ATTN_OK
@@ -252,14 +252,14 @@ def test_varlen_checks(lib):
 def test_varlen_workspace_and_pairs(lib):
     cq, ck = [0, 100, 100, 357], [0, 150, 170, 600]
     v = _varlen(cq, ck, causal=1, Hq=4, Hkv=2, d_h=128, d_v=64)
-    need = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v))
+    need = lib.attn_bwd_varlen_workspace_bytes(ctypes.byref(v), None)
     rows = cq[-1] * 4
     nqt = (257 + 127) // 128
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
     assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 16) + r256(3 * 2 * 8) + r256(rows * 128 * 4)
                     + r256(rows * 128 * 2) + r256(rows * 64 * 2))
     p = ctypes.c_void_p(512)
-    args = [ctypes.byref(v), None, ctypes.c_float(0.1)] + [p] * 10
+    args = [ctypes.byref(v), None, None, ctypes.c_float(0.1)] + [p] * 10
     assert lib.attn_bwd_varlen(*args, None, ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_varlen(*args, ctypes.c_void_p(512 + 16), ctypes.c_size_t(need), None) == bnd.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_varlen(*args, p, ctypes.c_size_t(need - 1), None) == bnd.ATTN_ERR_WORKSPACE
@@ -351,8 +351,8 @@ def test_strides_validated(lib):
     assert _call_fwd(lib, s, _mask(), strides=ctypes.byref(_strides(dk=(8, 8)))) == bnd.ATTN_ERR_SHAPE
     v = _varlen([0, 100], [0, 100])
     p = ctypes.c_void_p(256)
-    rc = lib.attn_fwd_varlen(ctypes.byref(v), ctypes.byref(_strides(q=(3 * 128 + 4, 128))), ctypes.c_float(0.1),
-                             p, p, p, p, p, None, p, ctypes.c_size_t(1 << 40), None)
+    rc = lib.attn_fwd_varlen(ctypes.byref(v), ctypes.byref(_strides(q=(3 * 128 + 4, 128))), None,
+                             ctypes.c_float(0.1), p, p, p, p, p, None, p, ctypes.c_size_t(1 << 40), None)
     assert rc == bnd.ATTN_ERR_ALIGN
 
 
@@ -383,3 +383,46 @@ def test_binding_reads_view_strides():
     one = torch.empty((1, n, H, 128), dtype=torch.bfloat16).transpose(1, 2)
     pst = bnd._strides_arg(False, q=one).contents
     assert (pst.q.row, pst.q.head) == (H * 128, 128)
+
+
+def test_rotary_checks_and_workspace_sizes(lib):
+    """attn_rotary: base finite and > 1, both position arrays present and
+    4-byte aligned, the optional rotated-row buffers 16-byte aligned, all
+    checked before any CUDA call; a workspace holds the rotated rows that
+    have no caller buffer (the forward's queries and keys, the backward's
+    keys)."""
+    s = _shape(n_q=100, n_k=300)
+    r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
+    rot = bnd.AttnRotary(10000.0, 256, 512)
+    f0 = lib.attn_fwd_workspace_bytes(ctypes.byref(s), None)
+    f1 = lib.attn_fwd_workspace_bytes(ctypes.byref(s), ctypes.byref(rot))
+    assert f1 == f0 + r256(2 * 100 * 4 * 128 * 2) + r256(2 * 300 * 2 * 128 * 2)
+    kept = bnd.AttnRotary(10000.0, 256, 512, 4096, 8192)
+    assert lib.attn_fwd_workspace_bytes(ctypes.byref(s), ctypes.byref(kept)) == f0
+    b0 = lib.attn_bwd_workspace_bytes(ctypes.byref(s), None)
+    b1 = lib.attn_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(rot))
+    assert b1 == b0 + r256(2 * 300 * 2 * 128 * 2)
+    assert lib.attn_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(kept)) == b0
+    v = _varlen([0, 3, 200], [0, 3, 300])
+    vf0 = lib.attn_fwd_varlen_workspace_bytes(ctypes.byref(v), None)
+    vf1 = lib.attn_fwd_varlen_workspace_bytes(ctypes.byref(v), ctypes.byref(rot))
+    assert vf1 == vf0 + r256(200 * 4 * 128 * 2) + r256(300 * 2 * 128 * 2)
+    bad = [(bnd.AttnRotary(1.0, 256, 512), bnd.ATTN_ERR_SCALE), (bnd.AttnRotary(float("nan"), 256, 512),
+                                                                   bnd.ATTN_ERR_SCALE),
+           (bnd.AttnRotary(10000.0, None, 512), bnd.ATTN_ERR_NULL), (bnd.AttnRotary(10000.0, 256, None),
+                                                                      bnd.ATTN_ERR_NULL),
+           (bnd.AttnRotary(10000.0, 258, 512), bnd.ATTN_ERR_ALIGN),
+           (bnd.AttnRotary(10000.0, 256, 512, 0x1008, None), bnd.ATTN_ERR_ALIGN)]
+    p = ctypes.c_void_p(256)
+    for r, code in bad:
+        assert _call_fwd(lib, s, _mask(), rotary=ctypes.byref(r)) == code
+        assert lib.attn_fwd_workspace_bytes(ctypes.byref(s), ctypes.byref(r)) == 0
+        assert lib.attn_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(r)) == 0
+        m = _mask()
+        assert lib.attn_bwd(ctypes.byref(s), ctypes.byref(m), None, ctypes.byref(r), ctypes.c_float(0.1),
+                            *([p] * 10), p, ctypes.c_size_t(1 << 40), None) == code
+    # a workspace sized without the rotary is too small for a call with one
+    m = _mask()
+    assert lib.attn_bwd(ctypes.byref(s), ctypes.byref(m), None, ctypes.byref(rot), ctypes.c_float(0.1),
+                        *([p] * 10), ctypes.c_void_p(512), ctypes.c_size_t(b0), None) == bnd.ATTN_ERR_WORKSPACE
+    assert _call_fwd(lib, s, _mask(), ws=512, ws_bytes=f0, rotary=ctypes.byref(rot)) == bnd.ATTN_ERR_WORKSPACE

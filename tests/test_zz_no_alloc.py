@@ -72,6 +72,7 @@ def test_noalloc_refuses_problems_beyond_its_buffer():
     assert esd.attn_bwd_workspace_bytes(4, 16, 16, 2048, 2048, 128, 128) > esd.attn_bwd_noalloc_max_scratch_bytes()
     mask = bnd.AttnMask(1, 0, bnd.ATTN_OFFSET_DEFAULT, ctypes.POINTER(ctypes.c_int32)())
     p = ctypes.c_void_p(256)
-    rc = lib.attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(mask), None, ctypes.c_float(0.088), p, p, p, p, None,
+    rc = lib.attn_bwd_noalloc(ctypes.byref(shape), ctypes.byref(mask), None, None, ctypes.c_float(0.088), p, p, p, p,
+                              None,
                               p, p, p, p, p, None)
     assert rc == esd.ATTN_ERR_WORKSPACE
