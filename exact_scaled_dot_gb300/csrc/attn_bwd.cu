@@ -529,7 +529,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // sl2 = scale log2e 2^-(k + q); and dS' = 2^g dS =
     // P (dP_acc cp + (-D) dmul) with cp = 2^(g - o - v), dmul = 2^g.
     float sl2 = p.scale_log2, cp = 1.f, dmul = 1.f;
-    uint32_t pw[32];
+    // The weights P of this thread's 64 columns, kept in fp32 from the P pass
+    // for the dS pass (the fp16 copy goes to tensor memory for dV).
+    float pf[64];
     // This thread's -LSE log2(e) and -D entries (query q0 + 64h + tid, for
     // tid < 64) of a step, loaded one step ahead so the global latency is
     // off the critical path.  Both are kept negated so that one paired
@@ -586,8 +588,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (!ok) break;
       tc_fence_after_sync();
       // P pass: this half's 64 scores in registers (two loads, one wait).
-      // P^T (fp16) goes into X over the columns already read; the same
-      // words stay in registers for the dS pass.
+      // P^T (fp16) goes into X over the columns already read; the fp32
+      // weights stay in registers for the dS pass (no fp16 unpacking there:
+      // 1.4-1.9 % of the main kernel on c3 and c5 in same-box runs).
       {
         uint32_t sa[32], sb[32];
         tmem_ld32_nowait(tX + 64 * h, sa);
@@ -619,9 +622,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
               x1 = (!row_masked && c + 1 >= cmin && (!PACKED || c + 1 < cmax)) ? x1 : -INFINITY;
             }
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            const uint32_t pk = pack_f16x2(p0, p1);
-            w[k >> 1] = pk;
-            pw[cq * 8 + (k >> 1)] = pk;
+            w[k >> 1] = pack_f16x2(p0, p1);
+            pf[cq * 16 + k] = p0;
+            pf[cq * 16 + k + 1] = p1;
           }
           tmem_st8_nowait(tX + 64 * h + cq * 8, w);
         }
@@ -660,8 +663,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const float g1 = __uint_as_float(cq < 2 ? da[r + 1] : db[r + 1]);
             float t0, t1, d0, d1;
             ffma2(t0, t1, g0, g1, cp, cp, nd[k], nd[k + 1]);
-            const uint32_t pp = pw[cq * 8 + (k >> 1)];
-            fmul2(d0, d1, f16_lo(pp), f16_hi(pp), t0, t1);
+            fmul2(d0, d1, pf[cq * 16 + k], pf[cq * 16 + k + 1], t0, t1);
             if (need_mask) {
               d0 = (!row_masked && c >= cmin && (!PACKED || c < cmax)) ? d0 : 0.f;
               d1 = (!row_masked && c + 1 >= cmin && (!PACKED || c + 1 < cmax)) ? d1 : 0.f;
