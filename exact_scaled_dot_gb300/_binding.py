@@ -44,7 +44,7 @@ EXPORTS = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_varlen_workspace_by
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight",
-           "attn_proj_bwd_input", "attn_rope", "attn_rope_qk")
+           "attn_proj_bwd_input", "attn_rope", "attn_rope_qk", "attn_bwd_head_split")
 
 
 class AttnError(RuntimeError):
@@ -114,6 +114,8 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_bwd_main.argtypes = [S, M, ST, RT, f, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
     lib.attn_bwd_finalize.argtypes = [S, ST, RT, f, _vp, ctypes.c_size_t, _vp, _vp]
     lib.attn_visible_pairs.argtypes = [S, M]
+    lib.attn_bwd_head_split.argtypes = [S, M]
+    lib.attn_bwd_head_split.restype = ctypes.c_int
     lib.attn_visible_pairs.restype = ctypes.c_int64
     lib.attn_get_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.attn_clear_status.argtypes = []
@@ -503,6 +505,16 @@ def attn_visible_pairs(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, causal=False, causal_o
     shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
     m = _MaskArg(causal, causal_offset, kv_len)
     return int(load().attn_visible_pairs(ctypes.byref(shape), ctypes.byref(m.mask)))
+
+
+def attn_bwd_head_split(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, causal=False, causal_offset=None, kv_len=None) -> int:
+    """How the backward main kernel splits each KV head's query heads on the current device (1 = not)."""
+    shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    rc = int(load().attn_bwd_head_split(ctypes.byref(shape), ctypes.byref(m.mask)))
+    if rc < 0:
+        raise AttnError(-rc, "attn_bwd_head_split")
+    return rc
 
 
 def attn_get_status() -> int:

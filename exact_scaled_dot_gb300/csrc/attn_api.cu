@@ -6,7 +6,10 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -321,6 +324,7 @@ struct DeviceInfo {
   bool probed = false;
   bool ok = false;
   unsigned int* status = nullptr;
+  int sms = 0;
 };
 
 std::mutex g_dev_mu;
@@ -342,6 +346,7 @@ int device_status_ptr(unsigned int** out) {
     void* sym = nullptr;
     if (major == 10 && minor == 3) {
       if (cudaGetSymbolAddress(&sym, g_attn_status) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ERR_CUDA;
       d.status = static_cast<unsigned int*>(sym);
       d.ok = true;
     }
@@ -350,6 +355,14 @@ int device_status_ptr(unsigned int** out) {
   if (!d.ok) return ATTN_ERR_DEVICE;
   *out = d.status;
   return ATTN_OK;
+}
+
+// SMs of the current device (after device_status_ptr succeeded on it).
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 148;
 }
 
 ShapeParams shape_params(const attn_shape* s) {
@@ -370,7 +383,9 @@ int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq 
 // fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h] | fp16 copy
 // of dO [rows * d_v], each 256-byte aligned.
 // With a rotary, then the rotated keys bf16 [tokens_k Hkv][d_h]
-// (contiguous in the keys' layout).
+// (contiguous in the keys' layout).  When the launch may split a KV head's
+// query heads across CTAs (head_split_possible), then the fp32 sums of dK
+// and dV, [tokens_k Hkv][d_h] and [tokens_k Hkv][d_v], one after the other.
 struct Workspace {
   float* D;
   float4* tilemax;
@@ -379,8 +394,71 @@ struct Workspace {
   void* Q16;
   void* dO16;
   void* Kr;
+  float* dKacc;
+  float* dVacc;
+  size_t kv_elems;
   size_t bytes;
 };
+
+// A query-head split is considered when the KV head groups have several
+// query heads and the launch has fewer than two CTAs per SM of the largest
+// part (152 SMs): longer launches fill the GPU by themselves.
+constexpr int64_t kSplitCtaLimit = 2 * 152;
+
+bool head_split_possible(int B, int Hq, int Hkv, int n_k) {
+  const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((n_k + kTileN - 1) / kTileN);
+  return Hq / Hkv > 1 && ctas < kSplitCtaLimit;
+}
+
+// The query-head split of the backward main kernel: 1, or the divisor z of
+// the group (up to 16) whose launch is predicted to finish first, by at
+// least 3 %.  The prediction dispatches the CTAs in launch order (blockIdx.x
+// fastest, then y, then z) to whichever of `sms` SMs frees first; a CTA
+// costs its visible (query tile, head) steps plus a fixed 5 steps of set-up
+// and epilogue, and 2 more when it adds its dK, dV share into the sums.
+int choose_head_split(const attn_shape* s, const MaskParams& m, int sms) {
+  if (!head_split_possible(s->B, s->Hq, s->Hkv, s->n_k)) return 1;
+  const int group = s->Hq / s->Hkv;
+  const int nkt = (s->n_k + kTileN - 1) / kTileN;
+  // Visible query tiles of key tile jt of batch element b.
+  std::vector<int> vis(static_cast<size_t>(s->B) * nkt);
+  for (int b = 0; b < s->B; ++b) {
+    const int64_t nq_b = query_len(m, s->n_q, b);
+    const int nqt = static_cast<int>((nq_b + kTileM - 1) / kTileM);
+    for (int jt = 0; jt < nkt; ++jt) {
+      const int64_t i_first = first_row_seeing_key(m, s->n_q, s->n_k, b, static_cast<int64_t>(jt) * kTileN);
+      vis[static_cast<size_t>(b) * nkt + jt] = i_first < nq_b ? nqt - static_cast<int>(i_first / kTileM) : 0;
+    }
+  }
+  auto makespan = [&](int z) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < sms; ++i) free_at.push(0.0);
+    double end = 0.0;
+    const double fixed = z > 1 ? 7.0 : 5.0;
+    for (int zz = 0; zz < z; ++zz)
+      for (int jt = 0; jt < nkt; ++jt)
+        for (int bk = 0; bk < s->B * s->Hkv; ++bk) {
+          const int b = bk / s->Hkv;
+          const double t = free_at.top() + vis[static_cast<size_t>(b) * nkt + jt] * (group / z) + fixed;
+          free_at.pop();
+          free_at.push(t);
+          end = std::max(end, t);
+        }
+    return end;
+  };
+  int best = 1;
+  double best_t = makespan(1);
+  const double base_t = best_t;
+  for (int z = 2; z <= std::min(group, 16); ++z) {
+    if (group % z) continue;
+    const double t = makespan(z);
+    if (t < best_t) {
+      best_t = t;
+      best = z;
+    }
+  }
+  return best_t < 0.97 * base_t ? best : 1;
+}
 
 // The rotary part of a workspace: tokens of the queries and keys (padded
 // B n, packed T), and which rotated rows live in the workspace (those
@@ -414,6 +492,15 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base, co
   if (rt.on && rt.k_ws) {
     w.Kr = b + end;
     end += round256(static_cast<size_t>(rt.k) * s->Hkv * s->d_h * 2);
+  }
+  w.dKacc = w.dVacc = nullptr;
+  w.kv_elems = 0;
+  if (head_split_possible(s->B, s->Hq, s->Hkv, s->n_k)) {
+    const size_t kv_rows = static_cast<size_t>(rt.k) * s->Hkv;
+    w.dKacc = reinterpret_cast<float*>(b + end);
+    w.dVacc = w.dKacc + kv_rows * s->d_h;
+    w.kv_elems = kv_rows * (s->d_h + s->d_v);
+    end += round256(w.kv_elems * sizeof(float));
   }
   w.bytes = end;
   return w;
@@ -723,6 +810,17 @@ const char* attn_strerror(int status) {
   }
 }
 
+int attn_bwd_head_split(const attn_shape* shape, const attn_mask* mask) {
+  if (check_shape(shape) != ATTN_OK) return -ATTN_ERR_SHAPE;
+  MaskParams m;
+  const int rc = build_mask(shape, mask, &m);
+  if (rc) return -rc;
+  unsigned int* status = nullptr;
+  const int dc = device_status_ptr(&status);
+  if (dc) return -dc;
+  return choose_head_split(shape, m, device_sms());
+}
+
 int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask) {
   if (check_shape(shape) != ATTN_OK) return -1;
   MaskParams m;
@@ -954,7 +1052,15 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_str
   if (rotary) p.rot = rotary_angles(rotary, rotary->pos_k, shape->d_h);
   else p.rot.pos = nullptr;
   p.status = status;
-  const cudaError_t e = launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, tdq, p, st);
+  p.hsplit = rotary ? 1 : choose_head_split(shape, p.mask, device_sms());
+  p.dKacc = w.dKacc;
+  p.dVacc = w.dVacc;
+  if (p.hsplit > 1 && launch_zero_f32(w.dKacc, static_cast<int64_t>(w.kv_elems), st) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  cudaError_t e = launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, tdq, p, st);
+  if (e == cudaSuccess && p.hsplit > 1)
+    e = launch_attn_bwd_kv_finalize(p.sh, p.lay, static_cast<int64_t>(shape->B) * shape->n_k, shape->d_h,
+                                    shape->d_v, w.dKacc, w.dVacc, dK, dV, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -1367,7 +1473,14 @@ int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, const att
   if (rotary) p.rot = rk;
   else p.rot.pos = nullptr;
   p.status = status;
+  p.hsplit = rotary ? 1 : choose_head_split(&d.shape, d.mask, device_sms());
+  p.dKacc = w.dKacc;
+  p.dVacc = w.dVacc;
+  if (p.hsplit > 1 && launch_zero_f32(w.dKacc, static_cast<int64_t>(w.kv_elems), st) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   e = launch_attn_bwd_main(v->d_h, v->d_v, tq, tk, tv, tdo, tdq, p, st);
+  if (e == cudaSuccess && p.hsplit > 1)
+    e = launch_attn_bwd_kv_finalize(sh, d.lay, d.total_k, v->d_h, v->d_v, w.dKacc, w.dVacc, dK, dV, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   // Packed accumulator rows: tokens of Hq heads.
   e = launch_attn_bwd_finalize(d.total_q * v->Hq * v->d_h, v->d_h, v->Hq, d.lay.sdq.row, d.lay.sdq.head,

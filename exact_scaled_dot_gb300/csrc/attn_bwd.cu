@@ -202,7 +202,7 @@ __device__ __noinline__ CtaScale cta_scale(const float* red, float2 qo) {
   return c;
 }
 
-template <int DH, int DV, bool PACKED, bool ROPE>
+template <int DH, int DV, bool PACKED, bool ROPE, bool SPLIT>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -239,8 +239,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   // kv_len get zeros); in the packed layout rows past the sequence belong to
   // another one.
   const int64_t k_row_end = PACKED ? klen : p.sh.n_k;
-  const int total = per_head * p.sh.group;
-  auto step_head = [&](int s) { return hkv * p.sh.group + s / per_head; };
+  // Query-head split (SPLIT): this CTA takes heads [z hps, (z + 1) hps) of
+  // the group, z = blockIdx.z.
+  const int hps = SPLIT ? p.sh.group / p.hsplit : p.sh.group;
+  const int total = per_head * hps;
+  const int head0 = hkv * p.sh.group + (SPLIT ? static_cast<int>(blockIdx.z) * hps : 0);
+  auto step_head = [&](int s) { return head0 + s / per_head; };
   auto step_q0 = [&](int s) { return (qt_first + s % per_head) * kTileM; };
 
   if (threadIdx.x == 0) {
@@ -845,7 +849,69 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       ok = wait_all(C::kBarDKDV, 0);
       tc_fence_after_sync();
     }
-    if (ok) {
+    if constexpr (SPLIT) {
+     if (ok) {
+      // This CTA's share of dK, dV, in fp32, added into the split's sums
+      // (dK turned back by the rotary first: the turn is linear).  The
+      // tensor-memory loads are warp-collective: every lane takes part, and
+      // only the rows inside the sequence are added.
+      const int64_t j = j0 + row;
+      const bool in = j < k_row_end;
+      if (total > 0) {
+        const float dk_scale = p.scale * exp2_int(-cs.g - cs.q);
+        const float dv_scale = exp2_int(-cs.o);
+        const int64_t arow = PACKED ? (static_cast<int64_t>(p.lay.cu_k[b]) + j) * p.sh.Hkv + hkv
+                                    : (static_cast<int64_t>(b) * p.sh.Hkv + hkv) * p.sh.n_k + j;
+        int32_t kpos = 0;
+        if constexpr (ROPE) kpos = in ? p.rot.pos[k_token(PACKED, p.lay, p.sh.n_k, b, j)] : 0;
+#pragma unroll 1
+        for (int cc = 0; cc < DH / 32; ++cc) {
+          tmem_ld32(tmem + lane_base + C::kTdK + cc * 32, rr);
+          float y[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) y[k] = __uint_as_float(rr[k]) * dk_scale;
+          if constexpr (ROPE) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float wh[4], wl[4];
+              rope_freqs4(p.rot.w_hi, p.rot.w_lo, 4 * cc + q4, wh, wl);
+              float4 t0, t1;
+              rope_angles4(kpos, wh, wl, t0, t1);
+              rope_transpose(t0, t1);
+              const float cs4[4] = {t0.x, t0.z, t1.x, t1.z}, sn4[4] = {t0.y, t0.w, t1.y, t1.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int k = 8 * q4 + 2 * q;
+                rot_block(y[k], y[k + 1], cs4[q], sn4[q], y[k], y[k + 1]);
+              }
+            }
+          }
+          float* dst = p.dKacc + arow * DH + cc * 32;
+          if (in) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * c), "f"(y[4 * c]),
+                           "f"(y[4 * c + 1]), "f"(y[4 * c + 2]), "f"(y[4 * c + 3])
+                           : "memory");
+          }
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < DV / 32; ++cc) {
+          tmem_ld32(tmem + lane_base + C::kTdV + cc * 32, rr);
+          float* dst = p.dVacc + arow * DV + cc * 32;
+          if (in) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * c),
+                           "f"(__uint_as_float(rr[4 * c]) * dv_scale), "f"(__uint_as_float(rr[4 * c + 1]) * dv_scale),
+                           "f"(__uint_as_float(rr[4 * c + 2]) * dv_scale),
+                           "f"(__uint_as_float(rr[4 * c + 3]) * dv_scale)
+                           : "memory");
+          }
+        }
+      }
+     }
+    } else if (ok) {
       const int64_t j = j0 + row;
       const bool in = j < k_row_end;
       uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) +
@@ -1337,18 +1403,67 @@ attn_bwd_finalize_kernel(int64_t n8, float scale, const float4* __restrict__ acc
   }
 }
 
+__global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ p, int64_t n4) {
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n4; k += nthreads)
+    p[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dK and dV of a query-head split: accumulator row r = token Hkv + h (packed)
+// or (b Hkv + h) n_k + j (padded), eight columns per work item, rounded to
+// bf16 into the caller's strided tensors.  The K items come first.
+struct KvFinParams {
+  int64_t rows;                // tokens_k Hkv
+  int32_t dh, dv, Hkv, n_k, packed;
+  TensorStrides sdk, sdv;
+  const float4* dKacc;
+  const float4* dVacc;
+  uint4* dK;
+  uint4* dV;
+};
+
+__global__ void __launch_bounds__(256) attn_bwd_kv_finalize_kernel(const __grid_constant__ KvFinParams p) {
+  const int64_t items_k = p.rows * (p.dh / 8);
+  const int64_t total = items_k + p.rows * (p.dv / 8);
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u0 < total; u0 += nthreads) {
+    const bool is_v = u0 >= items_k;
+    const int64_t u = is_v ? u0 - items_k : u0;
+    const int c8 = (is_v ? p.dv : p.dh) / 8;
+    const int64_t r = u / c8;
+    const int c = static_cast<int>(u - r * c8);
+    int64_t off;
+    const TensorStrides& st = is_v ? p.sdv : p.sdk;
+    if (p.packed) {
+      const int64_t t = r / p.Hkv, h = r - t * p.Hkv;
+      off = t * st.row + h * st.head;
+    } else {
+      const int64_t bh = r / p.n_k, j = r - bh * p.n_k;
+      off = bh * st.head + j * st.row;
+    }
+    const float4* a = (is_v ? p.dVacc : p.dKacc) + u * 2;
+    const float4 x = a[0], y = a[1];
+    (is_v ? p.dV : p.dK)[off / 8 + c] = make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w),
+                                                  pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+  }
+}
+
 template <int DH, int DV>
 cudaError_t launch_bwd_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                               const CUtensorMap& tmdO, const CUtensorMap& tmdQ, const BwdParams& p,
                               cudaStream_t stream) {
   using C = BwdCfg<DH, DV>;
-  auto kern = p.rot.pos ? (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, true>
-                                      : attn_bwd_main_kernel<DH, DV, false, true>)
-                      : (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, false>
-                                      : attn_bwd_main_kernel<DH, DV, false, false>);
+  // The split runs without a rotary only (the host never asks for both).
+  auto kern = p.rot.pos ? (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, true, false>
+                                        : attn_bwd_main_kernel<DH, DV, false, true, false>)
+              : p.hsplit > 1 ? (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, false, true>
+                                             : attn_bwd_main_kernel<DH, DV, false, false, true>)
+                             : (p.lay.packed ? attn_bwd_main_kernel<DH, DV, true, false, false>
+                                             : attn_bwd_main_kernel<DH, DV, false, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN));
+  dim3 grid(static_cast<unsigned>(p.sh.B * p.sh.Hkv), static_cast<unsigned>((p.sh.n_k + kTileN - 1) / kTileN),
+            static_cast<unsigned>(p.hsplit));
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, tmdO, tmdQ, p);
   return cudaGetLastError();
 }
@@ -1433,6 +1548,32 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams
   } else {
     return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_f32(float* ptr, int64_t n, cudaStream_t stream) {
+  const int64_t n4 = n / 4;
+  zero_f32_kernel<<<grid_for(n4), 256, 0, stream>>>(reinterpret_cast<float4*>(ptr), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_kv_finalize(const ShapeParams& sh, const LayoutParams& lay, int64_t tokens_k, int dh,
+                                        int dv, const float* dKacc, const float* dVacc, void* dK, void* dV,
+                                        cudaStream_t stream) {
+  KvFinParams p;
+  p.rows = tokens_k * sh.Hkv;
+  p.dh = dh;
+  p.dv = dv;
+  p.Hkv = sh.Hkv;
+  p.n_k = sh.n_k;
+  p.packed = lay.packed;
+  p.sdk = lay.sdk;
+  p.sdv = lay.sdv;
+  p.dKacc = reinterpret_cast<const float4*>(dKacc);
+  p.dVacc = reinterpret_cast<const float4*>(dVacc);
+  p.dK = static_cast<uint4*>(dK);
+  p.dV = static_cast<uint4*>(dV);
+  attn_bwd_kv_finalize_kernel<<<grid_for(p.rows * ((dh + dv) / 8)), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

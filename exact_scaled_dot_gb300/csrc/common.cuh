@@ -256,6 +256,13 @@ struct BwdParams {
   void* dV;                    // bf16 [B][Hkv][n_k][d_v]
   unsigned int* status;
   RotaryAngles rot;            // rotary: the keys' positions (dK turned back in the epilogue)
+  // Query-head split: blockIdx.z of hsplit takes group / hsplit of the KV
+  // head's query heads; with hsplit > 1 every CTA adds its fp32 share of dK,
+  // dV into dKacc, dVacc (rows [tokens_k Hkv][d], zeroed beforehand) instead
+  // of writing dK, dV.
+  int32_t hsplit;
+  float* dKacc;
+  float* dVacc;
 };
 
 
@@ -318,6 +325,14 @@ cudaError_t launch_rope_prep(const RopePrepParams& p, cudaStream_t stream);
 // heads_b = 0: one tensor (xb, yb unused).
 cudaError_t launch_rope(int64_t tokens, int d, int heads_a, int heads_b, const int32_t* pos, const float* w_hi,
                         const float* w_lo, int inverse, const void* xa, void* ya, const void* xb, void* yb, cudaStream_t stream);
+// Zero n floats (n a multiple of 4, 16-byte aligned).
+cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t stream);
+// dK, dV (bf16, caller strides) from the fp32 sums of a query-head split:
+// rows of (b, h) in the accumulators are [tokens_k Hkv][d] (padded token
+// b n_k + j, row (b Hkv + h) n_k + j; packed row token Hkv + h).
+cudaError_t launch_attn_bwd_kv_finalize(const ShapeParams& sh, const LayoutParams& lay, int64_t tokens_k, int dh,
+                                        int dv, const float* dKacc, const float* dVacc, void* dK, void* dV,
+                                        cudaStream_t stream);
 // dQ = scale * accumulator (elems elements of rows of dh); contiguous dQ, or
 // row r at (r / n_inner) s_outer + (r % n_inner) s_inner.  With rot_q (the
 // queries' positions) each row is turned back by its token's angles: the

@@ -69,6 +69,11 @@ WORKLOADS: Dict[str, Workload] = {
                                     seed=1004),
     "mqa_chunked_prefill": Workload("mqa_chunked_prefill", B=1, Hq=64, Hkv=1, nq=1024, nk=16384,
                                     dh=128, dv=128, causal=True, seed=1005),
+    # One causal MQA sequence: 32 key tiles, so the backward's CTAs (one per
+    # key tile of the single KV head) would fill a fifth of the GPU without
+    # the query-head split.  Not one of the five benchmark configurations.
+    "mqa_single_sequence": Workload("mqa_single_sequence", B=1, Hq=32, Hkv=1, nq=4096, nk=4096,
+                                    dh=128, dv=128, causal=True, seed=1006),
     # Short query blocks over a long key cache (decode and small chunks of new
     # queries): causal with the bottom-right offset n_k - n_q, ragged cache
     # lengths.  Forward only; HBM-bound (the K/V cache is read once).

@@ -241,7 +241,10 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
  * stages): row terms D, per-128-row-tile bounds used to scale dS, an fp32
  * dQ accumulator and fp16 copies of Q and dO, about
  * B*Hq*n_q*(6*d_h + 2*d_v + 4) bytes, plus with a rotary and no k_rot a
- * rotated copy of K, B*Hkv*n_k*2*d_h bytes.
+ * rotated copy of K, B*Hkv*n_k*2*d_h bytes, plus, when the KV head groups
+ * have several query heads and B*Hkv*ceil(n_k/128) < 304 (a launch that
+ * may split them, see attn_bwd_head_split), fp32 sums of dK and dV,
+ * B*Hkv*n_k*4*(d_h + d_v) bytes.
  * The layout is private to the library.  Returns 0 for an invalid shape or
  * rotary. */
 size_t attn_bwd_workspace_bytes(const attn_shape* shape, const attn_rotary* rotary);
@@ -327,6 +330,18 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_
 
 /* Size in bytes of the static buffer attn_bwd_noalloc uses. */
 size_t attn_bwd_noalloc_max_scratch_bytes(void);
+
+/* How attn_bwd_main divides the work of each KV head on the current
+ * device: 1 = one CTA per (batch, KV head, key tile), taking every query
+ * head of the group ("Appendix A.10", section A.10.5: dK, dV summed over
+ * the group); z > 1 = the group's query heads split over z CTAs, each adding
+ * its fp32 share of dK, dV into sums in the workspace that a last launch
+ * rounds into dK, dV.  Chosen when the launch has too few CTAs to fill the
+ * GPU (a long-history MQA chunk: one KV head, few key tiles) and the split
+ * is predicted to finish at least 3 % sooner; never with a rotary.
+ * Negative ATTN_ERR_* on an invalid shape or mask.  Informational: the
+ * calls choose by themselves. */
+int attn_bwd_head_split(const attn_shape* shape, const attn_mask* mask);
 
 /* Number of visible (i, j) pairs over all batch elements and query heads,
  * from the same closed form the kernels use to classify tiles; -1 on an

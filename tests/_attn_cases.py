@@ -73,6 +73,15 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rtol=RT
             f"worst at {idx}: gpu={got[idx]!r} ref={ref[idx]!r}")
 
 
+def assert_same_sum(got: torch.Tensor, ref: torch.Tensor, what: str):
+    """Two results of the same sums accumulated in a different order: dQ
+    always, dK and dV when the backward splits a KV head's query heads over
+    several CTAs (their fp32 shares are added in whatever order the CTAs
+    finish).  Equal up to the last bits of the fp32 sums, which can move the
+    bf16 rounding that follows by one unit (a relative 2^-8 to 2^-7)."""
+    assert_close(f64(got), f64(ref), what, atol=1e-3, rtol=8e-3)
+
+
 def max_err(got, ref) -> float:
     return float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))))
 

@@ -1,14 +1,14 @@
 """The three backward stage calls, run one by one on one workspace, give the
-same gradients as the composite attn_bwd (dK, dV bit for bit: the same
-kernels visit the same tiles in the same order; dQ within the parity
-tolerance, since its fp32 accumulation order varies between runs), and a
+same gradients as the composite attn_bwd (up to the order of fp32 sums:
+dQ's always varies between runs, dK's and dV's when the backward splits a
+KV head's query heads over several CTAs), and a
 workspace reused across two problems carries nothing over."""
 import pytest
 import torch
 
 from exact_scaled_dot_gb300.inputs import Workload, make_inputs
 
-from _attn_cases import assert_close, f64
+from _attn_cases import assert_close, assert_same_sum, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,8 @@ def test_stages_equal_composite(w):
     ws = torch.empty((esd.attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.nq, w.nk, w.dh, w.dv),),
                      dtype=torch.uint8, device="cuda:0")
     (dQ, dK, dV), (rQ, rK, rV) = _staged(w, inp, ws)
-    assert torch.equal(dK, rK) and torch.equal(dV, rV)
+    assert_same_sum(dK, rK, "dK")
+    assert_same_sum(dV, rV, "dV")
     assert_close(f64(dQ), f64(rQ), "dQ", atol=1e-3, rtol=1e-3)
 
 
@@ -66,5 +67,6 @@ def test_workspace_reused_across_problems():
     ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda:0")   # NaN patterns everywhere
     _staged(a, make_inputs(a), ws)
     (dQ, dK, dV), (rQ, rK, rV) = _staged(b, make_inputs(b), ws)
-    assert torch.equal(dK, rK) and torch.equal(dV, rV)
+    assert_same_sum(dK, rK, "dK")
+    assert_same_sum(dV, rV, "dV")
     assert_close(f64(dQ), f64(rQ), "dQ", atol=1e-3, rtol=1e-3)

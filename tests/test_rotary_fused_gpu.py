@@ -27,7 +27,7 @@ import torch
 
 from exact_scaled_dot_gb300.inputs import VarlenWorkload, Workload, make_inputs, make_varlen_inputs
 
-from _attn_cases import LSE_ATOL, assert_close, f64, problem_of
+from _attn_cases import LSE_ATOL, assert_close, assert_same_sum, f64, problem_of
 
 pytestmark = pytest.mark.gpu
 
@@ -156,7 +156,8 @@ def test_fused_forward_equals_separate_rotation(name):
 def test_fused_backward_agrees_with_separate_composition():
     """The separate composition rounds dQ~, dK~ to bf16 before turning them
     back; the fused backward turns them in fp32 and rounds once.  dV is the
-    same product of the same operands (bit for bit); dQ, dK agree within the
+    same product of the same operands (up to the order of its fp32 sums);
+    dQ, dK agree within the
     usual tolerance (the composition's extra rounding is 2^-9 of dQ~'s
     components, which can exceed the small element two components cancel to,
     so the bound is the absolute 1e-2, not one relative to dQ)."""
@@ -174,15 +175,14 @@ def test_fused_backward_agrees_with_separate_composition():
     dQr, dKr, dV = esd.attn_bwd(Qr, Kr, V, O, G, L, O_lo=Olo, causal=True, kv_len=kv)
     dQ, dK = _rope_padded_gpu(dQr, pq, base, inverse=True), _rope_padded_gpu(dKr, pq, base, inverse=True)
     torch.cuda.synchronize()
-    assert torch.equal(res["dV"], dV)
+    assert_same_sum(res["dV"], dV, "dV")
     assert_close(f64(res["dQ"]), f64(dQ), "dQ vs separate")
     assert_close(f64(res["dK"]), f64(dK), "dK vs separate")
 
 
 def test_staged_and_noalloc_backward_with_rotary():
     """The three stage calls with the same rotary, and attn_bwd_noalloc, equal
-    the composite attn_bwd (dK, dV bit for bit; dQ up to the order of its
-    fp32 accumulation)."""
+    the composite attn_bwd (up to the order of their fp32 sums)."""
     import exact_scaled_dot_gb300 as esd
     w = PADDED["mha_d64"]
     inp = make_inputs(w)
@@ -201,7 +201,8 @@ def test_staged_and_noalloc_backward_with_rotary():
     torch.cuda.synchronize()
     assert esd.attn_get_status() == 0
     for got in ((dQ, dK, dV), (nQ, nK, nV)):
-        assert torch.equal(got[1], res["dK"]) and torch.equal(got[2], res["dV"])
+        assert_same_sum(got[1], res["dK"], "dK")
+        assert_same_sum(got[2], res["dV"], "dV")
         assert_close(f64(got[0]), f64(res["dQ"]), "dQ", atol=1e-3, rtol=1e-3)
 
 
@@ -301,8 +302,8 @@ def test_rotary_with_strided_fused_qkv():
     torch.cuda.synchronize()
     assert esd.attn_get_status() == 0
     for i, name in enumerate(("O", "LSE", "dQ", "dK", "dV")):
-        if name == "dQ":
-            assert_close(f64(outs[0][i]), f64(outs[1][i]), name, atol=1e-3, rtol=1e-3)
+        if name in ("dQ", "dK", "dV"):
+            assert_same_sum(outs[0][i], outs[1][i], name)
         else:
             assert torch.equal(outs[0][i], outs[1][i]), name
 
@@ -312,7 +313,7 @@ def test_rotated_row_residuals(orc, name):
     """With q_rot, k_rot the forward leaves its rotated rows there (equal, bit
     for bit, to attn_rope's) and a backward given them reads them instead of
     rotating again: its gradients equal those of the backward that rotates
-    by itself (dK, dV bit for bit; dQ up to its accumulation order), and
+    by itself (up to the order of their fp32 sums), and
     match the oracle."""
     import exact_scaled_dot_gb300 as esd
     w = PADDED[name]
@@ -332,7 +333,8 @@ def test_rotated_row_residuals(orc, name):
     g2 = esd.attn_bwd(Q, K, V, O, G, L, O_lo=Olo, causal=w.causal, kv_len=kv, rotary=plain)
     torch.cuda.synchronize()
     assert esd.attn_get_status() == 0
-    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    assert_same_sum(g1[1], g2[1], "dK")
+    assert_same_sum(g1[2], g2[2], "dV")
     assert_close(f64(g1[0]), f64(g2[0]), "dQ", atol=1e-3, rtol=1e-3)
     ref = _oracle_rotary(orc, w, inp, pq.numpy(), pk.numpy(), base)
     for k, got in zip(("dQ", "dK", "dV"), g1):

@@ -15,9 +15,10 @@ copies, without copying:
   sequence-major [1, n, H, d] tensor.
 
 Each case is compared element by element with the fp64 oracle (the usual
-1e-2 + 2e-2 |ref|, LSE 1e-3) and bit for bit with the same call on
-contiguous copies (the kernels visit the same tiles in the same order; dQ is
-compared at 1e-3 since its fp32 accumulation order may differ).  Outputs
+1e-2 + 2e-2 |ref|, LSE 1e-3) and with the same call on contiguous copies:
+O, O_lo and LSE bit for bit (the kernels visit the same tiles in the same
+order), dQ, dK and dV at 1e-3 (fp32 sums whose order may differ: dQ always,
+dK and dV when the backward splits a KV head's query heads).  Outputs
 start as NaN, and the padding around every output view holds a sentinel that
 must survive: a kernel writing outside its view fails the test.
 """
@@ -26,7 +27,7 @@ import torch
 
 from exact_scaled_dot_gb300.inputs import VarlenWorkload, Workload, make_inputs, make_varlen_inputs
 
-from _attn_cases import LSE_ATOL, assert_close, f64, problem_of, varlen_reference
+from _attn_cases import LSE_ATOL, assert_close, assert_same_sum, f64, problem_of, varlen_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -152,8 +153,8 @@ def test_fused_qkv_packed_views(orc, name):
     _exact(O, O2, "O")
     _exact(O_lo, Olo2, "O_lo")
     _exact(LSE, L2, "LSE")
-    _exact(dK, dK2, "dK")
-    _exact(dV, dV2, "dV")
+    assert_same_sum(dK, dK2, "dK")
+    assert_same_sum(dV, dV2, "dV")
     assert_close(f64(dQ), f64(dQ2), "dQ vs contiguous", atol=1e-3, rtol=1e-3)
 
 
@@ -234,8 +235,8 @@ def test_padded_strided_views(orc, w):
     _exact(O, O2, "O")
     _exact(O_lo, Olo2, "O_lo")
     _exact(LSE, L2, "LSE")
-    _exact(dK, dK2, "dK")
-    _exact(dV, dV2, "dV")
+    assert_same_sum(dK, dK2, "dK")
+    assert_same_sum(dV, dV2, "dV")
     assert_close(f64(dQ), f64(dQ2), "dQ vs contiguous", atol=1e-3, rtol=1e-3)
 
 
@@ -271,8 +272,8 @@ def test_sequence_major_batch_element(orc):
     esd.attn_bwd_main(K, V, LSE, ws, dK3, dV3, shape=shape, causal=True)
     esd.attn_bwd_finalize(ws, dQ3, shape=shape)
     _status_ok()
-    _exact(dK3, dK, "staged dK")
-    _exact(dV3, dV, "staged dV")
+    assert_same_sum(dK3, dK, "staged dK")
+    assert_same_sum(dV3, dV, "staged dV")
     assert_close(f64(dQ3), f64(dQ), "staged dQ", atol=1e-3, rtol=1e-3)
 
 
