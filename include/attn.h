@@ -338,7 +338,9 @@ size_t attn_bwd_noalloc_max_scratch_bytes(void);
  * its fp32 share of dK, dV into sums in the workspace that a last launch
  * rounds into dK, dV.  Chosen when the launch has too few CTAs to fill the
  * GPU (a long-history MQA chunk: one KV head, few key tiles) and the split
- * is predicted to finish at least 3 % sooner; never with a rotary.
+ * is predicted to finish at least 3 % sooner; never with a rotary.  With
+ * a split, dK and dV are fp32 sums added in whatever order the CTAs finish
+ * (as dQ always is), so two runs may differ in the last bf16 unit.
  * Negative ATTN_ERR_* on an invalid shape or mask.  Informational: the
  * calls choose by themselves. */
 int attn_bwd_head_split(const attn_shape* shape, const attn_mask* mask);
