@@ -44,7 +44,7 @@ EXPORTS = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_varlen_workspace_by
            "attn_selftest_wait_timeout", "attn_strerror", "attn_abi_version", "attn_bwd_noalloc",
            "attn_bwd_noalloc_max_scratch_bytes", "attn_varlen_visible_pairs", "attn_fwd_varlen",
            "attn_bwd_varlen_workspace_bytes", "attn_bwd_varlen", "attn_proj_fwd", "attn_proj_bwd_weight",
-           "attn_proj_bwd_input", "attn_rope", "attn_rope_qk", "attn_bwd_head_split")
+           "attn_proj_bwd_input", "attn_rope", "attn_rope_qk", "attn_bwd_head_split", "attn_bwd_persistent")
 
 
 class AttnError(RuntimeError):
@@ -116,6 +116,8 @@ def load(path: Optional[Path] = None) -> ctypes.CDLL:
     lib.attn_visible_pairs.argtypes = [S, M]
     lib.attn_bwd_head_split.argtypes = [S, M]
     lib.attn_bwd_head_split.restype = ctypes.c_int
+    lib.attn_bwd_persistent.argtypes = [S, M, RT]
+    lib.attn_bwd_persistent.restype = ctypes.c_int
     lib.attn_visible_pairs.restype = ctypes.c_int64
     lib.attn_get_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.attn_clear_status.argtypes = []
@@ -515,6 +517,17 @@ def attn_bwd_head_split(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, causal=False, causal_
     if rc < 0:
         raise AttnError(-rc, "attn_bwd_head_split")
     return rc
+
+
+def attn_bwd_persistent(B, Hq, Hkv, n_q, n_k, d_h, d_v, *, causal=False, causal_offset=None, kv_len=None,
+                        rotary=None) -> bool:
+    """Whether the backward main kernel runs its persistent schedule for this problem on the current device."""
+    shape = make_shape(B, Hq, Hkv, n_q, n_k, d_h, d_v)
+    m = _MaskArg(causal, causal_offset, kv_len)
+    rc = int(load().attn_bwd_persistent(ctypes.byref(shape), ctypes.byref(m.mask), _rot_size_arg(rotary)))
+    if rc < 0:
+        raise AttnError(-rc, "attn_bwd_persistent")
+    return rc == 1
 
 
 def attn_get_status() -> int:

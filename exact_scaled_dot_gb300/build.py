@@ -19,7 +19,8 @@ BUILD = PKG / "_build"
 LIB = PKG / "libesd_attn.so"
 INCLUDE = PKG.parent / "include"
 
-SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu", "proj_gemm.cu", "rope.cu", "attn_api.cu"]
+SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "attn_bwd_persist.cu", "attn_decode.cu", "proj_gemm.cu", "rope.cu",
+           "attn_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

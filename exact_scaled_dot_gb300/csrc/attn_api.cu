@@ -379,9 +379,10 @@ ShapeParams shape_params(const attn_shape* s) {
 int64_t q_rows(const attn_shape* s) { return static_cast<int64_t>(s->B) * s->Hq * s->n_q; }
 
 // Backward workspace: D [rows] | per-query-tile maxima and fp16 exponents
-// float4 [B*Hq*nqt] | per-group fp16 exponents float2 [B*Hkv] |
-// fp32 dQ accumulator [rows * d_h] | fp16 copy of Q [rows * d_h] | fp16 copy
-// of dO [rows * d_v], each 256-byte aligned.
+// float4 [B*Hq*nqt] | per-group fp16 exponents float2 [B*Hkv] | the main
+// kernel's work counter (256 bytes) | fp32 dQ accumulator [rows * d_h] |
+// fp16 copy of Q [rows * d_h] | fp16 copy of dO [rows * d_v], each 256-byte
+// aligned.
 // With a rotary, then the rotated keys bf16 [tokens_k Hkv][d_h]
 // (contiguous in the keys' layout).  When the launch may split a KV head's
 // query heads across CTAs (head_split_possible), then the fp32 sums of dK
@@ -390,6 +391,7 @@ struct Workspace {
   float* D;
   float4* tilemax;
   float2* grpexp;
+  unsigned int* work_ctr;
   float* dQacc;
   void* Q16;
   void* dO16;
@@ -410,54 +412,91 @@ bool head_split_possible(int B, int Hq, int Hkv, int n_k) {
   return Hq / Hkv > 1 && ctas < kSplitCtaLimit;
 }
 
-// The query-head split of the backward main kernel: 1, or the divisor z of
-// the group (up to 16) whose launch is predicted to finish first, by at
-// least 3 %.  The prediction dispatches the CTAs in launch order (blockIdx.x
-// fastest, then y, then z) to whichever of `sms` SMs frees first; a CTA
-// costs its visible (query tile, head) steps plus a fixed 5 steps of set-up
-// and epilogue, and 2 more when it adds its dK, dV share into the sums.
-int choose_head_split(const attn_shape* s, const MaskParams& m, int sms) {
-  if (!head_split_possible(s->B, s->Hq, s->Hkv, s->n_k)) return 1;
+// The backward main kernel's plan: its schedule (one CTA per work item, or
+// persistent CTAs taking items from a counter) and the query-head split z
+// (1, or a divisor of the group up to 16 that splits each KV head's query
+// heads over z items).
+struct BwdPlan {
+  int hsplit;
+  bool persistent;
+};
+
+// Items whose mean step count (128-query tiles times query heads) exceeds
+// this run on the grid kernel: its steps are some 5-10 % faster, and with
+// this many steps its fixed cost per item (about 3.5 steps) matters less
+// than that.  Measured crossover on GB300: persistent ahead with 4, 8.5
+// and 33 steps per item, the grid kernel with 62 and 80.
+constexpr double kPersistentMaxSteps = 40.0;
+
+// The split z is the one predicted to finish first, by at least 3 %.  The
+// prediction hands the items out in the order the schedule starts them to
+// whichever of `sms` CTAs frees first.  Grid: in launch order (blockIdx.x,
+// the (batch, KV head) index, fastest, then the key tile, then z), an item
+// costing its visible (query tile, head) steps plus 5 steps of set-up and
+// epilogue (7 when it adds its dK, dV share into the sums).  Persistent: in
+// item number order ((batch, KV head) fastest, then z, then the key tile),
+// as the work counter hands them out, plus one step of hand-over between
+// items (two with the sums).
+BwdPlan choose_bwd_plan(const attn_shape* s, const MaskParams& m, int sms, bool rotary) {
   const int group = s->Hq / s->Hkv;
   const int nkt = (s->n_k + kTileN - 1) / kTileN;
+  const int bk_n = s->B * s->Hkv;
   // Visible query tiles of key tile jt of batch element b.
   std::vector<int> vis(static_cast<size_t>(s->B) * nkt);
+  double steps = 0.0, active = 0.0;
   for (int b = 0; b < s->B; ++b) {
     const int64_t nq_b = query_len(m, s->n_q, b);
     const int nqt = static_cast<int>((nq_b + kTileM - 1) / kTileM);
     for (int jt = 0; jt < nkt; ++jt) {
       const int64_t i_first = first_row_seeing_key(m, s->n_q, s->n_k, b, static_cast<int64_t>(jt) * kTileN);
-      vis[static_cast<size_t>(b) * nkt + jt] = i_first < nq_b ? nqt - static_cast<int>(i_first / kTileM) : 0;
+      const int v = i_first < nq_b ? nqt - static_cast<int>(i_first / kTileM) : 0;
+      vis[static_cast<size_t>(b) * nkt + jt] = v;
+      steps += static_cast<double>(v) * group * s->Hkv;
+      active += v > 0 ? s->Hkv : 0;
     }
   }
-  auto makespan = [&](int z) {
+  auto makespan = [&](int z, bool persistent) {
     std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
     for (int i = 0; i < sms; ++i) free_at.push(0.0);
     double end = 0.0;
-    const double fixed = z > 1 ? 7.0 : 5.0;
-    for (int zz = 0; zz < z; ++zz)
+    const double fixed = persistent ? (z > 1 ? 2.0 : 1.0) : (z > 1 ? 7.0 : 5.0);
+    auto take = [&](int jt, int bk) {
+      const int b = bk / s->Hkv;
+      const double t = free_at.top() + vis[static_cast<size_t>(b) * nkt + jt] * (group / z) + fixed;
+      free_at.pop();
+      free_at.push(t);
+      end = std::max(end, t);
+    };
+    if (persistent) {
       for (int jt = 0; jt < nkt; ++jt)
-        for (int bk = 0; bk < s->B * s->Hkv; ++bk) {
-          const int b = bk / s->Hkv;
-          const double t = free_at.top() + vis[static_cast<size_t>(b) * nkt + jt] * (group / z) + fixed;
-          free_at.pop();
-          free_at.push(t);
-          end = std::max(end, t);
-        }
+        for (int zz = 0; zz < z; ++zz)
+          for (int bk = 0; bk < bk_n; ++bk) take(jt, bk);
+    } else {
+      for (int zz = 0; zz < z; ++zz)
+        for (int jt = 0; jt < nkt; ++jt)
+          for (int bk = 0; bk < bk_n; ++bk) take(jt, bk);
+    }
     return end;
   };
-  int best = 1;
-  double best_t = makespan(1);
-  const double base_t = best_t;
-  for (int z = 2; z <= std::min(group, 16); ++z) {
-    if (group % z) continue;
-    const double t = makespan(z);
-    if (t < best_t) {
-      best_t = t;
-      best = z;
+  const bool may_split = !rotary && head_split_possible(s->B, s->Hq, s->Hkv, s->n_k);
+  auto best_split = [&](bool persistent) {
+    int best = 1;
+    double best_t = makespan(1, persistent);
+    const double base_t = best_t;
+    for (int z = 2; may_split && z <= std::min(group, 16); ++z) {
+      if (group % z) continue;
+      const double t = makespan(z, persistent);
+      if (t < best_t) {
+        best_t = t;
+        best = z;
+      }
     }
-  }
-  return best_t < 0.97 * base_t ? best : 1;
+    return best_t < 0.97 * base_t ? best : 1;
+  };
+  const int z_grid = best_split(false);
+  const double mean_steps = active > 0.0 ? steps / (active * z_grid) : 0.0;
+  if (mean_steps > kPersistentMaxSteps) return BwdPlan{z_grid, false};
+  return BwdPlan{best_split(true), true};
 }
 
 // The rotary part of a workspace: tokens of the queries and keys (padded
@@ -476,7 +515,8 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base, co
   const size_t tiles = static_cast<size_t>(s->B) * s->Hq * nqt;
   const size_t off_t = round256(rows * sizeof(float));
   const size_t off_g = off_t + round256(tiles * sizeof(float4));
-  const size_t off_a = off_g + round256(static_cast<size_t>(s->B) * s->Hkv * sizeof(float2));
+  const size_t off_c = off_g + round256(static_cast<size_t>(s->B) * s->Hkv * sizeof(float2));
+  const size_t off_a = off_c + 256;
   const size_t off_q = off_a + round256(rows * static_cast<size_t>(s->d_h) * sizeof(float));
   const size_t off_o = off_q + round256(rows * static_cast<size_t>(s->d_h) * 2);
   Workspace w;
@@ -484,6 +524,7 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base, co
   w.D = reinterpret_cast<float*>(b);
   w.tilemax = reinterpret_cast<float4*>(b + off_t);
   w.grpexp = reinterpret_cast<float2*>(b + off_g);
+  w.work_ctr = reinterpret_cast<unsigned int*>(b + off_c);
   w.dQacc = reinterpret_cast<float*>(b + off_a);
   w.Q16 = b + off_q;
   w.dO16 = b + off_o;
@@ -504,6 +545,20 @@ Workspace workspace_layout_rows(const attn_shape* s, size_t rows, void* base, co
   }
   w.bytes = end;
   return w;
+}
+
+// The persistent schedule's launch (unused by the grid schedule): one work
+// item per (batch, KV head, 128-key tile) and query-head share, one CTA per
+// SM (fewer when there are fewer items).  Needs p->sh and p->hsplit.  False when the item numbers
+// would not fit the kernel's int arithmetic (more than 2^30 items).
+bool set_bwd_schedule(BwdParams* p, const Workspace& w, int sms) {
+  const int64_t nkt = (p->sh.n_k + kTileN - 1) / kTileN;
+  const int64_t items = static_cast<int64_t>(p->sh.B) * p->sh.Hkv * nkt * p->hsplit;
+  if (items > (int64_t{1} << 30)) return false;
+  p->work_ctr = w.work_ctr;
+  p->nitems = static_cast<int32_t>(items);
+  p->ctas = static_cast<int32_t>(std::min<int64_t>(items, sms));
+  return true;
 }
 
 RotaryTokens rotary_tokens(const attn_rotary* r, int64_t q, int64_t k) {
@@ -818,7 +873,18 @@ int attn_bwd_head_split(const attn_shape* shape, const attn_mask* mask) {
   unsigned int* status = nullptr;
   const int dc = device_status_ptr(&status);
   if (dc) return -dc;
-  return choose_head_split(shape, m, device_sms());
+  return choose_bwd_plan(shape, m, device_sms(), false).hsplit;
+}
+
+int attn_bwd_persistent(const attn_shape* shape, const attn_mask* mask, const attn_rotary* rotary) {
+  if (check_shape(shape) != ATTN_OK) return -ATTN_ERR_SHAPE;
+  MaskParams m;
+  const int rc = build_mask(shape, mask, &m);
+  if (rc) return -rc;
+  unsigned int* status = nullptr;
+  const int dc = device_status_ptr(&status);
+  if (dc) return -dc;
+  return choose_bwd_plan(shape, m, device_sms(), rotary != nullptr).persistent ? 1 : 0;
 }
 
 int64_t attn_visible_pairs(const attn_shape* shape, const attn_mask* mask) {
@@ -983,7 +1049,8 @@ int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, co
     padded.sq = TensorStrides{shape->d_h, static_cast<int64_t>(shape->n_q) * shape->d_h};
   }
   const cudaError_t e = launch_attn_bwd_preprocess(shape_params(shape), padded, shape->d_v, shape->d_h, Q, O, O_lo,
-                                                   dO, w.D, w.tilemax, w.grpexp, w.dQacc, w.Q16, w.dO16,
+                                                   dO, w.D, w.tilemax, w.grpexp, w.work_ctr, w.dQacc, w.Q16,
+                                                   w.dO16,
                                                    turn ? &ra : nullptr, status, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -1052,9 +1119,12 @@ int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_str
   if (rotary) p.rot = rotary_angles(rotary, rotary->pos_k, shape->d_h);
   else p.rot.pos = nullptr;
   p.status = status;
-  p.hsplit = rotary ? 1 : choose_head_split(shape, p.mask, device_sms());
+  const BwdPlan plan = choose_bwd_plan(shape, p.mask, device_sms(), rotary != nullptr);
+  p.hsplit = plan.hsplit;
+  p.persistent = plan.persistent ? 1 : 0;
   p.dKacc = w.dKacc;
   p.dVacc = w.dVacc;
+  if (!set_bwd_schedule(&p, w, device_sms())) return ATTN_ERR_SHAPE;
   if (p.hsplit > 1 && launch_zero_f32(w.dKacc, static_cast<int64_t>(w.kv_elems), st) != cudaSuccess)
     return ATTN_ERR_CUDA;
   cudaError_t e = launch_attn_bwd_main(shape->d_h, shape->d_v, tq, tk, tv, tdo, tdq, p, st);
@@ -1444,7 +1514,7 @@ int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, const att
     }
   }
   cudaError_t e = launch_attn_bwd_preprocess(sh, play, v->d_v, v->d_h, Qa, O, O_lo, dO, w.D, w.tilemax, w.grpexp,
-                                             w.dQacc, w.Q16, w.dO16, turn_q ? &rq : nullptr, status, st);
+                                             w.work_ctr, w.dQacc, w.Q16, w.dO16, turn_q ? &rq : nullptr, status, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
   const bool k_ok =
@@ -1473,9 +1543,12 @@ int attn_bwd_varlen(const attn_varlen* v, const attn_strides* strides, const att
   if (rotary) p.rot = rk;
   else p.rot.pos = nullptr;
   p.status = status;
-  p.hsplit = rotary ? 1 : choose_head_split(&d.shape, d.mask, device_sms());
+  const BwdPlan plan = choose_bwd_plan(&d.shape, d.mask, device_sms(), rotary != nullptr);
+  p.hsplit = plan.hsplit;
+  p.persistent = plan.persistent ? 1 : 0;
   p.dKacc = w.dKacc;
   p.dVacc = w.dVacc;
+  if (!set_bwd_schedule(&p, w, device_sms())) return ATTN_ERR_SHAPE;
   if (p.hsplit > 1 && launch_zero_f32(w.dKacc, static_cast<int64_t>(w.kv_elems), st) != cudaSuccess)
     return ATTN_ERR_CUDA;
   e = launch_attn_bwd_main(v->d_h, v->d_v, tq, tk, tv, tdo, tdq, p, st);

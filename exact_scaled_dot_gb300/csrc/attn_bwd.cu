@@ -83,6 +83,7 @@
 #include "f16range.cuh"
 #include "ptx.cuh"
 #include "rotary.cuh"
+#include "bwd_scale.cuh"
 
 namespace esd {
 namespace {
@@ -154,52 +155,17 @@ struct BwdCfg {
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
 
-// The CTA's fp16 operand exponents (f16range.cuh): K16 = K 2^k and
-// V16 = V 2^v for its key tile, and Q16 = Q 2^q, dO16 = dO 2^o for every
-// query tile of its (batch, KV head) group (attn_bwd_group_exp_kernel gives
-// all of a group's tiles one q and one o, so no step needs a scale of its
-// own).  The products then carry
-//   S^T = K16 Q16^T = 2^(k + q) S_raw^T,   dP^T = V16 dO16^T = 2^(v + o) dP^T,
-//   dV_acc = P^T dO16 = 2^o dV,
-// and dS enters dQ and dK as fp16 dS' = 2^g dS, with g chosen from the bound
-// |dS_ij| <= max ||dO_i|| max ||v_j|| + max |D_i| (the preprocess's tile
-// maxima and the V tile's row norms) so that |dS'| < 2^14: no fp16
-// overflow, and small gradients stay far from the fp16 subnormals.  Then
-//   dQ_acc = dS' K16 = 2^(g + k) dS K,   dK_acc = dS'^T Q16 = 2^(g + q) dS^T Q,
-// all unscaled exactly.  Every exponent lies in [-30, 30], so each derived
-// multiplier is a normal fp32 power of two.
-struct CtaScale {
-  float mv;        // max_j ||v_j|| over the key tile
-  int v, q, o, g;
-  bool overflow;   // the bound needed g < -30: dS' may saturate
-};
-
 // From the score warps' reduction (per warp w: red[4w .. 4w+2] = max
 // ||v_j||, max ||dO_i||, max |D_i|) and the group's exponents (q, o).
-__device__ __noinline__ CtaScale cta_scale(const float* red, float2 qo) {
-  CtaScale c;
-  float mdo = 0.f, md = 0.f;
-  c.mv = 0.f;
+__device__ __forceinline__ CtaScale cta_scale(const float* red, float2 qo) {
+  float mv = 0.f, mdo = 0.f, md = 0.f;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    c.mv = fmaxf(c.mv, red[4 * w]);
+    mv = fmaxf(mv, red[4 * w]);
     mdo = fmaxf(mdo, red[4 * w + 1]);
     md = fmaxf(md, red[4 * w + 2]);
   }
-  c.v = f16_tile_exponent(c.mv);
-  if (c.v == kExpZero) c.v = 0;
-  c.q = static_cast<int>(qo.x);
-  c.o = static_cast<int>(qo.y);
-  int g = kExpLimit;
-  const float bound = mdo * c.mv + md;
-  if (bound > 0.f && bound < INFINITY) {
-    int E;
-    frexpf(bound, &E);   // bound < 2^E, so |dS| 2^(14 - E) < 2^14
-    g = min(g, 14 - E);
-  }
-  c.overflow = g < -kExpLimit;
-  c.g = c.overflow ? -kExpLimit : g;
-  return c;
+  return cta_scale_of(mv, mdo, md, qo);
 }
 
 template <int DH, int DV, bool PACKED, bool ROPE, bool SPLIT>
@@ -1234,6 +1200,7 @@ struct GroupExpParams {
   float2* grpexp;                     // [B Hkv]: the group's (e_Q, e_dO)
   uint4* Q16;
   uint4* dO16;
+  unsigned int* work_ctr;             // the main kernel's work counter, zeroed here
 };
 
 __device__ __forceinline__ uint4 f16x8_scaled(uint4 u, float sc) {
@@ -1251,6 +1218,7 @@ __global__ void __launch_bounds__(256) attn_bwd_group_exp_kernel(const __grid_co
   const int64_t nq_b = p.packed ? static_cast<int64_t>(p.cu_q[b + 1]) - p.cu_q[b] : p.n_q;
   const int nt = static_cast<int>((nq_b + kTileM - 1) / kTileM);
   const int items = p.group * nt;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.work_ctr = 0u;
   if (static_cast<int>(blockIdx.y) >= items) return;   // past the sequence (packed): no tile
   auto rec_of = [&](int idx) -> const float4* {
     return p.tilemax + static_cast<int64_t>(b * p.Hq + hk * p.group + idx / nt) * p.nqt + idx % nt;
@@ -1511,6 +1479,7 @@ void launch_pre_t(const ShapeParams& sh, const LayoutParams& lay, int nqt, const
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream) {
+  if (p.persistent) return launch_attn_bwd_main_persistent(dh, dv, tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
   if (dh == 128 && dv == 128) return launch_bwd_main_t<128, 128>(tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
   if (dh == 64 && dv == 64) return launch_bwd_main_t<64, 64>(tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
   if (dh == 128 && dv == 64) return launch_bwd_main_t<128, 64>(tmQ, tmK, tmV, tmdO, tmdQ, p, stream);
@@ -1519,8 +1488,9 @@ cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const C
 
 cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams& lay, int dv, int dh,
                                        const void* Q, const void* O, const void* O_lo, const void* dO, float* D,
-                                       float4* tilemax, float2* grpexp, float* dQacc, void* Q16, void* dO16,
-                                       const RotaryAngles* rot_q, unsigned int* status, cudaStream_t stream) {
+                                       float4* tilemax, float2* grpexp, unsigned int* work_ctr, float* dQacc,
+                                       void* Q16, void* dO16, const RotaryAngles* rot_q, unsigned int* status,
+                                       cudaStream_t stream) {
   const int nqt = (sh.n_q + kTileM - 1) / kTileM;
   GroupExpParams g;
   g.Hq = sh.Hq;
@@ -1534,6 +1504,7 @@ cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams
   g.grpexp = grpexp;
   g.Q16 = static_cast<uint4*>(Q16);
   g.dO16 = static_cast<uint4*>(dO16);
+  g.work_ctr = work_ctr;
   const int64_t gy = static_cast<int64_t>(sh.group) * nqt;
   const dim3 ggrid(static_cast<unsigned>(sh.B * sh.Hkv), static_cast<unsigned>(gy < 65535 ? gy : 65535));
   if (dv == 128 && dh == 128) {

@@ -263,6 +263,14 @@ struct BwdParams {
   int32_t hsplit;
   float* dKacc;
   float* dVacc;
+  // Schedule: persistent = 0, one CTA per work item (grid B Hkv x key tiles
+  // x hsplit); persistent = 1, ctas CTAs take the nitems work items (B Hkv
+  // key tiles, times hsplit), the first ctas by block index, the rest from
+  // *work_ctr (zeroed by the backward's first stage).
+  int32_t persistent;
+  unsigned int* work_ctr;
+  int32_t nitems;
+  int32_t ctas;
 };
 
 
@@ -314,11 +322,18 @@ cudaError_t launch_attn_decode(int dh, int dv, const CUtensorMap& tmK, const CUt
 cudaError_t launch_attn_bwd_main(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmdQ,
                                  const BwdParams& p, cudaStream_t stream);
+// The persistent schedule's kernels (attn_bwd_persist.cu); launch_attn_bwd_main
+// dispatches to it when p.persistent is set.
+cudaError_t launch_attn_bwd_main_persistent(int dh, int dv, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                            const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                            const CUtensorMap& tmdQ, const BwdParams& p, cudaStream_t stream);
 // rot_q: the queries' positions (rotary: Q is rotated as it is read), or nullptr.
+// work_ctr: the main kernel's work counter, zeroed by this stage.
 cudaError_t launch_attn_bwd_preprocess(const ShapeParams& sh, const LayoutParams& lay, int dv, int dh,
                                        const void* Q, const void* O, const void* O_lo, const void* dO, float* D,
-                                       float4* tilemax, float2* grpexp, float* dQacc, void* Q16, void* dO16,
-                                       const RotaryAngles* rot_q, unsigned int* status, cudaStream_t stream);
+                                       float4* tilemax, float2* grpexp, unsigned int* work_ctr, float* dQacc,
+                                       void* Q16, void* dO16, const RotaryAngles* rot_q, unsigned int* status,
+                                       cudaStream_t stream);
 cudaError_t launch_proj_gemm(int kind, const CUtensorMap* tA, const CUtensorMap* tB, const GemmParams& p,
                              cudaStream_t stream);
 cudaError_t launch_rope_prep(const RopePrepParams& p, cudaStream_t stream);

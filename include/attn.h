@@ -84,7 +84,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 11
+#define ATTN_ABI_VERSION 12
 
 /* Status codes. */
 #define ATTN_OK               0
@@ -238,9 +238,9 @@ int attn_fwd_decode(const attn_shape* shape, const attn_mask* mask, float scale,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace the backward needs (attn_bwd and its three
- * stages): row terms D, per-128-row-tile bounds used to scale dS, an fp32
- * dQ accumulator and fp16 copies of Q and dO, about
- * B*Hq*n_q*(6*d_h + 2*d_v + 4) bytes, plus with a rotary and no k_rot a
+ * stages): row terms D, per-128-row-tile bounds used to scale dS, the main
+ * kernel's work counter, an fp32 dQ accumulator and fp16 copies of Q and
+ * dO, about B*Hq*n_q*(6*d_h + 2*d_v + 4) bytes, plus with a rotary and no k_rot a
  * rotated copy of K, B*Hkv*n_k*2*d_h bytes, plus, when the KV head groups
  * have several query heads and B*Hkv*ceil(n_k/128) < 304 (a launch that
  * may split them, see attn_bwd_head_split), fp32 sums of dK and dV,
@@ -275,9 +275,10 @@ int attn_bwd(const attn_shape* shape, const attn_mask* mask, const attn_strides*
 
 /* Stage 1 of the backward: D_i = sum_l dO_il (O_il + O_lo_il) (= c_i of
  * A.10.7; O_lo required), per-tile bounds max ||dO_i|| and max |D_i|, a
- * zeroed dQ accumulator and Q and dO re-encoded as fp16 with per-tile
- * exponents (see attn_bwd), all in `workspace`.  Q is the forward's bf16
- * query tensor, dO the bf16 upstream gradient. */
+ * zeroed dQ accumulator, a zeroed work counter for stage 2 and Q and dO
+ * re-encoded as fp16 with per-tile exponents (see attn_bwd), all in
+ * `workspace`.  Q is the forward's bf16 query tensor, dO the bf16 upstream
+ * gradient. */
 int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, const attn_rotary* rotary,
                         const void* Q, const void* O,
                         const void* O_lo, const void* dO, void* workspace,
@@ -287,7 +288,11 @@ int attn_bwd_preprocess(const attn_shape* shape, const attn_strides* strides, co
  * workspace's fp16 copy of Q (written by stage 1), K and LSE, takes dO from
  * the workspace's fp16 copy (also written by stage 1), writes dK (scaled)
  * and dV (bf16) and adds the dS K products into the workspace's fp32 dQ
- * accumulator (zeroed by stage 1). */
+ * accumulator (zeroed by stage 1).  Under the persistent schedule (see
+ * attn_bwd_persistent) the CTAs take their work items from a counter in
+ * the workspace that stage 1 zeroes, so every stage 2 call needs a stage 1
+ * call on the same workspace before it (as the dQ accumulator already
+ * does). */
 int attn_bwd_main(const attn_shape* shape, const attn_mask* mask, const attn_strides* strides,
                   const attn_rotary* rotary, float scale,
                   const void* K, const void* V, const float* LSE,
@@ -332,18 +337,31 @@ int attn_bwd_noalloc(const attn_shape* shape, const attn_mask* mask, const attn_
 size_t attn_bwd_noalloc_max_scratch_bytes(void);
 
 /* How attn_bwd_main divides the work of each KV head on the current
- * device: 1 = one CTA per (batch, KV head, key tile), taking every query
- * head of the group ("Appendix A.10", section A.10.5: dK, dV summed over
- * the group); z > 1 = the group's query heads split over z CTAs, each adding
- * its fp32 share of dK, dV into sums in the workspace that a last launch
- * rounds into dK, dV.  Chosen when the launch has too few CTAs to fill the
- * GPU (a long-history MQA chunk: one KV head, few key tiles) and the split
- * is predicted to finish at least 3 % sooner; never with a rotary.  With
+ * device: 1 = one work item per (batch, KV head, key tile), taking every
+ * query head of the group ("Appendix A.10", section A.10.5: dK, dV summed
+ * over the group); z > 1 = the group's query heads split over z work items,
+ * each adding its fp32 share of dK, dV into sums in the workspace that a
+ * last launch rounds into dK, dV.  Chosen when there are too few items to
+ * keep every SM busy to the end (a long-history MQA chunk: one KV head,
+ * few key tiles) and the split is predicted to finish at least 3 % sooner;
+ * never with a rotary.  With
  * a split, dK and dV are fp32 sums added in whatever order the CTAs finish
  * (as dQ always is), so two runs may differ in the last bf16 unit.
  * Negative ATTN_ERR_* on an invalid shape or mask.  Informational: the
  * calls choose by themselves. */
 int attn_bwd_head_split(const attn_shape* shape, const attn_mask* mask);
+
+/* Which schedule attn_bwd_main runs on the current device (with this
+ * rotary, or NULL): 0 = one CTA per work item (batch, KV head, 128-key
+ * tile, query-head share), 1 = persistent, one CTA per SM taking the items
+ * from a counter in the workspace.  Same arithmetic and results either way
+ * (dK, dV bit for bit; dQ's fp32 sums in whatever order the items finish).
+ * The persistent schedule hides each item's fixed cost (loads, re-encoding,
+ * epilogue: about 3.5 steps' worth) behind its neighbours' steps but runs
+ * its steps a little slower, so it is taken when the mean item has at most
+ * 40 steps (128-query tiles times query heads).  Negative ATTN_ERR_* on an
+ * invalid shape or mask.  Informational. */
+int attn_bwd_persistent(const attn_shape* shape, const attn_mask* mask, const attn_rotary* rotary);
 
 /* Number of visible (i, j) pairs over all batch elements and query heads,
  * from the same closed form the kernels use to classify tiles; -1 on an

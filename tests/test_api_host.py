@@ -35,7 +35,7 @@ def test_header_declares_exactly_the_bound_symbols():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert esd.attn_abi_version() == 11
+    assert esd.attn_abi_version() == 12
 
 
 def test_strerror_covers_every_code(lib):
@@ -129,15 +129,15 @@ def test_bwd_workspace_checks(lib):
     need = lib.attn_bwd_workspace_bytes(ctypes.byref(s), None)
     rows = 2 * 4 * 100
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
-    # D | tile bounds and exponents | group exponents | fp32 dQ accumulator | fp16 copies of Q and dO |
-    # fp32 sums of dK, dV (a launch of 4 CTAs with two query heads per KV head may split them)
-    assert need == (r256(rows * 4) + r256(2 * 4 * 1 * 16) + r256(2 * 2 * 8) + r256(rows * 128 * 4)
+    # D | tile bounds and exponents | group exponents | work counter | fp32 dQ accumulator | fp16 copies of Q
+    # and dO | fp32 sums of dK, dV (a launch of 4 work items with two query heads per KV head may split them)
+    assert need == (r256(rows * 4) + r256(2 * 4 * 1 * 16) + r256(2 * 2 * 8) + 256 + r256(rows * 128 * 4)
                     + r256(rows * 128 * 2) + r256(rows * s.d_v * 2) + r256(2 * 100 * 2 * (128 + 128) * 4))
     # one query head per KV head: never split, no sums
     mha = _shape(Hq=2, Hkv=2)
     rows2 = 2 * 2 * 100
     assert lib.attn_bwd_workspace_bytes(ctypes.byref(mha), None) == (
-        r256(rows2 * 4) + r256(2 * 2 * 1 * 16) + r256(2 * 2 * 8) + r256(rows2 * 128 * 4) + r256(rows2 * 128 * 2)
+        r256(rows2 * 4) + r256(2 * 2 * 1 * 16) + r256(2 * 2 * 8) + 256 + r256(rows2 * 128 * 4) + r256(rows2 * 128 * 2)
         + r256(rows2 * 128 * 2))
     p = ctypes.c_void_p(256)
     m = _mask()
@@ -263,7 +263,7 @@ def test_varlen_workspace_and_pairs(lib):
     rows = cq[-1] * 4
     nqt = (257 + 127) // 128
     r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
-    assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 16) + r256(3 * 2 * 8) + r256(rows * 128 * 4)
+    assert need == (r256(rows * 4) + r256(3 * 4 * nqt * 16) + r256(3 * 2 * 8) + 256 + r256(rows * 128 * 4)
                     + r256(rows * 128 * 2) + r256(rows * 64 * 2) + r256(ck[-1] * 2 * (128 + 64) * 4))
     p = ctypes.c_void_p(512)
     args = [ctypes.byref(v), None, None, ctypes.c_float(0.1)] + [p] * 10

@@ -2,8 +2,9 @@
 "Appendix A.10", eq. A.10.7) checked on its own, in both layouts.
 
 White-box: the checks read the workspace through the library's private
-layout (row terms D, then the per-tile bounds, the fp32 dQ accumulator and
-the fp16 copies of Q and dO, each block starting on a 256-byte boundary).
+layout (row terms D, then the per-tile bounds, the group exponents, the
+main kernel's work counter, the fp32 dQ accumulator and the fp16 copies of
+Q and dO, each block starting on a 256-byte boundary).
 Per case:
   * each query tile's exponent follows from its largest magnitude M (15 - E
     for M = m 2^E, m in [0.5, 1), rounded down to a multiple of 4, clamped
@@ -12,7 +13,8 @@ Per case:
     non-zero entry (0 if there is none), for Q and for dO separately, and
     the fp16 copies of Q and dO equal torch's conversion of the rows times
     2^e_group, bit for bit (byte work: exact);
-  * the dQ accumulator rows are all +0.0 (the workspace starts as 0xFF, NaN);
+  * the dQ accumulator rows are all +0.0 (the workspace starts as 0xFF, NaN)
+    and the main kernel's work counter is 0;
   * D equals sum_l dO_il (O_il + O_lo_il) restated in fp64 from the same
     device tensors, within the fp32 summation bound 32 * 2^-24 * sum |terms|;
   * with O_lo, D equals the oracle's D (its own fp64 O) within
@@ -53,21 +55,23 @@ def _r256(x):
 
 
 def _views(ws, rows, tiles, groups, dh, dv):
-    """D [rows], tile records [tiles, 4] (bounds, e_Q, e_dO), group exponents [groups, 2], accumulator
-    [rows * dh], Q16 [rows, dh], dO16 [rows, dv]."""
+    """D [rows], tile records [tiles, 4] (bounds, e_Q, e_dO), group exponents [groups, 2], the main kernel's
+    work counter [1], accumulator [rows * dh], Q16 [rows, dh], dO16 [rows, dv]."""
     off_t = _r256(rows * 4)
     off_g = off_t + _r256(tiles * 16)
-    off_a = off_g + _r256(groups * 8)
+    off_c = off_g + _r256(groups * 8)
+    off_a = off_c + 256
     off_q = off_a + _r256(rows * dh * 4)
     off_o = off_q + _r256(rows * dh * 2)
     assert off_o + rows * dv * 2 <= ws.numel()
     D = ws[:rows * 4].view(torch.float32)
     tm = ws[off_t:off_t + tiles * 16].view(torch.float32).reshape(tiles, 4)
     grp = ws[off_g:off_g + groups * 8].view(torch.float32).reshape(groups, 2)
+    ctr = ws[off_c:off_c + 4].view(torch.int32)
     acc = ws[off_a:off_a + rows * dh * 4].view(torch.float32)
     q16 = ws[off_q:off_q + rows * dh * 2].view(torch.float16).reshape(rows, dh)
     do16 = ws[off_o:off_o + rows * dv * 2].view(torch.float16).reshape(rows, dv)
-    return D, tm, grp, acc, q16, do16
+    return D, tm, grp, ctr, acc, q16, do16
 
 
 def _same_bits(a, b):
@@ -157,7 +161,8 @@ def test_preprocess_padded(orc, w, mode):
     assert esd.attn_get_status() == 0
 
     rows, nqt = w.B * w.Hq * w.nq, math.ceil(w.nq / 128)
-    D, tm, grp, acc, q16, do16 = _views(ws, rows, w.B * w.Hq * nqt, w.B * w.Hkv, w.dh, w.dv)
+    D, tm, grp, ctr, acc, q16, do16 = _views(ws, rows, w.B * w.Hq * nqt, w.B * w.Hkv, w.dh, w.dv)
+    assert int(ctr.item()) == 0   # the main kernel's work counter (the workspace started as 0xFF)
     tm_c, grp_c = tm.cpu(), grp.cpu()
     Qr, dOr = Q.reshape(w.B, w.Hq, w.nq, w.dh), dO.reshape(w.B, w.Hq, w.nq, w.dv)
     q16r, do16r = q16.reshape(w.B, w.Hq, w.nq, w.dh), do16.reshape(w.B, w.Hq, w.nq, w.dv)
@@ -252,7 +257,7 @@ def test_preprocess_packed(w):
     lens = [int(inp.cu_q[b + 1]) - int(inp.cu_q[b]) for b in range(w.B)]
     nqt = math.ceil(max(max(lens), 1) / 128)
     rows = Tq * w.Hq
-    D, tm, grp, _acc, q16, do16 = _views(ws, rows, w.B * w.Hq * nqt, w.B * w.Hkv, w.dh, w.dv)
+    D, tm, grp, _ctr, _acc, q16, do16 = _views(ws, rows, w.B * w.Hq * nqt, w.B * w.Hkv, w.dh, w.dv)
     q16, do16 = q16.reshape(Tq, w.Hq, w.dh), do16.reshape(Tq, w.Hq, w.dv)
 
     ref, bound = _row_terms(O, O_lo, dO)                   # [Tq, Hq]
