@@ -29,7 +29,9 @@
 //               the query heads of its group and the query tiles that can
 //               see its keys, keeps dK and dV in tensor memory for the whole
 //               loop, and adds each tile's dS K product into the fp32 dQ
-//               accumulator with TMA reduce-add.
+//               accumulator with TMA reduce-add.  (attn_bwd_persist.cu
+//               holds the same kernel under a persistent schedule, which the
+//               host takes when the items have few steps.)
 //   finalize    dQ = scale * accumulator, rounded to bf16.
 //
 // Main-kernel warp roles (512 threads):
@@ -156,8 +158,9 @@ struct BwdCfg {
 };
 
 // From the score warps' reduction (per warp w: red[4w .. 4w+2] = max
-// ||v_j||, max ||dO_i||, max |D_i|) and the group's exponents (q, o).
-__device__ __forceinline__ CtaScale cta_scale(const float* red, float2 qo) {
+// ||v_j||, max ||dO_i||, max |D_i|) and the group's exponents (q, o).  (One
+// out-of-line copy for the two warpgroups that call it.)
+__device__ __noinline__ CtaScale cta_scale(const float* red, float2 qo) {
   float mv = 0.f, mdo = 0.f, md = 0.f;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {

@@ -122,6 +122,11 @@ struct BwdPCfg {
   static_assert(256 + DH + DV <= 512, "tensor memory budget");
 };
 
+// The item's multipliers (bwd_scale.cuh), in one out-of-line copy.
+__device__ __noinline__ CtaScale item_scale(float mv, float mdo, float md, float2 qo) {
+  return cta_scale_of(mv, mdo, md, qo);
+}
+
 // A work item of the main kernel: the 128-key tile kt of (batch, KV head)
 // bkv, with the z-th share of the group's query heads under a split.  Items
 // are numbered with bkv fastest, then z, then kt, so that under a causal
@@ -697,7 +702,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (ok) {
         int kexp = f16_tile_exponent(kmax);
         if (kexp == kExpZero) kexp = 0;
-        const CtaScale cs = cta_scale_of(mv, mdo, md, p.grpexp[it.bkv]);
+        const CtaScale cs = item_scale(mv, mdo, md, p.grpexp[it.bkv]);
         if (ts == 0) {
           if (f16_saturates(kmax, kexp) || f16_saturates(cs.mv, cs.v) || cs.overflow)
             record_status(p.status, ATTN_ERR_RANGE);

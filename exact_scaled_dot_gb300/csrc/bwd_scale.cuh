@@ -36,7 +36,7 @@ struct CtaScale {
 
 // From the key tile's maxima (max ||v_j||, and max ||dO_i||, max |D_i| over
 // the query tiles its steps visit) and the group's exponents (q, o).
-__device__ __noinline__ CtaScale cta_scale_of(float mv, float mdo, float md, float2 qo) {
+__device__ __forceinline__ CtaScale cta_scale_of(float mv, float mdo, float md, float2 qo) {
   CtaScale c;
   c.mv = mv;
   c.v = f16_tile_exponent(c.mv);
