@@ -902,13 +902,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             make_float4(__uint_as_float(v[4 * c]) * inv, __uint_as_float(v[4 * c + 1]) * inv,
                         __uint_as_float(v[4 * c + 2]) * inv, __uint_as_float(v[4 * c + 3]) * inv);
     };
-    auto reduce_round = [&](int first_box, int b, int row0, int nq_b, int head) {
+    // yz: the TMA coordinates of the warp's first row (worked out before the
+    // step's wait, so no shared-memory read sits between the rounds), in:
+    // whether that row is inside the sequence.
+    auto reduce_round = [&](int first_box, TmaYZ yz, bool in) {
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && row0 < nq_b) {
+      if (lane == 0 && in) {
         // (Rows of the box past the sequence hold zeros: adding them is a
         // no-op on whatever rows lie there.)
-        const TmaYZ yz = q_tma(PACKED, p.lay, p.sh.Hq, b, head, row0);
 #pragma unroll
         for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx)
           tma_reduce_add_3d(&tmdQ, smem_u32(wstage + bx * C::kDQBoxBytes), (first_box + bx) * C::kDQBoxCols, yz.y,
@@ -955,6 +957,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int s = 0; s < ro[4] && ok; ++s) {
           const int gs = ro[5] + s;
           const int row0 = qt * kTileM + static_cast<int>(quad) * 32;
+          const TmaYZ yz = q_tma(PACKED, p.lay, p.sh.Hq, ro[0], head, row0);
+          const bool row_in = row0 < ro[1];
           ok = wait_all(C::kBarDQFull, static_cast<uint32_t>(gs & 1));
           if (!ok) break;
           tc_fence_after_sync();
@@ -993,7 +997,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             staging_free();
 #pragma unroll
             for (int bx = 0; bx < C::kDQBoxesPerRound; ++bx) stage_box(wstage + bx * C::kDQBoxBytes, v[bx], inv);
-            reduce_round(rd * C::kDQBoxesPerRound, ro[0], row0, ro[1], head);
+            reduce_round(rd * C::kDQBoxesPerRound, yz, row_in);
           }
           __syncwarp();
           if (++qt == ro[3]) {
