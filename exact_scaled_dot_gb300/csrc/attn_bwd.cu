@@ -894,7 +894,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       // transpose of the rotation), formed here per 4-block chunk.
       int32_t kpos = 0;
       if constexpr (ROPE) kpos = in ? p.rot.pos[k_token(PACKED, p.lay, p.sh.n_k, b, j)] : 0;
-#pragma unroll
+      // (With the rotary the chunks stay rolled: each unrolled chunk would
+      // carry its own copy of the angle arithmetic.)
+      constexpr int kDkUnroll = ROPE ? 1 : DH / 32;
+#pragma unroll kDkUnroll
       for (int cc = 0; cc < DH / 32; ++cc) {
         uint32_t w[16];
         if (total > 0) {
