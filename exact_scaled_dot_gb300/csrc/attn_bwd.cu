@@ -1304,8 +1304,8 @@ attn_bwd_finalize_strided_kernel(int64_t n8, int c8, int n_inner, int64_t s_oute
 // The same with the rotary embedding: each 8-element chunk of the rotated
 // query's gradient turned back by its token's angles (the transpose of the
 // rotation) before it is rounded.  A work item is one chunk of one token for
-// a group of up to 8 query heads, so that the token's table entries are read
-// once per group.  Accumulator row and dQ offset of (token, h): padded
+// all its query heads, 8 at a time, so that the token's angles are formed
+// once per chunk.  Accumulator row and dQ offset of (token, h): padded
 // (token = b n_q + i) row (b Hq + h) n_q + i at (b Hq + h) s_head + i s_row;
 // packed row token Hq + h at token s_row + h s_head.
 __global__ void __launch_bounds__(256)
@@ -1313,14 +1313,11 @@ attn_bwd_finalize_rope_kernel(int64_t tokens, int c8, int Hq, int n_q, int packe
                               float scale, const float4* __restrict__ acc, const __grid_constant__ RotaryAngles rot,
                               uint4* __restrict__ dQ) {
   constexpr int kG = 8;
-  const int groups = (Hq + kG - 1) / kG;
-  const int64_t items = tokens * c8 * groups;
+  const int64_t items = tokens * c8;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < items; u += nthreads) {
-    const int64_t tg = u / c8;
-    const int c = static_cast<int>(u - tg * c8);
-    const int64_t tok = tg / groups;
-    const int h0 = static_cast<int>(tg - tok * groups) * kG;
+    const int64_t tok = u / c8;
+    const int c = static_cast<int>(u - tok * c8);
     int64_t row0, rstep, off0, ostep;
     if (packed) {
       row0 = tok * Hq;
@@ -1334,33 +1331,35 @@ attn_bwd_finalize_rope_kernel(int64_t tokens, int c8, int Hq, int n_q, int packe
       off0 = b * Hq * s_head + i * s_row;
       ostep = s_head;
     }
-    float4 a[kG], bb[kG];
-#pragma unroll
-    for (int g = 0; g < kG; ++g)
-      if (h0 + g < Hq) {
-        const int64_t k = (row0 + (h0 + g) * rstep) * c8 + c;
-        a[g] = acc[2 * k];
-        bb[g] = acc[2 * k + 1];
-      }
     float wh[4], wl[4];
     rope_freqs4(rot.w_hi, rot.w_lo, c, wh, wl);
     float4 t0, t1;
     rope_angles4(rot.pos[tok], wh, wl, t0, t1);
     rope_transpose(t0, t1);
     const float cs[4] = {t0.x, t0.z, t1.x, t1.z}, sn[4] = {t0.y, t0.w, t1.y, t1.w};
+    for (int h0 = 0; h0 < Hq; h0 += kG) {
+      float4 a[kG], bb[kG];
 #pragma unroll
-    for (int g = 0; g < kG; ++g) {
-      if (h0 + g >= Hq) break;
-      const float x[8] = {a[g].x * scale, a[g].y * scale, a[g].z * scale, a[g].w * scale,
-                          bb[g].x * scale, bb[g].y * scale, bb[g].z * scale, bb[g].w * scale};
-      uint32_t w[4];
+      for (int g = 0; g < kG; ++g)
+        if (h0 + g < Hq) {
+          const int64_t k = (row0 + (h0 + g) * rstep) * c8 + c;
+          a[g] = acc[2 * k];
+          bb[g] = acc[2 * k + 1];
+        }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float y0, y1;
-        rot_block(x[2 * q], x[2 * q + 1], cs[q], sn[q], y0, y1);
-        w[q] = pack_bf16x2(y0, y1);
+      for (int g = 0; g < kG; ++g) {
+        if (h0 + g >= Hq) break;
+        const float x[8] = {a[g].x * scale, a[g].y * scale, a[g].z * scale, a[g].w * scale,
+                            bb[g].x * scale, bb[g].y * scale, bb[g].z * scale, bb[g].w * scale};
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float y0, y1;
+          rot_block(x[2 * q], x[2 * q + 1], cs[q], sn[q], y0, y1);
+          w[q] = pack_bf16x2(y0, y1);
+        }
+        dQ[(off0 + (h0 + g) * ostep) / 8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      dQ[(off0 + (h0 + g) * ostep) / 8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -1562,7 +1561,7 @@ cudaError_t launch_attn_bwd_finalize(int64_t elems, int dh, int n_inner, int64_t
     // Padded rows are heads of n_inner = n_q rows (s_outer the head stride);
     // packed rows are tokens of n_inner = Hq heads (s_outer the token stride).
     const int64_t tokens = elems / (static_cast<int64_t>(Hq) * dh);
-    const int64_t items = tokens * (dh / 8) * ((Hq + 7) / 8);
+    const int64_t items = tokens * (dh / 8);
     attn_bwd_finalize_rope_kernel<<<grid_for(items), 256, 0, stream>>>(
         tokens, dh / 8, Hq, packed ? 0 : n_inner, packed ? 1 : 0, packed ? s_outer : s_inner,
         packed ? s_inner : s_outer, scale, reinterpret_cast<const float4*>(dQacc), *rot_q, static_cast<uint4*>(dQ));
