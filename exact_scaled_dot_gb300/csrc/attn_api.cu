@@ -480,10 +480,11 @@ BwdPlan choose_bwd_plan(const attn_shape* s, const MaskParams& m, int sms, bool 
   };
   const bool may_split = !rotary && head_split_possible(s->B, s->Hq, s->Hkv, s->n_k);
   auto best_split = [&](bool persistent) {
+    if (!may_split) return 1;   // (no simulation: large launches pay nothing here)
     int best = 1;
     double best_t = makespan(1, persistent);
     const double base_t = best_t;
-    for (int z = 2; may_split && z <= std::min(group, 16); ++z) {
+    for (int z = 2; z <= std::min(group, 16); ++z) {
       if (group % z) continue;
       const double t = makespan(z, persistent);
       if (t < best_t) {
