@@ -10,11 +10,11 @@
 // fp16 re-encoding, the pipeline's fill, the last dQ/dK products, the dK/dV
 // epilogue), against about 5k cycles per 128-query step: a quarter of the
 // time of an item with a few steps.  The persistent kernel hides most of it
-// behind the neighbouring items' steps, but its steps run some 5-10 % slower
-// (the roles' loops nest inside item loops, and the warps stall more often
-// on instruction fetch), so the host takes it only for items of few steps
-// (short query ranges, small heads groups, causal MHA), and the grid kernel
-// for long ones.
+// behind the neighbouring items' steps, but its steps run some 10-15 %
+// slower (the roles' loops nest inside item loops, and the warps stall more
+// often on instruction fetch), so the host takes it only for items of few
+// steps (short query ranges, small head groups, causal MHA), and the grid
+// kernel for long ones.
 //
 // Warp roles (512 threads), as in the grid kernel except where noted:
 //   warp 0      TMA producer; also publishes the item numbers and claims
